@@ -1,0 +1,383 @@
+"""Throughput of the offloading-aware MoE layer forward on GB300.
+
+One step = one whole layer forward (router + prefetch router + delta_hat,
+miss handling, permutation, grouped SwiGLU experts + shared experts, LoRE,
+combine) over one batch of synthetic tokens, through the library's C ABI.
+
+Default workload: the DeepSeek-V2-Lite-shaped layer (hidden 2048, 64 routed
+experts top-6, 2 shared experts, intermediate 1408, LoRE rank 16, 24 of 64
+experts resident by the batch prefetch set, HYBRID miss policy) decoding
+8 tokens per step.  Weights stream from HBM: the timed steps rotate over
+several copies of the layer's weights at distinct addresses, so the expert
+bytes one step reads are evicted from L2 (129 MB) before they are read again.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+        [--workload NAME]
+Multi-GPU (torchrun): each rank runs an independent replica on its own
+tokens (weak scaling, no data-path collective); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from workloads import CONFIGS, make_tokens, make_weights  # noqa: E402
+
+# name -> (layer config, tokens per step, phase)
+WORKLOADS = {
+    "dsv2lite-decode-T8": ("dsv2lite", 8, "decode"),
+    "dsv2lite-decode-T1": ("dsv2lite", 1, "decode"),
+    "granite-decode-T1": ("granite", 1, "decode"),
+    "granite-prefill-T1024": ("granite", 1024, "prefill"),
+    "mixtral-decode-T1": ("mixtral", 1, "decode"),
+    "mixtral-decode-T8": ("mixtral", 8, "decode"),
+    "mixtral-decode-T32": ("mixtral", 32, "decode"),
+    "qwen2-prefill-T4096": ("qwen2", 4096, "prefill"),
+}
+DEFAULT_WORKLOAD = "dsv2lite-decode-T8"
+METRIC = "MoE-layer tokens/sec (decode & prefill) and % of HBM/tensor roofline, 1xGB300"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=4000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            P = json.load(f)
+        return float(P["hbm_gbs"]), float(P.get("bf16_tflops", 1900.0)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, 1900.0, "fallback"
+
+
+def recorded_traffic(kernel_src: str, workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary of this kernel and
+    workload, if the kernel source is unchanged since it was taken."""
+    with open(os.path.join(ROOT, "expert_routing_ffn_gb300", "csrc", kernel_src), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    prof = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(prof):
+        return None
+    for name in sorted(os.listdir(prof)):
+        if not name.endswith(".md"):
+            continue
+        with open(os.path.join(prof, name)) as f:
+            txt = f.read()
+        m = re.search(r"traffic_per_launch_bytes:\s*([0-9.eE+]+)\s+source_sha256_16:\s*([0-9a-f]+)"
+                      r"\s+workload:\s*(\S+)", txt)
+        if m and m.group(2) == sha and m.group(3) == workload:
+            return float(m.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax = max(smax, float(f[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[4:8]):
+                if v.lower() in ("active", "0x1"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": smax or None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(cfg, W, T, seconds, batch_offset=0):
+    """The float64 oracle, as it stands, on a bounded sample of the workload:
+    batches of min(T, 32) tokens until `seconds` have passed (at least one)."""
+    import oracle
+    T = min(T, 32)
+    n_tok, t0, b = 0, time.perf_counter(), 0
+    while True:
+        x = make_tokens(cfg, T=T, batch=10_000 + batch_offset + b)
+        oracle.layer_forward(cfg, W, x)
+        n_tok += T
+        b += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": n_tok / el, "unit": "tokens/s", "cores": min(oracle.num_threads(), T),
+            "kind": "oracle",
+            "sample": f"{b} batches of {T} tokens ({n_tok} tokens, {el:.1f} s) through the float64 "
+                      f"CPU oracle, OpenMP over the tokens of a batch"}
+
+
+def run_reference(args, wl_name, cfg, T, world, rank):
+    """Reference arm: the float64 oracle timed on the host cores, one batch of
+    T tokens per step, for at most about two minutes."""
+    if rank != 0:
+        return
+    import oracle
+    T = min(T, 32)  # a step is a bounded sample of the batch (tokens are independent)
+    W = make_weights(cfg)
+    for i in range(min(args.warmup, 2)):
+        oracle.layer_forward(cfg, W, make_tokens(cfg, T=T, batch=20_000 + i))
+    budget, t0, n, steps = 120.0, time.perf_counter(), 0, 0
+    while steps < args.steps:
+        oracle.layer_forward(cfg, W, make_tokens(cfg, T=T, batch=30_000 + steps))
+        n += T
+        steps += 1
+        if time.perf_counter() - t0 > budget:
+            break
+    el = time.perf_counter() - t0
+    value = n / el
+    cores = min(oracle.num_threads(), T)
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": steps,
+            "warmup": min(args.warmup, 2), "ms_per_step": 1e3 * el / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": wl_name, "tokens_per_step": T},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{steps} steps of {T} tokens (of {args.steps} requested; "
+                                       f"capped at {budget:.0f} s)"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    wl_name = args.workload
+    cfg_name, T, phase = WORKLOADS[wl_name]
+    cfg = CONFIGS[cfg_name]
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, wl_name, cfg, T, world, rank)
+        return
+
+    import torch
+    import expert_routing_ffn_gb300 as moe
+    from expert_routing_ffn_gb300.layer import DeviceLayer, LayerBuffers, forward, layer_args
+
+    world, rank, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local if world > 1 else 0)
+    moe.lib()  # fails loudly if the CUDA library is missing
+    hbm_gbs, bf16_tflops, peak_src = peaks()
+
+    W = make_weights(cfg)
+    base = DeviceLayer(cfg, W, T, device=str(dev))
+    esize = 2 if cfg.wtype == "bf16" else 4
+    expert_bytes = 3 * cfg.I * cfg.d * esize
+    shared_bytes = cfg.n_shared * 3 * cfg.I_shared * cfg.d * esize
+    layer_bytes = cfg.N * expert_bytes + shared_bytes
+    # enough copies that the expert bytes of one step are pushed out of L2 (by
+    # at least twice its size) before the same copy is read again
+    step_bytes = min(cfg.N, T * cfg.k) * expert_bytes + shared_bytes
+    n_copies = int(min(16, max(2, math.ceil(1 + 2 * L2_BYTES / step_bytes))))
+    layers = [base] + [base.clone() for _ in range(n_copies - 1)]
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
+    bufs = [LayerBuffers(L, T) for L in layers]
+    xs = [torch.from_numpy(make_tokens(cfg, T=T, batch=1000 * rank + i)).to(dev).to(base.dt).contiguous()
+          for i in range(n_copies)]
+
+    def step(i):
+        c = i % n_copies
+        forward(layers[c], bufs[c], xs[c], stream=stream)
+
+    # eager warm-up, error check, then one CUDA graph per layer copy
+    for i in range(max(args.warmup, n_copies)):
+        step(i)
+    for L in layers:
+        st, det = moe.moe_check(L.ws)
+        if st != moe.MOE_OK:
+            raise RuntimeError(f"device error {moe.status_string(st)} ({det})")
+    graphs = []
+    n0 = moe.moe_launch_total()
+    for c in range(n_copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(c)
+        graphs.append(g)
+    launches_per_step = (moe.moe_launch_total() - n0) // n_copies
+    for i in range(args.warmup):
+        graphs[i % n_copies].replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index or 0) as clk:
+        ev0.record(stream)
+        for i in range(args.steps):
+            graphs[i % n_copies].replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms_total = max_over_ranks(world, ev0.elapsed_time(ev1))
+    ms_per_step = ms_total / args.steps
+    value = world * T * args.steps / (ms_total / 1e3)
+    clocks = clk.summary()
+
+    # ---- dominant kernel: the expert FFN stage, timed alone on the same stream
+    # (route/select/permute outputs of each copy are already in place)
+    fb = []
+    for c, L in enumerate(layers):
+        off = bufs[c].expert_offsets.cpu().numpy()
+        u = int((np.diff(off) > 0).sum())
+        fb.append(u * expert_bytes + shared_bytes)
+    n_k = max(50, min(2000, args.steps // 2))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_k)]
+    for i in range(n_k + n_copies):
+        c = i % n_copies
+        L, b = layers[c], bufs[c]
+        D = L.dims.with_T(T)
+        if i >= n_copies:
+            evs[i - n_copies][0].record(stream)
+        moe.moe_expert_ffn(D, xs[c], L.table, b.expert_offsets, b.perm, cfg.keep_frac, b.y_perm,
+                           b.y_shared, L.ws, stream)
+        if i >= n_copies:
+            evs[i - n_copies][1].record(stream)
+    torch.cuda.synchronize()
+    k_ms = [a.elapsed_time(b) for a, b in evs]
+    k_bytes = [fb[(i + n_copies) % n_copies] for i in range(n_k)]
+    achieved = sum(k_bytes) / (sum(k_ms) / 1e3) / 1e9
+    traffic = recorded_traffic("ffn_gemv.cu", wl_name)
+
+    # ---- end to end through the public API: pinned host x -> device, layer
+    # forward, result -> pinned host, every step
+    x_host = [xs[c].cpu().pin_memory() for c in range(n_copies)]
+    out_host = [torch.empty_like(bufs[c].out, device="cpu").pin_memory() for c in range(n_copies)]
+    n_e2e = max(20, min(args.steps, 1000))
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        c = i % n_copies
+        xs[c].copy_(x_host[c], non_blocking=True)
+        forward(layers[c], bufs[c], xs[c], stream=stream)
+        out_host[c].copy_(bufs[c].out, non_blocking=True)
+        stream.synchronize()
+    e2e_s = max_over_ranks(world, time.perf_counter() - t0)
+    e2e_value = world * T * n_e2e / e2e_s
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": cfg.wtype if cfg.wtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,0.02^2) weights, N(0,1) tokens; shapes of the named model)",
+        "config": {"workload": wl_name, "tokens_per_step": T, "d": cfg.d, "experts": cfg.N,
+                   "top_k": cfg.k, "intermediate": cfg.I, "shared_experts": cfg.n_shared,
+                   "miss_policy": ["exact", "substitute", "lore", "hybrid"][cfg.policy],
+                   "resident": cfg.n_resident, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: {n_copies} rotating layer copies of "
+                         f"{layer_bytes / 1e9:.2f} GB", "cuda_graph": True},
+        "roofline": {"kernel": "moe_expert_ffn (ffn_gemv_kernel + gemv_reduce_kernel)",
+                     "bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": achieved / hbm_gbs, "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": float(statistics.mean(fb)),
+                     "avg_launch_ms": statistics.mean(k_ms), "traffic": traffic},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": xs[0].numel() * xs[0].element_size(),
+                "d2h_bytes_per_step": bufs[0].out.numel() * 4, "steps": n_e2e,
+                "note": "moe_layer_forward per step with pinned-host copies and a stream sync, no graph"},
+        "gpu_launches": int(launches_per_step * args.steps),
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, W, T, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

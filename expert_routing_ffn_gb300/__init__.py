@@ -1,0 +1,322 @@
+"""Python binding of the GB300 MoE-layer C ABI (include/moe.h).
+
+Argument marshalling only: every function below checks tensor dtype, device,
+contiguity and size, then calls the C function of the same name in
+libmoe_gb300.so, where every step of the layer runs as a CUDA kernel.  There
+is no Python or CPU implementation of any step: if the library is missing the
+calls raise.
+
+Tensors are torch tensors on the current CUDA device.  uint64 expert masks
+are carried in int64 tensors (same bits).  `stream` defaults to torch's
+current stream.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CAPACITY = 0, 1, 2, 3
+MOE_ERR_CUDA, MOE_ERR_STAGING, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_INDEX = 4, 5, 6, 7
+MOE_DTYPE_F32, MOE_DTYPE_BF16 = 0, 1
+MOE_MISS_EXACT, MOE_MISS_SUBSTITUTE, MOE_MISS_LORE, MOE_MISS_HYBRID = 0, 1, 2, 3
+MOE_KIND_COMPUTE, MOE_KIND_FETCH, MOE_KIND_LORE = 0, 1, 2
+MOE_NUM_COUNTERS = 8
+COUNTER_NAMES = ["hit", "substitute", "lore", "fetch", "overlap", "delta_hat_sum",
+                 "delta_star_sum", "shortfall"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        extra = ""
+        if status == MOE_ERR_CUDA:
+            extra = " — " + lib().moe_last_error_detail().decode()
+        super().__init__(f"{where}: {status_string(status)} (status {status}){extra}")
+
+
+class moe_dims(C.Structure):
+    _fields_ = [(n, C.c_int) for n in ("T", "d", "N", "k", "I", "n_shared", "I_shared", "r",
+                                       "delta_max", "wtype", "renorm_topk")]
+
+    def with_T(self, T: int) -> "moe_dims":
+        d = moe_dims()
+        C.pointer(d)[0] = self
+        d.T = T
+        return d
+
+
+_VP = C.c_void_p
+
+
+class moe_layer_args(C.Structure):
+    _fields_ = [("x", _VP), ("x_pre", _VP), ("w_router", _VP), ("router_bias", _VP),
+                ("w_prefetch", _VP), ("w_ord", _VP), ("theta", _VP), ("tau", C.c_float),
+                ("n_resident", C.c_int), ("resident", _VP), ("use_prefetch_mask", C.c_int),
+                ("policy", C.c_int), ("gamma", C.c_float), ("keep_frac", C.c_float),
+                ("table", _VP), ("lore_a", _VP), ("lore_b", _VP)]
+
+
+class moe_layer_outputs(C.Structure):
+    _fields_ = [(n, _VP) for n in (
+        "topk_idx", "topk_gate", "router_prob", "delta_hat", "prefetch_mask", "delta_star",
+        "batch_resident", "final_idx", "final_gate", "final_kind", "fetch_mask", "counters",
+        "expert_offsets", "perm", "inv_perm", "y_perm", "y_shared", "y_lore", "out")]
+
+
+_lib = None
+_lock = threading.Lock()
+
+# argument type codes for the C prototypes
+_P, _I, _F, _U64, _SZ = _VP, C.c_int, C.c_float, C.c_uint64, C.c_size_t
+_DIMS = C.POINTER(moe_dims)
+_PROTOS = {
+    "moe_status_string": ([C.c_int], C.c_char_p),
+    "moe_launch_total": ([], C.c_uint64),
+    "moe_last_error_detail": ([], C.c_char_p),
+    "moe_workspace_size": ([_DIMS, C.POINTER(C.c_size_t)], C.c_int),
+    "moe_expert_table_size": ([_DIMS, C.POINTER(C.c_size_t)], C.c_int),
+    "moe_expert_table_init": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _SZ, _P], C.c_int),
+    "moe_route": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _F, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                   _P], C.c_int),
+    "moe_select_resident": ([_DIMS, _P, _P, _P, _P, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                             _P], C.c_int),
+    "moe_stage_experts": ([_DIMS, _U64, _P, _P, _P, _P, _P, _P, _P, _P, C.POINTER(C.c_size_t)],
+                          C.c_int),
+    "moe_permute": ([_DIMS, _P, _P, _P, _P, _P, _P, _SZ, _P], C.c_int),
+    "moe_expert_ffn": ([_DIMS, _P, _P, _P, _P, _F, _P, _P, _P, _SZ, _P], C.c_int),
+    "moe_lore": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P], C.c_int),
+    "moe_combine": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P], C.c_int),
+    "moe_layer_forward": ([_DIMS, C.POINTER(moe_layer_args), C.POINTER(moe_layer_outputs), _P, _SZ,
+                           _P], C.c_int),
+    "moe_check": ([_P, _P, C.POINTER(C.c_int), C.POINTER(C.c_int32)], C.c_int),
+    "moe_testing_fail_copies_after": ([C.c_int], None),
+}
+
+
+def lib():
+    """Load libmoe_gb300.so (built by build.py / __graft_entry__.build())."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build the CUDA library first "
+                                   "(python -m expert_routing_ffn_gb300.build)")
+            L = C.CDLL(LIB_PATH)
+            for name, (args, res) in _PROTOS.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().moe_status_string(status).decode()
+
+
+def _check(status: int, where: str):
+    if status != MOE_OK:
+        raise MoeError(status, where)
+
+
+def _stream(stream):
+    if stream is None:
+        return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return C.c_void_p(stream.cuda_stream)
+    return C.c_void_p(int(stream))
+
+
+def _ptr(t, dtype=None, numel=None, name="tensor", optional=False):
+    """Device pointer of a contiguous CUDA tensor (None -> NULL if optional)."""
+    if t is None:
+        if optional:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} has {t.numel()} elements, needs {numel}")
+    return C.c_void_p(t.data_ptr())
+
+
+def wdtype(dims: moe_dims):
+    return torch.bfloat16 if dims.wtype == MOE_DTYPE_BF16 else torch.float32
+
+
+def make_dims(T, d, N, k, I, n_shared=0, I_shared=0, r=0, delta_max=None, wtype="bf16",
+              renorm_topk=0) -> moe_dims:
+    D = moe_dims()
+    D.T, D.d, D.N, D.k, D.I = T, d, N, k, I
+    D.n_shared, D.I_shared, D.r = n_shared, I_shared, r
+    D.delta_max = N - k if delta_max is None else delta_max
+    D.wtype = MOE_DTYPE_BF16 if wtype in ("bf16", MOE_DTYPE_BF16) else MOE_DTYPE_F32
+    D.renorm_topk = renorm_topk
+    return D
+
+
+def moe_launch_total() -> int:
+    return int(lib().moe_launch_total())
+
+
+def moe_workspace_size(dims: moe_dims) -> int:
+    n = C.c_size_t()
+    _check(lib().moe_workspace_size(C.byref(dims), C.byref(n)), "moe_workspace_size")
+    return n.value
+
+
+def moe_expert_table_size(dims: moe_dims) -> int:
+    n = C.c_size_t()
+    _check(lib().moe_expert_table_size(C.byref(dims), C.byref(n)), "moe_expert_table_size")
+    return n.value
+
+
+def _ptr_array(tensors, name):
+    arr = (C.c_void_p * len(tensors))()
+    for i, t in enumerate(tensors):
+        arr[i] = _ptr(t, name=f"{name}[{i}]").value
+    return arr
+
+
+def moe_expert_table_init(dims, w_gate, w_up, w_down, sh_gate, sh_up, sh_down, table, stream=None):
+    """w_*: sequences of N device tensors [I, d]; sh_*: n_shared tensors [I_shared, d]."""
+    keep = [_ptr_array(w_gate, "w_gate"), _ptr_array(w_up, "w_up"), _ptr_array(w_down, "w_down")]
+    sh = [_ptr_array(s, n) if dims.n_shared else None for s, n in
+          ((sh_gate, "sh_gate"), (sh_up, "sh_up"), (sh_down, "sh_down"))]
+    _check(lib().moe_expert_table_init(
+        C.byref(dims), *[C.cast(a, C.c_void_p) for a in keep],
+        *[C.cast(a, C.c_void_p) if a is not None else None for a in sh],
+        _ptr(table, torch.uint8, name="table"), table.numel(), _stream(stream)),
+        "moe_expert_table_init")
+
+
+def moe_route(dims, x, w_router, router_bias, x_pre, w_prefetch, w_ord, theta, tau, n_resident,
+              topk_idx, topk_gate, router_prob, delta_hat, prefetch_mask, delta_star,
+              batch_resident, ws, stream=None):
+    T, d, N, k = dims.T, dims.d, dims.N, dims.k
+    wt = wdtype(dims)
+    _check(lib().moe_route(
+        C.byref(dims), _ptr(x, wt, T * d, "x"), _ptr(w_router, wt, N * d, "w_router"),
+        _ptr(router_bias, torch.float32, N, "router_bias", True),
+        _ptr(x_pre, wt, T * d, "x_pre", True), _ptr(w_prefetch, wt, N * d, "w_prefetch", True),
+        _ptr(w_ord, torch.float32, d, "w_ord", True),
+        _ptr(theta, torch.float32, dims.delta_max + 1, "theta", True), float(tau), int(n_resident),
+        _ptr(topk_idx, torch.int32, T * k, "topk_idx"), _ptr(topk_gate, torch.float32, T * k, "topk_gate"),
+        _ptr(router_prob, torch.float32, T * N, "router_prob"), _ptr(delta_hat, torch.int32, T, "delta_hat"),
+        _ptr(prefetch_mask, torch.int64, T, "prefetch_mask"),
+        _ptr(delta_star, torch.int32, T, "delta_star", True),
+        _ptr(batch_resident, torch.int64, 1, "batch_resident", True),
+        _ptr(ws, torch.uint8, name="ws"), ws.numel(), _stream(stream)), "moe_route")
+
+
+def moe_select_resident(dims, router_prob, topk_idx, prefetch_mask, resident, policy, gamma,
+                        delta_hat, delta_star, final_idx, final_gate, final_kind, fetch_mask,
+                        counters, ws, stream=None):
+    T, N, k = dims.T, dims.N, dims.k
+    _check(lib().moe_select_resident(
+        C.byref(dims), _ptr(router_prob, torch.float32, T * N, "router_prob"),
+        _ptr(topk_idx, torch.int32, T * k, "topk_idx"),
+        _ptr(prefetch_mask, torch.int64, T, "prefetch_mask", True),
+        _ptr(resident, torch.int64, 1, "resident", True), int(policy), float(gamma),
+        _ptr(delta_hat, torch.int32, T, "delta_hat", True),
+        _ptr(delta_star, torch.int32, T, "delta_star", True),
+        _ptr(final_idx, torch.int32, T * k, "final_idx"), _ptr(final_gate, torch.float32, T * k, "final_gate"),
+        _ptr(final_kind, torch.int32, T * k, "final_kind"),
+        _ptr(fetch_mask, torch.int64, 1, "fetch_mask", True),
+        _ptr(counters, torch.int32, MOE_NUM_COUNTERS, "counters", True),
+        _ptr(ws, torch.uint8, name="ws"), ws.numel(), _stream(stream)), "moe_select_resident")
+
+
+def moe_stage_experts(dims, host_fetch_mask: int, host_w_gate, host_w_up, host_w_down,
+                      dev_w_gate, dev_w_up, dev_w_down, stage_stream, done_event) -> int:
+    """host_w_*: sequences of N pinned CPU tensors; dev_w_*: N device tensors."""
+    def arr(ts, name, pinned):
+        a = (C.c_void_p * len(ts))()
+        for i, t in enumerate(ts):
+            if pinned and not t.is_pinned():
+                raise ValueError(f"{name}[{i}] must be pinned host memory")
+            a[i] = t.data_ptr()
+        return a
+    a = [arr(host_w_gate, "host_w_gate", True), arr(host_w_up, "host_w_up", True),
+         arr(host_w_down, "host_w_down", True), arr(dev_w_gate, "dev_w_gate", False),
+         arr(dev_w_up, "dev_w_up", False), arr(dev_w_down, "dev_w_down", False)]
+    n = C.c_size_t()
+    _check(lib().moe_stage_experts(C.byref(dims), C.c_uint64(host_fetch_mask & (2**64 - 1)),
+                                   *[C.cast(x, C.c_void_p) for x in a], _stream(stage_stream),
+                                   C.c_void_p(done_event.cuda_event), C.byref(n)),
+           "moe_stage_experts")
+    return n.value
+
+
+def moe_permute(dims, final_idx, final_kind, expert_offsets, perm, inv_perm, ws, stream=None):
+    T, N, k = dims.T, dims.N, dims.k
+    _check(lib().moe_permute(
+        C.byref(dims), _ptr(final_idx, torch.int32, T * k, "final_idx"),
+        _ptr(final_kind, torch.int32, T * k, "final_kind"),
+        _ptr(expert_offsets, torch.int32, N + 1, "expert_offsets"), _ptr(perm, torch.int32, T * k, "perm"),
+        _ptr(inv_perm, torch.int32, T * k, "inv_perm"), _ptr(ws, torch.uint8, name="ws"), ws.numel(),
+        _stream(stream)), "moe_permute")
+
+
+def moe_expert_ffn(dims, x, table, expert_offsets, perm, keep_frac, y_perm, y_shared, ws,
+                   stream=None):
+    T, d, N, k = dims.T, dims.d, dims.N, dims.k
+    _check(lib().moe_expert_ffn(
+        C.byref(dims), _ptr(x, wdtype(dims), T * d, "x"), _ptr(table, torch.uint8, name="table"),
+        _ptr(expert_offsets, torch.int32, N + 1, "expert_offsets"), _ptr(perm, torch.int32, T * k, "perm"),
+        float(keep_frac), _ptr(y_perm, torch.float32, T * k * d, "y_perm"),
+        _ptr(y_shared, torch.float32, T * d, "y_shared", True), _ptr(ws, torch.uint8, name="ws"),
+        ws.numel(), _stream(stream)), "moe_expert_ffn")
+
+
+def moe_lore(dims, x, final_idx, final_kind, final_gate, lore_a, lore_b, y_lore, stream=None):
+    T, d, N, k, r = dims.T, dims.d, dims.N, dims.k, dims.r
+    wt = wdtype(dims)
+    _check(lib().moe_lore(
+        C.byref(dims), _ptr(x, wt, T * d, "x"), _ptr(final_idx, torch.int32, T * k, "final_idx"),
+        _ptr(final_kind, torch.int32, T * k, "final_kind"), _ptr(final_gate, torch.float32, T * k, "final_gate"),
+        _ptr(lore_a, wt, N * r * d, "lore_a"), _ptr(lore_b, wt, N * d * r, "lore_b"),
+        _ptr(y_lore, torch.float32, T * d, "y_lore"), _stream(stream)), "moe_lore")
+
+
+def moe_combine(dims, y_perm, inv_perm, final_gate, final_kind, y_shared, y_lore, out, stream=None):
+    T, d, k = dims.T, dims.d, dims.k
+    _check(lib().moe_combine(
+        C.byref(dims), _ptr(y_perm, torch.float32, T * k * d, "y_perm"),
+        _ptr(inv_perm, torch.int32, T * k, "inv_perm"), _ptr(final_gate, torch.float32, T * k, "final_gate"),
+        _ptr(final_kind, torch.int32, T * k, "final_kind"),
+        _ptr(y_shared, torch.float32, T * d, "y_shared", True),
+        _ptr(y_lore, torch.float32, T * d, "y_lore", True), _ptr(out, torch.float32, T * d, "out"),
+        _stream(stream)), "moe_combine")
+
+
+def moe_layer_forward(dims, args: moe_layer_args, outs: moe_layer_outputs, ws, stream=None):
+    _check(lib().moe_layer_forward(C.byref(dims), C.byref(args), C.byref(outs),
+                                   _ptr(ws, torch.uint8, name="ws"), ws.numel(), _stream(stream)),
+           "moe_layer_forward")
+
+
+def moe_check(ws, stream=None):
+    """Synchronise and return (device_status, detail); clears the error word."""
+    st = C.c_int()
+    det = C.c_int32()
+    _check(lib().moe_check(_ptr(ws, torch.uint8, name="ws"), _stream(stream), C.byref(st), C.byref(det)),
+           "moe_check")
+    return st.value, det.value
+
+
+def moe_testing_fail_copies_after(n: int):
+    lib().moe_testing_fail_copies_after(int(n))
+
+
+from .layer import DeviceLayer, LayerBuffers  # noqa: E402,F401

@@ -1,0 +1,255 @@
+// Shared device helpers for the sm_103a MoE layer kernels: PTX wrappers for
+// mbarriers and bulk (TMA) copies, the device error word, bf16 unpacking,
+// and the workspace / FFN-plan layout used by the host launchers and the
+// kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------- constants
+constexpr int kMaxExperts = 64;       // expert sets are uint64 bitmasks
+constexpr int kMaxTopK = 8;
+constexpr int kGemvMaxRows = 8;       // rows per GEMV segment (register-resident)
+constexpr int kGemvMaxCtas = 512;     // upper bound of the GEMV grid (workspace sizing)
+constexpr int kAlign = 256;
+// Iteration bound of every spin wait; a wait that exceeds it records
+// MOE_ERR_TIMEOUT and gives up instead of hanging the GPU.
+constexpr uint32_t kSpinLimit = 1u << 24;
+
+// ---------------------------------------------------------------- error word
+struct DevError {
+    int code;
+    int detail;
+    int pad[14];
+};
+
+__device__ __forceinline__ void set_error(DevError* e, int code, int detail) {
+    if (atomicCAS(&e->code, 0, code) == 0) e->detail = detail;
+}
+
+// ---------------------------------------------------------------- FFN plan
+// One GEMV segment: up to kGemvMaxRows rows that share one expert's weights.
+// Its I channels occupy [ch_start, ch_start + I) of the global channel list,
+// which is split evenly over the G CTAs of the GEMV grid (P channels each).
+// CTA c writes a partial [rows, d] sum for every segment it overlaps at
+// partial row pbase + (c - c0) * rows.
+struct Seg {
+    int expert;     // 0..N-1 routed, N + s shared expert s
+    int row0;       // routed: first permuted position; shared: first token
+    int rows;
+    int I;
+    int ch_start;
+    int c0;         // first CTA that covers this segment
+    int npieces;
+    int pbase;      // first partial row
+};
+
+struct PlanHeader {
+    int n_seg;
+    int total_ch;
+    int P;          // channels per CTA
+    int G;          // GEMV grid
+    int rg;         // rows per segment
+    int n_partial_rows;
+    int n_routed_rows;
+    int pad[9];
+};
+
+// ---------------------------------------------------------------- workspace
+struct WsLayout {
+    size_t err, logits_r, logits_p, score, qp, plan_hdr, segs, seg_first, partial, total;
+    int max_segs, max_partial_rows;
+};
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Token rows per GEMV segment: the register budget of the GEMV kernel allows
+// 8 rows while a thread block covers d <= 2048 bf16 values, 4 above.  The
+// workspace sizing and the launch both take it from here.
+__host__ __device__ inline int gemv_rows(const moe_dims& D) {
+    if (D.wtype == MOE_DTYPE_BF16) return D.d <= 2048 ? 8 : 4;
+    return 8;
+}
+
+__host__ __device__ inline WsLayout ws_layout(const moe_dims& D) {
+    WsLayout L;
+    const size_t T = (size_t)(D.T > 0 ? D.T : 1), N = (size_t)D.N;
+    const size_t rows_routed = T * (size_t)D.k;
+    const size_t rows_shared = T * (size_t)D.n_shared;
+    const int rg = gemv_rows(D);
+    // segments: sum over experts of ceil(rows_e / rg) <= rows / rg + N, plus the
+    // shared experts' ceil(T / rg) each
+    L.max_segs = (int)(rows_routed / rg + N + (size_t)D.n_shared * (T / rg + 1) + 8);
+    // partial rows: sum over segments of pieces * rows <= rg * G + 2 * all rows
+    // (a segment of I channels spans at most I / P + 2 CTA ranges, P >= total / G)
+    L.max_partial_rows = (int)((size_t)rg * kGemvMaxCtas + 2 * (rows_routed + rows_shared) + 16);
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, kAlign); return at; };
+    L.err = take(sizeof(DevError));
+    L.logits_r = take(T * N * 4);
+    L.logits_p = take(T * N * 4);
+    L.score = take(T * 4);
+    L.qp = take(T * N * 4);
+    L.plan_hdr = take(sizeof(PlanHeader));
+    L.segs = take((size_t)L.max_segs * sizeof(Seg));
+    L.seg_first = take((N + (size_t)D.n_shared + 1) * 4);
+    L.partial = take((size_t)L.max_partial_rows * (size_t)D.d * 4);
+    L.total = o;
+    return L;
+}
+
+template <typename Tp>
+__host__ __device__ inline Tp* ws_at(void* ws, size_t off) {
+    return reinterpret_cast<Tp*>(static_cast<char*>(ws) + off);
+}
+
+// ---------------------------------------------------------------- expert table
+// Device-resident; filled by moe_expert_table_init.  Entry e < N: routed
+// expert e; entry N + s: shared expert s.
+struct alignas(64) ExpertEntry {
+    const void* w[3];   // gate, up, down: [I, d] each
+    int I;
+    int pad[9];
+    // TMA descriptors (tensor maps) for the tensor-core path: gate/up tiles
+    // (K-major) and down tiles (MN-major).
+    alignas(64) unsigned char tmap[3][128];
+};
+
+// ---------------------------------------------------------------- launch setup
+// Raise a kernel's dynamic shared-memory limit to the device maximum, once per
+// (kernel, device); later calls (for example inside a stream capture) only
+// look the pair up.
+cudaError_t allow_max_smem_impl(const void* kernel);
+
+template <typename K>
+inline cudaError_t allow_max_smem(K kernel) {
+    return allow_max_smem_impl(reinterpret_cast<const void*>(kernel));
+}
+
+// ---------------------------------------------------------------- bf16
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+template <typename W> struct Vec;
+template <> struct Vec<__nv_bfloat16> { static constexpr int n = 8; };
+template <> struct Vec<float> { static constexpr int n = 4; };
+
+// 16 bytes of weights -> fp32 values
+__device__ __forceinline__ void unpack16(const uint4& v, float* f, __nv_bfloat16*) {
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+__device__ __forceinline__ void unpack16(const uint4& v, float* f, float*) {
+    f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+}
+
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_f32(float v) { return v; }
+
+// packed fp32 FMA (two lanes per instruction on sm_100+)
+__device__ __forceinline__ void fma2(float& a0, float& a1, float x0, float x1, float y0, float y1) {
+    unsigned long long acc, xv, yv;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(xv) : "f"(x0), "f"(x1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(yv) : "f"(y0), "f"(y1));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(xv), "l"(yv));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc));
+}
+
+// ---------------------------------------------------------------- PTX: mbarrier / bulk copy
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: returns false after kSpinLimit unsuccessful tries.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kSpinLimit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// 1-D bulk copy global -> shared (TMA engine), completion on an mbarrier.
+// src, dst 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy) : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// ---------------------------------------------------------------- warp helpers
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Reduce 32 values per lane across the warp: afterwards lane l holds the
+// warp-wide sum of value l (a reduce-scatter by halving: 31 shuffles).
+__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 16, n = 32; o > 0; o >>= 1, n >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            float send = up ? v[i] : v[i + n / 2];
+            float keep = up ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0];
+}
+
+}  // namespace moe

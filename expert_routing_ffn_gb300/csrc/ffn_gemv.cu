@@ -1,0 +1,345 @@
+// Stage 3b, decode-size segments: SwiGLU expert FFN as an HBM-streaming GEMV.
+//
+// y = sum_i SiLU(x . Wg[i]) (x . Wu[i]) Wd[i, :]  (FloE method §1 with the
+// identity mask; weights channel-major [I, d] so that channel i's gate, up
+// and down rows are each one contiguous d-vector).
+//
+// Work split: the channels of every segment (an expert with up to RG token
+// rows) form one list, cut into G equal ranges, one per CTA (G = SMs).  A CTA
+// streams its range in stages of CH channels: one bulk copy (TMA engine) per
+// matrix per stage brings the CH gate, up and down rows into shared memory,
+// NS stages in flight, completion tracked by mbarriers.  Every weight byte is
+// read from HBM exactly once; the token rows are held in registers.
+//
+// Per stage: each thread owns one 16-byte chunk of d; it forms the partial
+// gate/up dot products of its chunk for every (channel, row), the block sums
+// them (warp reduce-scatter + shared memory), computes h = SiLU(g) * u, and
+// then adds h * Wd[channel, chunk] into its register accumulators for the
+// output columns of the same chunk.  When a CTA leaves a segment it writes
+// its partial output rows; a second kernel sums the partials of each row in a
+// fixed order (deterministic, no atomics).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+constexpr int kNSMax = 8;
+
+struct Producer {
+    const Seg* segs;
+    const ExpertEntry* table;
+    unsigned char* stage_mem;
+    uint64_t* bars;
+    size_t row_bytes, mat_bytes, stage_bytes;
+    int NS, CH, seg, ch, hi;
+    int issued;     // stages issued so far
+    uint64_t policy;
+
+    int n_seg;
+
+    __device__ __forceinline__ void issue(int stage_k) {
+        if (ch >= hi || seg >= n_seg) return;
+        const Seg S = segs[seg];
+        const int local = ch - S.ch_start;
+        const int seg_end = min(hi, S.ch_start + S.I) - S.ch_start;
+        const int nch = min(CH, seg_end - local);
+        const ExpertEntry& E = table[S.expert];
+        const int b = stage_k % NS;
+        unsigned char* buf = stage_mem + (size_t)b * stage_bytes;
+        const uint32_t bytes = (uint32_t)(nch * row_bytes);
+        mbar_arrive_expect_tx(&bars[b], 3 * bytes);
+#pragma unroll
+        for (int m = 0; m < 3; ++m)
+            bulk_g2s(buf + m * mat_bytes, static_cast<const char*>(E.w[m]) + (size_t)local * row_bytes,
+                     bytes, &bars[b], policy);
+        ch += nch;
+        if (ch >= S.ch_start + S.I) ++seg;
+        ++issued;
+    }
+};
+
+template <int V>
+__device__ __forceinline__ float dot_v(const float* a, const float* b) {
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < V; j += 2) fma2(s0, s1, a[j], a[j + 1], b[j], b[j + 1]);
+    return s0 + s1;
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.f + expf(-g)); }
+
+template <typename W, int RG, int CH, int ROWS>
+__device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, int llo, int lhi,
+                                           int cta, unsigned char* stage_mem, uint64_t* bars,
+                                           float (*red_s)[32], float (*h_s)[RG], int* s_abort,
+                                           int& stage_k, Producer& prod) {
+    constexpr int V = Vec<W>::n;
+    constexpr int NV = 2 * CH * ROWS;
+    static_assert(NV <= 32, "per-stage outputs must fit one warp reduce-scatter");
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    const int d = p.d;
+    const size_t row_bytes = (size_t)d * sizeof(W);
+    const size_t mat_bytes = (size_t)CH * row_bytes;
+    const size_t stage_bytes = 3 * mat_bytes;
+    const W* x = static_cast<const W*>(p.x);
+
+    float xr[ROWS][V];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+        const int token = S.expert < p.N ? p.perm[S.row0 + r] / p.topk : S.row0 + r;
+        const uint4 raw = reinterpret_cast<const uint4*>(x + (size_t)token * d)[tid];
+        unpack16(raw, xr[r], (W*)nullptr);
+    }
+    float yacc[ROWS][V];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+        for (int j = 0; j < V; ++j) yacc[r][j] = 0.f;
+
+    for (int i = llo; i < lhi; i += CH) {
+        const int nch = min(CH, lhi - i);
+        const int b = stage_k % p.NS;
+        const uint32_t par = (uint32_t)((stage_k / p.NS) & 1);
+        if (!mbar_wait(&bars[b], par)) {
+            set_error(p.err, MOE_ERR_TIMEOUT, cta);
+            *s_abort = 1;
+        }
+        const unsigned char* buf = stage_mem + (size_t)b * stage_bytes;
+        float v[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < CH; ++cc) {
+            if (cc < nch) {
+                float wg[V], wu[V];
+                unpack16(reinterpret_cast<const uint4*>(buf + cc * row_bytes)[tid], wg, (W*)nullptr);
+                unpack16(reinterpret_cast<const uint4*>(buf + mat_bytes + cc * row_bytes)[tid], wu,
+                         (W*)nullptr);
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    v[cc * 2 * ROWS + r] = dot_v<V>(wg, xr[r]);
+                    v[cc * 2 * ROWS + ROWS + r] = dot_v<V>(wu, xr[r]);
+                }
+            }
+        }
+        if (NV > 8) {
+            const float tot = warp_reduce_scatter32(v);
+            red_s[warp][lane] = tot;
+        } else {
+#pragma unroll
+            for (int q = 0; q < NV; ++q) {
+                const float t = warp_sum(v[q]);
+                if (lane == 0) red_s[warp][q] = t;
+            }
+        }
+        __syncthreads();
+        if (tid < CH * ROWS) {
+            const int cc = tid / ROWS, r = tid % ROWS;
+            float g = 0.f, u = 0.f;
+            for (int w = 0; w < nw; ++w) {
+                g += red_s[w][cc * 2 * ROWS + r];
+                u += red_s[w][cc * 2 * ROWS + ROWS + r];
+            }
+            h_s[cc][r] = cc < nch ? silu(g) * u : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int cc = 0; cc < CH; ++cc) {
+            if (cc < nch) {
+                float wd[V];
+                unpack16(reinterpret_cast<const uint4*>(buf + 2 * mat_bytes + cc * row_bytes)[tid], wd,
+                         (W*)nullptr);
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    const float h = h_s[cc][r];
+#pragma unroll
+                    for (int j = 0; j < V; j += 2) fma2(yacc[r][j], yacc[r][j + 1], h, h, wd[j], wd[j + 1]);
+                }
+            }
+        }
+        __syncthreads();
+        if (tid == 0) prod.issue(stage_k + p.NS);
+        ++stage_k;
+        if (*s_abort) break;
+    }
+    // partial output rows of this CTA for this segment
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+        float* dst = p.partial + ((size_t)(S.pbase + (cta - S.c0) * ROWS + r)) * d + (size_t)tid * V;
+#pragma unroll
+        for (int j = 0; j < V; j += 4)
+            *reinterpret_cast<float4*>(dst + j) = make_float4(yacc[r][j], yacc[r][j + 1], yacc[r][j + 2], yacc[r][j + 3]);
+    }
+}
+
+template <typename W, int RG, int CH, int MAXT>
+__global__ void __launch_bounds__(MAXT, 1) ffn_gemv_kernel(GemvParams p) {
+    __shared__ __align__(8) uint64_t bars[kNSMax];
+    __shared__ float red_s[MAXT / 32][32];
+    __shared__ float h_s[CH][RG];
+    __shared__ int s_abort;
+    extern __shared__ __align__(128) unsigned char stage_mem[];
+
+    const int tid = threadIdx.x;
+    const PlanHeader hdr = *p.hdr;
+    const int cta = blockIdx.x;
+    if (cta >= hdr.G) return;
+    const int lo = cta * hdr.P, hi = min(lo + hdr.P, hdr.total_ch);
+    if (lo >= hi || hdr.n_seg <= 0) return;
+    const size_t row_bytes = (size_t)p.d * sizeof(W);
+
+    int s_lo = 0, s_hi = hdr.n_seg - 1;
+    while (s_lo < s_hi) {
+        const int mid = (s_lo + s_hi + 1) >> 1;
+        if (p.segs[mid].ch_start <= lo) s_lo = mid; else s_hi = mid - 1;
+    }
+    const int seg0 = s_lo;
+
+    if (tid == 0) {
+        for (int b = 0; b < p.NS; ++b) mbar_init(&bars[b], 1);
+        fence_mbar_init();
+        s_abort = 0;
+    }
+    __syncthreads();
+
+    Producer prod;
+    prod.segs = p.segs; prod.table = p.table; prod.stage_mem = stage_mem; prod.bars = bars;
+    prod.row_bytes = row_bytes; prod.mat_bytes = CH * row_bytes; prod.stage_bytes = 3 * CH * row_bytes;
+    prod.NS = p.NS; prod.CH = CH; prod.seg = seg0; prod.ch = lo; prod.hi = hi; prod.issued = 0;
+    prod.n_seg = hdr.n_seg;
+    prod.policy = l2_evict_first_policy();
+    if (tid == 0)
+        for (int k = 0; k < p.NS; ++k) prod.issue(k);
+
+    int stage_k = 0;
+    int seg = seg0, ch = lo;
+    while (ch < hi && seg < hdr.n_seg) {
+        const Seg S = p.segs[seg];
+        const int llo = ch - S.ch_start;
+        const int lhi = min(hi, S.ch_start + S.I) - S.ch_start;
+        switch (S.rows) {
+#define MOE_PIECE(R)                                                                        \
+    case R:                                                                                 \
+        if (R <= RG) {                                                                      \
+            gemv_piece<W, RG, CH, (R <= RG ? R : 1)>(p, S, llo, lhi, cta, stage_mem, bars,  \
+                                                     red_s, h_s, &s_abort, stage_k, prod);  \
+        } else {                                                                            \
+            if (tid == 0) set_error(p.err, MOE_ERR_DEVICE_INDEX, seg);                      \
+            s_abort = 1;                                                                    \
+        }                                                                                   \
+        break;
+            MOE_PIECE(1) MOE_PIECE(2) MOE_PIECE(3) MOE_PIECE(4)
+            MOE_PIECE(5) MOE_PIECE(6) MOE_PIECE(7) MOE_PIECE(8)
+#undef MOE_PIECE
+            default:
+                if (tid == 0) set_error(p.err, MOE_ERR_DEVICE_INDEX, seg);
+                s_abort = 1;
+        }
+        __syncthreads();
+        if (s_abort) break;
+        ch = S.ch_start + lhi;
+        ++seg;
+    }
+    // after an abort, wait (bounded) for the copies still in flight before
+    // the CTA exits and its shared memory is released
+    if (tid == 0 && s_abort) {
+        for (int k = stage_k; k < prod.issued; ++k)
+            (void)mbar_wait(&bars[k % p.NS], (uint32_t)((k / p.NS) & 1));
+    }
+}
+
+// Sum the partial rows of each output row in piece order.
+__global__ void __launch_bounds__(256) gemv_reduce_kernel(const PlanHeader* __restrict__ hdr_p,
+                                                          const Seg* __restrict__ segs,
+                                                          const int32_t* __restrict__ seg_first,
+                                                          const int32_t* __restrict__ expert_offsets,
+                                                          const float* __restrict__ partial, int d,
+                                                          int N, int n_shared, int T, int routed_cap,
+                                                          float* __restrict__ y_perm,
+                                                          float* __restrict__ y_shared) {
+    const PlanHeader hdr = *hdr_p;
+    const int row = blockIdx.x;
+    const int rg = hdr.rg;
+    const int nd4 = d / 4;
+    if (row < routed_cap) {
+        const int pos = row;
+        if (pos >= hdr.n_routed_rows) return;
+        int lo = 0, hi = N - 1;  // expert e with offsets[e] <= pos < offsets[e+1]
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (expert_offsets[mid] <= pos) lo = mid; else hi = mid - 1;
+        }
+        const int e = lo;
+        const int local = pos - expert_offsets[e];
+        const int si = seg_first[e] + local / rg;
+        if (si < 0 || si >= hdr.n_seg) return;
+        const Seg S = segs[si];
+        const int r = local % rg;
+        if (S.pbase + (S.npieces - 1) * S.rows + r >= hdr.n_partial_rows) return;
+        for (int q = threadIdx.x; q < nd4; q += blockDim.x) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int pc = 0; pc < S.npieces; ++pc) {
+                const float4 v = reinterpret_cast<const float4*>(
+                    partial + (size_t)(S.pbase + pc * S.rows + r) * d)[q];
+                acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+            }
+            reinterpret_cast<float4*>(y_perm + (size_t)pos * d)[q] = acc;
+        }
+    } else {
+        const int t = row - routed_cap;
+        if (t >= T || n_shared == 0) return;
+        for (int q = threadIdx.x; q < nd4; q += blockDim.x) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s = 0; s < n_shared; ++s) {
+                const int si = seg_first[N + s] + t / rg;
+                if (si < 0 || si >= hdr.n_seg) continue;
+                const Seg S = segs[si];
+                const int r = t % rg;
+                if (S.pbase + (S.npieces - 1) * S.rows + r >= hdr.n_partial_rows) continue;
+                for (int pc = 0; pc < S.npieces; ++pc) {
+                    const float4 v = reinterpret_cast<const float4*>(
+                        partial + (size_t)(S.pbase + pc * S.rows + r) * d)[q];
+                    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+                }
+            }
+            reinterpret_cast<float4*>(y_shared + (size_t)t * d)[q] = acc;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+template <typename W, int RG, int CH, int MAXT>
+static cudaError_t launch_gemv_t(const GemvParams& p, int G, cudaStream_t st) {
+    const int threads = p.d / Vec<W>::n;
+    if (threads > MAXT || threads % 32) return cudaErrorInvalidValue;
+    const size_t smem = (size_t)p.NS * 3 * CH * p.d * sizeof(W);
+    cudaError_t e = allow_max_smem(ffn_gemv_kernel<W, RG, CH, MAXT>);
+    if (e != cudaSuccess) return e;
+    ffn_gemv_kernel<W, RG, CH, MAXT><<<G, threads, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+int gemv_stages(int d, bool bf16) {
+    const size_t stage = (size_t)3 * 2 * d * (bf16 ? 2 : 4);
+    int ns = (int)((200 * 1024) / stage);
+    return ns < 2 ? 2 : (ns > kNSMax ? kNSMax : ns);
+}
+
+cudaError_t launch_gemv(const GemvParams& p, int G, bool bf16, cudaStream_t st) {
+    if (bf16) {
+        if (p.d <= 2048) return launch_gemv_t<__nv_bfloat16, 8, 2, 256>(p, G, st);
+        return launch_gemv_t<__nv_bfloat16, 4, 2, 512>(p, G, st);
+    }
+    return launch_gemv_t<float, 8, 2, 256>(p, G, st);
+}
+
+cudaError_t launch_gemv_reduce(const GemvReduceArgs& a, cudaStream_t st) {
+    const int grid = a.routed_cap + (a.n_shared > 0 ? a.T : 0);
+    if (grid == 0) return cudaSuccess;
+    gemv_reduce_kernel<<<grid, 256, 0, st>>>(a.hdr, a.segs, a.seg_first, a.expert_offsets, a.partial,
+                                             a.d, a.N, a.n_shared, a.T, a.routed_cap, a.y_perm,
+                                             a.y_shared);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,87 @@
+// Launch interfaces of the kernels (host side of each .cu file).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+struct LogitsArgs {
+    const void *x, *x_pre, *w_router, *w_prefetch;
+    const float *bias, *w_ord;
+    int T, d, N, has_prefetch;
+    bool bf16;
+    float *logits_r, *logits_p, *score;
+};
+cudaError_t launch_logits(const LogitsArgs& a, cudaStream_t st);
+
+struct RouteSelectArgs {
+    const float *logits_r, *logits_p, *score, *theta;
+    float logit_tau;
+    int T, N, k, delta_max, has_prefetch;
+    int32_t* topk_idx; float* topk_gate; float* router_prob; int32_t* delta_hat;
+    uint64_t* prefetch_mask; int32_t* delta_star; float* qp;
+};
+cudaError_t launch_route_select(const RouteSelectArgs& a, cudaStream_t st);
+cudaError_t launch_batch_resident(const float* qp, int T, int N, int n_res, uint64_t* out,
+                                  cudaStream_t st);
+
+struct SelectArgs {
+    const float* router_prob; const int32_t* topk_idx; const uint64_t* prefetch_mask;
+    const uint64_t* resident; int policy; float gamma; const int32_t* delta_hat;
+    const int32_t* delta_star; int T, N, k, renorm;
+    int32_t* final_idx; float* final_gate; int32_t* final_kind; uint64_t* fetch_mask;
+    int32_t* counters; DevError* err;
+};
+cudaError_t launch_select_resident(const SelectArgs& a, cudaStream_t st);
+
+struct PermuteArgs {
+    const int32_t *final_idx, *final_kind;
+    int n_slots, N;
+    int32_t *expert_offsets, *perm, *inv_perm;
+    DevError* err;
+};
+cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st);
+
+struct PlanArgs {
+    const int32_t* expert_offsets;
+    int T, N, n_shared, I, I_shared, rg, G, max_segs, max_partial_rows;
+    PlanHeader* hdr; Seg* segs; int32_t* seg_first; DevError* err;
+};
+cudaError_t launch_plan_gemv(const PlanArgs& a, cudaStream_t st);
+
+struct GemvParams {
+    const void* x;
+    int d, N, topk, NS;
+    const int32_t* perm;
+    const ExpertEntry* table;
+    const PlanHeader* hdr;
+    const Seg* segs;
+    float* partial;
+    DevError* err;
+};
+int gemv_stages(int d, bool bf16);
+cudaError_t launch_gemv(const GemvParams& p, int G, bool bf16, cudaStream_t st);
+
+struct GemvReduceArgs {
+    const PlanHeader* hdr; const Seg* segs; const int32_t* seg_first; const int32_t* expert_offsets;
+    const float* partial; int d, N, n_shared, T, routed_cap;
+    float *y_perm, *y_shared;
+};
+cudaError_t launch_gemv_reduce(const GemvReduceArgs& a, cudaStream_t st);
+
+struct LoreArgs {
+    const void* x; const int32_t *final_idx, *final_kind; const float* final_gate;
+    const void *A, *B; int T, d, k, r, N; bool bf16; float* y_lore; DevError* err;
+};
+cudaError_t launch_lore(const LoreArgs& a, cudaStream_t st);
+
+struct CombineArgs {
+    const float* y_perm; const int32_t* inv_perm; const float* final_gate;
+    const int32_t* final_kind; const float *y_shared, *y_lore; int T, d, k; float* out;
+};
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
+
+}  // namespace moe

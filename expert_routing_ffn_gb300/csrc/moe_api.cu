@@ -1,0 +1,428 @@
+// C ABI of the MoE layer (include/moe.h): argument checks, workspace layout,
+// expert table, and the launch sequence of each stage.
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tma.h"
+
+using namespace moe;
+
+namespace moe {
+
+cudaError_t allow_max_smem_impl(const void* kernel) {
+    static std::mutex mu;
+    static std::vector<std::pair<const void*, int>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const auto& p : done)
+        if (p.first == kernel && p.second == dev) return cudaSuccess;
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kernel);
+    if (e != cudaSuccess) return e;
+    // static + dynamic shared memory of one block may not exceed the opt-in size
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - (int)fa.sharedSizeBytes);
+    if (e == cudaSuccess) done.emplace_back(kernel, dev);
+    return e;
+}
+
+}  // namespace moe
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_fail_copies_after{-1};
+
+inline void count(int n = 1) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+inline cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+
+#define MOE_TRY(expr)                                      \
+    do {                                                   \
+        moe_status _st = (expr);                           \
+        if (_st != MOE_OK) return _st;                     \
+    } while (0)
+
+thread_local char g_detail[256] = "";
+
+moe_status record_cuda(cudaError_t e, const char* what) {
+    std::snprintf(g_detail, sizeof(g_detail), "%s: %s (%s)", what, cudaGetErrorName(e),
+                  cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+}
+
+#define MOE_CUDA(expr)                                     \
+    do {                                                   \
+        cudaError_t _e = (expr);                           \
+        if (_e != cudaSuccess) return record_cuda(_e, #expr); \
+    } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_dims(const moe_dims* D) {
+    if (!D) return MOE_ERR_INVALID_ARG;
+    if (D->T < 0 || D->d <= 0 || D->N <= 0 || D->k <= 0 || D->I <= 0 || D->n_shared < 0 ||
+        D->r < 0 || D->delta_max < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (D->n_shared > 0 && D->I_shared <= 0) return MOE_ERR_INVALID_ARG;
+    if (D->wtype != MOE_DTYPE_BF16 && D->wtype != MOE_DTYPE_F32) return MOE_ERR_UNSUPPORTED;
+    if (D->N > kMaxExperts || D->k > kMaxTopK || D->k > D->N) return MOE_ERR_UNSUPPORTED;
+    if (D->delta_max > D->N - D->k) return MOE_ERR_INVALID_ARG;
+    if (D->d % 256 != 0) return MOE_ERR_UNSUPPORTED;
+    if (D->wtype == MOE_DTYPE_BF16 && D->d > 4096) return MOE_ERR_UNSUPPORTED;
+    if (D->wtype == MOE_DTYPE_F32 && D->d > 1024) return MOE_ERR_UNSUPPORTED;
+    if (D->r > 64) return MOE_ERR_UNSUPPORTED;
+    if (D->n_shared > 8) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+moe_status check_ws(const moe_dims* D, void* ws, size_t ws_bytes) {
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(ws) % kAlign) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < ws_layout(*D).total) return MOE_ERR_CAPACITY;
+    return MOE_OK;
+}
+
+int sm_count() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+int gemv_grid() {
+    int g = sm_count();
+    return g > kGemvMaxCtas ? kGemvMaxCtas : g;
+}
+
+bool bf16(const moe_dims* D) { return D->wtype == MOE_DTYPE_BF16; }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported dimensions or type";
+        case MOE_ERR_CAPACITY: return "capacity exceeded (buffer too small or available set < k)";
+        case MOE_ERR_CUDA: return "CUDA runtime error";
+        case MOE_ERR_STAGING: return "expert staging copy failed";
+        case MOE_ERR_TIMEOUT: return "bounded device wait timed out";
+        case MOE_ERR_DEVICE_INDEX: return "expert or slot index out of range";
+    }
+    return "unknown status";
+}
+
+uint64_t moe_launch_total(void) { return g_launches.load(); }
+
+const char* moe_last_error_detail(void) { return g_detail; }
+
+moe_status moe_workspace_size(const moe_dims* dims, size_t* bytes) {
+    MOE_TRY(check_dims(dims));
+    if (!bytes) return MOE_ERR_INVALID_ARG;
+    *bytes = ws_layout(*dims).total;
+    return MOE_OK;
+}
+
+moe_status moe_expert_table_size(const moe_dims* dims, size_t* bytes) {
+    MOE_TRY(check_dims(dims));
+    if (!bytes) return MOE_ERR_INVALID_ARG;
+    *bytes = (size_t)(dims->N + dims->n_shared) * sizeof(ExpertEntry);
+    return MOE_OK;
+}
+
+moe_status moe_expert_table_init(const moe_dims* dims, const void* const* host_w_gate,
+                                 const void* const* host_w_up, const void* const* host_w_down,
+                                 const void* const* host_sh_gate, const void* const* host_sh_up,
+                                 const void* const* host_sh_down, void* table, size_t table_bytes,
+                                 void* stream) {
+    MOE_TRY(check_dims(dims));
+    const int N = dims->N, ns = dims->n_shared;
+    if (!table || !host_w_gate || !host_w_up || !host_w_down) return MOE_ERR_INVALID_ARG;
+    if (ns > 0 && (!host_sh_gate || !host_sh_up || !host_sh_down)) return MOE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(table) % 64) return MOE_ERR_INVALID_ARG;
+    if (table_bytes < (size_t)(N + ns) * sizeof(ExpertEntry)) return MOE_ERR_CAPACITY;
+    std::vector<ExpertEntry> h((size_t)(N + ns));
+    std::memset(h.data(), 0, h.size() * sizeof(ExpertEntry));
+    for (int e = 0; e < N + ns; ++e) {
+        const bool sh = e >= N;
+        const void* const* src[3] = {sh ? host_sh_gate : host_w_gate, sh ? host_sh_up : host_w_up,
+                                     sh ? host_sh_down : host_w_down};
+        const int idx = sh ? e - N : e;
+        ExpertEntry& E = h[(size_t)e];
+        E.I = sh ? dims->I_shared : dims->I;
+        for (int m = 0; m < 3; ++m) {
+            const void* p = src[m][idx];
+            if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+            E.w[m] = p;
+        }
+        if (bf16(dims)) MOE_TRY(encode_expert_tmaps(E, dims->d));
+    }
+    MOE_CUDA(cudaMemcpyAsync(table, h.data(), h.size() * sizeof(ExpertEntry), cudaMemcpyHostToDevice,
+                             S(stream)));
+    MOE_CUDA(cudaStreamSynchronize(S(stream)));
+    return MOE_OK;
+}
+
+moe_status moe_route(const moe_dims* dims, const void* x, const void* w_router,
+                     const float* router_bias, const void* x_pre, const void* w_prefetch,
+                     const float* w_ord, const float* theta, float tau, int n_resident,
+                     int32_t* topk_idx, float* topk_gate, float* router_prob, int32_t* delta_hat,
+                     uint64_t* prefetch_mask, int32_t* delta_star, uint64_t* batch_resident,
+                     void* ws, size_t ws_bytes, void* stream) {
+    MOE_TRY(check_dims(dims));
+    MOE_TRY(check_ws(dims, ws, ws_bytes));
+    if (dims->T == 0) return MOE_OK;  // empty batch: nothing to do, buffers may be empty
+    if (!x || !w_router || !topk_idx || !topk_gate || !router_prob || !delta_hat || !prefetch_mask)
+        return MOE_ERR_INVALID_ARG;
+    const bool has_pref = w_prefetch != nullptr;
+    if (has_pref && (!w_ord || !theta || !(tau > 0.f && tau < 1.f))) return MOE_ERR_INVALID_ARG;
+    if (n_resident > 0 && (!has_pref || !batch_resident || n_resident > dims->N)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_router) || (x_pre && !aligned16(x_pre)) ||
+        (w_prefetch && !aligned16(w_prefetch)))
+        return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(*dims);
+    LogitsArgs la;
+    la.x = x; la.x_pre = x_pre; la.w_router = w_router; la.w_prefetch = w_prefetch;
+    la.bias = router_bias; la.w_ord = w_ord; la.T = dims->T; la.d = dims->d; la.N = dims->N;
+    la.has_prefetch = has_pref; la.bf16 = bf16(dims);
+    la.logits_r = ws_at<float>(ws, L.logits_r); la.logits_p = ws_at<float>(ws, L.logits_p);
+    la.score = ws_at<float>(ws, L.score);
+    MOE_CUDA(launch_logits(la, S(stream)));
+    count();
+    RouteSelectArgs ra;
+    ra.logits_r = la.logits_r; ra.logits_p = la.logits_p; ra.score = la.score; ra.theta = theta;
+    ra.logit_tau = has_pref ? (float)std::log((double)tau / (1.0 - (double)tau)) : 0.f;
+    ra.T = dims->T; ra.N = dims->N; ra.k = dims->k; ra.delta_max = dims->delta_max;
+    ra.has_prefetch = has_pref; ra.topk_idx = topk_idx; ra.topk_gate = topk_gate;
+    ra.router_prob = router_prob; ra.delta_hat = delta_hat; ra.prefetch_mask = prefetch_mask;
+    ra.delta_star = delta_star; ra.qp = n_resident > 0 ? ws_at<float>(ws, L.qp) : nullptr;
+    MOE_CUDA(launch_route_select(ra, S(stream)));
+    count();
+    if (n_resident > 0) {
+        MOE_CUDA(launch_batch_resident(ra.qp, dims->T, dims->N, n_resident, batch_resident, S(stream)));
+        count();
+    }
+    return MOE_OK;
+}
+
+moe_status moe_select_resident(const moe_dims* dims, const float* router_prob,
+                               const int32_t* topk_idx, const uint64_t* prefetch_mask,
+                               const uint64_t* resident, int policy, float gamma,
+                               const int32_t* delta_hat, const int32_t* delta_star,
+                               int32_t* final_idx, float* final_gate, int32_t* final_kind,
+                               uint64_t* fetch_mask, int32_t* counters, void* ws, size_t ws_bytes,
+                               void* stream) {
+    MOE_TRY(check_dims(dims));
+    MOE_TRY(check_ws(dims, ws, ws_bytes));
+    if (policy < MOE_MISS_EXACT || policy > MOE_MISS_HYBRID) return MOE_ERR_INVALID_ARG;
+    if ((policy == MOE_MISS_LORE || policy == MOE_MISS_HYBRID) && dims->r <= 0) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(*dims);
+    if (counters) MOE_CUDA(cudaMemsetAsync(counters, 0, MOE_NUM_COUNTERS * sizeof(int32_t), S(stream)));
+    if (fetch_mask) MOE_CUDA(cudaMemsetAsync(fetch_mask, 0, sizeof(uint64_t), S(stream)));
+    if (dims->T == 0) return MOE_OK;
+    if (!router_prob || !topk_idx || !final_idx || !final_gate || !final_kind) return MOE_ERR_INVALID_ARG;
+    SelectArgs a;
+    a.router_prob = router_prob; a.topk_idx = topk_idx; a.prefetch_mask = prefetch_mask;
+    a.resident = resident; a.policy = policy; a.gamma = gamma; a.delta_hat = delta_hat;
+    a.delta_star = delta_star; a.T = dims->T; a.N = dims->N; a.k = dims->k;
+    a.renorm = dims->renorm_topk; a.final_idx = final_idx; a.final_gate = final_gate;
+    a.final_kind = final_kind; a.fetch_mask = fetch_mask; a.counters = counters;
+    a.err = ws_at<DevError>(ws, L.err);
+    MOE_CUDA(launch_select_resident(a, S(stream)));
+    count();
+    return MOE_OK;
+}
+
+moe_status moe_stage_experts(const moe_dims* dims, uint64_t host_fetch_mask,
+                             const void* const* host_w_gate, const void* const* host_w_up,
+                             const void* const* host_w_down, void* const* dev_w_gate,
+                             void* const* dev_w_up, void* const* dev_w_down, void* stage_stream,
+                             void* done_event, size_t* bytes) {
+    MOE_TRY(check_dims(dims));
+    if (!host_w_gate || !host_w_up || !host_w_down || !dev_w_gate || !dev_w_up || !dev_w_down ||
+        !done_event || !bytes)
+        return MOE_ERR_INVALID_ARG;
+    const uint64_t vm = dims->N >= 64 ? ~0ull : ((1ull << dims->N) - 1ull);
+    if (host_fetch_mask & ~vm) return MOE_ERR_INVALID_ARG;
+    const size_t mat = (size_t)dims->I * dims->d * (bf16(dims) ? 2 : 4);
+    size_t queued = 0;
+    int fail_after = g_fail_copies_after.load();
+    int n_copies = 0;
+    for (int e = 0; e < dims->N; ++e) {
+        if (!((host_fetch_mask >> e) & 1)) continue;
+        const void* src[3] = {host_w_gate[e], host_w_up[e], host_w_down[e]};
+        void* dst[3] = {dev_w_gate[e], dev_w_up[e], dev_w_down[e]};
+        for (int m = 0; m < 3; ++m) {
+            if (!src[m] || !dst[m]) { *bytes = queued; return MOE_ERR_INVALID_ARG; }
+            if (fail_after >= 0 && n_copies >= fail_after) { *bytes = queued; return MOE_ERR_STAGING; }
+            if (cudaMemcpyAsync(dst[m], src[m], mat, cudaMemcpyHostToDevice, S(stage_stream)) !=
+                cudaSuccess) {
+                *bytes = queued;
+                return MOE_ERR_STAGING;
+            }
+            ++n_copies;
+            queued += mat;
+        }
+    }
+    *bytes = queued;
+    if (cudaEventRecord(reinterpret_cast<cudaEvent_t>(done_event), S(stage_stream)) != cudaSuccess)
+        return MOE_ERR_STAGING;
+    return MOE_OK;
+}
+
+// test hook: make the n-th and later copies of moe_stage_experts fail (-1: off)
+void moe_testing_fail_copies_after(int n) { g_fail_copies_after.store(n); }
+
+moe_status moe_permute(const moe_dims* dims, const int32_t* final_idx, const int32_t* final_kind,
+                       int32_t* expert_offsets, int32_t* perm, int32_t* inv_perm, void* ws,
+                       size_t ws_bytes, void* stream) {
+    MOE_TRY(check_dims(dims));
+    MOE_TRY(check_ws(dims, ws, ws_bytes));
+    if (!expert_offsets) return MOE_ERR_INVALID_ARG;
+    if (dims->T == 0) {
+        MOE_CUDA(cudaMemsetAsync(expert_offsets, 0, (dims->N + 1) * sizeof(int32_t), S(stream)));
+        return MOE_OK;
+    }
+    if (!final_idx || !final_kind || !perm || !inv_perm) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(*dims);
+    DevError* err = ws_at<DevError>(ws, L.err);
+    PermuteArgs a;
+    a.final_idx = final_idx; a.final_kind = final_kind; a.n_slots = dims->T * dims->k; a.N = dims->N;
+    a.expert_offsets = expert_offsets; a.perm = perm; a.inv_perm = inv_perm; a.err = err;
+    MOE_CUDA(launch_permute(a, S(stream)));
+    count();
+    PlanArgs pa;
+    pa.expert_offsets = expert_offsets; pa.T = dims->T; pa.N = dims->N; pa.n_shared = dims->n_shared;
+    pa.I = dims->I; pa.I_shared = dims->I_shared; pa.rg = gemv_rows(*dims);
+    pa.G = gemv_grid(); pa.max_segs = L.max_segs; pa.max_partial_rows = L.max_partial_rows;
+    pa.hdr = ws_at<PlanHeader>(ws, L.plan_hdr); pa.segs = ws_at<Seg>(ws, L.segs);
+    pa.seg_first = ws_at<int32_t>(ws, L.seg_first); pa.err = err;
+    MOE_CUDA(launch_plan_gemv(pa, S(stream)));
+    count();
+    return MOE_OK;
+}
+
+moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table,
+                          const int32_t* expert_offsets, const int32_t* perm, float keep_frac,
+                          float* y_perm, float* y_shared, void* ws, size_t ws_bytes, void* stream) {
+    MOE_TRY(check_dims(dims));
+    MOE_TRY(check_ws(dims, ws, ws_bytes));
+    if (!(keep_frac > 0.f && keep_frac <= 1.f)) return MOE_ERR_INVALID_ARG;
+    if (keep_frac < 1.f) return MOE_ERR_UNSUPPORTED;
+    if (dims->T == 0) return MOE_OK;
+    if (!x || !table || !expert_offsets || !perm || !y_perm) return MOE_ERR_INVALID_ARG;
+    if (dims->n_shared > 0 && !y_shared) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || reinterpret_cast<uintptr_t>(table) % 64) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(*dims);
+    GemvParams p;
+    p.x = x; p.d = dims->d; p.N = dims->N; p.topk = dims->k; p.NS = gemv_stages(dims->d, bf16(dims));
+    p.perm = perm; p.table = static_cast<const ExpertEntry*>(table);
+    p.hdr = ws_at<PlanHeader>(ws, L.plan_hdr); p.segs = ws_at<Seg>(ws, L.segs);
+    p.partial = ws_at<float>(ws, L.partial); p.err = ws_at<DevError>(ws, L.err);
+    MOE_CUDA(launch_gemv(p, gemv_grid(), bf16(dims), S(stream)));
+    count();
+    GemvReduceArgs r;
+    r.hdr = p.hdr; r.segs = p.segs; r.seg_first = ws_at<int32_t>(ws, L.seg_first);
+    r.expert_offsets = expert_offsets; r.partial = p.partial; r.d = dims->d; r.N = dims->N;
+    r.n_shared = dims->n_shared; r.T = dims->T; r.routed_cap = dims->T * dims->k;
+    r.y_perm = y_perm; r.y_shared = y_shared;
+    MOE_CUDA(launch_gemv_reduce(r, S(stream)));
+    count();
+    return MOE_OK;
+}
+
+moe_status moe_lore(const moe_dims* dims, const void* x, const int32_t* final_idx,
+                    const int32_t* final_kind, const float* final_gate, const void* lore_a,
+                    const void* lore_b, float* y_lore, void* stream) {
+    MOE_TRY(check_dims(dims));
+    if (dims->r <= 0) return MOE_ERR_INVALID_ARG;
+    if (dims->T == 0) return MOE_OK;
+    if (!x || !final_idx || !final_kind || !final_gate || !y_lore || !lore_a || !lore_b)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(lore_a)) return MOE_ERR_INVALID_ARG;
+    LoreArgs a;
+    a.x = x; a.final_idx = final_idx; a.final_kind = final_kind; a.final_gate = final_gate;
+    a.A = lore_a; a.B = lore_b; a.T = dims->T; a.d = dims->d; a.k = dims->k; a.r = dims->r;
+    // without a workspace there is no error word: a bad index skips the slot
+    a.N = dims->N; a.bf16 = bf16(dims); a.y_lore = y_lore; a.err = nullptr;
+    MOE_CUDA(launch_lore(a, S(stream)));
+    count();
+    return MOE_OK;
+}
+
+moe_status moe_combine(const moe_dims* dims, const float* y_perm, const int32_t* inv_perm,
+                       const float* final_gate, const int32_t* final_kind, const float* y_shared,
+                       const float* y_lore, float* out, void* stream) {
+    MOE_TRY(check_dims(dims));
+    if (dims->T == 0) return MOE_OK;
+    if (!y_perm || !inv_perm || !final_gate || !final_kind || !out) return MOE_ERR_INVALID_ARG;
+    CombineArgs a;
+    a.y_perm = y_perm; a.inv_perm = inv_perm; a.final_gate = final_gate; a.final_kind = final_kind;
+    a.y_shared = y_shared; a.y_lore = y_lore; a.T = dims->T; a.d = dims->d; a.k = dims->k; a.out = out;
+    MOE_CUDA(launch_combine(a, S(stream)));
+    count();
+    return MOE_OK;
+}
+
+moe_status moe_layer_forward(const moe_dims* dims, const moe_layer_args* A,
+                             const moe_layer_outputs* O, void* ws, size_t ws_bytes, void* stream) {
+    MOE_TRY(check_dims(dims));
+    if (!A || !O) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(moe_route(dims, A->x, A->w_router, A->router_bias, A->x_pre, A->w_prefetch, A->w_ord,
+                      A->theta, A->tau, A->n_resident, O->topk_idx, O->topk_gate, O->router_prob,
+                      O->delta_hat, O->prefetch_mask, O->delta_star, O->batch_resident, ws,
+                      ws_bytes, stream));
+    const uint64_t* resident = A->n_resident > 0 ? O->batch_resident : A->resident;
+    MOE_TRY(moe_select_resident(dims, O->router_prob, O->topk_idx,
+                                A->use_prefetch_mask ? O->prefetch_mask : nullptr, resident,
+                                A->policy, A->gamma, O->delta_hat, O->delta_star, O->final_idx,
+                                O->final_gate, O->final_kind, O->fetch_mask, O->counters, ws,
+                                ws_bytes, stream));
+    MOE_TRY(moe_permute(dims, O->final_idx, O->final_kind, O->expert_offsets, O->perm, O->inv_perm,
+                        ws, ws_bytes, stream));
+    MOE_TRY(moe_expert_ffn(dims, A->x, A->table, O->expert_offsets, O->perm, A->keep_frac,
+                           O->y_perm, O->y_shared, ws, ws_bytes, stream));
+    const bool lore = dims->r > 0 && A->lore_a && A->lore_b && O->y_lore;
+    if (lore)
+        MOE_TRY(moe_lore(dims, A->x, O->final_idx, O->final_kind, O->final_gate, A->lore_a,
+                         A->lore_b, O->y_lore, stream));
+    MOE_TRY(moe_combine(dims, O->y_perm, O->inv_perm, O->final_gate, O->final_kind,
+                        dims->n_shared > 0 ? O->y_shared : nullptr, lore ? O->y_lore : nullptr,
+                        O->out, stream));
+    return MOE_OK;
+}
+
+moe_status moe_check(void* ws, void* stream, moe_status* device_status, int32_t* detail) {
+    if (!ws || !device_status) return MOE_ERR_INVALID_ARG;
+    MOE_CUDA(cudaStreamSynchronize(S(stream)));
+    DevError h;
+    MOE_CUDA(cudaMemcpy(&h, ws, sizeof(int) * 2, cudaMemcpyDeviceToHost));
+    *device_status = (moe_status)h.code;
+    if (detail) *detail = h.detail;
+    MOE_CUDA(cudaMemset(ws, 0, sizeof(int) * 2));
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,149 @@
+// Stage 3a: token permutation by expert, and the FFN work plan.
+//
+// The layer's slots (t, s) that compute an expert (kinds COMPUTE and FETCH)
+// are grouped by expert into contiguous segments, stable in (t, s) order, so
+// that each expert's weights are streamed once for all of its tokens.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// One block per expert e.  Pass 1 counts the slots routed to experts below e
+// (the segment offset) and to e; pass 2 walks the slots in order and
+// scatters e's slots with a block-wide prefix over 1024-slot chunks.
+// Block 0 also marks LoRE / empty slots with inv_perm = -1.
+__global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict__ final_idx,
+                                                       const int32_t* __restrict__ final_kind,
+                                                       int n_slots, int N,
+                                                       int32_t* __restrict__ expert_offsets,
+                                                       int32_t* __restrict__ perm,
+                                                       int32_t* __restrict__ inv_perm,
+                                                       DevError* __restrict__ err) {
+    __shared__ int red_less[32], red_eq[32];
+    __shared__ int warp_pref[32];
+    __shared__ int s_off;
+    const int e = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    int less = 0, eq = 0;
+    for (int i = tid; i < n_slots; i += blockDim.x) {
+        const int x = final_idx[i];
+        const bool valid = x >= 0 && final_kind[i] != MOE_KIND_LORE;
+        if (x >= N) { if (e == 0) set_error(err, MOE_ERR_DEVICE_INDEX, i); continue; }
+        less += (valid && x < e) ? 1 : 0;
+        eq += (valid && x == e) ? 1 : 0;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        less += __shfl_xor_sync(0xffffffffu, less, o);
+        eq += __shfl_xor_sync(0xffffffffu, eq, o);
+    }
+    if (lane == 0) { red_less[warp] = less; red_eq[warp] = eq; }
+    __syncthreads();
+    if (tid == 0) {
+        int L = 0, E = 0;
+        for (int w = 0; w < nw; ++w) { L += red_less[w]; E += red_eq[w]; }
+        s_off = L;
+        expert_offsets[e] = L;
+        if (e == N - 1) expert_offsets[N] = L + E;
+    }
+    __syncthreads();
+    int running = s_off;
+    for (int base = 0; base < n_slots; base += blockDim.x) {
+        const int i = base + tid;
+        bool mine = false, valid = false;
+        if (i < n_slots) {
+            const int x = final_idx[i];
+            valid = x >= 0 && x < N && final_kind[i] != MOE_KIND_LORE;
+            mine = valid && x == e;
+            if (e == 0 && !valid) inv_perm[i] = -1;
+        }
+        const uint32_t b = __ballot_sync(0xffffffffu, mine);
+        if (lane == 0) warp_pref[warp] = __popc(b);
+        __syncthreads();
+        int before = 0, total = 0;
+        for (int w = 0; w < nw; ++w) {
+            const int c = warp_pref[w];
+            if (w < warp) before += c;
+            total += c;
+        }
+        if (mine) {
+            const int pos = running + before + __popc(b & ((1u << lane) - 1u));
+            perm[pos] = i;
+            inv_perm[i] = pos;
+        }
+        running += total;
+        __syncthreads();
+    }
+}
+
+// FFN plan for the GEMV path (one block, sequential over segments).
+// Segments: shared experts first (rows = tokens, in groups of rg), then each
+// routed expert's permuted rows in groups of rg.  Channels of all segments
+// form one list split evenly over G CTAs; see Seg in common.cuh.
+__global__ void plan_gemv_kernel(const int32_t* __restrict__ expert_offsets, int T, int N,
+                                 int n_shared, int I, int I_shared, int rg, int G, int max_segs,
+                                 int max_partial_rows, PlanHeader* __restrict__ hdr,
+                                 Seg* __restrict__ segs, int32_t* __restrict__ seg_first,
+                                 DevError* __restrict__ err) {
+    if (threadIdx.x != 0) return;
+    int n = 0, ch = 0;
+    auto add = [&](int expert, int row0, int rows, int Ie) {
+        if (n < max_segs) {
+            Seg s;
+            s.expert = expert; s.row0 = row0; s.rows = rows; s.I = Ie; s.ch_start = ch;
+            s.c0 = 0; s.npieces = 0; s.pbase = 0;
+            segs[n] = s;
+        }
+        ++n;
+        ch += Ie;
+    };
+    for (int s = 0; s < n_shared; ++s) {
+        seg_first[N + s] = n;
+        for (int r = 0; r < T; r += rg) add(N + s, r, min(rg, T - r), I_shared);
+    }
+    for (int e = 0; e < N; ++e) {
+        seg_first[e] = n;
+        const int a = expert_offsets[e], b = expert_offsets[e + 1];
+        for (int r = a; r < b; r += rg) add(e, r, min(rg, b - r), I);
+    }
+    seg_first[N + n_shared] = n;
+    PlanHeader h;
+    h.G = G; h.rg = rg;
+    // A plan that does not fit the workspace is published empty (no segment,
+    // no channel, no routed row): the FFN kernels then do nothing, and the
+    // error word says why, instead of indexing past the tables.
+    auto publish_empty = [&](int detail) {
+        set_error(err, MOE_ERR_CAPACITY, detail);
+        h.n_seg = 0; h.total_ch = 0; h.P = 1; h.n_partial_rows = 0; h.n_routed_rows = 0;
+        *hdr = h;
+    };
+    if (n > max_segs) { publish_empty(n); return; }
+    const int P = ch > 0 ? (ch + G - 1) / G : 1;
+    int pbase = 0;
+    for (int i = 0; i < n; ++i) {
+        Seg& s = segs[i];
+        s.c0 = s.ch_start / P;
+        s.npieces = (s.ch_start + s.I - 1) / P - s.c0 + 1;
+        s.pbase = pbase;
+        pbase += s.npieces * s.rows;
+    }
+    if (pbase > max_partial_rows) { publish_empty(pbase); return; }
+    h.n_seg = n; h.total_ch = ch; h.P = P; h.n_partial_rows = pbase;
+    h.n_routed_rows = expert_offsets[N];
+    *hdr = h;
+}
+
+cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st) {
+    permute_kernel<<<a.N, 1024, 0, st>>>(a.final_idx, a.final_kind, a.n_slots, a.N,
+                                         a.expert_offsets, a.perm, a.inv_perm, a.err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_plan_gemv(const PlanArgs& a, cudaStream_t st) {
+    plan_gemv_kernel<<<1, 32, 0, st>>>(a.expert_offsets, a.T, a.N, a.n_shared, a.I, a.I_shared,
+                                       a.rg, a.G, a.max_segs, a.max_partial_rows, a.hdr, a.segs,
+                                       a.seg_first, a.err);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,396 @@
+// Stage 1 and 2 kernels: router / prefetch-router logits, per-token warp
+// selection (softmax, top-k, ordinal-CDF budget, prefetch set, delta*), the
+// batch resident set, and the per-token miss handling (stall-free
+// substitution, LoRE, fetch).
+//
+// APEX: Adaptive Expert Prefetching for Edge MoE Inference — §4.1 (prefetch
+// router: linear + softmax on the pre-attention state), §4.2 (delta*,
+// p_delta = sigmoid(theta_delta - w.x), delta_hat = min{delta : p_delta >=
+// tau}), §4.3 (Algorithm 1 stall_free_select; correctness-preserving mode).
+// SPICE write-up, LoRE section: low-confidence misses use the surrogate.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Logits: one warp per output row o (router rows 0..N-1 on x, prefetch rows
+// N..2N-1 and the ordinal scorer row 2N on x_pre), for a tile of TT tokens.
+// Lanes split d in 16-byte chunks; each lane sums its chunk products in order
+// and the warp adds the 32 partial sums as a tree, which keeps the fp32
+// rounding error of a logit near 1e-7 (the decisions made on these logits are
+// compared bit-exactly with a float64 reference, away from near-ties).
+template <typename W, int TT>
+__global__ void __launch_bounds__(256) route_logits_kernel(
+    const W* __restrict__ x, const W* __restrict__ x_pre, const W* __restrict__ w_router,
+    const float* __restrict__ bias, const W* __restrict__ w_prefetch, const float* __restrict__ w_ord,
+    int T, int d, int N, int n_out, int rows_per_block, float* __restrict__ logits_r,
+    float* __restrict__ logits_p, float* __restrict__ score) {
+    constexpr int V = Vec<W>::n;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    W* xs = reinterpret_cast<W*>(smem_raw);                 // [TT][d]
+    W* xps = xs + (size_t)TT * d;                             // [TT][d] (x_pre)
+    const int t0 = blockIdx.x * TT;
+    const int nt = min(TT, T - t0);
+    const int nchunk = d / V;
+    const bool sep = (x_pre != x);
+    // stage the token tile (16-byte copies)
+    for (int i = threadIdx.x; i < TT * nchunk; i += blockDim.x) {
+        int t = i / nchunk, q = i % nchunk;
+        uint4 v = make_uint4(0, 0, 0, 0), vp = make_uint4(0, 0, 0, 0);
+        if (t < nt) {
+            v = reinterpret_cast<const uint4*>(x + (size_t)(t0 + t) * d)[q];
+            if (sep) vp = reinterpret_cast<const uint4*>(x_pre + (size_t)(t0 + t) * d)[q];
+        }
+        reinterpret_cast<uint4*>(xs + (size_t)t * d)[q] = v;
+        if (sep) reinterpret_cast<uint4*>(xps + (size_t)t * d)[q] = vp;
+    }
+    __syncthreads();
+    const W* xsp = sep ? xps : xs;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int o_begin = blockIdx.y * rows_per_block;
+    const int o_end = min(n_out, o_begin + rows_per_block);
+    for (int o = o_begin + warp; o < o_end; o += nw) {
+        const W* wrow;
+        const W* tile;
+        bool is_ord = false;
+        if (o < N) { wrow = w_router + (size_t)o * d; tile = xs; }
+        else if (o < 2 * N) { wrow = w_prefetch + (size_t)(o - N) * d; tile = xsp; }
+        else { wrow = nullptr; tile = xsp; is_ord = true; }
+        float acc[TT];
+#pragma unroll
+        for (int t = 0; t < TT; ++t) acc[t] = 0.f;
+        for (int q = lane; q < nchunk; q += 32) {
+            float wv[V];
+            if (!is_ord) {
+                uint4 raw = reinterpret_cast<const uint4*>(wrow)[q];
+                unpack16(raw, wv, (W*)nullptr);
+            } else {
+#pragma unroll
+                for (int j = 0; j < V; ++j) wv[j] = w_ord[q * V + j];
+            }
+#pragma unroll
+            for (int t = 0; t < TT; ++t) {
+                uint4 raw = reinterpret_cast<const uint4*>(tile + (size_t)t * d)[q];
+                float xv[V];
+                unpack16(raw, xv, (W*)nullptr);
+#pragma unroll
+                for (int j = 0; j < V; ++j) acc[t] = fmaf(xv[j], wv[j], acc[t]);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < TT; ++t) acc[t] = warp_sum(acc[t]);
+        if (lane == 0) {
+            for (int t = 0; t < nt; ++t) {
+                const int tok = t0 + t;
+                if (o < N) logits_r[(size_t)tok * N + o] = acc[t] + (bias ? bias[o] : 0.f);
+                else if (o < 2 * N) logits_p[(size_t)tok * N + (o - N)] = acc[t];
+                else score[tok] = acc[t];
+            }
+        }
+    }
+}
+
+// (value, index) argmax across the warp: larger value wins, equal values go
+// to the lower index.  Lanes with no candidate pass index = INT_MAX.
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        float ov = __shfl_xor_sync(0xffffffffu, v, o);
+        int oi = __shfl_xor_sync(0xffffffffu, i, o);
+        if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
+    }
+}
+
+// best of this lane's two candidates (experts lane, lane + 32) within `mask`
+__device__ __forceinline__ void lane_best(float v0, float v1, uint64_t mask, int lane, float& v, int& i) {
+    v = -INFINITY;
+    i = 0x7fffffff;
+    if ((mask >> lane) & 1) { v = v0; i = lane; }
+    if ((mask >> (lane + 32)) & 1) {
+        if (i == 0x7fffffff || v1 > v) { v = v1; i = lane + 32; }
+    }
+}
+
+__device__ __forceinline__ uint64_t valid_mask(int N) {
+    return N >= 64 ? ~0ull : ((1ull << N) - 1ull);
+}
+
+// ---------------------------------------------------------------------------
+// One warp per token: softmax, top-k, delta_hat, prefetch set, delta*.
+__global__ void __launch_bounds__(256) route_select_kernel(
+    const float* __restrict__ logits_r, const float* __restrict__ logits_p,
+    const float* __restrict__ score, const float* __restrict__ theta, float logit_tau, int T,
+    int N, int k, int delta_max, int has_prefetch, int32_t* __restrict__ topk_idx,
+    float* __restrict__ topk_gate, float* __restrict__ router_prob, int32_t* __restrict__ delta_hat,
+    uint64_t* __restrict__ prefetch_mask, int32_t* __restrict__ delta_star, float* __restrict__ qp) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= T) return;
+    const int t = warp;
+    const uint64_t vm = valid_mask(N);
+    const int e0 = lane, e1 = lane + 32;
+    const float l0 = e0 < N ? logits_r[(size_t)t * N + e0] : -INFINITY;
+    const float l1 = e1 < N ? logits_r[(size_t)t * N + e1] : -INFINITY;
+    // softmax
+    const float m = warp_max(fmaxf(l0, l1));
+    const float p0 = e0 < N ? expf(l0 - m) : 0.f;
+    const float p1 = e1 < N ? expf(l1 - m) : 0.f;
+    const float s = warp_sum(p0 + p1);
+    const float a0 = p0 / s, a1 = p1 / s;
+    if (e0 < N) router_prob[(size_t)t * N + e0] = a0;
+    if (e1 < N) router_prob[(size_t)t * N + e1] = a1;
+    // top-k of the logits, descending, lowest index on ties
+    uint64_t remaining = vm, routed = 0;
+    for (int j = 0; j < k; ++j) {
+        float v; int i;
+        lane_best(l0, l1, remaining, lane, v, i);
+        warp_argmax(v, i);
+        routed |= 1ull << i;
+        remaining &= ~(1ull << i);
+        if (lane == 0) {
+            topk_idx[(size_t)t * k + j] = i;
+        }
+        const float ai = __shfl_sync(0xffffffffu, i < 32 ? a0 : a1, i & 31);
+        if (lane == 0) topk_gate[(size_t)t * k + j] = ai;
+    }
+    if (!has_prefetch) {
+        if (lane == 0) {
+            delta_hat[t] = 0;
+            prefetch_mask[t] = ~0ull;
+            if (delta_star) delta_star[t] = 0;
+        }
+        return;
+    }
+    // delta_hat = smallest delta with theta_delta - s >= logit(tau)
+    // (the same test as sigmoid(theta_delta - s) >= tau; sigmoid is monotone)
+    const float sc = score[t];
+    const bool c0 = lane <= delta_max && (theta[lane] - sc) >= logit_tau;
+    const bool c1 = lane + 32 <= delta_max && (theta[lane + 32] - sc) >= logit_tau;
+    const uint32_t b0 = __ballot_sync(0xffffffffu, c0), b1 = __ballot_sync(0xffffffffu, c1);
+    int dh = delta_max;
+    if (b0) dh = __ffs(b0) - 1;
+    else if (b1) dh = 32 + __ffs(b1) - 1;
+    dh = min(dh, delta_max);
+    // rank of each expert in the prefetch logits
+    const float q0 = e0 < N ? logits_p[(size_t)t * N + e0] : -INFINITY;
+    const float q1 = e1 < N ? logits_p[(size_t)t * N + e1] : -INFINITY;
+    int r0 = 0, r1 = 0;
+    for (int j = 0; j < N; ++j) {
+        const float qj = __shfl_sync(0xffffffffu, j < 32 ? q0 : q1, j & 31);
+        r0 += (qj > q0 || (qj == q0 && j < e0)) ? 1 : 0;
+        r1 += (qj > q1 || (qj == q1 && j < e1)) ? 1 : 0;
+    }
+    const int lim = k + dh;
+    const uint32_t in0 = __ballot_sync(0xffffffffu, e0 < N && r0 < lim);
+    const uint32_t in1 = __ballot_sync(0xffffffffu, e1 < N && r1 < lim);
+    const uint64_t pm = (uint64_t)in0 | ((uint64_t)in1 << 32);
+    // delta* = max(0, max over routed experts of rank_p + 1 - k)
+    int worst = -1;
+    if ((routed >> e0) & 1) worst = max(worst, r0);
+    if ((routed >> e1) & 1) worst = max(worst, r1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) worst = max(worst, __shfl_xor_sync(0xffffffffu, worst, o));
+    if (lane == 0) {
+        delta_hat[t] = dh;
+        prefetch_mask[t] = pm;
+        if (delta_star) delta_star[t] = max(0, worst + 1 - k);
+    }
+    if (qp) {
+        const float mq = warp_max(fmaxf(q0, q1));
+        const float z0 = e0 < N ? expf(q0 - mq) : 0.f;
+        const float z1 = e1 < N ? expf(q1 - mq) : 0.f;
+        const float zs = warp_sum(z0 + z1);
+        if (e0 < N) qp[(size_t)t * N + e0] = z0 / zs;
+        if (e1 < N) qp[(size_t)t * N + e1] = z1 / zs;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Batch resident set: the n_res experts with the largest prefetch probability
+// summed over the tokens, in a fixed summation order (one block).
+__global__ void __launch_bounds__(1024) batch_resident_kernel(const float* __restrict__ qp, int T,
+                                                              int N, int n_res,
+                                                              uint64_t* __restrict__ out) {
+    __shared__ float part[16][64];
+    __shared__ float tot[64];
+    const int e = threadIdx.x & 63, g = threadIdx.x >> 6;  // 16 groups
+    float acc = 0.f;
+    if (e < N)
+        for (int t = g; t < T; t += 16) acc += qp[(size_t)t * N + e];
+    part[g][e] = acc;
+    __syncthreads();
+    if (threadIdx.x < 64) {
+        float s = 0.f;
+        for (int i = 0; i < 16; ++i) s += part[i][threadIdx.x];
+        tot[threadIdx.x] = s;
+    }
+    __syncthreads();
+    __shared__ uint32_t bits[2];
+    if (threadIdx.x < 64) {
+        const int me = threadIdx.x;
+        int rank = 0;
+        if (me < N) {
+            for (int j = 0; j < N; ++j)
+                rank += (tot[j] > tot[me] || (tot[j] == tot[me] && j < me)) ? 1 : 0;
+        }
+        const uint32_t b = __ballot_sync(0xffffffffu, me < N && rank < n_res);
+        if ((me & 31) == 0) bits[me >> 5] = b;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) *out = (uint64_t)bits[0] | ((uint64_t)bits[1] << 32);
+}
+
+// ---------------------------------------------------------------------------
+// Miss handling, one warp per token (APEX §4.3 Algorithm 1; SPICE LoRE).
+__global__ void __launch_bounds__(256) select_resident_kernel(
+    const float* __restrict__ router_prob, const int32_t* __restrict__ topk_idx,
+    const uint64_t* __restrict__ prefetch_mask, const uint64_t* __restrict__ resident, int policy,
+    float gamma, const int32_t* __restrict__ delta_hat, const int32_t* __restrict__ delta_star, int T,
+    int N, int k, int renorm, int32_t* __restrict__ final_idx, float* __restrict__ final_gate,
+    int32_t* __restrict__ final_kind, uint64_t* __restrict__ fetch_mask,
+    int32_t* __restrict__ counters, DevError* __restrict__ err) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= T) return;
+    const int t = warp;
+    const uint64_t vm = valid_mask(N);
+    const int e0 = lane, e1 = lane + 32;
+    const float a0 = e0 < N ? router_prob[(size_t)t * N + e0] : -INFINITY;
+    const float a1 = e1 < N ? router_prob[(size_t)t * N + e1] : -INFINITY;
+    uint64_t routed = 0;
+    bool bad = false;
+    for (int j = 0; j < k; ++j) {
+        const int e = topk_idx[(size_t)t * k + j];
+        if (e < 0 || e >= N) bad = true;
+        else routed |= 1ull << e;
+    }
+    if (bad) {
+        if (lane == 0) set_error(err, MOE_ERR_DEVICE_INDEX, t);
+        return;
+    }
+    const uint64_t pref = prefetch_mask ? prefetch_mask[t] : ~0ull;
+    const uint64_t res = resident ? *resident : ~0ull;
+    const uint64_t avail = pref & res & vm;
+    const uint64_t missing = routed & ~avail;
+    uint64_t lore = 0, fetch = 0, to_sub = 0;
+    for (uint64_t mm = missing; mm; mm &= mm - 1) {
+        const int e = __ffsll((long long)mm) - 1;
+        const uint64_t bit = 1ull << e;
+        const float ae = __shfl_sync(0xffffffffu, e < 32 ? a0 : a1, e & 31);
+        switch (policy) {
+            case MOE_MISS_EXACT: fetch |= bit; break;
+            case MOE_MISS_LORE: lore |= bit; break;
+            case MOE_MISS_SUBSTITUTE: to_sub |= bit; break;
+            default:
+                if (ae < gamma) lore |= bit; else to_sub |= bit;
+        }
+    }
+    // substitutes: the available, non-routed experts with the largest router
+    // probability, one per substituted miss
+    uint64_t pool = avail & ~routed, subs = 0;
+    const int n_sub = __popcll(to_sub);
+    bool shortfall = false;
+    for (int j = 0; j < n_sub; ++j) {
+        if (!pool) { shortfall = true; break; }
+        float v; int i;
+        lane_best(a0, a1, pool, lane, v, i);
+        warp_argmax(v, i);
+        subs |= 1ull << i;
+        pool &= ~(1ull << i);
+    }
+    const uint64_t fin = (routed & ~missing) | lore | fetch | subs;
+    // canonical slot order: descending router probability, lowest index first
+    uint64_t rem = fin;
+    float gsum = 0.f;
+    int idx[kMaxTopK];
+    float gate[kMaxTopK];
+    for (int j = 0; j < k; ++j) {
+        if (!rem) { idx[j] = -1; gate[j] = 0.f; continue; }
+        float v; int i;
+        lane_best(a0, a1, rem, lane, v, i);
+        warp_argmax(v, i);
+        idx[j] = i;
+        gate[j] = v;
+        gsum += v;
+        rem &= ~(1ull << i);
+    }
+    if (lane == 0) {
+        for (int j = 0; j < k; ++j) {
+            const size_t sl = (size_t)t * k + j;
+            const int e = idx[j];
+            final_idx[sl] = e;
+            final_gate[sl] = (renorm && gsum > 0.f) ? gate[j] / gsum : gate[j];
+            int kind = MOE_KIND_COMPUTE;
+            if (e >= 0 && ((lore >> e) & 1)) kind = MOE_KIND_LORE;
+            else if (e >= 0 && ((fetch >> e) & 1)) kind = MOE_KIND_FETCH;
+            final_kind[sl] = kind;
+        }
+        if (fetch_mask && fetch) atomicOr(reinterpret_cast<unsigned long long*>(fetch_mask),
+                                          (unsigned long long)fetch);
+        if (counters) {
+            atomicAdd(&counters[MOE_CNT_HIT], __popcll(routed & avail));
+            atomicAdd(&counters[MOE_CNT_SUBSTITUTE], __popcll(subs));
+            atomicAdd(&counters[MOE_CNT_LORE], __popcll(lore));
+            atomicAdd(&counters[MOE_CNT_FETCH], __popcll(fetch));
+            if (prefetch_mask) atomicAdd(&counters[MOE_CNT_OVERLAP], (routed & ~pref) == 0 ? 1 : 0);
+            if (delta_hat) atomicAdd(&counters[MOE_CNT_DELTA_HAT], delta_hat[t]);
+            if (delta_star) atomicAdd(&counters[MOE_CNT_DELTA_STAR], delta_star[t]);
+            if (shortfall) atomicAdd(&counters[MOE_CNT_SHORTFALL], 1);
+        }
+        if (shortfall) set_error(err, MOE_ERR_CAPACITY, t);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host launchers
+
+template <typename W>
+static cudaError_t launch_logits_t(const LogitsArgs& a, cudaStream_t st) {
+    constexpr int TT = 8;
+    const int n_out = a.has_prefetch ? 2 * a.N + 1 : a.N;
+    const int rows_per_block = 8;
+    dim3 grid((a.T + TT - 1) / TT, (n_out + rows_per_block - 1) / rows_per_block);
+    const size_t smem = (size_t)2 * TT * a.d * sizeof(W);
+    if (smem > 48 * 1024) {
+        cudaError_t e = allow_max_smem(route_logits_kernel<W, TT>);
+        if (e != cudaSuccess) return e;
+    }
+    route_logits_kernel<W, TT><<<grid, 256, smem, st>>>(
+        (const W*)a.x, (const W*)(a.x_pre ? a.x_pre : a.x), (const W*)a.w_router, a.bias,
+        (const W*)a.w_prefetch, a.w_ord, a.T, a.d, a.N, n_out, rows_per_block, a.logits_r,
+        a.logits_p, a.score);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_logits(const LogitsArgs& a, cudaStream_t st) {
+    return a.bf16 ? launch_logits_t<__nv_bfloat16>(a, st) : launch_logits_t<float>(a, st);
+}
+
+cudaError_t launch_route_select(const RouteSelectArgs& a, cudaStream_t st) {
+    const int warps = 8;
+    dim3 grid((a.T + warps - 1) / warps);
+    route_select_kernel<<<grid, warps * 32, 0, st>>>(
+        a.logits_r, a.logits_p, a.score, a.theta, a.logit_tau, a.T, a.N, a.k, a.delta_max,
+        a.has_prefetch, a.topk_idx, a.topk_gate, a.router_prob, a.delta_hat, a.prefetch_mask,
+        a.delta_star, a.qp);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_batch_resident(const float* qp, int T, int N, int n_res, uint64_t* out,
+                                  cudaStream_t st) {
+    batch_resident_kernel<<<1, 1024, 0, st>>>(qp, T, N, n_res, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_select_resident(const SelectArgs& a, cudaStream_t st) {
+    const int warps = 8;
+    dim3 grid((a.T + warps - 1) / warps);
+    select_resident_kernel<<<grid, warps * 32, 0, st>>>(
+        a.router_prob, a.topk_idx, a.prefetch_mask, a.resident, a.policy, a.gamma, a.delta_hat,
+        a.delta_star, a.T, a.N, a.k, a.renorm, a.final_idx, a.final_gate, a.final_kind,
+        a.fetch_mask, a.counters, a.err);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,160 @@
+"""Device-side holders for one MoE layer: weights, expert table, workspace and
+output buffers, wired to the C ABI.  Marshalling only — all arithmetic runs
+in the library's CUDA kernels."""
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import (MOE_NUM_COUNTERS, make_dims, moe_expert_table_init, moe_expert_table_size,
+               moe_layer_args, moe_layer_forward, moe_layer_outputs, moe_workspace_size)
+
+
+def as_i64(mask: int) -> int:
+    """uint64 bit pattern as a signed int64 value."""
+    mask &= (1 << 64) - 1
+    return mask - (1 << 64) if mask >= (1 << 63) else mask
+
+
+def as_u64(v: int) -> int:
+    return int(v) & ((1 << 64) - 1)
+
+
+class DeviceLayer:
+    """Weights of one layer on the GPU plus its expert table and workspace.
+
+    cfg: a workloads.LayerConfig; W: a workloads.LayerWeights (float32 arrays
+    holding the exact parameter values).  T_max: the largest token count the
+    workspace is sized for.
+    """
+
+    def __init__(self, cfg, W, T_max: int, device: str = "cuda"):
+        self.cfg = cfg
+        self.dims = make_dims(T_max, cfg.d, cfg.N, cfg.k, cfg.I, cfg.n_shared, cfg.I_shared, cfg.r,
+                              cfg.delta_max, cfg.wtype)
+        self.dt = torch.bfloat16 if cfg.wtype == "bf16" else torch.float32
+        dev = torch.device(device)
+        self.device = dev
+
+        def t(a, dt=None):
+            return torch.from_numpy(a).to(dev).to(dt or self.dt).contiguous()
+
+        self.w_router = t(W.w_router)
+        self.w_prefetch = t(W.w_prefetch)
+        self.w_ord = t(W.w_ord, torch.float32)
+        self.theta = t(W.theta, torch.float32)
+        self.router_bias = None if W.router_bias is None else t(W.router_bias, torch.float32)
+        self.w_gate = torch.empty((cfg.N, cfg.I, cfg.d), dtype=self.dt, device=dev)
+        self.w_up = torch.empty_like(self.w_gate)
+        self.w_down = torch.empty_like(self.w_gate)
+        for e in range(cfg.N):  # one expert at a time keeps host->device staging small
+            self.w_gate[e].copy_(torch.from_numpy(W.w_gate[e]))
+            self.w_up[e].copy_(torch.from_numpy(W.w_up[e]))
+            self.w_down[e].copy_(torch.from_numpy(W.w_down[e]))
+        ns = max(cfg.n_shared, 0)
+        self.sh_gate = t(W.sh_gate) if ns else None
+        self.sh_up = t(W.sh_up) if ns else None
+        self.sh_down = t(W.sh_down) if ns else None
+        self.lore_a = t(W.lore_a) if cfg.r > 0 else None
+        self.lore_b = t(W.lore_b) if cfg.r > 0 else None
+        self.table = torch.empty(moe_expert_table_size(self.dims), dtype=torch.uint8, device=dev)
+        self.ws = torch.zeros(moe_workspace_size(self.dims), dtype=torch.uint8, device=dev)
+        self.resident = torch.full((1,), as_i64((1 << 64) - 1), dtype=torch.int64, device=dev)
+        self.bind_table()
+
+    def bind_table(self):
+        sh = [list(self.sh_gate), list(self.sh_up), list(self.sh_down)] if self.cfg.n_shared else [None] * 3
+        moe_expert_table_init(self.dims, list(self.w_gate), list(self.w_up), list(self.w_down),
+                              *sh, self.table)
+
+    def set_resident(self, mask: int):
+        self.resident.fill_(as_i64(mask))
+
+    def clone(self) -> "DeviceLayer":
+        """Another copy of the layer: expert weights in new device buffers (same
+        values), its own expert table and workspace; router and LoRE tensors are
+        shared."""
+        other = object.__new__(DeviceLayer)
+        other.__dict__.update(self.__dict__)
+        for name in ("w_gate", "w_up", "w_down", "sh_gate", "sh_up", "sh_down"):
+            t = getattr(self, name)
+            setattr(other, name, None if t is None else t.clone())
+        other.table = torch.empty_like(self.table)
+        other.ws = torch.zeros_like(self.ws)
+        other.resident = self.resident.clone()
+        other.bind_table()
+        return other
+
+
+class LayerBuffers:
+    """Outputs of moe_layer_forward for up to T tokens."""
+
+    def __init__(self, layer: DeviceLayer, T: int):
+        cfg, dev = layer.cfg, layer.device
+        k, N, d = cfg.k, cfg.N, cfg.d
+        i32 = dict(dtype=torch.int32, device=dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        i64 = dict(dtype=torch.int64, device=dev)
+        self.T = T
+        self.topk_idx = torch.empty((T, k), **i32)
+        self.topk_gate = torch.empty((T, k), **f32)
+        self.router_prob = torch.empty((T, N), **f32)
+        self.delta_hat = torch.empty((T,), **i32)
+        self.prefetch_mask = torch.empty((T,), **i64)
+        self.delta_star = torch.empty((T,), **i32)
+        self.batch_resident = torch.zeros((1,), **i64)
+        self.final_idx = torch.empty((T, k), **i32)
+        self.final_gate = torch.empty((T, k), **f32)
+        self.final_kind = torch.empty((T, k), **i32)
+        self.fetch_mask = torch.zeros((1,), **i64)
+        self.counters = torch.zeros((MOE_NUM_COUNTERS,), **i32)
+        self.expert_offsets = torch.empty((N + 1,), **i32)
+        self.perm = torch.empty((T * k,), **i32)
+        self.inv_perm = torch.empty((T * k,), **i32)
+        self.y_perm = torch.empty((T * k, d), **f32)
+        self.y_shared = torch.empty((T, d), **f32) if cfg.n_shared else None
+        self.y_lore = torch.empty((T, d), **f32) if cfg.r > 0 else None
+        self.out = torch.empty((T, d), **f32)
+
+    def outputs_struct(self) -> moe_layer_outputs:
+        o = moe_layer_outputs()
+        for name, _ in moe_layer_outputs._fields_:
+            tns = getattr(self, name)
+            setattr(o, name, None if tns is None else tns.data_ptr())
+        return o
+
+
+def layer_args(layer: DeviceLayer, x, x_pre=None, policy=None, gamma=None, tau=None,
+               keep_frac=None, n_resident=None, use_prefetch_mask=None) -> moe_layer_args:
+    cfg = layer.cfg
+    a = moe_layer_args()
+    a.x = x.data_ptr()
+    a.x_pre = None if x_pre is None else x_pre.data_ptr()
+    a.w_router = layer.w_router.data_ptr()
+    a.router_bias = None if layer.router_bias is None else layer.router_bias.data_ptr()
+    a.w_prefetch = layer.w_prefetch.data_ptr()
+    a.w_ord = layer.w_ord.data_ptr()
+    a.theta = layer.theta.data_ptr()
+    a.tau = cfg.tau if tau is None else tau
+    a.n_resident = max(cfg.n_resident, 0) if n_resident is None else n_resident
+    a.resident = layer.resident.data_ptr()
+    a.use_prefetch_mask = int(cfg.use_prefetch_mask if use_prefetch_mask is None else use_prefetch_mask)
+    a.policy = cfg.policy if policy is None else policy
+    a.gamma = cfg.gamma if gamma is None else gamma
+    a.keep_frac = cfg.keep_frac if keep_frac is None else keep_frac
+    a.table = layer.table.data_ptr()
+    a.lore_a = None if layer.lore_a is None else layer.lore_a.data_ptr()
+    a.lore_b = None if layer.lore_b is None else layer.lore_b.data_ptr()
+    return a
+
+
+def forward(layer: DeviceLayer, bufs: LayerBuffers, x, stream=None, **kw):
+    """One layer forward through moe_layer_forward for x [T, d] (T <= bufs.T)."""
+    T = x.shape[0]
+    assert T <= bufs.T and x.is_contiguous() and x.dtype == layer.dt
+    dims = layer.dims.with_T(T)
+    args = layer_args(layer, x, **kw)
+    outs = bufs.outputs_struct()
+    moe_layer_forward(dims, args, outs, layer.ws, stream)
+    return bufs

@@ -1,0 +1,294 @@
+/*
+ * moe.h — C ABI of the GB300 (sm_103a) offloading-aware MoE layer forward.
+ *
+ * One MoE layer forward in five stages, each a call below:
+ *   1. moe_route            router softmax/top-k, APEX prefetch router,
+ *                           ordinal-CDF budget delta_hat, top-(k+delta_hat)
+ *                           prefetch set, delta* (metric)
+ *   2. moe_select_resident  stall-free substitution / LoRE / fetch per miss
+ *   3. moe_permute          token permutation by expert
+ *      moe_expert_ffn       grouped SwiGLU expert FFN (+ shared experts)
+ *   4. moe_lore             SPICE LoRE surrogate for LoRE slots
+ *   5. moe_combine          gate-weighted combine plus shared experts
+ * plus moe_stage_experts (pinned host -> HBM expert copies on a side stream)
+ * and moe_layer_forward (all stages chained on one stream).
+ *
+ * Conventions (all entry points):
+ *   - Every function returns moe_status; nothing aborts, traps, throws or
+ *     prints.  Host-detectable argument errors are returned before any work
+ *     is queued.  Errors found by a kernel (a bad expert index, an available
+ *     set smaller than k, a timed-out wait) are recorded in the device error
+ *     word inside the workspace and reported by moe_check().
+ *   - Pointers are DEVICE pointers unless the name starts with host_.
+ *     The caller allocates and owns every buffer, including the workspace
+ *     (size from moe_workspace_size) and the expert table (size from
+ *     moe_expert_table_size).  The library allocates no memory.
+ *   - All work is queued asynchronously on the caller's stream
+ *     (a cudaStream_t passed as void*; NULL = the legacy default stream).
+ *     Only moe_check(), moe_expert_table_init() and moe_stage_experts()'s
+ *     host-side bookkeeping synchronise.
+ *   - Row-major layouts throughout.  Activations and weights share the
+ *     layer's weight type (MOE_DTYPE_BF16 or MOE_DTYPE_F32); router
+ *     probabilities, gates and outputs are float32; indices int32; expert
+ *     sets are uint64 bitmasks (bit e = expert e, so N <= 64).
+ *   - Ties are broken towards the lowest expert / channel index.
+ *
+ * Sources (page titles and sections):
+ *   APEX: Adaptive Expert Prefetching for Edge MoE Inference (blog write-up),
+ *     §4.1 prefetch router, §4.2 delta* and the ordinal-logistic CDF,
+ *     §4.3 execution modes and Algorithm 1 (stall_free_select).
+ *   SPICE: Speculative Prefetching with Low-Rank Expert Surrogates and
+ *     Heterogeneous Orchestration for MoE Inference (PaperDaily write-up),
+ *     sections on the LoRE low-rank surrogate and CPU-GPU orchestration.
+ *   FloE: On-the-Fly MoE Inference on Memory-constrained GPU (paper notes),
+ *     method §1 (contextual sparsity forward), §3 (sparse GEMV, compact
+ *     asynchronous transfer).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* NULL where a buffer is required, bad size, misaligned pointer */
+    MOE_ERR_UNSUPPORTED = 2,   /* N > 64, k > 8, d not a multiple of 256, dtype not handled */
+    MOE_ERR_CAPACITY = 3,      /* workspace/table too small, or (device) |A_t| < k */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime call failed (launch, copy, event) */
+    MOE_ERR_STAGING = 5,       /* an expert copy could not be queued */
+    MOE_ERR_TIMEOUT = 6,       /* (device) a bounded wait inside a kernel gave up */
+    MOE_ERR_DEVICE_INDEX = 7   /* (device) an expert or slot index out of range */
+} moe_status;
+
+typedef enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1 } moe_dtype;
+
+/* What happens to a routed expert that is not in the available set A_t. */
+typedef enum {
+    MOE_MISS_EXACT = 0,       /* fetch it and compute it: output = plain MoE (APEX §4.3,
+                                 correctness-preserving mode) */
+    MOE_MISS_SUBSTITUTE = 1,  /* stall-free substitution (APEX §4.3, Algorithm 1) */
+    MOE_MISS_LORE = 2,        /* LoRE surrogate y_shared + B_e A_e x (SPICE, LoRE section) */
+    MOE_MISS_HYBRID = 3       /* router prob < gamma -> LoRE, else substitute */
+} moe_miss_policy;
+
+/* Kind of each final slot. */
+typedef enum { MOE_KIND_COMPUTE = 0, MOE_KIND_FETCH = 1, MOE_KIND_LORE = 2 } moe_slot_kind;
+
+/* Layer dimensions.  T: tokens in this call (<= the T the workspace was sized
+ * for); d: hidden size (multiple of 256); N: routed experts (<= 64);
+ * k: top-k (<= 8); I: routed-expert intermediate size (multiple of 64);
+ * n_shared / I_shared: shared experts and their intermediate size;
+ * r: LoRE rank (0: no LoRE factors); delta_max: largest prefetch budget
+ * (N - k); wtype: weight/activation type; renorm_topk: 1 to renormalise the
+ * final gates over the final set (0: gates are the router probabilities). */
+typedef struct {
+    int T, d, N, k, I, n_shared, I_shared, r, delta_max;
+    moe_dtype wtype;
+    int renorm_topk;
+} moe_dims;
+
+/* Slot counters written by moe_select_resident (int32[MOE_NUM_COUNTERS]). */
+enum {
+    MOE_CNT_HIT = 0,        /* routed and available: computed as routed */
+    MOE_CNT_SUBSTITUTE = 1, /* slots given to a substitute expert */
+    MOE_CNT_LORE = 2,       /* slots served by the LoRE surrogate */
+    MOE_CNT_FETCH = 3,      /* slots whose expert must be fetched (EXACT) */
+    MOE_CNT_OVERLAP = 4,    /* tokens whose routed set lies inside their prefetch set */
+    MOE_CNT_DELTA_HAT = 5,  /* sum over tokens of delta_hat */
+    MOE_CNT_DELTA_STAR = 6, /* sum over tokens of delta* */
+    MOE_CNT_SHORTFALL = 7,  /* tokens whose available set had fewer than k experts */
+    MOE_NUM_COUNTERS = 8
+};
+
+const char* moe_status_string(moe_status s);
+
+/* Bytes of device workspace needed for calls with these dims (T = the
+ * largest token count that will be passed).  The workspace holds router
+ * logits, the permutation plan, FFN intermediates and partial sums, and the
+ * device error word.  Zero-fill it once before first use (its error word
+ * must start clear); moe_check() clears the error word after reading it. */
+moe_status moe_workspace_size(const moe_dims* dims, size_t* bytes);
+
+/* Bytes of device memory for the expert table (per-expert weight pointers
+ * and TMA descriptors for N routed + n_shared shared experts). */
+moe_status moe_expert_table_size(const moe_dims* dims, size_t* bytes);
+
+/* Fill the expert table from HOST arrays of DEVICE pointers.
+ * host_w_gate/up/down[e]: expert e's [I, d] matrices (row i = intermediate
+ * channel i for all three: up/gate rows are the input projections of channel
+ * i, down row i is channel i's output projection).  host_sh_gate/up/down[s]:
+ * shared expert s's [I_shared, d] matrices (may be NULL if n_shared == 0).
+ * Every matrix must be 16-byte aligned.  Entries may point into one [N, I, d]
+ * block or anywhere else (a slot of an expert cache).  Synchronises `stream`.
+ * Call again after an expert moves to a new address. */
+moe_status moe_expert_table_init(const moe_dims* dims,
+                                 const void* const* host_w_gate, const void* const* host_w_up,
+                                 const void* const* host_w_down,
+                                 const void* const* host_sh_gate, const void* const* host_sh_up,
+                                 const void* const* host_sh_down,
+                                 void* table, size_t table_bytes, void* stream);
+
+/* Stage 1 — router and prefetch router (APEX §4.1-§4.2).
+ *   x [T,d]: layer input.  w_router [N,d], router_bias [N] (float32, NULL = none):
+ *   router logits l = x w_router^T + b; router_prob [T,N] = softmax(l);
+ *   topk_idx [T,k] = the k largest logits (descending, lowest index first on
+ *   ties); topk_gate [T,k] = router_prob of those experts.
+ *   x_pre [T,d] (NULL = x): input of the prefetch router (pre-attention state);
+ *   w_prefetch [N,d] (NULL = no prefetch router: delta_hat = 0, prefetch_mask
+ *   = all ones, delta_star = 0); w_ord [d] float32 and theta [delta_max+1]
+ *   float32 (non-decreasing): the ordinal-logistic CDF
+ *   p_delta = sigmoid(theta_delta - w.x_pre); delta_hat [T] = min{delta :
+ *   p_delta >= tau}, delta_max if none; prefetch_mask [T] = top-(k+delta_hat)
+ *   of the prefetch logits; delta_star [T] (NULL = skip) = min{delta : routed
+ *   set within top-(k+delta)}.
+ *   n_resident > 0 with batch_resident (device uint64, 1 element) also writes
+ *   the n_resident experts with the largest prefetch probability summed over
+ *   the T tokens (the set a prefetcher would stage for this batch).
+ * Errors: INVALID_ARG (NULL required buffer, tau outside (0,1)),
+ * UNSUPPORTED, CAPACITY (workspace too small), CUDA. */
+moe_status moe_route(const moe_dims* dims, const void* x, const void* w_router,
+                     const float* router_bias, const void* x_pre, const void* w_prefetch,
+                     const float* w_ord, const float* theta, float tau, int n_resident,
+                     int32_t* topk_idx, float* topk_gate, float* router_prob,
+                     int32_t* delta_hat, uint64_t* prefetch_mask, int32_t* delta_star,
+                     uint64_t* batch_resident, void* ws, size_t ws_bytes, void* stream);
+
+/* Stage 2 — miss handling (APEX §4.3 and Algorithm 1; SPICE LoRE section).
+ *   Available set A_t = resident (device uint64, NULL = all experts) AND
+ *   prefetch_mask[t] (NULL = all experts).  A routed expert outside A_t is
+ *   handled by `policy` (moe_miss_policy); HYBRID sends it to LoRE when its
+ *   router probability is below gamma and to substitution otherwise.
+ *   Substitutes are the available, non-routed experts with the largest
+ *   ORIGINAL router probability; each substitute carries its own probability
+ *   as gate.  Outputs, k slots per token in descending router probability:
+ *   final_idx [T,k], final_gate [T,k] (renormalised if dims->renorm_topk),
+ *   final_kind [T,k] (moe_slot_kind); fetch_mask (device uint64, NULL = skip)
+ *   = OR of the experts with a FETCH slot; counters (device int32
+ *   [MOE_NUM_COUNTERS], NULL = skip).  delta_hat, delta_star (NULL = skip)
+ *   only feed the counters.
+ *   A token whose A_t has fewer than k experts under SUBSTITUTE or HYBRID
+ *   keeps what it can, counts in MOE_CNT_SHORTFALL and sets MOE_ERR_CAPACITY
+ *   in the device error word.  LORE and HYBRID need dims->r > 0 (else
+ *   INVALID_ARG). */
+moe_status moe_select_resident(const moe_dims* dims, const float* router_prob,
+                               const int32_t* topk_idx, const uint64_t* prefetch_mask,
+                               const uint64_t* resident, int policy, float gamma,
+                               const int32_t* delta_hat, const int32_t* delta_star,
+                               int32_t* final_idx, float* final_gate, int32_t* final_kind,
+                               uint64_t* fetch_mask, int32_t* counters,
+                               void* ws, size_t ws_bytes, void* stream);
+
+/* Pinned host -> HBM copies of the experts in host_fetch_mask (a HOST value:
+ * read the device fetch_mask first), for the EXACT policy.  For each expert
+ * e in the mask, copies host_w_{gate,up,down}[e] (pinned host, [I,d] each)
+ * to dev_w_{gate,up,down}[e] (device) with cudaMemcpyAsync on stage_stream,
+ * then records done_event (a cudaEvent_t as void*) on stage_stream; the
+ * compute stream waits on that event before moe_expert_ffn.  *bytes receives
+ * the bytes queued.  Errors: INVALID_ARG, STAGING (a copy or the event
+ * record could not be queued; nothing further is queued). */
+moe_status moe_stage_experts(const moe_dims* dims, uint64_t host_fetch_mask,
+                             const void* const* host_w_gate, const void* const* host_w_up,
+                             const void* const* host_w_down,
+                             void* const* dev_w_gate, void* const* dev_w_up,
+                             void* const* dev_w_down, void* stage_stream, void* done_event,
+                             size_t* bytes);
+
+/* Stage 3a — token permutation by expert.
+ *   Slots (t, s) of kind COMPUTE or FETCH are grouped by expert, stable in
+ *   (t, s) order.  expert_offsets [N+1]: exclusive scan of per-expert counts;
+ *   perm [T*k]: perm[pos] = t*k + s for pos < expert_offsets[N];
+ *   inv_perm [T*k]: position of slot (t, s), -1 for LoRE slots.
+ *   Also writes the FFN work plan into the workspace. */
+moe_status moe_permute(const moe_dims* dims, const int32_t* final_idx,
+                       const int32_t* final_kind, int32_t* expert_offsets, int32_t* perm,
+                       int32_t* inv_perm, void* ws, size_t ws_bytes, void* stream);
+
+/* Stage 3b — grouped SwiGLU FFN over the permuted slots and the shared
+ * experts: y = (SiLU(X W_gate^T) (.) X W_up^T) W_down per expert (FloE method
+ * §1 with S_t = identity when keep_frac == 1).
+ *   x [T,d]; table: from moe_expert_table_init; expert_offsets/perm from
+ *   moe_permute (same call sequence, same workspace).
+ *   keep_frac in (0,1]: < 1 applies FloE contextual sparsity to routed
+ *   experts (keep the ceil(keep_frac*I) channels with the largest |x.W_up|
+ *   per token; gate and down only for kept channels).
+ *   y_perm [T*k, d] float32: row pos = the expert output for slot perm[pos]
+ *   (ungated); y_shared [T, d] float32 (NULL if n_shared == 0) = sum of the
+ *   shared experts' outputs.
+ *   Decode-size segments run as an HBM-streaming GEMV, larger ones as a
+ *   tcgen05 tensor-core grouped GEMM (bf16 only). */
+moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table,
+                          const int32_t* expert_offsets, const int32_t* perm, float keep_frac,
+                          float* y_perm, float* y_shared, void* ws, size_t ws_bytes,
+                          void* stream);
+
+/* Stage 4 — LoRE surrogate residual (SPICE, LoRE section):
+ *   y_lore[t] = sum over LoRE slots s of final_gate[t,s] * B_e (A_e x_t),
+ *   e = final_idx[t,s]; zero rows for tokens without LoRE slots.
+ *   lore_a [N, r, d], lore_b [N, d, r] in the layer's weight type;
+ *   y_lore [T, d] float32 (written). */
+moe_status moe_lore(const moe_dims* dims, const void* x, const int32_t* final_idx,
+                    const int32_t* final_kind, const float* final_gate, const void* lore_a,
+                    const void* lore_b, float* y_lore, void* stream);
+
+/* Stage 5 — combine:
+ *   out[t] = y_shared[t] * (1 + sum of LoRE-slot gates)
+ *          + sum over COMPUTE/FETCH slots of final_gate * y_perm[inv_perm[t,s]]
+ *          + y_lore[t]
+ *   (the LoRE slot stands for y_shared + B_e A_e x, SPICE LoRE section).
+ *   Slots are summed in slot order (deterministic).  y_shared, y_lore may be
+ *   NULL (zero).  out [T, d] float32. */
+moe_status moe_combine(const moe_dims* dims, const float* y_perm, const int32_t* inv_perm,
+                       const float* final_gate, const int32_t* final_kind,
+                       const float* y_shared, const float* y_lore, float* out, void* stream);
+
+/* All stages for one layer on one stream (no host synchronisation).  FETCH
+ * slots are computed from the table's current pointers: stage them first
+ * (moe_stage_experts) when the policy is EXACT. */
+typedef struct {
+    const void* x; const void* x_pre;
+    const void* w_router; const float* router_bias;
+    const void* w_prefetch; const float* w_ord; const float* theta; float tau;
+    int n_resident;               /* > 0: batch resident set from the prefetch router */
+    const uint64_t* resident;     /* used when n_resident <= 0 (NULL = all) */
+    int use_prefetch_mask;        /* A_t includes the per-token prefetch set */
+    int policy; float gamma; float keep_frac;
+    const void* table; const void* lore_a; const void* lore_b;
+} moe_layer_args;
+
+typedef struct {
+    int32_t* topk_idx; float* topk_gate; float* router_prob; int32_t* delta_hat;
+    uint64_t* prefetch_mask; int32_t* delta_star; uint64_t* batch_resident;
+    int32_t* final_idx; float* final_gate; int32_t* final_kind; uint64_t* fetch_mask;
+    int32_t* counters; int32_t* expert_offsets; int32_t* perm; int32_t* inv_perm;
+    float* y_perm; float* y_shared; float* y_lore; float* out;
+} moe_layer_outputs;
+
+moe_status moe_layer_forward(const moe_dims* dims, const moe_layer_args* args,
+                             const moe_layer_outputs* outs, void* ws, size_t ws_bytes,
+                             void* stream);
+
+/* Synchronise `stream`, read and clear the device error word of `ws`.
+ * *device_status receives MOE_OK or the first error a kernel recorded;
+ * *detail (may be NULL) a code-specific detail (token, expert or stage). */
+moe_status moe_check(void* ws, void* stream, moe_status* device_status, int32_t* detail);
+
+/* Text of the last MOE_ERR_CUDA on this host thread: the failing call and
+ * the CUDA error name and message ("" if none).  Valid until the next call
+ * on this thread. */
+const char* moe_last_error_detail(void);
+
+/* Total number of kernel launches this library has queued since it was
+ * loaded (all threads).  Read it before and after a region to count the
+ * kernels launched inside it. */
+uint64_t moe_launch_total(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

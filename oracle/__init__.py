@@ -47,7 +47,7 @@ def build(force: bool = False) -> str:
 class _Cfg(C.Structure):
     _fields_ = [(n, C.c_int) for n in ("T", "d", "N", "k", "I", "n_shared", "I_shared", "r",
                                        "delta_max", "renorm", "policy", "use_prefetch",
-                                       "m_keep", "has_prefetch")] + [
+                                       "m_keep", "has_prefetch", "route_only")] + [
         ("tau", C.c_double), ("gamma", C.c_double), ("resident", C.c_uint64)]
 
 
@@ -247,11 +247,13 @@ def resident_mask(cfg, W, x_batch) -> tuple[int, float]:
 
 def layer_forward(cfg, W, x, resident: int | None = None, x_pre=None, keep_m: int | None = None,
                   policy: int | None = None, gamma: float | None = None, tau: float | None = None,
-                  renorm: int = 0, use_prefetch: bool | None = None) -> LayerResult:
+                  renorm: int = 0, use_prefetch: bool | None = None,
+                  route_only: bool = False) -> LayerResult:
     """Run the whole layer for the tokens x [T, d].
 
     resident: batch-level resident mask (default: computed from x itself with
     the config's n_resident).  keep_m: FloE channels kept (default: dense).
+    route_only: stop after the routing decisions (outputs stay zero).
     """
     x = f32(x)
     T, d = x.shape
@@ -267,6 +269,7 @@ def layer_forward(cfg, W, x, resident: int | None = None, x_pre=None, keep_m: in
     c.use_prefetch = int(cfg.use_prefetch_mask if use_prefetch is None else use_prefetch)
     c.m_keep = cfg.I if keep_m is None else keep_m
     c.has_prefetch = 1
+    c.route_only = int(route_only)
     c.tau = cfg.tau if tau is None else tau
     c.gamma = cfg.gamma if gamma is None else gamma
     c.resident = resident
@@ -286,7 +289,8 @@ def layer_forward(cfg, W, x, resident: int | None = None, x_pre=None, keep_m: in
         delta_hat=np.zeros(T, np.int32), score=np.zeros(T), prefetch=np.zeros(T, np.uint64),
         delta_star=np.zeros(T, np.int32), final_idx=np.zeros((T, k), np.int32),
         final_gate=np.zeros((T, k)), final_kind=np.zeros((T, k), np.int32),
-        y_shared=np.zeros((T, d)), out=np.zeros((T, d)), margin=np.zeros((T, M_COUNT)),
+        y_shared=np.zeros((T, 0 if route_only else d)), out=np.zeros((T, 0 if route_only else d)),
+        margin=np.zeros((T, M_COUNT)),
         kept=np.zeros((T, k, c.m_keep), np.int32) if c.m_keep < cfg.I else None,
         status=np.zeros(T, np.int32), resident=resident, resident_gap=res_gap)
     o = _Outputs()

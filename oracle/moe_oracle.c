@@ -280,6 +280,7 @@ typedef struct {
     int use_prefetch;      /* available set includes the per-token prefetch set */
     int m_keep;            /* FloE channels kept per token (== I: dense) */
     int has_prefetch;      /* prefetch router present */
+    int route_only;        /* stop after the routing decisions (no expert math) */
     double tau, gamma;
     uint64_t resident;     /* batch-level resident mask */
 } orc_cfg;
@@ -436,6 +437,7 @@ static void one_token(const orc_cfg* c, const orc_inputs* in, const orc_outputs*
     }
 
     /* 6-7. experts, shared experts, LoRE, combine */
+    if (c->route_only) return;
     double* ysh = o->y_shared + (size_t)t * d;
     double* out = o->out + (size_t)t * d;
     for (int j = 0; j < d; ++j) { ysh[j] = 0.0; out[j] = 0.0; }

@@ -1,0 +1,130 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every
+function the headers declare, and rejects bad arguments on the host before
+any CUDA call.  No compute call is made here."""
+import ctypes as C
+import glob
+import os
+import re
+
+import pytest
+
+import expert_routing_ffn_gb300 as moe
+from workloads import CONFIGS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        txt = open(h).read()
+        txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+        names |= set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", txt))
+    return names
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    L = moe.lib()
+    names = _declared()
+    assert len(names) >= 15
+    for n in sorted(names):
+        assert hasattr(L, n), f"{n} declared in include/ but not exported"
+
+
+def test_status_strings():
+    for s in range(8):
+        assert moe.status_string(s) and "unknown" not in moe.status_string(s)
+    assert "unknown" in moe.status_string(99)
+
+
+@pytest.mark.parametrize("name", sorted(CONFIGS))
+def test_workspace_size_grows_with_T(name):
+    cfg = CONFIGS[name]
+    sizes = [moe.moe_workspace_size(moe.make_dims(T, cfg.d, cfg.N, cfg.k, cfg.I, cfg.n_shared,
+                                                  cfg.I_shared, cfg.r, wtype=cfg.wtype))
+             for T in (1, 8, 64, 1024)]
+    assert all(a < b for a, b in zip(sizes, sizes[1:]))
+    assert moe.moe_expert_table_size(moe.make_dims(1, cfg.d, cfg.N, cfg.k, cfg.I, cfg.n_shared,
+                                                   cfg.I_shared, cfg.r, wtype=cfg.wtype)) > 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(N=65), moe.MOE_ERR_UNSUPPORTED),
+    (dict(k=9, N=16), moe.MOE_ERR_UNSUPPORTED),
+    (dict(d=300), moe.MOE_ERR_UNSUPPORTED),
+    (dict(d=8192), moe.MOE_ERR_UNSUPPORTED),
+    (dict(wtype="f32", d=2048), moe.MOE_ERR_UNSUPPORTED),
+    (dict(k=0), moe.MOE_ERR_INVALID_ARG),
+    (dict(T=-1), moe.MOE_ERR_INVALID_ARG),
+    (dict(delta_max=60, N=8, k=2), moe.MOE_ERR_INVALID_ARG),
+    (dict(n_shared=1, I_shared=0), moe.MOE_ERR_INVALID_ARG),
+])
+def test_bad_dims_rejected(kw, status):
+    base = dict(T=4, d=256, N=8, k=2, I=64, n_shared=0, I_shared=0, r=0, wtype="bf16")
+    base.update(kw)
+    D = moe.make_dims(**base)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_workspace_size(D)
+    assert ei.value.status == status
+
+
+def _raw_dims(**kw):
+    base = dict(T=4, d=256, N=8, k=2, I=64, n_shared=0, I_shared=0, r=0, wtype="bf16")
+    base.update(kw)
+    return moe.make_dims(**base)
+
+
+def test_null_buffers_rejected_before_cuda():
+    L = moe.lib()
+    D = _raw_dims()
+    # no workspace
+    st = L.moe_route(C.byref(D), None, None, None, None, None, None, None, 0.9, 0, None, None, None,
+                     None, None, None, None, None, 0, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    # workspace present but too small
+    fake_ws = C.c_void_p(1 << 20)  # aligned, never dereferenced on this path
+    st = L.moe_permute(C.byref(D), None, None, None, None, None, fake_ws, 16, None)
+    assert st == moe.MOE_ERR_CAPACITY
+    st = L.moe_combine(C.byref(D), None, None, None, None, None, None, None, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    # LoRE needs a rank
+    st = L.moe_lore(C.byref(D), None, None, None, None, None, None, None, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    # a bad miss policy
+    n = moe.moe_workspace_size(D)
+    st = L.moe_select_resident(C.byref(D), None, None, None, None, 7, 0.1, None, None, None, None,
+                               None, None, None, fake_ws, n, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+
+
+def test_staging_failure_is_reported_on_the_host():
+    """An injected copy failure makes moe_stage_experts return
+    MOE_ERR_STAGING before anything is queued (no GPU fault involved)."""
+    L = moe.lib()
+    D = _raw_dims(N=4, k=2)
+    ptrs = (C.c_void_p * 4)(*[0x1000 * (i + 1) for i in range(4)])
+    n = C.c_size_t(123)
+    moe.moe_testing_fail_copies_after(0)
+    try:
+        st = L.moe_stage_experts(C.byref(D), 0b0101, ptrs, ptrs, ptrs, ptrs, ptrs, ptrs, None,
+                                 C.c_void_p(0x10), C.byref(n))
+    finally:
+        moe.moe_testing_fail_copies_after(-1)
+    assert st == moe.MOE_ERR_STAGING
+    assert n.value == 0
+    # a mask naming an expert beyond N is an argument error
+    st = L.moe_stage_experts(C.byref(D), 1 << 5, ptrs, ptrs, ptrs, ptrs, ptrs, ptrs, None,
+                             C.c_void_p(0x10), C.byref(n))
+    assert st == moe.MOE_ERR_INVALID_ARG
+
+
+def test_empty_mask_stages_nothing_without_gpu_calls_failing():
+    L = moe.lib()
+    D = _raw_dims(N=4, k=2)
+    ptrs = (C.c_void_p * 4)(*[0x1000 * (i + 1) for i in range(4)])
+    n = C.c_size_t(7)
+    st = L.moe_stage_experts(C.byref(D), 0, ptrs, ptrs, ptrs, ptrs, ptrs, ptrs, None,
+                             C.c_void_p(0x10), C.byref(n))
+    # with nothing to copy only the event record remains; without a GPU it fails as STAGING
+    assert st in (moe.MOE_OK, moe.MOE_ERR_STAGING)
+    assert n.value == 0

@@ -1,0 +1,208 @@
+"""Parity of the CUDA layer with the float64 oracle, through the C ABI.
+
+Every layer shape at its full size (the prefill layer's expert outputs on a
+seeded 512-token subset of the 4096-token batch, its routing on all tokens),
+plus ragged and edge cases.  GPU only.
+"""
+from functools import lru_cache
+
+import numpy as np
+import pytest
+import torch
+
+import expert_routing_ffn_gb300 as moe
+from expert_routing_ffn_gb300.layer import DeviceLayer, LayerBuffers, as_u64, forward
+import oracle
+from workloads import CONFIGS, make_tokens, make_weights
+
+from parity import check_output, check_routing, check_selection, to_np, x_device
+
+pytestmark = pytest.mark.gpu
+
+
+@lru_cache(maxsize=2)
+def _host(name):
+    cfg = CONFIGS[name]
+    return cfg, make_weights(cfg)
+
+
+_dev_cache = {}
+
+
+def _device(name, T):
+    key = name
+    if key in _dev_cache and _dev_cache[key].dims.T >= T:
+        return _dev_cache[key]
+    _dev_cache.clear()
+    torch.cuda.empty_cache()
+    cfg, W = _host(name)
+    _dev_cache[key] = DeviceLayer(cfg, W, max(T, cfg.T))
+    return _dev_cache[key]
+
+
+def _run(name, T, batch=0, **kw):
+    cfg, W = _host(name)
+    layer = _device(name, T)
+    x = make_tokens(cfg, T=T, batch=batch)
+    bufs = LayerBuffers(layer, T)
+    forward(layer, bufs, x_device(x, layer.dt), **kw)
+    st, det = moe.moe_check(layer.ws)
+    return cfg, W, layer, x, bufs, st, det
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 16), ("tiny", 1), ("tiny", 5), ("tiny", 64),
+                                    ("dsv2lite", 1), ("dsv2lite", 8), ("dsv2lite", 3),
+                                    ("granite", 1), ("granite", 37), ("granite", 1024),
+                                    ("mixtral", 1), ("mixtral", 8), ("mixtral", 32)])
+def test_layer_matches_oracle(name, T):
+    cfg, W, layer, x, bufs, st, det = _run(name, T)
+    assert st == moe.MOE_OK, (moe.status_string(st), det)
+    R = oracle.layer_forward(cfg, W, x)
+    if cfg.n_resident > 0:
+        assert R.resident_gap >= 1e-5
+        assert as_u64(to_np(bufs.batch_resident)[0]) == R.resident
+    check_routing(cfg, R, bufs)
+    check_selection(cfg, R, bufs)
+    check_output(cfg, R, bufs.out)
+
+
+def test_prefill_layer_qwen2_shape():
+    """4096-token prefill: routing on every token, outputs on a seeded subset."""
+    name, T = "qwen2", 4096
+    cfg, W, layer, x, bufs, st, det = _run(name, T)
+    assert st == moe.MOE_OK, (moe.status_string(st), det)
+    Rr = oracle.layer_forward(cfg, W, x, route_only=True)
+    assert Rr.resident_gap >= 1e-5
+    assert as_u64(to_np(bufs.batch_resident)[0]) == Rr.resident
+    check_routing(cfg, Rr, bufs)
+    check_selection(cfg, Rr, bufs)
+    rows = np.sort(np.random.default_rng(0).choice(T, 512, replace=False))
+    R = oracle.layer_forward(cfg, W, x[rows], resident=Rr.resident)
+    check_output(cfg, R, bufs.out, tokens=rows)
+
+
+@pytest.mark.parametrize("policy", [0, 1, 2, 3])
+def test_policies_tiny(policy):
+    cfg, W, layer, x, bufs, st, det = _run("tiny", 64, policy=policy)
+    assert st == moe.MOE_OK
+    R = oracle.layer_forward(cfg, W, x, policy=policy)
+    check_selection(cfg, R, bufs)
+    check_output(cfg, R, bufs.out)
+    kinds = np.bincount(to_np(bufs.final_kind).ravel(), minlength=3)
+    if policy == 0:
+        assert kinds[1] > 0
+    if policy in (2, 3):
+        assert kinds[2] > 0
+
+
+def test_stagewise_calls_equal_layer_forward():
+    """The six stage calls in sequence give bitwise the same output as
+    moe_layer_forward."""
+    cfg, W, layer, x, bufs, st, _ = _run("tiny", 16)
+    D = layer.dims.with_T(16)
+    xd = x_device(x, layer.dt)
+    b = LayerBuffers(layer, 16)
+    moe.moe_route(D, xd, layer.w_router, layer.router_bias, None, layer.w_prefetch, layer.w_ord,
+                  layer.theta, cfg.tau, 0, b.topk_idx, b.topk_gate, b.router_prob, b.delta_hat,
+                  b.prefetch_mask, b.delta_star, None, layer.ws)
+    moe.moe_select_resident(D, b.router_prob, b.topk_idx, b.prefetch_mask, None, cfg.policy,
+                            cfg.gamma, b.delta_hat, b.delta_star, b.final_idx, b.final_gate,
+                            b.final_kind, b.fetch_mask, b.counters, layer.ws)
+    moe.moe_permute(D, b.final_idx, b.final_kind, b.expert_offsets, b.perm, b.inv_perm, layer.ws)
+    moe.moe_expert_ffn(D, xd, layer.table, b.expert_offsets, b.perm, 1.0, b.y_perm, b.y_shared,
+                       layer.ws)
+    moe.moe_lore(D, xd, b.final_idx, b.final_kind, b.final_gate, layer.lore_a, layer.lore_b, b.y_lore)
+    moe.moe_combine(D, b.y_perm, b.inv_perm, b.final_gate, b.final_kind, b.y_shared, b.y_lore, b.out)
+    assert moe.moe_check(layer.ws)[0] == moe.MOE_OK
+    assert torch.equal(b.out, bufs.out)
+
+
+def test_permutation_invariants():
+    cfg, W, layer, x, bufs, st, _ = _run("granite", 1024)
+    off = to_np(bufs.expert_offsets)
+    perm = to_np(bufs.perm)
+    inv = to_np(bufs.inv_perm)
+    fi = to_np(bufs.final_idx).ravel()
+    fk = to_np(bufs.final_kind).ravel()
+    valid = (fi >= 0) & (fk != moe.MOE_KIND_LORE)
+    counts = np.bincount(fi[valid], minlength=cfg.N)
+    assert off[0] == 0 and (np.diff(off) == counts).all()
+    n = off[-1]
+    assert n == valid.sum()
+    assert (inv[perm[:n]] == np.arange(n)).all()
+    assert (inv[~valid] == -1).all()
+    for e in range(cfg.N):  # stable: slots of one expert in increasing slot order
+        seg = perm[off[e]:off[e + 1]]
+        assert (np.diff(seg) > 0).all() and (fi[seg] == e).all()
+
+
+def test_deterministic():
+    _, _, layer, x, b1, _, _ = _run("dsv2lite", 8)
+    o1 = b1.out.clone()
+    _, _, _, _, b2, _, _ = _run("dsv2lite", 8)
+    assert torch.equal(o1, b2.out)
+
+
+def test_empty_batch():
+    cfg, W = _host("tiny")
+    layer = _device("tiny", 16)
+    bufs = LayerBuffers(layer, 1)
+    x = torch.empty((0, cfg.d), dtype=layer.dt, device="cuda")
+    forward(layer, bufs, x)
+    assert moe.moe_check(layer.ws)[0] == moe.MOE_OK
+
+
+def test_capacity_shortfall_reported_on_device():
+    """An available set smaller than k under SUBSTITUTE is reported through
+    the device error word (MOE_ERR_CAPACITY), without a fault."""
+    cfg, W = _host("tiny")
+    layer = _device("tiny", 16)
+    x = make_tokens(cfg, T=4)
+    bufs = LayerBuffers(layer, 4)
+    layer.set_resident(0b1)
+    try:
+        forward(layer, bufs, x_device(x, layer.dt), policy=moe.MOE_MISS_SUBSTITUTE,
+                use_prefetch_mask=0, n_resident=0)
+        st, det = moe.moe_check(layer.ws)
+        assert st == moe.MOE_ERR_CAPACITY
+        assert to_np(bufs.counters)[7] == 4
+    finally:
+        layer.set_resident((1 << 64) - 1)
+    # the error word was cleared by moe_check and the context is still usable
+    forward(layer, bufs, x_device(x, layer.dt))
+    assert moe.moe_check(layer.ws)[0] == moe.MOE_OK
+
+
+def test_counters_match_oracle():
+    cfg, W, layer, x, bufs, st, _ = _run("granite", 1024)
+    R = oracle.layer_forward(cfg, W, x)
+    c = to_np(bufs.counters)
+    assert not R.excluded().any(), "near-tie tokens: counters are compared on exact inputs only"
+    assert c[5] == R.delta_hat.sum()
+    assert c[6] == R.delta_star.sum()
+    overlap = sum(all((int(R.prefetch[t]) >> int(e)) & 1 for e in R.topk_idx[t]) for t in range(len(x)))
+    assert c[4] == overlap
+    routed_kept = sum(len(set(R.topk_idx[t]) & set(R.final_idx[t])) for t in range(len(x)))
+    assert c[0] == routed_kept
+    assert c[0] + c[1] == (R.final_idx >= 0).sum()
+
+
+def test_all_tokens_on_the_same_experts():
+    """Worst case for the FFN plan: a router bias sends every token to the same
+    k experts (the most rows per expert, the most segments)."""
+    cfg, W = _host("granite")
+    Wb = type(W)(**{**W.__dict__})
+    bias = np.zeros(cfg.N, np.float32)
+    bias[:cfg.k] = 50.0
+    Wb.router_bias = bias
+    layer = DeviceLayer(cfg, Wb, 1024)
+    x = make_tokens(cfg, T=1024)
+    bufs = LayerBuffers(layer, 1024)
+    forward(layer, bufs, x_device(x, layer.dt), use_prefetch_mask=0)
+    st, det = moe.moe_check(layer.ws)
+    assert st == moe.MOE_OK, (moe.status_string(st), det)
+    off = to_np(bufs.expert_offsets)
+    assert (np.diff(off)[:cfg.k] == 1024).all()
+    R = oracle.layer_forward(cfg, Wb, x, use_prefetch=False)
+    check_selection(cfg, R, bufs)
+    check_output(cfg, R, bufs.out)
