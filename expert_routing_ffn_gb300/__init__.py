@@ -90,6 +90,7 @@ _PROTOS = {
                           C.c_int),
     "moe_permute": ([_DIMS, _P, _P, _P, _P, _P, _P, _SZ, _P], C.c_int),
     "moe_expert_ffn": ([_DIMS, _P, _P, _P, _P, _F, _P, _P, _P, _SZ, _P], C.c_int),
+    "moe_expert_ffn_noalloc": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P], C.c_int),
     "moe_lore": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P], C.c_int),
     "moe_combine": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P], C.c_int),
     "moe_layer_forward": ([_DIMS, C.POINTER(moe_layer_args), C.POINTER(moe_layer_outputs), _P, _SZ,
@@ -277,6 +278,20 @@ def moe_expert_ffn(dims, x, table, expert_offsets, perm, keep_frac, y_perm, y_sh
         float(keep_frac), _ptr(y_perm, torch.float32, T * k * d, "y_perm"),
         _ptr(y_shared, torch.float32, T * d, "y_shared", True), _ptr(ws, torch.uint8, name="ws"),
         ws.numel(), _stream(stream)), "moe_expert_ffn")
+
+
+def moe_expert_ffn_noalloc(dims, x, table, expert_offsets, perm, y_perm, y_shared,
+                           device_status=None, stream=None):
+    """moe_expert_ffn with the library's fixed device scratch instead of a
+    workspace, for callers that cannot allocate device memory at run time."""
+    T, d, N, k = dims.T, dims.d, dims.N, dims.k
+    _check(lib().moe_expert_ffn_noalloc(
+        C.byref(dims), _ptr(x, wdtype(dims), T * d, "x"), _ptr(table, torch.uint8, name="table"),
+        _ptr(expert_offsets, torch.int32, N + 1, "expert_offsets"), _ptr(perm, torch.int32, T * k, "perm"),
+        _ptr(y_perm, torch.float32, T * k * d, "y_perm"),
+        _ptr(y_shared, torch.float32, T * d, "y_shared", True),
+        _ptr(device_status, torch.int32, 2, "device_status", True), _stream(stream)),
+        "moe_expert_ffn_noalloc")
 
 
 def moe_lore(dims, x, final_idx, final_kind, final_gate, lore_a, lore_b, y_lore, stream=None):

@@ -226,6 +226,28 @@ moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table
                           float* y_perm, float* y_shared, void* ws, size_t ws_bytes,
                           void* stream);
 
+/* moe_expert_ffn without a workspace, for callers that cannot allocate device
+ * memory when they run the layer: an engine plugin handed only its inputs and
+ * outputs, a decode loop that cannot pay the device-wide synchronisation of
+ * cudaMalloc/cudaFree, or work recorded into a CUDA graph.  The source pages
+ * have no counterpart of this call; it is a deployment convenience.
+ *   Same inputs and outputs as moe_expert_ffn (dense experts only, i.e.
+ *   keep_frac = 1), with expert_offsets/perm from moe_permute.  The plan,
+ *   partial sums and error word live in a 16 MiB array that the library
+ *   holds on every GPU it is loaded on, until the process exits.  Batches
+ *   whose scratch would exceed 16 MiB are rejected with MOE_ERR_CAPACITY
+ *   before anything is queued (decode sizes fit: e.g. 32 tokens at d = 2048
+ *   or d = 4096).  device_status (device int32[2], may be NULL) receives the
+ *   call's device error code and detail when its kernels have run.
+ *   The first call on a device looks the array up (cudaGetSymbolAddress);
+ *   make it outside of any stream capture.  All calls share the array: calls
+ *   whose kernels overlap on the GPU race, so order them on one stream.
+ *   Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call. */
+moe_status moe_expert_ffn_noalloc(const moe_dims* dims, const void* x, const void* table,
+                                  const int32_t* expert_offsets, const int32_t* perm,
+                                  float* y_perm, float* y_shared, int32_t* device_status,
+                                  void* stream);
+
 /* Stage 4 — LoRE surrogate residual (SPICE, LoRE section):
  *   y_lore[t] = sum over LoRE slots s of final_gate[t,s] * B_e (A_e x_t),
  *   e = final_idx[t,s]; zero rows for tokens without LoRE slots.
