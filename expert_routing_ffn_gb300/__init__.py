@@ -91,7 +91,7 @@ _PROTOS = {
     "moe_permute": ([_DIMS, _P, _P, _P, _P, _P, _P, _SZ, _P], C.c_int),
     "moe_expert_ffn": ([_DIMS, _P, _P, _P, _P, _F, _P, _P, _P, _SZ, _P], C.c_int),
     "moe_expert_ffn_noalloc": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P], C.c_int),
-    "moe_lore": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P], C.c_int),
+    "moe_lore": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P], C.c_int),
     "moe_combine": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P], C.c_int),
     "moe_layer_forward": ([_DIMS, C.POINTER(moe_layer_args), C.POINTER(moe_layer_outputs), _P, _SZ,
                            _P], C.c_int),
@@ -294,14 +294,15 @@ def moe_expert_ffn_noalloc(dims, x, table, expert_offsets, perm, y_perm, y_share
         "moe_expert_ffn_noalloc")
 
 
-def moe_lore(dims, x, final_idx, final_kind, final_gate, lore_a, lore_b, y_lore, stream=None):
+def moe_lore(dims, x, final_idx, final_kind, final_gate, lore_a, lore_b, y_lore, ws, stream=None):
     T, d, N, k, r = dims.T, dims.d, dims.N, dims.k, dims.r
     wt = wdtype(dims)
     _check(lib().moe_lore(
         C.byref(dims), _ptr(x, wt, T * d, "x"), _ptr(final_idx, torch.int32, T * k, "final_idx"),
         _ptr(final_kind, torch.int32, T * k, "final_kind"), _ptr(final_gate, torch.float32, T * k, "final_gate"),
         _ptr(lore_a, wt, N * r * d, "lore_a"), _ptr(lore_b, wt, N * d * r, "lore_b"),
-        _ptr(y_lore, torch.float32, T * d, "y_lore"), _stream(stream)), "moe_lore")
+        _ptr(y_lore, torch.float32, T * d, "y_lore"), _ptr(ws, torch.uint8, name="ws"), ws.numel(),
+        _stream(stream)), "moe_lore")
 
 
 def moe_combine(dims, y_perm, inv_perm, final_gate, final_kind, y_shared, y_lore, out, stream=None):

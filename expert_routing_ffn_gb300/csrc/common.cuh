@@ -63,18 +63,18 @@ struct PlanHeader {
 
 // ---------------------------------------------------------------- workspace
 struct WsLayout {
-    size_t err, logits_r, logits_p, score, qp, plan_hdr, segs, seg_first, partial, total;
+    size_t err, ticket, logits_r, logits_p, score, qp, plan_hdr, segs, seg_first, lore_z, partial,
+        total;
     int max_segs, max_partial_rows;
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Token rows per GEMV segment: the register budget of the GEMV kernel allows
-// 8 rows while a thread block covers d <= 2048 bf16 values, 4 above.  The
-// workspace sizing and the launch both take it from here.
+// Token rows per GEMV segment (the token rows of a segment stay in registers;
+// 4 rows keep a bf16 GEMV thread within the register budget of two CTAs per
+// SM).  The workspace sizing and the launch both take it from here.
 __host__ __device__ inline int gemv_rows(const moe_dims& D) {
-    if (D.wtype == MOE_DTYPE_BF16) return D.d <= 2048 ? 8 : 4;
-    return 8;
+    return D.wtype == MOE_DTYPE_BF16 ? 4 : 8;
 }
 
 __host__ __device__ inline WsLayout ws_layout(const moe_dims& D) {
@@ -92,6 +92,7 @@ __host__ __device__ inline WsLayout ws_layout(const moe_dims& D) {
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, kAlign); return at; };
     L.err = take(sizeof(DevError));
+    L.ticket = take(64);  // arrival counters of last-block-finishes kernels (left at 0)
     L.logits_r = take(T * N * 4);
     L.logits_p = take(T * N * 4);
     L.score = take(T * 4);
@@ -99,6 +100,7 @@ __host__ __device__ inline WsLayout ws_layout(const moe_dims& D) {
     L.plan_hdr = take(sizeof(PlanHeader));
     L.segs = take((size_t)L.max_segs * sizeof(Seg));
     L.seg_first = take((N + (size_t)D.n_shared + 1) * 4);
+    L.lore_z = take(rows_routed * (size_t)(D.r > 0 ? D.r : 1) * 4);
     L.partial = take((size_t)L.max_partial_rows * (size_t)D.d * 4);
     L.total = o;
     return L;
@@ -250,6 +252,24 @@ __device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32]) {
         }
     }
     return v[0];
+}
+
+// Reduce 16 values per lane across the warp: afterwards lane l holds the
+// warp-wide sum of value (l >> 1) & 15 (halving steps over lane bits 4..1,
+// then one exchange over bit 0: 16 shuffles).
+__device__ __forceinline__ float warp_reduce_scatter16(float (&v)[16]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 16, n = 16; o > 1; o >>= 1, n >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            float send = up ? v[i] : v[i + n / 2];
+            float keep = up ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
 }  // namespace moe

@@ -5,17 +5,20 @@
 // and down rows are each one contiguous d-vector).
 //
 // Work split: the channels of every segment (an expert with up to RG token
-// rows) form one list, cut into G equal ranges, one per CTA (G = SMs).  A CTA
-// streams its range in stages of CH channels: one bulk copy (TMA engine) per
-// matrix per stage brings the CH gate, up and down rows into shared memory,
-// NS stages in flight, completion tracked by mbarriers.  Every weight byte is
-// read from HBM exactly once; the token rows are held in registers.
+// rows) form one list, cut into G equal ranges, one per CTA (G = SMs x CTAs
+// per SM).  A CTA streams its range in stages of CH channels: one bulk copy
+// (TMA engine) per matrix per stage brings the CH gate, up and down rows into
+// shared memory, NS stages in flight, completion tracked by mbarriers.  Every
+// weight byte is read from HBM exactly once; the token rows are held in
+// registers.
 //
 // Per stage: each thread owns one 16-byte chunk of d; it forms the partial
-// gate/up dot products of its chunk for every (channel, row), the block sums
-// them (warp reduce-scatter + shared memory), computes h = SiLU(g) * u, and
-// then adds h * Wd[channel, chunk] into its register accumulators for the
-// output columns of the same chunk.  When a CTA leaves a segment it writes
+// gate/up dot products of its chunk for every (channel, row), each warp sums
+// them with a reduce-scatter, one block barrier publishes the per-warp sums,
+// every warp then forms h = SiLU(g) * u itself and adds h * Wd[channel,
+// chunk] into its register accumulators for the output columns of the same
+// chunk.  The barrier also proves the previous stage's buffer is free, so
+// thread 0 refills it right there (no second barrier per stage).  When a CTA leaves a segment it writes
 // its partial output rows; a second kernel sums the partials of each row in a
 // fixed order (deterministic, no atomics).
 #include "common.cuh"
@@ -25,33 +28,34 @@ namespace moe {
 
 constexpr int kNSMax = 8;
 
+// Issues the bulk copies of one CTA's stages, in the order they are read.
+// Run by thread 0 only.
 struct Producer {
     const Seg* segs;
     const ExpertEntry* table;
     unsigned char* stage_mem;
-    uint64_t* bars;
+    uint64_t* full;
     size_t row_bytes, mat_bytes, stage_bytes;
-    int NS, CH, seg, ch, hi;
-    int issued;     // stages issued so far
+    int NS, CH, seg, ch, hi, n_seg;
+    int issued;
     uint64_t policy;
 
-    int n_seg;
+    __device__ __forceinline__ bool done() const { return ch >= hi || seg >= n_seg; }
 
-    __device__ __forceinline__ void issue(int stage_k) {
-        if (ch >= hi || seg >= n_seg) return;
+    __device__ __forceinline__ void issue() {
         const Seg S = segs[seg];
         const int local = ch - S.ch_start;
         const int seg_end = min(hi, S.ch_start + S.I) - S.ch_start;
         const int nch = min(CH, seg_end - local);
         const ExpertEntry& E = table[S.expert];
-        const int b = stage_k % NS;
+        const int b = issued % NS;
         unsigned char* buf = stage_mem + (size_t)b * stage_bytes;
         const uint32_t bytes = (uint32_t)(nch * row_bytes);
-        mbar_arrive_expect_tx(&bars[b], 3 * bytes);
+        mbar_arrive_expect_tx(&full[b], 3 * bytes);
 #pragma unroll
         for (int m = 0; m < 3; ++m)
             bulk_g2s(buf + m * mat_bytes, static_cast<const char*>(E.w[m]) + (size_t)local * row_bytes,
-                     bytes, &bars[b], policy);
+                     bytes, &full[b], policy);
         ch += nch;
         if (ch >= S.ch_start + S.I) ++seg;
         ++issued;
@@ -68,15 +72,29 @@ __device__ __forceinline__ float dot_v(const float* a, const float* b) {
 
 __device__ __forceinline__ float silu(float g) { return g / (1.f + expf(-g)); }
 
-template <typename W, int RG, int CH, int ROWS>
+// Barrier among the block's threads (named barrier 1, separate from the
+// __syncthreads used between segment pieces).
+__device__ __forceinline__ void consumer_sync(int n_threads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(n_threads) : "memory");
+}
+
+struct GemvShared {
+    uint64_t* full;
+    float* red;        // [2][n_warps][32]
+    int* abort_flag;
+    unsigned char* stage_mem;
+    Producer* prod;    // thread 0's copy issuer
+};
+
+// One segment piece: channels [llo, lhi) of segment S, ROWS token rows.
+template <typename W, int CH, int ROWS>
 __device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, int llo, int lhi,
-                                           int cta, unsigned char* stage_mem, uint64_t* bars,
-                                           float (*red_s)[32], float (*h_s)[RG], int* s_abort,
-                                           int& stage_k, Producer& prod) {
+                                           int cta, const GemvShared& sh, int n_cons,
+                                           int& stage_k) {
     constexpr int V = Vec<W>::n;
     constexpr int NV = 2 * CH * ROWS;
     static_assert(NV <= 32, "per-stage outputs must fit one warp reduce-scatter");
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = n_cons >> 5;
     const int d = p.d;
     const size_t row_bytes = (size_t)d * sizeof(W);
     const size_t mat_bytes = (size_t)CH * row_bytes;
@@ -100,14 +118,16 @@ __device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, in
         const int nch = min(CH, lhi - i);
         const int b = stage_k % p.NS;
         const uint32_t par = (uint32_t)((stage_k / p.NS) & 1);
-        if (!mbar_wait(&bars[b], par)) {
+        if (!mbar_wait(&sh.full[b], par)) {
             set_error(p.err, MOE_ERR_TIMEOUT, cta);
-            *s_abort = 1;
+            *sh.abort_flag = 1;
         }
-        const unsigned char* buf = stage_mem + (size_t)b * stage_bytes;
-        float v[32];
+        const unsigned char* buf = sh.stage_mem + (size_t)b * stage_bytes;
+        // partial gate/up dot products of this thread's 16-byte chunk
+        constexpr int NB = NV <= 16 ? 16 : 32;
+        float v[NB];
 #pragma unroll
-        for (int q = 0; q < 32; ++q) v[q] = 0.f;
+        for (int q = 0; q < NB; ++q) v[q] = 0.f;
 #pragma unroll
         for (int cc = 0; cc < CH; ++cc) {
             if (cc < nch) {
@@ -122,27 +142,30 @@ __device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, in
                 }
             }
         }
-        if (NV > 8) {
-            const float tot = warp_reduce_scatter32(v);
-            red_s[warp][lane] = tot;
+        // block sum: warp reduce-scatter, one consumer barrier, then every
+        // warp reads the per-warp sums (double-buffered by stage parity)
+        float* red = sh.red + (size_t)(stage_k & 1) * nw * 32;
+        if constexpr (NB == 16) {
+            const float t = warp_reduce_scatter16(v);
+            if ((lane & 1) == 0) red[warp * 32 + (lane >> 1)] = t;
         } else {
-#pragma unroll
-            for (int q = 0; q < NV; ++q) {
-                const float t = warp_sum(v[q]);
-                if (lane == 0) red_s[warp][q] = t;
-            }
+            red[warp * 32 + lane] = warp_reduce_scatter32(v);
         }
-        __syncthreads();
-        if (tid < CH * ROWS) {
-            const int cc = tid / ROWS, r = tid % ROWS;
+        consumer_sync(n_cons);
+        // every thread has finished the previous stage, so its buffer can be
+        // refilled with the stage NS - 1 ahead of this one
+        if (tid == 0 && stage_k > 0 && !sh.prod->done()) sh.prod->issue();
+        float hq = 0.f;
+        if (lane < CH * ROWS) {
+            const int cc = lane / ROWS, r = lane % ROWS;
             float g = 0.f, u = 0.f;
             for (int w = 0; w < nw; ++w) {
-                g += red_s[w][cc * 2 * ROWS + r];
-                u += red_s[w][cc * 2 * ROWS + ROWS + r];
+                g += red[w * 32 + cc * 2 * ROWS + r];
+                u += red[w * 32 + cc * 2 * ROWS + ROWS + r];
             }
-            h_s[cc][r] = cc < nch ? silu(g) * u : 0.f;
+            hq = cc < nch ? silu(g) * u : 0.f;
         }
-        __syncthreads();
+        // down projection: y[r, chunk] += h[c, r] * Wd[c, chunk]
 #pragma unroll
         for (int cc = 0; cc < CH; ++cc) {
             if (cc < nch) {
@@ -151,16 +174,14 @@ __device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, in
                          (W*)nullptr);
 #pragma unroll
                 for (int r = 0; r < ROWS; ++r) {
-                    const float h = h_s[cc][r];
+                    const float h = __shfl_sync(0xffffffffu, hq, cc * ROWS + r);
 #pragma unroll
                     for (int j = 0; j < V; j += 2) fma2(yacc[r][j], yacc[r][j + 1], h, h, wd[j], wd[j + 1]);
                 }
             }
         }
-        __syncthreads();
-        if (tid == 0) prod.issue(stage_k + p.NS);
         ++stage_k;
-        if (*s_abort) break;
+        if (*sh.abort_flag) break;
     }
     // partial output rows of this CTA for this segment
 #pragma unroll
@@ -172,15 +193,17 @@ __device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, in
     }
 }
 
+// Block = one thread per 16-byte chunk of d.  Thread 0 also issues the
+// stage copies.
 template <typename W, int RG, int CH, int MAXT>
-__global__ void __launch_bounds__(MAXT, 1) ffn_gemv_kernel(GemvParams p) {
-    __shared__ __align__(8) uint64_t bars[kNSMax];
-    __shared__ float red_s[MAXT / 32][32];
-    __shared__ float h_s[CH][RG];
+__device__ __forceinline__ void ffn_gemv_body(const GemvParams& p) {
+    __shared__ __align__(8) uint64_t full[kNSMax];
+    __shared__ float red_s[2 * (MAXT / 32) * 32];
     __shared__ int s_abort;
     extern __shared__ __align__(128) unsigned char stage_mem[];
 
     const int tid = threadIdx.x;
+    const int n_cons = blockDim.x;
     const PlanHeader hdr = *p.hdr;
     const int cta = blockIdx.x;
     if (cta >= hdr.G) return;
@@ -195,22 +218,23 @@ __global__ void __launch_bounds__(MAXT, 1) ffn_gemv_kernel(GemvParams p) {
     }
     const int seg0 = s_lo;
 
+    Producer prod;
     if (tid == 0) {
-        for (int b = 0; b < p.NS; ++b) mbar_init(&bars[b], 1);
+        for (int b = 0; b < p.NS; ++b) mbar_init(&full[b], 1);
         fence_mbar_init();
         s_abort = 0;
+        prod.segs = p.segs; prod.table = p.table; prod.stage_mem = stage_mem; prod.full = full;
+        prod.row_bytes = row_bytes; prod.mat_bytes = CH * row_bytes;
+        prod.stage_bytes = 3 * CH * row_bytes; prod.NS = p.NS; prod.CH = CH; prod.seg = seg0;
+        prod.ch = lo; prod.hi = hi; prod.n_seg = hdr.n_seg; prod.issued = 0;
+        prod.policy = l2_evict_first_policy();
+        // fill every buffer but the one the first refill will use
+        for (int k = 0; k < p.NS && !prod.done(); ++k) prod.issue();
     }
     __syncthreads();
 
-    Producer prod;
-    prod.segs = p.segs; prod.table = p.table; prod.stage_mem = stage_mem; prod.bars = bars;
-    prod.row_bytes = row_bytes; prod.mat_bytes = CH * row_bytes; prod.stage_bytes = 3 * CH * row_bytes;
-    prod.NS = p.NS; prod.CH = CH; prod.seg = seg0; prod.ch = lo; prod.hi = hi; prod.issued = 0;
-    prod.n_seg = hdr.n_seg;
-    prod.policy = l2_evict_first_policy();
-    if (tid == 0)
-        for (int k = 0; k < p.NS; ++k) prod.issue(k);
-
+    GemvShared sh;
+    sh.full = full; sh.red = red_s; sh.abort_flag = &s_abort; sh.stage_mem = stage_mem; sh.prod = &prod;
     int stage_k = 0;
     int seg = seg0, ch = lo;
     while (ch < hi && seg < hdr.n_seg) {
@@ -221,8 +245,7 @@ __global__ void __launch_bounds__(MAXT, 1) ffn_gemv_kernel(GemvParams p) {
 #define MOE_PIECE(R)                                                                        \
     case R:                                                                                 \
         if (R <= RG) {                                                                      \
-            gemv_piece<W, RG, CH, (R <= RG ? R : 1)>(p, S, llo, lhi, cta, stage_mem, bars,  \
-                                                     red_s, h_s, &s_abort, stage_k, prod);  \
+            gemv_piece<W, CH, (R <= RG ? R : 1)>(p, S, llo, lhi, cta, sh, n_cons, stage_k);  \
         } else {                                                                            \
             if (tid == 0) set_error(p.err, MOE_ERR_DEVICE_INDEX, seg);                      \
             s_abort = 1;                                                                    \
@@ -236,7 +259,7 @@ __global__ void __launch_bounds__(MAXT, 1) ffn_gemv_kernel(GemvParams p) {
                 s_abort = 1;
         }
         __syncthreads();
-        if (s_abort) break;
+        if (*(volatile int*)&s_abort) break;
         ch = S.ch_start + lhi;
         ++seg;
     }
@@ -244,8 +267,22 @@ __global__ void __launch_bounds__(MAXT, 1) ffn_gemv_kernel(GemvParams p) {
     // the CTA exits and its shared memory is released
     if (tid == 0 && s_abort) {
         for (int k = stage_k; k < prod.issued; ++k)
-            (void)mbar_wait(&bars[k % p.NS], (uint32_t)((k / p.NS) & 1));
+            (void)mbar_wait(&full[k % p.NS], (uint32_t)((k / p.NS) & 1));
     }
+}
+
+// The register file is split over the SM's four sub-partitions, each taking
+// a quarter of the resident warps: 16 warps per SM allow 128 registers per
+// thread.  Two CTAs of 256 threads per SM (d <= 2048) ...
+template <typename W, int RG, int CH>
+__global__ void __launch_bounds__(256, 2) ffn_gemv_kernel_x2(GemvParams p) {
+    ffn_gemv_body<W, RG, CH, 256>(p);
+}
+
+// ... or one CTA of up to 512 threads (d <= 4096).
+template <typename W, int RG, int CH>
+__global__ void __launch_bounds__(512, 1) ffn_gemv_kernel_x1(GemvParams p) {
+    ffn_gemv_body<W, RG, CH, 512>(p);
 }
 
 // Sum the partial rows of each output row in piece order.
@@ -257,13 +294,15 @@ __global__ void __launch_bounds__(256) gemv_reduce_kernel(const PlanHeader* __re
                                                           int N, int n_shared, int T, int routed_cap,
                                                           float* __restrict__ y_perm,
                                                           float* __restrict__ y_shared) {
-    const PlanHeader hdr = *hdr_p;
+    const int n_seg = hdr_p->n_seg, n_routed_rows = hdr_p->n_routed_rows;
+    const int n_partial_rows = hdr_p->n_partial_rows;
     const int row = blockIdx.x;
-    const int rg = hdr.rg;
+    const int rg = hdr_p->rg;
     const int nd4 = d / 4;
+    const int q0 = blockIdx.y * blockDim.x;  // first float4 column of this block
     if (row < routed_cap) {
         const int pos = row;
-        if (pos >= hdr.n_routed_rows) return;
+        if (pos >= n_routed_rows) return;
         int lo = 0, hi = N - 1;  // expert e with offsets[e] <= pos < offsets[e+1]
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
@@ -272,11 +311,12 @@ __global__ void __launch_bounds__(256) gemv_reduce_kernel(const PlanHeader* __re
         const int e = lo;
         const int local = pos - expert_offsets[e];
         const int si = seg_first[e] + local / rg;
-        if (si < 0 || si >= hdr.n_seg) return;
+        if (si < 0 || si >= n_seg) return;
         const Seg S = segs[si];
         const int r = local % rg;
-        if (S.pbase + (S.npieces - 1) * S.rows + r >= hdr.n_partial_rows) return;
-        for (int q = threadIdx.x; q < nd4; q += blockDim.x) {
+        if (S.pbase + (S.npieces - 1) * S.rows + r >= n_partial_rows) return;
+        const int q = q0 + threadIdx.x;
+        if (q < nd4) {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int pc = 0; pc < S.npieces; ++pc) {
                 const float4 v = reinterpret_cast<const float4*>(
@@ -288,14 +328,15 @@ __global__ void __launch_bounds__(256) gemv_reduce_kernel(const PlanHeader* __re
     } else {
         const int t = row - routed_cap;
         if (t >= T || n_shared == 0) return;
-        for (int q = threadIdx.x; q < nd4; q += blockDim.x) {
+        const int q = q0 + threadIdx.x;
+        if (q < nd4) {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int s = 0; s < n_shared; ++s) {
                 const int si = seg_first[N + s] + t / rg;
-                if (si < 0 || si >= hdr.n_seg) continue;
+                if (si < 0 || si >= n_seg) continue;
                 const Seg S = segs[si];
                 const int r = t % rg;
-                if (S.pbase + (S.npieces - 1) * S.rows + r >= hdr.n_partial_rows) continue;
+                if (S.pbase + (S.npieces - 1) * S.rows + r >= n_partial_rows) continue;
                 for (int pc = 0; pc < S.npieces; ++pc) {
                     const float4 v = reinterpret_cast<const float4*>(
                         partial + (size_t)(S.pbase + pc * S.rows + r) * d)[q];
@@ -308,34 +349,47 @@ __global__ void __launch_bounds__(256) gemv_reduce_kernel(const PlanHeader* __re
 }
 
 // ---------------------------------------------------------------------------
-template <typename W, int RG, int CH, int MAXT>
-static cudaError_t launch_gemv_t(const GemvParams& p, int G, cudaStream_t st) {
-    const int threads = p.d / Vec<W>::n;
-    if (threads > MAXT || threads % 32) return cudaErrorInvalidValue;
-    const size_t smem = (size_t)p.NS * 3 * CH * p.d * sizeof(W);
-    cudaError_t e = allow_max_smem(ffn_gemv_kernel<W, RG, CH, MAXT>);
+// Instantiations: bf16 with d <= 2048 runs 2 CTAs per SM, larger d one CTA
+// per SM; 4 rows per segment for bf16 (gemv_rows), 8 for the small fp32 layer.
+template <typename K>
+static cudaError_t launch_gemv_k(K kernel, int maxt, int vec, int ch, int esize, const GemvParams& p,
+                                 int G, cudaStream_t st) {
+    const int threads = p.d / vec;
+    if (threads > maxt || threads % 32) return cudaErrorInvalidValue;
+    const size_t smem = (size_t)p.NS * 3 * ch * p.d * esize;
+    cudaError_t e = allow_max_smem(kernel);
     if (e != cudaSuccess) return e;
-    ffn_gemv_kernel<W, RG, CH, MAXT><<<G, threads, smem, st>>>(p);
-    return cudaGetLastError();
+    kernel<<<G, threads, smem, st>>>(p);
+    return note_launch(reinterpret_cast<const void*>(kernel), threads, smem, cudaGetLastError());
+}
+
+static int gemv_ctas_per_sm(int d, bool bf16) { return (bf16 && d <= 2048) || !bf16 ? 2 : 1; }
+
+int gemv_grid_for(int d, bool bf16, int sms) {
+    const int g = sms * gemv_ctas_per_sm(d, bf16);
+    return g > kGemvMaxCtas ? kGemvMaxCtas : g;
 }
 
 int gemv_stages(int d, bool bf16) {
     const size_t stage = (size_t)3 * 2 * d * (bf16 ? 2 : 4);
-    int ns = (int)((200 * 1024) / stage);
+    const size_t budget = gemv_ctas_per_sm(d, bf16) == 2 ? 100 * 1024 : 200 * 1024;
+    int ns = (int)(budget / stage);
     return ns < 2 ? 2 : (ns > kNSMax ? kNSMax : ns);
 }
 
 cudaError_t launch_gemv(const GemvParams& p, int G, bool bf16, cudaStream_t st) {
     if (bf16) {
-        if (p.d <= 2048) return launch_gemv_t<__nv_bfloat16, 8, 2, 256>(p, G, st);
-        return launch_gemv_t<__nv_bfloat16, 4, 2, 512>(p, G, st);
+        if (p.d <= 2048)
+            return launch_gemv_k(ffn_gemv_kernel_x2<__nv_bfloat16, 4, 2>, 256, 8, 2, 2, p, G, st);
+        return launch_gemv_k(ffn_gemv_kernel_x1<__nv_bfloat16, 4, 2>, 512, 8, 2, 2, p, G, st);
     }
-    return launch_gemv_t<float, 8, 2, 256>(p, G, st);
+    return launch_gemv_k(ffn_gemv_kernel_x2<float, 8, 2>, 256, 4, 2, 4, p, G, st);
 }
 
 cudaError_t launch_gemv_reduce(const GemvReduceArgs& a, cudaStream_t st) {
-    const int grid = a.routed_cap + (a.n_shared > 0 ? a.T : 0);
-    if (grid == 0) return cudaSuccess;
+    const int rows = a.routed_cap + (a.n_shared > 0 ? a.T : 0);
+    if (rows == 0) return cudaSuccess;
+    dim3 grid(rows, (a.d / 4 + 255) / 256);
     gemv_reduce_kernel<<<grid, 256, 0, st>>>(a.hdr, a.segs, a.seg_first, a.expert_offsets, a.partial,
                                              a.d, a.N, a.n_shared, a.T, a.routed_cap, a.y_perm,
                                              a.y_shared);

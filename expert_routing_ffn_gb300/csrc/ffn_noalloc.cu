@@ -106,7 +106,7 @@ extern "C" moe_status moe_expert_ffn_noalloc(const moe_dims* dims, const void* x
     void* base = nullptr;
     int sms = 0;
     if (scratch_for_current_device(&base, &sms) != cudaSuccess) return MOE_ERR_CUDA;
-    const int G = sms > moe::kGemvMaxCtas ? moe::kGemvMaxCtas : sms;
+    const int G = moe::gemv_grid_for(dims->d, dims->wtype == MOE_DTYPE_BF16, sms);
     const ScratchLayout L = scratch_layout(*dims, G);
     if (L.total > kScratchBytes) return MOE_ERR_CAPACITY;  // batch too large for 16 MiB
     const bool bf16 = dims->wtype == MOE_DTYPE_BF16;

@@ -8,6 +8,10 @@
 
 namespace moe {
 
+// On a failed launch: remember the kernel's resource attributes and the
+// launch shape for moe_last_error_detail(); returns e.
+cudaError_t note_launch(const void* kernel, int threads, size_t dyn_smem, cudaError_t e);
+
 struct LogitsArgs {
     const void *x, *x_pre, *w_router, *w_prefetch;
     const float *bias, *w_ord;
@@ -43,13 +47,14 @@ struct PermuteArgs {
     int32_t *expert_offsets, *perm, *inv_perm;
     DevError* err;
 };
-cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st);
-
 struct PlanArgs {
     const int32_t* expert_offsets;
     int T, N, n_shared, I, I_shared, rg, G, max_segs, max_partial_rows;
     PlanHeader* hdr; Seg* segs; int32_t* seg_first; DevError* err;
 };
+// permutation + FFN plan in one launch (the last block builds the plan)
+cudaError_t launch_permute(const PermuteArgs& a, const PlanArgs& plan, int* ticket, cudaStream_t st);
+// the FFN plan alone
 cudaError_t launch_plan_gemv(const PlanArgs& a, cudaStream_t st);
 
 struct GemvParams {
@@ -63,6 +68,7 @@ struct GemvParams {
     DevError* err;
 };
 int gemv_stages(int d, bool bf16);
+int gemv_grid_for(int d, bool bf16, int sms);
 cudaError_t launch_gemv(const GemvParams& p, int G, bool bf16, cudaStream_t st);
 
 struct GemvReduceArgs {
@@ -74,7 +80,7 @@ cudaError_t launch_gemv_reduce(const GemvReduceArgs& a, cudaStream_t st);
 
 struct LoreArgs {
     const void* x; const int32_t *final_idx, *final_kind; const float* final_gate;
-    const void *A, *B; int T, d, k, r, N; bool bf16; float* y_lore; DevError* err;
+    const void *A, *B; int T, d, k, r, N; bool bf16; float* z; float* y_lore; DevError* err;
 };
 cudaError_t launch_lore(const LoreArgs& a, cudaStream_t st);
 

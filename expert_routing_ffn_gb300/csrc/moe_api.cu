@@ -13,7 +13,20 @@
 
 using namespace moe;
 
+static thread_local char g_launch_note[256] = "";
+
 namespace moe {
+
+cudaError_t note_launch(const void* kernel, int threads, size_t dyn_smem, cudaError_t e) {
+    if (e == cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kernel) == cudaSuccess)
+        std::snprintf(g_launch_note, sizeof(g_launch_note),
+                      "kernel regs=%d maxThreads=%d staticSmem=%zu maxDynSmem=%d; launch threads=%d "
+                      "dynSmem=%zu", fa.numRegs, fa.maxThreadsPerBlock, fa.sharedSizeBytes,
+                      fa.maxDynamicSharedSizeBytes, threads, dyn_smem);
+    return e;
+}
 
 cudaError_t allow_max_smem_impl(const void* kernel) {
     static std::mutex mu;
@@ -55,11 +68,12 @@ inline cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
         if (_st != MOE_OK) return _st;                     \
     } while (0)
 
-thread_local char g_detail[256] = "";
+thread_local char g_detail[512] = "";
 
 moe_status record_cuda(cudaError_t e, const char* what) {
-    std::snprintf(g_detail, sizeof(g_detail), "%s: %s (%s)", what, cudaGetErrorName(e),
-                  cudaGetErrorString(e));
+    std::snprintf(g_detail, sizeof(g_detail), "%s: %s (%s)%s%s", what, cudaGetErrorName(e),
+                  cudaGetErrorString(e), g_launch_note[0] ? "; " : "", g_launch_note);
+    g_launch_note[0] = 0;
     return MOE_ERR_CUDA;
 }
 
@@ -109,9 +123,8 @@ int sm_count() {
     return cache[dev];
 }
 
-int gemv_grid() {
-    int g = sm_count();
-    return g > kGemvMaxCtas ? kGemvMaxCtas : g;
+int gemv_grid(const moe_dims* D) {
+    return gemv_grid_for(D->d, D->wtype == MOE_DTYPE_BF16, sm_count());
 }
 
 bool bf16(const moe_dims* D) { return D->wtype == MOE_DTYPE_BF16; }
@@ -311,15 +324,13 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* final_idx, const int
     PermuteArgs a;
     a.final_idx = final_idx; a.final_kind = final_kind; a.n_slots = dims->T * dims->k; a.N = dims->N;
     a.expert_offsets = expert_offsets; a.perm = perm; a.inv_perm = inv_perm; a.err = err;
-    MOE_CUDA(launch_permute(a, S(stream)));
-    count();
     PlanArgs pa;
     pa.expert_offsets = expert_offsets; pa.T = dims->T; pa.N = dims->N; pa.n_shared = dims->n_shared;
     pa.I = dims->I; pa.I_shared = dims->I_shared; pa.rg = gemv_rows(*dims);
-    pa.G = gemv_grid(); pa.max_segs = L.max_segs; pa.max_partial_rows = L.max_partial_rows;
+    pa.G = gemv_grid(dims); pa.max_segs = L.max_segs; pa.max_partial_rows = L.max_partial_rows;
     pa.hdr = ws_at<PlanHeader>(ws, L.plan_hdr); pa.segs = ws_at<Seg>(ws, L.segs);
     pa.seg_first = ws_at<int32_t>(ws, L.seg_first); pa.err = err;
-    MOE_CUDA(launch_plan_gemv(pa, S(stream)));
+    MOE_CUDA(launch_permute(a, pa, ws_at<int>(ws, L.ticket), S(stream)));
     count();
     return MOE_OK;
 }
@@ -341,7 +352,7 @@ moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table
     p.perm = perm; p.table = static_cast<const ExpertEntry*>(table);
     p.hdr = ws_at<PlanHeader>(ws, L.plan_hdr); p.segs = ws_at<Seg>(ws, L.segs);
     p.partial = ws_at<float>(ws, L.partial); p.err = ws_at<DevError>(ws, L.err);
-    MOE_CUDA(launch_gemv(p, gemv_grid(), bf16(dims), S(stream)));
+    MOE_CUDA(launch_gemv(p, gemv_grid(dims), bf16(dims), S(stream)));
     count();
     GemvReduceArgs r;
     r.hdr = p.hdr; r.segs = p.segs; r.seg_first = ws_at<int32_t>(ws, L.seg_first);
@@ -355,9 +366,10 @@ moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table
 
 moe_status moe_lore(const moe_dims* dims, const void* x, const int32_t* final_idx,
                     const int32_t* final_kind, const float* final_gate, const void* lore_a,
-                    const void* lore_b, float* y_lore, void* stream) {
+                    const void* lore_b, float* y_lore, void* ws, size_t ws_bytes, void* stream) {
     MOE_TRY(check_dims(dims));
     if (dims->r <= 0) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_ws(dims, ws, ws_bytes));
     if (dims->T == 0) return MOE_OK;
     if (!x || !final_idx || !final_kind || !final_gate || !y_lore || !lore_a || !lore_b)
         return MOE_ERR_INVALID_ARG;
@@ -365,10 +377,11 @@ moe_status moe_lore(const moe_dims* dims, const void* x, const int32_t* final_id
     LoreArgs a;
     a.x = x; a.final_idx = final_idx; a.final_kind = final_kind; a.final_gate = final_gate;
     a.A = lore_a; a.B = lore_b; a.T = dims->T; a.d = dims->d; a.k = dims->k; a.r = dims->r;
-    // without a workspace there is no error word: a bad index skips the slot
-    a.N = dims->N; a.bf16 = bf16(dims); a.y_lore = y_lore; a.err = nullptr;
+    const WsLayout L = ws_layout(*dims);
+    a.N = dims->N; a.bf16 = bf16(dims); a.y_lore = y_lore;
+    a.z = ws_at<float>(ws, L.lore_z); a.err = ws_at<DevError>(ws, L.err);
     MOE_CUDA(launch_lore(a, S(stream)));
-    count();
+    count(2);
     return MOE_OK;
 }
 
@@ -407,7 +420,7 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_layer_args* A,
     const bool lore = dims->r > 0 && A->lore_a && A->lore_b && O->y_lore;
     if (lore)
         MOE_TRY(moe_lore(dims, A->x, O->final_idx, O->final_kind, O->final_gate, A->lore_a,
-                         A->lore_b, O->y_lore, stream));
+                         A->lore_b, O->y_lore, ws, ws_bytes, stream));
     MOE_TRY(moe_combine(dims, O->y_perm, O->inv_perm, O->final_gate, O->final_kind,
                         dims->n_shared > 0 ? O->y_shared : nullptr, lore ? O->y_lore : nullptr,
                         O->out, stream));

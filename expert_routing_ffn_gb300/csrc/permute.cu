@@ -8,20 +8,27 @@
 
 namespace moe {
 
+__device__ void build_plan(const PlanArgs& a, const int* off);
+
 // One block per expert e.  Pass 1 counts the slots routed to experts below e
 // (the segment offset) and to e; pass 2 walks the slots in order and
 // scatters e's slots with a block-wide prefix over 1024-slot chunks.
 // Block 0 also marks LoRE / empty slots with inv_perm = -1.
+// The last block to finish (arrival counter `ticket`, left at 0 afterwards)
+// also builds the FFN plan from the complete expert_offsets.
 __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict__ final_idx,
                                                        const int32_t* __restrict__ final_kind,
                                                        int n_slots, int N,
                                                        int32_t* __restrict__ expert_offsets,
                                                        int32_t* __restrict__ perm,
                                                        int32_t* __restrict__ inv_perm,
-                                                       DevError* __restrict__ err) {
+                                                       DevError* __restrict__ err, PlanArgs plan,
+                                                       int* __restrict__ ticket) {
     __shared__ int red_less[32], red_eq[32];
     __shared__ int warp_pref[32];
     __shared__ int s_off;
+    __shared__ int s_last;
+    __shared__ int s_offsets[kMaxExperts + 1];
     const int e = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
     int less = 0, eq = 0;
@@ -74,75 +81,92 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
         running += total;
         __syncthreads();
     }
+    if (tid == 0) {
+        __threadfence();
+        s_last = atomicAdd(ticket, 1) == (int)gridDim.x - 1;
+    }
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        for (int i = tid; i <= N; i += blockDim.x) s_offsets[i] = __ldcg(&expert_offsets[i]);
+        __syncthreads();
+        if (tid == 0) {
+            build_plan(plan, s_offsets);
+            *ticket = 0;
+        }
+    }
 }
 
-// FFN plan for the GEMV path (one block, sequential over segments).
+// FFN plan for the GEMV path (one thread, sequential over segments).
 // Segments: shared experts first (rows = tokens, in groups of rg), then each
 // routed expert's permuted rows in groups of rg.  Channels of all segments
 // form one list split evenly over G CTAs; see Seg in common.cuh.
-__global__ void plan_gemv_kernel(const int32_t* __restrict__ expert_offsets, int T, int N,
-                                 int n_shared, int I, int I_shared, int rg, int G, int max_segs,
-                                 int max_partial_rows, PlanHeader* __restrict__ hdr,
-                                 Seg* __restrict__ segs, int32_t* __restrict__ seg_first,
-                                 DevError* __restrict__ err) {
-    if (threadIdx.x != 0) return;
+// `off` holds expert_offsets[0..N] (shared memory).
+__device__ void build_plan(const PlanArgs& a, const int* off) {
+    const int T = a.T, N = a.N, n_shared = a.n_shared, rg = a.rg, G = a.G;
     int n = 0, ch = 0;
     auto add = [&](int expert, int row0, int rows, int Ie) {
-        if (n < max_segs) {
+        if (n < a.max_segs) {
             Seg s;
             s.expert = expert; s.row0 = row0; s.rows = rows; s.I = Ie; s.ch_start = ch;
             s.c0 = 0; s.npieces = 0; s.pbase = 0;
-            segs[n] = s;
+            a.segs[n] = s;
         }
         ++n;
         ch += Ie;
     };
     for (int s = 0; s < n_shared; ++s) {
-        seg_first[N + s] = n;
-        for (int r = 0; r < T; r += rg) add(N + s, r, min(rg, T - r), I_shared);
+        a.seg_first[N + s] = n;
+        for (int r = 0; r < T; r += rg) add(N + s, r, min(rg, T - r), a.I_shared);
     }
     for (int e = 0; e < N; ++e) {
-        seg_first[e] = n;
-        const int a = expert_offsets[e], b = expert_offsets[e + 1];
-        for (int r = a; r < b; r += rg) add(e, r, min(rg, b - r), I);
+        a.seg_first[e] = n;
+        const int lo = off[e], hi = off[e + 1];
+        for (int r = lo; r < hi; r += rg) add(e, r, min(rg, hi - r), a.I);
     }
-    seg_first[N + n_shared] = n;
+    a.seg_first[N + n_shared] = n;
     PlanHeader h;
     h.G = G; h.rg = rg;
     // A plan that does not fit the workspace is published empty (no segment,
     // no channel, no routed row): the FFN kernels then do nothing, and the
     // error word says why, instead of indexing past the tables.
     auto publish_empty = [&](int detail) {
-        set_error(err, MOE_ERR_CAPACITY, detail);
+        set_error(a.err, MOE_ERR_CAPACITY, detail);
         h.n_seg = 0; h.total_ch = 0; h.P = 1; h.n_partial_rows = 0; h.n_routed_rows = 0;
-        *hdr = h;
+        *a.hdr = h;
     };
-    if (n > max_segs) { publish_empty(n); return; }
+    if (n > a.max_segs) { publish_empty(n); return; }
     const int P = ch > 0 ? (ch + G - 1) / G : 1;
     int pbase = 0;
     for (int i = 0; i < n; ++i) {
-        Seg& s = segs[i];
+        Seg& s = a.segs[i];
         s.c0 = s.ch_start / P;
         s.npieces = (s.ch_start + s.I - 1) / P - s.c0 + 1;
         s.pbase = pbase;
         pbase += s.npieces * s.rows;
     }
-    if (pbase > max_partial_rows) { publish_empty(pbase); return; }
+    if (pbase > a.max_partial_rows) { publish_empty(pbase); return; }
     h.n_seg = n; h.total_ch = ch; h.P = P; h.n_partial_rows = pbase;
-    h.n_routed_rows = expert_offsets[N];
-    *hdr = h;
+    h.n_routed_rows = off[N];
+    *a.hdr = h;
 }
 
-cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st) {
+__global__ void plan_gemv_kernel(PlanArgs a) {
+    __shared__ int off[kMaxExperts + 1];
+    for (int i = threadIdx.x; i <= a.N; i += blockDim.x) off[i] = __ldcg(&a.expert_offsets[i]);
+    __syncthreads();
+    if (threadIdx.x == 0) build_plan(a, off);
+}
+
+cudaError_t launch_permute(const PermuteArgs& a, const PlanArgs& plan, int* ticket,
+                           cudaStream_t st) {
     permute_kernel<<<a.N, 1024, 0, st>>>(a.final_idx, a.final_kind, a.n_slots, a.N,
-                                         a.expert_offsets, a.perm, a.inv_perm, a.err);
+                                         a.expert_offsets, a.perm, a.inv_perm, a.err, plan, ticket);
     return cudaGetLastError();
 }
 
 cudaError_t launch_plan_gemv(const PlanArgs& a, cudaStream_t st) {
-    plan_gemv_kernel<<<1, 32, 0, st>>>(a.expert_offsets, a.T, a.N, a.n_shared, a.I, a.I_shared,
-                                       a.rg, a.G, a.max_segs, a.max_partial_rows, a.hdr, a.segs,
-                                       a.seg_first, a.err);
+    plan_gemv_kernel<<<1, 32, 0, st>>>(a);
     return cudaGetLastError();
 }
 

@@ -349,14 +349,16 @@ template <typename W>
 static cudaError_t launch_logits_t(const LogitsArgs& a, cudaStream_t st) {
     constexpr int TT = 8;
     const int n_out = a.has_prefetch ? 2 * a.N + 1 : a.N;
+    const int t_tiles = (a.T + TT - 1) / TT;
     const int rows_per_block = 8;
-    dim3 grid((a.T + TT - 1) / TT, (n_out + rows_per_block - 1) / rows_per_block);
+    const int threads = 256;
+    dim3 grid(t_tiles, (n_out + rows_per_block - 1) / rows_per_block);
     const size_t smem = (size_t)2 * TT * a.d * sizeof(W);
     if (smem > 48 * 1024) {
         cudaError_t e = allow_max_smem(route_logits_kernel<W, TT>);
         if (e != cudaSuccess) return e;
     }
-    route_logits_kernel<W, TT><<<grid, 256, smem, st>>>(
+    route_logits_kernel<W, TT><<<grid, threads, smem, st>>>(
         (const W*)a.x, (const W*)(a.x_pre ? a.x_pre : a.x), (const W*)a.w_router, a.bias,
         (const W*)a.w_prefetch, a.w_ord, a.T, a.d, a.N, n_out, rows_per_block, a.logits_r,
         a.logits_p, a.score);

@@ -252,10 +252,11 @@ moe_status moe_expert_ffn_noalloc(const moe_dims* dims, const void* x, const voi
  *   y_lore[t] = sum over LoRE slots s of final_gate[t,s] * B_e (A_e x_t),
  *   e = final_idx[t,s]; zero rows for tokens without LoRE slots.
  *   lore_a [N, r, d], lore_b [N, d, r] in the layer's weight type;
- *   y_lore [T, d] float32 (written). */
+ *   y_lore [T, d] float32 (written).  The rank-r projections A_e x_t go
+ *   through the workspace. */
 moe_status moe_lore(const moe_dims* dims, const void* x, const int32_t* final_idx,
                     const int32_t* final_kind, const float* final_gate, const void* lore_a,
-                    const void* lore_b, float* y_lore, void* stream);
+                    const void* lore_b, float* y_lore, void* ws, size_t ws_bytes, void* stream);
 
 /* Stage 5 — combine:
  *   out[t] = y_shared[t] * (1 + sum of LoRE-slot gates)

@@ -88,7 +88,7 @@ def test_null_buffers_rejected_before_cuda():
     st = L.moe_combine(C.byref(D), None, None, None, None, None, None, None, None)
     assert st == moe.MOE_ERR_INVALID_ARG
     # LoRE needs a rank
-    st = L.moe_lore(C.byref(D), None, None, None, None, None, None, None, None)
+    st = L.moe_lore(C.byref(D), None, None, None, None, None, None, None, None, 0, None)
     assert st == moe.MOE_ERR_INVALID_ARG
     # a bad miss policy
     n = moe.moe_workspace_size(D)

@@ -111,7 +111,8 @@ def test_stagewise_calls_equal_layer_forward():
     moe.moe_permute(D, b.final_idx, b.final_kind, b.expert_offsets, b.perm, b.inv_perm, layer.ws)
     moe.moe_expert_ffn(D, xd, layer.table, b.expert_offsets, b.perm, 1.0, b.y_perm, b.y_shared,
                        layer.ws)
-    moe.moe_lore(D, xd, b.final_idx, b.final_kind, b.final_gate, layer.lore_a, layer.lore_b, b.y_lore)
+    moe.moe_lore(D, xd, b.final_idx, b.final_kind, b.final_gate, layer.lore_a, layer.lore_b, b.y_lore,
+                 layer.ws)
     moe.moe_combine(D, b.y_perm, b.inv_perm, b.final_gate, b.final_kind, b.y_shared, b.y_lore, b.out)
     assert moe.moe_check(layer.ws)[0] == moe.MOE_OK
     assert torch.equal(b.out, bufs.out)
