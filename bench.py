@@ -306,13 +306,18 @@ def main():
     clocks = clk.summary()
 
     # ---- dominant kernel: the expert FFN stage, timed alone on the same stream
-    # (route/select/permute outputs of each copy are already in place)
-    fb = []
+    # (route/select/permute outputs of each copy are already in place).
+    # Decode: algorithmic bytes = weights of the distinct experts computed plus
+    # the shared experts.  Prefill: algorithmic FLOPs = 2 * 3 * d * I per
+    # computed (token, expert) row plus 2 * 3 * d * I_shared per token and
+    # shared expert.
+    fb, ff = [], []
     for c, L in enumerate(layers):
         off = bufs[c].expert_offsets.cpu().numpy()
         u = int((np.diff(off) > 0).sum())
         fb.append(u * expert_bytes + shared_bytes)
-    n_k = max(50, min(2000, args.steps // 2))
+        ff.append(6.0 * cfg.d * (int(off[-1]) * cfg.I + T * cfg.n_shared * cfg.I_shared))
+    n_k = max(10 if phase == "prefill" else 50, min(2000, args.steps // 2))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_k)]
     for i in range(n_k + n_copies):
         c = i % n_copies
@@ -327,14 +332,28 @@ def main():
     torch.cuda.synchronize()
     k_ms = [a.elapsed_time(b) for a, b in evs]
     k_bytes = [fb[(i + n_copies) % n_copies] for i in range(n_k)]
-    achieved = sum(k_bytes) / (sum(k_ms) / 1e3) / 1e9
-    traffic = recorded_traffic("ffn_gemv.cu", wl_name)
+    k_flops = [ff[(i + n_copies) % n_copies] for i in range(n_k)]
+    if phase == "decode":
+        achieved = sum(k_bytes) / (sum(k_ms) / 1e3) / 1e9
+        roof = {"kernel": "moe_expert_ffn (ffn_gemv_kernel + gemv_reduce_kernel)", "bound": "hbm",
+                "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
+                "peak_source": peak_src, "algorithmic_bytes_per_launch": float(statistics.mean(fb)),
+                "avg_launch_ms": statistics.mean(k_ms),
+                "traffic": recorded_traffic("ffn_gemv.cu", wl_name)}
+    else:
+        achieved = sum(k_flops) / (sum(k_ms) / 1e3) / 1e12
+        roof = {"kernel": "moe_expert_ffn (gather + ffn_tc_kernel<1> + ffn_tc_kernel<2>)",
+                "bound": "tensor", "achieved": achieved, "peak": bf16_tflops, "unit": "TFLOP/s",
+                "frac": achieved / bf16_tflops, "peak_source": peak_src + " bf16 burst",
+                "algorithmic_flops_per_launch": float(statistics.mean(ff)),
+                "avg_launch_ms": statistics.mean(k_ms),
+                "traffic": recorded_traffic("ffn_tc.cu", wl_name)}
 
     # ---- end to end through the public API: pinned host x -> device, layer
     # forward, result -> pinned host, every step
     x_host = [xs[c].cpu().pin_memory() for c in range(n_copies)]
     out_host = [torch.empty_like(bufs[c].out, device="cpu").pin_memory() for c in range(n_copies)]
-    n_e2e = max(20, min(args.steps, 1000))
+    n_e2e = max(5 if phase == "prefill" else 20, min(args.steps, 1000))
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -359,11 +378,7 @@ def main():
                    "resident": cfg.n_resident, "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: {n_copies} rotating layer copies of "
                          f"{layer_bytes / 1e9:.2f} GB", "cuda_graph": True},
-        "roofline": {"kernel": "moe_expert_ffn (ffn_gemv_kernel + gemv_reduce_kernel)",
-                     "bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
-                     "frac": achieved / hbm_gbs, "peak_source": peak_src,
-                     "algorithmic_bytes_per_launch": float(statistics.mean(fb)),
-                     "avg_launch_ms": statistics.mean(k_ms), "traffic": traffic},
+        "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": xs[0].numel() * xs[0].element_size(),
                 "d2h_bytes_per_step": bufs[0].out.numel() * 4, "steps": n_e2e,
                 "note": "moe_layer_forward per step with pinned-host copies and a stream sync, no graph"},

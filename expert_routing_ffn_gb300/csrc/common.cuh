@@ -61,10 +61,33 @@ struct PlanHeader {
     int pad[9];
 };
 
+// Tensor-core (prefill) plan: one segment per routed expert with rows, plus
+// one segment for all shared experts (their channels stacked).  Phase-1
+// tiles of a segment: m_tiles x n1 (128-channel tiles), phase-2 tiles:
+// m_tiles x d/256; tile index = first tile + nt * m_tiles + mt.
+struct TcSeg {
+    int shared, expert, row0, rows, m_tiles, n1, tile1, tile2;
+};
+struct TcPlan {
+    int n_seg, n_tiles1, n_tiles2;
+    int pad[13];
+    TcSeg seg[kMaxExperts + 1];
+};
+
+// Batches above this many tokens run the expert FFN on the tensor cores
+// (bf16 layers whose I, I_shared are multiples of 128).
+constexpr int kTcMinTokens = 64;
+
+__host__ __device__ inline bool tc_usable(const moe_dims& D) {
+    return D.wtype == MOE_DTYPE_BF16 && D.I % 128 == 0 && (D.n_shared == 0 || D.I_shared % 128 == 0) &&
+           D.d % 256 == 0;
+}
+__host__ __device__ inline bool use_tc(const moe_dims& D) { return tc_usable(D) && D.T > kTcMinTokens; }
+
 // ---------------------------------------------------------------- workspace
 struct WsLayout {
-    size_t err, ticket, logits_r, logits_p, score, qp, plan_hdr, segs, seg_first, lore_z, partial,
-        total;
+    size_t err, ticket, logits_r, logits_p, score, qp, plan_hdr, segs, seg_first, lore_z, tc_plan,
+        x_perm, h_routed, h_shared, partial, total;
     int max_segs, max_partial_rows;
 };
 
@@ -80,8 +103,12 @@ __host__ __device__ inline int gemv_rows(const moe_dims& D) {
 __host__ __device__ inline WsLayout ws_layout(const moe_dims& D) {
     WsLayout L;
     const size_t T = (size_t)(D.T > 0 ? D.T : 1), N = (size_t)D.N;
-    const size_t rows_routed = T * (size_t)D.k;
-    const size_t rows_shared = T * (size_t)D.n_shared;
+    const bool tc = use_tc(D);
+    // the GEMV (and its partial sums) only serves batches of <= kTcMinTokens
+    // tokens when the tensor-core path takes the larger ones
+    const size_t Tg = tc ? (size_t)kTcMinTokens : T;
+    const size_t rows_routed = Tg * (size_t)D.k;
+    const size_t rows_shared = Tg * (size_t)D.n_shared;
     const int rg = gemv_rows(D);
     // segments: sum over experts of ceil(rows_e / rg) <= rows / rg + N, plus the
     // shared experts' ceil(T / rg) each
@@ -100,7 +127,11 @@ __host__ __device__ inline WsLayout ws_layout(const moe_dims& D) {
     L.plan_hdr = take(sizeof(PlanHeader));
     L.segs = take((size_t)L.max_segs * sizeof(Seg));
     L.seg_first = take((N + (size_t)D.n_shared + 1) * 4);
-    L.lore_z = take(rows_routed * (size_t)(D.r > 0 ? D.r : 1) * 4);
+    L.lore_z = take(T * (size_t)D.k * (size_t)(D.r > 0 ? D.r : 1) * 4);
+    L.tc_plan = take(sizeof(TcPlan));
+    L.x_perm = take(tc ? T * D.k * (size_t)D.d * 2 : 0);
+    L.h_routed = take(tc ? T * D.k * (size_t)D.I * 2 : 0);
+    L.h_shared = take(tc ? T * (size_t)D.n_shared * D.I_shared * 2 : 0);
     L.partial = take((size_t)L.max_partial_rows * (size_t)D.d * 4);
     L.total = o;
     return L;

@@ -119,6 +119,7 @@ extern "C" moe_status moe_expert_ffn_noalloc(const moe_dims* dims, const void* x
     pa.max_segs = L.max_segs; pa.max_partial_rows = L.max_partial_rows;
     pa.hdr = moe::ws_at<moe::PlanHeader>(base, L.hdr); pa.segs = moe::ws_at<moe::Seg>(base, L.segs);
     pa.seg_first = moe::ws_at<int32_t>(base, L.seg_first); pa.err = err;
+    pa.d = dims->d; pa.tc_plan = nullptr;
     if (moe::launch_plan_gemv(pa, s) != cudaSuccess) return MOE_ERR_CUDA;
 
     moe::GemvParams p;

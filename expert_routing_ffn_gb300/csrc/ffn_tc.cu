@@ -1,0 +1,406 @@
+// Stage 3b, prefill-size batches: the grouped SwiGLU expert FFN on the
+// 5th-generation tensor cores (tcgen05, accumulators in tensor memory), fed
+// by TMA.  Two persistent launches:
+//   phase 1: for every (expert segment, 128-row tile, 128-channel tile):
+//            [gate | up] = X_tile . [Wg_tile ; Wu_tile]^T  (M=128, N=256)
+//            epilogue h = SiLU(gate) * up  -> h (bf16)
+//   phase 2: for every (segment, 128-row tile, 256-column tile of d):
+//            y = h_tile . Wd  (K = I; Wd is [I, d], an MN-major operand)
+//            epilogue -> y (fp32, ungated)
+// Shared experts form one segment whose channels are the concatenation of
+// all shared experts (so phase 2 sums them, as y_shared requires).
+//
+// Block: warp 0 issues TMA loads (4-stage ring of 48 KB), warp 1 allocates
+// tensor memory and issues the MMAs (one thread), warps 2-5 drain the
+// accumulators (one TMEM lane = one tile row per thread).  Accumulators are
+// double-buffered (2 x 256 columns) so the epilogue of one tile overlaps the
+// MMAs of the next.  Every wait is bounded by a clock budget; a timeout sets
+// MOE_ERR_TIMEOUT and all roles leave their loops.
+#include <cuda.h>
+
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tma.h"
+
+namespace moe {
+
+constexpr int kTcBM = 128, kTcBN = 256, kTcStages = 4, kTcThreads = 192;
+constexpr uint32_t kTcStageA = kTcBM * kTcBK * 2;  // 16 KB
+constexpr uint32_t kTcStageB = kTcBN * kTcBK * 2;  // 32 KB
+constexpr uint32_t kTcStageBytes = kTcStageA + kTcStageB;
+constexpr uint32_t kTcSmemBytes = kTcStages * kTcStageBytes + 1024;  // + alignment slack
+constexpr long long kTcWaitCycles = 4000000000LL;                   // ~2 s at 2 GHz
+
+struct TcParams {
+    CUtensorMap map_a_shared;  // phase 1: x [T, d];         phase 2: h_shared [T, ns*Is]
+    CUtensorMap map_a_routed;  // phase 1: x_perm [T*k, d];  phase 2: h_routed [T*k, I]
+    const ExpertEntry* table;
+    const TcPlan* plan;
+    void* out_shared;          // phase 1: h_shared (bf16);  phase 2: y_shared (fp32)
+    void* out_routed;          // phase 1: h_routed (bf16);  phase 2: y_perm (fp32)
+    long long ld_out_shared, ld_out_routed;  // row strides (elements)
+    int d, N, I, I_shared, n_shared;
+    DevError* err;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+// Wait on an mbarrier phase; give up when another role has aborted
+// (honor_abort) or after the clock budget (records MOE_ERR_TIMEOUT).
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                        DevError* err, int where, bool honor_abort = true) {
+    const long long t0 = clock64();
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63) == 63) {
+            if (honor_abort && *abort_flag) return false;
+            if (clock64() - t0 > kTcWaitCycles) {
+                set_error(err, MOE_ERR_TIMEOUT, where);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int c0, int c1,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(bar)) : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading and
+// stride byte offsets (all >> 4), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: D f32, A and B bf16, A K-major,
+// B K-major (b_mn = 0) or MN-major (b_mn = 1), N and M as given.
+__host__ __device__ constexpr uint32_t tc_idesc(int M, int N, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15},"
+        " [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&p);
+}
+
+// ---------------------------------------------------------------- tiles
+struct TcTile {
+    int seg, mt, nt;
+};
+
+template <int PHASE>
+__device__ __forceinline__ bool tc_tile(const TcPlan& P, int t, TcTile& out) {
+    const int total = PHASE == 1 ? P.n_tiles1 : P.n_tiles2;
+    if (t >= total) return false;
+    int s = 0;
+    while (s + 1 < P.n_seg && (PHASE == 1 ? P.seg[s + 1].tile1 : P.seg[s + 1].tile2) <= t) ++s;
+    const TcSeg& S = P.seg[s];
+    const int local = t - (PHASE == 1 ? S.tile1 : S.tile2);
+    out.seg = s;
+    out.mt = local % S.m_tiles;
+    out.nt = local / S.m_tiles;
+    return true;
+}
+
+// ---------------------------------------------------------------- kernel
+template <int PHASE>
+__global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_constant__ TcParams p) {
+    extern __shared__ unsigned char tc_smem_raw[];
+    __shared__ __align__(8) uint64_t full[kTcStages], empty[kTcStages], tfull[2], tempty[2], drain;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int abort_s;
+    __shared__ TcPlan plan_s;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t smem_base = (smem_u32(tc_smem_raw) + 1023u) & ~1023u;
+    volatile int* abort_flag = &abort_s;
+
+    for (int i = tid; i < (int)(sizeof(TcPlan) / 4); i += blockDim.x)
+        reinterpret_cast<int*>(&plan_s)[i] = reinterpret_cast<const int*>(p.plan)[i];
+    if (tid == 0) {
+        for (int s = 0; s < kTcStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);  // one arrival per epilogue warp
+        }
+        mbar_init(&drain, 1);
+        fence_mbar_init();
+        abort_s = 0;
+    }
+    if (warp == 1) {  // tensor memory: 512 columns = two 128x256 fp32 accumulators
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;"
+                     ::"r"(smem_u32(&tmem_base_s)));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = tmem_base_s;
+    const TcPlan& P = plan_s;
+    const int d = p.d;
+
+    if (warp == 0) {
+        // ---------------- TMA producer
+        if (lane == 0) {
+            int it = 0;
+            TcTile tl;
+            for (int t = blockIdx.x; tc_tile<PHASE>(P, t, tl) && !*abort_flag; t += gridDim.x) {
+                const TcSeg& S = P.seg[tl.seg];
+                const CUtensorMap* amap = S.shared ? &p.map_a_shared : &p.map_a_routed;
+                const int arow = S.row0 + tl.mt * kTcBM;
+                const int nk = PHASE == 1 ? d / (int)kTcBK
+                                          : (S.shared ? p.n_shared * p.I_shared : p.I) / (int)kTcBK;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int st = it % kTcStages;
+                    const uint32_t par = ((it / kTcStages) & 1) ^ 1;
+                    if (!tc_wait(&empty[st], par, abort_flag, p.err, 1)) break;
+                    const uint32_t a_dst = smem_base + st * kTcStageBytes;
+                    const uint32_t b_dst = a_dst + kTcStageA;
+                    mbar_arrive_expect_tx(&full[st], kTcStageBytes);
+                    tma_load_2d(a_dst, amap, kb * kTcBK, arow, &full[st]);
+                    if (PHASE == 1) {
+                        int e, nrow;
+                        if (S.shared) {
+                            const int per = p.I_shared / 128;
+                            e = p.N + tl.nt / per;
+                            nrow = (tl.nt % per) * 128;
+                        } else {
+                            e = S.expert;
+                            nrow = tl.nt * 128;
+                        }
+                        const ExpertEntry* E = p.table + e;
+                        tma_load_2d(b_dst, E->tmap[0], kb * kTcBK, nrow, &full[st]);
+                        tma_load_2d(b_dst + kTcStageB / 2, E->tmap[1], kb * kTcBK, nrow, &full[st]);
+                    } else {
+                        int e, krow;
+                        if (S.shared) {
+                            const int k0 = kb * kTcBK;
+                            e = p.N + k0 / p.I_shared;
+                            krow = k0 % p.I_shared;
+                        } else {
+                            e = S.expert;
+                            krow = kb * kTcBK;
+                        }
+                        const ExpertEntry* E = p.table + e;
+#pragma unroll
+                        for (int j = 0; j < kTcBN / 64; ++j)
+                            tma_load_2d(b_dst + j * (64 * kTcBK * 2), E->tmap[2], tl.nt * kTcBN + j * 64,
+                                        krow, &full[st]);
+                    }
+                }
+            }
+            // wait for the last loads in flight before the block may exit
+            for (int k = (it > kTcStages ? it - kTcStages : 0); k < it; ++k)
+                (void)tc_wait(&full[k % kTcStages], (k / kTcStages) & 1, abort_flag, p.err, 2, false);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc_idesc(kTcBM, kTcBN, PHASE == 1 ? 0 : 1);
+            int it = 0, local = 0;
+            TcTile tl;
+            for (int t = blockIdx.x; tc_tile<PHASE>(P, t, tl) && !*abort_flag; t += gridDim.x, ++local) {
+                const TcSeg& S = P.seg[tl.seg];
+                const int ab = local & 1;
+                if (!tc_wait(&tempty[ab], ((local >> 1) & 1) ^ 1, abort_flag, p.err, 3)) break;
+                tc_fence_after();
+                const uint32_t tmem_d = tmem_base + ab * kTcBN;
+                const int nk = PHASE == 1 ? d / (int)kTcBK
+                                          : (S.shared ? p.n_shared * p.I_shared : p.I) / (int)kTcBK;
+                bool ok = true;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int st = it % kTcStages;
+                    if (!tc_wait(&full[st], (it / kTcStages) & 1, abort_flag, p.err, 4)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_base + st * kTcStageBytes;
+                    const uint32_t b_addr = a_addr + kTcStageA;
+#pragma unroll
+                    for (int kk = 0; kk < (int)kTcBK / 16; ++kk) {
+                        const uint64_t ad = smem_desc(a_addr + kk * 32, 16, 1024);
+                        const uint64_t bd = PHASE == 1 ? smem_desc(b_addr + kk * 32, 16, 1024)
+                                                       : smem_desc(b_addr + kk * 16 * 128, 64 * kTcBK * 2, 1024);
+                        tc_mma(tmem_d, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+                    }
+                    tc_commit(&empty[st]);  // frees the stage when these MMAs are done
+                }
+                if (!ok) break;
+                tc_commit(&tfull[ab]);      // accumulator ready for the epilogue
+            }
+            // every MMA this thread issued has finished before tensor memory
+            // is released
+            tc_commit(&drain);
+            (void)tc_wait(&drain, 0, abort_flag, p.err, 6, false);
+        }
+    } else {
+        // ---------------- epilogue: warps 2..5, thread = accumulator row
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        int local = 0;
+        TcTile tl;
+        // decisions stay warp-uniform: tcgen05.ld is a whole-warp instruction
+        for (int t = blockIdx.x; tc_tile<PHASE>(P, t, tl); t += gridDim.x, ++local) {
+            if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+            const TcSeg& S = P.seg[tl.seg];
+            const int ab = local & 1;
+            bool ok = true;
+            if (lane == 0) ok = tc_wait(&tfull[ab], (local >> 1) & 1, abort_flag, p.err, 5);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + ab * kTcBN;
+            const int row_in_seg = tl.mt * kTcBM + r;
+            const bool valid = row_in_seg < S.rows;
+            const long long grow = (long long)S.row0 + row_in_seg;
+            if (PHASE == 1) {
+                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(S.shared ? p.out_shared : p.out_routed);
+                const long long ld = S.shared ? p.ld_out_shared : p.ld_out_routed;
+                __nv_bfloat16* dst = out + grow * ld + (long long)tl.nt * 128;
+#pragma unroll 1
+                for (int c = 0; c < 128; c += 16) {
+                    float g[16], u[16];
+                    tmem_ld16(taddr + c, g);
+                    tmem_ld16(taddr + 128 + c, u);
+                    if (valid) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float h0 = g[2 * i] / (1.f + expf(-g[2 * i])) * u[2 * i];
+                            const float h1 = g[2 * i + 1] / (1.f + expf(-g[2 * i + 1])) * u[2 * i + 1];
+                            w[i] = pack_bf16x2(h0, h1);
+                        }
+                        reinterpret_cast<uint4*>(dst + c)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        reinterpret_cast<uint4*>(dst + c)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    }
+                }
+            } else {
+                float* out = static_cast<float*>(S.shared ? p.out_shared : p.out_routed);
+                const long long ld = S.shared ? p.ld_out_shared : p.ld_out_routed;
+                float* dst = out + grow * ld + (long long)tl.nt * kTcBN;
+#pragma unroll 1
+                for (int c = 0; c < kTcBN; c += 16) {
+                    float v[16];
+                    tmem_ld16(taddr + c, v);
+                    if (valid) {
+#pragma unroll
+                        for (int i = 0; i < 16; i += 4)
+                            *reinterpret_cast<float4*>(dst + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[ab]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base));
+    }
+}
+
+// ---------------------------------------------------------------- gather
+// x_perm[pos] = x[perm[pos] / k] for the routed rows (bf16, 16-byte copies).
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x,
+                                                          const int32_t* __restrict__ perm,
+                                                          const int32_t* __restrict__ expert_offsets,
+                                                          int N, int k, int chunks_per_row,
+                                                          int rows_cap, uint4* __restrict__ x_perm) {
+    const int n_rows = expert_offsets[N];
+    for (int pos = blockIdx.x; pos < n_rows && pos < rows_cap; pos += gridDim.x) {
+        const int tok = perm[pos] / k;
+        for (int c = threadIdx.x; c < chunks_per_row; c += blockDim.x)
+            x_perm[(size_t)pos * chunks_per_row + c] = x[(size_t)tok * chunks_per_row + c];
+    }
+}
+
+// ---------------------------------------------------------------- host
+cudaError_t launch_tc_ffn(const TcLaunch& a, cudaStream_t st) {
+    const int chunks = a.d / 8;
+    const int g_rows = a.rows_cap < 4096 ? (a.rows_cap > 0 ? a.rows_cap : 1) : 4096;
+    gather_rows_kernel<<<g_rows, 256, 0, st>>>(static_cast<const uint4*>(a.x), a.perm,
+                                               a.expert_offsets, a.N, a.k, chunks, a.rows_cap,
+                                               static_cast<uint4*>(a.x_perm));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    TcParams p1;
+    std::memset(&p1, 0, sizeof(p1));
+    if (encode_bf16_2d(&p1.map_a_shared, a.x, a.d, a.T, (uint64_t)a.d * 2, kTcBK, kTcBM) != MOE_OK ||
+        encode_bf16_2d(&p1.map_a_routed, a.x_perm, a.d, a.rows_cap, (uint64_t)a.d * 2, kTcBK, kTcBM) != MOE_OK)
+        return cudaErrorInvalidValue;
+    p1.table = a.table; p1.plan = a.plan;
+    p1.out_shared = a.h_shared; p1.out_routed = a.h_routed;
+    p1.ld_out_shared = (long long)a.n_shared * a.I_shared; p1.ld_out_routed = a.I;
+    p1.d = a.d; p1.N = a.N; p1.I = a.I; p1.I_shared = a.I_shared; p1.n_shared = a.n_shared; p1.err = a.err;
+
+    TcParams p2 = p1;
+    const uint64_t hs_cols = (uint64_t)a.n_shared * a.I_shared;
+    if (a.n_shared > 0 &&
+        encode_bf16_2d(&p2.map_a_shared, a.h_shared, hs_cols, a.T, hs_cols * 2, kTcBK, kTcBM) != MOE_OK)
+        return cudaErrorInvalidValue;
+    if (encode_bf16_2d(&p2.map_a_routed, a.h_routed, a.I, a.rows_cap, (uint64_t)a.I * 2, kTcBK, kTcBM) != MOE_OK)
+        return cudaErrorInvalidValue;
+    p2.out_shared = a.y_shared; p2.out_routed = a.y_perm;
+    p2.ld_out_shared = a.d; p2.ld_out_routed = a.d;
+
+    e = allow_max_smem(ffn_tc_kernel<1>);
+    if (e != cudaSuccess) return e;
+    e = allow_max_smem(ffn_tc_kernel<2>);
+    if (e != cudaSuccess) return e;
+    ffn_tc_kernel<1><<<a.grid, kTcThreads, kTcSmemBytes, st>>>(p1);
+    e = note_launch(reinterpret_cast<const void*>(ffn_tc_kernel<1>), kTcThreads, kTcSmemBytes,
+                    cudaGetLastError());
+    if (e != cudaSuccess) return e;
+    ffn_tc_kernel<2><<<a.grid, kTcThreads, kTcSmemBytes, st>>>(p2);
+    return note_launch(reinterpret_cast<const void*>(ffn_tc_kernel<2>), kTcThreads, kTcSmemBytes,
+                       cudaGetLastError());
+}
+
+}  // namespace moe

@@ -49,8 +49,9 @@ struct PermuteArgs {
 };
 struct PlanArgs {
     const int32_t* expert_offsets;
-    int T, N, n_shared, I, I_shared, rg, G, max_segs, max_partial_rows;
+    int T, N, n_shared, I, I_shared, rg, G, max_segs, max_partial_rows, d;
     PlanHeader* hdr; Seg* segs; int32_t* seg_first; DevError* err;
+    TcPlan* tc_plan;  // also built when non-null
 };
 // permutation + FFN plan in one launch (the last block builds the plan)
 cudaError_t launch_permute(const PermuteArgs& a, const PlanArgs& plan, int* ticket, cudaStream_t st);
@@ -77,6 +78,14 @@ struct GemvReduceArgs {
     float *y_perm, *y_shared;
 };
 cudaError_t launch_gemv_reduce(const GemvReduceArgs& a, cudaStream_t st);
+
+struct TcLaunch {
+    const void* x; const int32_t* perm; const int32_t* expert_offsets; const ExpertEntry* table;
+    const TcPlan* plan; void* x_perm; void* h_routed; void* h_shared; float* y_perm; float* y_shared;
+    int T, d, N, k, I, I_shared, n_shared, rows_cap, grid; DevError* err;
+};
+// tensor-core expert FFN: gather, phase 1 (gate/up + SwiGLU), phase 2 (down)
+cudaError_t launch_tc_ffn(const TcLaunch& a, cudaStream_t st);
 
 struct LoreArgs {
     const void* x; const int32_t *final_idx, *final_kind; const float* final_gate;

@@ -329,7 +329,8 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* final_idx, const int
     pa.I = dims->I; pa.I_shared = dims->I_shared; pa.rg = gemv_rows(*dims);
     pa.G = gemv_grid(dims); pa.max_segs = L.max_segs; pa.max_partial_rows = L.max_partial_rows;
     pa.hdr = ws_at<PlanHeader>(ws, L.plan_hdr); pa.segs = ws_at<Seg>(ws, L.segs);
-    pa.seg_first = ws_at<int32_t>(ws, L.seg_first); pa.err = err;
+    pa.seg_first = ws_at<int32_t>(ws, L.seg_first); pa.err = err; pa.d = dims->d;
+    pa.tc_plan = use_tc(*dims) ? ws_at<TcPlan>(ws, L.tc_plan) : nullptr;
     MOE_CUDA(launch_permute(a, pa, ws_at<int>(ws, L.ticket), S(stream)));
     count();
     return MOE_OK;
@@ -347,6 +348,19 @@ moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table
     if (dims->n_shared > 0 && !y_shared) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || reinterpret_cast<uintptr_t>(table) % 64) return MOE_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(*dims);
+    if (use_tc(*dims)) {
+        TcLaunch t;
+        t.x = x; t.perm = perm; t.expert_offsets = expert_offsets;
+        t.table = static_cast<const ExpertEntry*>(table); t.plan = ws_at<TcPlan>(ws, L.tc_plan);
+        t.x_perm = ws_at<void>(ws, L.x_perm); t.h_routed = ws_at<void>(ws, L.h_routed);
+        t.h_shared = ws_at<void>(ws, L.h_shared); t.y_perm = y_perm; t.y_shared = y_shared;
+        t.T = dims->T; t.d = dims->d; t.N = dims->N; t.k = dims->k; t.I = dims->I;
+        t.I_shared = dims->I_shared; t.n_shared = dims->n_shared; t.rows_cap = dims->T * dims->k;
+        t.grid = sm_count(); t.err = ws_at<DevError>(ws, L.err);
+        MOE_CUDA(launch_tc_ffn(t, S(stream)));
+        count(3);
+        return MOE_OK;
+    }
     GemvParams p;
     p.x = x; p.d = dims->d; p.N = dims->N; p.topk = dims->k; p.NS = gemv_stages(dims->d, bf16(dims));
     p.perm = perm; p.table = static_cast<const ExpertEntry*>(table);

@@ -9,6 +9,7 @@
 namespace moe {
 
 __device__ void build_plan(const PlanArgs& a, const int* off);
+__device__ void build_tc_plan(const PlanArgs& a, const int* off);
 
 // One block per expert e.  Pass 1 counts the slots routed to experts below e
 // (the segment offset) and to e; pass 2 walks the slots in order and
@@ -91,7 +92,9 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
         for (int i = tid; i <= N; i += blockDim.x) s_offsets[i] = __ldcg(&expert_offsets[i]);
         __syncthreads();
         if (tid == 0) {
-            build_plan(plan, s_offsets);
+            // only the plan of the path moe_expert_ffn will take
+            if (plan.tc_plan) build_tc_plan(plan, s_offsets);
+            else build_plan(plan, s_offsets);
             *ticket = 0;
         }
     }
@@ -149,6 +152,25 @@ __device__ void build_plan(const PlanArgs& a, const int* off) {
     h.n_seg = n; h.total_ch = ch; h.P = P; h.n_partial_rows = pbase;
     h.n_routed_rows = off[N];
     *a.hdr = h;
+}
+
+// Tensor-core plan (see TcPlan): shared-expert group first, then every
+// routed expert with rows.
+__device__ void build_tc_plan(const PlanArgs& a, const int* off) {
+    TcPlan& P = *a.tc_plan;
+    int n = 0, t1 = 0, t2 = 0;
+    const int n2 = a.d / 256;
+    auto add = [&](int shared, int expert, int row0, int rows, int n1) {
+        TcSeg& s = P.seg[n++];
+        s.shared = shared; s.expert = expert; s.row0 = row0; s.rows = rows;
+        s.m_tiles = (rows + 127) / 128; s.n1 = n1; s.tile1 = t1; s.tile2 = t2;
+        t1 += s.m_tiles * n1;
+        t2 += s.m_tiles * n2;
+    };
+    if (a.n_shared > 0) add(1, a.N, 0, a.T, a.n_shared * a.I_shared / 128);
+    for (int e = 0; e < a.N; ++e)
+        if (off[e + 1] > off[e]) add(0, e, off[e], off[e + 1] - off[e], a.I / 128);
+    P.n_seg = n; P.n_tiles1 = t1; P.n_tiles2 = t2;
 }
 
 __global__ void plan_gemv_kernel(PlanArgs a) {

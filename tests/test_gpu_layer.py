@@ -53,7 +53,9 @@ def _run(name, T, batch=0, **kw):
 @pytest.mark.parametrize("name,T", [("tiny", 16), ("tiny", 1), ("tiny", 5), ("tiny", 64),
                                     ("dsv2lite", 1), ("dsv2lite", 8), ("dsv2lite", 3),
                                     ("granite", 1), ("granite", 37), ("granite", 1024),
-                                    ("mixtral", 1), ("mixtral", 8), ("mixtral", 32)])
+                                    ("granite", 65), ("granite", 200), ("dsv2lite", 96),
+                                    ("mixtral", 1), ("mixtral", 8), ("mixtral", 32),
+                                    ("mixtral", 100)])
 def test_layer_matches_oracle(name, T):
     cfg, W, layer, x, bufs, st, det = _run(name, T)
     assert st == moe.MOE_OK, (moe.status_string(st), det)
