@@ -366,6 +366,29 @@ def main():
     e2e_s = max_over_ranks(world, time.perf_counter() - t0)
     e2e_value = world * T * n_e2e / e2e_s
 
+    # ---- expert staging over the host link (EXACT-mode fetches): copy every
+    # expert of one layer copy from pinned host memory with moe_stage_experts
+    n_stage = min(cfg.N, 8)
+    host_w = [[layers[0].w_gate[e].cpu().pin_memory() for e in range(cfg.N)],
+              [layers[0].w_up[e].cpu().pin_memory() for e in range(cfg.N)],
+              [layers[0].w_down[e].cpu().pin_memory() for e in range(cfg.N)]]
+    side = torch.cuda.Stream(device=dev)
+    done = torch.cuda.Event()
+    mask = (1 << n_stage) - 1
+    D1 = layers[0].dims.with_T(T)
+    moe.moe_stage_experts(D1, mask, *host_w, list(layers[0].w_gate), list(layers[0].w_up),
+                          list(layers[0].w_down), side, done)
+    side.synchronize()
+    t0 = time.perf_counter()
+    reps = 3
+    for _ in range(reps):
+        nbytes = moe.moe_stage_experts(D1, mask, *host_w, list(layers[0].w_gate), list(layers[0].w_up),
+                                       list(layers[0].w_down), side, done)
+    side.synchronize()
+    stage_s = time.perf_counter() - t0
+    staging = {"gbps": reps * nbytes / stage_s / 1e9, "bytes_per_call": nbytes,
+               "experts_per_call": n_stage, "note": "pinned host -> HBM, cudaMemcpyAsync on a side stream"}
+
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -383,6 +406,7 @@ def main():
                 "d2h_bytes_per_step": bufs[0].out.numel() * 4, "steps": n_e2e,
                 "note": "moe_layer_forward per step with pinned-host copies and a stream sync, no graph"},
         "gpu_launches": int(launches_per_step * args.steps),
+        "staging": staging,
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:

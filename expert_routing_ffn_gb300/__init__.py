@@ -251,6 +251,8 @@ def moe_stage_experts(dims, host_fetch_mask: int, host_w_gate, host_w_up, host_w
     a = [arr(host_w_gate, "host_w_gate", True), arr(host_w_up, "host_w_up", True),
          arr(host_w_down, "host_w_down", True), arr(dev_w_gate, "dev_w_gate", False),
          arr(dev_w_up, "dev_w_up", False), arr(dev_w_down, "dev_w_down", False)]
+    if done_event.cuda_event == 0:  # torch creates the CUDA event on its first record
+        done_event.record(stage_stream)
     n = C.c_size_t()
     _check(lib().moe_stage_experts(C.byref(dims), C.c_uint64(host_fetch_mask & (2**64 - 1)),
                                    *[C.cast(x, C.c_void_p) for x in a], _stream(stage_stream),

@@ -80,7 +80,18 @@ __global__ void __launch_bounds__(256) lore_b_kernel(const int32_t* __restrict__
     for (int i = 0; i < n; ++i) {
         const int e = final_idx[(size_t)t * k + s_e[i]];
         const W* brow = B + ((size_t)e * d + j) * r;
-        for (int q = 0; q < r; ++q) acc = fmaf(to_f32(brow[q]), s_z[i * r + q], acc);
+        const float* zz = s_z + i * r;
+        if ((r * (int)sizeof(W)) % 16 == 0) {
+            // 16-byte loads of the rank row B_e[j, :]
+            for (int q = 0; q < r; q += Vec<W>::n) {
+                float bv[Vec<W>::n];
+                unpack16(*reinterpret_cast<const uint4*>(brow + q), bv, (W*)nullptr);
+#pragma unroll
+                for (int u = 0; u < Vec<W>::n; ++u) acc = fmaf(bv[u], zz[q + u], acc);
+            }
+        } else {
+            for (int q = 0; q < r; ++q) acc = fmaf(to_f32(brow[q]), zz[q], acc);
+        }
     }
     y_lore[(size_t)t * d + j] = acc;
 }

@@ -91,6 +91,102 @@ __global__ void __launch_bounds__(256) route_logits_kernel(
     }
 }
 
+// Large batches: a register-tiled version of the same logits.  Block tile =
+// 64 tokens x 64 output rows, K in chunks of 32 through shared memory (fp32,
+// x stored K-major so a thread reads 4 tokens with one 16-byte load).  Each
+// thread owns 4 tokens x 4 rows.  Every chunk's 32 products are summed into a
+// fresh partial that is then added to the running total (blocked summation),
+// keeping the rounding error of a logit near 1e-7.
+template <typename W>
+__global__ void __launch_bounds__(256) route_logits_tiled_kernel(
+    const W* __restrict__ x, const W* __restrict__ x_pre, const W* __restrict__ w_router,
+    const float* __restrict__ bias, const W* __restrict__ w_prefetch, const float* __restrict__ w_ord,
+    int T, int d, int N, int n_out, float* __restrict__ logits_r, float* __restrict__ logits_p,
+    float* __restrict__ score) {
+    constexpr int TT = 64, TO = 64, KC = 32;
+    __shared__ __align__(16) float xs[KC][TT];    // router input x
+    __shared__ __align__(16) float xps[KC][TT];   // prefetch input x_pre
+    __shared__ __align__(16) float ws[KC][TO];
+    const int t0 = blockIdx.x * TT, o0 = blockIdx.y * TO;
+    const int tid = threadIdx.x;
+    const int tq = tid & 15, oq = tid >> 4;       // 16 token quads x 16 row quads
+    const bool sep = x_pre != x;
+    float acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+    for (int k0 = 0; k0 < d; k0 += KC) {
+        // stage 64 x 32 values of x (and x_pre) and of the 64 weight rows,
+        // 16 bytes per load (8 bf16 / 4 fp32), transposed into K-major smem
+        constexpr int V = Vec<W>::n;
+        for (int i = tid; i < TT * KC / V; i += 256) {
+            const int tt = i / (KC / V), kv = (i % (KC / V)) * V, tok = t0 + tt;
+            float v[V], vp[V];
+#pragma unroll
+            for (int u = 0; u < V; ++u) { v[u] = 0.f; vp[u] = 0.f; }
+            if (tok < T) {
+                unpack16(*reinterpret_cast<const uint4*>(x + (size_t)tok * d + k0 + kv), v, (W*)nullptr);
+                if (sep) unpack16(*reinterpret_cast<const uint4*>(x_pre + (size_t)tok * d + k0 + kv), vp, (W*)nullptr);
+            }
+#pragma unroll
+            for (int u = 0; u < V; ++u) {
+                xs[kv + u][tt] = v[u];
+                xps[kv + u][tt] = sep ? vp[u] : v[u];
+            }
+        }
+        for (int i = tid; i < TO * KC / V; i += 256) {
+            const int oo = i / (KC / V), kv = (i % (KC / V)) * V, o = o0 + oo;
+            float v[V];
+#pragma unroll
+            for (int u = 0; u < V; ++u) v[u] = 0.f;
+            if (o < N) unpack16(*reinterpret_cast<const uint4*>(w_router + (size_t)o * d + k0 + kv), v, (W*)nullptr);
+            else if (o < 2 * N) unpack16(*reinterpret_cast<const uint4*>(w_prefetch + (size_t)(o - N) * d + k0 + kv), v, (W*)nullptr);
+            else if (o < n_out)
+#pragma unroll
+                for (int u = 0; u < V; ++u) v[u] = w_ord[k0 + kv + u];
+#pragma unroll
+            for (int u = 0; u < V; ++u) ws[kv + u][oo] = v[u];
+        }
+        __syncthreads();
+        float part[4][4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) part[a][b] = 0.f;
+        // rows o < N use x, the prefetch rows and the scorer use x_pre
+        const bool pre = o0 + oq * 4 >= N;
+#pragma unroll 8
+        for (int kk = 0; kk < KC; ++kk) {
+            const float4 xv = *reinterpret_cast<const float4*>(pre ? &xps[kk][tq * 4] : &xs[kk][tq * 4]);
+            const float4 wv = *reinterpret_cast<const float4*>(&ws[kk][oq * 4]);
+            const float xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < 4; b += 2)
+                    fma2(part[a][b], part[a][b + 1], xa[a], xa[a], wa[b], wa[b + 1]);
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) acc[a][b] += part[a][b];
+        __syncthreads();
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const int tok = t0 + tq * 4 + a;
+        if (tok >= T) continue;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int o = o0 + oq * 4 + b;
+            if (o < N) logits_r[(size_t)tok * N + o] = acc[a][b] + (bias ? bias[o] : 0.f);
+            else if (o < 2 * N) logits_p[(size_t)tok * N + (o - N)] = acc[a][b];
+            else if (o < n_out) score[tok] = acc[a][b];
+        }
+    }
+}
+
 // (value, index) argmax across the warp: larger value wins, equal values go
 // to the lower index.  Lanes with no candidate pass index = INT_MAX.
 __device__ __forceinline__ void warp_argmax(float& v, int& i) {
@@ -348,6 +444,16 @@ __global__ void __launch_bounds__(256) select_resident_kernel(
 template <typename W>
 static cudaError_t launch_logits_t(const LogitsArgs& a, cudaStream_t st) {
     constexpr int TT = 8;
+    // (a row quad must not straddle the router / prefetch-router boundary when
+    // the two routers read different inputs)
+    if (a.T >= 2048 && (a.x_pre == nullptr || a.x_pre == a.x || a.N % 4 == 0)) {
+        const int n_out = a.has_prefetch ? 2 * a.N + 1 : a.N;
+        dim3 grid((a.T + 63) / 64, (n_out + 63) / 64);
+        route_logits_tiled_kernel<W><<<grid, 256, 0, st>>>(
+            (const W*)a.x, (const W*)(a.x_pre ? a.x_pre : a.x), (const W*)a.w_router, a.bias,
+            (const W*)a.w_prefetch, a.w_ord, a.T, a.d, a.N, n_out, a.logits_r, a.logits_p, a.score);
+        return cudaGetLastError();
+    }
     const int n_out = a.has_prefetch ? 2 * a.N + 1 : a.N;
     const int t_tiles = (a.T + TT - 1) / TT;
     const int rows_per_block = 8;

@@ -209,3 +209,52 @@ def test_all_tokens_on_the_same_experts():
     R = oracle.layer_forward(cfg, Wb, x, use_prefetch=False)
     check_selection(cfg, R, bufs)
     check_output(cfg, R, bufs.out)
+
+
+def test_exact_policy_with_staging_matches_plain_moe():
+    """Correctness-preserving mode (APEX §4.3): experts outside the resident set
+    are fetched from pinned host memory on a side stream (their device slots
+    are first overwritten with NaN, so an unstaged or late copy would show)
+    and the layer output equals the plain MoE layer."""
+    cfg, W = _host("dsv2lite")
+    T = 8
+    layer = _device("dsv2lite", T)
+    D = layer.dims.with_T(T)
+    x = make_tokens(cfg, T=T, batch=3)
+    xd = x_device(x, layer.dt)
+    b = LayerBuffers(layer, T)
+    moe.moe_route(D, xd, layer.w_router, layer.router_bias, None, layer.w_prefetch, layer.w_ord,
+                  layer.theta, cfg.tau, cfg.n_resident, b.topk_idx, b.topk_gate, b.router_prob,
+                  b.delta_hat, b.prefetch_mask, b.delta_star, b.batch_resident, layer.ws)
+    moe.moe_select_resident(D, b.router_prob, b.topk_idx, None, b.batch_resident, moe.MOE_MISS_EXACT,
+                            0.0, b.delta_hat, b.delta_star, b.final_idx, b.final_gate, b.final_kind,
+                            b.fetch_mask, b.counters, layer.ws)
+    fetch = as_u64(int(b.fetch_mask.item()))
+    assert fetch != 0, "this batch fetches at least one expert"
+    ids = [e for e in range(cfg.N) if (fetch >> e) & 1]
+    host = [[t.cpu().pin_memory() for t in mats] for mats in (layer.w_gate, layer.w_up, layer.w_down)]
+    saved = [(layer.w_gate[e].clone(), layer.w_up[e].clone(), layer.w_down[e].clone()) for e in ids]
+    try:
+        for e in ids:
+            for m in (layer.w_gate, layer.w_up, layer.w_down):
+                m[e].fill_(float("nan"))
+        side = torch.cuda.Stream()
+        done = torch.cuda.Event()
+        nbytes = moe.moe_stage_experts(D, fetch, *host, list(layer.w_gate), list(layer.w_up),
+                                       list(layer.w_down), side, done)
+        assert nbytes == len(ids) * 3 * cfg.I * cfg.d * 2
+        torch.cuda.current_stream().wait_event(done)
+        moe.moe_permute(D, b.final_idx, b.final_kind, b.expert_offsets, b.perm, b.inv_perm, layer.ws)
+        moe.moe_expert_ffn(D, xd, layer.table, b.expert_offsets, b.perm, 1.0, b.y_perm, b.y_shared,
+                           layer.ws)
+        moe.moe_combine(D, b.y_perm, b.inv_perm, b.final_gate, b.final_kind, b.y_shared, None, b.out)
+        st, det = moe.moe_check(layer.ws)
+        assert st == moe.MOE_OK, (moe.status_string(st), det)
+        kinds = to_np(b.final_kind)
+        assert (kinds == moe.MOE_KIND_FETCH).sum() == to_np(b.counters)[3] > 0
+        R = oracle.layer_forward(cfg, W, x, policy=moe.MOE_MISS_EXACT)
+        check_selection(cfg, R, b)
+        check_output(cfg, R, b.out)
+    finally:
+        for e, (g, u, dn) in zip(ids, saved):
+            layer.w_gate[e].copy_(g); layer.w_up[e].copy_(u); layer.w_down[e].copy_(dn)
