@@ -36,7 +36,7 @@ import numpy as np  # noqa: E402
 
 from workloads import CONFIGS, make_tokens, make_weights  # noqa: E402
 
-# name -> (layer config, tokens per step, phase)
+# name -> (layer config, tokens per step, phase[, FloE keep fraction])
 WORKLOADS = {
     "dsv2lite-decode-T8": ("dsv2lite", 8, "decode"),
     "dsv2lite-decode-T1": ("dsv2lite", 1, "decode"),
@@ -45,6 +45,8 @@ WORKLOADS = {
     "mixtral-decode-T1": ("mixtral", 1, "decode"),
     "mixtral-decode-T8": ("mixtral", 8, "decode"),
     "mixtral-decode-T32": ("mixtral", 32, "decode"),
+    "mixtral-floe10-decode-T1": ("mixtral", 1, "decode", 0.1),
+    "mixtral-floe10-decode-T8": ("mixtral", 8, "decode", 0.1),
     "qwen2-prefill-T4096": ("qwen2", 4096, "prefill"),
 }
 DEFAULT_WORKLOAD = "dsv2lite-decode-T8"
@@ -232,8 +234,10 @@ def run_reference(args, wl_name, cfg, T, world, rank):
 def main():
     args = parse()
     wl_name = args.workload
-    cfg_name, T, phase = WORKLOADS[wl_name]
+    cfg_name, T, phase = WORKLOADS[wl_name][:3]
     cfg = CONFIGS[cfg_name]
+    if len(WORKLOADS[wl_name]) > 3:
+        cfg = cfg.with_(keep_frac=WORKLOADS[wl_name][3])
     if args.impl == "reference":
         world = int(os.environ.get("WORLD_SIZE", "1"))
         rank = int(os.environ.get("RANK", "0"))
@@ -315,7 +319,23 @@ def main():
     for c, L in enumerate(layers):
         off = bufs[c].expert_offsets.cpu().numpy()
         u = int((np.diff(off) > 0).sum())
-        fb.append(u * expert_bytes + shared_bytes)
+        if cfg.keep_frac < 1.0:
+            # FloE: dense up rows + gate/down rows of the union of kept channels
+            moe.moe_expert_ffn(L.dims.with_T(T), xs[c], L.table, bufs[c].expert_offsets, bufs[c].perm,
+                               cfg.keep_frac, bufs[c].y_perm, bufs[c].y_shared, L.ws, stream)
+            torch.cuda.synchronize()
+            ptr, words = moe.moe_floe_kept_mask(L.dims.with_T(T), L.ws)
+            o = ptr - L.ws.data_ptr()
+            kept = L.ws[o:o + int(off[-1]) * words * 4].view(torch.int32).cpu().numpy().view(np.uint32)
+            kept = kept.reshape(-1, words)
+            union_rows = 0
+            for e in range(cfg.N):
+                if off[e + 1] > off[e]:
+                    union_rows += int(np.unpackbits(np.bitwise_or.reduce(kept[off[e]:off[e + 1]], axis=0)
+                                                    .view(np.uint8)).sum())
+            fb.append(u * cfg.I * cfg.d * esize + union_rows * 2 * cfg.d * esize + shared_bytes)
+        else:
+            fb.append(u * expert_bytes + shared_bytes)
         ff.append(6.0 * cfg.d * (int(off[-1]) * cfg.I + T * cfg.n_shared * cfg.I_shared))
     n_k = max(10 if phase == "prefill" else 50, min(2000, args.steps // 2))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_k)]
@@ -335,7 +355,9 @@ def main():
     k_flops = [ff[(i + n_copies) % n_copies] for i in range(n_k)]
     if phase == "decode":
         achieved = sum(k_bytes) / (sum(k_ms) / 1e3) / 1e9
-        roof = {"kernel": "moe_expert_ffn (ffn_gemv_kernel + gemv_reduce_kernel)", "bound": "hbm",
+        kname = ("moe_expert_ffn (floe up/select/union/plan + sparse ffn_gemv_kernel + gemv_reduce_kernel)"
+                 if cfg.keep_frac < 1.0 else "moe_expert_ffn (ffn_gemv_kernel + gemv_reduce_kernel)")
+        roof = {"kernel": kname, "bound": "hbm",
                 "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
                 "peak_source": peak_src, "algorithmic_bytes_per_launch": float(statistics.mean(fb)),
                 "avg_launch_ms": statistics.mean(k_ms),
@@ -397,6 +419,7 @@ def main():
         "data": "synthetic (seeded N(0,0.02^2) weights, N(0,1) tokens; shapes of the named model)",
         "config": {"workload": wl_name, "tokens_per_step": T, "d": cfg.d, "experts": cfg.N,
                    "top_k": cfg.k, "intermediate": cfg.I, "shared_experts": cfg.n_shared,
+                   "floe_keep_frac": cfg.keep_frac,
                    "miss_policy": ["exact", "substitute", "lore", "hybrid"][cfg.policy],
                    "resident": cfg.n_resident, "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: {n_copies} rotating layer copies of "

@@ -90,6 +90,7 @@ _PROTOS = {
                           C.c_int),
     "moe_permute": ([_DIMS, _P, _P, _P, _P, _P, _P, _SZ, _P], C.c_int),
     "moe_expert_ffn": ([_DIMS, _P, _P, _P, _P, _F, _P, _P, _P, _SZ, _P], C.c_int),
+    "moe_floe_kept_mask": ([_DIMS, _P, _SZ, C.POINTER(C.c_void_p), C.POINTER(C.c_int32)], C.c_int),
     "moe_expert_ffn_noalloc": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P], C.c_int),
     "moe_lore": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P], C.c_int),
     "moe_combine": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P], C.c_int),
@@ -280,6 +281,16 @@ def moe_expert_ffn(dims, x, table, expert_offsets, perm, keep_frac, y_perm, y_sh
         float(keep_frac), _ptr(y_perm, torch.float32, T * k * d, "y_perm"),
         _ptr(y_shared, torch.float32, T * d, "y_shared", True), _ptr(ws, torch.uint8, name="ws"),
         ws.numel(), _stream(stream)), "moe_expert_ffn")
+
+
+def moe_floe_kept_mask(dims, ws):
+    """Device pointer and words per row of the FloE kept-channel bitsets left
+    in `ws` by the last moe_expert_ffn call with keep_frac < 1."""
+    ptr = C.c_void_p()
+    words = C.c_int32()
+    _check(lib().moe_floe_kept_mask(C.byref(dims), _ptr(ws, torch.uint8, name="ws"), ws.numel(),
+                                    C.byref(ptr), C.byref(words)), "moe_floe_kept_mask")
+    return ptr.value, words.value
 
 
 def moe_expert_ffn_noalloc(dims, x, table, expert_offsets, perm, y_perm, y_shared,

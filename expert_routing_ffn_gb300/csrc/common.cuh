@@ -48,7 +48,10 @@ struct Seg {
     int c0;         // first CTA that covers this segment
     int npieces;
     int pbase;      // first partial row
+    int list_off;   // FloE: offset of this expert's channel list (-1: dense, channels 0..I-1;
+                    // kUpOnly: dense up projection only, u written to the workspace)
 };
+constexpr int kUpOnly = -2;
 
 struct PlanHeader {
     int n_seg;
@@ -87,7 +90,7 @@ __host__ __device__ inline bool use_tc(const moe_dims& D) { return tc_usable(D) 
 // ---------------------------------------------------------------- workspace
 struct WsLayout {
     size_t err, ticket, logits_r, logits_p, score, qp, plan_hdr, segs, seg_first, lore_z, tc_plan,
-        x_perm, h_routed, h_shared, partial, total;
+        x_perm, h_routed, h_shared, floe_u, floe_kept, floe_list, floe_count, partial, total;
     int max_segs, max_partial_rows;
 };
 
@@ -132,6 +135,11 @@ __host__ __device__ inline WsLayout ws_layout(const moe_dims& D) {
     L.x_perm = take(tc ? T * D.k * (size_t)D.d * 2 : 0);
     L.h_routed = take(tc ? T * D.k * (size_t)D.I * 2 : 0);
     L.h_shared = take(tc ? T * (size_t)D.n_shared * D.I_shared * 2 : 0);
+    // FloE (decode batches only)
+    L.floe_u = take(rows_routed * (size_t)D.I * 4);
+    L.floe_kept = take(rows_routed * (size_t)((D.I + 31) / 32) * 4);
+    L.floe_list = take(N * (size_t)D.I * 4);
+    L.floe_count = take(N * 4);
     L.partial = take((size_t)L.max_partial_rows * (size_t)D.d * 4);
     L.total = o;
     return L;

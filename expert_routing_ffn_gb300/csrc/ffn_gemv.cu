@@ -26,13 +26,14 @@
 
 namespace moe {
 
-constexpr int kNSMax = 8;
+constexpr int kNSMax = 24;  // up-only launches use 3 x NS stages
 
 // Issues the bulk copies of one CTA's stages, in the order they are read.
 // Run by thread 0 only.
 struct Producer {
     const Seg* segs;
     const ExpertEntry* table;
+    const int32_t* list;  // FloE channel lists
     unsigned char* stage_mem;
     uint64_t* full;
     size_t row_bytes, mat_bytes, stage_bytes;
@@ -51,11 +52,30 @@ struct Producer {
         const int b = issued % NS;
         unsigned char* buf = stage_mem + (size_t)b * stage_bytes;
         const uint32_t bytes = (uint32_t)(nch * row_bytes);
-        mbar_arrive_expect_tx(&full[b], 3 * bytes);
+        if (S.list_off == kUpOnly) {
+            // FloE first pass: the up rows only (a stage is one third of a
+            // dense stage, so three times as many are in flight)
+            mbar_arrive_expect_tx(&full[b], bytes);
+            bulk_g2s(buf, static_cast<const char*>(E.w[1]) + (size_t)local * row_bytes, bytes, &full[b],
+                     policy);
+        } else if (S.list_off >= 0) {
+            // FloE: gate and down rows of the listed channels only
+            mbar_arrive_expect_tx(&full[b], 2 * bytes);
+            for (int c = 0; c < nch; ++c) {
+                const size_t row = (size_t)list[S.list_off + local + c];
+                bulk_g2s(buf + c * row_bytes, static_cast<const char*>(E.w[0]) + row * row_bytes,
+                         (uint32_t)row_bytes, &full[b], policy);
+                bulk_g2s(buf + 2 * mat_bytes + c * row_bytes,
+                         static_cast<const char*>(E.w[2]) + row * row_bytes, (uint32_t)row_bytes, &full[b],
+                         policy);
+            }
+        } else {
+            mbar_arrive_expect_tx(&full[b], 3 * bytes);
 #pragma unroll
-        for (int m = 0; m < 3; ++m)
-            bulk_g2s(buf + m * mat_bytes, static_cast<const char*>(E.w[m]) + (size_t)local * row_bytes,
-                     bytes, &full[b], policy);
+            for (int m = 0; m < 3; ++m)
+                bulk_g2s(buf + m * mat_bytes, static_cast<const char*>(E.w[m]) + (size_t)local * row_bytes,
+                         bytes, &full[b], policy);
+        }
         ch += nch;
         if (ch >= S.ch_start + S.I) ++seg;
         ++issued;
@@ -98,8 +118,11 @@ __device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, in
     const int d = p.d;
     const size_t row_bytes = (size_t)d * sizeof(W);
     const size_t mat_bytes = (size_t)CH * row_bytes;
-    const size_t stage_bytes = 3 * mat_bytes;
     const W* x = static_cast<const W*>(p.x);
+    const bool sparse = S.list_off >= 0;  // FloE segment: gate/down of listed channels
+    const bool up_only = S.list_off == kUpOnly;  // FloE first pass: u = x . W_up only
+    const int NS = up_only ? 3 * p.NS : p.NS;
+    const size_t stage_bytes = up_only ? mat_bytes : 3 * mat_bytes;
 
     float xr[ROWS][V];
 #pragma unroll
@@ -116,8 +139,8 @@ __device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, in
 
     for (int i = llo; i < lhi; i += CH) {
         const int nch = min(CH, lhi - i);
-        const int b = stage_k % p.NS;
-        const uint32_t par = (uint32_t)((stage_k / p.NS) & 1);
+        const int b = stage_k % NS;
+        const uint32_t par = (uint32_t)((stage_k / NS) & 1);
         if (!mbar_wait(&sh.full[b], par)) {
             set_error(p.err, MOE_ERR_TIMEOUT, cta);
             *sh.abort_flag = 1;
@@ -131,14 +154,18 @@ __device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, in
 #pragma unroll
         for (int cc = 0; cc < CH; ++cc) {
             if (cc < nch) {
-                float wg[V], wu[V];
-                unpack16(reinterpret_cast<const uint4*>(buf + cc * row_bytes)[tid], wg, (W*)nullptr);
-                unpack16(reinterpret_cast<const uint4*>(buf + mat_bytes + cc * row_bytes)[tid], wu,
-                         (W*)nullptr);
+                if (!up_only) {
+                    float wg[V];
+                    unpack16(reinterpret_cast<const uint4*>(buf + cc * row_bytes)[tid], wg, (W*)nullptr);
 #pragma unroll
-                for (int r = 0; r < ROWS; ++r) {
-                    v[cc * 2 * ROWS + r] = dot_v<V>(wg, xr[r]);
-                    v[cc * 2 * ROWS + ROWS + r] = dot_v<V>(wu, xr[r]);
+                    for (int r = 0; r < ROWS; ++r) v[cc * 2 * ROWS + r] = dot_v<V>(wg, xr[r]);
+                }
+                if (!sparse) {
+                    float wu[V];
+                    const unsigned char* ub = up_only ? buf : buf + mat_bytes;
+                    unpack16(reinterpret_cast<const uint4*>(ub + cc * row_bytes)[tid], wu, (W*)nullptr);
+#pragma unroll
+                    for (int r = 0; r < ROWS; ++r) v[cc * 2 * ROWS + ROWS + r] = dot_v<V>(wu, xr[r]);
                 }
             }
         }
@@ -163,12 +190,25 @@ __device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, in
                 g += red[w * 32 + cc * 2 * ROWS + r];
                 u += red[w * 32 + cc * 2 * ROWS + ROWS + r];
             }
-            hq = cc < nch ? silu(g) * u : 0.f;
+            if (cc < nch && up_only) {
+                // FloE first pass: store u and skip the down projection
+                p.floe_u[(size_t)(S.row0 + r) * p.I + i + cc] = u;
+                hq = 0.f;
+            } else if (cc < nch && sparse) {
+                // FloE: u from the dense up projection, h only on this row's kept channels
+                const int ch = p.floe_list[S.list_off + i + cc];
+                const size_t row = (size_t)(S.row0 + r);
+                u = p.floe_u[row * p.I + ch];
+                const bool keep = (p.floe_kept[row * p.words + (ch >> 5)] >> (ch & 31)) & 1u;
+                hq = keep ? silu(g) * u : 0.f;
+            } else {
+                hq = cc < nch ? silu(g) * u : 0.f;
+            }
         }
         // down projection: y[r, chunk] += h[c, r] * Wd[c, chunk]
 #pragma unroll
         for (int cc = 0; cc < CH; ++cc) {
-            if (cc < nch) {
+            if (cc < nch && !up_only) {
                 float wd[V];
                 unpack16(reinterpret_cast<const uint4*>(buf + 2 * mat_bytes + cc * row_bytes)[tid], wd,
                          (W*)nullptr);
@@ -184,6 +224,7 @@ __device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, in
         if (*sh.abort_flag) break;
     }
     // partial output rows of this CTA for this segment
+    if (up_only) return;
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) {
         float* dst = p.partial + ((size_t)(S.pbase + (cta - S.c0) * ROWS + r)) * d + (size_t)tid * V;
@@ -218,18 +259,22 @@ __device__ __forceinline__ void ffn_gemv_body(const GemvParams& p) {
     }
     const int seg0 = s_lo;
 
+    // an up-only launch (FloE first pass) splits every stage buffer in three
+    const int NSx = p.up_pass ? 3 * p.NS : p.NS;
     Producer prod;
     if (tid == 0) {
-        for (int b = 0; b < p.NS; ++b) mbar_init(&full[b], 1);
+        for (int b = 0; b < NSx; ++b) mbar_init(&full[b], 1);
         fence_mbar_init();
         s_abort = 0;
-        prod.segs = p.segs; prod.table = p.table; prod.stage_mem = stage_mem; prod.full = full;
+        prod.segs = p.segs; prod.table = p.table; prod.list = p.floe_list; prod.stage_mem = stage_mem;
+        prod.full = full;
         prod.row_bytes = row_bytes; prod.mat_bytes = CH * row_bytes;
-        prod.stage_bytes = 3 * CH * row_bytes; prod.NS = p.NS; prod.CH = CH; prod.seg = seg0;
+        prod.stage_bytes = (p.up_pass ? 1 : 3) * CH * row_bytes; prod.NS = NSx; prod.CH = CH;
+        prod.seg = seg0;
         prod.ch = lo; prod.hi = hi; prod.n_seg = hdr.n_seg; prod.issued = 0;
         prod.policy = l2_evict_first_policy();
         // fill every buffer but the one the first refill will use
-        for (int k = 0; k < p.NS && !prod.done(); ++k) prod.issue();
+        for (int k = 0; k < NSx && !prod.done(); ++k) prod.issue();
     }
     __syncthreads();
 
@@ -267,7 +312,7 @@ __device__ __forceinline__ void ffn_gemv_body(const GemvParams& p) {
     // the CTA exits and its shared memory is released
     if (tid == 0 && s_abort) {
         for (int k = stage_k; k < prod.issued; ++k)
-            (void)mbar_wait(&full[k % p.NS], (uint32_t)((k / p.NS) & 1));
+            (void)mbar_wait(&full[k % NSx], (uint32_t)((k / NSx) & 1));
     }
 }
 
@@ -374,10 +419,12 @@ int gemv_stages(int d, bool bf16) {
     const size_t stage = (size_t)3 * 2 * d * (bf16 ? 2 : 4);
     const size_t budget = gemv_ctas_per_sm(d, bf16) == 2 ? 100 * 1024 : 200 * 1024;
     int ns = (int)(budget / stage);
-    return ns < 2 ? 2 : (ns > kNSMax ? kNSMax : ns);
+    // at most kNSMax / 3: an up-only launch runs three stages per buffer
+    return ns < 2 ? 2 : (ns > kNSMax / 3 ? kNSMax / 3 : ns);
 }
 
-cudaError_t launch_gemv(const GemvParams& p, int G, bool bf16, cudaStream_t st) {
+cudaError_t launch_gemv(const GemvParams& p, int G, bool bf16, cudaStream_t st, bool floe) {
+    (void)floe;  // the sparse mode is chosen per segment (Seg::list_off)
     if (bf16) {
         if (p.d <= 2048)
             return launch_gemv_k(ffn_gemv_kernel_x2<__nv_bfloat16, 4, 2>, 256, 8, 2, 2, p, G, st);

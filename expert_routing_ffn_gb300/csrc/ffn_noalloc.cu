@@ -126,6 +126,8 @@ extern "C" moe_status moe_expert_ffn_noalloc(const moe_dims* dims, const void* x
     p.x = x; p.d = dims->d; p.N = dims->N; p.topk = dims->k; p.NS = moe::gemv_stages(dims->d, bf16);
     p.perm = perm; p.table = static_cast<const moe::ExpertEntry*>(table);
     p.hdr = pa.hdr; p.segs = pa.segs; p.partial = moe::ws_at<float>(base, L.partial); p.err = err;
+    p.floe_u = nullptr; p.floe_kept = nullptr; p.floe_list = nullptr; p.I = dims->I; p.words = 0;
+    p.up_pass = 0;
     if (moe::launch_gemv(p, G, bf16, s) != cudaSuccess) return MOE_ERR_CUDA;
 
     moe::GemvReduceArgs r;

@@ -61,6 +61,12 @@ cudaError_t launch_plan_gemv(const PlanArgs& a, cudaStream_t st);
 struct GemvParams {
     const void* x;
     int d, N, topk, NS;
+    // FloE sparse mode (routed segments with list_off >= 0)
+    float* floe_u;                // [rows, I] up projections (written by the up-only pass)
+    const uint32_t* floe_kept;    // [rows, words] kept-channel bitsets
+    const int32_t* floe_list;     // [N, I] union channel lists
+    int I, words;
+    int up_pass;                  // 1: every segment is up-only (FloE first pass)
     const int32_t* perm;
     const ExpertEntry* table;
     const PlanHeader* hdr;
@@ -70,7 +76,17 @@ struct GemvParams {
 };
 int gemv_stages(int d, bool bf16);
 int gemv_grid_for(int d, bool bf16, int sms);
-cudaError_t launch_gemv(const GemvParams& p, int G, bool bf16, cudaStream_t st);
+cudaError_t launch_gemv(const GemvParams& p, int G, bool bf16, cudaStream_t st, bool floe = false);
+
+struct FloeArgs {
+    const void* x; const int32_t* perm; const int32_t* expert_offsets; const ExpertEntry* table;
+    int d, I, N, topk, m, words, rows_cap;
+    float* u; uint32_t* kept; int32_t* list; int32_t* count;
+};
+// FloE: up-only plan + GEMV pass, selection, unions and the sparse GEMV plan
+// (5 launches)
+cudaError_t launch_floe_prepare(const FloeArgs& f, const PlanArgs& plan, const GemvParams& gp, int G,
+                                cudaStream_t st);
 
 struct GemvReduceArgs {
     const PlanHeader* hdr; const Seg* segs; const int32_t* seg_first; const int32_t* expert_offsets;

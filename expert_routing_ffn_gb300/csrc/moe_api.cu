@@ -342,7 +342,9 @@ moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table
     MOE_TRY(check_dims(dims));
     MOE_TRY(check_ws(dims, ws, ws_bytes));
     if (!(keep_frac > 0.f && keep_frac <= 1.f)) return MOE_ERR_INVALID_ARG;
-    if (keep_frac < 1.f) return MOE_ERR_UNSUPPORTED;
+    const bool floe = keep_frac < 1.f;
+    // FloE sparsity runs on the decode (GEMV) path for bf16 layers
+    if (floe && (use_tc(*dims) || !bf16(dims))) return MOE_ERR_UNSUPPORTED;
     if (dims->T == 0) return MOE_OK;
     if (!x || !table || !expert_offsets || !perm || !y_perm) return MOE_ERR_INVALID_ARG;
     if (dims->n_shared > 0 && !y_shared) return MOE_ERR_INVALID_ARG;
@@ -366,6 +368,28 @@ moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table
     p.perm = perm; p.table = static_cast<const ExpertEntry*>(table);
     p.hdr = ws_at<PlanHeader>(ws, L.plan_hdr); p.segs = ws_at<Seg>(ws, L.segs);
     p.partial = ws_at<float>(ws, L.partial); p.err = ws_at<DevError>(ws, L.err);
+    p.floe_u = ws_at<float>(ws, L.floe_u); p.floe_kept = ws_at<uint32_t>(ws, L.floe_kept);
+    p.floe_list = ws_at<int32_t>(ws, L.floe_list); p.I = dims->I; p.words = (dims->I + 31) / 32;
+    p.up_pass = 0;
+    if (floe) {
+        FloeArgs f;
+        f.x = x; f.perm = perm; f.expert_offsets = expert_offsets; f.table = p.table;
+        f.d = dims->d; f.I = dims->I; f.N = dims->N; f.topk = dims->k;
+        f.m = (int)std::ceil((double)keep_frac * dims->I - 1e-6);
+        if (f.m < 1) f.m = 1;
+        f.words = p.words; f.rows_cap = dims->T * dims->k;
+        f.u = ws_at<float>(ws, L.floe_u); f.kept = ws_at<uint32_t>(ws, L.floe_kept);
+        f.list = ws_at<int32_t>(ws, L.floe_list); f.count = ws_at<int32_t>(ws, L.floe_count);
+        PlanArgs pa;
+        pa.expert_offsets = expert_offsets; pa.T = dims->T; pa.N = dims->N;
+        pa.n_shared = dims->n_shared; pa.I = dims->I; pa.I_shared = dims->I_shared;
+        pa.rg = gemv_rows(*dims); pa.G = gemv_grid(dims); pa.max_segs = L.max_segs;
+        pa.max_partial_rows = L.max_partial_rows; pa.d = dims->d;
+        pa.hdr = ws_at<PlanHeader>(ws, L.plan_hdr); pa.segs = ws_at<Seg>(ws, L.segs);
+        pa.seg_first = ws_at<int32_t>(ws, L.seg_first); pa.err = p.err; pa.tc_plan = nullptr;
+        MOE_CUDA(launch_floe_prepare(f, pa, p, gemv_grid(dims), S(stream)));
+        count(5);
+    }
     MOE_CUDA(launch_gemv(p, gemv_grid(dims), bf16(dims), S(stream)));
     count();
     GemvReduceArgs r;
@@ -375,6 +399,17 @@ moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table
     r.y_perm = y_perm; r.y_shared = y_shared;
     MOE_CUDA(launch_gemv_reduce(r, S(stream)));
     count();
+    return MOE_OK;
+}
+
+moe_status moe_floe_kept_mask(const moe_dims* dims, void* ws, size_t ws_bytes, const uint32_t** kept,
+                              int32_t* words_per_row) {
+    MOE_TRY(check_dims(dims));
+    MOE_TRY(check_ws(dims, ws, ws_bytes));
+    if (!kept || !words_per_row) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(*dims);
+    *kept = ws_at<const uint32_t>(ws, L.floe_kept);
+    *words_per_row = (dims->I + 31) / 32;
     return MOE_OK;
 }
 

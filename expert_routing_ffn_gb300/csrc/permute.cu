@@ -112,7 +112,7 @@ __device__ void build_plan(const PlanArgs& a, const int* off) {
         if (n < a.max_segs) {
             Seg s;
             s.expert = expert; s.row0 = row0; s.rows = rows; s.I = Ie; s.ch_start = ch;
-            s.c0 = 0; s.npieces = 0; s.pbase = 0;
+            s.c0 = 0; s.npieces = 0; s.pbase = 0; s.list_off = -1;
             a.segs[n] = s;
         }
         ++n;

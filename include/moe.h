@@ -214,8 +214,11 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* final_idx,
  *   x [T,d]; table: from moe_expert_table_init; expert_offsets/perm from
  *   moe_permute (same call sequence, same workspace).
  *   keep_frac in (0,1]: < 1 applies FloE contextual sparsity to routed
- *   experts (keep the ceil(keep_frac*I) channels with the largest |x.W_up|
- *   per token; gate and down only for kept channels).
+ *   experts (keep the m = ceil(keep_frac*I) channels with the largest
+ *   |x.W_up| per token, lowest channel index among equal values; gate and
+ *   down rows read only for the union of the kept channels of an expert's
+ *   tokens, each token using its own mask).  Decode batches (T <= 64) of
+ *   bf16 layers only; otherwise MOE_ERR_UNSUPPORTED.
  *   y_perm [T*k, d] float32: row pos = the expert output for slot perm[pos]
  *   (ungated); y_shared [T, d] float32 (NULL if n_shared == 0) = sum of the
  *   shared experts' outputs.
@@ -225,6 +228,14 @@ moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table
                           const int32_t* expert_offsets, const int32_t* perm, float keep_frac,
                           float* y_perm, float* y_shared, void* ws, size_t ws_bytes,
                           void* stream);
+
+/* Diagnostic: where the last moe_expert_ffn call with keep_frac < 1 left the
+ * FloE kept-channel bitsets inside `ws` (FloE method §1, the mask S_t):
+ * *kept = device uint32 [rows][*words_per_row], one row per permuted
+ * position (the order of perm), bit i = channel i kept.  Valid until the
+ * next call that uses the workspace. */
+moe_status moe_floe_kept_mask(const moe_dims* dims, void* ws, size_t ws_bytes, const uint32_t** kept,
+                              int32_t* words_per_row);
 
 /* moe_expert_ffn without a workspace, for callers that cannot allocate device
  * memory when they run the layer: an engine plugin handed only its inputs and

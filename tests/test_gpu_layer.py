@@ -258,3 +258,41 @@ def test_exact_policy_with_staging_matches_plain_moe():
     finally:
         for e, (g, u, dn) in zip(ids, saved):
             layer.w_gate[e].copy_(g); layer.w_up[e].copy_(u); layer.w_down[e].copy_(dn)
+
+
+@pytest.mark.parametrize("T", [1, 8, 32])
+def test_floe_sparse_matches_oracle(T):
+    """FloE contextual sparsity (method §1): each token keeps the m channels
+    with the largest |x W_up| (m = ceil(0.1 I) = 1434 for I = 14336); the kept
+    sets are bit-exact and the outputs within the bf16 tolerance."""
+    cfg, W = _host("mixtral")
+    layer = _device("mixtral", T)
+    kf = np.float32(0.1)
+    m = int(np.ceil(float(kf) * cfg.I - 1e-6))
+    assert m == 1434
+    x = make_tokens(cfg, T=T, batch=5)
+    bufs = LayerBuffers(layer, T)
+    forward(layer, bufs, x_device(x, layer.dt), keep_frac=float(kf))
+    st, det = moe.moe_check(layer.ws)
+    assert st == moe.MOE_OK, (moe.status_string(st), det)
+    R = oracle.layer_forward(cfg, W, x, keep_m=m)
+    check_selection(cfg, R, bufs)
+    check_output(cfg, R, bufs.out)
+    ptr, words = moe.moe_floe_kept_mask(layer.dims.with_T(T), layer.ws)
+    rows = int(bufs.expert_offsets[-1])
+    off = ptr - layer.ws.data_ptr()
+    kept = layer.ws[off:off + rows * words * 4].view(torch.int32).cpu().numpy().view(np.uint32)
+    kept = kept.reshape(rows, words)
+    inv = to_np(bufs.inv_perm).reshape(T, cfg.k)
+    fi = to_np(bufs.final_idx)
+    keep_tok = ~R.excluded()
+    n_checked = 0
+    for t in np.nonzero(keep_tok)[0]:
+        for s in range(cfg.k):
+            e = fi[t, s]
+            pos = inv[t, s]
+            so = list(R.final_idx[t]).index(e)
+            bits = np.unpackbits(kept[pos].view(np.uint8), bitorder="little")[:cfg.I]
+            assert (np.nonzero(bits)[0] == R.kept[t, so]).all(), f"kept channels differ (token {t})"
+            n_checked += 1
+    assert n_checked > 0
