@@ -116,6 +116,9 @@ __host__ __device__ inline WsLayout ws_layout(const moe_dims& D) {
     // segments: sum over experts of ceil(rows_e / rg) <= rows / rg + N, plus the
     // shared experts' ceil(T / rg) each
     L.max_segs = (int)(rows_routed / rg + N + (size_t)D.n_shared * (T / rg + 1) + 8);
+    // the FloE up-only pass plans 2 rows per segment: sum_e ceil(rows_e / 2)
+    const int up_segs = (int)(rows_routed / 2 + N + 8);
+    if (up_segs > L.max_segs) L.max_segs = up_segs;
     // partial rows: sum over segments of pieces * rows <= rg * G + 2 * all rows
     // (a segment of I channels spans at most I / P + 2 CTA ranges, P >= total / G)
     L.max_partial_rows = (int)((size_t)rg * kGemvMaxCtas + 2 * (rows_routed + rows_shared) + 16);

@@ -26,7 +26,7 @@
 
 namespace moe {
 
-constexpr int kNSMax = 24;  // up-only launches use 3 x NS stages
+constexpr int kNSMax = 8;
 
 // Issues the bulk copies of one CTA's stages, in the order they are read.
 // Run by thread 0 only.
@@ -47,14 +47,14 @@ struct Producer {
         const Seg S = segs[seg];
         const int local = ch - S.ch_start;
         const int seg_end = min(hi, S.ch_start + S.I) - S.ch_start;
-        const int nch = min(CH, seg_end - local);
+        // an up-only stage holds 3 x CH up rows (the whole stage buffer)
+        const int nch = min(S.list_off == kUpOnly ? 3 * CH : CH, seg_end - local);
         const ExpertEntry& E = table[S.expert];
         const int b = issued % NS;
         unsigned char* buf = stage_mem + (size_t)b * stage_bytes;
         const uint32_t bytes = (uint32_t)(nch * row_bytes);
         if (S.list_off == kUpOnly) {
-            // FloE first pass: the up rows only (a stage is one third of a
-            // dense stage, so three times as many are in flight)
+            // FloE first pass: up rows only, 3 x CH of them per stage
             mbar_arrive_expect_tx(&full[b], bytes);
             bulk_g2s(buf, static_cast<const char*>(E.w[1]) + (size_t)local * row_bytes, bytes, &full[b],
                      policy);
@@ -120,9 +120,7 @@ __device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, in
     const size_t mat_bytes = (size_t)CH * row_bytes;
     const W* x = static_cast<const W*>(p.x);
     const bool sparse = S.list_off >= 0;  // FloE segment: gate/down of listed channels
-    const bool up_only = S.list_off == kUpOnly;  // FloE first pass: u = x . W_up only
-    const int NS = up_only ? 3 * p.NS : p.NS;
-    const size_t stage_bytes = up_only ? mat_bytes : 3 * mat_bytes;
+    const size_t stage_bytes = 3 * mat_bytes;
 
     float xr[ROWS][V];
 #pragma unroll
@@ -139,8 +137,8 @@ __device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, in
 
     for (int i = llo; i < lhi; i += CH) {
         const int nch = min(CH, lhi - i);
-        const int b = stage_k % NS;
-        const uint32_t par = (uint32_t)((stage_k / NS) & 1);
+        const int b = stage_k % p.NS;
+        const uint32_t par = (uint32_t)((stage_k / p.NS) & 1);
         if (!mbar_wait(&sh.full[b], par)) {
             set_error(p.err, MOE_ERR_TIMEOUT, cta);
             *sh.abort_flag = 1;
@@ -154,16 +152,14 @@ __device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, in
 #pragma unroll
         for (int cc = 0; cc < CH; ++cc) {
             if (cc < nch) {
-                if (!up_only) {
-                    float wg[V];
-                    unpack16(reinterpret_cast<const uint4*>(buf + cc * row_bytes)[tid], wg, (W*)nullptr);
+                float wg[V];
+                unpack16(reinterpret_cast<const uint4*>(buf + cc * row_bytes)[tid], wg, (W*)nullptr);
 #pragma unroll
-                    for (int r = 0; r < ROWS; ++r) v[cc * 2 * ROWS + r] = dot_v<V>(wg, xr[r]);
-                }
+                for (int r = 0; r < ROWS; ++r) v[cc * 2 * ROWS + r] = dot_v<V>(wg, xr[r]);
                 if (!sparse) {
                     float wu[V];
-                    const unsigned char* ub = up_only ? buf : buf + mat_bytes;
-                    unpack16(reinterpret_cast<const uint4*>(ub + cc * row_bytes)[tid], wu, (W*)nullptr);
+                    unpack16(reinterpret_cast<const uint4*>(buf + mat_bytes + cc * row_bytes)[tid], wu,
+                             (W*)nullptr);
 #pragma unroll
                     for (int r = 0; r < ROWS; ++r) v[cc * 2 * ROWS + ROWS + r] = dot_v<V>(wu, xr[r]);
                 }
@@ -190,11 +186,7 @@ __device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, in
                 g += red[w * 32 + cc * 2 * ROWS + r];
                 u += red[w * 32 + cc * 2 * ROWS + ROWS + r];
             }
-            if (cc < nch && up_only) {
-                // FloE first pass: store u and skip the down projection
-                p.floe_u[(size_t)(S.row0 + r) * p.I + i + cc] = u;
-                hq = 0.f;
-            } else if (cc < nch && sparse) {
+            if (cc < nch && sparse) {
                 // FloE: u from the dense up projection, h only on this row's kept channels
                 const int ch = p.floe_list[S.list_off + i + cc];
                 const size_t row = (size_t)(S.row0 + r);
@@ -208,7 +200,7 @@ __device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, in
         // down projection: y[r, chunk] += h[c, r] * Wd[c, chunk]
 #pragma unroll
         for (int cc = 0; cc < CH; ++cc) {
-            if (cc < nch && !up_only) {
+            if (cc < nch) {
                 float wd[V];
                 unpack16(reinterpret_cast<const uint4*>(buf + 2 * mat_bytes + cc * row_bytes)[tid], wd,
                          (W*)nullptr);
@@ -224,13 +216,68 @@ __device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, in
         if (*sh.abort_flag) break;
     }
     // partial output rows of this CTA for this segment
-    if (up_only) return;
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) {
         float* dst = p.partial + ((size_t)(S.pbase + (cta - S.c0) * ROWS + r)) * d + (size_t)tid * V;
 #pragma unroll
         for (int j = 0; j < V; j += 4)
             *reinterpret_cast<float4*>(dst + j) = make_float4(yacc[r][j], yacc[r][j + 1], yacc[r][j + 2], yacc[r][j + 3]);
+    }
+}
+
+// FloE first pass over one segment piece: u[row, ch] = x_row . W_up[ch, :]
+// for ROWS <= 2 token rows, 3 x CH up rows per stage, no down projection.
+template <typename W, int CHU, int ROWS>
+__device__ __forceinline__ void gemv_piece_up(const GemvParams& p, const Seg& S, int llo, int lhi,
+                                              int cta, const GemvShared& sh, int n_cons, int& stage_k) {
+    constexpr int V = Vec<W>::n;
+    static_assert(CHU * ROWS <= 16, "per-stage outputs must fit one 16-value reduce-scatter");
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = n_cons >> 5;
+    const int d = p.d;
+    const size_t row_bytes = (size_t)d * sizeof(W);
+    const size_t stage_bytes = (size_t)CHU * row_bytes;
+    const W* x = static_cast<const W*>(p.x);
+    float xr[ROWS][V];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+        const int token = p.perm[S.row0 + r] / p.topk;
+        unpack16(reinterpret_cast<const uint4*>(x + (size_t)token * d)[tid], xr[r], (W*)nullptr);
+    }
+    for (int i = llo; i < lhi; i += CHU) {
+        const int nch = min(CHU, lhi - i);
+        const int b = stage_k % p.NS;
+        if (!mbar_wait(&sh.full[b], (uint32_t)((stage_k / p.NS) & 1))) {
+            set_error(p.err, MOE_ERR_TIMEOUT, cta);
+            *sh.abort_flag = 1;
+        }
+        const unsigned char* buf = sh.stage_mem + (size_t)b * stage_bytes;
+        float v[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) v[q] = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < CHU; ++cc) {
+            if (cc < nch) {
+                float wu[V];
+                unpack16(reinterpret_cast<const uint4*>(buf + cc * row_bytes)[tid], wu, (W*)nullptr);
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) v[cc * ROWS + r] = dot_v<V>(wu, xr[r]);
+            }
+        }
+        float* red = sh.red + (size_t)(stage_k & 1) * nw * 32;
+        const float t = warp_reduce_scatter16(v);
+        if ((lane & 1) == 0) red[warp * 32 + (lane >> 1)] = t;
+        consumer_sync(n_cons);
+        if (tid == 0 && stage_k > 0 && !sh.prod->done()) sh.prod->issue();
+        if (warp == 0 && lane < CHU * ROWS) {
+            const int cc = lane / ROWS, r = lane % ROWS;
+            if (cc < nch) {
+                float u = 0.f;
+                for (int w = 0; w < nw; ++w) u += red[w * 32 + lane];
+                p.floe_u[(size_t)(S.row0 + r) * p.I + i + cc] = u;
+            }
+        }
+        ++stage_k;
+        if (*sh.abort_flag) break;
     }
 }
 
@@ -259,8 +306,7 @@ __device__ __forceinline__ void ffn_gemv_body(const GemvParams& p) {
     }
     const int seg0 = s_lo;
 
-    // an up-only launch (FloE first pass) splits every stage buffer in three
-    const int NSx = p.up_pass ? 3 * p.NS : p.NS;
+    const int NSx = p.NS;
     Producer prod;
     if (tid == 0) {
         for (int b = 0; b < NSx; ++b) mbar_init(&full[b], 1);
@@ -269,7 +315,7 @@ __device__ __forceinline__ void ffn_gemv_body(const GemvParams& p) {
         prod.segs = p.segs; prod.table = p.table; prod.list = p.floe_list; prod.stage_mem = stage_mem;
         prod.full = full;
         prod.row_bytes = row_bytes; prod.mat_bytes = CH * row_bytes;
-        prod.stage_bytes = (p.up_pass ? 1 : 3) * CH * row_bytes; prod.NS = NSx; prod.CH = CH;
+        prod.stage_bytes = 3 * CH * row_bytes; prod.NS = NSx; prod.CH = CH;
         prod.seg = seg0;
         prod.ch = lo; prod.hi = hi; prod.n_seg = hdr.n_seg; prod.issued = 0;
         prod.policy = l2_evict_first_policy();
@@ -286,7 +332,11 @@ __device__ __forceinline__ void ffn_gemv_body(const GemvParams& p) {
         const Seg S = p.segs[seg];
         const int llo = ch - S.ch_start;
         const int lhi = min(hi, S.ch_start + S.I) - S.ch_start;
-        switch (S.rows) {
+        if (S.list_off == kUpOnly) {
+            if (S.rows == 1) gemv_piece_up<W, 3 * CH, 1>(p, S, llo, lhi, cta, sh, n_cons, stage_k);
+            else if (S.rows == 2) gemv_piece_up<W, 3 * CH, 2>(p, S, llo, lhi, cta, sh, n_cons, stage_k);
+            else { if (tid == 0) set_error(p.err, MOE_ERR_DEVICE_INDEX, seg); s_abort = 1; }
+        } else switch (S.rows) {
 #define MOE_PIECE(R)                                                                        \
     case R:                                                                                 \
         if (R <= RG) {                                                                      \

@@ -21,7 +21,7 @@
 
 namespace moe {
 
-// Plan of the first FloE pass: every routed expert's rows in groups of rg
+// Plan of the first FloE pass: every routed expert's rows in groups of 2
 // over all I channels, up projection only (no partial outputs).
 __global__ void floe_up_plan_kernel(PlanArgs a) {
     __shared__ int off[kMaxExperts + 1];
@@ -30,10 +30,10 @@ __global__ void floe_up_plan_kernel(PlanArgs a) {
     if (threadIdx.x != 0) return;
     int n = 0, ch = 0;
     for (int e = 0; e < a.N; ++e)
-        for (int r = off[e]; r < off[e + 1]; r += a.rg) {
+        for (int r = off[e]; r < off[e + 1]; r += 2) {
             if (n < a.max_segs) {
                 Seg s;
-                s.expert = e; s.row0 = r; s.rows = min(a.rg, off[e + 1] - r); s.I = a.I; s.ch_start = ch;
+                s.expert = e; s.row0 = r; s.rows = min(2, off[e + 1] - r); s.I = a.I; s.ch_start = ch;
                 s.c0 = 0; s.npieces = 0; s.pbase = 0; s.list_off = kUpOnly;
                 a.segs[n] = s;
             }
@@ -75,8 +75,14 @@ __global__ void __launch_bounds__(1024) floe_select_kernel(const float* __restri
         for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
         __syncthreads();
         const uint32_t prefix = s_prefix;
-        for (int i = tid; i < I; i += blockDim.x)
-            if ((keys[i] & mask) == prefix) atomicAdd(&hist[(keys[i] >> shift) & 255u], 1);
+        // lanes with the same bin add once (|u| values share few high bins)
+        for (int base = 0; base < I; base += blockDim.x) {
+            const int i = base + tid;
+            const bool act = i < I && (keys[i] & mask) == prefix;
+            const int bin = act ? (int)((keys[i] >> shift) & 255u) : 256;
+            const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+            if (act && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+        }
         __syncthreads();
         if (tid == 0) {
             int cum = 0, rem = s_remaining;
