@@ -39,7 +39,7 @@ __device__ __forceinline__ void set_error(DevError* e, int code, int detail) {
 // which is split evenly over the G CTAs of the GEMV grid (P channels each).
 // CTA c writes a partial [rows, d] sum for every segment it overlaps at
 // partial row pbase + (c - c0) * rows.
-struct Seg {
+struct alignas(16) Seg {
     int expert;     // 0..N-1 routed, N + s shared expert s
     int row0;       // routed: first permuted position; shared: first token
     int rows;

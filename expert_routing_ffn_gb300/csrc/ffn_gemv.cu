@@ -107,7 +107,7 @@ struct GemvShared {
 };
 
 // One segment piece: channels [llo, lhi) of segment S, ROWS token rows.
-template <typename W, int CH, int ROWS>
+template <typename W, int CH, int ROWS, bool FLOE>
 __device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, int llo, int lhi,
                                            int cta, const GemvShared& sh, int n_cons,
                                            int& stage_k) {
@@ -119,7 +119,7 @@ __device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, in
     const size_t row_bytes = (size_t)d * sizeof(W);
     const size_t mat_bytes = (size_t)CH * row_bytes;
     const W* x = static_cast<const W*>(p.x);
-    const bool sparse = S.list_off >= 0;  // FloE segment: gate/down of listed channels
+    const bool sparse = FLOE && S.list_off >= 0;  // FloE segment: gate/down of listed channels
     const size_t stage_bytes = 3 * mat_bytes;
 
     float xr[ROWS][V];
@@ -186,7 +186,7 @@ __device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, in
                 g += red[w * 32 + cc * 2 * ROWS + r];
                 u += red[w * 32 + cc * 2 * ROWS + ROWS + r];
             }
-            if (cc < nch && sparse) {
+            if (FLOE && cc < nch && sparse) {
                 // FloE: u from the dense up projection, h only on this row's kept channels
                 const int ch = p.floe_list[S.list_off + i + cc];
                 const size_t row = (size_t)(S.row0 + r);
@@ -283,7 +283,7 @@ __device__ __forceinline__ void gemv_piece_up(const GemvParams& p, const Seg& S,
 
 // Block = one thread per 16-byte chunk of d.  Thread 0 also issues the
 // stage copies.
-template <typename W, int RG, int CH, int MAXT>
+template <typename W, int RG, int CH, int MAXT, bool FLOE>
 __device__ __forceinline__ void ffn_gemv_body(const GemvParams& p) {
     __shared__ __align__(8) uint64_t full[kNSMax];
     __shared__ float red_s[2 * (MAXT / 32) * 32];
@@ -332,7 +332,7 @@ __device__ __forceinline__ void ffn_gemv_body(const GemvParams& p) {
         const Seg S = p.segs[seg];
         const int llo = ch - S.ch_start;
         const int lhi = min(hi, S.ch_start + S.I) - S.ch_start;
-        if (S.list_off == kUpOnly) {
+        if (FLOE && S.list_off == kUpOnly) {
             if (S.rows == 1) gemv_piece_up<W, 3 * CH, 1>(p, S, llo, lhi, cta, sh, n_cons, stage_k);
             else if (S.rows == 2) gemv_piece_up<W, 3 * CH, 2>(p, S, llo, lhi, cta, sh, n_cons, stage_k);
             else { if (tid == 0) set_error(p.err, MOE_ERR_DEVICE_INDEX, seg); s_abort = 1; }
@@ -340,7 +340,7 @@ __device__ __forceinline__ void ffn_gemv_body(const GemvParams& p) {
 #define MOE_PIECE(R)                                                                        \
     case R:                                                                                 \
         if (R <= RG) {                                                                      \
-            gemv_piece<W, CH, (R <= RG ? R : 1)>(p, S, llo, lhi, cta, sh, n_cons, stage_k);  \
+            gemv_piece<W, CH, (R <= RG ? R : 1), FLOE>(p, S, llo, lhi, cta, sh, n_cons, stage_k); \
         } else {                                                                            \
             if (tid == 0) set_error(p.err, MOE_ERR_DEVICE_INDEX, seg);                      \
             s_abort = 1;                                                                    \
@@ -369,15 +369,15 @@ __device__ __forceinline__ void ffn_gemv_body(const GemvParams& p) {
 // The register file is split over the SM's four sub-partitions, each taking
 // a quarter of the resident warps: 16 warps per SM allow 128 registers per
 // thread.  Two CTAs of 256 threads per SM (d <= 2048) ...
-template <typename W, int RG, int CH>
+template <typename W, int RG, int CH, bool FLOE>
 __global__ void __launch_bounds__(256, 2) ffn_gemv_kernel_x2(GemvParams p) {
-    ffn_gemv_body<W, RG, CH, 256>(p);
+    ffn_gemv_body<W, RG, CH, 256, FLOE>(p);
 }
 
 // ... or one CTA of up to 512 threads (d <= 4096).
-template <typename W, int RG, int CH>
+template <typename W, int RG, int CH, bool FLOE>
 __global__ void __launch_bounds__(512, 1) ffn_gemv_kernel_x1(GemvParams p) {
-    ffn_gemv_body<W, RG, CH, 512>(p);
+    ffn_gemv_body<W, RG, CH, 512, FLOE>(p);
 }
 
 // Sum the partial rows of each output row in piece order.
@@ -469,18 +469,20 @@ int gemv_stages(int d, bool bf16) {
     const size_t stage = (size_t)3 * 2 * d * (bf16 ? 2 : 4);
     const size_t budget = gemv_ctas_per_sm(d, bf16) == 2 ? 100 * 1024 : 200 * 1024;
     int ns = (int)(budget / stage);
-    // at most kNSMax / 3: an up-only launch runs three stages per buffer
-    return ns < 2 ? 2 : (ns > kNSMax / 3 ? kNSMax / 3 : ns);
+    return ns < 2 ? 2 : (ns > kNSMax ? kNSMax : ns);
 }
 
+// floe = true selects the instantiation with the FloE modes (up-only and
+// sparse segments); the dense instantiation carries none of their code.
 cudaError_t launch_gemv(const GemvParams& p, int G, bool bf16, cudaStream_t st, bool floe) {
-    (void)floe;  // the sparse mode is chosen per segment (Seg::list_off)
     if (bf16) {
         if (p.d <= 2048)
-            return launch_gemv_k(ffn_gemv_kernel_x2<__nv_bfloat16, 4, 2>, 256, 8, 2, 2, p, G, st);
-        return launch_gemv_k(ffn_gemv_kernel_x1<__nv_bfloat16, 4, 2>, 512, 8, 2, 2, p, G, st);
+            return floe ? launch_gemv_k(ffn_gemv_kernel_x2<__nv_bfloat16, 4, 2, true>, 256, 8, 2, 2, p, G, st)
+                        : launch_gemv_k(ffn_gemv_kernel_x2<__nv_bfloat16, 4, 2, false>, 256, 8, 2, 2, p, G, st);
+        return floe ? launch_gemv_k(ffn_gemv_kernel_x1<__nv_bfloat16, 4, 2, true>, 512, 8, 2, 2, p, G, st)
+                    : launch_gemv_k(ffn_gemv_kernel_x1<__nv_bfloat16, 4, 2, false>, 512, 8, 2, 2, p, G, st);
     }
-    return launch_gemv_k(ffn_gemv_kernel_x2<float, 8, 2>, 256, 4, 2, 4, p, G, st);
+    return launch_gemv_k(ffn_gemv_kernel_x2<float, 8, 2, false>, 256, 4, 2, 4, p, G, st);
 }
 
 cudaError_t launch_gemv_reduce(const GemvReduceArgs& a, cudaStream_t st) {

@@ -230,7 +230,7 @@ cudaError_t launch_floe_prepare(const FloeArgs& f, const PlanArgs& plan, const G
     if (e != cudaSuccess) return e;
     GemvParams up = gp;
     up.up_pass = 1;
-    e = launch_gemv(up, G, true, st);
+    e = launch_gemv(up, G, true, st, true);
     if (e != cudaSuccess) return e;
     const size_t sel_smem = ((size_t)f.I + f.words) * sizeof(uint32_t);
     e = allow_max_smem(floe_select_kernel);

@@ -390,7 +390,7 @@ moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table
         MOE_CUDA(launch_floe_prepare(f, pa, p, gemv_grid(dims), S(stream)));
         count(5);
     }
-    MOE_CUDA(launch_gemv(p, gemv_grid(dims), bf16(dims), S(stream)));
+    MOE_CUDA(launch_gemv(p, gemv_grid(dims), bf16(dims), S(stream), floe));
     count();
     GemvReduceArgs r;
     r.hdr = p.hdr; r.segs = p.segs; r.seg_first = ws_at<int32_t>(ws, L.seg_first);
