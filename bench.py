@@ -78,10 +78,14 @@ def peaks():
 
 
 def recorded_traffic(kernel_src: str, workload: str):
-    """Per-launch DRAM bytes from the committed ncu summary of this kernel and
-    workload, if the kernel source is unchanged since it was taken."""
-    with open(os.path.join(ROOT, "expert_routing_ffn_gb300", "csrc", kernel_src), "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    """Per-launch DRAM bytes (read + write) of the FFN stage from the committed
+    ncu summary for this workload, if the kernel source and the shared header
+    are unchanged since the counters were taken (else None)."""
+    h = hashlib.sha256()
+    for src in (kernel_src, "common.cuh"):
+        with open(os.path.join(ROOT, "expert_routing_ffn_gb300", "csrc", src), "rb") as f:
+            h.update(f.read())
+    sha = h.hexdigest()[:16]
     prof = os.path.join(ROOT, "profiles")
     if not os.path.isdir(prof):
         return None
