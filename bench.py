@@ -357,19 +357,24 @@ def main():
     k_ms = [a.elapsed_time(b) for a, b in evs]
     k_bytes = [fb[(i + n_copies) % n_copies] for i in range(n_k)]
     k_flops = [ff[(i + n_copies) % n_copies] for i in range(n_k)]
+    path = moe.moe_expert_ffn_path(layers[0].dims.with_T(T), cfg.keep_frac)
     if phase == "decode":
         achieved = sum(k_bytes) / (sum(k_ms) / 1e3) / 1e9
-        kname = ("moe_expert_ffn (floe up/select/union/plan + sparse ffn_gemv_kernel + gemv_reduce_kernel)"
-                 if cfg.keep_frac < 1.0 else "moe_expert_ffn (ffn_gemv_kernel + gemv_reduce_kernel)")
-        roof = {"kernel": kname, "bound": "hbm",
+        kname, ksrc = {
+            "tc-decode": ("moe_expert_ffn (gather_rows_kernel + ffn_tcd_kernel + gemv_reduce_kernel)",
+                          "ffn_tcd.cu"),
+            "gemv-floe": ("moe_expert_ffn (floe up/select/union/plan + sparse ffn_gemv_kernel"
+                          " + gemv_reduce_kernel)", "ffn_gemv.cu"),
+        }.get(path, ("moe_expert_ffn (ffn_gemv_kernel + gemv_reduce_kernel)", "ffn_gemv.cu"))
+        roof = {"kernel": kname, "ffn_path": path, "bound": "hbm",
                 "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
                 "peak_source": peak_src, "algorithmic_bytes_per_launch": float(statistics.mean(fb)),
                 "avg_launch_ms": statistics.mean(k_ms),
-                "traffic": recorded_traffic("ffn_gemv.cu", wl_name)}
+                "traffic": recorded_traffic(ksrc, wl_name)}
     else:
         achieved = sum(k_flops) / (sum(k_ms) / 1e3) / 1e12
         roof = {"kernel": "moe_expert_ffn (gather + ffn_tc_kernel<1> + ffn_tc_kernel<2>)",
-                "bound": "tensor", "achieved": achieved, "peak": bf16_tflops, "unit": "TFLOP/s",
+                "ffn_path": path, "bound": "tensor", "achieved": achieved, "peak": bf16_tflops, "unit": "TFLOP/s",
                 "frac": achieved / bf16_tflops, "peak_source": peak_src + " bf16 burst",
                 "algorithmic_flops_per_launch": float(statistics.mean(ff)),
                 "avg_launch_ms": statistics.mean(k_ms),

@@ -78,6 +78,7 @@ _DIMS = C.POINTER(moe_dims)
 _PROTOS = {
     "moe_status_string": ([C.c_int], C.c_char_p),
     "moe_launch_total": ([], C.c_uint64),
+    "moe_expert_ffn_path": ([C.POINTER(moe_dims), C.c_float], C.c_char_p),
     "moe_last_error_detail": ([], C.c_char_p),
     "moe_workspace_size": ([_DIMS, C.POINTER(C.c_size_t)], C.c_int),
     "moe_expert_table_size": ([_DIMS, C.POINTER(C.c_size_t)], C.c_int),
@@ -169,6 +170,11 @@ def make_dims(T, d, N, k, I, n_shared=0, I_shared=0, r=0, delta_max=None, wtype=
 
 def moe_launch_total() -> int:
     return int(lib().moe_launch_total())
+
+
+def moe_expert_ffn_path(dims: moe_dims, keep_frac: float = 1.0) -> str:
+    """Which kernels moe_expert_ffn runs for these dimensions (no device work)."""
+    return lib().moe_expert_ffn_path(C.byref(dims), float(keep_frac)).decode()
 
 
 def moe_workspace_size(dims: moe_dims) -> int:

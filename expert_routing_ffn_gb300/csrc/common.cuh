@@ -87,6 +87,28 @@ __host__ __device__ inline bool tc_usable(const moe_dims& D) {
 }
 __host__ __device__ inline bool use_tc(const moe_dims& D) { return tc_usable(D) && D.T > kTcMinTokens; }
 
+// Decode-size batches of bf16 layers whose d is a multiple of 128 and whose
+// expert widths are multiples of 16 run the dense expert FFN on the tensor
+// cores too, with the weight rows as the MMA's M side and the (few) token
+// rows of a segment as its N side.
+#ifndef MOE_DECODE_TC
+#define MOE_DECODE_TC 1
+#endif
+__host__ __device__ inline bool tcd_shapes(const moe_dims& D) {
+    return MOE_DECODE_TC && D.wtype == MOE_DTYPE_BF16 && D.d % 128 == 0 && D.I % 16 == 0 &&
+           (D.n_shared == 0 || D.I_shared % 16 == 0);
+}
+// 1..3 tokens stay on the CUDA-core GEMV, which streams faster at one or two
+// rows per expert (the tensor-core path pays a pipeline fill per CTA piece).
+constexpr int kTcdMinTokens = 4;
+__host__ __device__ inline bool tcd_usable(const moe_dims& D) {
+    return tcd_shapes(D) && !use_tc(D) && D.T >= kTcdMinTokens;
+}
+// Token rows per segment on that path (the MMA's N): up to 32 tokens every
+// expert's rows of the batch fit one segment, so each weight is read once.
+__host__ __device__ inline int tcd_rows(int T) { return T <= 16 ? 16 : 32; }
+constexpr int kTcdMaxCtas = 160;  // grid of that path: min(SMs, kTcdMaxCtas)
+
 // ---------------------------------------------------------------- workspace
 struct WsLayout {
     size_t err, ticket, logits_r, logits_p, score, qp, plan_hdr, segs, seg_first, lore_z, tc_plan,
@@ -113,15 +135,21 @@ __host__ __device__ inline WsLayout ws_layout(const moe_dims& D) {
     const size_t rows_routed = Tg * (size_t)D.k;
     const size_t rows_shared = Tg * (size_t)D.n_shared;
     const int rg = gemv_rows(D);
+    // a workspace sized for T serves every batch of at most T tokens: the
+    // decode tensor-core path may run for any of them up to kTcMinTokens
+    const bool tcd = tcd_shapes(D);
+    const int rg_tcd = tcd ? tcd_rows((int)(T < (size_t)kTcMinTokens ? T : (size_t)kTcMinTokens)) : 0;
     // segments: sum over experts of ceil(rows_e / rg) <= rows / rg + N, plus the
-    // shared experts' ceil(T / rg) each
+    // shared experts' ceil(T / rg) each (the smallest rg gives the most)
     L.max_segs = (int)(rows_routed / rg + N + (size_t)D.n_shared * (T / rg + 1) + 8);
     // the FloE up-only pass plans 2 rows per segment: sum_e ceil(rows_e / 2)
     const int up_segs = (int)(rows_routed / 2 + N + 8);
     if (up_segs > L.max_segs) L.max_segs = up_segs;
     // partial rows: sum over segments of pieces * rows <= rg * G + 2 * all rows
     // (a segment of I channels spans at most I / P + 2 CTA ranges, P >= total / G)
-    L.max_partial_rows = (int)((size_t)rg * kGemvMaxCtas + 2 * (rows_routed + rows_shared) + 16);
+    const size_t spread = (size_t)rg * kGemvMaxCtas > (size_t)rg_tcd * kTcdMaxCtas
+                              ? (size_t)rg * kGemvMaxCtas : (size_t)rg_tcd * kTcdMaxCtas;
+    L.max_partial_rows = (int)(spread + 2 * (rows_routed + rows_shared) + 16);
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, kAlign); return at; };
     L.err = take(sizeof(DevError));
@@ -135,7 +163,7 @@ __host__ __device__ inline WsLayout ws_layout(const moe_dims& D) {
     L.seg_first = take((N + (size_t)D.n_shared + 1) * 4);
     L.lore_z = take(T * (size_t)D.k * (size_t)(D.r > 0 ? D.r : 1) * 4);
     L.tc_plan = take(sizeof(TcPlan));
-    L.x_perm = take(tc ? T * D.k * (size_t)D.d * 2 : 0);
+    L.x_perm = take(tc || tcd ? T * D.k * (size_t)D.d * 2 : 0);
     L.h_routed = take(tc ? T * D.k * (size_t)D.I * 2 : 0);
     L.h_shared = take(tc ? T * (size_t)D.n_shared * D.I_shared * 2 : 0);
     // FloE (decode batches only)
@@ -163,6 +191,9 @@ struct alignas(64) ExpertEntry {
     // TMA descriptors (tensor maps) for the tensor-core path: gate/up tiles
     // (K-major) and down tiles (MN-major).
     alignas(64) unsigned char tmap[3][128];
+    // The decode tensor-core path: gate, up and down in boxes of 16 rows x 64
+    // values (its channel ranges are multiples of 16).
+    alignas(64) unsigned char tmap_dec[3][128];
 };
 
 // ---------------------------------------------------------------- launch setup
@@ -243,10 +274,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait: returns false after kSpinLimit unsuccessful tries.
+// Non-blocking probe: true when the phase of the given parity has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: returns false after kSpinLimit unsuccessful tries or about
+// one second of wall-clock time (%globaltimer, ns), whichever comes first.
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+constexpr uint64_t kWaitNs = 1000000000ull;
+#ifndef MOE_WAIT_POLL
+#define MOE_WAIT_POLL 0
+#endif
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1; i < kSpinLimit; ++i) {
+        if (MOE_WAIT_POLL ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+        if ((i & 255) == 0 && global_ns() - t0 > kWaitNs) return false;
+    }
     return false;
 }
 
@@ -294,6 +350,33 @@ __device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32]) {
         }
     }
     return v[0];
+}
+
+// Reduce NV values per lane across the warp (NV a power of two, 2..32):
+// halving steps over lane bits 4 .. 5 - log2(NV), then plain sums over the
+// remaining low lane bits.  Afterwards lane l holds the warp-wide sum of
+// value l >> (5 - log2(NV)).  NV - 1 + 5 - log2(NV) shuffles.
+template <int NV>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[NV]) {
+    static_assert(NV >= 2 && NV <= 32 && (NV & (NV - 1)) == 0, "NV: power of two in 2..32");
+    const int lane = threadIdx.x & 31;
+    constexpr int L = NV == 2 ? 1 : NV == 4 ? 2 : NV == 8 ? 3 : NV == 16 ? 4 : 5;
+#pragma unroll
+    for (int o = 16, n = NV; n > 1; o >>= 1, n >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            float send = up ? v[i] : v[i + n / 2];
+            float keep = up ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    float t = v[0];
+    if constexpr (L < 5) {
+#pragma unroll
+        for (int o = 1 << (4 - L); o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    }
+    return t;
 }
 
 // Reduce 16 values per lane across the warp: afterwards lane l holds the

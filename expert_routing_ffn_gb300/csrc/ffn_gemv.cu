@@ -40,44 +40,57 @@ struct Producer {
     int NS, CH, seg, ch, hi, n_seg;
     int issued;
     uint64_t policy;
+    // the segment being issued and its expert's weights, loaded once per
+    // segment (a dependent global load per stage would sit on the pipeline's
+    // critical path)
+    int cached;
+    int c_start, c_I, c_list_off;
+    const char* w[3];
 
     __device__ __forceinline__ bool done() const { return ch >= hi || seg >= n_seg; }
 
-    __device__ __forceinline__ void issue() {
+    __device__ __forceinline__ void load_seg() {
         const Seg S = segs[seg];
-        const int local = ch - S.ch_start;
-        const int seg_end = min(hi, S.ch_start + S.I) - S.ch_start;
-        // an up-only stage holds 3 x CH up rows (the whole stage buffer)
-        const int nch = min(S.list_off == kUpOnly ? 3 * CH : CH, seg_end - local);
         const ExpertEntry& E = table[S.expert];
+        c_start = S.ch_start; c_I = S.I; c_list_off = S.list_off;
+#pragma unroll
+        for (int m = 0; m < 3; ++m) w[m] = static_cast<const char*>(E.w[m]);
+        cached = seg;
+    }
+
+    __device__ __forceinline__ void issue() {
+        if (cached != seg) load_seg();
+        const int local = ch - c_start;
+        const int seg_end = min(hi, c_start + c_I) - c_start;
+        // an up-only stage holds 3 x CH up rows (the whole stage buffer)
+        const int nch = min(c_list_off == kUpOnly ? 3 * CH : CH, seg_end - local);
         const int b = issued % NS;
         unsigned char* buf = stage_mem + (size_t)b * stage_bytes;
         const uint32_t bytes = (uint32_t)(nch * row_bytes);
-        if (S.list_off == kUpOnly) {
+        if (c_list_off == kUpOnly) {
             // FloE first pass: up rows only, 3 x CH of them per stage
             mbar_arrive_expect_tx(&full[b], bytes);
-            bulk_g2s(buf, static_cast<const char*>(E.w[1]) + (size_t)local * row_bytes, bytes, &full[b],
-                     policy);
-        } else if (S.list_off >= 0) {
+            bulk_g2s(buf, w[1] + (size_t)local * row_bytes, bytes, &full[b], policy);
+        } else if (c_list_off >= 0) {
             // FloE: gate and down rows of the listed channels only
             mbar_arrive_expect_tx(&full[b], 2 * bytes);
+            // the list entries of the stage are loaded together (nch <= 2)
+            const int r0 = list[c_list_off + local];
+            const int r1 = nch > 1 ? list[c_list_off + local + 1] : 0;
             for (int c = 0; c < nch; ++c) {
-                const size_t row = (size_t)list[S.list_off + local + c];
-                bulk_g2s(buf + c * row_bytes, static_cast<const char*>(E.w[0]) + row * row_bytes,
-                         (uint32_t)row_bytes, &full[b], policy);
-                bulk_g2s(buf + 2 * mat_bytes + c * row_bytes,
-                         static_cast<const char*>(E.w[2]) + row * row_bytes, (uint32_t)row_bytes, &full[b],
-                         policy);
+                const size_t row = (size_t)(c == 0 ? r0 : r1);
+                bulk_g2s(buf + c * row_bytes, w[0] + row * row_bytes, (uint32_t)row_bytes, &full[b], policy);
+                bulk_g2s(buf + 2 * mat_bytes + c * row_bytes, w[2] + row * row_bytes, (uint32_t)row_bytes,
+                         &full[b], policy);
             }
         } else {
             mbar_arrive_expect_tx(&full[b], 3 * bytes);
 #pragma unroll
             for (int m = 0; m < 3; ++m)
-                bulk_g2s(buf + m * mat_bytes, static_cast<const char*>(E.w[m]) + (size_t)local * row_bytes,
-                         bytes, &full[b], policy);
+                bulk_g2s(buf + m * mat_bytes, w[m] + (size_t)local * row_bytes, bytes, &full[b], policy);
         }
         ch += nch;
-        if (ch >= S.ch_start + S.I) ++seg;
+        if (ch >= c_start + c_I) ++seg;
         ++issued;
     }
 };
@@ -145,7 +158,8 @@ __device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, in
         }
         const unsigned char* buf = sh.stage_mem + (size_t)b * stage_bytes;
         // partial gate/up dot products of this thread's 16-byte chunk
-        constexpr int NB = NV <= 16 ? 16 : 32;
+        constexpr int NB = NV <= 2 ? 2 : NV <= 4 ? 4 : NV <= 8 ? 8 : NV <= 16 ? 16 : 32;
+        constexpr int SH = NB == 2 ? 4 : NB == 4 ? 3 : NB == 8 ? 2 : NB == 16 ? 1 : 0;  // 5 - log2(NB)
         float v[NB];
 #pragma unroll
         for (int q = 0; q < NB; ++q) v[q] = 0.f;
@@ -168,12 +182,8 @@ __device__ __forceinline__ void gemv_piece(const GemvParams& p, const Seg& S, in
         // block sum: warp reduce-scatter, one consumer barrier, then every
         // warp reads the per-warp sums (double-buffered by stage parity)
         float* red = sh.red + (size_t)(stage_k & 1) * nw * 32;
-        if constexpr (NB == 16) {
-            const float t = warp_reduce_scatter16(v);
-            if ((lane & 1) == 0) red[warp * 32 + (lane >> 1)] = t;
-        } else {
-            red[warp * 32 + lane] = warp_reduce_scatter32(v);
-        }
+        const float t = warp_reduce_scatter<NB>(v);
+        if ((lane & ((1 << SH) - 1)) == 0) red[warp * 32 + (lane >> SH)] = t;
         consumer_sync(n_cons);
         // every thread has finished the previous stage, so its buffer can be
         // refilled with the stage NS - 1 ahead of this one
@@ -231,7 +241,10 @@ template <typename W, int CHU, int ROWS>
 __device__ __forceinline__ void gemv_piece_up(const GemvParams& p, const Seg& S, int llo, int lhi,
                                               int cta, const GemvShared& sh, int n_cons, int& stage_k) {
     constexpr int V = Vec<W>::n;
-    static_assert(CHU * ROWS <= 16, "per-stage outputs must fit one 16-value reduce-scatter");
+    constexpr int NV = CHU * ROWS;
+    static_assert(NV <= 16, "per-stage outputs must fit one 16-value reduce-scatter");
+    constexpr int NB = NV <= 2 ? 2 : NV <= 4 ? 4 : NV <= 8 ? 8 : 16;
+    constexpr int SH = NB == 2 ? 4 : NB == 4 ? 3 : NB == 8 ? 2 : 1;  // 5 - log2(NB)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = n_cons >> 5;
     const int d = p.d;
     const size_t row_bytes = (size_t)d * sizeof(W);
@@ -251,9 +264,9 @@ __device__ __forceinline__ void gemv_piece_up(const GemvParams& p, const Seg& S,
             *sh.abort_flag = 1;
         }
         const unsigned char* buf = sh.stage_mem + (size_t)b * stage_bytes;
-        float v[16];
+        float v[NB];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) v[q] = 0.f;
+        for (int q = 0; q < NB; ++q) v[q] = 0.f;
 #pragma unroll
         for (int cc = 0; cc < CHU; ++cc) {
             if (cc < nch) {
@@ -264,8 +277,8 @@ __device__ __forceinline__ void gemv_piece_up(const GemvParams& p, const Seg& S,
             }
         }
         float* red = sh.red + (size_t)(stage_k & 1) * nw * 32;
-        const float t = warp_reduce_scatter16(v);
-        if ((lane & 1) == 0) red[warp * 32 + (lane >> 1)] = t;
+        const float t = warp_reduce_scatter<NB>(v);
+        if ((lane & ((1 << SH) - 1)) == 0) red[warp * 32 + (lane >> SH)] = t;
         consumer_sync(n_cons);
         if (tid == 0 && stage_k > 0 && !sh.prod->done()) sh.prod->issue();
         if (warp == 0 && lane < CHU * ROWS) {
@@ -317,7 +330,7 @@ __device__ __forceinline__ void ffn_gemv_body(const GemvParams& p) {
         prod.row_bytes = row_bytes; prod.mat_bytes = CH * row_bytes;
         prod.stage_bytes = 3 * CH * row_bytes; prod.NS = NSx; prod.CH = CH;
         prod.seg = seg0;
-        prod.ch = lo; prod.hi = hi; prod.n_seg = hdr.n_seg; prod.issued = 0;
+        prod.ch = lo; prod.hi = hi; prod.n_seg = hdr.n_seg; prod.issued = 0; prod.cached = -1;
         prod.policy = l2_evict_first_policy();
         // fill every buffer but the one the first refill will use
         for (int k = 0; k < NSx && !prod.done(); ++k) prod.issue();

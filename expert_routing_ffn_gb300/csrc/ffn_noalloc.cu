@@ -115,7 +115,7 @@ extern "C" moe_status moe_expert_ffn_noalloc(const moe_dims* dims, const void* x
 
     moe::PlanArgs pa;
     pa.expert_offsets = expert_offsets; pa.T = dims->T; pa.N = dims->N; pa.n_shared = dims->n_shared;
-    pa.I = dims->I; pa.I_shared = dims->I_shared; pa.rg = moe::gemv_rows(*dims); pa.G = G;
+    pa.I = dims->I; pa.I_shared = dims->I_shared; pa.rg = moe::gemv_rows(*dims); pa.G = G; pa.p_align = 1;
     pa.max_segs = L.max_segs; pa.max_partial_rows = L.max_partial_rows;
     pa.hdr = moe::ws_at<moe::PlanHeader>(base, L.hdr); pa.segs = moe::ws_at<moe::Seg>(base, L.segs);
     pa.seg_first = moe::ws_at<int32_t>(base, L.seg_first); pa.err = err;

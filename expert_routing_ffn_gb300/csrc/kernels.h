@@ -50,6 +50,7 @@ struct PermuteArgs {
 struct PlanArgs {
     const int32_t* expert_offsets;
     int T, N, n_shared, I, I_shared, rg, G, max_segs, max_partial_rows, d;
+    int p_align;      // channels per CTA rounded up to a multiple of this
     PlanHeader* hdr; Seg* segs; int32_t* seg_first; DevError* err;
     TcPlan* tc_plan;  // also built when non-null
 };
@@ -102,6 +103,18 @@ struct TcLaunch {
 };
 // tensor-core expert FFN: gather, phase 1 (gate/up + SwiGLU), phase 2 (down)
 cudaError_t launch_tc_ffn(const TcLaunch& a, cudaStream_t st);
+// x_perm[pos] = x[perm[pos] / k] for the routed rows (bf16 rows of d values)
+cudaError_t launch_gather_rows(const void* x, const int32_t* perm, const int32_t* expert_offsets, int N,
+                               int k, int d, int rows_cap, void* x_perm, cudaStream_t st);
+
+struct TcdLaunch {
+    const void* x; const int32_t* perm; const int32_t* expert_offsets; const ExpertEntry* table;
+    const PlanHeader* hdr; const Seg* segs; void* x_perm; float* partial;
+    int T, d, N, k, rows_cap, nt, grid; DevError* err;
+};
+// decode-size expert FFN on the tensor cores: gather + one launch writing the
+// GEMV plan's partial rows (summed by launch_gemv_reduce)
+cudaError_t launch_tcd_ffn(const TcdLaunch& a, cudaStream_t st);
 
 struct LoreArgs {
     const void* x; const int32_t *final_idx, *final_kind; const float* final_gate;

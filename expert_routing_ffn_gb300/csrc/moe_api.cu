@@ -129,6 +129,8 @@ int gemv_grid(const moe_dims* D) {
 
 bool bf16(const moe_dims* D) { return D->wtype == MOE_DTYPE_BF16; }
 
+int tcd_grid() { return sm_count() < kTcdMaxCtas ? sm_count() : kTcdMaxCtas; }
+
 }  // namespace
 
 extern "C" {
@@ -326,8 +328,13 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* final_idx, const int
     a.expert_offsets = expert_offsets; a.perm = perm; a.inv_perm = inv_perm; a.err = err;
     PlanArgs pa;
     pa.expert_offsets = expert_offsets; pa.T = dims->T; pa.N = dims->N; pa.n_shared = dims->n_shared;
-    pa.I = dims->I; pa.I_shared = dims->I_shared; pa.rg = gemv_rows(*dims);
-    pa.G = gemv_grid(dims); pa.max_segs = L.max_segs; pa.max_partial_rows = L.max_partial_rows;
+    pa.I = dims->I; pa.I_shared = dims->I_shared;
+    if (tcd_usable(*dims)) {  // the plan of the decode tensor-core path
+        pa.rg = tcd_rows(dims->T); pa.G = tcd_grid(); pa.p_align = 16;
+    } else {
+        pa.rg = gemv_rows(*dims); pa.G = gemv_grid(dims); pa.p_align = 1;
+    }
+    pa.max_segs = L.max_segs; pa.max_partial_rows = L.max_partial_rows;
     pa.hdr = ws_at<PlanHeader>(ws, L.plan_hdr); pa.segs = ws_at<Seg>(ws, L.segs);
     pa.seg_first = ws_at<int32_t>(ws, L.seg_first); pa.err = err; pa.d = dims->d;
     pa.tc_plan = use_tc(*dims) ? ws_at<TcPlan>(ws, L.tc_plan) : nullptr;
@@ -363,6 +370,26 @@ moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table
         count(3);
         return MOE_OK;
     }
+    if (!floe && tcd_usable(*dims)) {
+        // decode-size batch on the tensor cores (plan built by moe_permute)
+        TcdLaunch t;
+        t.x = x; t.perm = perm; t.expert_offsets = expert_offsets;
+        t.table = static_cast<const ExpertEntry*>(table);
+        t.hdr = ws_at<PlanHeader>(ws, L.plan_hdr); t.segs = ws_at<Seg>(ws, L.segs);
+        t.x_perm = ws_at<void>(ws, L.x_perm); t.partial = ws_at<float>(ws, L.partial);
+        t.T = dims->T; t.d = dims->d; t.N = dims->N; t.k = dims->k; t.rows_cap = dims->T * dims->k;
+        t.nt = tcd_rows(dims->T); t.grid = tcd_grid(); t.err = ws_at<DevError>(ws, L.err);
+        MOE_CUDA(launch_tcd_ffn(t, S(stream)));
+        count(2);
+        GemvReduceArgs r;
+        r.hdr = t.hdr; r.segs = t.segs; r.seg_first = ws_at<int32_t>(ws, L.seg_first);
+        r.expert_offsets = expert_offsets; r.partial = t.partial; r.d = dims->d; r.N = dims->N;
+        r.n_shared = dims->n_shared; r.T = dims->T; r.routed_cap = dims->T * dims->k;
+        r.y_perm = y_perm; r.y_shared = y_shared;
+        MOE_CUDA(launch_gemv_reduce(r, S(stream)));
+        count();
+        return MOE_OK;
+    }
     GemvParams p;
     p.x = x; p.d = dims->d; p.N = dims->N; p.topk = dims->k; p.NS = gemv_stages(dims->d, bf16(dims));
     p.perm = perm; p.table = static_cast<const ExpertEntry*>(table);
@@ -383,7 +410,7 @@ moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table
         PlanArgs pa;
         pa.expert_offsets = expert_offsets; pa.T = dims->T; pa.N = dims->N;
         pa.n_shared = dims->n_shared; pa.I = dims->I; pa.I_shared = dims->I_shared;
-        pa.rg = gemv_rows(*dims); pa.G = gemv_grid(dims); pa.max_segs = L.max_segs;
+        pa.rg = gemv_rows(*dims); pa.G = gemv_grid(dims); pa.p_align = 1; pa.max_segs = L.max_segs;
         pa.max_partial_rows = L.max_partial_rows; pa.d = dims->d;
         pa.hdr = ws_at<PlanHeader>(ws, L.plan_hdr); pa.segs = ws_at<Seg>(ws, L.segs);
         pa.seg_first = ws_at<int32_t>(ws, L.seg_first); pa.err = p.err; pa.tc_plan = nullptr;
@@ -400,6 +427,15 @@ moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table
     MOE_CUDA(launch_gemv_reduce(r, S(stream)));
     count();
     return MOE_OK;
+}
+
+const char* moe_expert_ffn_path(const moe_dims* dims, float keep_frac) {
+    if (!dims || check_dims(dims) != MOE_OK || !(keep_frac > 0.f && keep_frac <= 1.f)) return "unsupported";
+    const bool floe = keep_frac < 1.f;
+    if (floe) return use_tc(*dims) || !bf16(dims) ? "unsupported" : "gemv-floe";
+    if (use_tc(*dims)) return "tc-prefill";
+    if (tcd_usable(*dims)) return "tc-decode";
+    return "gemv";
 }
 
 moe_status moe_floe_kept_mask(const moe_dims* dims, void* ws, size_t ws_bytes, const uint32_t** kept,

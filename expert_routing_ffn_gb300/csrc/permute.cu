@@ -139,7 +139,8 @@ __device__ void build_plan(const PlanArgs& a, const int* off) {
         *a.hdr = h;
     };
     if (n > a.max_segs) { publish_empty(n); return; }
-    const int P = ch > 0 ? (ch + G - 1) / G : 1;
+    const int al = a.p_align > 1 ? a.p_align : 1;
+    const int P = ch > 0 ? ((ch + G - 1) / G + al - 1) / al * al : al;
     int pbase = 0;
     for (int i = 0; i < n; ++i) {
         Seg& s = a.segs[i];

@@ -56,7 +56,16 @@ moe_status encode_expert_tmaps(ExpertEntry& E, int d) {
             s != MOE_OK)
             return s;
     // down: MN-major tiles of 64 hidden values (contiguous) x 64 channels (K)
-    return encode_bf16_2d(E.tmap[2], E.w[2], (uint64_t)d, (uint64_t)E.I, (uint64_t)d * 2, 64, kTcBK);
+    if (moe_status s = encode_bf16_2d(E.tmap[2], E.w[2], (uint64_t)d, (uint64_t)E.I, (uint64_t)d * 2, 64, kTcBK);
+        s != MOE_OK)
+        return s;
+    // decode path: all three in 16-row boxes of 64 values
+    for (int m = 0; m < 3; ++m)
+        if (moe_status s = encode_bf16_2d(E.tmap_dec[m], E.w[m], (uint64_t)d, (uint64_t)E.I,
+                                          (uint64_t)d * 2, kTcBK, 16);
+            s != MOE_OK)
+            return s;
+    return MOE_OK;
 }
 
 }  // namespace moe

@@ -222,12 +222,23 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* final_idx,
  *   y_perm [T*k, d] float32: row pos = the expert output for slot perm[pos]
  *   (ungated); y_shared [T, d] float32 (NULL if n_shared == 0) = sum of the
  *   shared experts' outputs.
- *   Decode-size segments run as an HBM-streaming GEMV, larger ones as a
- *   tcgen05 tensor-core grouped GEMM (bf16 only). */
+ *   Kernels (moe_expert_ffn_path names the choice for a call): batches of
+ *   more than 64 tokens of bf16 layers run as a tcgen05 tensor-core grouped
+ *   GEMM; dense bf16 batches of 4..64 tokens (d a multiple of 128, expert
+ *   widths multiples of 16) as a tcgen05 GEMM with the weight rows on the
+ *   MMA's M side; the rest (1..3 tokens, fp32 layers, FloE) as an
+ *   HBM-streaming CUDA-core GEMV. */
 moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table,
                           const int32_t* expert_offsets, const int32_t* perm, float keep_frac,
                           float* y_perm, float* y_shared, void* ws, size_t ws_bytes,
                           void* stream);
+
+/* Which kernels moe_expert_ffn runs for these dimensions and keep_frac: a
+ * static string, "tc-prefill" (gather + two tensor-core GEMM launches),
+ * "tc-decode" (gather + tensor-core GEMM + partial-row reduction), "gemv"
+ * (CUDA-core GEMV + reduction), "gemv-floe" (FloE preparation + sparse GEMV
+ * + reduction) or "unsupported".  No device work. */
+const char* moe_expert_ffn_path(const moe_dims* dims, float keep_frac);
 
 /* Diagnostic: where the last moe_expert_ffn call with keep_frac < 1 left the
  * FloE kept-channel bitsets inside `ws` (FloE method §1, the mask S_t):

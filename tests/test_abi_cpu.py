@@ -128,3 +128,27 @@ def test_empty_mask_stages_nothing_without_gpu_calls_failing():
     # with nothing to copy only the event record remains; without a GPU it fails as STAGING
     assert st in (moe.MOE_OK, moe.MOE_ERR_STAGING)
     assert n.value == 0
+
+
+def _dims(name, T):
+    c = CONFIGS[name]
+    return moe.make_dims(T, c.d, c.N, c.k, c.I, c.n_shared, c.I_shared, c.r, c.delta_max, c.wtype)
+
+
+@pytest.mark.parametrize("name,T,keep,path", [
+    ("tiny", 16, 1.0, "gemv"),               # fp32 layer: CUDA-core GEMV
+    ("dsv2lite", 1, 1.0, "gemv"),            # 1..3 tokens: CUDA-core GEMV
+    ("dsv2lite", 3, 1.0, "gemv"),
+    ("dsv2lite", 4, 1.0, "tc-decode"),       # 4..64 tokens: tensor-core decode GEMM
+    ("dsv2lite", 8, 1.0, "tc-decode"),
+    ("mixtral", 32, 1.0, "tc-decode"),
+    ("granite", 64, 1.0, "tc-decode"),
+    ("granite", 65, 1.0, "tc-prefill"),      # > 64 tokens: grouped tensor-core GEMM
+    ("qwen2", 4096, 1.0, "tc-prefill"),
+    ("mixtral", 8, 0.1, "gemv-floe"),        # FloE sparsity on the GEMV
+    ("mixtral", 128, 0.1, "unsupported"),    # FloE is decode-only
+    ("tiny", 16, 0.5, "unsupported"),        # ... and bf16-only
+    ("dsv2lite", 8, 0.0, "unsupported"),     # keep_frac outside (0, 1]
+])
+def test_expert_ffn_path_choice(name, T, keep, path):
+    assert moe.moe_expert_ffn_path(_dims(name, T), keep) == path
