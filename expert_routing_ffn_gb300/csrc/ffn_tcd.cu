@@ -174,11 +174,16 @@ __global__ void __launch_bounds__(kTcdThreads, 1) ffn_tcd_kernel(const __grid_co
                             const int st = acquire(2u * rows * 128u + C::kX);
                             if (st < 0) { ok = false; break; }
                             const uint32_t dst = smem_base + st * C::kStage;
-                            for (int j = 0; j < rows / 16; ++j) {
-                                tma_load_2d_hint(dst + j * 2048, E->tmap_dec[0], kc * 64, c0 + t * 128 + j * 16,
-                                                 &full[st], pol_w);
-                                tma_load_2d_hint(dst + kTcdW + j * 2048, E->tmap_dec[1], kc * 64,
-                                                 c0 + t * 128 + j * 16, &full[st], pol_w);
+                            if (rows == 128) {  // whole tile: one 128-row box per matrix
+                                tma_load_2d_hint(dst, E->tmap[0], kc * 64, c0 + t * 128, &full[st], pol_w);
+                                tma_load_2d_hint(dst + kTcdW, E->tmap[1], kc * 64, c0 + t * 128, &full[st], pol_w);
+                            } else {
+                                for (int j = 0; j < rows / 16; ++j) {
+                                    tma_load_2d_hint(dst + j * 2048, E->tmap_dec[0], kc * 64,
+                                                     c0 + t * 128 + j * 16, &full[st], pol_w);
+                                    tma_load_2d_hint(dst + kTcdW + j * 2048, E->tmap_dec[1], kc * 64,
+                                                     c0 + t * 128 + j * 16, &full[st], pol_w);
+                                }
                             }
                             tma_load_2d(dst + 2 * kTcdW, xm, kc * 64, S.row0, &full[st]);
                         }
@@ -190,12 +195,17 @@ __global__ void __launch_bounds__(kTcdThreads, 1) ffn_tcd_kernel(const __grid_co
                             const int st = acquire(2u * rows * 128u);
                             if (st < 0) { ok = false; break; }
                             const uint32_t dst = smem_base + st * C::kStage;
-                            for (int j = 0; j < rows / 16; ++j)
+                            // whole 64-row blocks with the 64-row down map, the rest in 16-row boxes
+                            const int r64 = rows & ~63;
 #pragma unroll
-                                for (int hf = 0; hf < 2; ++hf)
-                                    tma_load_2d_hint(dst + hf * kTcdW + j * 2048, E->tmap_dec[2],
-                                                     dc * 128 + hf * 64, c0 + t * 128 + j * 16, &full[st],
-                                                     pol_w);
+                            for (int hf = 0; hf < 2; ++hf) {
+                                for (int q = 0; q < r64; q += 64)
+                                    tma_load_2d_hint(dst + hf * kTcdW + q * 128, E->tmap[2], dc * 128 + hf * 64,
+                                                     c0 + t * 128 + q, &full[st], pol_w);
+                                for (int q = r64; q < rows; q += 16)
+                                    tma_load_2d_hint(dst + hf * kTcdW + q * 128, E->tmap_dec[2],
+                                                     dc * 128 + hf * 64, c0 + t * 128 + q, &full[st], pol_w);
+                            }
                         }
                     }
                 }

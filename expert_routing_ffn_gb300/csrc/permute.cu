@@ -91,68 +91,185 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
         __threadfence();
         for (int i = tid; i <= N; i += blockDim.x) s_offsets[i] = __ldcg(&expert_offsets[i]);
         __syncthreads();
-        if (tid == 0) {
-            // only the plan of the path moe_expert_ffn will take
-            if (plan.tc_plan) build_tc_plan(plan, s_offsets);
-            else build_plan(plan, s_offsets);
-            *ticket = 0;
+        // only the plan of the path moe_expert_ffn will take
+        if (plan.tc_plan) {
+            if (tid == 0) build_tc_plan(plan, s_offsets);
+        } else {
+            build_plan(plan, s_offsets);
         }
+        if (tid == 0) *ticket = 0;
     }
 }
 
-// FFN plan for the GEMV path (one thread, sequential over segments).
+// Exclusive block-wide scan of one int per thread (blockDim.x a multiple of
+// 32, at most 1024); returns the thread's prefix, *total the block sum.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* total) {
+    __shared__ int warp_sums[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    __syncthreads();  // warp_sums may still be read by a previous call
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += u;
+        }
+        if (lane < nw) warp_sums[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const int before = (warp > 0 ? warp_sums[warp - 1] : 0) + incl - v;
+    *total = warp_sums[nw - 1];
+    return before;
+}
+
+// FFN plan for the GEMV and decode tensor-core paths, built by a whole block
+// (every thread must call it; `off` = expert_offsets[0..N] in shared memory).
 // Segments: shared experts first (rows = tokens, in groups of rg), then each
 // routed expert's permuted rows in groups of rg.  Channels of all segments
-// form one list split evenly over G CTAs; see Seg in common.cuh.
-// `off` holds expert_offsets[0..N] (shared memory).
+// form one list split over G CTAs in ranges of P (a multiple of p_align);
+// see Seg in common.cuh.
 __device__ void build_plan(const PlanArgs& a, const int* off) {
-    const int T = a.T, N = a.N, n_shared = a.n_shared, rg = a.rg, G = a.G;
-    int n = 0, ch = 0;
-    auto add = [&](int expert, int row0, int rows, int Ie) {
-        if (n < a.max_segs) {
-            Seg s;
-            s.expert = expert; s.row0 = row0; s.rows = rows; s.I = Ie; s.ch_start = ch;
-            s.c0 = 0; s.npieces = 0; s.pbase = 0; s.list_off = -1;
-            a.segs[n] = s;
-        }
-        ++n;
-        ch += Ie;
-    };
-    for (int s = 0; s < n_shared; ++s) {
-        a.seg_first[N + s] = n;
-        for (int r = 0; r < T; r += rg) add(N + s, r, min(rg, T - r), a.I_shared);
+    __shared__ int seg_start[kMaxExperts + 9];  // per expert slot: shared s, then routed e
+    __shared__ int s_n;
+    const int T = a.T, N = a.N, ns = a.n_shared, rg = a.rg, G = a.G;
+    const int n_slots = ns + N;
+    const int tid = threadIdx.x;
+    int cnt = 0;
+    if (tid < n_slots) {
+        const int rows = tid < ns ? T : off[tid - ns + 1] - off[tid - ns];
+        cnt = (rows + rg - 1) / rg;
     }
-    for (int e = 0; e < N; ++e) {
-        a.seg_first[e] = n;
-        const int lo = off[e], hi = off[e + 1];
-        for (int r = lo; r < hi; r += rg) add(e, r, min(rg, hi - r), a.I);
-    }
-    a.seg_first[N + n_shared] = n;
+    int tot;
+    const int first = block_exclusive_scan(cnt, &tot);
+    if (tid < n_slots) seg_start[tid] = first;
+    if (tid == 0) { seg_start[n_slots] = tot; s_n = tot; }
+    __syncthreads();
+    const int n = s_n;
     PlanHeader h;
-    h.G = G; h.rg = rg;
+    h.G = G; h.rg = rg; h.n_seg = 0; h.total_ch = 0; h.P = 1; h.n_partial_rows = 0; h.n_routed_rows = 0;
     // A plan that does not fit the workspace is published empty (no segment,
     // no channel, no routed row): the FFN kernels then do nothing, and the
     // error word says why, instead of indexing past the tables.
-    auto publish_empty = [&](int detail) {
-        set_error(a.err, MOE_ERR_CAPACITY, detail);
-        h.n_seg = 0; h.total_ch = 0; h.P = 1; h.n_partial_rows = 0; h.n_routed_rows = 0;
-        *a.hdr = h;
-    };
-    if (n > a.max_segs) { publish_empty(n); return; }
-    const int al = a.p_align > 1 ? a.p_align : 1;
-    const int P = ch > 0 ? ((ch + G - 1) / G + al - 1) / al * al : al;
-    int pbase = 0;
-    for (int i = 0; i < n; ++i) {
-        Seg& s = a.segs[i];
-        s.c0 = s.ch_start / P;
-        s.npieces = (s.ch_start + s.I - 1) / P - s.c0 + 1;
-        s.pbase = pbase;
-        pbase += s.npieces * s.rows;
+    if (n > a.max_segs) {
+        if (tid == 0) { set_error(a.err, MOE_ERR_CAPACITY, n); *a.hdr = h; }
+        return;
     }
-    if (pbase > a.max_partial_rows) { publish_empty(pbase); return; }
-    h.n_seg = n; h.total_ch = ch; h.P = P; h.n_partial_rows = pbase;
-    h.n_routed_rows = off[N];
-    *a.hdr = h;
+    if (tid < n_slots) a.seg_first[tid < ns ? N + tid : tid - ns] = seg_start[tid];
+    if (tid == 0) a.seg_first[N + ns] = n;
+    const int ns_segs = ns > 0 ? seg_start[ns] : 0;  // shared segments come first
+    const int total_ch = ns_segs * a.I_shared + (n - ns_segs) * a.I;
+    const int al = a.p_align > 1 ? a.p_align : 1;
+    const int P = total_ch > 0 ? ((total_ch + G - 1) / G + al - 1) / al * al : al;
+    // one thread per segment (in passes of blockDim.x), partial-row bases by scan
+    int carry = 0;
+    for (int base = 0; base < n; base += blockDim.x) {
+        const int i = base + tid;
+        Seg S;
+        int w = 0;
+        if (i < n) {
+            // expert slot of segment i: the last slot whose first segment is <= i
+            int lo = 0, hi = n_slots - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (seg_start[mid] <= i) lo = mid; else hi = mid - 1;
+            }
+            const int j = i - seg_start[lo];  // segment index within the slot
+            if (lo < ns) {
+                S.expert = N + lo; S.row0 = j * rg; S.rows = min(rg, T - j * rg); S.I = a.I_shared;
+                S.ch_start = i * a.I_shared;
+            } else {
+                const int e = lo - ns;
+                S.expert = e; S.row0 = off[e] + j * rg; S.rows = min(rg, off[e + 1] - S.row0); S.I = a.I;
+                S.ch_start = ns_segs * a.I_shared + (i - ns_segs) * a.I;
+            }
+            S.c0 = S.ch_start / P;
+            S.npieces = (S.ch_start + S.I - 1) / P - S.c0 + 1;
+            S.list_off = -1;
+            w = S.npieces * S.rows;
+        }
+        int tw;
+        const int pb = block_exclusive_scan(w, &tw);
+        if (i < n) {
+            S.pbase = carry + pb;
+            a.segs[i] = S;
+        }
+        carry += tw;
+    }
+    if (tid == 0) {
+        if (carry > a.max_partial_rows) {
+            set_error(a.err, MOE_ERR_CAPACITY, carry);
+            *a.hdr = h;
+            return;
+        }
+        h.n_seg = n; h.total_ch = total_ch; h.P = P; h.n_partial_rows = carry; h.n_routed_rows = off[N];
+        *a.hdr = h;
+    }
+}
+
+// Up to 1024 slots: one block, one thread per slot.  Slots with the same
+// expert in a warp are ranked by __match_any_sync; per-warp counts per expert,
+// scanned over warps and then over experts, give every slot its position
+// (stable in slot order, as in permute_kernel).  The same block then builds
+// the FFN plan.
+__global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __restrict__ final_idx,
+                                                             const int32_t* __restrict__ final_kind,
+                                                             int n_slots, int N,
+                                                             int32_t* __restrict__ expert_offsets,
+                                                             int32_t* __restrict__ perm,
+                                                             int32_t* __restrict__ inv_perm,
+                                                             DevError* __restrict__ err, PlanArgs plan) {
+    __shared__ int cnt[32][kMaxExperts];  // per warp and expert: count, then exclusive prefix over warps
+    __shared__ int s_off[kMaxExperts + 1];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    for (int i = tid; i < 32 * kMaxExperts; i += blockDim.x) (&cnt[0][0])[i] = 0;
+    int key = -1;  // expert of this slot, -1: no computed expert (LoRE, empty, past the end)
+    if (tid < n_slots) {
+        const int x = final_idx[tid];
+        if (x >= N) set_error(err, MOE_ERR_DEVICE_INDEX, tid);
+        if (x >= 0 && x < N && final_kind[tid] != MOE_KIND_LORE) key = x;
+    }
+    __syncthreads();
+    const uint32_t peers = __match_any_sync(0xffffffffu, key);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (key >= 0 && rank == 0) cnt[warp][key] = __popc(peers);
+    __syncthreads();
+    int tot = 0;
+    if (tid < N) {
+        for (int w = 0; w < nw; ++w) {
+            const int c = cnt[w][tid];
+            cnt[w][tid] = tot;
+            tot += c;
+        }
+    }
+    int all;
+    const int first = block_exclusive_scan(tid < N ? tot : 0, &all);
+    if (tid < N) s_off[tid] = first;
+    if (tid == 0) s_off[N] = all;
+    __syncthreads();
+    if (tid <= N) expert_offsets[tid] = s_off[tid];
+    if (tid < n_slots) {
+        if (key >= 0) {
+            const int pos = s_off[key] + cnt[warp][key] + rank;
+            perm[pos] = tid;
+            inv_perm[tid] = pos;
+        } else {
+            inv_perm[tid] = -1;
+        }
+    }
+    // only the plan of the path moe_expert_ffn will take
+    if (plan.tc_plan) {
+        if (tid == 0) build_tc_plan(plan, s_off);
+    } else {
+        build_plan(plan, s_off);
+    }
 }
 
 // Tensor-core plan (see TcPlan): shared-expert group first, then every
@@ -174,22 +291,28 @@ __device__ void build_tc_plan(const PlanArgs& a, const int* off) {
     P.n_seg = n; P.n_tiles1 = t1; P.n_tiles2 = t2;
 }
 
-__global__ void plan_gemv_kernel(PlanArgs a) {
+__global__ void __launch_bounds__(256) plan_gemv_kernel(PlanArgs a) {
     __shared__ int off[kMaxExperts + 1];
     for (int i = threadIdx.x; i <= a.N; i += blockDim.x) off[i] = __ldcg(&a.expert_offsets[i]);
     __syncthreads();
-    if (threadIdx.x == 0) build_plan(a, off);
+    build_plan(a, off);
 }
 
 cudaError_t launch_permute(const PermuteArgs& a, const PlanArgs& plan, int* ticket,
                            cudaStream_t st) {
+    if (a.n_slots <= 1024) {
+        const int threads = a.n_slots <= 256 ? 256 : 1024;
+        permute_small_kernel<<<1, threads, 0, st>>>(a.final_idx, a.final_kind, a.n_slots, a.N,
+                                                   a.expert_offsets, a.perm, a.inv_perm, a.err, plan);
+        return cudaGetLastError();
+    }
     permute_kernel<<<a.N, 1024, 0, st>>>(a.final_idx, a.final_kind, a.n_slots, a.N,
                                          a.expert_offsets, a.perm, a.inv_perm, a.err, plan, ticket);
     return cudaGetLastError();
 }
 
 cudaError_t launch_plan_gemv(const PlanArgs& a, cudaStream_t st) {
-    plan_gemv_kernel<<<1, 32, 0, st>>>(a);
+    plan_gemv_kernel<<<1, 256, 0, st>>>(a);
     return cudaGetLastError();
 }
 
