@@ -56,6 +56,23 @@ struct PlanArgs {
 };
 // permutation + FFN plan in one launch (the last block builds the plan)
 cudaError_t launch_permute(const PermuteArgs& a, const PlanArgs& plan, int* ticket, cudaStream_t st);
+
+// The routing front end of a small batch (T * k <= kFrontMaxSlots) in one
+// launch: the blocks compute the router / prefetch logits, the last block to
+// finish runs selection, the batch resident set (n_resident > 0), miss
+// handling (zeroing counters and fetch mask first) and the permutation with
+// the FFN plan, with the same device code as the stage-wise kernels.
+constexpr int kFrontMaxSlots = 256;
+struct FrontArgs {
+    LogitsArgs la;
+    RouteSelectArgs ra;
+    int n_resident; uint64_t* batch_resident;
+    SelectArgs sa;
+    PermuteArgs pa;
+    PlanArgs plan;
+    int* ticket;
+};
+cudaError_t launch_route_front(const FrontArgs& a, cudaStream_t st);
 // the FFN plan alone
 cudaError_t launch_plan_gemv(const PlanArgs& a, cudaStream_t st);
 
@@ -121,6 +138,19 @@ struct LoreArgs {
     const void *A, *B; int T, d, k, r, N; bool bf16; float* z; float* y_lore; DevError* err;
 };
 cudaError_t launch_lore(const LoreArgs& a, cudaStream_t st);
+// z = g A_e x only (the first half of launch_lore)
+cudaError_t launch_lore_z(const LoreArgs& a, cudaStream_t st);
+
+struct EpilogueArgs {
+    const PlanHeader* hdr; const Seg* segs; const int32_t* seg_first; const int32_t* expert_offsets;
+    const float* partial;
+    const int32_t *inv_perm, *final_idx, *final_kind; const float* final_gate;
+    const float* z; const void* lore_b;  // lore_b NULL: no LoRE term
+    int T, d, N, k, r, n_shared; bool bf16;
+    float *y_perm, *y_shared, *y_lore, *out;
+};
+// partial-row reduction + LoRE B + combine in one launch (moe_layer_forward)
+cudaError_t launch_layer_epilogue(const EpilogueArgs& a, cudaStream_t st);
 
 struct CombineArgs {
     const float* y_perm; const int32_t* inv_perm; const float* final_gate;

@@ -144,6 +144,151 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     }
 }
 
+// moe_layer_forward's tail when the expert FFN left per-CTA partial rows
+// (GEMV and decode tensor-core paths).  Block = token t x 128 columns of d;
+// lane = 4 columns.  Warp w sums the partial rows of the slots s = w, w + 8,
+// ... (one y_perm row each) and warp 7 also those of the shared experts
+// (y_shared); the LoRE term (B rows times z) is formed by warp 0 after them;
+// warp 0 then combines in slot order and writes out.  Every sum runs in the
+// order of the separate kernels (gemv_reduce_kernel, lore_b_kernel,
+// combine_kernel), so the result is bitwise the one of the stage-wise calls.
+template <typename W>
+__global__ void __launch_bounds__(256) layer_epilogue_kernel(const EpilogueArgs a) {
+    const int t = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int q = blockIdx.y * 32 + lane;  // float4 column group
+    const int k = a.k, r = a.r, d = a.d, N = a.N;
+    __shared__ int s_pos[kMaxTopK], s_e[kMaxTopK], s_lore[kMaxTopK];
+    __shared__ float s_g[kMaxTopK];
+    __shared__ float s_lg;
+    __shared__ int s_nl;
+    __shared__ float s_z[kMaxTopK * 64];
+    __shared__ float4 s_y[kMaxTopK][32];
+    __shared__ float4 s_sh[32];
+    if (threadIdx.x == 0) {
+        float lg = 0.f;
+        int nl = 0;
+        for (int s = 0; s < k; ++s) {
+            const size_t sl = (size_t)t * k + s;
+            s_pos[s] = a.inv_perm[sl];
+            s_g[s] = a.final_gate[sl];
+            s_e[s] = a.final_idx[sl];
+            if (a.final_kind[sl] == MOE_KIND_LORE) {
+                lg += a.final_gate[sl];
+                const int e = a.final_idx[sl];
+                if (a.lore_b && e >= 0 && e < N) s_lore[nl++] = s;
+            }
+        }
+        s_lg = lg;
+        s_nl = nl;
+    }
+    __syncthreads();
+    const int nl = s_nl;
+    for (int i = threadIdx.x; i < nl * r; i += blockDim.x)
+        s_z[i] = a.z[((size_t)t * k + s_lore[i / r]) * r + (i % r)];
+    const bool col_ok = q < d / 4;
+    const PlanHeader hdr = *a.hdr;
+    const int rg = hdr.rg;
+    // sum of the pieces of segment si, row `row` (in piece order)
+    auto add_pieces = [&](float4& acc, int si, int row) {
+        if (si < 0 || si >= hdr.n_seg) return;
+        const Seg S = a.segs[si];
+        if (S.pbase + (S.npieces - 1) * S.rows + row >= hdr.n_partial_rows) return;
+        const float* base = a.partial + (size_t)(S.pbase + row) * d;
+        const size_t step = (size_t)S.rows * d;
+        int pc = 0;
+        for (; pc + 4 <= S.npieces; pc += 4) {  // four loads in flight, added in order
+            const float4 v0 = reinterpret_cast<const float4*>(base + (pc + 0) * step)[q];
+            const float4 v1 = reinterpret_cast<const float4*>(base + (pc + 1) * step)[q];
+            const float4 v2 = reinterpret_cast<const float4*>(base + (pc + 2) * step)[q];
+            const float4 v3 = reinterpret_cast<const float4*>(base + (pc + 3) * step)[q];
+            acc.x += v0.x; acc.y += v0.y; acc.z += v0.z; acc.w += v0.w;
+            acc.x += v1.x; acc.y += v1.y; acc.z += v1.z; acc.w += v1.w;
+            acc.x += v2.x; acc.y += v2.y; acc.z += v2.z; acc.w += v2.w;
+            acc.x += v3.x; acc.y += v3.y; acc.z += v3.z; acc.w += v3.w;
+        }
+        for (; pc < S.npieces; ++pc) {
+            const float4 v = reinterpret_cast<const float4*>(base + pc * step)[q];
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+    };
+    if (col_ok) {
+        for (int s = warp; s < k; s += 8) {
+            const int pos = s_pos[s];
+            if (pos < 0) continue;
+            float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+            const int e = s_e[s];
+            if (e >= 0 && e < N && pos < hdr.n_routed_rows) {
+                const int local = pos - a.expert_offsets[e];
+                add_pieces(y, a.seg_first[e] + local / rg, local % rg);
+            }
+            reinterpret_cast<float4*>(a.y_perm + (size_t)pos * d)[q] = y;
+            s_y[s][lane] = y;
+        }
+        if (warp == 7 && a.n_shared > 0) {
+            float4 sh = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s = 0; s < a.n_shared; ++s) add_pieces(sh, a.seg_first[N + s] + t / rg, t % rg);
+            reinterpret_cast<float4*>(a.y_shared + (size_t)t * d)[q] = sh;
+            s_sh[lane] = sh;
+        }
+    }
+    __syncthreads();
+    if (warp != 0 || !col_ok) return;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (a.n_shared > 0) {
+        const float4 sh = s_sh[lane];
+        const float scale = 1.f + s_lg;
+        acc.x = sh.x * scale; acc.y = sh.y * scale; acc.z = sh.z * scale; acc.w = sh.w * scale;
+    }
+    for (int s = 0; s < k; ++s) {
+        if (s_pos[s] < 0) continue;
+        const float4 y = s_y[s][lane];
+        const float g = s_g[s];
+        acc.x = fmaf(g, y.x, acc.x); acc.y = fmaf(g, y.y, acc.y);
+        acc.z = fmaf(g, y.z, acc.z); acc.w = fmaf(g, y.w, acc.w);
+    }
+    if (a.lore_b) {
+        float yl[4] = {0.f, 0.f, 0.f, 0.f};
+        const W* B = static_cast<const W*>(a.lore_b);
+        for (int i = 0; i < nl; ++i) {
+            const int e = s_e[s_lore[i]];
+            const float* zz = s_z + i * r;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const W* brow = B + ((size_t)e * d + q * 4 + c) * r;
+                float accl = yl[c];
+                for (int qq = 0; qq < r; ++qq) accl = fmaf(to_f32(brow[qq]), zz[qq], accl);
+                yl[c] = accl;
+            }
+        }
+        reinterpret_cast<float4*>(a.y_lore + (size_t)t * d)[q] = make_float4(yl[0], yl[1], yl[2], yl[3]);
+        acc.x += yl[0]; acc.y += yl[1]; acc.z += yl[2]; acc.w += yl[3];
+    }
+    reinterpret_cast<float4*>(a.out + (size_t)t * d)[q] = acc;
+}
+
+cudaError_t launch_layer_epilogue(const EpilogueArgs& a, cudaStream_t st) {
+    if (a.T == 0) return cudaSuccess;
+    dim3 grid(a.T, (a.d / 4 + 31) / 32);
+    if (a.bf16) layer_epilogue_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(a);
+    else layer_epilogue_kernel<float><<<grid, 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_lore_z(const LoreArgs& a, cudaStream_t st) {
+    if (a.T == 0) return cudaSuccess;
+    dim3 gz(a.T * a.k, (a.r + 3) / 4);
+    if (a.bf16)
+        lore_z_kernel<__nv_bfloat16><<<gz, 128, 0, st>>>(
+            (const __nv_bfloat16*)a.x, a.final_idx, a.final_kind, a.final_gate,
+            (const __nv_bfloat16*)a.A, a.d, a.k, a.r, a.N, a.z, a.err);
+    else
+        lore_z_kernel<float><<<gz, 128, 0, st>>>((const float*)a.x, a.final_idx, a.final_kind,
+                                                      a.final_gate, (const float*)a.A, a.d, a.k,
+                                                      a.r, a.N, a.z, a.err);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_lore(const LoreArgs& a, cudaStream_t st) {
     if (a.T == 0) return cudaSuccess;
     const int n_slots = a.T * a.k;

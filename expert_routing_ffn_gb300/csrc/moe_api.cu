@@ -131,6 +131,76 @@ bool bf16(const moe_dims* D) { return D->wtype == MOE_DTYPE_BF16; }
 
 int tcd_grid() { return sm_count() < kTcdMaxCtas ? sm_count() : kTcdMaxCtas; }
 
+// Argument checks and launch arguments of the routing stages (T > 0), shared
+// by the stage-wise calls and the fused front end of moe_layer_forward.
+moe_status prep_route(const moe_dims* dims, const void* x, const void* w_router, const float* router_bias,
+                      const void* x_pre, const void* w_prefetch, const float* w_ord, const float* theta,
+                      float tau, int n_resident, int32_t* topk_idx, float* topk_gate, float* router_prob,
+                      int32_t* delta_hat, uint64_t* prefetch_mask, int32_t* delta_star,
+                      uint64_t* batch_resident, void* ws, LogitsArgs& la, RouteSelectArgs& ra) {
+    if (!x || !w_router || !topk_idx || !topk_gate || !router_prob || !delta_hat || !prefetch_mask)
+        return MOE_ERR_INVALID_ARG;
+    const bool has_pref = w_prefetch != nullptr;
+    if (has_pref && (!w_ord || !theta || !(tau > 0.f && tau < 1.f))) return MOE_ERR_INVALID_ARG;
+    if (n_resident > 0 && (!has_pref || !batch_resident || n_resident > dims->N)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_router) || (x_pre && !aligned16(x_pre)) ||
+        (w_prefetch && !aligned16(w_prefetch)))
+        return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(*dims);
+    la.x = x; la.x_pre = x_pre; la.w_router = w_router; la.w_prefetch = w_prefetch;
+    la.bias = router_bias; la.w_ord = w_ord; la.T = dims->T; la.d = dims->d; la.N = dims->N;
+    la.has_prefetch = has_pref; la.bf16 = bf16(dims);
+    la.logits_r = ws_at<float>(ws, L.logits_r); la.logits_p = ws_at<float>(ws, L.logits_p);
+    la.score = ws_at<float>(ws, L.score);
+    ra.logits_r = la.logits_r; ra.logits_p = la.logits_p; ra.score = la.score; ra.theta = theta;
+    ra.logit_tau = has_pref ? (float)std::log((double)tau / (1.0 - (double)tau)) : 0.f;
+    ra.T = dims->T; ra.N = dims->N; ra.k = dims->k; ra.delta_max = dims->delta_max;
+    ra.has_prefetch = has_pref; ra.topk_idx = topk_idx; ra.topk_gate = topk_gate;
+    ra.router_prob = router_prob; ra.delta_hat = delta_hat; ra.prefetch_mask = prefetch_mask;
+    ra.delta_star = delta_star; ra.qp = n_resident > 0 ? ws_at<float>(ws, L.qp) : nullptr;
+    return MOE_OK;
+}
+
+moe_status prep_select(const moe_dims* dims, const float* router_prob, const int32_t* topk_idx,
+                       const uint64_t* prefetch_mask, const uint64_t* resident, int policy, float gamma,
+                       const int32_t* delta_hat, const int32_t* delta_star, int32_t* final_idx,
+                       float* final_gate, int32_t* final_kind, uint64_t* fetch_mask, int32_t* counters,
+                       void* ws, SelectArgs& a) {
+    if (policy < MOE_MISS_EXACT || policy > MOE_MISS_HYBRID) return MOE_ERR_INVALID_ARG;
+    if ((policy == MOE_MISS_LORE || policy == MOE_MISS_HYBRID) && dims->r <= 0) return MOE_ERR_INVALID_ARG;
+    if (!router_prob || !topk_idx || !final_idx || !final_gate || !final_kind) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(*dims);
+    a.router_prob = router_prob; a.topk_idx = topk_idx; a.prefetch_mask = prefetch_mask;
+    a.resident = resident; a.policy = policy; a.gamma = gamma; a.delta_hat = delta_hat;
+    a.delta_star = delta_star; a.T = dims->T; a.N = dims->N; a.k = dims->k;
+    a.renorm = dims->renorm_topk; a.final_idx = final_idx; a.final_gate = final_gate;
+    a.final_kind = final_kind; a.fetch_mask = fetch_mask; a.counters = counters;
+    a.err = ws_at<DevError>(ws, L.err);
+    return MOE_OK;
+}
+
+moe_status prep_permute(const moe_dims* dims, const int32_t* final_idx, const int32_t* final_kind,
+                        int32_t* expert_offsets, int32_t* perm, int32_t* inv_perm, void* ws, PermuteArgs& a,
+                        PlanArgs& pa) {
+    if (!expert_offsets || !final_idx || !final_kind || !perm || !inv_perm) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(*dims);
+    DevError* err = ws_at<DevError>(ws, L.err);
+    a.final_idx = final_idx; a.final_kind = final_kind; a.n_slots = dims->T * dims->k; a.N = dims->N;
+    a.expert_offsets = expert_offsets; a.perm = perm; a.inv_perm = inv_perm; a.err = err;
+    pa.expert_offsets = expert_offsets; pa.T = dims->T; pa.N = dims->N; pa.n_shared = dims->n_shared;
+    pa.I = dims->I; pa.I_shared = dims->I_shared;
+    if (tcd_usable(*dims)) {  // the plan of the decode tensor-core path
+        pa.rg = tcd_rows(dims->T); pa.G = tcd_grid(); pa.p_align = 16;
+    } else {
+        pa.rg = gemv_rows(*dims); pa.G = gemv_grid(dims); pa.p_align = 1;
+    }
+    pa.max_segs = L.max_segs; pa.max_partial_rows = L.max_partial_rows;
+    pa.hdr = ws_at<PlanHeader>(ws, L.plan_hdr); pa.segs = ws_at<Seg>(ws, L.segs);
+    pa.seg_first = ws_at<int32_t>(ws, L.seg_first); pa.err = err; pa.d = dims->d;
+    pa.tc_plan = use_tc(*dims) ? ws_at<TcPlan>(ws, L.tc_plan) : nullptr;
+    return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -209,30 +279,13 @@ moe_status moe_route(const moe_dims* dims, const void* x, const void* w_router,
     MOE_TRY(check_dims(dims));
     MOE_TRY(check_ws(dims, ws, ws_bytes));
     if (dims->T == 0) return MOE_OK;  // empty batch: nothing to do, buffers may be empty
-    if (!x || !w_router || !topk_idx || !topk_gate || !router_prob || !delta_hat || !prefetch_mask)
-        return MOE_ERR_INVALID_ARG;
-    const bool has_pref = w_prefetch != nullptr;
-    if (has_pref && (!w_ord || !theta || !(tau > 0.f && tau < 1.f))) return MOE_ERR_INVALID_ARG;
-    if (n_resident > 0 && (!has_pref || !batch_resident || n_resident > dims->N)) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(w_router) || (x_pre && !aligned16(x_pre)) ||
-        (w_prefetch && !aligned16(w_prefetch)))
-        return MOE_ERR_INVALID_ARG;
-    const WsLayout L = ws_layout(*dims);
     LogitsArgs la;
-    la.x = x; la.x_pre = x_pre; la.w_router = w_router; la.w_prefetch = w_prefetch;
-    la.bias = router_bias; la.w_ord = w_ord; la.T = dims->T; la.d = dims->d; la.N = dims->N;
-    la.has_prefetch = has_pref; la.bf16 = bf16(dims);
-    la.logits_r = ws_at<float>(ws, L.logits_r); la.logits_p = ws_at<float>(ws, L.logits_p);
-    la.score = ws_at<float>(ws, L.score);
+    RouteSelectArgs ra;
+    MOE_TRY(prep_route(dims, x, w_router, router_bias, x_pre, w_prefetch, w_ord, theta, tau, n_resident,
+                       topk_idx, topk_gate, router_prob, delta_hat, prefetch_mask, delta_star, batch_resident,
+                       ws, la, ra));
     MOE_CUDA(launch_logits(la, S(stream)));
     count();
-    RouteSelectArgs ra;
-    ra.logits_r = la.logits_r; ra.logits_p = la.logits_p; ra.score = la.score; ra.theta = theta;
-    ra.logit_tau = has_pref ? (float)std::log((double)tau / (1.0 - (double)tau)) : 0.f;
-    ra.T = dims->T; ra.N = dims->N; ra.k = dims->k; ra.delta_max = dims->delta_max;
-    ra.has_prefetch = has_pref; ra.topk_idx = topk_idx; ra.topk_gate = topk_gate;
-    ra.router_prob = router_prob; ra.delta_hat = delta_hat; ra.prefetch_mask = prefetch_mask;
-    ra.delta_star = delta_star; ra.qp = n_resident > 0 ? ws_at<float>(ws, L.qp) : nullptr;
     MOE_CUDA(launch_route_select(ra, S(stream)));
     count();
     if (n_resident > 0) {
@@ -253,18 +306,12 @@ moe_status moe_select_resident(const moe_dims* dims, const float* router_prob,
     MOE_TRY(check_ws(dims, ws, ws_bytes));
     if (policy < MOE_MISS_EXACT || policy > MOE_MISS_HYBRID) return MOE_ERR_INVALID_ARG;
     if ((policy == MOE_MISS_LORE || policy == MOE_MISS_HYBRID) && dims->r <= 0) return MOE_ERR_INVALID_ARG;
-    const WsLayout L = ws_layout(*dims);
     if (counters) MOE_CUDA(cudaMemsetAsync(counters, 0, MOE_NUM_COUNTERS * sizeof(int32_t), S(stream)));
     if (fetch_mask) MOE_CUDA(cudaMemsetAsync(fetch_mask, 0, sizeof(uint64_t), S(stream)));
     if (dims->T == 0) return MOE_OK;
-    if (!router_prob || !topk_idx || !final_idx || !final_gate || !final_kind) return MOE_ERR_INVALID_ARG;
     SelectArgs a;
-    a.router_prob = router_prob; a.topk_idx = topk_idx; a.prefetch_mask = prefetch_mask;
-    a.resident = resident; a.policy = policy; a.gamma = gamma; a.delta_hat = delta_hat;
-    a.delta_star = delta_star; a.T = dims->T; a.N = dims->N; a.k = dims->k;
-    a.renorm = dims->renorm_topk; a.final_idx = final_idx; a.final_gate = final_gate;
-    a.final_kind = final_kind; a.fetch_mask = fetch_mask; a.counters = counters;
-    a.err = ws_at<DevError>(ws, L.err);
+    MOE_TRY(prep_select(dims, router_prob, topk_idx, prefetch_mask, resident, policy, gamma, delta_hat,
+                        delta_star, final_idx, final_gate, final_kind, fetch_mask, counters, ws, a));
     MOE_CUDA(launch_select_resident(a, S(stream)));
     count();
     return MOE_OK;
@@ -320,32 +367,26 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* final_idx, const int
         MOE_CUDA(cudaMemsetAsync(expert_offsets, 0, (dims->N + 1) * sizeof(int32_t), S(stream)));
         return MOE_OK;
     }
-    if (!final_idx || !final_kind || !perm || !inv_perm) return MOE_ERR_INVALID_ARG;
-    const WsLayout L = ws_layout(*dims);
-    DevError* err = ws_at<DevError>(ws, L.err);
     PermuteArgs a;
-    a.final_idx = final_idx; a.final_kind = final_kind; a.n_slots = dims->T * dims->k; a.N = dims->N;
-    a.expert_offsets = expert_offsets; a.perm = perm; a.inv_perm = inv_perm; a.err = err;
     PlanArgs pa;
-    pa.expert_offsets = expert_offsets; pa.T = dims->T; pa.N = dims->N; pa.n_shared = dims->n_shared;
-    pa.I = dims->I; pa.I_shared = dims->I_shared;
-    if (tcd_usable(*dims)) {  // the plan of the decode tensor-core path
-        pa.rg = tcd_rows(dims->T); pa.G = tcd_grid(); pa.p_align = 16;
-    } else {
-        pa.rg = gemv_rows(*dims); pa.G = gemv_grid(dims); pa.p_align = 1;
-    }
-    pa.max_segs = L.max_segs; pa.max_partial_rows = L.max_partial_rows;
-    pa.hdr = ws_at<PlanHeader>(ws, L.plan_hdr); pa.segs = ws_at<Seg>(ws, L.segs);
-    pa.seg_first = ws_at<int32_t>(ws, L.seg_first); pa.err = err; pa.d = dims->d;
-    pa.tc_plan = use_tc(*dims) ? ws_at<TcPlan>(ws, L.tc_plan) : nullptr;
+    MOE_TRY(prep_permute(dims, final_idx, final_kind, expert_offsets, perm, inv_perm, ws, a, pa));
+    const WsLayout L = ws_layout(*dims);
     MOE_CUDA(launch_permute(a, pa, ws_at<int>(ws, L.ticket), S(stream)));
     count();
     return MOE_OK;
 }
 
-moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table,
-                          const int32_t* expert_offsets, const int32_t* perm, float keep_frac,
-                          float* y_perm, float* y_shared, void* ws, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The expert FFN; reduce = false leaves the partial rows of the GEMV and
+// decode tensor-core paths unsummed (moe_layer_forward's fused epilogue sums
+// them).  The tensor-core prefill path writes y_perm / y_shared directly.
+moe_status expert_ffn_impl(const moe_dims* dims, const void* x, const void* table,
+                           const int32_t* expert_offsets, const int32_t* perm, float keep_frac,
+                           float* y_perm, float* y_shared, void* ws, size_t ws_bytes, void* stream,
+                           bool reduce) {
     MOE_TRY(check_dims(dims));
     MOE_TRY(check_ws(dims, ws, ws_bytes));
     if (!(keep_frac > 0.f && keep_frac <= 1.f)) return MOE_ERR_INVALID_ARG;
@@ -381,6 +422,7 @@ moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table
         t.nt = tcd_rows(dims->T); t.grid = tcd_grid(); t.err = ws_at<DevError>(ws, L.err);
         MOE_CUDA(launch_tcd_ffn(t, S(stream)));
         count(2);
+        if (!reduce) return MOE_OK;
         GemvReduceArgs r;
         r.hdr = t.hdr; r.segs = t.segs; r.seg_first = ws_at<int32_t>(ws, L.seg_first);
         r.expert_offsets = expert_offsets; r.partial = t.partial; r.d = dims->d; r.N = dims->N;
@@ -419,6 +461,7 @@ moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table
     }
     MOE_CUDA(launch_gemv(p, gemv_grid(dims), bf16(dims), S(stream), floe));
     count();
+    if (!reduce) return MOE_OK;
     GemvReduceArgs r;
     r.hdr = p.hdr; r.segs = p.segs; r.seg_first = ws_at<int32_t>(ws, L.seg_first);
     r.expert_offsets = expert_offsets; r.partial = p.partial; r.d = dims->d; r.N = dims->N;
@@ -427,6 +470,17 @@ moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table
     MOE_CUDA(launch_gemv_reduce(r, S(stream)));
     count();
     return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table,
+                          const int32_t* expert_offsets, const int32_t* perm, float keep_frac,
+                          float* y_perm, float* y_shared, void* ws, size_t ws_bytes, void* stream) {
+    return expert_ffn_impl(dims, x, table, expert_offsets, perm, keep_frac, y_perm, y_shared, ws, ws_bytes,
+                           stream, true);
 }
 
 const char* moe_expert_ffn_path(const moe_dims* dims, float keep_frac) {
@@ -488,21 +542,70 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_layer_args* A,
                              const moe_layer_outputs* O, void* ws, size_t ws_bytes, void* stream) {
     MOE_TRY(check_dims(dims));
     if (!A || !O) return MOE_ERR_INVALID_ARG;
-    MOE_TRY(moe_route(dims, A->x, A->w_router, A->router_bias, A->x_pre, A->w_prefetch, A->w_ord,
-                      A->theta, A->tau, A->n_resident, O->topk_idx, O->topk_gate, O->router_prob,
-                      O->delta_hat, O->prefetch_mask, O->delta_star, O->batch_resident, ws,
-                      ws_bytes, stream));
     const uint64_t* resident = A->n_resident > 0 ? O->batch_resident : A->resident;
-    MOE_TRY(moe_select_resident(dims, O->router_prob, O->topk_idx,
-                                A->use_prefetch_mask ? O->prefetch_mask : nullptr, resident,
-                                A->policy, A->gamma, O->delta_hat, O->delta_star, O->final_idx,
-                                O->final_gate, O->final_kind, O->fetch_mask, O->counters, ws,
-                                ws_bytes, stream));
-    MOE_TRY(moe_permute(dims, O->final_idx, O->final_kind, O->expert_offsets, O->perm, O->inv_perm,
-                        ws, ws_bytes, stream));
+    const uint64_t* pref_mask = A->use_prefetch_mask ? O->prefetch_mask : nullptr;
+    if (dims->T > 0 && dims->T * dims->k <= kFrontMaxSlots) {
+        // small batch: routing, selection, resident set, misses and the
+        // permutation in one launch (same device code as the stage-wise calls)
+        MOE_TRY(check_ws(dims, ws, ws_bytes));
+        FrontArgs f;
+        MOE_TRY(prep_route(dims, A->x, A->w_router, A->router_bias, A->x_pre, A->w_prefetch, A->w_ord,
+                           A->theta, A->tau, A->n_resident, O->topk_idx, O->topk_gate, O->router_prob,
+                           O->delta_hat, O->prefetch_mask, O->delta_star, O->batch_resident, ws, f.la, f.ra));
+        MOE_TRY(prep_select(dims, O->router_prob, O->topk_idx, pref_mask, resident, A->policy, A->gamma,
+                            O->delta_hat, O->delta_star, O->final_idx, O->final_gate, O->final_kind,
+                            O->fetch_mask, O->counters, ws, f.sa));
+        MOE_TRY(prep_permute(dims, O->final_idx, O->final_kind, O->expert_offsets, O->perm, O->inv_perm, ws,
+                             f.pa, f.plan));
+        f.n_resident = A->n_resident; f.batch_resident = O->batch_resident;
+        f.ticket = ws_at<int>(ws, ws_layout(*dims).ticket) + 1;
+        MOE_CUDA(launch_route_front(f, S(stream)));
+        count();
+    } else {
+        MOE_TRY(moe_route(dims, A->x, A->w_router, A->router_bias, A->x_pre, A->w_prefetch, A->w_ord,
+                          A->theta, A->tau, A->n_resident, O->topk_idx, O->topk_gate, O->router_prob,
+                          O->delta_hat, O->prefetch_mask, O->delta_star, O->batch_resident, ws,
+                          ws_bytes, stream));
+        MOE_TRY(moe_select_resident(dims, O->router_prob, O->topk_idx, pref_mask, resident,
+                                    A->policy, A->gamma, O->delta_hat, O->delta_star, O->final_idx,
+                                    O->final_gate, O->final_kind, O->fetch_mask, O->counters, ws,
+                                    ws_bytes, stream));
+        MOE_TRY(moe_permute(dims, O->final_idx, O->final_kind, O->expert_offsets, O->perm, O->inv_perm,
+                            ws, ws_bytes, stream));
+    }
+    const bool lore = dims->r > 0 && A->lore_a && A->lore_b && O->y_lore;
+    if (!use_tc(*dims) && dims->T > 0) {
+        // partial-row paths: FFN without its reduction, LoRE z, then one
+        // launch for reduction + LoRE B + combine
+        MOE_TRY(expert_ffn_impl(dims, A->x, A->table, O->expert_offsets, O->perm, A->keep_frac, O->y_perm,
+                                O->y_shared, ws, ws_bytes, stream, false));
+        const WsLayout L = ws_layout(*dims);
+        if (lore) {
+            LoreArgs la;
+            la.x = A->x; la.final_idx = O->final_idx; la.final_kind = O->final_kind;
+            la.final_gate = O->final_gate; la.A = A->lore_a; la.B = A->lore_b; la.T = dims->T; la.d = dims->d;
+            la.k = dims->k; la.r = dims->r; la.N = dims->N; la.bf16 = bf16(dims);
+            la.z = ws_at<float>(ws, L.lore_z); la.y_lore = O->y_lore; la.err = ws_at<DevError>(ws, L.err);
+            MOE_CUDA(launch_lore_z(la, S(stream)));
+            count();
+        }
+        EpilogueArgs ea;
+        ea.hdr = ws_at<PlanHeader>(ws, L.plan_hdr); ea.segs = ws_at<Seg>(ws, L.segs);
+        ea.seg_first = ws_at<int32_t>(ws, L.seg_first); ea.expert_offsets = O->expert_offsets;
+        ea.partial = ws_at<float>(ws, L.partial);
+        ea.inv_perm = O->inv_perm; ea.final_idx = O->final_idx; ea.final_kind = O->final_kind;
+        ea.final_gate = O->final_gate; ea.z = ws_at<float>(ws, L.lore_z); ea.lore_b = lore ? A->lore_b : nullptr;
+        ea.T = dims->T; ea.d = dims->d; ea.N = dims->N; ea.k = dims->k; ea.r = dims->r;
+        ea.n_shared = dims->n_shared; ea.bf16 = bf16(dims);
+        ea.y_perm = O->y_perm; ea.y_shared = O->y_shared; ea.y_lore = O->y_lore; ea.out = O->out;
+        if (!ea.out || !ea.y_perm || !O->inv_perm || (dims->n_shared > 0 && !ea.y_shared))
+            return MOE_ERR_INVALID_ARG;
+        MOE_CUDA(launch_layer_epilogue(ea, S(stream)));
+        count();
+        return MOE_OK;
+    }
     MOE_TRY(moe_expert_ffn(dims, A->x, A->table, O->expert_offsets, O->perm, A->keep_frac,
                            O->y_perm, O->y_shared, ws, ws_bytes, stream));
-    const bool lore = dims->r > 0 && A->lore_a && A->lore_b && O->y_lore;
     if (lore)
         MOE_TRY(moe_lore(dims, A->x, O->final_idx, O->final_kind, O->final_gate, A->lore_a,
                          A->lore_b, O->y_lore, ws, ws_bytes, stream));

@@ -5,11 +5,10 @@
 // that each expert's weights are streamed once for all of its tokens.
 #include "common.cuh"
 #include "kernels.h"
+#include "plan.cuh"
 
 namespace moe {
 
-__device__ void build_plan(const PlanArgs& a, const int* off);
-__device__ void build_tc_plan(const PlanArgs& a, const int* off);
 
 // One block per expert e.  Pass 1 counts the slots routed to experts below e
 // (the segment offset) and to e; pass 2 walks the slots in order and
@@ -101,124 +100,6 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
     }
 }
 
-// Exclusive block-wide scan of one int per thread (blockDim.x a multiple of
-// 32, at most 1024); returns the thread's prefix, *total the block sum.
-__device__ __forceinline__ int block_exclusive_scan(int v, int* total) {
-    __shared__ int warp_sums[32];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += u;
-    }
-    __syncthreads();  // warp_sums may still be read by a previous call
-    if (lane == 31) warp_sums[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        int w = lane < nw ? warp_sums[lane] : 0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int u = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += u;
-        }
-        if (lane < nw) warp_sums[lane] = w;  // inclusive over warps
-    }
-    __syncthreads();
-    const int before = (warp > 0 ? warp_sums[warp - 1] : 0) + incl - v;
-    *total = warp_sums[nw - 1];
-    return before;
-}
-
-// FFN plan for the GEMV and decode tensor-core paths, built by a whole block
-// (every thread must call it; `off` = expert_offsets[0..N] in shared memory).
-// Segments: shared experts first (rows = tokens, in groups of rg), then each
-// routed expert's permuted rows in groups of rg.  Channels of all segments
-// form one list split over G CTAs in ranges of P (a multiple of p_align);
-// see Seg in common.cuh.
-__device__ void build_plan(const PlanArgs& a, const int* off) {
-    __shared__ int seg_start[kMaxExperts + 9];  // per expert slot: shared s, then routed e
-    __shared__ int s_n;
-    const int T = a.T, N = a.N, ns = a.n_shared, rg = a.rg, G = a.G;
-    const int n_slots = ns + N;
-    const int tid = threadIdx.x;
-    int cnt = 0;
-    if (tid < n_slots) {
-        const int rows = tid < ns ? T : off[tid - ns + 1] - off[tid - ns];
-        cnt = (rows + rg - 1) / rg;
-    }
-    int tot;
-    const int first = block_exclusive_scan(cnt, &tot);
-    if (tid < n_slots) seg_start[tid] = first;
-    if (tid == 0) { seg_start[n_slots] = tot; s_n = tot; }
-    __syncthreads();
-    const int n = s_n;
-    PlanHeader h;
-    h.G = G; h.rg = rg; h.n_seg = 0; h.total_ch = 0; h.P = 1; h.n_partial_rows = 0; h.n_routed_rows = 0;
-    // A plan that does not fit the workspace is published empty (no segment,
-    // no channel, no routed row): the FFN kernels then do nothing, and the
-    // error word says why, instead of indexing past the tables.
-    if (n > a.max_segs) {
-        if (tid == 0) { set_error(a.err, MOE_ERR_CAPACITY, n); *a.hdr = h; }
-        return;
-    }
-    if (tid < n_slots) a.seg_first[tid < ns ? N + tid : tid - ns] = seg_start[tid];
-    if (tid == 0) a.seg_first[N + ns] = n;
-    const int ns_segs = ns > 0 ? seg_start[ns] : 0;  // shared segments come first
-    const int total_ch = ns_segs * a.I_shared + (n - ns_segs) * a.I;
-    const int al = a.p_align > 1 ? a.p_align : 1;
-    const int P = total_ch > 0 ? ((total_ch + G - 1) / G + al - 1) / al * al : al;
-    // one thread per segment (in passes of blockDim.x), partial-row bases by scan
-    int carry = 0;
-    for (int base = 0; base < n; base += blockDim.x) {
-        const int i = base + tid;
-        Seg S;
-        int w = 0;
-        if (i < n) {
-            // expert slot of segment i: the last slot whose first segment is <= i
-            int lo = 0, hi = n_slots - 1;
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (seg_start[mid] <= i) lo = mid; else hi = mid - 1;
-            }
-            const int j = i - seg_start[lo];  // segment index within the slot
-            if (lo < ns) {
-                S.expert = N + lo; S.row0 = j * rg; S.rows = min(rg, T - j * rg); S.I = a.I_shared;
-                S.ch_start = i * a.I_shared;
-            } else {
-                const int e = lo - ns;
-                S.expert = e; S.row0 = off[e] + j * rg; S.rows = min(rg, off[e + 1] - S.row0); S.I = a.I;
-                S.ch_start = ns_segs * a.I_shared + (i - ns_segs) * a.I;
-            }
-            S.c0 = S.ch_start / P;
-            S.npieces = (S.ch_start + S.I - 1) / P - S.c0 + 1;
-            S.list_off = -1;
-            w = S.npieces * S.rows;
-        }
-        int tw;
-        const int pb = block_exclusive_scan(w, &tw);
-        if (i < n) {
-            S.pbase = carry + pb;
-            a.segs[i] = S;
-        }
-        carry += tw;
-    }
-    if (tid == 0) {
-        if (carry > a.max_partial_rows) {
-            set_error(a.err, MOE_ERR_CAPACITY, carry);
-            *a.hdr = h;
-            return;
-        }
-        h.n_seg = n; h.total_ch = total_ch; h.P = P; h.n_partial_rows = carry; h.n_routed_rows = off[N];
-        *a.hdr = h;
-    }
-}
-
-// Up to 1024 slots: one block, one thread per slot.  Slots with the same
-// expert in a warp are ranked by __match_any_sync; per-warp counts per expert,
-// scanned over warps and then over experts, give every slot its position
-// (stable in slot order, as in permute_kernel).  The same block then builds
-// the FFN plan.
 __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __restrict__ final_idx,
                                                              const int32_t* __restrict__ final_kind,
                                                              int n_slots, int N,
@@ -226,69 +107,7 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __re
                                                              int32_t* __restrict__ perm,
                                                              int32_t* __restrict__ inv_perm,
                                                              DevError* __restrict__ err, PlanArgs plan) {
-    __shared__ int cnt[32][kMaxExperts];  // per warp and expert: count, then exclusive prefix over warps
-    __shared__ int s_off[kMaxExperts + 1];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-    for (int i = tid; i < 32 * kMaxExperts; i += blockDim.x) (&cnt[0][0])[i] = 0;
-    int key = -1;  // expert of this slot, -1: no computed expert (LoRE, empty, past the end)
-    if (tid < n_slots) {
-        const int x = final_idx[tid];
-        if (x >= N) set_error(err, MOE_ERR_DEVICE_INDEX, tid);
-        if (x >= 0 && x < N && final_kind[tid] != MOE_KIND_LORE) key = x;
-    }
-    __syncthreads();
-    const uint32_t peers = __match_any_sync(0xffffffffu, key);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    if (key >= 0 && rank == 0) cnt[warp][key] = __popc(peers);
-    __syncthreads();
-    int tot = 0;
-    if (tid < N) {
-        for (int w = 0; w < nw; ++w) {
-            const int c = cnt[w][tid];
-            cnt[w][tid] = tot;
-            tot += c;
-        }
-    }
-    int all;
-    const int first = block_exclusive_scan(tid < N ? tot : 0, &all);
-    if (tid < N) s_off[tid] = first;
-    if (tid == 0) s_off[N] = all;
-    __syncthreads();
-    if (tid <= N) expert_offsets[tid] = s_off[tid];
-    if (tid < n_slots) {
-        if (key >= 0) {
-            const int pos = s_off[key] + cnt[warp][key] + rank;
-            perm[pos] = tid;
-            inv_perm[tid] = pos;
-        } else {
-            inv_perm[tid] = -1;
-        }
-    }
-    // only the plan of the path moe_expert_ffn will take
-    if (plan.tc_plan) {
-        if (tid == 0) build_tc_plan(plan, s_off);
-    } else {
-        build_plan(plan, s_off);
-    }
-}
-
-// Tensor-core plan (see TcPlan): shared-expert group first, then every
-// routed expert with rows.
-__device__ void build_tc_plan(const PlanArgs& a, const int* off) {
-    TcPlan& P = *a.tc_plan;
-    int n = 0, t1 = 0, t2 = 0;
-    const int n2 = a.d / 256;
-    auto add = [&](int shared, int expert, int row0, int rows, int n1) {
-        TcSeg& s = P.seg[n++];
-        s.shared = shared; s.expert = expert; s.row0 = row0; s.rows = rows;
-        s.m_tiles = (rows + 127) / 128; s.n1 = n1; s.tile1 = t1; s.tile2 = t2;
-        t1 += s.m_tiles * n1;
-        t2 += s.m_tiles * n2;
-    };
-    if (a.n_shared > 0) add(1, a.N, 0, a.T, a.n_shared * a.I_shared / 128);
-    for (int e = 0; e < a.N; ++e)
-        if (off[e + 1] > off[e]) add(0, e, off[e], off[e + 1] - off[e], a.I / 128);
-    P.n_seg = n; P.n_tiles1 = t1; P.n_tiles2 = t2;
+    permute_block(final_idx, final_kind, n_slots, N, expert_offsets, perm, inv_perm, err, plan);
 }
 
 __global__ void __launch_bounds__(256) plan_gemv_kernel(PlanArgs a) {

@@ -10,6 +10,7 @@
 // SPICE write-up, LoRE section: low-confidence misses use the surrogate.
 #include "common.cuh"
 #include "kernels.h"
+#include "plan.cuh"
 
 namespace moe {
 
@@ -21,13 +22,12 @@ namespace moe {
 // rounding error of a logit near 1e-7 (the decisions made on these logits are
 // compared bit-exactly with a float64 reference, away from near-ties).
 template <typename W, int TT>
-__global__ void __launch_bounds__(256) route_logits_kernel(
+__device__ __forceinline__ void logits_tile(
     const W* __restrict__ x, const W* __restrict__ x_pre, const W* __restrict__ w_router,
     const float* __restrict__ bias, const W* __restrict__ w_prefetch, const float* __restrict__ w_ord,
     int T, int d, int N, int n_out, int rows_per_block, float* __restrict__ logits_r,
-    float* __restrict__ logits_p, float* __restrict__ score) {
+    float* __restrict__ logits_p, float* __restrict__ score, unsigned char* smem_raw) {
     constexpr int V = Vec<W>::n;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
     W* xs = reinterpret_cast<W*>(smem_raw);                 // [TT][d]
     W* xps = xs + (size_t)TT * d;                             // [TT][d] (x_pre)
     const int t0 = blockIdx.x * TT;
@@ -89,6 +89,17 @@ __global__ void __launch_bounds__(256) route_logits_kernel(
             }
         }
     }
+}
+
+template <typename W, int TT>
+__global__ void __launch_bounds__(256) route_logits_kernel(
+    const W* __restrict__ x, const W* __restrict__ x_pre, const W* __restrict__ w_router,
+    const float* __restrict__ bias, const W* __restrict__ w_prefetch, const float* __restrict__ w_ord,
+    int T, int d, int N, int n_out, int rows_per_block, float* __restrict__ logits_r,
+    float* __restrict__ logits_p, float* __restrict__ score) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    logits_tile<W, TT>(x, x_pre, w_router, bias, w_prefetch, w_ord, T, d, N, n_out, rows_per_block, logits_r,
+                       logits_p, score, smem_raw);
 }
 
 // Large batches: a register-tiled version of the same logits.  Block tile =
@@ -214,16 +225,13 @@ __device__ __forceinline__ uint64_t valid_mask(int N) {
 
 // ---------------------------------------------------------------------------
 // One warp per token: softmax, top-k, delta_hat, prefetch set, delta*.
-__global__ void __launch_bounds__(256) route_select_kernel(
-    const float* __restrict__ logits_r, const float* __restrict__ logits_p,
-    const float* __restrict__ score, const float* __restrict__ theta, float logit_tau, int T,
+__device__ __forceinline__ void route_select_token(
+    int t, const float* __restrict__ logits_r, const float* __restrict__ logits_p,
+    const float* __restrict__ score, const float* __restrict__ theta, float logit_tau,
     int N, int k, int delta_max, int has_prefetch, int32_t* __restrict__ topk_idx,
     float* __restrict__ topk_gate, float* __restrict__ router_prob, int32_t* __restrict__ delta_hat,
     uint64_t* __restrict__ prefetch_mask, int32_t* __restrict__ delta_star, float* __restrict__ qp) {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (warp >= T) return;
-    const int t = warp;
     const uint64_t vm = valid_mask(N);
     const int e0 = lane, e1 = lane + 32;
     const float l0 = e0 < N ? logits_r[(size_t)t * N + e0] : -INFINITY;
@@ -302,19 +310,34 @@ __global__ void __launch_bounds__(256) route_select_kernel(
     }
 }
 
+__global__ void __launch_bounds__(256) route_select_kernel(
+    const float* __restrict__ logits_r, const float* __restrict__ logits_p,
+    const float* __restrict__ score, const float* __restrict__ theta, float logit_tau, int T,
+    int N, int k, int delta_max, int has_prefetch, int32_t* __restrict__ topk_idx,
+    float* __restrict__ topk_gate, float* __restrict__ router_prob, int32_t* __restrict__ delta_hat,
+    uint64_t* __restrict__ prefetch_mask, int32_t* __restrict__ delta_star, float* __restrict__ qp) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (warp >= T) return;
+    route_select_token(warp, logits_r, logits_p, score, theta, logit_tau, N, k, delta_max, has_prefetch,
+                       topk_idx, topk_gate, router_prob, delta_hat, prefetch_mask, delta_star, qp);
+}
+
 // ---------------------------------------------------------------------------
 // Batch resident set: the n_res experts with the largest prefetch probability
-// summed over the tokens, in a fixed summation order (one block).
-__global__ void __launch_bounds__(1024) batch_resident_kernel(const float* __restrict__ qp, int T,
-                                                              int N, int n_res,
-                                                              uint64_t* __restrict__ out) {
+// summed over the tokens, in a fixed summation order (16 token groups per
+// expert, then the groups in order; any block size).
+__device__ __forceinline__ void batch_resident_block(const float* __restrict__ qp, int T, int N, int n_res,
+                                                     uint64_t* __restrict__ out) {
     __shared__ float part[16][64];
     __shared__ float tot[64];
-    const int e = threadIdx.x & 63, g = threadIdx.x >> 6;  // 16 groups
-    float acc = 0.f;
-    if (e < N)
-        for (int t = g; t < T; t += 16) acc += qp[(size_t)t * N + e];
-    part[g][e] = acc;
+    __shared__ uint32_t bits[2];
+    for (int idx = threadIdx.x; idx < 16 * 64; idx += blockDim.x) {
+        const int e = idx & 63, g = idx >> 6;
+        float acc = 0.f;
+        if (e < N)
+            for (int t = g; t < T; t += 16) acc += qp[(size_t)t * N + e];
+        part[g][e] = acc;
+    }
     __syncthreads();
     if (threadIdx.x < 64) {
         float s = 0.f;
@@ -322,7 +345,6 @@ __global__ void __launch_bounds__(1024) batch_resident_kernel(const float* __res
         tot[threadIdx.x] = s;
     }
     __syncthreads();
-    __shared__ uint32_t bits[2];
     if (threadIdx.x < 64) {
         const int me = threadIdx.x;
         int rank = 0;
@@ -337,19 +359,22 @@ __global__ void __launch_bounds__(1024) batch_resident_kernel(const float* __res
     if (threadIdx.x == 0) *out = (uint64_t)bits[0] | ((uint64_t)bits[1] << 32);
 }
 
+__global__ void __launch_bounds__(1024) batch_resident_kernel(const float* __restrict__ qp, int T,
+                                                              int N, int n_res,
+                                                              uint64_t* __restrict__ out) {
+    batch_resident_block(qp, T, N, n_res, out);
+}
+
 // ---------------------------------------------------------------------------
 // Miss handling, one warp per token (APEX §4.3 Algorithm 1; SPICE LoRE).
-__global__ void __launch_bounds__(256) select_resident_kernel(
-    const float* __restrict__ router_prob, const int32_t* __restrict__ topk_idx,
+__device__ __forceinline__ void select_token(
+    int t, const float* __restrict__ router_prob, const int32_t* __restrict__ topk_idx,
     const uint64_t* __restrict__ prefetch_mask, const uint64_t* __restrict__ resident, int policy,
-    float gamma, const int32_t* __restrict__ delta_hat, const int32_t* __restrict__ delta_star, int T,
+    float gamma, const int32_t* __restrict__ delta_hat, const int32_t* __restrict__ delta_star,
     int N, int k, int renorm, int32_t* __restrict__ final_idx, float* __restrict__ final_gate,
     int32_t* __restrict__ final_kind, uint64_t* __restrict__ fetch_mask,
     int32_t* __restrict__ counters, DevError* __restrict__ err) {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (warp >= T) return;
-    const int t = warp;
     const uint64_t vm = valid_mask(N);
     const int e0 = lane, e1 = lane + 32;
     const float a0 = e0 < N ? router_prob[(size_t)t * N + e0] : -INFINITY;
@@ -436,6 +461,82 @@ __global__ void __launch_bounds__(256) select_resident_kernel(
         }
         if (shortfall) set_error(err, MOE_ERR_CAPACITY, t);
     }
+}
+
+__global__ void __launch_bounds__(256) select_resident_kernel(
+    const float* __restrict__ router_prob, const int32_t* __restrict__ topk_idx,
+    const uint64_t* __restrict__ prefetch_mask, const uint64_t* __restrict__ resident, int policy,
+    float gamma, const int32_t* __restrict__ delta_hat, const int32_t* __restrict__ delta_star, int T,
+    int N, int k, int renorm, int32_t* __restrict__ final_idx, float* __restrict__ final_gate,
+    int32_t* __restrict__ final_kind, uint64_t* __restrict__ fetch_mask,
+    int32_t* __restrict__ counters, DevError* __restrict__ err) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (warp >= T) return;
+    select_token(warp, router_prob, topk_idx, prefetch_mask, resident, policy, gamma, delta_hat, delta_star, N,
+                 k, renorm, final_idx, final_gate, final_kind, fetch_mask, counters, err);
+}
+
+// ---------------------------------------------------------------------------
+// Fused front end of a small batch (see launch_route_front).
+template <typename W, int TT>
+__global__ void __launch_bounds__(256) route_front_kernel(const __grid_constant__ FrontArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __shared__ int s_last;
+    const LogitsArgs& la = a.la;
+    const int n_out = la.has_prefetch ? 2 * la.N + 1 : la.N;
+    logits_tile<W, TT>((const W*)la.x, (const W*)(la.x_pre ? la.x_pre : la.x), (const W*)la.w_router, la.bias,
+                       (const W*)la.w_prefetch, la.w_ord, la.T, la.d, la.N, n_out, 8, la.logits_r, la.logits_p,
+                       la.score, smem_raw);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = atomicAdd(a.ticket, 1) == (int)(gridDim.x * gridDim.y) - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const RouteSelectArgs& ra = a.ra;
+    for (int t = warp; t < ra.T; t += nw)
+        route_select_token(t, ra.logits_r, ra.logits_p, ra.score, ra.theta, ra.logit_tau, ra.N, ra.k,
+                           ra.delta_max, ra.has_prefetch, ra.topk_idx, ra.topk_gate, ra.router_prob,
+                           ra.delta_hat, ra.prefetch_mask, ra.delta_star, ra.qp);
+    __syncthreads();
+    if (a.n_resident > 0) batch_resident_block(ra.qp, ra.T, ra.N, a.n_resident, a.batch_resident);
+    const SelectArgs& sa = a.sa;
+    if (threadIdx.x == 0) {
+        if (sa.counters)
+            for (int i = 0; i < MOE_NUM_COUNTERS; ++i) sa.counters[i] = 0;
+        if (sa.fetch_mask) *sa.fetch_mask = 0ull;
+    }
+    __syncthreads();
+    for (int t = warp; t < sa.T; t += nw)
+        select_token(t, sa.router_prob, sa.topk_idx, sa.prefetch_mask, sa.resident, sa.policy, sa.gamma,
+                     sa.delta_hat, sa.delta_star, sa.N, sa.k, sa.renorm, sa.final_idx, sa.final_gate,
+                     sa.final_kind, sa.fetch_mask, sa.counters, sa.err);
+    __syncthreads();
+    const PermuteArgs& pa = a.pa;
+    permute_block(pa.final_idx, pa.final_kind, pa.n_slots, pa.N, pa.expert_offsets, pa.perm, pa.inv_perm,
+                  pa.err, a.plan);
+    if (threadIdx.x == 0) *a.ticket = 0;
+}
+
+template <typename W>
+static cudaError_t launch_front_t(const FrontArgs& a, cudaStream_t st) {
+    constexpr int TT = 8;
+    const LogitsArgs& la = a.la;
+    const int n_out = la.has_prefetch ? 2 * la.N + 1 : la.N;
+    dim3 grid((la.T + TT - 1) / TT, (n_out + 7) / 8);
+    const size_t smem = (size_t)2 * TT * la.d * sizeof(W);
+    cudaError_t e = allow_max_smem(route_front_kernel<W, TT>);
+    if (e != cudaSuccess) return e;
+    route_front_kernel<W, TT><<<grid, 256, smem, st>>>(a);
+    return note_launch(reinterpret_cast<const void*>(route_front_kernel<W, TT>), 256, smem, cudaGetLastError());
+}
+
+cudaError_t launch_route_front(const FrontArgs& a, cudaStream_t st) {
+    if (a.pa.n_slots > kFrontMaxSlots || a.la.T >= 2048) return cudaErrorInvalidValue;
+    return a.la.bf16 ? launch_front_t<__nv_bfloat16>(a, st) : launch_front_t<float>(a, st);
 }
 
 // ---------------------------------------------------------------------------
