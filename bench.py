@@ -361,7 +361,7 @@ def main():
     if phase == "decode":
         achieved = sum(k_bytes) / (sum(k_ms) / 1e3) / 1e9
         kname, ksrc = {
-            "tc-decode": ("moe_expert_ffn (gather_rows_kernel + ffn_tcd_kernel + gemv_reduce_kernel)",
+            "tc-decode": ("moe_expert_ffn (ffn_tcd_kernel + gemv_reduce_kernel)",
                           "ffn_tcd.cu"),
             "gemv-floe": ("moe_expert_ffn (floe up/select/union/plan + sparse ffn_gemv_kernel"
                           " + gemv_reduce_kernel)", "ffn_gemv.cu"),

@@ -26,6 +26,11 @@
 // chunks add to them).  The GEMV's reduction kernel then sums the partial
 // rows of each output row in a fixed order.
 //
+// Token rows: a shared-expert segment's rows are consecutive tokens of x (one
+// box of NT rows); a routed segment's rows of a batch of up to 16 tokens are
+// loaded straight from x, one 128-byte box per token (its tokens looked up in
+// perm once), those of larger batches from a gathered copy x_perm (one box).
+//
 // Block: warp 0 issues the TMA loads (ring of kNS stages), warp 1 allocates
 // tensor memory and issues the MMAs, warps 2-5 run the epilogues (thread =
 // tensor-memory lane = channel in phase A, column of d in phase B).  Every
@@ -60,8 +65,11 @@ struct TcdCfg {
 };
 
 struct TcdParams {
-    CUtensorMap map_x;   // x [T, d], box {64, NT}      (shared-expert segments: rows = tokens)
-    CUtensorMap map_xp;  // x_perm [T*k, d], box {64, NT} (routed segments: rows = permuted positions)
+    CUtensorMap map_x;   // x [T, d], box {64, NT}: shared-expert segments (rows = tokens t0 ..)
+    CUtensorMap map_x1;  // x [T, d], box {64, 1}:  routed segments, one token row per box (NT = 16)
+    CUtensorMap map_xp;  // x_perm [T*k, d], box {64, NT}: routed segments, gathered rows (NT = 32)
+    const int32_t* perm;  // permuted position -> slot t * k + s
+    int topk;
     const ExpertEntry* table;
     const PlanHeader* hdr;
     const Seg* segs;
@@ -160,10 +168,16 @@ __global__ void __launch_bounds__(kTcdThreads, 1) ffn_tcd_kernel(const __grid_co
                 mbar_arrive_expect_tx(&full[st], bytes);
                 return st;
             };
+            int tok[NT];  // routed segment: the token of each row
             while (ok && walk.next(S, llo, lhi)) {
                 const ExpertEntry* E = p.table + S.expert;
                 const bool shared = S.expert >= p.N;
-                const CUtensorMap* xm = shared ? &p.map_x : &p.map_xp;
+                // routed rows of up to 16 tokens: one box per row straight from x; of 32:
+                // one box from the gathered copy
+                const bool per_row = !shared && NT == 16;
+                if (per_row)
+                    for (int i = 0; i < S.rows && i < NT; ++i) tok[i] = p.perm[S.row0 + i] / p.topk;
+                const uint32_t xbytes = per_row ? (uint32_t)min(S.rows, NT) * 128u : C::kX;
                 for (int c0 = llo; ok && c0 < lhi; c0 += HT * 128) {
                     const int clen = min(HT * 128, lhi - c0);
                     const int ntl = (clen + 127) / 128;
@@ -171,7 +185,7 @@ __global__ void __launch_bounds__(kTcdThreads, 1) ffn_tcd_kernel(const __grid_co
                     for (int t = 0; ok && t < ntl; ++t) {
                         const int rows = min(128, clen - t * 128);
                         for (int kc = 0; kc < nkA; ++kc, ++it) {
-                            const int st = acquire(2u * rows * 128u + C::kX);
+                            const int st = acquire(2u * rows * 128u + xbytes);
                             if (st < 0) { ok = false; break; }
                             const uint32_t dst = smem_base + st * C::kStage;
                             if (rows == 128) {  // whole tile: one 128-row box per matrix
@@ -185,7 +199,13 @@ __global__ void __launch_bounds__(kTcdThreads, 1) ffn_tcd_kernel(const __grid_co
                                                      c0 + t * 128 + j * 16, &full[st], pol_w);
                                 }
                             }
-                            tma_load_2d(dst + 2 * kTcdW, xm, kc * 64, S.row0, &full[st]);
+                            if (per_row) {
+                                for (int i = 0; i < S.rows && i < NT; ++i)
+                                    tma_load_2d(dst + 2 * kTcdW + i * 128, &p.map_x1, kc * 64, tok[i], &full[st]);
+                            } else {
+                                tma_load_2d(dst + 2 * kTcdW, shared ? &p.map_x : &p.map_xp, kc * 64, S.row0,
+                                            &full[st]);
+                            }
                         }
                     }
                     // phase B: Wd rows of every tile, 128 columns of d per stage
@@ -384,9 +404,16 @@ static cudaError_t launch_tcd_nt(const TcdLaunch& a, cudaStream_t st) {
     TcdParams p;
     std::memset(&p, 0, sizeof(p));
     if (encode_bf16_2d(&p.map_x, a.x, a.d, a.T, (uint64_t)a.d * 2, 64, NT) != MOE_OK ||
-        encode_bf16_2d(&p.map_xp, a.x_perm, a.d, a.rows_cap > 0 ? a.rows_cap : 1, (uint64_t)a.d * 2, 64, NT) !=
-            MOE_OK)
+        encode_bf16_2d(&p.map_x1, a.x, a.d, a.T, (uint64_t)a.d * 2, 64, 1) != MOE_OK)
         return cudaErrorInvalidValue;
+    if (NT == 32) {
+        cudaError_t e = launch_gather_rows(a.x, a.perm, a.expert_offsets, a.N, a.k, a.d, a.rows_cap, a.x_perm, st);
+        if (e != cudaSuccess) return e;
+        if (encode_bf16_2d(&p.map_xp, a.x_perm, a.d, a.rows_cap > 0 ? a.rows_cap : 1, (uint64_t)a.d * 2, 64, NT) !=
+            MOE_OK)
+            return cudaErrorInvalidValue;
+    }
+    p.perm = a.perm; p.topk = a.k;
     p.table = a.table; p.hdr = a.hdr; p.segs = a.segs; p.partial = a.partial;
     p.d = a.d; p.N = a.N; p.err = a.err;
     cudaError_t e = allow_max_smem(ffn_tcd_kernel<NT>);
@@ -398,8 +425,6 @@ static cudaError_t launch_tcd_nt(const TcdLaunch& a, cudaStream_t st) {
 
 cudaError_t launch_tcd_ffn(const TcdLaunch& a, cudaStream_t st) {
     if (a.d % 128 != 0) return cudaErrorInvalidValue;
-    cudaError_t e = launch_gather_rows(a.x, a.perm, a.expert_offsets, a.N, a.k, a.d, a.rows_cap, a.x_perm, st);
-    if (e != cudaSuccess) return e;
     switch (a.nt) {
         case 16: return launch_tcd_nt<16>(a, st);
         case 32: return launch_tcd_nt<32>(a, st);

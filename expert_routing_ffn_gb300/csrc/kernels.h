@@ -57,12 +57,14 @@ struct PlanArgs {
 // permutation + FFN plan in one launch (the last block builds the plan)
 cudaError_t launch_permute(const PermuteArgs& a, const PlanArgs& plan, int* ticket, cudaStream_t st);
 
-// The routing front end of a small batch (T * k <= kFrontMaxSlots) in one
+// The routing front end of a small batch (T <= kFrontMaxTokens, T * k <=
+// kFrontMaxSlots) in one
 // launch: the blocks compute the router / prefetch logits, the last block to
 // finish runs selection, the batch resident set (n_resident > 0), miss
 // handling (zeroing counters and fetch mask first) and the permutation with
 // the FFN plan, with the same device code as the stage-wise kernels.
 constexpr int kFrontMaxSlots = 256;
+constexpr int kFrontMaxTokens = 64;
 struct FrontArgs {
     LogitsArgs la;
     RouteSelectArgs ra;
@@ -129,8 +131,8 @@ struct TcdLaunch {
     const PlanHeader* hdr; const Seg* segs; void* x_perm; float* partial;
     int T, d, N, k, rows_cap, nt, grid; DevError* err;
 };
-// decode-size expert FFN on the tensor cores: gather + one launch writing the
-// GEMV plan's partial rows (summed by launch_gemv_reduce)
+// decode-size expert FFN on the tensor cores: one launch writing the GEMV
+// plan's partial rows (summed by launch_gemv_reduce)
 cudaError_t launch_tcd_ffn(const TcdLaunch& a, cudaStream_t st);
 
 struct LoreArgs {

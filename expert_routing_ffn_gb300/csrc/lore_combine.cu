@@ -148,8 +148,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 // (GEMV and decode tensor-core paths).  Block = token t x 128 columns of d;
 // lane = 4 columns.  Warp w sums the partial rows of the slots s = w, w + 8,
 // ... (one y_perm row each) and warp 7 also those of the shared experts
-// (y_shared); the LoRE term (B rows times z) is formed by warp 0 after them;
-// warp 0 then combines in slot order and writes out.  Every sum runs in the
+// (y_shared); warp 6 forms the LoRE term (B rows times z); warp 0 then
+// combines in slot order and writes out.  Every sum runs in the
 // order of the separate kernels (gemv_reduce_kernel, lore_b_kernel,
 // combine_kernel), so the result is bitwise the one of the stage-wise calls.
 template <typename W>
@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(256) layer_epilogue_kernel(const EpilogueArgs 
     __shared__ float s_z[kMaxTopK * 64];
     __shared__ float4 s_y[kMaxTopK][32];
     __shared__ float4 s_sh[32];
+    __shared__ float4 s_yl[32];
     if (threadIdx.x == 0) {
         float lg = 0.f;
         int nl = 0;
@@ -186,6 +187,7 @@ __global__ void __launch_bounds__(256) layer_epilogue_kernel(const EpilogueArgs 
     const int nl = s_nl;
     for (int i = threadIdx.x; i < nl * r; i += blockDim.x)
         s_z[i] = a.z[((size_t)t * k + s_lore[i / r]) * r + (i % r)];
+    __syncthreads();  // s_z complete before the LoRE warp reads it
     const bool col_ok = q < d / 4;
     const PlanHeader hdr = *a.hdr;
     const int rg = hdr.rg;
@@ -232,6 +234,39 @@ __global__ void __launch_bounds__(256) layer_epilogue_kernel(const EpilogueArgs 
             s_sh[lane] = sh;
         }
     }
+    // LoRE term y_lore[t, j] = sum over LoRE slots, then over q, of B_e[j, q] z[q]
+    // (warp 6; the order of lore_b_kernel)
+    if (warp == 6 && a.lore_b) {
+        float yl[4] = {0.f, 0.f, 0.f, 0.f};
+        if (col_ok) {
+            const W* B = static_cast<const W*>(a.lore_b);
+            constexpr int V = Vec<W>::n;
+            const bool vec = (r * (int)sizeof(W)) % 16 == 0;
+            for (int i = 0; i < nl; ++i) {
+                const int e = s_e[s_lore[i]];
+                const float* zz = s_z + i * r;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const W* brow = B + ((size_t)e * d + q * 4 + c) * r;
+                    float accl = yl[c];
+                    if (vec) {
+                        for (int qq = 0; qq < r; qq += V) {
+                            float bv[V];
+                            unpack16(*reinterpret_cast<const uint4*>(brow + qq), bv, (W*)nullptr);
+#pragma unroll
+                            for (int u = 0; u < V; ++u) accl = fmaf(bv[u], zz[qq + u], accl);
+                        }
+                    } else {
+                        for (int qq = 0; qq < r; ++qq) accl = fmaf(to_f32(brow[qq]), zz[qq], accl);
+                    }
+                    yl[c] = accl;
+                }
+            }
+            const float4 v = make_float4(yl[0], yl[1], yl[2], yl[3]);
+            reinterpret_cast<float4*>(a.y_lore + (size_t)t * d)[q] = v;
+            s_yl[lane] = v;
+        }
+    }
     __syncthreads();
     if (warp != 0 || !col_ok) return;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -248,21 +283,8 @@ __global__ void __launch_bounds__(256) layer_epilogue_kernel(const EpilogueArgs 
         acc.z = fmaf(g, y.z, acc.z); acc.w = fmaf(g, y.w, acc.w);
     }
     if (a.lore_b) {
-        float yl[4] = {0.f, 0.f, 0.f, 0.f};
-        const W* B = static_cast<const W*>(a.lore_b);
-        for (int i = 0; i < nl; ++i) {
-            const int e = s_e[s_lore[i]];
-            const float* zz = s_z + i * r;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const W* brow = B + ((size_t)e * d + q * 4 + c) * r;
-                float accl = yl[c];
-                for (int qq = 0; qq < r; ++qq) accl = fmaf(to_f32(brow[qq]), zz[qq], accl);
-                yl[c] = accl;
-            }
-        }
-        reinterpret_cast<float4*>(a.y_lore + (size_t)t * d)[q] = make_float4(yl[0], yl[1], yl[2], yl[3]);
-        acc.x += yl[0]; acc.y += yl[1]; acc.z += yl[2]; acc.w += yl[3];
+        const float4 yl = s_yl[lane];
+        acc.x += yl.x; acc.y += yl.y; acc.z += yl.z; acc.w += yl.w;
     }
     reinterpret_cast<float4*>(a.out + (size_t)t * d)[q] = acc;
 }

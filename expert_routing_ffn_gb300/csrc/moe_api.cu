@@ -131,6 +131,31 @@ bool bf16(const moe_dims* D) { return D->wtype == MOE_DTYPE_BF16; }
 
 int tcd_grid() { return sm_count() < kTcdMaxCtas ? sm_count() : kTcdMaxCtas; }
 
+// A second stream per device on which moe_layer_forward runs the LoRE z
+// kernel beside the expert FFN (fork and join by events; under stream capture
+// this becomes a parallel branch of the graph).  Created on first use.
+struct SideStream {
+    std::mutex mu;
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+SideStream* side_stream() {
+    static std::mutex mu;
+    static SideStream per_dev[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    SideStream& sd = per_dev[dev];
+    if (!sd.s) {
+        if (cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+        if (cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess)
+            return nullptr;
+    }
+    return &sd;
+}
+
 // Argument checks and launch arguments of the routing stages (T > 0), shared
 // by the stage-wise calls and the fused front end of moe_layer_forward.
 moe_status prep_route(const moe_dims* dims, const void* x, const void* w_router, const float* router_bias,
@@ -421,7 +446,7 @@ moe_status expert_ffn_impl(const moe_dims* dims, const void* x, const void* tabl
         t.T = dims->T; t.d = dims->d; t.N = dims->N; t.k = dims->k; t.rows_cap = dims->T * dims->k;
         t.nt = tcd_rows(dims->T); t.grid = tcd_grid(); t.err = ws_at<DevError>(ws, L.err);
         MOE_CUDA(launch_tcd_ffn(t, S(stream)));
-        count(2);
+        count(t.nt == 32 ? 2 : 1);  // + the row gather for 32-row segments
         if (!reduce) return MOE_OK;
         GemvReduceArgs r;
         r.hdr = t.hdr; r.segs = t.segs; r.seg_first = ws_at<int32_t>(ws, L.seg_first);
@@ -544,7 +569,7 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_layer_args* A,
     if (!A || !O) return MOE_ERR_INVALID_ARG;
     const uint64_t* resident = A->n_resident > 0 ? O->batch_resident : A->resident;
     const uint64_t* pref_mask = A->use_prefetch_mask ? O->prefetch_mask : nullptr;
-    if (dims->T > 0 && dims->T * dims->k <= kFrontMaxSlots) {
+    if (dims->T > 0 && dims->T <= kFrontMaxTokens && dims->T * dims->k <= kFrontMaxSlots) {
         // small batch: routing, selection, resident set, misses and the
         // permutation in one launch (same device code as the stage-wise calls)
         MOE_TRY(check_ws(dims, ws, ws_bytes));
@@ -577,17 +602,28 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_layer_args* A,
     if (!use_tc(*dims) && dims->T > 0) {
         // partial-row paths: FFN without its reduction, LoRE z, then one
         // launch for reduction + LoRE B + combine
-        MOE_TRY(expert_ffn_impl(dims, A->x, A->table, O->expert_offsets, O->perm, A->keep_frac, O->y_perm,
-                                O->y_shared, ws, ws_bytes, stream, false));
         const WsLayout L = ws_layout(*dims);
         if (lore) {
+            // LoRE z = g A_e x on the side stream, beside the expert FFN
             LoreArgs la;
             la.x = A->x; la.final_idx = O->final_idx; la.final_kind = O->final_kind;
             la.final_gate = O->final_gate; la.A = A->lore_a; la.B = A->lore_b; la.T = dims->T; la.d = dims->d;
             la.k = dims->k; la.r = dims->r; la.N = dims->N; la.bf16 = bf16(dims);
             la.z = ws_at<float>(ws, L.lore_z); la.y_lore = O->y_lore; la.err = ws_at<DevError>(ws, L.err);
-            MOE_CUDA(launch_lore_z(la, S(stream)));
+            SideStream* sd = side_stream();
+            if (!sd) return MOE_ERR_CUDA;
+            std::lock_guard<std::mutex> lock(sd->mu);
+            MOE_CUDA(cudaEventRecord(sd->fork, S(stream)));
+            MOE_CUDA(cudaStreamWaitEvent(sd->s, sd->fork, 0));
+            MOE_CUDA(launch_lore_z(la, sd->s));
             count();
+            MOE_CUDA(cudaEventRecord(sd->join, sd->s));
+            MOE_TRY(expert_ffn_impl(dims, A->x, A->table, O->expert_offsets, O->perm, A->keep_frac, O->y_perm,
+                                    O->y_shared, ws, ws_bytes, stream, false));
+            MOE_CUDA(cudaStreamWaitEvent(S(stream), sd->join, 0));
+        } else {
+            MOE_TRY(expert_ffn_impl(dims, A->x, A->table, O->expert_offsets, O->perm, A->keep_frac, O->y_perm,
+                                    O->y_shared, ws, ws_bytes, stream, false));
         }
         EpilogueArgs ea;
         ea.hdr = ws_at<PlanHeader>(ws, L.plan_hdr); ea.segs = ws_at<Seg>(ws, L.segs);

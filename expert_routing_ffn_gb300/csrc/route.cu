@@ -34,16 +34,30 @@ __device__ __forceinline__ void logits_tile(
     const int nt = min(TT, T - t0);
     const int nchunk = d / V;
     const bool sep = (x_pre != x);
-    // stage the token tile (16-byte copies)
-    for (int i = threadIdx.x; i < TT * nchunk; i += blockDim.x) {
-        int t = i / nchunk, q = i % nchunk;
-        uint4 v = make_uint4(0, 0, 0, 0), vp = make_uint4(0, 0, 0, 0);
-        if (t < nt) {
-            v = reinterpret_cast<const uint4*>(x + (size_t)(t0 + t) * d)[q];
-            if (sep) vp = reinterpret_cast<const uint4*>(x_pre + (size_t)(t0 + t) * d)[q];
+    // stage the token tile (16-byte copies, eight loads in flight per thread)
+    constexpr int U = 8;
+    for (int i0 = threadIdx.x; i0 < TT * nchunk; i0 += blockDim.x * U) {
+        uint4 v[U], vp[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * blockDim.x;
+            const int t = i / nchunk, q = i % nchunk;
+            v[u] = make_uint4(0, 0, 0, 0);
+            vp[u] = make_uint4(0, 0, 0, 0);
+            if (i < TT * nchunk && t < nt) {
+                v[u] = reinterpret_cast<const uint4*>(x + (size_t)(t0 + t) * d)[q];
+                if (sep) vp[u] = reinterpret_cast<const uint4*>(x_pre + (size_t)(t0 + t) * d)[q];
+            }
         }
-        reinterpret_cast<uint4*>(xs + (size_t)t * d)[q] = v;
-        if (sep) reinterpret_cast<uint4*>(xps + (size_t)t * d)[q] = vp;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * blockDim.x;
+            if (i < TT * nchunk) {
+                const int t = i / nchunk, q = i % nchunk;
+                reinterpret_cast<uint4*>(xs + (size_t)t * d)[q] = v[u];
+                if (sep) reinterpret_cast<uint4*>(xps + (size_t)t * d)[q] = vp[u];
+            }
+        }
     }
     __syncthreads();
     const W* xsp = sep ? xps : xs;
@@ -60,22 +74,38 @@ __device__ __forceinline__ void logits_tile(
         float acc[TT];
 #pragma unroll
         for (int t = 0; t < TT; ++t) acc[t] = 0.f;
-        for (int q = lane; q < nchunk; q += 32) {
-            float wv[V];
+        // the lane's weight chunks q = lane, lane + 32, ... in groups of QU,
+        // all loads of a group in flight before the products (same order of
+        // accumulation as one chunk at a time)
+        constexpr int QU = 8;
+        for (int q0 = lane; q0 < nchunk; q0 += 32 * QU) {
+            uint4 wraw[QU];
             if (!is_ord) {
-                uint4 raw = reinterpret_cast<const uint4*>(wrow)[q];
-                unpack16(raw, wv, (W*)nullptr);
-            } else {
 #pragma unroll
-                for (int j = 0; j < V; ++j) wv[j] = w_ord[q * V + j];
+                for (int u = 0; u < QU; ++u) {
+                    const int q = q0 + 32 * u;
+                    wraw[u] = q < nchunk ? reinterpret_cast<const uint4*>(wrow)[q] : make_uint4(0, 0, 0, 0);
+                }
             }
 #pragma unroll
-            for (int t = 0; t < TT; ++t) {
-                uint4 raw = reinterpret_cast<const uint4*>(tile + (size_t)t * d)[q];
-                float xv[V];
-                unpack16(raw, xv, (W*)nullptr);
+            for (int u = 0; u < QU; ++u) {
+                const int q = q0 + 32 * u;
+                if (q >= nchunk) break;
+                float wv[V];
+                if (!is_ord) {
+                    unpack16(wraw[u], wv, (W*)nullptr);
+                } else {
 #pragma unroll
-                for (int j = 0; j < V; ++j) acc[t] = fmaf(xv[j], wv[j], acc[t]);
+                    for (int j = 0; j < V; ++j) wv[j] = w_ord[q * V + j];
+                }
+#pragma unroll
+                for (int t = 0; t < TT; ++t) {
+                    uint4 raw = reinterpret_cast<const uint4*>(tile + (size_t)t * d)[q];
+                    float xv[V];
+                    unpack16(raw, xv, (W*)nullptr);
+#pragma unroll
+                    for (int j = 0; j < V; ++j) acc[t] = fmaf(xv[j], wv[j], acc[t]);
+                }
             }
         }
 #pragma unroll
@@ -477,7 +507,27 @@ __global__ void __launch_bounds__(256) select_resident_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// Fused front end of a small batch (see launch_route_front).
+// Fused front end of a small batch (see launch_route_front).  After the
+// logits, the last block keeps every per-token intermediate in shared memory
+// (the token-tile staging area, free by then): it loads the logits once,
+// runs selection, resident set and miss handling on shared copies, writes the
+// outputs out with coalesced stores and permutes from the shared copies.
+struct FrontSmem {  // byte offsets into the dynamic shared memory
+    int lr, lp, sc, prob, qp, tki, tkg, dh, pm, ds, fi, fg, fk, bres, total;
+};
+
+__host__ __device__ inline FrontSmem front_smem(int T, int N, int k) {
+    FrontSmem f;
+    int o = 0;
+    auto take = [&](int bytes) { const int at = o; o = (o + bytes + 15) & ~15; return at; };
+    f.lr = take(T * N * 4); f.lp = take(T * N * 4); f.sc = take(T * 4); f.prob = take(T * N * 4);
+    f.qp = take(T * N * 4); f.tki = take(T * k * 4); f.tkg = take(T * k * 4); f.dh = take(T * 4);
+    f.pm = take(T * 8); f.ds = take(T * 4); f.fi = take(T * k * 4); f.fg = take(T * k * 4);
+    f.fk = take(T * k * 4); f.bres = take(8);
+    f.total = o;
+    return f;
+}
+
 template <typename W, int TT>
 __global__ void __launch_bounds__(256) route_front_kernel(const __grid_constant__ FrontArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -495,30 +545,67 @@ __global__ void __launch_bounds__(256) route_front_kernel(const __grid_constant_
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, nw = blockDim.x >> 5;
     const RouteSelectArgs& ra = a.ra;
-    for (int t = warp; t < ra.T; t += nw)
-        route_select_token(t, ra.logits_r, ra.logits_p, ra.score, ra.theta, ra.logit_tau, ra.N, ra.k,
-                           ra.delta_max, ra.has_prefetch, ra.topk_idx, ra.topk_gate, ra.router_prob,
-                           ra.delta_hat, ra.prefetch_mask, ra.delta_star, ra.qp);
-    __syncthreads();
-    if (a.n_resident > 0) batch_resident_block(ra.qp, ra.T, ra.N, a.n_resident, a.batch_resident);
     const SelectArgs& sa = a.sa;
-    if (threadIdx.x == 0) {
+    const int T = ra.T, N = ra.N, k = ra.k;
+    const FrontSmem F = front_smem(T, N, k);
+    float* lr = reinterpret_cast<float*>(smem_raw + F.lr);
+    float* lp = reinterpret_cast<float*>(smem_raw + F.lp);
+    float* sc = reinterpret_cast<float*>(smem_raw + F.sc);
+    float* prob = reinterpret_cast<float*>(smem_raw + F.prob);
+    float* qp = reinterpret_cast<float*>(smem_raw + F.qp);
+    int32_t* tki = reinterpret_cast<int32_t*>(smem_raw + F.tki);
+    float* tkg = reinterpret_cast<float*>(smem_raw + F.tkg);
+    int32_t* dh = reinterpret_cast<int32_t*>(smem_raw + F.dh);
+    uint64_t* pm = reinterpret_cast<uint64_t*>(smem_raw + F.pm);
+    int32_t* ds = reinterpret_cast<int32_t*>(smem_raw + F.ds);
+    int32_t* fi = reinterpret_cast<int32_t*>(smem_raw + F.fi);
+    float* fg = reinterpret_cast<float*>(smem_raw + F.fg);
+    int32_t* fk = reinterpret_cast<int32_t*>(smem_raw + F.fk);
+    uint64_t* bres = reinterpret_cast<uint64_t*>(smem_raw + F.bres);
+    // the other blocks' logits, once (past L1)
+    for (int i = tid; i < T * N; i += blockDim.x) {
+        lr[i] = __ldcg(ra.logits_r + i);
+        if (ra.has_prefetch) lp[i] = __ldcg(ra.logits_p + i);
+    }
+    if (ra.has_prefetch)
+        for (int i = tid; i < T; i += blockDim.x) sc[i] = __ldcg(ra.score + i);
+    __syncthreads();
+    for (int t = warp; t < T; t += nw)
+        route_select_token(t, lr, lp, sc, ra.theta, ra.logit_tau, N, k, ra.delta_max, ra.has_prefetch, tki, tkg,
+                           prob, dh, pm, ra.delta_star ? ds : nullptr, ra.qp ? qp : nullptr);
+    __syncthreads();
+    for (int i = tid; i < T * N; i += blockDim.x) ra.router_prob[i] = prob[i];
+    for (int i = tid; i < T * k; i += blockDim.x) { ra.topk_idx[i] = tki[i]; ra.topk_gate[i] = tkg[i]; }
+    for (int i = tid; i < T; i += blockDim.x) {
+        ra.delta_hat[i] = dh[i];
+        ra.prefetch_mask[i] = pm[i];
+        if (ra.delta_star) ra.delta_star[i] = ds[i];
+    }
+    if (a.n_resident > 0) {
+        batch_resident_block(qp, T, N, a.n_resident, bres);
+        if (tid == 0) *a.batch_resident = *bres;
+    }
+    if (tid == 0) {
         if (sa.counters)
             for (int i = 0; i < MOE_NUM_COUNTERS; ++i) sa.counters[i] = 0;
         if (sa.fetch_mask) *sa.fetch_mask = 0ull;
     }
     __syncthreads();
-    for (int t = warp; t < sa.T; t += nw)
-        select_token(t, sa.router_prob, sa.topk_idx, sa.prefetch_mask, sa.resident, sa.policy, sa.gamma,
-                     sa.delta_hat, sa.delta_star, sa.N, sa.k, sa.renorm, sa.final_idx, sa.final_gate,
-                     sa.final_kind, sa.fetch_mask, sa.counters, sa.err);
+    const uint64_t* resident = a.n_resident > 0 ? bres : sa.resident;
+    for (int t = warp; t < T; t += nw)
+        select_token(t, prob, tki, sa.prefetch_mask ? pm : nullptr, resident, sa.policy, sa.gamma, dh,
+                     sa.delta_star ? ds : nullptr, N, k, sa.renorm, fi, fg, fk, sa.fetch_mask, sa.counters, sa.err);
     __syncthreads();
+    for (int i = tid; i < T * k; i += blockDim.x) {
+        sa.final_idx[i] = fi[i];
+        sa.final_gate[i] = fg[i];
+        sa.final_kind[i] = fk[i];
+    }
     const PermuteArgs& pa = a.pa;
-    permute_block(pa.final_idx, pa.final_kind, pa.n_slots, pa.N, pa.expert_offsets, pa.perm, pa.inv_perm,
-                  pa.err, a.plan);
-    if (threadIdx.x == 0) *a.ticket = 0;
+    permute_block(fi, fk, pa.n_slots, pa.N, pa.expert_offsets, pa.perm, pa.inv_perm, pa.err, a.plan);
+    if (tid == 0) *a.ticket = 0;
 }
 
 template <typename W>
@@ -527,7 +614,9 @@ static cudaError_t launch_front_t(const FrontArgs& a, cudaStream_t st) {
     const LogitsArgs& la = a.la;
     const int n_out = la.has_prefetch ? 2 * la.N + 1 : la.N;
     dim3 grid((la.T + TT - 1) / TT, (n_out + 7) / 8);
-    const size_t smem = (size_t)2 * TT * la.d * sizeof(W);
+    const size_t stage = (size_t)2 * TT * la.d * sizeof(W);
+    const size_t tail = (size_t)front_smem(la.T, la.N, a.ra.k).total;
+    const size_t smem = stage > tail ? stage : tail;
     cudaError_t e = allow_max_smem(route_front_kernel<W, TT>);
     if (e != cudaSuccess) return e;
     route_front_kernel<W, TT><<<grid, 256, smem, st>>>(a);
@@ -535,7 +624,7 @@ static cudaError_t launch_front_t(const FrontArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_route_front(const FrontArgs& a, cudaStream_t st) {
-    if (a.pa.n_slots > kFrontMaxSlots || a.la.T >= 2048) return cudaErrorInvalidValue;
+    if (a.pa.n_slots > kFrontMaxSlots || a.la.T > kFrontMaxTokens) return cudaErrorInvalidValue;
     return a.la.bf16 ? launch_front_t<__nv_bfloat16>(a, st) : launch_front_t<float>(a, st);
 }
 

@@ -235,7 +235,8 @@ moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table
 
 /* Which kernels moe_expert_ffn runs for these dimensions and keep_frac: a
  * static string, "tc-prefill" (gather + two tensor-core GEMM launches),
- * "tc-decode" (gather + tensor-core GEMM + partial-row reduction), "gemv"
+ * "tc-decode" (tensor-core GEMM + partial-row reduction, and a row gather
+ * first for batches of 17..64 tokens), "gemv"
  * (CUDA-core GEMV + reduction), "gemv-floe" (FloE preparation + sparse GEMV
  * + reduction) or "unsupported".  No device work. */
 const char* moe_expert_ffn_path(const moe_dims* dims, float keep_frac);
