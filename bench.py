@@ -154,15 +154,19 @@ class ClockSampler:
 
 
 def dist_setup(n_gpus):
+    """Rank bookkeeping from the torchrun environment.  One process per GPU
+    (NCCL); without CUDA (the multi-process tests on CPU) the gloo backend."""
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    cuda = torch.cuda.is_available()
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
+        if cuda:
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if cuda else "gloo")
+    elif cuda:
         torch.cuda.set_device(0)
     return world, rank, local
 
@@ -178,9 +182,20 @@ def max_over_ranks(world, v: float) -> float:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_batch(rank: int, i: int) -> int:
+    """Token batch id of layer copy i on a rank: every replica its own tokens."""
+    return 1000 * rank + i
+
+
+def whole_job_tokens_per_s(world: int, T: int, steps: int, ms_max: float) -> float:
+    """Tokens all ranks processed / the slowest rank's time (weak scaling)."""
+    return world * T * steps / (ms_max / 1e3)
 
 
 def cpu_baseline(cfg, W, T, seconds, batch_offset=0):
@@ -273,7 +288,7 @@ def main():
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.set_stream(stream)
     bufs = [LayerBuffers(L, T) for L in layers]
-    xs = [torch.from_numpy(make_tokens(cfg, T=T, batch=1000 * rank + i)).to(dev).to(base.dt).contiguous()
+    xs = [torch.from_numpy(make_tokens(cfg, T=T, batch=replica_batch(rank, i))).to(dev).to(base.dt).contiguous()
           for i in range(n_copies)]
 
     def step(i):
@@ -312,7 +327,7 @@ def main():
     barrier(world)
     ms_total = max_over_ranks(world, ev0.elapsed_time(ev1))
     ms_per_step = ms_total / args.steps
-    value = world * T * args.steps / (ms_total / 1e3)
+    value = whole_job_tokens_per_s(world, T, args.steps, ms_total)
     clocks = clk.summary()
 
     # ---- dominant kernel: the expert FFN stage, timed alone on the same stream
