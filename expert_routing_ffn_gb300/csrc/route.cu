@@ -262,10 +262,11 @@ __device__ __forceinline__ void route_select_token(
     float* __restrict__ topk_gate, float* __restrict__ router_prob, int32_t* __restrict__ delta_hat,
     uint64_t* __restrict__ prefetch_mask, int32_t* __restrict__ delta_star, float* __restrict__ qp) {
     const int lane = threadIdx.x & 31;
-    const uint64_t vm = valid_mask(N);
     const int e0 = lane, e1 = lane + 32;
     const float l0 = e0 < N ? logits_r[(size_t)t * N + e0] : -INFINITY;
     const float l1 = e1 < N ? logits_r[(size_t)t * N + e1] : -INFINITY;
+    const float q0 = has_prefetch && e0 < N ? logits_p[(size_t)t * N + e0] : -INFINITY;
+    const float q1 = has_prefetch && e1 < N ? logits_p[(size_t)t * N + e1] : -INFINITY;
     // softmax
     const float m = warp_max(fmaxf(l0, l1));
     const float p0 = e0 < N ? expf(l0 - m) : 0.f;
@@ -274,20 +275,26 @@ __device__ __forceinline__ void route_select_token(
     const float a0 = p0 / s, a1 = p1 / s;
     if (e0 < N) router_prob[(size_t)t * N + e0] = a0;
     if (e1 < N) router_prob[(size_t)t * N + e1] = a1;
-    // top-k of the logits, descending, lowest index on ties
-    uint64_t remaining = vm, routed = 0;
-    for (int j = 0; j < k; ++j) {
-        float v; int i;
-        lane_best(l0, l1, remaining, lane, v, i);
-        warp_argmax(v, i);
-        routed |= 1ull << i;
-        remaining &= ~(1ull << i);
-        if (lane == 0) {
-            topk_idx[(size_t)t * k + j] = i;
-        }
-        const float ai = __shfl_sync(0xffffffffu, i < 32 ? a0 : a1, i & 31);
-        if (lane == 0) topk_gate[(size_t)t * k + j] = ai;
+    // Ranks in descending order, lowest index first on ties, of the router
+    // logits (g) and the prefetch logits (r): the number of experts ahead of
+    // e0 / e1.  One pass of independent comparisons, eight shuffles in flight
+    // (experts past N hold -inf and are never ahead).
+    int g0 = 0, g1 = 0, r0 = 0, r1 = 0;
+#pragma unroll 8
+    for (int j = 0; j < 64; ++j) {
+        const float lj = __shfl_sync(0xffffffffu, j < 32 ? l0 : l1, j & 31);
+        const float qj = __shfl_sync(0xffffffffu, j < 32 ? q0 : q1, j & 31);
+        g0 += (lj > l0 || (lj == l0 && j < e0)) ? 1 : 0;
+        g1 += (lj > l1 || (lj == l1 && j < e1)) ? 1 : 0;
+        r0 += (qj > q0 || (qj == q0 && j < e0)) ? 1 : 0;
+        r1 += (qj > q1 || (qj == q1 && j < e1)) ? 1 : 0;
     }
+    // top-k of the logits: the experts of rank < k, each at its rank
+    const bool tk0 = e0 < N && g0 < k, tk1 = e1 < N && g1 < k;
+    if (tk0) { topk_idx[(size_t)t * k + g0] = e0; topk_gate[(size_t)t * k + g0] = a0; }
+    if (tk1) { topk_idx[(size_t)t * k + g1] = e1; topk_gate[(size_t)t * k + g1] = a1; }
+    const uint64_t routed = (uint64_t)__ballot_sync(0xffffffffu, tk0) |
+                            ((uint64_t)__ballot_sync(0xffffffffu, tk1) << 32);
     if (!has_prefetch) {
         if (lane == 0) {
             delta_hat[t] = 0;
@@ -306,15 +313,6 @@ __device__ __forceinline__ void route_select_token(
     if (b0) dh = __ffs(b0) - 1;
     else if (b1) dh = 32 + __ffs(b1) - 1;
     dh = min(dh, delta_max);
-    // rank of each expert in the prefetch logits
-    const float q0 = e0 < N ? logits_p[(size_t)t * N + e0] : -INFINITY;
-    const float q1 = e1 < N ? logits_p[(size_t)t * N + e1] : -INFINITY;
-    int r0 = 0, r1 = 0;
-    for (int j = 0; j < N; ++j) {
-        const float qj = __shfl_sync(0xffffffffu, j < 32 ? q0 : q1, j & 31);
-        r0 += (qj > q0 || (qj == q0 && j < e0)) ? 1 : 0;
-        r1 += (qj > q1 || (qj == q1 && j < e1)) ? 1 : 0;
-    }
     const int lim = k + dh;
     const uint32_t in0 = __ballot_sync(0xffffffffu, e0 < N && r0 < lim);
     const uint32_t in1 = __ballot_sync(0xffffffffu, e1 < N && r1 < lim);
@@ -452,19 +450,28 @@ __device__ __forceinline__ void select_token(
     }
     const uint64_t fin = (routed & ~missing) | lore | fetch | subs;
     // canonical slot order: descending router probability, lowest index first
-    uint64_t rem = fin;
+    // (each final expert's rank among the at most k final experts)
+    int c0 = 0, c1 = 0;
+    for (uint64_t m = fin; m; m &= m - 1) {
+        const int j = __ffsll((long long)m) - 1;
+        const float aj = __shfl_sync(0xffffffffu, j < 32 ? a0 : a1, j & 31);
+        c0 += (aj > a0 || (aj == a0 && j < e0)) ? 1 : 0;
+        c1 += (aj > a1 || (aj == a1 && j < e1)) ? 1 : 0;
+    }
+    const bool f0 = (fin >> e0) & 1, f1 = (fin >> e1) & 1;
     float gsum = 0.f;
     int idx[kMaxTopK];
     float gate[kMaxTopK];
     for (int j = 0; j < k; ++j) {
-        if (!rem) { idx[j] = -1; gate[j] = 0.f; continue; }
-        float v; int i;
-        lane_best(a0, a1, rem, lane, v, i);
-        warp_argmax(v, i);
+        const bool own0 = f0 && c0 == j, own1 = f1 && c1 == j;
+        const uint32_t b = __ballot_sync(0xffffffffu, own0 || own1);
+        if (!b) { idx[j] = -1; gate[j] = 0.f; continue; }
+        const int owner = __ffs(b) - 1;
+        const float v = __shfl_sync(0xffffffffu, own0 ? a0 : a1, owner);
+        const int i = __shfl_sync(0xffffffffu, own0 ? e0 : e1, owner);
         idx[j] = i;
         gate[j] = v;
         gsum += v;
-        rem &= ~(1ull << i);
     }
     if (lane == 0) {
         for (int j = 0; j < k; ++j) {
