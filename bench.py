@@ -437,6 +437,22 @@ def main():
     staging = {"gbps": reps * nbytes / stage_s / 1e9, "bytes_per_call": nbytes,
                "experts_per_call": n_stage, "note": "pinned host -> HBM, cudaMemcpyAsync on a side stream"}
 
+    # ---- routing statistics of the last layer forward of each copy (the
+    # counters of moe_select_resident: hit / substitute / LoRE / fetch slots,
+    # overlap of the routed set with the prefetch set, mean delta_hat, delta*)
+    torch.cuda.synchronize()
+    cnt = np.zeros(moe.MOE_NUM_COUNTERS, np.int64)
+    for c in range(n_copies):
+        cnt += bufs[c].counters.cpu().numpy().astype(np.int64)
+    toks = n_copies * T
+    routing = {"tokens": toks, "slots": toks * cfg.k,
+               "hit": int(cnt[0]), "substitute": int(cnt[1]), "lore": int(cnt[2]), "fetch": int(cnt[3]),
+               "shortfall_tokens": int(cnt[7]),
+               # counted only when the prefetch set takes part in the selection
+               "overlap_rate": float(cnt[4]) / toks if cfg.use_prefetch_mask else None,
+               "mean_delta_hat": float(cnt[5]) / toks, "mean_delta_star": float(cnt[6]) / toks,
+               "tau": cfg.tau, "gamma": cfg.gamma}
+
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -456,6 +472,7 @@ def main():
                 "note": "moe_layer_forward per step with pinned-host copies and a stream sync, no graph"},
         "gpu_launches": int(launches_per_step * args.steps),
         "staging": staging,
+        "routing": routing,
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -99,6 +99,7 @@ _PROTOS = {
                            _P], C.c_int),
     "moe_check": ([_P, _P, C.POINTER(C.c_int), C.POINTER(C.c_int32)], C.c_int),
     "moe_testing_fail_copies_after": ([C.c_int], None),
+    "moe_testing_wait_timeout": ([C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
 }
 
 
@@ -352,6 +353,13 @@ def moe_check(ws, stream=None):
 
 def moe_testing_fail_copies_after(n: int):
     lib().moe_testing_fail_copies_after(int(n))
+
+
+def moe_testing_wait_timeout(ws, stream=None):
+    """Queue a kernel whose device wait cannot finish; it times out (about 1 s)
+    and records MOE_ERR_TIMEOUT in ws's error word (read it with moe_check)."""
+    _check(lib().moe_testing_wait_timeout(C.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size(),
+                                          _stream(stream)), "moe_testing_wait_timeout")
 
 
 from .layer import DeviceLayer, LayerBuffers  # noqa: E402,F401

@@ -154,6 +154,10 @@ struct EpilogueArgs {
 // partial-row reduction + LoRE B + combine in one launch (moe_layer_forward)
 cudaError_t launch_layer_epilogue(const EpilogueArgs& a, cudaStream_t st);
 
+// test probe: a bounded wait on an mbarrier nothing arrives on (records
+// MOE_ERR_TIMEOUT in err)
+cudaError_t launch_wait_timeout_probe(DevError* err, cudaStream_t st);
+
 struct CombineArgs {
     const float* y_perm; const int32_t* inv_perm; const float* final_gate;
     const int32_t* final_kind; const float *y_shared, *y_lore; int T, d, k; float* out;

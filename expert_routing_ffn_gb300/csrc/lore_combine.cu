@@ -297,6 +297,25 @@ cudaError_t launch_layer_epilogue(const EpilogueArgs& a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+// One warp waits on a fresh mbarrier (arrival count 1) that no thread ever
+// arrives on: the wait gives up after its wall-clock bound and the kernel
+// records MOE_ERR_TIMEOUT, as every wait of the library does.
+__global__ void wait_timeout_probe_kernel(DevError* err) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const bool done = mbar_wait(&bar, 0);
+    if (!done && threadIdx.x == 0) set_error(err, MOE_ERR_TIMEOUT, -3);
+}
+
+cudaError_t launch_wait_timeout_probe(DevError* err, cudaStream_t st) {
+    wait_timeout_probe_kernel<<<1, 32, 0, st>>>(err);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_lore_z(const LoreArgs& a, cudaStream_t st) {
     if (a.T == 0) return cudaSuccess;
     dim3 gz(a.T * a.k, (a.r + 3) / 4);

@@ -9,6 +9,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "../../include/moe_testing.h"
 #include "tma.h"
 
 using namespace moe;
@@ -381,6 +382,13 @@ moe_status moe_stage_experts(const moe_dims* dims, uint64_t host_fetch_mask,
 
 // test hook: make the n-th and later copies of moe_stage_experts fail (-1: off)
 void moe_testing_fail_copies_after(int n) { g_fail_copies_after.store(n); }
+
+moe_status moe_testing_wait_timeout(void* ws, size_t ws_bytes, void* stream) {
+    if (!ws || ws_bytes < kAlign || reinterpret_cast<uintptr_t>(ws) % kAlign) return MOE_ERR_INVALID_ARG;
+    MOE_CUDA(launch_wait_timeout_probe(static_cast<DevError*>(ws), S(stream)));
+    count();
+    return MOE_OK;
+}
 
 moe_status moe_permute(const moe_dims* dims, const int32_t* final_idx, const int32_t* final_kind,
                        int32_t* expert_offsets, int32_t* perm, int32_t* inv_perm, void* ws,

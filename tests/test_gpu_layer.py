@@ -296,3 +296,18 @@ def test_floe_sparse_matches_oracle(T):
             assert (np.nonzero(bits)[0] == R.kept[t, so]).all(), f"kept channels differ (token {t})"
             n_checked += 1
     assert n_checked > 0
+
+
+def test_bounded_wait_times_out_and_the_context_stays_usable():
+    """A device wait that can never finish (an mbarrier nothing arrives on)
+    ends after its wall-clock bound with MOE_ERR_TIMEOUT in the error word, not
+    with a hang or a trap; the next layer call on the same context is exact."""
+    layer = _device("tiny", 16)
+    moe.moe_testing_wait_timeout(layer.ws)
+    st, det = moe.moe_check(layer.ws)
+    assert (st, det) == (moe.MOE_ERR_TIMEOUT, -3)
+    assert moe.moe_check(layer.ws) == (moe.MOE_OK, 0)  # moe_check cleared the word
+    cfg, W, layer, x, bufs, st, det = _run("tiny", 16)
+    assert st == moe.MOE_OK
+    R = oracle.layer_forward(cfg, W, x)
+    check_output(cfg, R, bufs.out)
