@@ -145,6 +145,10 @@ __global__ void __launch_bounds__(256) route_logits_tiled_kernel(
     int T, int d, int N, int n_out, float* __restrict__ logits_r, float* __restrict__ logits_p,
     float* __restrict__ score) {
     constexpr int TT = 64, TO = 64, KC = 32;
+    constexpr int V = Vec<W>::n;
+    constexpr int XL = TT * KC / V / 256;  // 16-byte loads per thread per chunk (token tiles)
+    constexpr int WL = TO * KC / V / 256;  // (weight rows)
+    static_assert(XL >= 1 && WL >= 1, "tile and chunk sizes");
     __shared__ __align__(16) float xs[KC][TT];    // router input x
     __shared__ __align__(16) float xps[KC][TT];   // prefetch input x_pre
     __shared__ __align__(16) float ws[KC][TO];
@@ -152,50 +156,68 @@ __global__ void __launch_bounds__(256) route_logits_tiled_kernel(
     const int tid = threadIdx.x;
     const int tq = tid & 15, oq = tid >> 4;       // 16 token quads x 16 row quads
     const bool sep = x_pre != x;
+    const int n_rows = 2 * N;                     // router rows, then prefetch rows (the scorer runs apart)
     float acc[4][4];
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
-    for (int k0 = 0; k0 < d; k0 += KC) {
-        // stage 64 x 32 values of x (and x_pre) and of the 64 weight rows,
-        // 16 bytes per load (8 bf16 / 4 fp32), transposed into K-major smem
-        constexpr int V = Vec<W>::n;
-        for (int i = tid; i < TT * KC / V; i += 256) {
-            const int tt = i / (KC / V), kv = (i % (KC / V)) * V, tok = t0 + tt;
-            float v[V], vp[V];
+    // the next chunk's global loads, issued before the current chunk's products
+    uint4 rx[XL], rxp[XL], rw[WL];
+    auto load = [&](int k0) {
 #pragma unroll
-            for (int u = 0; u < V; ++u) { v[u] = 0.f; vp[u] = 0.f; }
+        for (int j = 0; j < XL; ++j) {
+            const int i = tid + j * 256;
+            const int tt = i / (KC / V), kv = (i % (KC / V)) * V, tok = t0 + tt;
+            rx[j] = make_uint4(0, 0, 0, 0);
+            rxp[j] = make_uint4(0, 0, 0, 0);
             if (tok < T) {
-                unpack16(*reinterpret_cast<const uint4*>(x + (size_t)tok * d + k0 + kv), v, (W*)nullptr);
-                if (sep) unpack16(*reinterpret_cast<const uint4*>(x_pre + (size_t)tok * d + k0 + kv), vp, (W*)nullptr);
+                rx[j] = *reinterpret_cast<const uint4*>(x + (size_t)tok * d + k0 + kv);
+                if (sep) rxp[j] = *reinterpret_cast<const uint4*>(x_pre + (size_t)tok * d + k0 + kv);
             }
+        }
+#pragma unroll
+        for (int j = 0; j < WL; ++j) {
+            const int i = tid + j * 256;
+            const int oo = i / (KC / V), kv = (i % (KC / V)) * V, o = o0 + oo;
+            rw[j] = make_uint4(0, 0, 0, 0);
+            if (o < N) rw[j] = *reinterpret_cast<const uint4*>(w_router + (size_t)o * d + k0 + kv);
+            else if (o < n_rows) rw[j] = *reinterpret_cast<const uint4*>(w_prefetch + (size_t)(o - N) * d + k0 + kv);
+        }
+    };
+    load(0);
+    for (int k0 = 0; k0 < d; k0 += KC) {
+        // registers -> K-major shared tiles (fp32)
+#pragma unroll
+        for (int j = 0; j < XL; ++j) {
+            const int i = tid + j * 256;
+            const int tt = i / (KC / V), kv = (i % (KC / V)) * V;
+            float v[V], vp[V];
+            unpack16(rx[j], v, (W*)nullptr);
+            unpack16(rxp[j], vp, (W*)nullptr);
 #pragma unroll
             for (int u = 0; u < V; ++u) {
                 xs[kv + u][tt] = v[u];
                 xps[kv + u][tt] = sep ? vp[u] : v[u];
             }
         }
-        for (int i = tid; i < TO * KC / V; i += 256) {
-            const int oo = i / (KC / V), kv = (i % (KC / V)) * V, o = o0 + oo;
+#pragma unroll
+        for (int j = 0; j < WL; ++j) {
+            const int i = tid + j * 256;
+            const int oo = i / (KC / V), kv = (i % (KC / V)) * V;
             float v[V];
-#pragma unroll
-            for (int u = 0; u < V; ++u) v[u] = 0.f;
-            if (o < N) unpack16(*reinterpret_cast<const uint4*>(w_router + (size_t)o * d + k0 + kv), v, (W*)nullptr);
-            else if (o < 2 * N) unpack16(*reinterpret_cast<const uint4*>(w_prefetch + (size_t)(o - N) * d + k0 + kv), v, (W*)nullptr);
-            else if (o < n_out)
-#pragma unroll
-                for (int u = 0; u < V; ++u) v[u] = w_ord[k0 + kv + u];
+            unpack16(rw[j], v, (W*)nullptr);
 #pragma unroll
             for (int u = 0; u < V; ++u) ws[kv + u][oo] = v[u];
         }
         __syncthreads();
+        if (k0 + KC < d) load(k0 + KC);
         float part[4][4];
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll
             for (int b = 0; b < 4; ++b) part[a][b] = 0.f;
-        // rows o < N use x, the prefetch rows and the scorer use x_pre
+        // rows o < N use x, the prefetch rows use x_pre
         const bool pre = o0 + oq * 4 >= N;
 #pragma unroll 8
         for (int kk = 0; kk < KC; ++kk) {
@@ -222,10 +244,35 @@ __global__ void __launch_bounds__(256) route_logits_tiled_kernel(
         for (int b = 0; b < 4; ++b) {
             const int o = o0 + oq * 4 + b;
             if (o < N) logits_r[(size_t)tok * N + o] = acc[a][b] + (bias ? bias[o] : 0.f);
-            else if (o < 2 * N) logits_p[(size_t)tok * N + (o - N)] = acc[a][b];
-            else if (o < n_out) score[tok] = acc[a][b];
+            else if (o < n_rows) logits_p[(size_t)tok * N + (o - N)] = acc[a][b];
         }
     }
+    (void)n_out;
+    (void)w_ord;
+    (void)score;
+}
+
+// The ordinal scorer s = w . x_pre for large batches: one warp per token,
+// lanes over 16-byte chunks of d, each lane's products in order, then a warp
+// tree (the accumulation of route_logits_kernel).
+template <typename W>
+__global__ void __launch_bounds__(256) route_score_kernel(const W* __restrict__ x_pre,
+                                                          const float* __restrict__ w_ord, int T, int d,
+                                                          float* __restrict__ score) {
+    constexpr int V = Vec<W>::n;
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;
+    const uint4* xr = reinterpret_cast<const uint4*>(x_pre + (size_t)t * d);
+    float acc = 0.f;
+    for (int q = lane; q < d / V; q += 32) {
+        float xv[V];
+        unpack16(xr[q], xv, (W*)nullptr);
+#pragma unroll
+        for (int j = 0; j < V; ++j) acc = fmaf(xv[j], w_ord[q * V + j], acc);
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) score[t] = acc;
 }
 
 // (value, index) argmax across the warp: larger value wins, equal values go
@@ -644,11 +691,15 @@ static cudaError_t launch_logits_t(const LogitsArgs& a, cudaStream_t st) {
     // (a row quad must not straddle the router / prefetch-router boundary when
     // the two routers read different inputs)
     if (a.T >= 2048 && (a.x_pre == nullptr || a.x_pre == a.x || a.N % 4 == 0)) {
-        const int n_out = a.has_prefetch ? 2 * a.N + 1 : a.N;
-        dim3 grid((a.T + 63) / 64, (n_out + 63) / 64);
+        const int rows = a.has_prefetch ? 2 * a.N : a.N;
+        dim3 grid((a.T + 63) / 64, (rows + 63) / 64);
         route_logits_tiled_kernel<W><<<grid, 256, 0, st>>>(
             (const W*)a.x, (const W*)(a.x_pre ? a.x_pre : a.x), (const W*)a.w_router, a.bias,
-            (const W*)a.w_prefetch, a.w_ord, a.T, a.d, a.N, n_out, a.logits_r, a.logits_p, a.score);
+            (const W*)a.w_prefetch, a.w_ord, a.T, a.d, a.N, rows, a.logits_r, a.logits_p, a.score);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess || !a.has_prefetch) return e;
+        route_score_kernel<W><<<(a.T + 7) / 8, 256, 0, st>>>((const W*)(a.x_pre ? a.x_pre : a.x), a.w_ord, a.T,
+                                                             a.d, a.score);
         return cudaGetLastError();
     }
     const int n_out = a.has_prefetch ? 2 * a.N + 1 : a.N;
