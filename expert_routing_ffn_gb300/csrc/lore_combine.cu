@@ -9,7 +9,7 @@
 namespace moe {
 
 // z[t, s, :] = g_s * A_e x_t for a LoRE slot (t, s) (zero for other slots):
-// one block per slot, warps over the r rank rows, lanes over d.
+// one block per slot, its warps over the r rank rows, lanes over d.
 template <typename W>
 __global__ void __launch_bounds__(256) lore_z_kernel(const W* __restrict__ x,
                                                      const int32_t* __restrict__ final_idx,
@@ -22,11 +22,10 @@ __global__ void __launch_bounds__(256) lore_z_kernel(const W* __restrict__ x,
     const int slot = blockIdx.x;
     const int t = slot / k;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-    const int q_begin = blockIdx.y * nw, q_end = min(r, q_begin + nw);  // one rank row per warp
+    const int q_begin = 0, q_end = r;  // rank rows q = warp, warp + nw, ...
     const int e = final_idx[slot];
     if (final_kind[slot] != MOE_KIND_LORE || e < 0 || e >= N) {
-        if (final_kind[slot] == MOE_KIND_LORE && err && tid == 0 && blockIdx.y == 0)
-            set_error(err, MOE_ERR_DEVICE_INDEX, slot);
+        if (final_kind[slot] == MOE_KIND_LORE && err && tid == 0) set_error(err, MOE_ERR_DEVICE_INDEX, slot);
         for (int q = q_begin + tid; q < q_end; q += blockDim.x) z[(size_t)slot * r + q] = 0.f;
         return;
     }
@@ -61,14 +60,17 @@ __global__ void __launch_bounds__(256) lore_b_kernel(const int32_t* __restrict__
     __shared__ int s_e[kMaxTopK];
     __shared__ float s_z[kMaxTopK * 64];
     __shared__ int s_n;
-    if (threadIdx.x == 0) {
-        int n = 0;
-        for (int s = 0; s < k; ++s) {
+    if (threadIdx.x < 32) {  // one lane per slot, LoRE slots compacted in slot order
+        const int s = threadIdx.x;
+        bool is_lore = false;
+        if (s < k) {
             const size_t sl = (size_t)t * k + s;
             const int e = final_idx[sl];
-            if (final_kind[sl] == MOE_KIND_LORE && e >= 0 && e < N) s_e[n++] = s;
+            is_lore = final_kind[sl] == MOE_KIND_LORE && e >= 0 && e < N;
         }
-        s_n = n;
+        const uint32_t b = __ballot_sync(0xffffffffu, is_lore);
+        if (is_lore) s_e[__popc(b & ((1u << s) - 1u))] = s;
+        if (s == 0) s_n = __popc(b);
     }
     __syncthreads();
     const int n = s_n;
@@ -107,17 +109,20 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       int k, float* __restrict__ out) {
     const int t = blockIdx.x;
     const int q = blockIdx.y * blockDim.x + threadIdx.x;  // float4 column group
-    __shared__ int s_pos[kMaxTopK];
+    __shared__ int s_pos[kMaxTopK], s_kind[kMaxTopK];
     __shared__ float s_g[kMaxTopK];
     __shared__ float s_lg;
-    if (threadIdx.x == 0) {
+    if (threadIdx.x < k) {  // one thread per slot
+        const size_t sl = (size_t)t * k + threadIdx.x;
+        s_pos[threadIdx.x] = inv_perm[sl];
+        s_g[threadIdx.x] = final_gate[sl];
+        s_kind[threadIdx.x] = final_kind[sl];
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {  // the LoRE gates summed in slot order
         float lg = 0.f;
-        for (int s = 0; s < k; ++s) {
-            const size_t sl = (size_t)t * k + s;
-            s_pos[s] = inv_perm[sl];
-            s_g[s] = final_gate[sl];
-            if (final_kind[sl] == MOE_KIND_LORE) lg += final_gate[sl];
-        }
+        for (int s = 0; s < k; ++s)
+            if (s_kind[s] == MOE_KIND_LORE) lg += s_g[s];
         s_lg = lg;
     }
     __syncthreads();
@@ -166,22 +171,28 @@ __global__ void __launch_bounds__(256) layer_epilogue_kernel(const EpilogueArgs 
     __shared__ float4 s_y[kMaxTopK][32];
     __shared__ float4 s_sh[32];
     __shared__ float4 s_yl[32];
-    if (threadIdx.x == 0) {
-        float lg = 0.f;
-        int nl = 0;
-        for (int s = 0; s < k; ++s) {
+    __shared__ int s_kind[kMaxTopK];
+    if (threadIdx.x < 32) {  // one lane per slot
+        const int s = threadIdx.x;
+        bool lore_term = false;
+        if (s < k) {
             const size_t sl = (size_t)t * k + s;
             s_pos[s] = a.inv_perm[sl];
             s_g[s] = a.final_gate[sl];
             s_e[s] = a.final_idx[sl];
-            if (a.final_kind[sl] == MOE_KIND_LORE) {
-                lg += a.final_gate[sl];
-                const int e = a.final_idx[sl];
-                if (a.lore_b && e >= 0 && e < N) s_lore[nl++] = s;
-            }
+            s_kind[s] = a.final_kind[sl];
+            lore_term = s_kind[s] == MOE_KIND_LORE && a.lore_b && s_e[s] >= 0 && s_e[s] < N;
         }
-        s_lg = lg;
-        s_nl = nl;
+        const uint32_t b = __ballot_sync(0xffffffffu, lore_term);
+        if (lore_term) s_lore[__popc(b & ((1u << s) - 1u))] = s;
+        __syncwarp();
+        if (s == 0) {  // the LoRE gates summed in slot order
+            float lg = 0.f;
+            for (int j = 0; j < k; ++j)
+                if (s_kind[j] == MOE_KIND_LORE) lg += s_g[j];
+            s_lg = lg;
+            s_nl = __popc(b);
+        }
     }
     __syncthreads();
     const int nl = s_nl;
@@ -318,13 +329,13 @@ cudaError_t launch_wait_timeout_probe(DevError* err, cudaStream_t st) {
 
 cudaError_t launch_lore_z(const LoreArgs& a, cudaStream_t st) {
     if (a.T == 0) return cudaSuccess;
-    dim3 gz(a.T * a.k, (a.r + 3) / 4);
+    const dim3 gz(a.T * a.k);
     if (a.bf16)
-        lore_z_kernel<__nv_bfloat16><<<gz, 128, 0, st>>>(
+        lore_z_kernel<__nv_bfloat16><<<gz, 256, 0, st>>>(
             (const __nv_bfloat16*)a.x, a.final_idx, a.final_kind, a.final_gate,
             (const __nv_bfloat16*)a.A, a.d, a.k, a.r, a.N, a.z, a.err);
     else
-        lore_z_kernel<float><<<gz, 128, 0, st>>>((const float*)a.x, a.final_idx, a.final_kind,
+        lore_z_kernel<float><<<gz, 256, 0, st>>>((const float*)a.x, a.final_idx, a.final_kind,
                                                       a.final_gate, (const float*)a.A, a.d, a.k,
                                                       a.r, a.N, a.z, a.err);
     return cudaGetLastError();
@@ -333,17 +344,17 @@ cudaError_t launch_lore_z(const LoreArgs& a, cudaStream_t st) {
 cudaError_t launch_lore(const LoreArgs& a, cudaStream_t st) {
     if (a.T == 0) return cudaSuccess;
     const int n_slots = a.T * a.k;
-    dim3 gz(n_slots, (a.r + 3) / 4);  // 4 warps = 4 rank rows per block
+    const dim3 gz(n_slots);
     dim3 gb(a.T, (a.d + 255) / 256);
     if (a.bf16) {
-        lore_z_kernel<__nv_bfloat16><<<gz, 128, 0, st>>>(
+        lore_z_kernel<__nv_bfloat16><<<gz, 256, 0, st>>>(
             (const __nv_bfloat16*)a.x, a.final_idx, a.final_kind, a.final_gate,
             (const __nv_bfloat16*)a.A, a.d, a.k, a.r, a.N, a.z, a.err);
         lore_b_kernel<__nv_bfloat16><<<gb, 256, 0, st>>>(a.final_idx, a.final_kind,
                                                          (const __nv_bfloat16*)a.B, a.d, a.k, a.r,
                                                          a.N, a.z, a.y_lore);
     } else {
-        lore_z_kernel<float><<<gz, 128, 0, st>>>((const float*)a.x, a.final_idx, a.final_kind,
+        lore_z_kernel<float><<<gz, 256, 0, st>>>((const float*)a.x, a.final_idx, a.final_kind,
                                                       a.final_gate, (const float*)a.A, a.d, a.k,
                                                       a.r, a.N, a.z, a.err);
         lore_b_kernel<float><<<gb, 256, 0, st>>>(a.final_idx, a.final_kind, (const float*)a.B, a.d,
