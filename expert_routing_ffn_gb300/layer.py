@@ -7,8 +7,9 @@ import ctypes as C
 
 import torch
 
-from . import (MOE_NUM_COUNTERS, make_dims, moe_expert_table_init, moe_expert_table_size,
-               moe_layer_args, moe_layer_forward, moe_layer_outputs, moe_workspace_size)
+from . import (MOE_NUM_COUNTERS, _check, _stream, lib, make_dims, moe_expert_table_init,
+               moe_expert_table_size, moe_layer_args, moe_layer_forward, moe_layer_outputs,
+               moe_workspace_size)
 
 
 def as_i64(mask: int) -> int:
@@ -77,6 +78,7 @@ class DeviceLayer:
         shared."""
         other = object.__new__(DeviceLayer)
         other.__dict__.update(self.__dict__)
+        other.__dict__.pop("_call_cache", None)  # cached ABI structs point at this layer's tensors
         for name in ("w_gate", "w_up", "w_down", "sh_gate", "sh_up", "sh_down"):
             t = getattr(self, name)
             setattr(other, name, None if t is None else t.clone())
@@ -118,10 +120,14 @@ class LayerBuffers:
         self.out = torch.empty((T, d), **f32)
 
     def outputs_struct(self) -> moe_layer_outputs:
-        o = moe_layer_outputs()
-        for name, _ in moe_layer_outputs._fields_:
-            tns = getattr(self, name)
-            setattr(o, name, None if tns is None else tns.data_ptr())
+        """The output pointers for the ABI (built once: the buffers never move)."""
+        o = getattr(self, "_outs", None)
+        if o is None:
+            o = moe_layer_outputs()
+            for name, _ in moe_layer_outputs._fields_:
+                tns = getattr(self, name)
+                setattr(o, name, None if tns is None else tns.data_ptr())
+            self._outs = o
         return o
 
 
@@ -150,11 +156,24 @@ def layer_args(layer: DeviceLayer, x, x_pre=None, policy=None, gamma=None, tau=N
 
 
 def forward(layer: DeviceLayer, bufs: LayerBuffers, x, stream=None, **kw):
-    """One layer forward through moe_layer_forward for x [T, d] (T <= bufs.T)."""
+    """One layer forward through moe_layer_forward for x [T, d] (T <= bufs.T).
+
+    The ABI structs of a call (dims for T, the layer arguments for this x and
+    these options, the output pointers) are built once and reused while the
+    tensors stay where they are, so a decode loop pays only the ABI call."""
     T = x.shape[0]
     assert T <= bufs.T and x.is_contiguous() and x.dtype == layer.dt
-    dims = layer.dims.with_T(T)
-    args = layer_args(layer, x, **kw)
+    cache = layer.__dict__.setdefault("_call_cache", {})
+    key = (T, x.data_ptr(), tuple(sorted(kw.items())), layer.ws.data_ptr())
+    hit = cache.get(key)
+    if hit is None:
+        if len(cache) > 64:
+            cache.clear()
+        hit = (layer.dims.with_T(T), layer_args(layer, x, **kw), C.c_void_p(layer.ws.data_ptr()),
+               layer.ws.numel())
+        cache[key] = hit
+    dims, args, ws_ptr, ws_bytes = hit
     outs = bufs.outputs_struct()
-    moe_layer_forward(dims, args, outs, layer.ws, stream)
+    _check(lib().moe_layer_forward(C.byref(dims), C.byref(args), C.byref(outs), ws_ptr, ws_bytes,
+                                   _stream(stream)), "moe_layer_forward")
     return bufs
