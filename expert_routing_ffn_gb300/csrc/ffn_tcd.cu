@@ -74,7 +74,8 @@ struct TcdParams {
     const PlanHeader* hdr;
     const Seg* segs;
     float* partial;
-    int d, N;
+    float* u_out;  // up-only mode: u[pos, channel] (fp32, row = permuted position, I columns)
+    int d, N, I;
     DevError* err;
 };
 
@@ -108,7 +109,9 @@ __device__ __forceinline__ bool tcd_begin(const TcdParams& p, TcdWalk& w) {
     return true;
 }
 
-template <int NT>
+// UP = true: FloE's first pass, U = W_up x only (phase A without gate, no
+// phase B), written to p.u_out for every routed row and channel of the plan.
+template <int NT, bool UP>
 __global__ void __launch_bounds__(kTcdThreads, 1) ffn_tcd_kernel(const __grid_constant__ TcdParams p) {
     using C = TcdCfg<NT>;
     constexpr int NS = C::kNS, HT = C::kHT;
@@ -185,16 +188,18 @@ __global__ void __launch_bounds__(kTcdThreads, 1) ffn_tcd_kernel(const __grid_co
                     for (int t = 0; ok && t < ntl; ++t) {
                         const int rows = min(128, clen - t * 128);
                         for (int kc = 0; kc < nkA; ++kc, ++it) {
-                            const int st = acquire(2u * rows * 128u + xbytes);
+                            const int st = acquire((UP ? 1u : 2u) * rows * 128u + xbytes);
                             if (st < 0) { ok = false; break; }
                             const uint32_t dst = smem_base + st * C::kStage;
                             if (rows == 128) {  // whole tile: one 128-row box per matrix
-                                tma_load_2d_hint(dst, E->tmap[0], kc * 64, c0 + t * 128, &full[st], pol_w);
+                                if (!UP)
+                                    tma_load_2d_hint(dst, E->tmap[0], kc * 64, c0 + t * 128, &full[st], pol_w);
                                 tma_load_2d_hint(dst + kTcdW, E->tmap[1], kc * 64, c0 + t * 128, &full[st], pol_w);
                             } else {
                                 for (int j = 0; j < rows / 16; ++j) {
-                                    tma_load_2d_hint(dst + j * 2048, E->tmap_dec[0], kc * 64,
-                                                     c0 + t * 128 + j * 16, &full[st], pol_w);
+                                    if (!UP)
+                                        tma_load_2d_hint(dst + j * 2048, E->tmap_dec[0], kc * 64,
+                                                         c0 + t * 128 + j * 16, &full[st], pol_w);
                                     tma_load_2d_hint(dst + kTcdW + j * 2048, E->tmap_dec[1], kc * 64,
                                                      c0 + t * 128 + j * 16, &full[st], pol_w);
                                 }
@@ -209,7 +214,7 @@ __global__ void __launch_bounds__(kTcdThreads, 1) ffn_tcd_kernel(const __grid_co
                         }
                     }
                     // phase B: Wd rows of every tile, 128 columns of d per stage
-                    for (int dc = 0; ok && dc < nkB; ++dc) {
+                    for (int dc = 0; !UP && ok && dc < nkB; ++dc) {
                         for (int t = 0; t < ntl; ++t, ++it) {
                             const int rows = min(128, clen - t * 128);
                             const int st = acquire(2u * rows * 128u);
@@ -264,7 +269,7 @@ __global__ void __launch_bounds__(kTcdThreads, 1) ffn_tcd_kernel(const __grid_co
                             for (int kk = 0; kk < 4; ++kk) {
                                 const uint64_t bx = smem_desc(a + 2 * kTcdW + kk * 32, 16, 1024);
                                 const uint32_t acc = (kc | kk) ? 1u : 0u;
-                                tc_mma(tg, smem_desc(a + kk * 32, 16, 1024), bx, idA, acc);
+                                if (!UP) tc_mma(tg, smem_desc(a + kk * 32, 16, 1024), bx, idA, acc);
                                 tc_mma(tu, smem_desc(a + kTcdW + kk * 32, 16, 1024), bx, idA, acc);
                             }
                             tc_commit(&empty[st]);
@@ -272,33 +277,35 @@ __global__ void __launch_bounds__(kTcdThreads, 1) ffn_tcd_kernel(const __grid_co
                         if (!ok) break;
                         tc_commit(&afull[ab]);
                     }
-                    // every h tile of the chunk written by the epilogue
-                    for (int t = 0; ok && t < ntl; ++t) {
-                        if (!tc_wait(&hready[t], hph[t] & 1, abort_flag, p.err, 15)) ok = false;
-                        ++hph[t];
-                    }
-                    tc_fence_after();
-                    for (int dc = 0; ok && dc < nkB; ++dc, ++ny) {
-                        const int yb = ny & 1;
-                        if (!tc_wait(&yempty[yb], ((ny >> 1) & 1) ^ 1, abort_flag, p.err, 16)) { ok = false; break; }
-                        tc_fence_after();
-                        const uint32_t ty = tmem_base + 4 * NT + yb * NT;
-                        for (int t = 0; t < ntl; ++t, ++it) {
-                            const int rows = min(128, clen - t * 128);
-                            const int st = it % NS;
-                            if (!tc_wait(&full[st], (it / NS) & 1, abort_flag, p.err, 17)) { ok = false; break; }
-                            tc_fence_after();
-                            const uint32_t a = smem_base + st * C::kStage;
-                            const uint32_t hb = h_base + t * C::kHTile;
-                            for (int j = 0; j < rows / 16; ++j) {
-                                const uint64_t ad = smem_desc(a + j * 2048, kTcdW, 1024);
-                                const uint64_t bd = smem_desc(hb + (j >> 2) * (NT * 128) + (j & 3) * 32, 16, 1024);
-                                tc_mma(ty, ad, bd, idB, (t | j) ? 1u : 0u);
-                            }
-                            tc_commit(&empty[st]);
+                    if constexpr (!UP) {
+                        // every h tile of the chunk written by the epilogue
+                        for (int t = 0; ok && t < ntl; ++t) {
+                            if (!tc_wait(&hready[t], hph[t] & 1, abort_flag, p.err, 15)) ok = false;
+                            ++hph[t];
                         }
-                        if (!ok) break;
-                        tc_commit(&yfull[yb]);
+                        tc_fence_after();
+                        for (int dc = 0; ok && dc < nkB; ++dc, ++ny) {
+                            const int yb = ny & 1;
+                            if (!tc_wait(&yempty[yb], ((ny >> 1) & 1) ^ 1, abort_flag, p.err, 16)) { ok = false; break; }
+                            tc_fence_after();
+                            const uint32_t ty = tmem_base + 4 * NT + yb * NT;
+                            for (int t = 0; t < ntl; ++t, ++it) {
+                                const int rows = min(128, clen - t * 128);
+                                const int st = it % NS;
+                                if (!tc_wait(&full[st], (it / NS) & 1, abort_flag, p.err, 17)) { ok = false; break; }
+                                tc_fence_after();
+                                const uint32_t a = smem_base + st * C::kStage;
+                                const uint32_t hb = h_base + t * C::kHTile;
+                                for (int j = 0; j < rows / 16; ++j) {
+                                    const uint64_t ad = smem_desc(a + j * 2048, kTcdW, 1024);
+                                    const uint64_t bd = smem_desc(hb + (j >> 2) * (NT * 128) + (j & 3) * 32, 16, 1024);
+                                    tc_mma(ty, ad, bd, idB, (t | j) ? 1u : 0u);
+                                }
+                                tc_commit(&empty[st]);
+                            }
+                            if (!ok) break;
+                            tc_commit(&yfull[yb]);
+                        }
                     }
                 }
             }
@@ -333,6 +340,24 @@ __global__ void __launch_bounds__(kTcdThreads, 1) ffn_tcd_kernel(const __grid_co
                     tc_fence_after();
                     const int rows = min(128, clen - t * 128);
                     const uint32_t tg = tmem_base + lane_off + ab * 2 * NT;
+                    if (UP) {
+                        // u[row0 + tok, channel] for this thread's channel
+                        const int ch = c0 + t * 128 + r;
+#pragma unroll 1
+                        for (int c = 0; c < NT && c < R; c += 16) {
+                            float u[16];
+                            tmem_ld16(tg + NT + c, u);
+                            if (r < rows) {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    if (c + i < R) p.u_out[(size_t)(S.row0 + c + i) * p.I + ch] = u[i];
+                            }
+                        }
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&aempty[ab]);
+                        continue;
+                    }
                     unsigned char* hb = tcd_smem_raw + (h_base - smem_u32(tcd_smem_raw)) + t * C::kHTile +
                                         (r >> 6) * (NT * 128);
                     const int cin = r & 63;
@@ -362,7 +387,7 @@ __global__ void __launch_bounds__(kTcdThreads, 1) ffn_tcd_kernel(const __grid_co
                 }
                 if (!ok) break;
                 // phase B epilogues: Y columns of d -> partial rows
-                for (int dc = 0; dc < nkB; ++dc, ++ny) {
+                for (int dc = 0; !UP && dc < nkB; ++dc, ++ny) {
                     const int yb = ny & 1;
                     if (!wait_warp(&yfull[yb], (ny >> 1) & 1, 20)) { ok = false; break; }
                     tc_fence_after();
@@ -398,7 +423,7 @@ __global__ void __launch_bounds__(kTcdThreads, 1) ffn_tcd_kernel(const __grid_co
     }
 }
 
-template <int NT>
+template <int NT, bool UP>
 static cudaError_t launch_tcd_nt(const TcdLaunch& a, cudaStream_t st) {
     using C = TcdCfg<NT>;
     TcdParams p;
@@ -415,19 +440,20 @@ static cudaError_t launch_tcd_nt(const TcdLaunch& a, cudaStream_t st) {
     }
     p.perm = a.perm; p.topk = a.k;
     p.table = a.table; p.hdr = a.hdr; p.segs = a.segs; p.partial = a.partial;
-    p.d = a.d; p.N = a.N; p.err = a.err;
-    cudaError_t e = allow_max_smem(ffn_tcd_kernel<NT>);
+    p.u_out = a.u_out; p.d = a.d; p.N = a.N; p.I = a.I; p.err = a.err;
+    auto kernel = ffn_tcd_kernel<NT, UP>;
+    cudaError_t e = allow_max_smem(kernel);
     if (e != cudaSuccess) return e;
-    ffn_tcd_kernel<NT><<<a.grid, kTcdThreads, C::kSmem, st>>>(p);
-    return note_launch(reinterpret_cast<const void*>(ffn_tcd_kernel<NT>), kTcdThreads, C::kSmem,
-                       cudaGetLastError());
+    kernel<<<a.grid, kTcdThreads, C::kSmem, st>>>(p);
+    return note_launch(reinterpret_cast<const void*>(kernel), kTcdThreads, C::kSmem, cudaGetLastError());
 }
 
 cudaError_t launch_tcd_ffn(const TcdLaunch& a, cudaStream_t st) {
     if (a.d % 128 != 0) return cudaErrorInvalidValue;
+    const bool up = a.u_out != nullptr;
     switch (a.nt) {
-        case 16: return launch_tcd_nt<16>(a, st);
-        case 32: return launch_tcd_nt<32>(a, st);
+        case 16: return up ? launch_tcd_nt<16, true>(a, st) : launch_tcd_nt<16, false>(a, st);
+        case 32: return up ? launch_tcd_nt<32, true>(a, st) : launch_tcd_nt<32, false>(a, st);
     }
     return cudaErrorInvalidValue;
 }

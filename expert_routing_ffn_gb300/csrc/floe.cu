@@ -225,12 +225,28 @@ __global__ void floe_plan_kernel(PlanArgs a, const int32_t* __restrict__ count) 
 
 cudaError_t launch_floe_prepare(const FloeArgs& f, const PlanArgs& plan, const GemvParams& gp, int G,
                                 cudaStream_t st) {
-    floe_up_plan_kernel<<<1, 64, 0, st>>>(plan);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    GemvParams up = gp;
-    up.up_pass = 1;
-    e = launch_gemv(up, G, true, st, true);
+    cudaError_t e;
+    if (f.tc_nt > 0) {
+        // up pass on the decode tensor cores: the routed rows in segments of
+        // tc_nt, 16-aligned channel ranges, U written to u
+        PlanArgs pu = plan;
+        pu.rg = f.tc_nt; pu.G = f.tc_grid; pu.p_align = 16; pu.n_shared = 0;
+        e = launch_plan_gemv(pu, st);
+        if (e != cudaSuccess) return e;
+        TcdLaunch t;
+        t.x = f.x; t.perm = f.perm; t.expert_offsets = f.expert_offsets; t.table = f.table;
+        t.hdr = plan.hdr; t.segs = plan.segs; t.x_perm = f.x_perm; t.partial = nullptr;
+        t.T = f.T; t.d = f.d; t.N = f.N; t.k = f.topk; t.rows_cap = f.rows_cap; t.nt = f.tc_nt;
+        t.grid = f.tc_grid; t.u_out = f.u; t.I = f.I; t.err = plan.err;
+        e = launch_tcd_ffn(t, st);
+    } else {
+        floe_up_plan_kernel<<<1, 64, 0, st>>>(plan);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        GemvParams up = gp;
+        up.up_pass = 1;
+        e = launch_gemv(up, G, true, st, true);
+    }
     if (e != cudaSuccess) return e;
     const size_t sel_smem = ((size_t)f.I + f.words) * sizeof(uint32_t);
     e = allow_max_smem(floe_select_kernel);

@@ -102,6 +102,9 @@ struct FloeArgs {
     const void* x; const int32_t* perm; const int32_t* expert_offsets; const ExpertEntry* table;
     int d, I, N, topk, m, words, rows_cap;
     float* u; uint32_t* kept; int32_t* list; int32_t* count;
+    // up pass on the decode tensor cores (tc_nt > 0: its rows per segment,
+    // grid, x_perm for 32-row segments), else on the GEMV
+    int tc_nt, tc_grid; void* x_perm; int T;
 };
 // FloE: up-only plan + GEMV pass, selection, unions and the sparse GEMV plan
 // (5 launches)
@@ -129,7 +132,10 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* perm, const int32_t
 struct TcdLaunch {
     const void* x; const int32_t* perm; const int32_t* expert_offsets; const ExpertEntry* table;
     const PlanHeader* hdr; const Seg* segs; void* x_perm; float* partial;
-    int T, d, N, k, rows_cap, nt, grid; DevError* err;
+    int T, d, N, k, rows_cap, nt, grid;
+    float* u_out;  // non-NULL: FloE up pass only, u [rows, I] (fp32); no partial rows
+    int I;
+    DevError* err;
 };
 // decode-size expert FFN on the tensor cores: one launch writing the GEMV
 // plan's partial rows (summed by launch_gemv_reduce)

@@ -452,7 +452,8 @@ moe_status expert_ffn_impl(const moe_dims* dims, const void* x, const void* tabl
         t.hdr = ws_at<PlanHeader>(ws, L.plan_hdr); t.segs = ws_at<Seg>(ws, L.segs);
         t.x_perm = ws_at<void>(ws, L.x_perm); t.partial = ws_at<float>(ws, L.partial);
         t.T = dims->T; t.d = dims->d; t.N = dims->N; t.k = dims->k; t.rows_cap = dims->T * dims->k;
-        t.nt = tcd_rows(dims->T); t.grid = tcd_grid(); t.err = ws_at<DevError>(ws, L.err);
+        t.nt = tcd_rows(dims->T); t.grid = tcd_grid(); t.u_out = nullptr; t.I = dims->I;
+        t.err = ws_at<DevError>(ws, L.err);
         MOE_CUDA(launch_tcd_ffn(t, S(stream)));
         count(t.nt == 32 ? 2 : 1);  // + the row gather for 32-row segments
         if (!reduce) return MOE_OK;
@@ -482,6 +483,9 @@ moe_status expert_ffn_impl(const moe_dims* dims, const void* x, const void* tabl
         f.words = p.words; f.rows_cap = dims->T * dims->k;
         f.u = ws_at<float>(ws, L.floe_u); f.kept = ws_at<uint32_t>(ws, L.floe_kept);
         f.list = ws_at<int32_t>(ws, L.floe_list); f.count = ws_at<int32_t>(ws, L.floe_count);
+        // the up pass of 4..64 tokens on the decode tensor cores
+        f.tc_nt = tcd_shapes(*dims) && dims->T >= kTcdMinTokens ? tcd_rows(dims->T) : 0;
+        f.tc_grid = tcd_grid(); f.x_perm = ws_at<void>(ws, L.x_perm); f.T = dims->T;
         PlanArgs pa;
         pa.expert_offsets = expert_offsets; pa.T = dims->T; pa.N = dims->N;
         pa.n_shared = dims->n_shared; pa.I = dims->I; pa.I_shared = dims->I_shared;
