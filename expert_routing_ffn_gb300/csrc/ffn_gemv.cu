@@ -305,6 +305,7 @@ __device__ __forceinline__ void ffn_gemv_body(const GemvParams& p) {
 
     const int tid = threadIdx.x;
     const int n_cons = blockDim.x;
+    grid_dep_wait();  // the plan and perm come from the previous kernels
     const PlanHeader hdr = *p.hdr;
     const int cta = blockIdx.x;
     if (cta >= hdr.G) return;
@@ -404,6 +405,7 @@ __global__ void __launch_bounds__(256) gemv_reduce_kernel(const PlanHeader* __re
                                                           float* __restrict__ y_shared) {
     const int n_seg = hdr_p->n_seg, n_routed_rows = hdr_p->n_routed_rows;
     const int n_partial_rows = hdr_p->n_partial_rows;
+    grid_dep_wait();
     const int row = blockIdx.x;
     const int rg = hdr_p->rg;
     const int nd4 = d / 4;
@@ -467,8 +469,8 @@ static cudaError_t launch_gemv_k(K kernel, int maxt, int vec, int ch, int esize,
     const size_t smem = (size_t)p.NS * 3 * ch * p.d * esize;
     cudaError_t e = allow_max_smem(kernel);
     if (e != cudaSuccess) return e;
-    kernel<<<G, threads, smem, st>>>(p);
-    return note_launch(reinterpret_cast<const void*>(kernel), threads, smem, cudaGetLastError());
+    e = launch_pdl(kernel, dim3(G), dim3(threads), smem, st, p);
+    return note_launch(reinterpret_cast<const void*>(kernel), threads, smem, e);
 }
 
 static int gemv_ctas_per_sm(int d, bool bf16) { return (bf16 && d <= 2048) || !bf16 ? 2 : 1; }
@@ -502,10 +504,8 @@ cudaError_t launch_gemv_reduce(const GemvReduceArgs& a, cudaStream_t st) {
     const int rows = a.routed_cap + (a.n_shared > 0 ? a.T : 0);
     if (rows == 0) return cudaSuccess;
     dim3 grid(rows, (a.d / 4 + 255) / 256);
-    gemv_reduce_kernel<<<grid, 256, 0, st>>>(a.hdr, a.segs, a.seg_first, a.expert_offsets, a.partial,
-                                             a.d, a.N, a.n_shared, a.T, a.routed_cap, a.y_perm,
-                                             a.y_shared);
-    return cudaGetLastError();
+    return launch_pdl(gemv_reduce_kernel, grid, dim3(256), 0, st, a.hdr, a.segs, a.seg_first, a.expert_offsets,
+                      a.partial, a.d, a.N, a.n_shared, a.T, a.routed_cap, a.y_perm, a.y_shared);
 }
 
 }  // namespace moe

@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(kTcdThreads, 1) ffn_tcd_kernel(const __grid_co
     tc_fence_after();
     const uint32_t tmem_base = tmem_base_s;
     // tensor-memory columns: G/U of phase-A buffer b at b*2NT (+NT), Y buffer b at 4NT + b*NT
+    grid_dep_wait();  // the plan, perm and x come from the previous kernels
     TcdWalk walk;
     const bool has_work = tcd_begin(p, walk);
 
@@ -235,6 +236,7 @@ __global__ void __launch_bounds__(kTcdThreads, 1) ffn_tcd_kernel(const __grid_co
                     }
                 }
             }
+            grid_dep_launch();  // every load issued: the next kernel may start its prologue
             // wait for the last loads in flight before the block may exit
             for (int k = (it > NS ? it - NS : 0); k < it; ++k)
                 (void)tc_wait(&full[k % NS], (k / NS) & 1, abort_flag, p.err, 12, false);
@@ -444,8 +446,8 @@ static cudaError_t launch_tcd_nt(const TcdLaunch& a, cudaStream_t st) {
     auto kernel = ffn_tcd_kernel<NT, UP>;
     cudaError_t e = allow_max_smem(kernel);
     if (e != cudaSuccess) return e;
-    kernel<<<a.grid, kTcdThreads, C::kSmem, st>>>(p);
-    return note_launch(reinterpret_cast<const void*>(kernel), kTcdThreads, C::kSmem, cudaGetLastError());
+    e = launch_pdl(kernel, dim3(a.grid), dim3(kTcdThreads), C::kSmem, st, p);
+    return note_launch(reinterpret_cast<const void*>(kernel), kTcdThreads, C::kSmem, e);
 }
 
 cudaError_t launch_tcd_ffn(const TcdLaunch& a, cudaStream_t st) {

@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 // combine_kernel), so the result is bitwise the one of the stage-wise calls.
 template <typename W>
 __global__ void __launch_bounds__(256) layer_epilogue_kernel(const EpilogueArgs a) {
+    grid_dep_wait();  // the FFN's partial rows
     const int t = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int q = blockIdx.y * 32 + lane;  // float4 column group
@@ -303,9 +304,8 @@ __global__ void __launch_bounds__(256) layer_epilogue_kernel(const EpilogueArgs 
 cudaError_t launch_layer_epilogue(const EpilogueArgs& a, cudaStream_t st) {
     if (a.T == 0) return cudaSuccess;
     dim3 grid(a.T, (a.d / 4 + 31) / 32);
-    if (a.bf16) layer_epilogue_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(a);
-    else layer_epilogue_kernel<float><<<grid, 256, 0, st>>>(a);
-    return cudaGetLastError();
+    return a.bf16 ? launch_pdl(layer_epilogue_kernel<__nv_bfloat16>, grid, dim3(256), 0, st, a)
+                  : launch_pdl(layer_epilogue_kernel<float>, grid, dim3(256), 0, st, a);
 }
 
 // One warp waits on a fresh mbarrier (arrival count 1) that no thread ever

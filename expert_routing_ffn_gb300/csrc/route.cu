@@ -599,6 +599,7 @@ __global__ void __launch_bounds__(256) route_front_kernel(const __grid_constant_
     __syncthreads();
     if (!s_last) return;
     __threadfence();
+    grid_dep_launch();  // the FFN may start its prologue during the per-token stages
     const int tid = threadIdx.x, warp = tid >> 5, nw = blockDim.x >> 5;
     const RouteSelectArgs& ra = a.ra;
     const SelectArgs& sa = a.sa;
