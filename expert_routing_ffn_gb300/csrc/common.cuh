@@ -333,6 +333,30 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
 
+// The shared experts' weights do not depend on routing: an FFN kernel that
+// starts while the routing kernel still runs (dependent launch) can pull its
+// 1/G share of them into L2 before grid_dep_wait(), with HBM otherwise idle.
+// One warp issues untracked bulk prefetches of at most 32 KB; every matrix
+// holds I * d elements with d a multiple of 64, so each piece is a multiple
+// of 16 bytes at a 16-byte aligned address.
+__device__ __forceinline__ void l2_prefetch_shared_experts(const ExpertEntry* table, int N, int n_shared, int d,
+                                                           int esize, int cta, int G, int lane) {
+    constexpr size_t kPiece = 32768;
+    for (int s = 0; s < n_shared; ++s) {
+        const ExpertEntry& E = table[N + s];
+        const size_t bytes = (size_t)E.I * d * esize;
+        const size_t share = ((bytes + (size_t)G - 1) / G + 15) & ~(size_t)15;
+        const size_t lo = (size_t)cta * share, hi = min(lo + share, bytes);
+        for (int m = 0; m < 3; ++m) {
+            const char* base = static_cast<const char*>(E.w[m]);
+            for (size_t off = lo + (size_t)lane * kPiece; off < hi; off += 32 * kPiece) {
+                const uint32_t n = (uint32_t)min(kPiece, hi - off);
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + off), "r"(n) : "memory");
+            }
+        }
+    }
+}
+
 template <typename... Params, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                               Args&&... args) {

@@ -305,6 +305,8 @@ __device__ __forceinline__ void ffn_gemv_body(const GemvParams& p) {
 
     const int tid = threadIdx.x;
     const int n_cons = blockDim.x;
+    if (!FLOE && tid < 32 && p.prefetch_shared > 0)
+        l2_prefetch_shared_experts(p.table, p.N, p.prefetch_shared, p.d, (int)sizeof(W), blockIdx.x, gridDim.x, tid);
     grid_dep_wait();  // the plan and perm come from the previous kernels
     const PlanHeader hdr = *p.hdr;
     const int cta = blockIdx.x;

@@ -127,7 +127,7 @@ extern "C" moe_status moe_expert_ffn_noalloc(const moe_dims* dims, const void* x
     p.perm = perm; p.table = static_cast<const moe::ExpertEntry*>(table);
     p.hdr = pa.hdr; p.segs = pa.segs; p.partial = moe::ws_at<float>(base, L.partial); p.err = err;
     p.floe_u = nullptr; p.floe_kept = nullptr; p.floe_list = nullptr; p.I = dims->I; p.words = 0;
-    p.up_pass = 0;
+    p.up_pass = 0; p.prefetch_shared = 0;
     if (moe::launch_gemv(p, G, bf16, s) != cudaSuccess) return MOE_ERR_CUDA;
 
     moe::GemvReduceArgs r;

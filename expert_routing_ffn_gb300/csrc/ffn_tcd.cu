@@ -77,6 +77,7 @@ struct TcdParams {
     float* u_out;  // up-only mode: u[pos, channel] (fp32, row = permuted position, I columns)
     int d, N, I;
     DevError* err;
+    int n_prefetch;  // shared experts to pull into L2 before the dependent-launch wait
 };
 
 // One CTA's pieces of segments, as every role walks them.
@@ -154,6 +155,8 @@ __global__ void __launch_bounds__(kTcdThreads, 1) ffn_tcd_kernel(const __grid_co
     tc_fence_after();
     const uint32_t tmem_base = tmem_base_s;
     // tensor-memory columns: G/U of phase-A buffer b at b*2NT (+NT), Y buffer b at 4NT + b*NT
+    if (warp == 0 && p.n_prefetch > 0)
+        l2_prefetch_shared_experts(p.table, p.N, p.n_prefetch, d, 2, blockIdx.x, gridDim.x, lane);
     grid_dep_wait();  // the plan, perm and x come from the previous kernels
     TcdWalk walk;
     const bool has_work = tcd_begin(p, walk);
@@ -443,6 +446,7 @@ static cudaError_t launch_tcd_nt(const TcdLaunch& a, cudaStream_t st) {
     p.perm = a.perm; p.topk = a.k;
     p.table = a.table; p.hdr = a.hdr; p.segs = a.segs; p.partial = a.partial;
     p.u_out = a.u_out; p.d = a.d; p.N = a.N; p.I = a.I; p.err = a.err;
+    p.n_prefetch = a.u_out ? 0 : a.prefetch_shared;
     auto kernel = ffn_tcd_kernel<NT, UP>;
     cudaError_t e = allow_max_smem(kernel);
     if (e != cudaSuccess) return e;

@@ -237,7 +237,7 @@ cudaError_t launch_floe_prepare(const FloeArgs& f, const PlanArgs& plan, const G
         t.x = f.x; t.perm = f.perm; t.expert_offsets = f.expert_offsets; t.table = f.table;
         t.hdr = plan.hdr; t.segs = plan.segs; t.x_perm = f.x_perm; t.partial = nullptr;
         t.T = f.T; t.d = f.d; t.N = f.N; t.k = f.topk; t.rows_cap = f.rows_cap; t.nt = f.tc_nt;
-        t.grid = f.tc_grid; t.u_out = f.u; t.I = f.I; t.err = plan.err;
+        t.grid = f.tc_grid; t.u_out = f.u; t.I = f.I; t.err = plan.err; t.prefetch_shared = 0;
         e = launch_tcd_ffn(t, st);
     } else {
         floe_up_plan_kernel<<<1, 64, 0, st>>>(plan);
@@ -245,6 +245,7 @@ cudaError_t launch_floe_prepare(const FloeArgs& f, const PlanArgs& plan, const G
         if (e != cudaSuccess) return e;
         GemvParams up = gp;
         up.up_pass = 1;
+        up.prefetch_shared = 0;
         e = launch_gemv(up, G, true, st, true);
     }
     if (e != cudaSuccess) return e;

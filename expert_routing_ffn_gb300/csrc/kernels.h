@@ -93,6 +93,7 @@ struct GemvParams {
     const Seg* segs;
     float* partial;
     DevError* err;
+    int prefetch_shared;          // > 0: that many shared experts pulled into L2 before the wait on routing
 };
 int gemv_stages(int d, bool bf16);
 int gemv_grid_for(int d, bool bf16, int sms);
@@ -136,6 +137,7 @@ struct TcdLaunch {
     float* u_out;  // non-NULL: FloE up pass only, u [rows, I] (fp32); no partial rows
     int I;
     DevError* err;
+    int prefetch_shared;  // > 0: that many shared experts pulled into L2 before the wait on routing
 };
 // decode-size expert FFN on the tensor cores: one launch writing the GEMV
 // plan's partial rows (summed by launch_gemv_reduce)

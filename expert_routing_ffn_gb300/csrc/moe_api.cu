@@ -419,7 +419,7 @@ namespace {
 moe_status expert_ffn_impl(const moe_dims* dims, const void* x, const void* table,
                            const int32_t* expert_offsets, const int32_t* perm, float keep_frac,
                            float* y_perm, float* y_shared, void* ws, size_t ws_bytes, void* stream,
-                           bool reduce) {
+                           bool reduce, bool prefetch_shared = false) {
     MOE_TRY(check_dims(dims));
     MOE_TRY(check_ws(dims, ws, ws_bytes));
     if (!(keep_frac > 0.f && keep_frac <= 1.f)) return MOE_ERR_INVALID_ARG;
@@ -453,7 +453,7 @@ moe_status expert_ffn_impl(const moe_dims* dims, const void* x, const void* tabl
         t.x_perm = ws_at<void>(ws, L.x_perm); t.partial = ws_at<float>(ws, L.partial);
         t.T = dims->T; t.d = dims->d; t.N = dims->N; t.k = dims->k; t.rows_cap = dims->T * dims->k;
         t.nt = tcd_rows(dims->T); t.grid = tcd_grid(); t.u_out = nullptr; t.I = dims->I;
-        t.err = ws_at<DevError>(ws, L.err);
+        t.err = ws_at<DevError>(ws, L.err); t.prefetch_shared = prefetch_shared ? dims->n_shared : 0;
         MOE_CUDA(launch_tcd_ffn(t, S(stream)));
         count(t.nt == 32 ? 2 : 1);  // + the row gather for 32-row segments
         if (!reduce) return MOE_OK;
@@ -473,7 +473,7 @@ moe_status expert_ffn_impl(const moe_dims* dims, const void* x, const void* tabl
     p.partial = ws_at<float>(ws, L.partial); p.err = ws_at<DevError>(ws, L.err);
     p.floe_u = ws_at<float>(ws, L.floe_u); p.floe_kept = ws_at<uint32_t>(ws, L.floe_kept);
     p.floe_list = ws_at<int32_t>(ws, L.floe_list); p.I = dims->I; p.words = (dims->I + 31) / 32;
-    p.up_pass = 0;
+    p.up_pass = 0; p.prefetch_shared = prefetch_shared && !floe ? dims->n_shared : 0;
     if (floe) {
         FloeArgs f;
         f.x = x; f.perm = perm; f.expert_offsets = expert_offsets; f.table = p.table;
@@ -631,11 +631,11 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_layer_args* A,
             count();
             MOE_CUDA(cudaEventRecord(sd->join, sd->s));
             MOE_TRY(expert_ffn_impl(dims, A->x, A->table, O->expert_offsets, O->perm, A->keep_frac, O->y_perm,
-                                    O->y_shared, ws, ws_bytes, stream, false));
+                                    O->y_shared, ws, ws_bytes, stream, false, true));
             MOE_CUDA(cudaStreamWaitEvent(S(stream), sd->join, 0));
         } else {
             MOE_TRY(expert_ffn_impl(dims, A->x, A->table, O->expert_offsets, O->perm, A->keep_frac, O->y_perm,
-                                    O->y_shared, ws, ws_bytes, stream, false));
+                                    O->y_shared, ws, ws_bytes, stream, false, true));
         }
         EpilogueArgs ea;
         ea.hdr = ws_at<PlanHeader>(ws, L.plan_hdr); ea.segs = ws_at<Seg>(ws, L.segs);
