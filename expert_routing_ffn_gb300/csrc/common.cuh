@@ -17,6 +17,7 @@ namespace moe {
 // ---------------------------------------------------------------- constants
 constexpr int kMaxExperts = 64;       // expert sets are uint64 bitmasks
 constexpr int kMaxTopK = 8;
+constexpr int kMaxShared = 8;         // shared experts per layer
 constexpr int kGemvMaxRows = 8;       // rows per GEMV segment (register-resident)
 constexpr int kGemvMaxCtas = 512;     // upper bound of the GEMV grid (workspace sizing)
 constexpr int kAlign = 256;
@@ -65,6 +66,144 @@ struct PlanHeader {
     int n_routed_rows;
     int pad[9];
 };
+
+// The partial rows of one (segment, row) are summed in one fixed two-level
+// order, shared by every kernel that reduces them so that their results agree
+// bitwise: the segment's pieces form at most kSumChunks runs of
+// ceil(npieces / kSumChunks) consecutive pieces; each run is summed in piece
+// order from zero, then the run sums are added in run order from zero.  The
+// runs are independent, so different warps sum them at once: a row spread over
+// a few hundred CTAs then costs a few dependent L2 round trips, not one per
+// piece.  A work item is a group of consecutive runs of at most eight pieces
+// in all (or one longer run), whose loads are all in flight together.
+constexpr int kSumChunks = 8;
+__device__ __forceinline__ int sum_run_len(int npieces) { return (npieces + kSumChunks - 1) / kSumChunks; }
+__device__ __forceinline__ int sum_runs(int npieces) {
+    const int c = sum_run_len(npieces);
+    return c > 0 ? (npieces + c - 1) / c : 0;
+}
+__device__ __forceinline__ int sum_runs_per_item(int npieces) {
+    const int c = sum_run_len(npieces);
+    return c >= 8 ? 1 : 8 / c;
+}
+__device__ __forceinline__ int sum_items(int npieces) {
+    const int rpi = sum_runs_per_item(npieces);
+    return (sum_runs(npieces) + rpi - 1) / rpi;
+}
+__device__ __forceinline__ void add4(float4& a, const float4& b) {
+    a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+}
+// Item `item` of segment S, row `row`, float4 column q of d: each of its runs'
+// sums goes to runs[c * 32] (c = run index).
+__device__ __forceinline__ void partial_item_runs(const float* __restrict__ partial, const Seg& S, int row,
+                                                  int d, int q, int item, float4* runs) {
+    const int len = sum_run_len(S.npieces), rpi = sum_runs_per_item(S.npieces);
+    int run = item * rpi;
+    const int p_end = min((run + rpi) * len, S.npieces);
+    const float4* base = reinterpret_cast<const float4*>(partial + (size_t)(S.pbase + row) * d) + q;
+    const size_t step = (size_t)S.rows * (size_t)(d / 4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int left = len;  // pieces still to add to the current run
+    for (int p = run * len; p < p_end; p += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (p + i < p_end) v[i] = __ldcg(base + (size_t)(p + i) * step);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (p + i < p_end) {
+                add4(acc, v[i]);
+                if (--left == 0 || p + i + 1 == p_end) {
+                    runs[run * 32] = acc;
+                    acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    left = len;
+                    ++run;
+                }
+            }
+        }
+    }
+}
+// The same sum of one whole (segment, row) by one thread: its runs' sums are
+// added as they complete, which is unit_table_sum's arithmetic.  For segments
+// of few pieces (the decode tensor-core path), where one thread per column
+// has all the loads in flight anyway.
+__device__ __forceinline__ float4 partial_unit_sum(const float* __restrict__ partial, const Seg& S, int row,
+                                                   int d, int q) {
+    const int len = sum_run_len(S.npieces), np = S.npieces;
+    const float4* base = reinterpret_cast<const float4*>(partial + (size_t)(S.pbase + row) * d) + q;
+    const size_t step = (size_t)S.rows * (size_t)(d / 4);
+    float4 y = make_float4(0.f, 0.f, 0.f, 0.f), acc = y;
+    int left = len;
+    for (int p = 0; p < np; p += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (p + i < np) v[i] = __ldcg(base + (size_t)(p + i) * step);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (p + i < np) {
+                add4(acc, v[i]);
+                if (--left == 0 || p + i + 1 == np) {
+                    add4(y, acc);
+                    acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    left = len;
+                }
+            }
+        }
+    }
+    return y;
+}
+// A segment row's partial rows are all inside the partial buffer.
+__device__ __forceinline__ bool seg_row_ok(const Seg& S, int row, int n_partial_rows) {
+    return S.npieces > 0 && S.pbase + (S.npieces - 1) * S.rows + row < n_partial_rows;
+}
+// Segment rows ("units") that feed one output, as a block sums them.  Warp 0
+// publishes them (lane order = unit order; `has`: this lane holds one) with
+// the first work item of each; then every warp takes items round robin.
+constexpr int kMaxUnits = kMaxTopK + kMaxShared;
+struct UnitTable {
+    Seg seg[kMaxUnits];
+    int row[kMaxUnits];
+    int item0[kMaxUnits + 1];
+    int n;
+};
+__device__ __forceinline__ int unit_table_publish(UnitTable& U, bool has, const Seg& S, int row) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t lt = (1u << lane) - 1u;
+    const uint32_t ub = __ballot_sync(0xffffffffu, has);
+    const int u = __popc(ub & lt);
+    const int items = has ? sum_items(S.npieces) : 0;
+    int incl = items;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (has) { U.seg[u] = S; U.row[u] = row; U.item0[u] = incl - items; }
+    if (lane == 31) { U.n = __popc(ub); U.item0[__popc(ub)] = incl; }
+    return has ? u : -1;
+}
+// Sum the runs of every item of the table into runs[(u * kSumChunks + c) * 32 + lane],
+// the items taken round robin by warps w = 0..nw-1 (this one: w).
+__device__ __forceinline__ void unit_table_runs(const UnitTable& U, const float* __restrict__ partial, int d,
+                                                int q, float4* runs, int w, int nw) {
+    const int lane = threadIdx.x & 31;
+    const int n_items = U.item0[U.n];
+    for (int i = w; i < n_items; i += nw) {
+        int u = 0;
+        while (u + 1 < U.n && U.item0[u + 1] <= i) ++u;
+        partial_item_runs(partial, U.seg[u], U.row[u], d, q, i - U.item0[u],
+                          runs + (size_t)u * kSumChunks * 32 + lane);
+    }
+}
+// Unit u's sum: its runs in order, from zero.
+__device__ __forceinline__ float4 unit_table_sum(const UnitTable& U, int u, const float4* runs) {
+    const int lane = threadIdx.x & 31;
+    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int nr = sum_runs(U.seg[u].npieces);
+    for (int c = 0; c < nr; ++c) add4(y, runs[((size_t)u * kSumChunks + c) * 32 + lane]);
+    return y;
+}
 
 // Tensor-core (prefill) plan: one segment per routed expert with rows, plus
 // one segment for all shared experts (their channels stacked).  Phase-1

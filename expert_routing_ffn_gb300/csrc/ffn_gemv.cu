@@ -396,7 +396,15 @@ __global__ void __launch_bounds__(512, 1) ffn_gemv_kernel_x1(GemvParams p) {
     ffn_gemv_body<W, RG, CH, 512, FLOE>(p);
 }
 
-// Sum the partial rows of each output row in piece order.
+// Sum the partial rows of each output row (in the order of partial_item_runs
+// and unit_table_sum).  The row's segment rows ("units": one for a y_perm
+// row, one per shared expert for a y_shared row) are looked up by warp 0.
+// direct = 0 (GEMV partials, up to a few hundred pieces a segment): block =
+// one output row x 32 float4 columns of d; all warps sum the units' runs into
+// dynamic shared memory (max(1, n_shared) * kSumChunks * 32 float4), then warp
+// 0 adds them up.  direct = 1 (decode tensor-core partials, a few pieces a
+// segment): block = one output row x 256 float4 columns, one thread per
+// column sums its units alone (partial_unit_sum, the same arithmetic).
 __global__ void __launch_bounds__(256) gemv_reduce_kernel(const PlanHeader* __restrict__ hdr_p,
                                                           const Seg* __restrict__ segs,
                                                           const int32_t* __restrict__ seg_first,
@@ -404,60 +412,73 @@ __global__ void __launch_bounds__(256) gemv_reduce_kernel(const PlanHeader* __re
                                                           const float* __restrict__ partial, int d,
                                                           int N, int n_shared, int T, int routed_cap,
                                                           float* __restrict__ y_perm,
-                                                          float* __restrict__ y_shared) {
-    const int n_seg = hdr_p->n_seg, n_routed_rows = hdr_p->n_routed_rows;
-    const int n_partial_rows = hdr_p->n_partial_rows;
+                                                          float* __restrict__ y_shared, int direct) {
+    __shared__ UnitTable U;
+    extern __shared__ float4 s_runs[];
     grid_dep_wait();
     const int row = blockIdx.x;
-    const int rg = hdr_p->rg;
-    const int nd4 = d / 4;
-    const int q0 = blockIdx.y * blockDim.x;  // first float4 column of this block
-    if (row < routed_cap) {
-        const int pos = row;
-        if (pos >= n_routed_rows) return;
-        int lo = 0, hi = N - 1;  // expert e with offsets[e] <= pos < offsets[e+1]
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (expert_offsets[mid] <= pos) lo = mid; else hi = mid - 1;
-        }
-        const int e = lo;
-        const int local = pos - expert_offsets[e];
-        const int si = seg_first[e] + local / rg;
-        if (si < 0 || si >= n_seg) return;
-        const Seg S = segs[si];
-        const int r = local % rg;
-        if (S.pbase + (S.npieces - 1) * S.rows + r >= n_partial_rows) return;
-        const int q = q0 + threadIdx.x;
-        if (q < nd4) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int pc = 0; pc < S.npieces; ++pc) {
-                const float4 v = reinterpret_cast<const float4*>(
-                    partial + (size_t)(S.pbase + pc * S.rows + r) * d)[q];
-                acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-            }
-            reinterpret_cast<float4*>(y_perm + (size_t)pos * d)[q] = acc;
-        }
-    } else {
-        const int t = row - routed_cap;
-        if (t >= T || n_shared == 0) return;
-        const int q = q0 + threadIdx.x;
-        if (q < nd4) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s = 0; s < n_shared; ++s) {
-                const int si = seg_first[N + s] + t / rg;
-                if (si < 0 || si >= n_seg) continue;
-                const Seg S = segs[si];
-                const int r = t % rg;
-                if (S.pbase + (S.npieces - 1) * S.rows + r >= n_partial_rows) continue;
-                for (int pc = 0; pc < S.npieces; ++pc) {
-                    const float4 v = reinterpret_cast<const float4*>(
-                        partial + (size_t)(S.pbase + pc * S.rows + r) * d)[q];
-                    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const bool routed = row < routed_cap;
+    if (!routed && (row - routed_cap >= T || n_shared == 0)) return;
+    if (warp == 0) {
+        // lane 0: the routed row's segment; lane s < n_shared: shared expert s
+        const PlanHeader& hdr = *hdr_p;
+        bool has = false;
+        Seg S;
+        int srow = 0;
+        if (routed) {
+            if (row < hdr.n_routed_rows) {
+                // expert e with offsets[e] <= row < offsets[e+1]: offsets are
+                // non-decreasing from 0, so e = #{e < N : offsets[e] <= row} - 1
+                const bool lo = lane < N && expert_offsets[lane] <= row;
+                const bool hi = lane + 32 < N && expert_offsets[lane + 32] <= row;
+                const int e = __popc(__ballot_sync(0xffffffffu, lo)) + __popc(__ballot_sync(0xffffffffu, hi)) - 1;
+                if (lane == 0 && e >= 0) {
+                    const int local = row - expert_offsets[e];
+                    const int si = seg_first[e] + local / hdr.rg;
+                    if (si >= 0 && si < hdr.n_seg) {
+                        S = segs[si]; srow = local % hdr.rg;
+                        has = seg_row_ok(S, srow, hdr.n_partial_rows);
+                    }
                 }
             }
-            reinterpret_cast<float4*>(y_shared + (size_t)t * d)[q] = acc;
+        } else if (lane < n_shared) {
+            const int t = row - routed_cap;
+            const int si = seg_first[N + lane] + t / hdr.rg;
+            if (si >= 0 && si < hdr.n_seg) {
+                S = segs[si]; srow = t % hdr.rg;
+                has = seg_row_ok(S, srow, hdr.n_partial_rows);
+            }
         }
+        unit_table_publish(U, has, S, srow);
     }
+    __syncthreads();
+    // a routed row past the computed rows, or a bad plan entry (error word set
+    // by the plan): nothing to write
+    if (routed && U.n == 0) return;
+    float* out = routed ? y_perm + (size_t)row * d : y_shared + (size_t)(row - routed_cap) * d;
+    if (direct) {
+        const int q = blockIdx.y * blockDim.x + threadIdx.x;
+        if (q >= d / 4) return;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int u = 0; u < U.n; ++u) {
+            const float4 y = partial_unit_sum(partial, U.seg[u], U.row[u], d, q);
+            if (routed) acc = y; else add4(acc, y);
+        }
+        reinterpret_cast<float4*>(out)[q] = acc;
+        return;
+    }
+    const int q = blockIdx.y * 32 + lane;
+    const bool col_ok = q < d / 4;
+    if (col_ok) unit_table_runs(U, partial, d, q, s_runs, warp, blockDim.x >> 5);
+    __syncthreads();
+    if (warp != 0 || !col_ok) return;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < U.n; ++u) {
+        const float4 y = unit_table_sum(U, u, s_runs);
+        if (routed) acc = y; else add4(acc, y);
+    }
+    reinterpret_cast<float4*>(out)[q] = acc;
 }
 
 // ---------------------------------------------------------------------------
@@ -505,9 +526,12 @@ cudaError_t launch_gemv(const GemvParams& p, int G, bool bf16, cudaStream_t st, 
 cudaError_t launch_gemv_reduce(const GemvReduceArgs& a, cudaStream_t st) {
     const int rows = a.routed_cap + (a.n_shared > 0 ? a.T : 0);
     if (rows == 0) return cudaSuccess;
-    dim3 grid(rows, (a.d / 4 + 255) / 256);
-    return launch_pdl(gemv_reduce_kernel, grid, dim3(256), 0, st, a.hdr, a.segs, a.seg_first, a.expert_offsets,
-                      a.partial, a.d, a.N, a.n_shared, a.T, a.routed_cap, a.y_perm, a.y_shared);
+    const int cols = a.direct ? 256 : 32;  // float4 columns per block
+    dim3 grid(rows, (a.d / 4 + cols - 1) / cols);
+    const size_t smem =
+        a.direct ? 0 : (size_t)(a.n_shared > 1 ? a.n_shared : 1) * kSumChunks * 32 * sizeof(float4);
+    return launch_pdl(gemv_reduce_kernel, grid, dim3(256), smem, st, a.hdr, a.segs, a.seg_first, a.expert_offsets,
+                      a.partial, a.d, a.N, a.n_shared, a.T, a.routed_cap, a.y_perm, a.y_shared, a.direct ? 1 : 0);
 }
 
 }  // namespace moe

@@ -133,7 +133,7 @@ extern "C" moe_status moe_expert_ffn_noalloc(const moe_dims* dims, const void* x
     moe::GemvReduceArgs r;
     r.hdr = pa.hdr; r.segs = pa.segs; r.seg_first = pa.seg_first; r.expert_offsets = expert_offsets;
     r.partial = p.partial; r.d = dims->d; r.N = dims->N; r.n_shared = dims->n_shared; r.T = dims->T;
-    r.routed_cap = dims->T * dims->k; r.y_perm = y_perm; r.y_shared = y_shared;
+    r.routed_cap = dims->T * dims->k; r.y_perm = y_perm; r.y_shared = y_shared; r.direct = false;
     if (moe::launch_gemv_reduce(r, s) != cudaSuccess) return MOE_ERR_CUDA;
 
     if (device_status &&

@@ -116,6 +116,7 @@ struct GemvReduceArgs {
     const PlanHeader* hdr; const Seg* segs; const int32_t* seg_first; const int32_t* expert_offsets;
     const float* partial; int d, N, n_shared, T, routed_cap;
     float *y_perm, *y_shared;
+    bool direct;  // one thread per column (segments of few pieces: decode tensor-core partials)
 };
 cudaError_t launch_gemv_reduce(const GemvReduceArgs& a, cudaStream_t st);
 
@@ -158,6 +159,7 @@ struct EpilogueArgs {
     const float* z; const void* lore_b;  // lore_b NULL: no LoRE term
     int T, d, N, k, r, n_shared; bool bf16;
     float *y_perm, *y_shared, *y_lore, *out;
+    bool direct;  // as GemvReduceArgs::direct
 };
 // partial-row reduction + LoRE B + combine in one launch (moe_layer_forward)
 cudaError_t launch_layer_epilogue(const EpilogueArgs& a, cudaStream_t st);

@@ -150,42 +150,84 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 }
 
 // moe_layer_forward's tail when the expert FFN left per-CTA partial rows
-// (GEMV and decode tensor-core paths).  Block = token t x 128 columns of d;
-// lane = 4 columns.  Warp w sums the partial rows of the slots s = w, w + 8,
-// ... (one y_perm row each) and warp 7 also those of the shared experts
-// (y_shared); warp 6 forms the LoRE term (B rows times z); warp 0 then
-// combines in slot order and writes out.  Every sum runs in the
-// order of the separate kernels (gemv_reduce_kernel, lore_b_kernel,
-// combine_kernel), so the result is bitwise the one of the stage-wise calls.
-template <typename W>
-__global__ void __launch_bounds__(256) layer_epilogue_kernel(const EpilogueArgs a) {
+// (GEMV and decode tensor-core paths).  Block = token t x 128 columns of d
+// (lane = 4 columns).  A "unit" is one segment row feeding the token: the
+// y_perm row of a computed slot, or one shared expert's row.  Warp 0 reads
+// the slots; then the last warp forms the LoRE term (z, then B rows times z)
+// while the others sum the units:
+//  - not DIRECT (GEMV partials, up to eight runs a unit): warp 0 also looks up
+//    the units; warps 0..nw-2 sum all units' runs into dynamic shared memory
+//    ((k + n_shared) * kSumChunks * 32 float4), then warp s < k adds up slot
+//    s's runs and warp kMaxTopK the shared experts';
+//  - DIRECT (decode tensor-core partials, a few pieces a segment): warp s < k
+//    looks up and sums slot s's unit, warp nw-2 the shared experts'
+//    (partial_unit_sum).
+// Warp 0 then combines in slot order.  Every sum runs in the order of the
+// separate kernels (gemv_reduce_kernel, lore_b_kernel, combine_kernel), so
+// the result is bitwise the one of the stage-wise calls.
+template <typename W, bool DIRECT>
+__global__ void __launch_bounds__(DIRECT ? 256 : 1024) layer_epilogue_kernel(const EpilogueArgs a) {
     grid_dep_wait();  // the FFN's partial rows
     const int t = blockIdx.x;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int q = blockIdx.y * 32 + lane;  // float4 column group
     const int k = a.k, r = a.r, d = a.d, N = a.N;
-    __shared__ int s_pos[kMaxTopK], s_e[kMaxTopK], s_lore[kMaxTopK];
+    const int lore_warp = nw - 1, shared_warp = DIRECT ? nw - 2 : kMaxTopK;
+    __shared__ int s_pos[kMaxTopK], s_e[kMaxTopK], s_lore[kMaxTopK], s_kind[kMaxTopK];
     __shared__ float s_g[kMaxTopK];
     __shared__ float s_lg;
-    __shared__ int s_nl;
+    __shared__ int s_nl, s_nslot_u;
+    __shared__ int s_slot_unit[kMaxTopK];  // unit of slot s, -1: none (y = 0)
+    __shared__ UnitTable U;
     __shared__ float s_z[kMaxTopK * 64];
     __shared__ float4 s_y[kMaxTopK][32];
     __shared__ float4 s_sh[32];
     __shared__ float4 s_yl[32];
-    __shared__ int s_kind[kMaxTopK];
-    if (threadIdx.x < 32) {  // one lane per slot
-        const int s = threadIdx.x;
-        bool lore_term = false;
+    extern __shared__ float4 s_runs[];
+    const PlanHeader& hdr = *a.hdr;
+    // the segment row of slot s (pos, e), or of shared expert j
+    auto slot_seg = [&](int pos, int e, Seg& S, int& row) {
+        if (pos < 0 || e < 0 || e >= N || pos >= hdr.n_routed_rows) return false;
+        const int local = pos - a.expert_offsets[e];
+        const int si = a.seg_first[e] + local / hdr.rg;
+        if (si < 0 || si >= hdr.n_seg) return false;
+        S = a.segs[si];
+        row = local % hdr.rg;
+        return seg_row_ok(S, row, hdr.n_partial_rows);
+    };
+    auto shared_seg = [&](int j, Seg& S, int& row) {
+        const int si = a.seg_first[N + j] + t / hdr.rg;
+        if (si < 0 || si >= hdr.n_seg) return false;
+        S = a.segs[si];
+        row = t % hdr.rg;
+        return seg_row_ok(S, row, hdr.n_partial_rows);
+    };
+    if (warp == 0) {
+        // lanes 0..k-1: slot s = lane; lanes kMaxTopK..: shared expert lane - kMaxTopK
+        const int s = lane;
+        bool lore_term = false, has = false;
+        Seg S;
+        int urow = 0;
         if (s < k) {
             const size_t sl = (size_t)t * k + s;
-            s_pos[s] = a.inv_perm[sl];
+            const int pos = a.inv_perm[sl];
+            const int e = a.final_idx[sl];
+            s_pos[s] = pos;
             s_g[s] = a.final_gate[sl];
-            s_e[s] = a.final_idx[sl];
+            s_e[s] = e;
             s_kind[s] = a.final_kind[sl];
-            lore_term = s_kind[s] == MOE_KIND_LORE && a.lore_b && s_e[s] >= 0 && s_e[s] < N;
+            lore_term = s_kind[s] == MOE_KIND_LORE && a.lore_b && e >= 0 && e < N;
+            if (!DIRECT) has = slot_seg(pos, e, S, urow);
+        } else if (!DIRECT && s >= kMaxTopK && s - kMaxTopK < a.n_shared) {
+            has = shared_seg(s - kMaxTopK, S, urow);
         }
         const uint32_t b = __ballot_sync(0xffffffffu, lore_term);
         if (lore_term) s_lore[__popc(b & ((1u << s) - 1u))] = s;
+        if (!DIRECT) {
+            const int u = unit_table_publish(U, has, S, urow);
+            if (s < k) s_slot_unit[s] = u;
+        }
+        const uint32_t sb = __ballot_sync(0xffffffffu, has && s < kMaxTopK);
         __syncwarp();
         if (s == 0) {  // the LoRE gates summed in slot order
             float lg = 0.f;
@@ -193,62 +235,17 @@ __global__ void __launch_bounds__(256) layer_epilogue_kernel(const EpilogueArgs 
                 if (s_kind[j] == MOE_KIND_LORE) lg += s_g[j];
             s_lg = lg;
             s_nl = __popc(b);
+            s_nslot_u = __popc(sb);
         }
     }
     __syncthreads();
-    const int nl = s_nl;
-    for (int i = threadIdx.x; i < nl * r; i += blockDim.x)
-        s_z[i] = a.z[((size_t)t * k + s_lore[i / r]) * r + (i % r)];
-    __syncthreads();  // s_z complete before the LoRE warp reads it
     const bool col_ok = q < d / 4;
-    const PlanHeader hdr = *a.hdr;
-    const int rg = hdr.rg;
-    // sum of the pieces of segment si, row `row` (in piece order)
-    auto add_pieces = [&](float4& acc, int si, int row) {
-        if (si < 0 || si >= hdr.n_seg) return;
-        const Seg S = a.segs[si];
-        if (S.pbase + (S.npieces - 1) * S.rows + row >= hdr.n_partial_rows) return;
-        const float* base = a.partial + (size_t)(S.pbase + row) * d;
-        const size_t step = (size_t)S.rows * d;
-        int pc = 0;
-        for (; pc + 4 <= S.npieces; pc += 4) {  // four loads in flight, added in order
-            const float4 v0 = reinterpret_cast<const float4*>(base + (pc + 0) * step)[q];
-            const float4 v1 = reinterpret_cast<const float4*>(base + (pc + 1) * step)[q];
-            const float4 v2 = reinterpret_cast<const float4*>(base + (pc + 2) * step)[q];
-            const float4 v3 = reinterpret_cast<const float4*>(base + (pc + 3) * step)[q];
-            acc.x += v0.x; acc.y += v0.y; acc.z += v0.z; acc.w += v0.w;
-            acc.x += v1.x; acc.y += v1.y; acc.z += v1.z; acc.w += v1.w;
-            acc.x += v2.x; acc.y += v2.y; acc.z += v2.z; acc.w += v2.w;
-            acc.x += v3.x; acc.y += v3.y; acc.z += v3.z; acc.w += v3.w;
-        }
-        for (; pc < S.npieces; ++pc) {
-            const float4 v = reinterpret_cast<const float4*>(base + pc * step)[q];
-            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-        }
-    };
-    if (col_ok) {
-        for (int s = warp; s < k; s += 8) {
-            const int pos = s_pos[s];
-            if (pos < 0) continue;
-            float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-            const int e = s_e[s];
-            if (e >= 0 && e < N && pos < hdr.n_routed_rows) {
-                const int local = pos - a.expert_offsets[e];
-                add_pieces(y, a.seg_first[e] + local / rg, local % rg);
-            }
-            reinterpret_cast<float4*>(a.y_perm + (size_t)pos * d)[q] = y;
-            s_y[s][lane] = y;
-        }
-        if (warp == 7 && a.n_shared > 0) {
-            float4 sh = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s = 0; s < a.n_shared; ++s) add_pieces(sh, a.seg_first[N + s] + t / rg, t % rg);
-            reinterpret_cast<float4*>(a.y_shared + (size_t)t * d)[q] = sh;
-            s_sh[lane] = sh;
-        }
-    }
     // LoRE term y_lore[t, j] = sum over LoRE slots, then over q, of B_e[j, q] z[q]
-    // (warp 6; the order of lore_b_kernel)
-    if (warp == 6 && a.lore_b) {
+    // (the order of lore_b_kernel)
+    if (warp == lore_warp && a.lore_b) {
+        const int nl = s_nl;
+        for (int i = lane; i < nl * r; i += 32) s_z[i] = a.z[((size_t)t * k + s_lore[i / r]) * r + (i % r)];
+        __syncwarp();
         float yl[4] = {0.f, 0.f, 0.f, 0.f};
         if (col_ok) {
             const W* B = static_cast<const W*>(a.lore_b);
@@ -279,6 +276,47 @@ __global__ void __launch_bounds__(256) layer_epilogue_kernel(const EpilogueArgs 
             s_yl[lane] = v;
         }
     }
+    if (DIRECT) {
+        if (col_ok && warp < k) {
+            const int s = warp, pos = s_pos[s];
+            if (pos >= 0) {
+                Seg S;
+                int row = 0;
+                const float4 y = slot_seg(pos, s_e[s], S, row) ? partial_unit_sum(a.partial, S, row, d, q)
+                                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                reinterpret_cast<float4*>(a.y_perm + (size_t)pos * d)[q] = y;
+                s_y[s][lane] = y;
+            }
+        }
+        if (col_ok && warp == shared_warp && a.n_shared > 0) {
+            float4 sh = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < a.n_shared; ++j) {
+                Seg S;
+                int row = 0;
+                if (shared_seg(j, S, row)) add4(sh, partial_unit_sum(a.partial, S, row, d, q));
+            }
+            reinterpret_cast<float4*>(a.y_shared + (size_t)t * d)[q] = sh;
+            s_sh[lane] = sh;
+        }
+    } else {
+        if (col_ok && warp != lore_warp) unit_table_runs(U, a.partial, d, q, s_runs, warp, nw - 1);
+        __syncthreads();  // the run sums complete
+        if (col_ok && warp < k) {
+            const int s = warp, pos = s_pos[s];
+            if (pos >= 0) {
+                const int u = s_slot_unit[s];
+                const float4 y = u >= 0 ? unit_table_sum(U, u, s_runs) : make_float4(0.f, 0.f, 0.f, 0.f);
+                reinterpret_cast<float4*>(a.y_perm + (size_t)pos * d)[q] = y;
+                s_y[s][lane] = y;
+            }
+        }
+        if (col_ok && warp == shared_warp && a.n_shared > 0) {
+            float4 sh = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int u = s_nslot_u; u < U.n; ++u) add4(sh, unit_table_sum(U, u, s_runs));
+            reinterpret_cast<float4*>(a.y_shared + (size_t)t * d)[q] = sh;
+            s_sh[lane] = sh;
+        }
+    }
     __syncthreads();
     if (warp != 0 || !col_ok) return;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -301,11 +339,27 @@ __global__ void __launch_bounds__(256) layer_epilogue_kernel(const EpilogueArgs 
     reinterpret_cast<float4*>(a.out + (size_t)t * d)[q] = acc;
 }
 
+// GEMV partials (segments spread over up to two CTAs per SM, so a token's
+// units have up to eight runs each): 32 warps per block share the runs.
+// Direct (few pieces per segment): 8 warps.
+template <typename K>
+static cudaError_t launch_epilogue_k(K kernel, const EpilogueArgs& a, cudaStream_t st) {
+    cudaError_t e = allow_max_smem(kernel);
+    if (e != cudaSuccess) return e;
+    const size_t smem = a.direct ? 0 : (size_t)(a.k + a.n_shared) * kSumChunks * 32 * sizeof(float4);
+    const int threads = a.direct ? 256 : 1024;
+    dim3 grid(a.T, (a.d / 4 + 31) / 32);
+    return launch_pdl(kernel, grid, dim3(threads), smem, st, a);
+}
+
 cudaError_t launch_layer_epilogue(const EpilogueArgs& a, cudaStream_t st) {
     if (a.T == 0) return cudaSuccess;
-    dim3 grid(a.T, (a.d / 4 + 31) / 32);
-    return a.bf16 ? launch_pdl(layer_epilogue_kernel<__nv_bfloat16>, grid, dim3(256), 0, st, a)
-                  : launch_pdl(layer_epilogue_kernel<float>, grid, dim3(256), 0, st, a);
+    if (a.k > kMaxTopK || a.n_shared > kMaxShared) return cudaErrorInvalidValue;
+    if (a.direct)
+        return a.bf16 ? launch_epilogue_k(layer_epilogue_kernel<__nv_bfloat16, true>, a, st)
+                      : launch_epilogue_k(layer_epilogue_kernel<float, true>, a, st);
+    return a.bf16 ? launch_epilogue_k(layer_epilogue_kernel<__nv_bfloat16, false>, a, st)
+                  : launch_epilogue_k(layer_epilogue_kernel<float, false>, a, st);
 }
 
 // One warp waits on a fresh mbarrier (arrival count 1) that no thread ever

@@ -99,7 +99,7 @@ moe_status check_dims(const moe_dims* D) {
     if (D->wtype == MOE_DTYPE_BF16 && D->d > 4096) return MOE_ERR_UNSUPPORTED;
     if (D->wtype == MOE_DTYPE_F32 && D->d > 1024) return MOE_ERR_UNSUPPORTED;
     if (D->r > 64) return MOE_ERR_UNSUPPORTED;
-    if (D->n_shared > 8) return MOE_ERR_UNSUPPORTED;
+    if (D->n_shared > kMaxShared) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
 }
 
@@ -461,7 +461,7 @@ moe_status expert_ffn_impl(const moe_dims* dims, const void* x, const void* tabl
         r.hdr = t.hdr; r.segs = t.segs; r.seg_first = ws_at<int32_t>(ws, L.seg_first);
         r.expert_offsets = expert_offsets; r.partial = t.partial; r.d = dims->d; r.N = dims->N;
         r.n_shared = dims->n_shared; r.T = dims->T; r.routed_cap = dims->T * dims->k;
-        r.y_perm = y_perm; r.y_shared = y_shared;
+        r.y_perm = y_perm; r.y_shared = y_shared; r.direct = true;
         MOE_CUDA(launch_gemv_reduce(r, S(stream)));
         count();
         return MOE_OK;
@@ -503,7 +503,7 @@ moe_status expert_ffn_impl(const moe_dims* dims, const void* x, const void* tabl
     r.hdr = p.hdr; r.segs = p.segs; r.seg_first = ws_at<int32_t>(ws, L.seg_first);
     r.expert_offsets = expert_offsets; r.partial = p.partial; r.d = dims->d; r.N = dims->N;
     r.n_shared = dims->n_shared; r.T = dims->T; r.routed_cap = dims->T * dims->k;
-    r.y_perm = y_perm; r.y_shared = y_shared;
+    r.y_perm = y_perm; r.y_shared = y_shared; r.direct = false;
     MOE_CUDA(launch_gemv_reduce(r, S(stream)));
     count();
     return MOE_OK;
@@ -645,6 +645,7 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_layer_args* A,
         ea.final_gate = O->final_gate; ea.z = ws_at<float>(ws, L.lore_z); ea.lore_b = lore ? A->lore_b : nullptr;
         ea.T = dims->T; ea.d = dims->d; ea.N = dims->N; ea.k = dims->k; ea.r = dims->r;
         ea.n_shared = dims->n_shared; ea.bf16 = bf16(dims);
+        ea.direct = A->keep_frac >= 1.f && tcd_usable(*dims);  // the partials of the decode tensor-core path
         ea.y_perm = O->y_perm; ea.y_shared = O->y_shared; ea.y_lore = O->y_lore; ea.out = O->out;
         if (!ea.out || !ea.y_perm || !O->inv_perm || (dims->n_shared > 0 && !ea.y_shared))
             return MOE_ERR_INVALID_ARG;
