@@ -3,11 +3,10 @@
 //
 // Who needs this: code that must not allocate device memory at the moment it
 // runs the layer — an engine plugin whose enqueue step is handed only its
-// inputs and outputs (the host engine owns the whole memory budget), a
+// inputs and outputs (the host engine owns the whole memory budget), or a
 // decode loop that cannot afford the device-wide synchronisation that
-// cudaMalloc/cudaFree imply, or a caller that records its work into a CUDA
-// graph where allocation calls are not allowed.  Such callers can still
-// provide inputs and outputs; this entry point supplies the rest.
+// cudaMalloc/cudaFree imply.  Such callers can still provide inputs and
+// outputs; this entry point supplies the rest.
 //
 // The scratch is a file-scope __device__ array of kScratchBytes (16 MiB).
 // Every GPU that loads this library holds it until the process exits.  It

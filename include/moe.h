@@ -251,9 +251,10 @@ moe_status moe_floe_kept_mask(const moe_dims* dims, void* ws, size_t ws_bytes, c
 
 /* moe_expert_ffn without a workspace, for callers that cannot allocate device
  * memory when they run the layer: an engine plugin handed only its inputs and
- * outputs, a decode loop that cannot pay the device-wide synchronisation of
- * cudaMalloc/cudaFree, or work recorded into a CUDA graph.  The source pages
- * have no counterpart of this call; it is a deployment convenience.
+ * outputs (the host engine owns the whole memory budget), or a decode loop
+ * that cannot pay the device-wide synchronisation of cudaMalloc/cudaFree.
+ * The source pages have no counterpart of this call; it is a deployment
+ * convenience.
  *   Same inputs and outputs as moe_expert_ffn (dense experts only, i.e.
  *   keep_frac = 1), with expert_offsets/perm from moe_permute.  The plan,
  *   partial sums and error word live in a 16 MiB array that the library

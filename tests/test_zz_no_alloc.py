@@ -2,9 +2,8 @@
 
 Some callers cannot allocate device memory at the moment they run the layer
 (an engine plugin that is handed only its inputs and outputs, a decode loop
-that cannot pay cudaMalloc's device-wide synchronisation, work recorded into
-a CUDA graph).  For them the library keeps a fixed 16 MiB scratch array per
-GPU.  This file checks, through the C ABI, that the entry point gives the
+that cannot pay cudaMalloc's device-wide synchronisation).  For them the
+library keeps a fixed 16 MiB scratch array per GPU.  This file checks, through the C ABI, that the entry point gives the
 same expert outputs as the workspace-based moe_expert_ffn on two calls in a
 row (with different routing, so the second call runs over the first call's
 leftovers in the shared array), and that a batch too large for the array is
