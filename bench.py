@@ -380,6 +380,7 @@ def main():
         kname, ksrc = {
             "tc-decode": ("moe_expert_ffn (ffn_tcd_kernel + gemv_reduce_kernel)",
                           "ffn_tcd.cu"),
+            "gemv-1tok": ("moe_expert_ffn (ffn_gemv1_kernel + gemv_reduce_kernel)", "ffn_gemv1.cu"),
             "gemv-floe": ("moe_expert_ffn (floe up/select/union/plan + sparse ffn_gemv_kernel"
                           " + gemv_reduce_kernel)", "ffn_gemv.cu"),
         }.get(path, ("moe_expert_ffn (ffn_gemv_kernel + gemv_reduce_kernel)", "ffn_gemv.cu"))

@@ -496,7 +496,12 @@ static cudaError_t launch_gemv_k(K kernel, int maxt, int vec, int ch, int esize,
     return note_launch(reinterpret_cast<const void*>(kernel), threads, smem, e);
 }
 
-static int gemv_ctas_per_sm(int d, bool bf16) { return (bf16 && d <= 2048) || !bf16 ? 2 : 1; }
+static int gemv_ctas_per_sm(int d, bool bf16) {
+#ifdef MOE_XP_GEMV_ONE_CTA
+    if (bf16) return 1;
+#endif
+    return (bf16 && d <= 2048) || !bf16 ? 2 : 1;
+}
 
 int gemv_grid_for(int d, bool bf16, int sms) {
     const int g = sms * gemv_ctas_per_sm(d, bf16);
@@ -514,7 +519,11 @@ int gemv_stages(int d, bool bf16) {
 // sparse segments); the dense instantiation carries none of their code.
 cudaError_t launch_gemv(const GemvParams& p, int G, bool bf16, cudaStream_t st, bool floe) {
     if (bf16) {
+#ifdef MOE_XP_GEMV_ONE_CTA
+        if (false)
+#else
         if (p.d <= 2048)
+#endif
             return floe ? launch_gemv_k(ffn_gemv_kernel_x2<__nv_bfloat16, 4, 2, true>, 256, 8, 2, 2, p, G, st)
                         : launch_gemv_k(ffn_gemv_kernel_x2<__nv_bfloat16, 4, 2, false>, 256, 8, 2, 2, p, G, st);
         return floe ? launch_gemv_k(ffn_gemv_kernel_x1<__nv_bfloat16, 4, 2, true>, 512, 8, 2, 2, p, G, st)

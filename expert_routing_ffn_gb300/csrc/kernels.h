@@ -98,6 +98,10 @@ struct GemvParams {
 int gemv_stages(int d, bool bf16);
 int gemv_grid_for(int d, bool bf16, int sms);
 cudaError_t launch_gemv(const GemvParams& p, int G, bool bf16, cudaStream_t st, bool floe = false);
+// one-token batches (every segment one row) of dense bf16 layers with d = 1536
+// or 2048: one channel per warp, the same plan and partial rows as launch_gemv
+bool gemv1_usable(int T, int d, bool bf16, bool floe);
+cudaError_t launch_gemv1(const GemvParams& p, int G, cudaStream_t st);
 
 struct FloeArgs {
     const void* x; const int32_t* perm; const int32_t* expert_offsets; const ExpertEntry* table;

@@ -496,7 +496,10 @@ moe_status expert_ffn_impl(const moe_dims* dims, const void* x, const void* tabl
         MOE_CUDA(launch_floe_prepare(f, pa, p, gemv_grid(dims), S(stream)));
         count(5);
     }
-    MOE_CUDA(launch_gemv(p, gemv_grid(dims), bf16(dims), S(stream), floe));
+    if (gemv1_usable(dims->T, dims->d, bf16(dims), floe))
+        MOE_CUDA(launch_gemv1(p, gemv_grid(dims), S(stream)));
+    else
+        MOE_CUDA(launch_gemv(p, gemv_grid(dims), bf16(dims), S(stream), floe));
     count();
     if (!reduce) return MOE_OK;
     GemvReduceArgs r;
@@ -526,6 +529,7 @@ const char* moe_expert_ffn_path(const moe_dims* dims, float keep_frac) {
     if (floe) return use_tc(*dims) || !bf16(dims) ? "unsupported" : "gemv-floe";
     if (use_tc(*dims)) return "tc-prefill";
     if (tcd_usable(*dims)) return "tc-decode";
+    if (gemv1_usable(dims->T, dims->d, bf16(dims), false)) return "gemv-1tok";
     return "gemv";
 }
 

@@ -227,7 +227,8 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* final_idx,
  *   GEMM; dense bf16 batches of 4..64 tokens (d a multiple of 128, expert
  *   widths multiples of 16) as a tcgen05 GEMM with the weight rows on the
  *   MMA's M side; the rest (1..3 tokens, fp32 layers, FloE) as an
- *   HBM-streaming CUDA-core GEMV. */
+ *   HBM-streaming CUDA-core GEMV (for one token of a dense bf16 layer with
+ *   d = 1536 or 2048, one channel per warp). */
 moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table,
                           const int32_t* expert_offsets, const int32_t* perm, float keep_frac,
                           float* y_perm, float* y_shared, void* ws, size_t ws_bytes,
@@ -236,9 +237,10 @@ moe_status moe_expert_ffn(const moe_dims* dims, const void* x, const void* table
 /* Which kernels moe_expert_ffn runs for these dimensions and keep_frac: a
  * static string, "tc-prefill" (gather + two tensor-core GEMM launches),
  * "tc-decode" (tensor-core GEMM + partial-row reduction, and a row gather
- * first for batches of 17..64 tokens), "gemv"
- * (CUDA-core GEMV + reduction), "gemv-floe" (FloE preparation + sparse GEMV
- * + reduction) or "unsupported".  No device work. */
+ * first for batches of 17..64 tokens), "gemv" (CUDA-core GEMV + reduction),
+ * "gemv-1tok" (the one-token CUDA-core GEMV, a channel per warp, +
+ * reduction), "gemv-floe" (FloE preparation + sparse GEMV + reduction) or
+ * "unsupported".  No device work. */
 const char* moe_expert_ffn_path(const moe_dims* dims, float keep_frac);
 
 /* Diagnostic: where the last moe_expert_ffn call with keep_frac < 1 left the

@@ -137,7 +137,10 @@ def _dims(name, T):
 
 @pytest.mark.parametrize("name,T,keep,path", [
     ("tiny", 16, 1.0, "gemv"),               # fp32 layer: CUDA-core GEMV
-    ("dsv2lite", 1, 1.0, "gemv"),            # 1..3 tokens: CUDA-core GEMV
+    ("dsv2lite", 1, 1.0, "gemv-1tok"),       # one token, d 1536 / 2048: a channel per warp
+    ("granite", 1, 1.0, "gemv-1tok"),
+    ("mixtral", 1, 1.0, "gemv"),             # 1..3 tokens: CUDA-core GEMV
+    ("dsv2lite", 2, 1.0, "gemv"),
     ("dsv2lite", 3, 1.0, "gemv"),
     ("dsv2lite", 4, 1.0, "tc-decode"),       # 4..64 tokens: tensor-core decode GEMM
     ("dsv2lite", 8, 1.0, "tc-decode"),

@@ -97,26 +97,39 @@ def test_policies_tiny(policy):
         assert kinds[2] > 0
 
 
-def test_stagewise_calls_equal_layer_forward():
+@pytest.mark.parametrize("name,T", [("tiny", 16),        # fp32 GEMV
+                                    ("dsv2lite", 1),     # one-token GEMV, LoRE slots, shared experts
+                                    ("granite", 1),      # one-token GEMV, d = 1536
+                                    ("dsv2lite", 3),     # GEMV with rows per segment
+                                    ("dsv2lite", 8)])    # decode tensor-core path
+def test_stagewise_calls_equal_layer_forward(name, T):
     """The six stage calls in sequence give bitwise the same output as
-    moe_layer_forward."""
-    cfg, W, layer, x, bufs, st, _ = _run("tiny", 16)
-    D = layer.dims.with_T(16)
+    moe_layer_forward (whose epilogue fuses the partial-row sum, the LoRE B
+    term and the combine)."""
+    cfg, W, layer, x, bufs, st, _ = _run(name, T)
+    assert st == moe.MOE_OK
+    D = layer.dims.with_T(T)
     xd = x_device(x, layer.dt)
-    b = LayerBuffers(layer, 16)
+    b = LayerBuffers(layer, T)
+    n_res = max(cfg.n_resident, 0)
     moe.moe_route(D, xd, layer.w_router, layer.router_bias, None, layer.w_prefetch, layer.w_ord,
-                  layer.theta, cfg.tau, 0, b.topk_idx, b.topk_gate, b.router_prob, b.delta_hat,
-                  b.prefetch_mask, b.delta_star, None, layer.ws)
-    moe.moe_select_resident(D, b.router_prob, b.topk_idx, b.prefetch_mask, None, cfg.policy,
+                  layer.theta, cfg.tau, n_res, b.topk_idx, b.topk_gate, b.router_prob, b.delta_hat,
+                  b.prefetch_mask, b.delta_star, b.batch_resident if n_res > 0 else None, layer.ws)
+    moe.moe_select_resident(D, b.router_prob, b.topk_idx,
+                            b.prefetch_mask if cfg.use_prefetch_mask else None,
+                            b.batch_resident if n_res > 0 else layer.resident, cfg.policy,
                             cfg.gamma, b.delta_hat, b.delta_star, b.final_idx, b.final_gate,
                             b.final_kind, b.fetch_mask, b.counters, layer.ws)
     moe.moe_permute(D, b.final_idx, b.final_kind, b.expert_offsets, b.perm, b.inv_perm, layer.ws)
     moe.moe_expert_ffn(D, xd, layer.table, b.expert_offsets, b.perm, 1.0, b.y_perm, b.y_shared,
                        layer.ws)
-    moe.moe_lore(D, xd, b.final_idx, b.final_kind, b.final_gate, layer.lore_a, layer.lore_b, b.y_lore,
-                 layer.ws)
-    moe.moe_combine(D, b.y_perm, b.inv_perm, b.final_gate, b.final_kind, b.y_shared, b.y_lore, b.out)
+    if cfg.r > 0:
+        moe.moe_lore(D, xd, b.final_idx, b.final_kind, b.final_gate, layer.lore_a, layer.lore_b,
+                     b.y_lore, layer.ws)
+    moe.moe_combine(D, b.y_perm, b.inv_perm, b.final_gate, b.final_kind, b.y_shared,
+                    b.y_lore if cfg.r > 0 else None, b.out)
     assert moe.moe_check(layer.ws)[0] == moe.MOE_OK
+    assert torch.equal(b.final_idx, bufs.final_idx)
     assert torch.equal(b.out, bufs.out)
 
 
