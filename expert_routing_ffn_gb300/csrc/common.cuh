@@ -21,6 +21,7 @@ constexpr int kMaxShared = 8;         // shared experts per layer
 constexpr int kGemvMaxRows = 8;       // rows per GEMV segment (register-resident)
 constexpr int kGemvMaxCtas = 512;     // upper bound of the GEMV grid (workspace sizing)
 constexpr int kAlign = 256;
+constexpr int kPermChunk = 1024;      // slots per block of the multi-block permutation
 // Iteration bound of every spin wait; a wait that exceeds it records
 // MOE_ERR_TIMEOUT and gives up instead of hanging the GPU.
 constexpr uint32_t kSpinLimit = 1u << 24;
@@ -252,7 +253,7 @@ constexpr int kTcdMaxCtas = 160;  // grid of that path: min(SMs, kTcdMaxCtas)
 
 // ---------------------------------------------------------------- workspace
 struct WsLayout {
-    size_t err, ticket, logits_r, logits_p, score, qp, plan_hdr, segs, seg_first, lore_z, tc_plan,
+    size_t err, ticket, logits_r, logits_p, score, qp, plan_hdr, segs, seg_first, perm_counts, lore_z, tc_plan,
         x_perm, h_routed, h_shared, floe_u, floe_kept, floe_list, floe_count, partial, total;
     int max_segs, max_partial_rows;
 };
@@ -302,6 +303,8 @@ __host__ __device__ inline WsLayout ws_layout(const moe_dims& D) {
     L.plan_hdr = take(sizeof(PlanHeader));
     L.segs = take((size_t)L.max_segs * sizeof(Seg));
     L.seg_first = take((N + (size_t)D.n_shared + 1) * 4);
+    // per 1024-slot chunk and expert: slot counts of the multi-block permutation
+    L.perm_counts = take((T * (size_t)D.k + kPermChunk - 1) / kPermChunk * kMaxExperts * 4);
     L.lore_z = take(T * (size_t)D.k * (size_t)(D.r > 0 ? D.r : 1) * 4);
     L.tc_plan = take(sizeof(TcPlan));
     L.x_perm = take(tc || tcd ? T * D.k * (size_t)D.d * 2 : 0);

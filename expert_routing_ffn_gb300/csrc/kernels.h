@@ -55,7 +55,9 @@ struct PlanArgs {
     TcPlan* tc_plan;  // also built when non-null
 };
 // permutation + FFN plan in one launch (the last block builds the plan)
-cudaError_t launch_permute(const PermuteArgs& a, const PlanArgs& plan, int* ticket, cudaStream_t st);
+// counts: workspace of ceil(n_slots / kPermChunk) * kMaxExperts ints (batches
+// of more than 1024 slots)
+cudaError_t launch_permute(const PermuteArgs& a, const PlanArgs& plan, int32_t* counts, cudaStream_t st);
 
 // The routing front end of a small batch (T <= kFrontMaxTokens, T * k <=
 // kFrontMaxSlots) in one

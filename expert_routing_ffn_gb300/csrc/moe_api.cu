@@ -404,7 +404,7 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* final_idx, const int
     PlanArgs pa;
     MOE_TRY(prep_permute(dims, final_idx, final_kind, expert_offsets, perm, inv_perm, ws, a, pa));
     const WsLayout L = ws_layout(*dims);
-    MOE_CUDA(launch_permute(a, pa, ws_at<int>(ws, L.ticket), S(stream)));
+    MOE_CUDA(launch_permute(a, pa, ws_at<int32_t>(ws, L.perm_counts), S(stream)));
     count();
     return MOE_OK;
 }

@@ -10,93 +10,116 @@
 namespace moe {
 
 
-// One block per expert e.  Pass 1 counts the slots routed to experts below e
-// (the segment offset) and to e; pass 2 walks the slots in order and
-// scatters e's slots with a block-wide prefix over 1024-slot chunks.
-// Block 0 also marks LoRE / empty slots with inv_perm = -1.
-// The last block to finish (arrival counter `ticket`, left at 0 afterwards)
-// also builds the FFN plan from the complete expert_offsets.
-__global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict__ final_idx,
-                                                       const int32_t* __restrict__ final_kind,
-                                                       int n_slots, int N,
-                                                       int32_t* __restrict__ expert_offsets,
-                                                       int32_t* __restrict__ perm,
-                                                       int32_t* __restrict__ inv_perm,
-                                                       DevError* __restrict__ err, PlanArgs plan,
-                                                       int* __restrict__ ticket) {
-    __shared__ int red_less[32], red_eq[32];
-    __shared__ int warp_pref[32];
-    __shared__ int s_off;
-    __shared__ int s_last;
-    __shared__ int s_offsets[kMaxExperts + 1];
-    const int e = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-    int less = 0, eq = 0;
-    for (int i = tid; i < n_slots; i += blockDim.x) {
-        const int x = final_idx[i];
-        const bool valid = x >= 0 && final_kind[i] != MOE_KIND_LORE;
-        if (x >= N) { if (e == 0) set_error(err, MOE_ERR_DEVICE_INDEX, i); continue; }
-        less += (valid && x < e) ? 1 : 0;
-        eq += (valid && x == e) ? 1 : 0;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        less += __shfl_xor_sync(0xffffffffu, less, o);
-        eq += __shfl_xor_sync(0xffffffffu, eq, o);
-    }
-    if (lane == 0) { red_less[warp] = less; red_eq[warp] = eq; }
+// Batches of more than 1024 slots: two launches over chunks of kPermChunk
+// slots, one block (one thread per slot) per chunk.
+//  1. permute_count_kernel: the chunk's slot count per expert -> counts[c][e].
+//  2. permute_scatter_kernel: every block scans the count table (expert
+//     offsets, and the slots of earlier chunks per expert), ranks its slots
+//     within the chunk (per-warp ranks by __match_any_sync, then earlier warps)
+//     and scatters them; the order is stable in slot order, as in
+//     permute_block.  Block 0 writes expert_offsets and builds the FFN plan.
+__device__ __forceinline__ int permute_key(const int32_t* __restrict__ final_idx,
+                                           const int32_t* __restrict__ final_kind, int i, int n_slots, int N,
+                                           DevError* __restrict__ err) {
+    if (i >= n_slots) return -1;
+    const int x = final_idx[i];
+    if (x >= N) { set_error(err, MOE_ERR_DEVICE_INDEX, i); return -1; }
+    return (x >= 0 && final_kind[i] != MOE_KIND_LORE) ? x : -1;
+}
+
+// per warp and expert: the warp's slot count; returns this slot's rank among
+// the warp's slots of the same expert
+__device__ __forceinline__ int permute_warp_counts(int key, int (*cnt)[kMaxExperts]) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t peers = __match_any_sync(0xffffffffu, key);
+    if (key >= 0 && __popc(peers & ((1u << lane) - 1u)) == 0) cnt[warp][key] = __popc(peers);
+    return __popc(peers & ((1u << lane) - 1u));
+}
+
+__global__ void __launch_bounds__(kPermChunk) permute_count_kernel(const int32_t* __restrict__ final_idx,
+                                                                   const int32_t* __restrict__ final_kind,
+                                                                   int n_slots, int N,
+                                                                   int32_t* __restrict__ counts,
+                                                                   DevError* __restrict__ err) {
+    __shared__ int cnt[kPermChunk / 32][kMaxExperts];
+    const int tid = threadIdx.x, nw = blockDim.x >> 5;
+    for (int i = tid; i < nw * kMaxExperts; i += blockDim.x) (&cnt[0][0])[i] = 0;
     __syncthreads();
-    if (tid == 0) {
-        int L = 0, E = 0;
-        for (int w = 0; w < nw; ++w) { L += red_less[w]; E += red_eq[w]; }
-        s_off = L;
-        expert_offsets[e] = L;
-        if (e == N - 1) expert_offsets[N] = L + E;
+    const int key = permute_key(final_idx, final_kind, blockIdx.x * kPermChunk + tid, n_slots, N, err);
+    (void)permute_warp_counts(key, cnt);
+    __syncthreads();
+    if (tid < N) {
+        int tot = 0;
+        for (int w = 0; w < nw; ++w) tot += cnt[w][tid];
+        counts[(size_t)blockIdx.x * kMaxExperts + tid] = tot;
+    }
+    grid_dep_launch();
+}
+
+__global__ void __launch_bounds__(kPermChunk) permute_scatter_kernel(const int32_t* __restrict__ final_idx,
+                                                                     const int32_t* __restrict__ final_kind,
+                                                                     int n_slots, int N,
+                                                                     const int32_t* __restrict__ counts,
+                                                                     int32_t* __restrict__ expert_offsets,
+                                                                     int32_t* __restrict__ perm,
+                                                                     int32_t* __restrict__ inv_perm,
+                                                                     PlanArgs plan) {
+    __shared__ int cnt[kPermChunk / 32][kMaxExperts];  // per warp and expert, then exclusive over warps
+    __shared__ int base[kMaxExperts];                    // first position of this chunk's slots per expert
+    __shared__ int s_off[kMaxExperts + 1];
+    const int c = blockIdx.x, n_chunks = gridDim.x;
+    const int tid = threadIdx.x, warp = tid >> 5, nw = blockDim.x >> 5;
+    for (int i = tid; i < nw * kMaxExperts; i += blockDim.x) (&cnt[0][0])[i] = 0;
+    const int slot = c * kPermChunk + tid;
+    // final_idx / final_kind come from the previous kernels (the count
+    // kernel reported bad indices already)
+    grid_dep_wait();
+    int key = -1;
+    if (slot < n_slots) {
+        const int x = final_idx[slot];
+        if (x >= 0 && x < N && final_kind[slot] != MOE_KIND_LORE) key = x;
     }
     __syncthreads();
-    int running = s_off;
-    for (int base = 0; base < n_slots; base += blockDim.x) {
-        const int i = base + tid;
-        bool mine = false, valid = false;
-        if (i < n_slots) {
-            const int x = final_idx[i];
-            valid = x >= 0 && x < N && final_kind[i] != MOE_KIND_LORE;
-            mine = valid && x == e;
-            if (e == 0 && !valid) inv_perm[i] = -1;
+    const int rank = permute_warp_counts(key, cnt);
+    // expert totals and this chunk's start per expert, from the count table
+    int before = 0, tot = 0;
+    if (tid < N) {
+        for (int q = 0; q < n_chunks; ++q) {
+            const int v = __ldcg(counts + (size_t)q * kMaxExperts + tid);
+            if (q < c) before += v;
+            tot += v;
         }
-        const uint32_t b = __ballot_sync(0xffffffffu, mine);
-        if (lane == 0) warp_pref[warp] = __popc(b);
-        __syncthreads();
-        int before = 0, total = 0;
+    }
+    int all;
+    const int first = block_exclusive_scan(tid < N ? tot : 0, &all);  // syncs: cnt complete after it
+    if (tid < N) { s_off[tid] = first; base[tid] = first + before; }
+    if (tid == 0) s_off[N] = all;
+    if (tid < N) {
+        int run = 0;
         for (int w = 0; w < nw; ++w) {
-            const int c = warp_pref[w];
-            if (w < warp) before += c;
-            total += c;
+            const int v = cnt[w][tid];
+            cnt[w][tid] = run;
+            run += v;
         }
-        if (mine) {
-            const int pos = running + before + __popc(b & ((1u << lane) - 1u));
-            perm[pos] = i;
-            inv_perm[i] = pos;
-        }
-        running += total;
-        __syncthreads();
-    }
-    if (tid == 0) {
-        __threadfence();
-        s_last = atomicAdd(ticket, 1) == (int)gridDim.x - 1;
     }
     __syncthreads();
-    if (s_last) {
-        __threadfence();
-        for (int i = tid; i <= N; i += blockDim.x) s_offsets[i] = __ldcg(&expert_offsets[i]);
-        __syncthreads();
+    if (slot < n_slots) {
+        if (key >= 0) {
+            const int pos = base[key] + cnt[warp][key] + rank;
+            perm[pos] = slot;
+            inv_perm[slot] = pos;
+        } else {
+            inv_perm[slot] = -1;
+        }
+    }
+    if (c == 0) {
+        if (tid <= N) expert_offsets[tid] = s_off[tid];
         // only the plan of the path moe_expert_ffn will take
         if (plan.tc_plan) {
-            if (tid == 0) build_tc_plan(plan, s_offsets);
+            if (tid == 0) build_tc_plan(plan, s_off);
         } else {
-            build_plan(plan, s_offsets);
+            build_plan(plan, s_off);
         }
-        if (tid == 0) *ticket = 0;
     }
 }
 
@@ -117,7 +140,7 @@ __global__ void __launch_bounds__(256) plan_gemv_kernel(PlanArgs a) {
     build_plan(a, off);
 }
 
-cudaError_t launch_permute(const PermuteArgs& a, const PlanArgs& plan, int* ticket,
+cudaError_t launch_permute(const PermuteArgs& a, const PlanArgs& plan, int32_t* counts,
                            cudaStream_t st) {
     if (a.n_slots <= 1024) {
         const int threads = a.n_slots <= 256 ? 256 : 1024;
@@ -125,9 +148,14 @@ cudaError_t launch_permute(const PermuteArgs& a, const PlanArgs& plan, int* tick
                                                    a.expert_offsets, a.perm, a.inv_perm, a.err, plan);
         return cudaGetLastError();
     }
-    permute_kernel<<<a.N, 1024, 0, st>>>(a.final_idx, a.final_kind, a.n_slots, a.N,
-                                         a.expert_offsets, a.perm, a.inv_perm, a.err, plan, ticket);
-    return cudaGetLastError();
+    const int n_chunks = (a.n_slots + kPermChunk - 1) / kPermChunk;
+    permute_count_kernel<<<n_chunks, kPermChunk, 0, st>>>(a.final_idx, a.final_kind, a.n_slots, a.N, counts,
+                                                          a.err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_pdl(permute_scatter_kernel, dim3(n_chunks), dim3(kPermChunk), 0, st, a.final_idx,
+                      a.final_kind, a.n_slots, a.N, (const int32_t*)counts, a.expert_offsets, a.perm,
+                      a.inv_perm, plan);
 }
 
 cudaError_t launch_plan_gemv(const PlanArgs& a, cudaStream_t st) {

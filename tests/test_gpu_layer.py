@@ -101,7 +101,8 @@ def test_policies_tiny(policy):
                                     ("dsv2lite", 1),     # one-token GEMV, LoRE slots, shared experts
                                     ("granite", 1),      # one-token GEMV, d = 1536
                                     ("dsv2lite", 3),     # GEMV with rows per segment
-                                    ("dsv2lite", 8)])    # decode tensor-core path
+                                    ("dsv2lite", 8),     # decode tensor-core path
+                                    ("granite", 200)])   # prefill: chunked permutation, tensor-core GEMM
 def test_stagewise_calls_equal_layer_forward(name, T):
     """The six stage calls in sequence give bitwise the same output as
     moe_layer_forward (whose epilogue fuses the partial-row sum, the LoRE B
