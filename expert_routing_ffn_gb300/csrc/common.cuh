@@ -253,7 +253,8 @@ constexpr int kTcdMaxCtas = 160;  // grid of that path: min(SMs, kTcdMaxCtas)
 
 // ---------------------------------------------------------------- workspace
 struct WsLayout {
-    size_t err, ticket, logits_r, logits_p, score, qp, plan_hdr, segs, seg_first, perm_counts, lore_z, tc_plan,
+    size_t err, ticket, logits_r, logits_p, score, qp, plan_hdr, segs, seg_first, perm_counts, lore_z,
+        lore_off, lore_list, lore_pos, lore_counts, lore_zp, lore_v, tc_plan,
         x_perm, h_routed, h_shared, floe_u, floe_kept, floe_list, floe_count, partial, total;
     int max_segs, max_partial_rows;
 };
@@ -306,6 +307,15 @@ __host__ __device__ inline WsLayout ws_layout(const moe_dims& D) {
     // per 1024-slot chunk and expert: slot counts of the multi-block permutation
     L.perm_counts = take((T * (size_t)D.k + kPermChunk - 1) / kPermChunk * kMaxExperts * 4);
     L.lore_z = take(T * (size_t)D.k * (size_t)(D.r > 0 ? D.r : 1) * 4);
+    // LoRE slots grouped by expert and their B_e z rows (batches of more than
+    // kTcMinTokens tokens: the condition of lore_grouped_usable)
+    const bool lore_grouped = D.r > 0 && D.T > kTcMinTokens;
+    L.lore_off = take(lore_grouped ? (N + 1) * 4 : 0);
+    L.lore_list = take(lore_grouped ? T * D.k * 4 : 0);
+    L.lore_pos = take(lore_grouped ? T * D.k * 4 : 0);
+    L.lore_counts = take(lore_grouped ? (T * (size_t)D.k + kPermChunk - 1) / kPermChunk * kMaxExperts * 4 : 0);
+    L.lore_zp = take(lore_grouped ? 8 * T * (size_t)D.k * (size_t)(D.r > 0 ? D.r : 1) * 4 : 0);  // 8 d-splits
+    L.lore_v = take(lore_grouped ? T * (size_t)D.k * (size_t)D.d * 4 : 0);
     L.tc_plan = take(sizeof(TcPlan));
     L.x_perm = take(tc || tcd ? T * D.k * (size_t)D.d * 2 : 0);
     L.h_routed = take(tc ? T * D.k * (size_t)D.I * 2 : 0);

@@ -58,6 +58,10 @@ struct PlanArgs {
 // counts: workspace of ceil(n_slots / kPermChunk) * kMaxExperts ints (batches
 // of more than 1024 slots)
 cudaError_t launch_permute(const PermuteArgs& a, const PlanArgs& plan, int32_t* counts, cudaStream_t st);
+// the LoRE slots grouped by expert, stable in slot order (two launches):
+// expert_offsets [N + 1], perm = grouped position -> slot, inv_perm = slot ->
+// grouped position or -1
+cudaError_t launch_group_lore(const PermuteArgs& a, int32_t* counts, cudaStream_t st);
 
 // The routing front end of a small batch (T <= kFrontMaxTokens, T * k <=
 // kFrontMaxSlots) in one
@@ -153,8 +157,13 @@ cudaError_t launch_tcd_ffn(const TcdLaunch& a, cudaStream_t st);
 struct LoreArgs {
     const void* x; const int32_t *final_idx, *final_kind; const float* final_gate;
     const void *A, *B; int T, d, k, r, N; bool bf16; float* z; float* y_lore; DevError* err;
+    // batches of more than kTcMinTokens tokens: the LoRE slots grouped by
+    // expert (workspace), and the per-slot B_e z rows
+    int32_t *g_off, *g_list, *g_pos, *g_counts; float *zp, *v;
 };
 cudaError_t launch_lore(const LoreArgs& a, cudaStream_t st);
+// whether launch_lore takes the grouped path (given the workspace buffers)
+bool lore_grouped_usable(int T, int d, int r, bool bf16);
 // z = g A_e x only (the first half of launch_lore)
 cudaError_t launch_lore_z(const LoreArgs& a, cudaStream_t st);
 

@@ -98,6 +98,273 @@ __global__ void __launch_bounds__(256) lore_b_kernel(const int32_t* __restrict__
     y_lore[(size_t)t * d + j] = acc;
 }
 
+// ---------------------------------------------------------------------------
+// Large batches: the LoRE slots grouped by expert (launch_group_lore), so that
+// A_e and B_e are read once per tile of up to kLoreTile slots of e instead of
+// once per slot.  Tile index -> (expert, first grouped position) from the
+// per-expert tile counts; every block walks tiles blockIdx.x, + gridDim.x, ...
+// Both products are register-tiled on the CUDA cores (rank r <= 64 is too
+// narrow a GEMM side to pay for a tensor-core pipeline): operands staged in
+// shared memory K-major as fp32, thread = 4 x 4 outputs from two 16-byte
+// shared loads per step.
+constexpr int kLoreTile = 64;
+constexpr int kLoreKC = 32;  // values of d per shared-memory chunk (z pass)
+constexpr int kLoreKS = 8;   // d split over this many blocks per tile (z pass)
+
+// the expert and first grouped position of tile `tile`; false past the last tile
+__device__ __forceinline__ bool lore_tile_of(const int* s_off, int N, int tile, int& e, int& first) {
+    int t0 = 0;
+    for (int x = 0; x < N; ++x) {
+        const int n = (s_off[x + 1] - s_off[x] + kLoreTile - 1) / kLoreTile;
+        if (tile < t0 + n) { e = x; first = s_off[x] + (tile - t0) * kLoreTile; return true; }
+        t0 += n;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void fma4x4(float (&acc)[4][4], const float4& a, const float4& b) {
+    const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        fma2(acc[i][0], acc[i][1], av[i], av[i], b.x, b.y);
+        fma2(acc[i][2], acc[i][3], av[i], av[i], b.z, b.w);
+    }
+}
+
+// zp[ks, pos, q] = A_e[q, d-range ks] . x_t[d-range ks] for the slots of a
+// tile (pos = grouped position): d is split over kLoreKS blocks (blockIdx.y),
+// whose partials lore_b_grouped_kernel adds in ks order.  Thread (slot quad
+// sq, rank quad rq), 4 r threads computing; d in chunks of kLoreKC, the next
+// chunk's global loads in flight during the current one.
+template <typename W>
+__global__ void __launch_bounds__(256) lore_z_grouped_kernel(const W* __restrict__ x,
+                                                             const W* __restrict__ A,
+                                                             const int32_t* __restrict__ g_off,
+                                                             const int32_t* __restrict__ g_list, int d, int k,
+                                                             int r, int N, int n_pos, float* __restrict__ zp) {
+    constexpr int V = Vec<W>::n;
+    constexpr int CV = kLoreKC / V;                    // 16-byte vectors per row and chunk
+    constexpr int XL = (kLoreTile * CV + 255) / 256;   // x vectors per thread and chunk
+    constexpr int AL = (64 * CV + 255) / 256;          // A vectors per thread and chunk (r <= 64)
+    __shared__ __align__(16) float xs[kLoreKC][kLoreTile];
+    __shared__ __align__(16) float as[kLoreKC][64];
+    __shared__ int s_off[kMaxExperts + 1];
+    __shared__ int s_tok[kLoreTile];
+    const int tid = threadIdx.x, sq = tid & 15, rq = tid >> 4;
+    const bool computes = rq * 4 < r;
+    for (int i = tid; i <= N; i += blockDim.x) s_off[i] = g_off[i];
+    __syncthreads();
+    int e, first;
+    for (int tile = blockIdx.x; lore_tile_of(s_off, N, tile, e, first); tile += gridDim.x) {
+        const int nt = min(kLoreTile, s_off[e + 1] - first);
+        if (tid < kLoreTile) s_tok[tid] = tid < nt ? g_list[first + tid] / k : -1;
+        __syncthreads();
+        const W* Ae = A + (size_t)e * r * d;
+        uint4 rx[XL], ra[AL];
+        auto load = [&](int k0) {
+#pragma unroll
+            for (int j = 0; j < XL; ++j) {
+                const int i = tid + 256 * j, row = i % kLoreTile, cv = i / kLoreTile;
+                rx[j] = make_uint4(0, 0, 0, 0);
+                if (cv < CV && s_tok[row] >= 0 && k0 + cv * V < d)
+                    rx[j] = *reinterpret_cast<const uint4*>(x + (size_t)s_tok[row] * d + k0 + cv * V);
+            }
+#pragma unroll
+            for (int j = 0; j < AL; ++j) {
+                const int i = tid + 256 * j, q = i % 64, cv = i / 64;
+                ra[j] = make_uint4(0, 0, 0, 0);
+                if (cv < CV && q < r && k0 + cv * V < d)
+                    ra[j] = *reinterpret_cast<const uint4*>(Ae + (size_t)q * d + k0 + cv * V);
+            }
+        };
+        float acc[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+        const int n_chunks = (d + kLoreKC - 1) / kLoreKC, ks = blockIdx.y;
+        const int k_begin = ks * n_chunks / kLoreKS * kLoreKC;
+        const int k_end = min(d, (ks + 1) * n_chunks / kLoreKS * kLoreKC);
+        if (k_begin < k_end) load(k_begin);
+        for (int k0 = k_begin; k0 < k_end; k0 += kLoreKC) {
+#pragma unroll
+            for (int j = 0; j < XL; ++j) {
+                const int i = tid + 256 * j, row = i % kLoreTile, cv = i / kLoreTile;
+                if (cv < CV) {
+                    float v[V];
+                    unpack16(rx[j], v, (W*)nullptr);
+#pragma unroll
+                    for (int u = 0; u < V; ++u) xs[cv * V + u][row] = v[u];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < AL; ++j) {
+                const int i = tid + 256 * j, q = i % 64, cv = i / 64;
+                if (cv < CV) {
+                    float v[V];
+                    unpack16(ra[j], v, (W*)nullptr);
+#pragma unroll
+                    for (int u = 0; u < V; ++u) as[cv * V + u][q] = v[u];
+                }
+            }
+            __syncthreads();
+            if (k0 + kLoreKC < k_end) load(k0 + kLoreKC);
+            if (computes) {
+                const int kc = min(kLoreKC, d - k0);
+                if (kc == kLoreKC) {
+#pragma unroll
+                    for (int kk = 0; kk < kLoreKC; ++kk)
+                        fma4x4(acc, *reinterpret_cast<const float4*>(&xs[kk][sq * 4]),
+                               *reinterpret_cast<const float4*>(&as[kk][rq * 4]));
+                } else {
+                    for (int kk = 0; kk < kc; ++kk)
+                        fma4x4(acc, *reinterpret_cast<const float4*>(&xs[kk][sq * 4]),
+                               *reinterpret_cast<const float4*>(&as[kk][rq * 4]));
+                }
+            }
+            __syncthreads();
+        }
+        if (computes) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int p = sq * 4 + i;
+                if (p >= nt) continue;
+                *reinterpret_cast<float4*>(zp + ((size_t)ks * n_pos + first + p) * r + rq * 4) =
+                    make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+            }
+        }
+        __syncthreads();  // s_tok is rewritten by the next tile
+    }
+}
+
+// zg[pos, :] = g_slot * (the kLoreKS partials zp[., pos, :] added in order),
+// for the n = g_off[N] grouped positions; one thread per 4 rank values.
+__global__ void __launch_bounds__(256) lore_z_sum_kernel(const float* __restrict__ final_gate,
+                                                         const int32_t* __restrict__ g_off,
+                                                         const int32_t* __restrict__ g_list, int r, int N,
+                                                         int n_pos, const float* __restrict__ zp,
+                                                         float* __restrict__ zg) {
+    const int n = g_off[N];
+    const int r4 = r / 4;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n * r4; i += gridDim.x * blockDim.x) {
+        const int pos = i / r4, q4 = i % r4;
+        float4 p[kLoreKS];
+#pragma unroll
+        for (int ks = 0; ks < kLoreKS; ++ks)
+            p[ks] = *reinterpret_cast<const float4*>(zp + ((size_t)ks * n_pos + pos) * r + q4 * 4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int ks = 0; ks < kLoreKS; ++ks) add4(acc, p[ks]);
+        const float g = final_gate[g_list[pos]];
+        *reinterpret_cast<float4*>(zg + (size_t)pos * r + q4 * 4) =
+            make_float4(g * acc.x, g * acc.y, g * acc.z, g * acc.w);
+    }
+}
+
+// v[pos, c] = B_e[c, :] . zg[pos] for the slots of a tile (pos = grouped
+// position) and the columns c of this block's share of d (blockIdx.y of
+// kLoreBY shares, in chunks of 64 columns, the next chunk's B_e rows in flight
+// during the current one).  Thread (slot quad, column quad).
+constexpr int kLoreBY = 4;
+template <typename W>
+__global__ void __launch_bounds__(256) lore_b_grouped_kernel(const W* __restrict__ B,
+                                                             const int32_t* __restrict__ g_off, int d, int r,
+                                                             int N, const float* __restrict__ zg,
+                                                             float* __restrict__ v) {
+    constexpr int V = Vec<W>::n;
+    constexpr int TC = 64;                 // columns per chunk
+    constexpr int BL = (64 * TC / V + 255) / 256;  // B vectors per thread and chunk (r <= 64)
+    __shared__ __align__(16) float zs[64][kLoreTile];  // [q][slot]
+    __shared__ __align__(16) float bs[64][TC];         // [q][column]
+    __shared__ int s_off[kMaxExperts + 1];
+    const int tid = threadIdx.x, sq = tid & 15, cq = tid >> 4;
+    const int n_chunks = (d + TC - 1) / TC;
+    const int ch_begin = blockIdx.y * n_chunks / kLoreBY, ch_end = (blockIdx.y + 1) * n_chunks / kLoreBY;
+    const int rv = r / V;  // r * sizeof(W) is a multiple of 16 on this path
+    for (int i = tid; i <= N; i += blockDim.x) s_off[i] = g_off[i];
+    __syncthreads();
+    int e, first;
+    for (int tile = blockIdx.x; lore_tile_of(s_off, N, tile, e, first); tile += gridDim.x) {
+        const int nt = min(kLoreTile, s_off[e + 1] - first);
+        // z rows: 64 x r / 4 float4, two per thread at r = 32
+        for (int i0 = tid; i0 < kLoreTile * r / 4; i0 += 2 * blockDim.x) {
+            float4 zz[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int i = i0 + u * blockDim.x, row = i % kLoreTile;
+                zz[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (i < kLoreTile * r / 4 && row < nt)
+                    zz[u] = *reinterpret_cast<const float4*>(zg + (size_t)(first + row) * r + (i / kLoreTile) * 4);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int i = i0 + u * blockDim.x, row = i % kLoreTile, q4 = i / kLoreTile;
+                if (i < kLoreTile * r / 4) {
+                    zs[q4 * 4 + 0][row] = zz[u].x; zs[q4 * 4 + 1][row] = zz[u].y;
+                    zs[q4 * 4 + 2][row] = zz[u].z; zs[q4 * 4 + 3][row] = zz[u].w;
+                }
+            }
+        }
+        const W* Be = B + (size_t)e * d * r;
+        uint4 rb[BL];
+        auto load = [&](int ch) {
+#pragma unroll
+            for (int j = 0; j < BL; ++j) {
+                const int i = tid + 256 * j, col = i % TC, qv = i / TC, c = ch * TC + col;
+                rb[j] = make_uint4(0, 0, 0, 0);
+                if (qv < rv && c < d) rb[j] = *reinterpret_cast<const uint4*>(Be + (size_t)c * r + qv * V);
+            }
+        };
+        if (ch_begin < ch_end) load(ch_begin);
+        for (int ch = ch_begin; ch < ch_end; ++ch) {
+            __syncthreads();  // bs free (previous chunk), zs written (first chunk)
+#pragma unroll
+            for (int j = 0; j < BL; ++j) {
+                const int i = tid + 256 * j, col = i % TC, qv = i / TC;
+                if (qv < rv) {
+                    float b[V];
+                    unpack16(rb[j], b, (W*)nullptr);
+#pragma unroll
+                    for (int u = 0; u < V; ++u) bs[qv * V + u][col] = b[u];
+                }
+            }
+            __syncthreads();
+            if (ch + 1 < ch_end) load(ch + 1);
+            float acc[4][4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[i][c] = 0.f;
+            for (int q = 0; q < r; ++q)
+                fma4x4(acc, *reinterpret_cast<const float4*>(&zs[q][sq * 4]),
+                       *reinterpret_cast<const float4*>(&bs[q][cq * 4]));
+            const int col = ch * TC + cq * 4;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (sq * 4 + i >= nt || col >= d) continue;
+                *reinterpret_cast<float4*>(v + (size_t)(first + sq * 4 + i) * d + col) =
+                    make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+            }
+        }
+        __syncthreads();  // zs is rewritten by the next tile
+    }
+}
+
+// y_lore[t] = the token's LoRE rows v[pos], added in slot order from zero.
+__global__ void __launch_bounds__(256) lore_sum_kernel(const int32_t* __restrict__ g_pos, const float* __restrict__ v,
+                                                       int d, int k, float* __restrict__ y_lore) {
+    const int t = blockIdx.x;
+    const int q = blockIdx.y * blockDim.x + threadIdx.x;  // float4 column group
+    __shared__ int s_pos[kMaxTopK];
+    if (threadIdx.x < k) s_pos[threadIdx.x] = g_pos[(size_t)t * k + threadIdx.x];
+    __syncthreads();
+    if (q >= d / 4) return;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < k; ++s)
+        if (s_pos[s] >= 0) add4(acc, reinterpret_cast<const float4*>(v + (size_t)s_pos[s] * d)[q]);
+    reinterpret_cast<float4*>(y_lore + (size_t)t * d)[q] = acc;
+}
+
 // out[t] = y_shared[t] (1 + sum of LoRE gates) + sum_s g_s y_perm[inv_perm[t,s]]
 //        + y_lore[t]; slots in order.
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y_perm,
@@ -395,8 +662,35 @@ cudaError_t launch_lore_z(const LoreArgs& a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+template <typename W>
+static cudaError_t launch_lore_grouped(const LoreArgs& a, cudaStream_t st) {
+    PermuteArgs pa;
+    pa.final_idx = a.final_idx; pa.final_kind = a.final_kind; pa.n_slots = a.T * a.k; pa.N = a.N;
+    pa.expert_offsets = a.g_off; pa.perm = a.g_list; pa.inv_perm = a.g_pos; pa.err = a.err;
+    cudaError_t e = launch_group_lore(pa, a.g_counts, st);
+    if (e != cudaSuccess) return e;
+    // tiles: at most T*k / kLoreTile + N
+    const int n_pos = a.T * a.k;
+    const int tiles = n_pos / kLoreTile + a.N;
+    const int gz = tiles < 160 ? tiles : 160;
+    lore_z_grouped_kernel<W><<<dim3(gz, kLoreKS), 256, 0, st>>>((const W*)a.x, (const W*)a.A, a.g_off, a.g_list,
+                                                                 a.d, a.k, a.r, a.N, n_pos, a.zp);
+    lore_z_sum_kernel<<<4 * 152, 256, 0, st>>>(a.final_gate, a.g_off, a.g_list, a.r, a.N, n_pos, a.zp, a.z);
+    const int gx = tiles < 304 ? tiles : 304;
+    lore_b_grouped_kernel<W><<<dim3(gx, kLoreBY), 256, 0, st>>>((const W*)a.B, a.g_off, a.d, a.r, a.N, a.z, a.v);
+    lore_sum_kernel<<<dim3(a.T, (a.d / 4 + 255) / 256), 256, 0, st>>>(a.g_pos, a.v, a.d, a.k, a.y_lore);
+    return cudaGetLastError();
+}
+
+bool lore_grouped_usable(int T, int d, int r, bool bf16) {
+    const int esize = bf16 ? 2 : 4;
+    return T > kTcMinTokens && r <= 64 && (r * esize) % 16 == 0 && d % 4 == 0 && (d * esize) % 16 == 0;
+}
+
 cudaError_t launch_lore(const LoreArgs& a, cudaStream_t st) {
     if (a.T == 0) return cudaSuccess;
+    if (a.v && lore_grouped_usable(a.T, a.d, a.r, a.bf16))
+        return a.bf16 ? launch_lore_grouped<__nv_bfloat16>(a, st) : launch_lore_grouped<float>(a, st);
     const int n_slots = a.T * a.k;
     const dim3 gz(n_slots);
     dim3 gb(a.T, (a.d + 255) / 256);

@@ -560,8 +560,14 @@ moe_status moe_lore(const moe_dims* dims, const void* x, const int32_t* final_id
     const WsLayout L = ws_layout(*dims);
     a.N = dims->N; a.bf16 = bf16(dims); a.y_lore = y_lore;
     a.z = ws_at<float>(ws, L.lore_z); a.err = ws_at<DevError>(ws, L.err);
+    // (the workspace holds the grouped path's buffers for these dimensions)
+    const bool grouped = lore_grouped_usable(dims->T, dims->d, dims->r, bf16(dims));
+    a.g_off = ws_at<int32_t>(ws, L.lore_off); a.g_list = ws_at<int32_t>(ws, L.lore_list);
+    a.g_pos = ws_at<int32_t>(ws, L.lore_pos); a.g_counts = ws_at<int32_t>(ws, L.lore_counts);
+    a.zp = ws_at<float>(ws, L.lore_zp);
+    a.v = grouped ? ws_at<float>(ws, L.lore_v) : nullptr;
     MOE_CUDA(launch_lore(a, S(stream)));
-    count(2);
+    count(grouped ? 5 : 2);
     return MOE_OK;
 }
 

@@ -18,13 +18,16 @@ namespace moe {
 //     within the chunk (per-warp ranks by __match_any_sync, then earlier warps)
 //     and scatters them; the order is stable in slot order, as in
 //     permute_block.  Block 0 writes expert_offsets and builds the FFN plan.
+// LORE = true groups the LoRE slots instead (moe_lore's grouped path; no plan).
+template <bool LORE>
 __device__ __forceinline__ int permute_key(const int32_t* __restrict__ final_idx,
                                            const int32_t* __restrict__ final_kind, int i, int n_slots, int N,
                                            DevError* __restrict__ err) {
     if (i >= n_slots) return -1;
     const int x = final_idx[i];
-    if (x >= N) { set_error(err, MOE_ERR_DEVICE_INDEX, i); return -1; }
-    return (x >= 0 && final_kind[i] != MOE_KIND_LORE) ? x : -1;
+    const bool lore = final_kind[i] == MOE_KIND_LORE;
+    if (x >= N && (!LORE || lore)) { if (err) set_error(err, MOE_ERR_DEVICE_INDEX, i); return -1; }
+    return (x >= 0 && x < N && lore == LORE) ? x : -1;
 }
 
 // per warp and expert: the warp's slot count; returns this slot's rank among
@@ -36,6 +39,7 @@ __device__ __forceinline__ int permute_warp_counts(int key, int (*cnt)[kMaxExper
     return __popc(peers & ((1u << lane) - 1u));
 }
 
+template <bool LORE>
 __global__ void __launch_bounds__(kPermChunk) permute_count_kernel(const int32_t* __restrict__ final_idx,
                                                                    const int32_t* __restrict__ final_kind,
                                                                    int n_slots, int N,
@@ -45,7 +49,7 @@ __global__ void __launch_bounds__(kPermChunk) permute_count_kernel(const int32_t
     const int tid = threadIdx.x, nw = blockDim.x >> 5;
     for (int i = tid; i < nw * kMaxExperts; i += blockDim.x) (&cnt[0][0])[i] = 0;
     __syncthreads();
-    const int key = permute_key(final_idx, final_kind, blockIdx.x * kPermChunk + tid, n_slots, N, err);
+    const int key = permute_key<LORE>(final_idx, final_kind, blockIdx.x * kPermChunk + tid, n_slots, N, err);
     (void)permute_warp_counts(key, cnt);
     __syncthreads();
     if (tid < N) {
@@ -56,6 +60,7 @@ __global__ void __launch_bounds__(kPermChunk) permute_count_kernel(const int32_t
     grid_dep_launch();
 }
 
+template <bool LORE>
 __global__ void __launch_bounds__(kPermChunk) permute_scatter_kernel(const int32_t* __restrict__ final_idx,
                                                                      const int32_t* __restrict__ final_kind,
                                                                      int n_slots, int N,
@@ -74,11 +79,7 @@ __global__ void __launch_bounds__(kPermChunk) permute_scatter_kernel(const int32
     // final_idx / final_kind come from the previous kernels (the count
     // kernel reported bad indices already)
     grid_dep_wait();
-    int key = -1;
-    if (slot < n_slots) {
-        const int x = final_idx[slot];
-        if (x >= 0 && x < N && final_kind[slot] != MOE_KIND_LORE) key = x;
-    }
+    const int key = permute_key<LORE>(final_idx, final_kind, slot, n_slots, N, nullptr);
     __syncthreads();
     const int rank = permute_warp_counts(key, cnt);
     // expert totals and this chunk's start per expert, from the count table
@@ -114,6 +115,7 @@ __global__ void __launch_bounds__(kPermChunk) permute_scatter_kernel(const int32
     }
     if (c == 0) {
         if (tid <= N) expert_offsets[tid] = s_off[tid];
+        if (LORE) return;
         // only the plan of the path moe_expert_ffn will take
         if (plan.tc_plan) {
             if (tid == 0) build_tc_plan(plan, s_off);
@@ -149,13 +151,26 @@ cudaError_t launch_permute(const PermuteArgs& a, const PlanArgs& plan, int32_t* 
         return cudaGetLastError();
     }
     const int n_chunks = (a.n_slots + kPermChunk - 1) / kPermChunk;
-    permute_count_kernel<<<n_chunks, kPermChunk, 0, st>>>(a.final_idx, a.final_kind, a.n_slots, a.N, counts,
-                                                          a.err);
+    permute_count_kernel<false><<<n_chunks, kPermChunk, 0, st>>>(a.final_idx, a.final_kind, a.n_slots, a.N,
+                                                                 counts, a.err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_pdl(permute_scatter_kernel, dim3(n_chunks), dim3(kPermChunk), 0, st, a.final_idx,
+    return launch_pdl(permute_scatter_kernel<false>, dim3(n_chunks), dim3(kPermChunk), 0, st, a.final_idx,
                       a.final_kind, a.n_slots, a.N, (const int32_t*)counts, a.expert_offsets, a.perm,
                       a.inv_perm, plan);
+}
+
+cudaError_t launch_group_lore(const PermuteArgs& a, int32_t* counts, cudaStream_t st) {
+    const int n_chunks = (a.n_slots + kPermChunk - 1) / kPermChunk;
+    permute_count_kernel<true><<<n_chunks, kPermChunk, 0, st>>>(a.final_idx, a.final_kind, a.n_slots, a.N,
+                                                                counts, a.err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    PlanArgs none;
+    none.tc_plan = nullptr;
+    return launch_pdl(permute_scatter_kernel<true>, dim3(n_chunks), dim3(kPermChunk), 0, st, a.final_idx,
+                      a.final_kind, a.n_slots, a.N, (const int32_t*)counts, a.expert_offsets, a.perm,
+                      a.inv_perm, none);
 }
 
 cudaError_t launch_plan_gemv(const PlanArgs& a, cudaStream_t st) {

@@ -50,7 +50,7 @@ def _run(name, T, batch=0, **kw):
     return cfg, W, layer, x, bufs, st, det
 
 
-@pytest.mark.parametrize("name,T", [("tiny", 16), ("tiny", 1), ("tiny", 5), ("tiny", 64),
+@pytest.mark.parametrize("name,T", [("tiny", 16), ("tiny", 1), ("tiny", 5), ("tiny", 64), ("tiny", 100),
                                     ("dsv2lite", 1), ("dsv2lite", 8), ("dsv2lite", 3),
                                     ("granite", 1), ("granite", 37), ("granite", 1024),
                                     ("granite", 65), ("granite", 200), ("dsv2lite", 96),
