@@ -253,7 +253,7 @@ constexpr int kTcdMaxCtas = 160;  // grid of that path: min(SMs, kTcdMaxCtas)
 
 // ---------------------------------------------------------------- workspace
 struct WsLayout {
-    size_t err, ticket, logits_r, logits_p, score, qp, plan_hdr, segs, seg_first, perm_counts, lore_z,
+    size_t err, ticket, logits_r, logits_p, score, route_part, qp, plan_hdr, segs, seg_first, perm_counts, lore_z,
         lore_off, lore_list, lore_pos, lore_counts, lore_zp, lore_v, tc_plan,
         x_perm, h_routed, h_shared, floe_u, floe_kept, floe_list, floe_count, partial, total;
     int max_segs, max_partial_rows;
@@ -300,6 +300,9 @@ __host__ __device__ inline WsLayout ws_layout(const moe_dims& D) {
     L.logits_r = take(T * N * 4);
     L.logits_p = take(T * N * 4);
     L.score = take(T * 4);
+    // split-d partial logits of the tensor-core router (bf16 batches of more
+    // than kTcMinTokens tokens): up to 8 splits x T x 2N fp32
+    L.route_part = take(D.wtype == MOE_DTYPE_BF16 && D.T > kTcMinTokens ? 8 * T * 2 * N * 4 : 0);
     L.qp = take(T * N * 4);
     L.plan_hdr = take(sizeof(PlanHeader));
     L.segs = take((size_t)L.max_segs * sizeof(Seg));

@@ -18,8 +18,17 @@ struct LogitsArgs {
     int T, d, N, has_prefetch;
     bool bf16;
     float *logits_r, *logits_p, *score;
+    // tensor-core path (batches of more than kTcMinTokens bf16 tokens): the
+    // split-d partial logits (workspace), SM count, device error word
+    float* part;
+    int sms;
+    DevError* err;
 };
 cudaError_t launch_logits(const LogitsArgs& a, cudaStream_t st);
+// router + prefetch-router logits as one tensor-core GEMM (route_tc.cu)
+bool route_tc_usable(int T, int d, int N, bool bf16, bool has_prefetch, bool sep_pre);
+size_t route_tc_part_bytes(int T, int N);
+cudaError_t launch_route_tc(const LogitsArgs& a, float* part, cudaStream_t st);
 
 struct RouteSelectArgs {
     const float *logits_r, *logits_p, *score, *theta;

@@ -178,6 +178,7 @@ moe_status prep_route(const moe_dims* dims, const void* x, const void* w_router,
     la.has_prefetch = has_pref; la.bf16 = bf16(dims);
     la.logits_r = ws_at<float>(ws, L.logits_r); la.logits_p = ws_at<float>(ws, L.logits_p);
     la.score = ws_at<float>(ws, L.score);
+    la.part = ws_at<float>(ws, L.route_part); la.sms = sm_count(); la.err = ws_at<DevError>(ws, L.err);
     ra.logits_r = la.logits_r; ra.logits_p = la.logits_p; ra.score = la.score; ra.theta = theta;
     ra.logit_tau = has_pref ? (float)std::log((double)tau / (1.0 - (double)tau)) : 0.f;
     ra.T = dims->T; ra.N = dims->N; ra.k = dims->k; ra.delta_max = dims->delta_max;

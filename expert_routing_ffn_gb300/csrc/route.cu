@@ -689,6 +689,14 @@ cudaError_t launch_route_front(const FrontArgs& a, cudaStream_t st) {
 template <typename W>
 static cudaError_t launch_logits_t(const LogitsArgs& a, cudaStream_t st) {
     constexpr int TT = 8;
+    const bool sep_pre = a.x_pre != nullptr && a.x_pre != a.x;
+    if (a.part && route_tc_usable(a.T, a.d, a.N, a.bf16, a.has_prefetch, sep_pre)) {
+        cudaError_t e = launch_route_tc(a, a.part, st);
+        if (e != cudaSuccess || !a.has_prefetch) return e;
+        route_score_kernel<W><<<(a.T + 7) / 8, 256, 0, st>>>((const W*)(a.x_pre ? a.x_pre : a.x), a.w_ord, a.T,
+                                                             a.d, a.score);
+        return cudaGetLastError();
+    }
     // (a row quad must not straddle the router / prefetch-router boundary when
     // the two routers read different inputs)
     if (a.T >= 2048 && (a.x_pre == nullptr || a.x_pre == a.x || a.N % 4 == 0)) {
