@@ -567,7 +567,7 @@ __global__ void __launch_bounds__(256) select_resident_kernel(
 // runs selection, resident set and miss handling on shared copies, writes the
 // outputs out with coalesced stores and permutes from the shared copies.
 struct FrontSmem {  // byte offsets into the dynamic shared memory
-    int lr, lp, sc, prob, qp, tki, tkg, dh, pm, ds, fi, fg, fk, bres, total;
+    int lr, lp, sc, prob, qp, tki, tkg, dh, pm, ds, fi, fg, fk, bres, th, total;
 };
 
 __host__ __device__ inline FrontSmem front_smem(int T, int N, int k) {
@@ -577,7 +577,7 @@ __host__ __device__ inline FrontSmem front_smem(int T, int N, int k) {
     f.lr = take(T * N * 4); f.lp = take(T * N * 4); f.sc = take(T * 4); f.prob = take(T * N * 4);
     f.qp = take(T * N * 4); f.tki = take(T * k * 4); f.tkg = take(T * k * 4); f.dh = take(T * 4);
     f.pm = take(T * 8); f.ds = take(T * 4); f.fi = take(T * k * 4); f.fg = take(T * k * 4);
-    f.fk = take(T * k * 4); f.bres = take(8);
+    f.fk = take(T * k * 4); f.bres = take(8); f.th = take(kMaxExperts * 4);  // theta (delta_max + 1 <= N)
     f.total = o;
     return f;
 }
@@ -619,16 +619,19 @@ __global__ void __launch_bounds__(256) route_front_kernel(const __grid_constant_
     float* fg = reinterpret_cast<float*>(smem_raw + F.fg);
     int32_t* fk = reinterpret_cast<int32_t*>(smem_raw + F.fk);
     uint64_t* bres = reinterpret_cast<uint64_t*>(smem_raw + F.bres);
+    float* th = reinterpret_cast<float*>(smem_raw + F.th);
     // the other blocks' logits, once (past L1)
     for (int i = tid; i < T * N; i += blockDim.x) {
         lr[i] = __ldcg(ra.logits_r + i);
         if (ra.has_prefetch) lp[i] = __ldcg(ra.logits_p + i);
     }
-    if (ra.has_prefetch)
+    if (ra.has_prefetch) {
         for (int i = tid; i < T; i += blockDim.x) sc[i] = __ldcg(ra.score + i);
+        for (int i = tid; i <= ra.delta_max; i += blockDim.x) th[i] = ra.theta[i];  // with the logits, not later
+    }
     __syncthreads();
     for (int t = warp; t < T; t += nw)
-        route_select_token(t, lr, lp, sc, ra.theta, ra.logit_tau, N, k, ra.delta_max, ra.has_prefetch, tki, tkg,
+        route_select_token(t, lr, lp, sc, th, ra.logit_tau, N, k, ra.delta_max, ra.has_prefetch, tki, tkg,
                            prob, dh, pm, ra.delta_star ? ds : nullptr, ra.qp ? qp : nullptr);
     __syncthreads();
     for (int i = tid; i < T * N; i += blockDim.x) ra.router_prob[i] = prob[i];
