@@ -253,7 +253,7 @@ constexpr int kTcdMaxCtas = 160;  // grid of that path: min(SMs, kTcdMaxCtas)
 
 // ---------------------------------------------------------------- workspace
 struct WsLayout {
-    size_t err, ticket, logits_r, logits_p, score, route_part, qp, plan_hdr, segs, seg_first, perm_counts, lore_z,
+    size_t err, ticket, logits_r, logits_p, score, route_part, qp, res_part, plan_hdr, segs, seg_first, perm_counts, lore_z,
         lore_off, lore_list, lore_pos, lore_counts, lore_zp, lore_v, tc_plan,
         x_perm, h_routed, h_shared, floe_u, floe_kept, floe_list, floe_count, partial, total;
     int max_segs, max_partial_rows;
@@ -304,6 +304,7 @@ __host__ __device__ inline WsLayout ws_layout(const moe_dims& D) {
     // than kTcMinTokens tokens): up to 8 splits x T x 2N fp32
     L.route_part = take(D.wtype == MOE_DTYPE_BF16 && D.T > kTcMinTokens ? 8 * T * 2 * N * 4 : 0);
     L.qp = take(T * N * 4);
+    L.res_part = take(32 * kMaxExperts * 4);  // partial sums of the batch resident set
     L.plan_hdr = take(sizeof(PlanHeader));
     L.segs = take((size_t)L.max_segs * sizeof(Seg));
     L.seg_first = take((N + (size_t)D.n_shared + 1) * 4);

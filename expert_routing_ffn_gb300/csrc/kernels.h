@@ -38,7 +38,8 @@ struct RouteSelectArgs {
     uint64_t* prefetch_mask; int32_t* delta_star; float* qp;
 };
 cudaError_t launch_route_select(const RouteSelectArgs& a, cudaStream_t st);
-cudaError_t launch_batch_resident(const float* qp, int T, int N, int n_res, uint64_t* out,
+// part: workspace of 32 x kMaxExperts floats (large batches)
+cudaError_t launch_batch_resident(const float* qp, int T, int N, int n_res, uint64_t* out, float* part,
                                   cudaStream_t st);
 
 struct SelectArgs {

@@ -316,7 +316,8 @@ moe_status moe_route(const moe_dims* dims, const void* x, const void* w_router,
     MOE_CUDA(launch_route_select(ra, S(stream)));
     count();
     if (n_resident > 0) {
-        MOE_CUDA(launch_batch_resident(ra.qp, dims->T, dims->N, n_resident, batch_resident, S(stream)));
+        MOE_CUDA(launch_batch_resident(ra.qp, dims->T, dims->N, n_resident, batch_resident,
+                                       ws_at<float>(ws, ws_layout(*dims).res_part), S(stream)));
         count();
     }
     return MOE_OK;

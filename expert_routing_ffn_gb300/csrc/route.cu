@@ -440,6 +440,52 @@ __global__ void __launch_bounds__(1024) batch_resident_kernel(const float* __res
     batch_resident_block(qp, T, N, n_res, out);
 }
 
+// Large batches: kResParts blocks each sum a contiguous range of tokens per
+// expert (thread = expert x token quarter, the quarters then added in order),
+// and one block adds the partial sums in block order and ranks the experts.
+constexpr int kResParts = 32;
+__global__ void __launch_bounds__(256) batch_resident_part_kernel(const float* __restrict__ qp, int T, int N,
+                                                                  float* __restrict__ part) {
+    __shared__ float q4[4][kMaxExperts];
+    const int e = threadIdx.x & 63, quarter = threadIdx.x >> 6;
+    const int t0 = (int)((long long)blockIdx.x * T / kResParts), t1 = (int)((long long)(blockIdx.x + 1) * T / kResParts);
+    const int n = t1 - t0, q0 = t0 + quarter * n / 4, q1 = t0 + (quarter + 1) * n / 4;
+    float acc = 0.f;
+    if (e < N) {
+        int t = q0;
+        for (; t + 8 <= q1; t += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = qp[(size_t)(t + u) * N + e];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) acc += v[u];
+        }
+        for (; t < q1; ++t) acc += qp[(size_t)t * N + e];
+    }
+    q4[quarter][e] = acc;
+    __syncthreads();
+    if (threadIdx.x < kMaxExperts)
+        part[blockIdx.x * kMaxExperts + e] = q4[0][e] + q4[1][e] + q4[2][e] + q4[3][e];
+}
+
+__global__ void __launch_bounds__(64) batch_resident_final_kernel(const float* __restrict__ part, int N, int n_res,
+                                                                  uint64_t* __restrict__ out) {
+    __shared__ float tot[kMaxExperts];
+    __shared__ uint32_t bits[2];
+    const int me = threadIdx.x;
+    float s = 0.f;
+    for (int b = 0; b < kResParts; ++b) s += part[b * kMaxExperts + me];
+    tot[me] = s;
+    __syncthreads();
+    int rank = 0;
+    if (me < N)
+        for (int j = 0; j < N; ++j) rank += (tot[j] > tot[me] || (tot[j] == tot[me] && j < me)) ? 1 : 0;
+    const uint32_t b = __ballot_sync(0xffffffffu, me < N && rank < n_res);
+    if ((me & 31) == 0) bits[me >> 5] = b;
+    __syncthreads();
+    if (me == 0) *out = (uint64_t)bits[0] | ((uint64_t)bits[1] << 32);
+}
+
 // ---------------------------------------------------------------------------
 // Miss handling, one warp per token (APEX §4.3 Algorithm 1; SPICE LoRE).
 __device__ __forceinline__ void select_token(
@@ -554,10 +600,25 @@ __global__ void __launch_bounds__(256) select_resident_kernel(
     int N, int k, int renorm, int32_t* __restrict__ final_idx, float* __restrict__ final_gate,
     int32_t* __restrict__ final_kind, uint64_t* __restrict__ fetch_mask,
     int32_t* __restrict__ counters, DevError* __restrict__ err) {
+    // the block's counters and fetch mask gathered in shared memory, then one
+    // global atomic each (every token adding to the same global counters
+    // serialised on them)
+    __shared__ int32_t s_cnt[MOE_NUM_COUNTERS];
+    __shared__ unsigned long long s_fetch;
+    if (threadIdx.x < MOE_NUM_COUNTERS) s_cnt[threadIdx.x] = 0;
+    if (threadIdx.x == 0) s_fetch = 0ull;
+    __syncthreads();
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (warp >= T) return;
-    select_token(warp, router_prob, topk_idx, prefetch_mask, resident, policy, gamma, delta_hat, delta_star, N,
-                 k, renorm, final_idx, final_gate, final_kind, fetch_mask, counters, err);
+    if (warp < T)
+        select_token(warp, router_prob, topk_idx, prefetch_mask, resident, policy, gamma, delta_hat, delta_star,
+                     N, k, renorm, final_idx, final_gate, final_kind,
+                     fetch_mask ? reinterpret_cast<uint64_t*>(&s_fetch) : nullptr, counters ? s_cnt : nullptr,
+                     err);
+    __syncthreads();
+    if (counters && threadIdx.x < MOE_NUM_COUNTERS && s_cnt[threadIdx.x])
+        atomicAdd(&counters[threadIdx.x], s_cnt[threadIdx.x]);
+    if (fetch_mask && threadIdx.x == 0 && s_fetch)
+        atomicOr(reinterpret_cast<unsigned long long*>(fetch_mask), s_fetch);
 }
 
 // ---------------------------------------------------------------------------
@@ -745,9 +806,14 @@ cudaError_t launch_route_select(const RouteSelectArgs& a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_batch_resident(const float* qp, int T, int N, int n_res, uint64_t* out,
+cudaError_t launch_batch_resident(const float* qp, int T, int N, int n_res, uint64_t* out, float* part,
                                   cudaStream_t st) {
-    batch_resident_kernel<<<1, 1024, 0, st>>>(qp, T, N, n_res, out);
+    if (T >= 8 * kResParts && part) {
+        batch_resident_part_kernel<<<kResParts, 256, 0, st>>>(qp, T, N, part);
+        batch_resident_final_kernel<<<1, 64, 0, st>>>(part, N, n_res, out);
+    } else {
+        batch_resident_kernel<<<1, 1024, 0, st>>>(qp, T, N, n_res, out);
+    }
     return cudaGetLastError();
 }
 
