@@ -84,15 +84,32 @@ __global__ void __launch_bounds__(1024) floe_select_kernel(const float* __restri
             if (act && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
         }
         __syncthreads();
-        if (tid == 0) {
-            int cum = 0, rem = s_remaining;
-            for (int bin = 255; bin >= 0; --bin) {
-                if (cum + hist[bin] >= rem) {
-                    s_prefix = prefix | ((uint32_t)bin << shift);
-                    s_remaining = rem - cum;
-                    break;
+        if (warp == 0) {
+            // the first bin, in descending order, at which the running count
+            // reaches the number still to keep: lane L holds bins 255 - 8L ..
+            // 248 - 8L, an exclusive scan over lanes, and the one lane whose
+            // span holds the crossing walks its eight bins
+            int v[8], sum = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) { v[j] = hist[255 - (8 * lane + j)]; sum += v[j]; }
+            int incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += t;
+            }
+            const int rem = s_remaining;
+            int cum = incl - sum;
+            if (cum < rem && rem <= incl) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (cum + v[j] >= rem) {
+                        s_prefix = prefix | ((uint32_t)(255 - (8 * lane + j)) << shift);
+                        s_remaining = rem - cum;
+                        break;
+                    }
+                    cum += v[j];
                 }
-                cum += hist[bin];
             }
         }
         mask |= 255u << shift;
