@@ -94,6 +94,9 @@ def lib():
             L.orc_lore.argtypes = [C.c_int, C.c_int, _FP, _FP, _FP, _DP]
             L.orc_batch_resident.argtypes = [C.c_int, C.c_int, _DP, C.c_int, _DP]
             L.orc_batch_resident.restype = C.c_uint64
+            L.orc_cache_update.argtypes = [C.c_int, C.c_int, _IP, C.c_double, C.c_int, _DP, C.c_uint64,
+                                           C.POINTER(C.c_int), _DP]
+            L.orc_cache_update.restype = C.c_uint64
             L.orc_layer_forward.argtypes = [C.POINTER(_Cfg), C.POINTER(_Inputs), C.POINTER(_Outputs)]
             _lib = L
     return _lib
@@ -204,6 +207,17 @@ def batch_resident(lp, n_res):
     gap = C.c_double()
     m = lib().orc_batch_resident(T, N, _d(lp), n_res, C.byref(gap))
     return int(m), gap.value
+
+
+def cache_update(routed, heat, decay, capacity, old_cache):
+    """One decode step of the persistent expert cache (ELMoE-3D heat map with
+    decay): returns (new cache mask, updated heat [float64], hits, boundary gap)."""
+    routed = np.ascontiguousarray(np.asarray(routed).ravel(), np.int32)
+    heat = np.array(heat, np.float64, copy=True)
+    hits, gap = C.c_int(), C.c_double()
+    m = lib().orc_cache_update(len(heat), len(routed), routed.ctypes.data_as(_IP), float(decay), int(capacity),
+                               _d(heat), C.c_uint64(old_cache), C.byref(hits), C.byref(gap))
+    return int(m), heat, hits.value, gap.value
 
 
 # ---- whole layer ---------------------------------------------------------

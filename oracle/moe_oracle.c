@@ -23,6 +23,10 @@
  *     surrogate" (y_e ~ y_shared + B_e A_e h).
  *   - shared experts, combine         : SPICE write-up, LoRE section (the
  *     always-active shared expert) and the gate-weighted MoE sum.
+ *   - persistent expert cache         : ELMoE-3D (CSDN post), expert-axis
+ *     elasticity: heat statistics, top-K subset, dynamic update, and the
+ *     practice note on heat decay (multiply every heat by a factor just
+ *     below 1 each step).
  *
  * Inputs are float32 arrays whose values are the layer's exact parameters
  * (bf16-representable for bf16 layers); each element is converted to double
@@ -271,6 +275,37 @@ uint64_t orc_batch_resident(int T, int N, const double* lp, int n_res, double* g
     if (gap) *gap = (n_res < N) ? sum[idx[n_res - 1]] - sum[idx[n_res]] : INFINITY;
     free(sum); free(q); free(idx);
     return mask;
+}
+
+/* Persistent expert cache, one decode step (ELMoE-3D, expert-axis
+ * elasticity: "heat" statistics of the experts the routing function selects,
+ * the most frequently activated top-K kept, updated as the activation pattern
+ * changes; heat decay per time step from the practice note).
+ *   routed[n_slots]: the experts the router selected this step (-1: none).
+ *   heat[N] (in/out): heat_e <- decay * heat_e + #{slots routed to e}.
+ *   Returns the new cache: the C experts of largest heat, lowest index on
+ *   ties (all N if C >= N).  *gap = heat of the C-th minus the (C+1)-th.
+ *   *hits = routed slots whose expert is in old_cache (the cache the step
+ *   ran with). */
+uint64_t orc_cache_update(int N, int n_slots, const int* routed, double decay, int C, double* heat,
+                          uint64_t old_cache, int* hits, double* gap) {
+    int h = 0;
+    int* count = (int*)calloc((size_t)N, sizeof(int));
+    for (int i = 0; i < n_slots; ++i) {
+        const int e = routed[i];
+        if (e < 0 || e >= N) continue;
+        count[e] += 1;
+        if ((old_cache >> e) & 1) h += 1;
+    }
+    for (int e = 0; e < N; ++e) heat[e] = decay * heat[e] + (double)count[e];
+    int* idx = (int*)malloc(sizeof(int) * (size_t)N);
+    orc_topk(N, N, heat, idx);
+    uint64_t cache = 0;
+    for (int i = 0; i < C && i < N; ++i) cache |= (uint64_t)1 << idx[i];
+    if (gap) *gap = (C > 0 && C < N) ? heat[idx[C - 1]] - heat[idx[C]] : INFINITY;
+    if (hits) *hits = h;
+    free(count); free(idx);
+    return cache;
 }
 
 typedef struct {

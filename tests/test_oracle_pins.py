@@ -431,3 +431,58 @@ def test_capacity_shortfall_flagged():
     cfg, W, x = _small(policy=1, use_prefetch_mask=False)
     R = oracle.layer_forward(cfg, W, x, resident=0b1)  # one expert available, k = 2
     assert (R.status == 1).all()
+
+
+# ---- persistent expert cache (ELMoE-3D heat map with decay) ----------------
+
+def test_cache_heat_closed_form_and_extremes():
+    """The same routed slots every step: heat is the geometric series
+    count * (1 - decay^S) / (1 - decay); decay 1 is plain counting, decay 0
+    keeps this step's counts only."""
+    rng = np.random.default_rng(7)
+    N, C, S = 12, 4, 9
+    routed = rng.integers(0, N, size=10)
+    counts = np.bincount(routed, minlength=N).astype(np.float64)
+    for decay in (0.0, 0.5, 0.99, 1.0):
+        heat, cache = np.zeros(N), 0
+        for _ in range(S):
+            cache, heat, _, _ = oracle.cache_update(routed, heat, decay, C, cache)
+        series = S if decay == 1.0 else (1.0 - decay ** S) / (1.0 - decay)
+        np.testing.assert_allclose(heat, counts * series, rtol=1e-12, atol=0)
+
+
+def test_cache_is_top_c_by_heat_with_low_index_ties():
+    """Brute force over random histories: every cached expert has at least
+    the heat of every other, equal heat goes to the lower index, the cache
+    has exactly min(C, N) members and hits count routed slots in the old
+    cache."""
+    rng = np.random.default_rng(11)
+    for trial in range(200):
+        N = int(rng.integers(2, 16))
+        C = int(rng.integers(1, N + 2))
+        heat = rng.integers(0, 4, size=N).astype(np.float64)  # integers: many ties
+        old = int(rng.integers(0, 1 << N))
+        routed = rng.integers(-1, N, size=int(rng.integers(0, 12)))
+        cache, new_heat, hits, gap = oracle.cache_update(routed, heat, 0.5, C, old)
+        expect = 0.5 * heat + np.bincount(routed[routed >= 0], minlength=N)
+        np.testing.assert_array_equal(new_heat, expect)
+        members = [e for e in range(N) if (cache >> e) & 1]
+        assert len(members) == min(C, N)
+        for e in members:
+            for o in range(N):
+                if (cache >> o) & 1:
+                    continue
+                assert expect[e] > expect[o] or (expect[e] == expect[o] and e < o)
+        assert hits == sum(1 for e in routed if e >= 0 and (old >> int(e)) & 1)
+        if C < N:
+            order = sorted(range(N), key=lambda e: (-expect[e], e))
+            assert gap == expect[order[C - 1]] - expect[order[C]]
+
+
+def test_cache_hand_worked_step():
+    """Routed {0, 1, 1, 3} from zero heat, C = 2: heat (1, 2, 0, 1, 0); the
+    tie between experts 0 and 3 goes to 0."""
+    cache, heat, hits, gap = oracle.cache_update([0, 1, 1, 3], np.zeros(5), 0.9, 2, 0b01000)
+    assert cache == 0b00011
+    np.testing.assert_array_equal(heat, [1, 2, 0, 1, 0])
+    assert hits == 1 and gap == 0.0
