@@ -95,6 +95,7 @@ _PROTOS = {
     "moe_expert_ffn_noalloc": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P], C.c_int),
     "moe_lore": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P], C.c_int),
     "moe_combine": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P], C.c_int),
+    "moe_cache_update": ([_DIMS, _P, C.c_float, C.c_int, _P, _P, _P, _P, _P], C.c_int),
     "moe_layer_forward": ([_DIMS, C.POINTER(moe_layer_args), C.POINTER(moe_layer_outputs), _P, _SZ,
                            _P], C.c_int),
     "moe_check": ([_P, _P, C.POINTER(C.c_int), C.POINTER(C.c_int32)], C.c_int),
@@ -334,6 +335,16 @@ def moe_combine(dims, y_perm, inv_perm, final_gate, final_kind, y_shared, y_lore
         _ptr(y_shared, torch.float32, T * d, "y_shared", True),
         _ptr(y_lore, torch.float32, T * d, "y_lore", True), _ptr(out, torch.float32, T * d, "out"),
         _stream(stream)), "moe_combine")
+
+
+def moe_cache_update(dims, topk_idx, decay, capacity, heat, cache_mask, admit_mask=None, stats=None,
+                     stream=None):
+    T, N, k = dims.T, dims.N, dims.k
+    _check(lib().moe_cache_update(
+        C.byref(dims), _ptr(topk_idx, torch.int32, T * k, "topk_idx"), float(decay), int(capacity),
+        _ptr(heat, torch.float32, N, "heat"), _ptr(cache_mask, torch.int64, 1, "cache_mask"),
+        _ptr(admit_mask, torch.int64, 1, "admit_mask", True), _ptr(stats, torch.int32, 4, "stats", True),
+        _stream(stream)), "moe_cache_update")
 
 
 def moe_layer_forward(dims, args: moe_layer_args, outs: moe_layer_outputs, ws, stream=None):

@@ -193,6 +193,10 @@ cudaError_t launch_layer_epilogue(const EpilogueArgs& a, cudaStream_t st);
 // MOE_ERR_TIMEOUT in err)
 cudaError_t launch_wait_timeout_probe(DevError* err, cudaStream_t st);
 
+// persistent expert cache, one decode step (cache.cu)
+cudaError_t launch_cache_update(const int32_t* topk_idx, int n_slots, int N, float decay, int capacity, float* heat,
+                                uint64_t* cache, uint64_t* admit, int32_t* stats, cudaStream_t st);
+
 struct CombineArgs {
     const float* y_perm; const int32_t* inv_perm; const float* final_gate;
     const int32_t* final_kind; const float *y_shared, *y_lore; int T, d, k; float* out;

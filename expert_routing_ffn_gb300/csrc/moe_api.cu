@@ -573,6 +573,18 @@ moe_status moe_lore(const moe_dims* dims, const void* x, const int32_t* final_id
     return MOE_OK;
 }
 
+moe_status moe_cache_update(const moe_dims* dims, const int32_t* topk_idx, float decay, int capacity,
+                            float* heat, uint64_t* cache_mask, uint64_t* admit_mask, int32_t* stats,
+                            void* stream) {
+    MOE_TRY(check_dims(dims));
+    if (!topk_idx || !heat || !cache_mask) return MOE_ERR_INVALID_ARG;
+    if (!(decay >= 0.f && decay <= 1.f) || capacity < 0) return MOE_ERR_INVALID_ARG;
+    MOE_CUDA(launch_cache_update(topk_idx, dims->T * dims->k, dims->N, decay, capacity, heat, cache_mask, admit_mask,
+                                 stats, S(stream)));
+    count();
+    return MOE_OK;
+}
+
 moe_status moe_combine(const moe_dims* dims, const float* y_perm, const int32_t* inv_perm,
                        const float* final_gate, const int32_t* final_kind, const float* y_shared,
                        const float* y_lore, float* out, void* stream) {

@@ -284,6 +284,29 @@ moe_status moe_lore(const moe_dims* dims, const void* x, const int32_t* final_id
                     const int32_t* final_kind, const float* final_gate, const void* lore_a,
                     const void* lore_b, float* y_lore, void* ws, size_t ws_bytes, void* stream);
 
+/* Persistent expert cache across decode steps (beyond the single layer
+ * forward; ELMoE-3D, expert-axis elasticity: heat statistics of the experts
+ * the routing function selects, the most frequently activated top-K kept
+ * resident and refreshed as the pattern drifts, heat decaying by a factor
+ * just below 1 each step).  One step, after the layer ran with its resident
+ * mask = *cache_mask (moe_layer_args.resident, n_resident = 0):
+ *   heat[e]     <- decay * heat[e] + #{slots of topk_idx routed to e}
+ *                  (float32, a rounded product then a rounded sum)
+ *   *cache_mask <- the `capacity` experts of largest heat, lowest index on
+ *                  ties (every expert if capacity >= N)
+ *   *admit_mask <- new cache & ~old cache: the experts to stage in before the
+ *                  next step (may be NULL)
+ *   stats[0..3] += routed slots whose expert was in the old cache (hits),
+ *                  routed slots, experts admitted, experts evicted (stats may
+ *                  be NULL; the caller zeroes it).
+ * topk_idx [T, k] int32 (moe_route's routed experts, before miss handling);
+ * heat [N] float32, cache_mask / admit_mask uint64, stats int32[4]: device
+ * pointers.  Errors: INVALID_ARG (NULL topk_idx / heat / cache_mask, decay
+ * outside [0, 1], capacity < 0), UNSUPPORTED (N > 64).  Asynchronous. */
+moe_status moe_cache_update(const moe_dims* dims, const int32_t* topk_idx, float decay, int capacity,
+                            float* heat, uint64_t* cache_mask, uint64_t* admit_mask, int32_t* stats,
+                            void* stream);
+
 /* Stage 5 — combine:
  *   out[t] = y_shared[t] * (1 + sum of LoRE-slot gates)
  *          + sum over COMPUTE/FETCH slots of final_gate * y_perm[inv_perm[t,s]]

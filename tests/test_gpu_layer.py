@@ -312,6 +312,63 @@ def test_floe_sparse_matches_oracle(T):
     assert n_checked > 0
 
 
+def test_expert_cache_over_decode_steps_matches_oracle():
+    """Persistent expert cache (ELMoE-3D heat map with decay) over 48
+    one-token decode steps of the DS-V2-Lite-shaped layer: each step runs the
+    layer with resident = the cache, then moe_cache_update.  Every step is
+    checked against the oracle's update from the same routed experts and the
+    same incoming heat: heat within float32 rounding, the new cache bit-exact
+    unless the oracle's heat gap at the capacity boundary is a near-tie, and
+    the hit / slot / admit / evict counters exactly.  The layer's routing is
+    checked against the oracle on every step too."""
+    name, S, C, decay = "dsv2lite", 48, 24, 0.99
+    cfg, W = _host(name)
+    layer = _device(name, 1)
+    bufs = LayerBuffers(layer, 1)
+    dev = layer.ws.device
+    heat = torch.zeros(cfg.N, dtype=torch.float32, device=dev)
+    admit = torch.zeros(1, dtype=torch.int64, device=dev)
+    stats = torch.zeros(4, dtype=torch.int32, device=dev)
+    cache0 = (1 << C) - 1  # a predefined initial subset: experts 0 .. C-1
+    layer.set_resident(cache0)
+    h = np.zeros(cfg.N)
+    cache = cache0
+    want = np.zeros(4, np.int64)
+    near = 0
+    try:
+        for s in range(S):
+            x = make_tokens(cfg, T=1, batch=100 + s)
+            forward(layer, bufs, x_device(x, layer.dt), n_resident=0)
+            R = oracle.layer_forward(cfg, W, x, resident=cache, route_only=True)
+            check_routing(cfg, R, bufs)
+            check_selection(cfg, R, bufs)
+            heat_in = heat.double().cpu().numpy()
+            moe.moe_cache_update(layer.dims.with_T(1), bufs.topk_idx, decay, C, heat, layer.resident, admit, stats)
+            torch.cuda.synchronize()
+            routed = to_np(bufs.topk_idx).ravel()
+            new, h, hits, gap = oracle.cache_update(routed, heat_in, decay, C, cache)
+            np.testing.assert_allclose(heat.double().cpu().numpy(), h, rtol=2e-6, atol=1e-6)
+            got = as_u64(to_np(layer.resident)[0])
+            if gap >= 1e-5 * (1.0 + float(np.max(h))):
+                assert got == new, (s, hex(got), hex(new))
+            else:
+                near += 1
+            want += [hits, len(routed), bin(got & ~cache).count("1"), bin(cache & ~got).count("1")]
+            assert as_u64(to_np(admit)[0]) == got & ~cache
+            cache = got
+        assert st_ok(layer)
+        np.testing.assert_array_equal(to_np(stats).astype(np.int64), want)
+        assert near < S // 4
+        assert want[2] > 0  # the heat map moved experts in over these steps
+    finally:
+        layer.set_resident((1 << 64) - 1)
+
+
+def st_ok(layer):
+    st, _ = moe.moe_check(layer.ws)
+    return st == moe.MOE_OK
+
+
 def test_bounded_wait_times_out_and_the_context_stays_usable():
     """A device wait that can never finish (an mbarrier nothing arrives on)
     ends after its wall-clock bound with MOE_ERR_TIMEOUT in the error word, not
