@@ -11,6 +11,11 @@ experts resident by the batch prefetch set, HYBRID miss policy) decoding
 several copies of the layer's weights at distinct addresses, so the expert
 bytes one step reads are evicted from L2 (129 MB) before they are read again.
 
+Other workloads (--workload): the Granite, Mixtral (dense and FloE 10 %) and
+Qwen2-57B shapes, and dsv2lite-cache-decode-T1: one-token decode steps over a
+persistent expert cache (capacity 24, heat decay 0.99) that moe_cache_update
+refreshes every step; its line adds the cache's hit rate and admitted experts.
+
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
         [--workload NAME]
 Multi-GPU (torchrun): each rank runs an independent replica on its own
@@ -48,7 +53,13 @@ WORKLOADS = {
     "mixtral-floe10-decode-T1": ("mixtral", 1, "decode", 0.1),
     "mixtral-floe10-decode-T8": ("mixtral", 8, "decode", 0.1),
     "qwen2-prefill-T4096": ("qwen2", 4096, "prefill"),
+    "dsv2lite-cache-decode-T1": ("dsv2lite", 1, "decode"),
 }
+# Multi-step decode with a persistent expert cache (ELMoE-3D heat map with
+# decay): the layer runs every step with resident = the cache, which
+# moe_cache_update then refreshes from the step's routed experts.
+# name -> (cache capacity, heat decay, distinct one-token steps replayed)
+CACHE_WORKLOADS = {"dsv2lite-cache-decode-T1": (24, 0.99, 64)}
 DEFAULT_WORKLOAD = "dsv2lite-decode-T8"
 METRIC = "MoE-layer tokens/sec (decode & prefill) and % of HBM/tensor roofline, 1xGB300"
 FALLBACK_HBM_GBS = 6800.0
@@ -288,12 +299,28 @@ def main():
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.set_stream(stream)
     bufs = [LayerBuffers(L, T) for L in layers]
+    cache_cfg = CACHE_WORKLOADS.get(wl_name)
+    n_x = cache_cfg[2] if cache_cfg else n_copies  # distinct token batches replayed
     xs = [torch.from_numpy(make_tokens(cfg, T=T, batch=replica_batch(rank, i))).to(dev).to(base.dt).contiguous()
-          for i in range(n_copies)]
+          for i in range(n_x)]
+    if cache_cfg:
+        # one cache for the layer: every weight copy reads the same resident mask
+        capacity, decay = cache_cfg[0], cache_cfg[1]
+        cache_t = torch.full((1,), (1 << capacity) - 1, dtype=torch.int64, device=dev)  # predefined start set
+        heat_t = torch.zeros(cfg.N, dtype=torch.float32, device=dev)
+        admit_t = torch.zeros(1, dtype=torch.int64, device=dev)
+        cstats_t = torch.zeros(4, dtype=torch.int32, device=dev)
+        for L in layers:
+            L.resident = cache_t
 
     def step(i):
         c = i % n_copies
-        forward(layers[c], bufs[c], xs[c], stream=stream)
+        if cache_cfg:
+            forward(layers[c], bufs[c], xs[i % n_x], stream=stream, n_resident=0)
+            moe.moe_cache_update(layers[c].dims.with_T(T), bufs[c].topk_idx, decay, capacity, heat_t, cache_t,
+                                 admit_t, cstats_t, stream)
+        else:
+            forward(layers[c], bufs[c], xs[c], stream=stream)
 
     # eager warm-up, error check, then one CUDA graph per layer copy
     for i in range(max(args.warmup, n_copies)):
@@ -303,16 +330,19 @@ def main():
         if st != moe.MOE_OK:
             raise RuntimeError(f"device error {moe.status_string(st)} ({det})")
     graphs = []
+    n_graphs = max(n_copies, n_x)
     n0 = moe.moe_launch_total()
-    for c in range(n_copies):
+    for c in range(n_graphs):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             step(c)
         graphs.append(g)
-    launches_per_step = (moe.moe_launch_total() - n0) // n_copies
+    launches_per_step = (moe.moe_launch_total() - n0) // n_graphs
     for i in range(args.warmup):
-        graphs[i % n_copies].replay()
+        graphs[i % n_graphs].replay()
     torch.cuda.synchronize()
+    if cache_cfg:
+        cstats_t.zero_()
 
     # ---- timed region: exactly K steps
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -321,7 +351,7 @@ def main():
     with ClockSampler(dev.index or 0) as clk:
         ev0.record(stream)
         for i in range(args.steps):
-            graphs[i % n_copies].replay()
+            graphs[i % n_graphs].replay()
         ev1.record(stream)
         torch.cuda.synchronize()
     barrier(world)
@@ -398,22 +428,61 @@ def main():
                 "avg_launch_ms": statistics.mean(k_ms),
                 "traffic": recorded_traffic("ffn_tc.cu", wl_name)}
 
+    # the cache counters of the timed steps
+    cache_info = None
+    if cache_cfg:
+        cs = cstats_t.cpu().numpy().astype(np.int64)
+        steps_done = args.steps
+        cache_info = {"capacity": capacity, "decay": decay, "start": f"experts 0..{capacity - 1}",
+                      "hit_rate": float(cs[0]) / max(1, cs[1]), "miss_rate": 1.0 - float(cs[0]) / max(1, cs[1]),
+                      "admitted_per_step": float(cs[2]) / steps_done, "evicted_per_step": float(cs[3]) / steps_done,
+                      "stage_bytes_per_step": float(cs[2]) / steps_done * expert_bytes,
+                      "note": "timed steps: layer (resident = cache, HYBRID misses) + cache update; the e2e "
+                              "loop also stages every admitted expert from pinned host memory before the "
+                              "next step"}
+
     # ---- end to end through the public API: pinned host x -> device, layer
     # forward, result -> pinned host, every step
-    x_host = [xs[c].cpu().pin_memory() for c in range(n_copies)]
+    x_host = [xs[c].cpu().pin_memory() for c in range(n_x)]
     out_host = [torch.empty_like(bufs[c].out, device="cpu").pin_memory() for c in range(n_copies)]
     n_e2e = max(5 if phase == "prefill" else 20, min(args.steps, 1000))
+    if cache_cfg:
+        host_w_c = [[layers[0].w_gate[e].cpu().pin_memory() for e in range(cfg.N)],
+                    [layers[0].w_up[e].cpu().pin_memory() for e in range(cfg.N)],
+                    [layers[0].w_down[e].cpu().pin_memory() for e in range(cfg.N)]]
+        side_c = torch.cuda.Stream(device=dev)
+        done_c = torch.cuda.Event()
+        admit_host = torch.zeros(1, dtype=torch.int64).pin_memory()
+        staged_bytes = 0
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(n_e2e):
         c = i % n_copies
-        xs[c].copy_(x_host[c], non_blocking=True)
-        forward(layers[c], bufs[c], xs[c], stream=stream)
+        xc = xs[i % n_x]
+        xc.copy_(x_host[i % n_x], non_blocking=True)
+        if cache_cfg:
+            forward(layers[c], bufs[c], xc, stream=stream, n_resident=0)
+            moe.moe_cache_update(layers[c].dims.with_T(T), bufs[c].topk_idx, decay, capacity, heat_t, cache_t,
+                                 admit_t, None, stream)
+            admit_host.copy_(admit_t, non_blocking=True)
+        else:
+            forward(layers[c], bufs[c], xc, stream=stream)
         out_host[c].copy_(bufs[c].out, non_blocking=True)
         stream.synchronize()
+        if cache_cfg and int(admit_host[0]) != 0:
+            # the experts entering the cache, copied into the weights the next
+            # step reads before it may start
+            nxt = (i + 1) % n_copies
+            staged_bytes += moe.moe_stage_experts(
+                layers[nxt].dims.with_T(T), int(admit_host[0]) & ((1 << 64) - 1), *host_w_c,
+                list(layers[nxt].w_gate), list(layers[nxt].w_up), list(layers[nxt].w_down), side_c, done_c)
+            stream.wait_event(done_c)
+    torch.cuda.synchronize()
     e2e_s = max_over_ranks(world, time.perf_counter() - t0)
     e2e_value = world * T * n_e2e / e2e_s
+    if cache_cfg:
+        cache_info["e2e_staged_bytes_per_step"] = staged_bytes / n_e2e
 
     # ---- expert staging over the host link (EXACT-mode fetches): copy every
     # expert of one layer copy from pinned host memory with moe_stage_experts
@@ -476,6 +545,13 @@ def main():
         "routing": routing,
         "clocks": clocks,
     }
+    if cache_info:
+        line["config"]["resident"] = f"expert cache of {capacity} (heat decay {decay})"
+        line["e2e"]["h2d_bytes_per_step"] += cache_info["e2e_staged_bytes_per_step"]
+        line["e2e"]["d2h_bytes_per_step"] += 8
+        line["e2e"]["note"] += "; plus the cache update, the admitted-expert mask read back and the admitted " \
+                               "experts staged from pinned host memory"
+        line["cache"] = cache_info
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, W, T, args.cpu_seconds)
     if rank == 0:
