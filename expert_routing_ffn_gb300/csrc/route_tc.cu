@@ -179,14 +179,13 @@ cudaError_t launch_route_tc(const LogitsArgs& a, float* part, cudaStream_t st) {
     std::memset(&p, 0, sizeof(p));
     p.T = a.T; p.d = a.d; p.N = a.N; p.n_out = a.has_prefetch ? 2 * a.N : a.N;
     p.part = part;
-    p.err = nullptr;
+    p.err = a.err;
     if (encode_bf16_2d(&p.map_x, a.x, a.d, a.T, (uint64_t)a.d * 2, kTcBK, kRtBM) != MOE_OK ||
         encode_bf16_2d(&p.map_wr, a.w_router, a.d, a.N, (uint64_t)a.d * 2, kTcBK, a.N) != MOE_OK)
         return cudaErrorInvalidValue;
     if (a.has_prefetch &&
         encode_bf16_2d(&p.map_wp, a.w_prefetch, a.d, a.N, (uint64_t)a.d * 2, kTcBK, a.N) != MOE_OK)
         return cudaErrorInvalidValue;
-    p.err = a.err;
     const int m_tiles = (a.T + kRtBM - 1) / kRtBM, nkb = a.d / (int)kTcBK;
     int splits = (a.sms > 0 ? a.sms : 148) / m_tiles;
     splits = splits < 1 ? 1 : splits > kRtMaxSplits ? kRtMaxSplits : splits;
