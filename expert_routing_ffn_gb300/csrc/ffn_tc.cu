@@ -14,8 +14,11 @@
 // tensor memory and issues the MMAs (one thread), warps 2-5 drain the
 // accumulators (one TMEM lane = one tile row per thread).  Accumulators are
 // double-buffered (2 x 256 columns) so the epilogue of one tile overlaps the
-// MMAs of the next.  Every wait is bounded by a clock budget; a timeout sets
-// MOE_ERR_TIMEOUT and all roles leave their loops.
+// MMAs of the next.  The epilogue writes its output through shared memory
+// and TMA stores, 32 rows x 128 bytes at a time: a thread owns a row, so
+// direct stores would touch 32 cache lines per warp instruction.  Every wait
+// is bounded by a clock budget; a timeout sets MOE_ERR_TIMEOUT and all roles
+// leave their loops.
 #include <cuda.h>
 
 #include <cstring>
@@ -31,11 +34,14 @@ constexpr int kTcBM = 128, kTcBN = 256, kTcStages = 4, kTcThreads = 192;
 constexpr uint32_t kTcStageA = kTcBM * kTcBK * 2;  // 16 KB
 constexpr uint32_t kTcStageB = kTcBN * kTcBK * 2;  // 32 KB
 constexpr uint32_t kTcStageBytes = kTcStageA + kTcStageB;
-constexpr uint32_t kTcSmemBytes = kTcStages * kTcStageBytes + 1024;  // + alignment slack
+constexpr uint32_t kTcOutBox = 32 * 128;  // one epilogue warp's staging box: 32 rows x 128 bytes
+constexpr uint32_t kTcSmemBytes = kTcStages * kTcStageBytes + 4 * kTcOutBox + 1024;  // + alignment slack
 
 struct TcParams {
     CUtensorMap map_a_shared;  // phase 1: x [T, d];         phase 2: h_shared [T, ns*Is]
     CUtensorMap map_a_routed;  // phase 1: x_perm [T*k, d];  phase 2: h_routed [T*k, I]
+    CUtensorMap map_out_shared;  // phase 1: h_shared (bf16, 64 x 32 boxes); phase 2: y_shared (fp32, 32 x 32)
+    CUtensorMap map_out_routed;  // phase 1: h_routed;                       phase 2: y_perm
     const ExpertEntry* table;
     const TcPlan* plan;
     void* out_shared;          // phase 1: h_shared (bf16);  phase 2: y_shared (fp32)
@@ -64,9 +70,49 @@ __device__ __forceinline__ bool tc_tile(const TcPlan& P, int t, TcTile& out) {
     return true;
 }
 
+// ---------------------------------------------------------------- epilogue stores
+// 32 consecutive accumulator columns of this thread's TMEM lane, one wait.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// shared-memory writes of this thread become visible to the TMA (async) proxy
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int c0, int c1, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
+                 ::"l"(tmap), "r"(c0), "r"(c1), "r"(src) : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// the staging box may be rewritten: every committed store has read it
+__device__ __forceinline__ void tma_store_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// every committed store has completed
+__device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // ---------------------------------------------------------------- kernel
 template <int PHASE>
 __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_constant__ TcParams p) {
+    grid_dep_wait();  // the plan, x_perm / h: no tensor memory taken before it
     extern __shared__ unsigned char tc_smem_raw[];
     __shared__ __align__(8) uint64_t full[kTcStages], empty[kTcStages], tfull[2], tempty[2], drain;
     __shared__ uint32_t tmem_base_s;
@@ -198,8 +244,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
         }
     } else {
         // ---------------- epilogue: warps 2..5, thread = accumulator row
+        // A warp whose 32 rows all lie in the tile's segment stages each
+        // 32-row x 128-byte piece in its shared-memory box (128-byte swizzle:
+        // 16-byte chunk j of row i sits at chunk j ^ (i & 7), the layout of
+        // the output tensor map) and writes it with one TMA store; the warp
+        // that holds a segment's ragged end stores its valid rows directly
+        // (the rows after them belong to the next segment).
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
+        const uint32_t obox = smem_base + kTcStages * kTcStageBytes + quarter * kTcOutBox;
+        const uint32_t orow = obox + lane * 128;
+        const uint32_t sw = lane & 7;
         int local = 0;
         TcTile tl;
         // decisions stay warp-uniform: tcgen05.ld is a whole-warp instruction
@@ -214,26 +269,47 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + ab * kTcBN;
             const int row_in_seg = tl.mt * kTcBM + r;
             const bool valid = row_in_seg < S.rows;
+            const bool boxed = tl.mt * kTcBM + quarter * 32 + 32 <= S.rows;
+            const int box_row = S.row0 + tl.mt * kTcBM + quarter * 32;
+            const CUtensorMap* omap = S.shared ? &p.map_out_shared : &p.map_out_routed;
             const long long grow = (long long)S.row0 + row_in_seg;
             if (PHASE == 1) {
                 __nv_bfloat16* out = static_cast<__nv_bfloat16*>(S.shared ? p.out_shared : p.out_routed);
                 const long long ld = S.shared ? p.ld_out_shared : p.ld_out_routed;
                 __nv_bfloat16* dst = out + grow * ld + (long long)tl.nt * 128;
 #pragma unroll 1
-                for (int c = 0; c < 128; c += 16) {
-                    float g[16], u[16];
-                    tmem_ld16(taddr + c, g);
-                    tmem_ld16(taddr + 128 + c, u);
-                    if (valid) {
-                        uint32_t w[8];
+                for (int c = 0; c < 128; c += 64) {  // 64 channels = one 128-byte box row
+                    if (boxed) {
+                        if (lane == 0) tma_store_wait_read();
+                        __syncwarp();
+                    }
+#pragma unroll 1
+                    for (int hh = 0; hh < 2; ++hh) {
+                        float g[32], u[32];
+                        tmem_ld32(taddr + c + hh * 32, g);
+                        tmem_ld32(taddr + 128 + c + hh * 32, u);
+                        uint32_t w[16];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
+                        for (int i = 0; i < 16; ++i) {
                             const float h0 = g[2 * i] / (1.f + expf(-g[2 * i])) * u[2 * i];
                             const float h1 = g[2 * i + 1] / (1.f + expf(-g[2 * i + 1])) * u[2 * i + 1];
                             w[i] = pack_bf16x2(h0, h1);
                         }
-                        reinterpret_cast<uint4*>(dst + c)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                        reinterpret_cast<uint4*>(dst + c)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        if (boxed) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                st_shared_v4(orow + ((((uint32_t)(hh * 4 + q)) ^ sw) << 4), w[4 * q], w[4 * q + 1],
+                                             w[4 * q + 2], w[4 * q + 3]);
+                        } else if (valid) {
+                            uint4* o = reinterpret_cast<uint4*>(dst + c + hh * 32);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) o[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                        }
+                    }
+                    if (boxed) {
+                        fence_async_smem();
+                        __syncwarp();
+                        if (lane == 0) tma_store_2d(omap, tl.nt * 128 + c, box_row, obox);
                     }
                 }
             } else {
@@ -241,12 +317,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                 const long long ld = S.shared ? p.ld_out_shared : p.ld_out_routed;
                 float* dst = out + grow * ld + (long long)tl.nt * kTcBN;
 #pragma unroll 1
-                for (int c = 0; c < kTcBN; c += 16) {
-                    float v[16];
-                    tmem_ld16(taddr + c, v);
-                    if (valid) {
+                for (int c = 0; c < kTcBN; c += 32) {  // 32 columns = one 128-byte box row
+                    float v[32];
+                    tmem_ld32(taddr + c, v);
+                    if (boxed) {
+                        if (lane == 0) tma_store_wait_read();
+                        __syncwarp();
 #pragma unroll
-                        for (int i = 0; i < 16; i += 4)
+                        for (int q = 0; q < 8; ++q)
+                            st_shared_v4(orow + (((uint32_t)q ^ sw) << 4), __float_as_uint(v[4 * q]),
+                                         __float_as_uint(v[4 * q + 1]), __float_as_uint(v[4 * q + 2]),
+                                         __float_as_uint(v[4 * q + 3]));
+                        fence_async_smem();
+                        __syncwarp();
+                        if (lane == 0) tma_store_2d(omap, tl.nt * kTcBN + c, box_row, obox);
+                    } else if (valid) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
                             *reinterpret_cast<float4*>(dst + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
                     }
                 }
@@ -255,6 +342,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[ab]);
         }
+        // the block's shared memory stays allocated until these stores have
+        // read it, and the output is complete when the grid ends
+        if (lane == 0) tma_store_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -272,6 +363,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                           const int32_t* __restrict__ expert_offsets,
                                                           int N, int k, int chunks_per_row,
                                                           int rows_cap, uint4* __restrict__ x_perm) {
+    grid_dep_wait();  // the previous kernels' outputs (dependent launch)
     const int n_rows = expert_offsets[N];
     for (int pos = blockIdx.x; pos < n_rows && pos < rows_cap; pos += gridDim.x) {
         const int tok = perm[pos] / k;
@@ -285,9 +377,8 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* perm, const int32_t
                                int k, int d, int rows_cap, void* x_perm, cudaStream_t st) {
     const int chunks = d / 8;
     const int g_rows = rows_cap < 4096 ? (rows_cap > 0 ? rows_cap : 1) : 4096;
-    gather_rows_kernel<<<g_rows, 256, 0, st>>>(static_cast<const uint4*>(x), perm, expert_offsets, N, k,
-                                               chunks, rows_cap, static_cast<uint4*>(x_perm));
-    return cudaGetLastError();
+    return launch_pdl(gather_rows_kernel, dim3(g_rows), dim3(256), 0, st, static_cast<const uint4*>(x), perm,
+                      expert_offsets, N, k, chunks, rows_cap, static_cast<uint4*>(x_perm));
 }
 
 cudaError_t launch_tc_ffn(const TcLaunch& a, cudaStream_t st) {
@@ -302,29 +393,38 @@ cudaError_t launch_tc_ffn(const TcLaunch& a, cudaStream_t st) {
     p1.table = a.table; p1.plan = a.plan;
     p1.out_shared = a.h_shared; p1.out_routed = a.h_routed;
     p1.ld_out_shared = (long long)a.n_shared * a.I_shared; p1.ld_out_routed = a.I;
+    // epilogue store maps: 128-byte x 32-row boxes
+    const uint64_t hs_cols = (uint64_t)a.n_shared * a.I_shared;
+    if (a.n_shared > 0 &&
+        encode_bf16_2d(&p1.map_out_shared, a.h_shared, hs_cols, a.T, hs_cols * 2, 64, 32) != MOE_OK)
+        return cudaErrorInvalidValue;
+    if (encode_bf16_2d(&p1.map_out_routed, a.h_routed, a.I, a.rows_cap, (uint64_t)a.I * 2, 64, 32) != MOE_OK)
+        return cudaErrorInvalidValue;
     p1.d = a.d; p1.N = a.N; p1.I = a.I; p1.I_shared = a.I_shared; p1.n_shared = a.n_shared; p1.err = a.err;
 
     TcParams p2 = p1;
-    const uint64_t hs_cols = (uint64_t)a.n_shared * a.I_shared;
     if (a.n_shared > 0 &&
         encode_bf16_2d(&p2.map_a_shared, a.h_shared, hs_cols, a.T, hs_cols * 2, kTcBK, kTcBM) != MOE_OK)
         return cudaErrorInvalidValue;
     if (encode_bf16_2d(&p2.map_a_routed, a.h_routed, a.I, a.rows_cap, (uint64_t)a.I * 2, kTcBK, kTcBM) != MOE_OK)
         return cudaErrorInvalidValue;
     p2.out_shared = a.y_shared; p2.out_routed = a.y_perm;
+    if (a.n_shared > 0 &&
+        encode_f32_2d(&p2.map_out_shared, a.y_shared, a.d, a.T, (uint64_t)a.d * 4, 32, 32) != MOE_OK)
+        return cudaErrorInvalidValue;
+    if (encode_f32_2d(&p2.map_out_routed, a.y_perm, a.d, a.rows_cap, (uint64_t)a.d * 4, 32, 32) != MOE_OK)
+        return cudaErrorInvalidValue;
     p2.ld_out_shared = a.d; p2.ld_out_routed = a.d;
 
     e = allow_max_smem(ffn_tc_kernel<1>);
     if (e != cudaSuccess) return e;
     e = allow_max_smem(ffn_tc_kernel<2>);
     if (e != cudaSuccess) return e;
-    ffn_tc_kernel<1><<<a.grid, kTcThreads, kTcSmemBytes, st>>>(p1);
     e = note_launch(reinterpret_cast<const void*>(ffn_tc_kernel<1>), kTcThreads, kTcSmemBytes,
-                    cudaGetLastError());
+                    launch_pdl(ffn_tc_kernel<1>, dim3(a.grid), dim3(kTcThreads), kTcSmemBytes, st, p1));
     if (e != cudaSuccess) return e;
-    ffn_tc_kernel<2><<<a.grid, kTcThreads, kTcSmemBytes, st>>>(p2);
     return note_launch(reinterpret_cast<const void*>(ffn_tc_kernel<2>), kTcThreads, kTcSmemBytes,
-                       cudaGetLastError());
+                       launch_pdl(ffn_tc_kernel<2>, dim3(a.grid), dim3(kTcThreads), kTcSmemBytes, st, p2));
 }
 
 }  // namespace moe

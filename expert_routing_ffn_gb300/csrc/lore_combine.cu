@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(256) lore_z_grouped_kernel(const W* __restrict
                                                              const int32_t* __restrict__ g_off,
                                                              const int32_t* __restrict__ g_list, int d, int k,
                                                              int r, int N, int n_pos, float* __restrict__ zp) {
+    grid_dep_wait();  // the previous kernels' outputs (dependent launch)
     constexpr int V = Vec<W>::n;
     constexpr int CV = kLoreKC / V;                    // 16-byte vectors per row and chunk
     constexpr int XL = (kLoreTile * CV + 255) / 256;   // x vectors per thread and chunk
@@ -244,6 +245,7 @@ __global__ void __launch_bounds__(256) lore_z_sum_kernel(const float* __restrict
                                                          const int32_t* __restrict__ g_list, int r, int N,
                                                          int n_pos, const float* __restrict__ zp,
                                                          float* __restrict__ zg) {
+    grid_dep_wait();  // the previous kernels' outputs (dependent launch)
     const int n = g_off[N];
     const int r4 = r / 4;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n * r4; i += gridDim.x * blockDim.x) {
@@ -271,6 +273,7 @@ __global__ void __launch_bounds__(256) lore_b_grouped_kernel(const W* __restrict
                                                              const int32_t* __restrict__ g_off, int d, int r,
                                                              int N, const float* __restrict__ zg,
                                                              float* __restrict__ v) {
+    grid_dep_wait();  // the previous kernels' outputs (dependent launch)
     constexpr int V = Vec<W>::n;
     constexpr int TC = 64;                 // columns per chunk
     constexpr int BL = (64 * TC / V + 255) / 256;  // B vectors per thread and chunk (r <= 64)
@@ -353,6 +356,7 @@ __global__ void __launch_bounds__(256) lore_b_grouped_kernel(const W* __restrict
 // y_lore[t] = the token's LoRE rows v[pos], added in slot order from zero.
 __global__ void __launch_bounds__(256) lore_sum_kernel(const int32_t* __restrict__ g_pos, const float* __restrict__ v,
                                                        int d, int k, float* __restrict__ y_lore) {
+    grid_dep_wait();  // the previous kernels' outputs (dependent launch)
     const int t = blockIdx.x;
     const int q = blockIdx.y * blockDim.x + threadIdx.x;  // float4 column group
     __shared__ int s_pos[kMaxTopK];
@@ -374,6 +378,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const float* __restrict__ y_shared,
                                                       const float* __restrict__ y_lore, int d,
                                                       int k, float* __restrict__ out) {
+    grid_dep_wait();  // the previous kernels' outputs (dependent launch)
     const int t = blockIdx.x;
     const int q = blockIdx.y * blockDim.x + threadIdx.x;  // float4 column group
     __shared__ int s_pos[kMaxTopK], s_kind[kMaxTopK];
@@ -673,13 +678,18 @@ static cudaError_t launch_lore_grouped(const LoreArgs& a, cudaStream_t st) {
     const int n_pos = a.T * a.k;
     const int tiles = n_pos / kLoreTile + a.N;
     const int gz = tiles < 160 ? tiles : 160;
-    lore_z_grouped_kernel<W><<<dim3(gz, kLoreKS), 256, 0, st>>>((const W*)a.x, (const W*)a.A, a.g_off, a.g_list,
-                                                                 a.d, a.k, a.r, a.N, n_pos, a.zp);
-    lore_z_sum_kernel<<<4 * 152, 256, 0, st>>>(a.final_gate, a.g_off, a.g_list, a.r, a.N, n_pos, a.zp, a.z);
+    e = launch_pdl(lore_z_grouped_kernel<W>, dim3(gz, kLoreKS), dim3(256), 0, st, (const W*)a.x, (const W*)a.A,
+                   (const int32_t*)a.g_off, (const int32_t*)a.g_list, a.d, a.k, a.r, a.N, n_pos, a.zp);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(lore_z_sum_kernel, dim3(4 * 152), dim3(256), 0, st, a.final_gate, (const int32_t*)a.g_off,
+                   (const int32_t*)a.g_list, a.r, a.N, n_pos, (const float*)a.zp, a.z);
+    if (e != cudaSuccess) return e;
     const int gx = tiles < 304 ? tiles : 304;
-    lore_b_grouped_kernel<W><<<dim3(gx, kLoreBY), 256, 0, st>>>((const W*)a.B, a.g_off, a.d, a.r, a.N, a.z, a.v);
-    lore_sum_kernel<<<dim3(a.T, (a.d / 4 + 255) / 256), 256, 0, st>>>(a.g_pos, a.v, a.d, a.k, a.y_lore);
-    return cudaGetLastError();
+    e = launch_pdl(lore_b_grouped_kernel<W>, dim3(gx, kLoreBY), dim3(256), 0, st, (const W*)a.B,
+                   (const int32_t*)a.g_off, a.d, a.r, a.N, (const float*)a.z, a.v);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(lore_sum_kernel, dim3(a.T, (a.d / 4 + 255) / 256), dim3(256), 0, st, (const int32_t*)a.g_pos,
+                      (const float*)a.v, a.d, a.k, a.y_lore);
 }
 
 bool lore_grouped_usable(int T, int d, int r, bool bf16) {
@@ -714,9 +724,8 @@ cudaError_t launch_lore(const LoreArgs& a, cudaStream_t st) {
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
     if (a.T == 0) return cudaSuccess;
     dim3 grid(a.T, (a.d / 4 + 255) / 256);
-    combine_kernel<<<grid, 256, 0, st>>>(a.y_perm, a.inv_perm, a.final_gate, a.final_kind, a.y_shared,
-                                        a.y_lore, a.d, a.k, a.out);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, grid, dim3(256), 0, st, a.y_perm, a.inv_perm, a.final_gate, a.final_kind,
+                      a.y_shared, a.y_lore, a.d, a.k, a.out);
 }
 
 }  // namespace moe

@@ -434,6 +434,8 @@ moe_status expert_ffn_impl(const moe_dims* dims, const void* x, const void* tabl
     if (!aligned16(x) || reinterpret_cast<uintptr_t>(table) % 64) return MOE_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(*dims);
     if (use_tc(*dims)) {
+        // the epilogue writes y_perm / y_shared with TMA stores
+        if (!aligned16(y_perm) || (y_shared && !aligned16(y_shared))) return MOE_ERR_INVALID_ARG;
         TcLaunch t;
         t.x = x; t.perm = perm; t.expert_offsets = expert_offsets;
         t.table = static_cast<const ExpertEntry*>(table); t.plan = ws_at<TcPlan>(ws, L.tc_plan);

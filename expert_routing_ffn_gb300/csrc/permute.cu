@@ -45,6 +45,7 @@ __global__ void __launch_bounds__(kPermChunk) permute_count_kernel(const int32_t
                                                                    int n_slots, int N,
                                                                    int32_t* __restrict__ counts,
                                                                    DevError* __restrict__ err) {
+    grid_dep_wait();  // the previous kernels' outputs (dependent launch)
     __shared__ int cnt[kPermChunk / 32][kMaxExperts];
     const int tid = threadIdx.x, nw = blockDim.x >> 5;
     for (int i = tid; i < nw * kMaxExperts; i += blockDim.x) (&cnt[0][0])[i] = 0;
@@ -151,9 +152,8 @@ cudaError_t launch_permute(const PermuteArgs& a, const PlanArgs& plan, int32_t* 
         return cudaGetLastError();
     }
     const int n_chunks = (a.n_slots + kPermChunk - 1) / kPermChunk;
-    permute_count_kernel<false><<<n_chunks, kPermChunk, 0, st>>>(a.final_idx, a.final_kind, a.n_slots, a.N,
-                                                                 counts, a.err);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(permute_count_kernel<false>, dim3(n_chunks), dim3(kPermChunk), 0, st, a.final_idx,
+                               a.final_kind, a.n_slots, a.N, counts, a.err);
     if (e != cudaSuccess) return e;
     return launch_pdl(permute_scatter_kernel<false>, dim3(n_chunks), dim3(kPermChunk), 0, st, a.final_idx,
                       a.final_kind, a.n_slots, a.N, (const int32_t*)counts, a.expert_offsets, a.perm,
@@ -162,9 +162,8 @@ cudaError_t launch_permute(const PermuteArgs& a, const PlanArgs& plan, int32_t* 
 
 cudaError_t launch_group_lore(const PermuteArgs& a, int32_t* counts, cudaStream_t st) {
     const int n_chunks = (a.n_slots + kPermChunk - 1) / kPermChunk;
-    permute_count_kernel<true><<<n_chunks, kPermChunk, 0, st>>>(a.final_idx, a.final_kind, a.n_slots, a.N,
-                                                                counts, a.err);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(permute_count_kernel<true>, dim3(n_chunks), dim3(kPermChunk), 0, st, a.final_idx,
+                               a.final_kind, a.n_slots, a.N, counts, a.err);
     if (e != cudaSuccess) return e;
     PlanArgs none;
     none.tc_plan = nullptr;

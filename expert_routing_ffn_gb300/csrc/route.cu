@@ -259,6 +259,7 @@ template <typename W>
 __global__ void __launch_bounds__(256) route_score_kernel(const W* __restrict__ x_pre,
                                                           const float* __restrict__ w_ord, int T, int d,
                                                           float* __restrict__ score) {
+    grid_dep_wait();  // the previous kernels' outputs (dependent launch)
     constexpr int V = Vec<W>::n;
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -391,6 +392,7 @@ __global__ void __launch_bounds__(256) route_select_kernel(
     int N, int k, int delta_max, int has_prefetch, int32_t* __restrict__ topk_idx,
     float* __restrict__ topk_gate, float* __restrict__ router_prob, int32_t* __restrict__ delta_hat,
     uint64_t* __restrict__ prefetch_mask, int32_t* __restrict__ delta_star, float* __restrict__ qp) {
+    grid_dep_wait();  // the previous kernels' outputs (dependent launch)
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (warp >= T) return;
     route_select_token(warp, logits_r, logits_p, score, theta, logit_tau, N, k, delta_max, has_prefetch,
@@ -446,6 +448,7 @@ __global__ void __launch_bounds__(1024) batch_resident_kernel(const float* __res
 constexpr int kResParts = 32;
 __global__ void __launch_bounds__(256) batch_resident_part_kernel(const float* __restrict__ qp, int T, int N,
                                                                   float* __restrict__ part) {
+    grid_dep_wait();  // the previous kernels' outputs (dependent launch)
     __shared__ float q4[4][kMaxExperts];
     const int e = threadIdx.x & 63, quarter = threadIdx.x >> 6;
     const int t0 = (int)((long long)blockIdx.x * T / kResParts), t1 = (int)((long long)(blockIdx.x + 1) * T / kResParts);
@@ -470,6 +473,7 @@ __global__ void __launch_bounds__(256) batch_resident_part_kernel(const float* _
 
 __global__ void __launch_bounds__(64) batch_resident_final_kernel(const float* __restrict__ part, int N, int n_res,
                                                                   uint64_t* __restrict__ out) {
+    grid_dep_wait();  // the previous kernels' outputs (dependent launch)
     __shared__ float tot[kMaxExperts];
     __shared__ uint32_t bits[2];
     const int me = threadIdx.x;
@@ -600,6 +604,7 @@ __global__ void __launch_bounds__(256) select_resident_kernel(
     int N, int k, int renorm, int32_t* __restrict__ final_idx, float* __restrict__ final_gate,
     int32_t* __restrict__ final_kind, uint64_t* __restrict__ fetch_mask,
     int32_t* __restrict__ counters, DevError* __restrict__ err) {
+    grid_dep_wait();  // the previous kernels' outputs (dependent launch)
     // the block's counters and fetch mask gathered in shared memory, then one
     // global atomic each (every token adding to the same global counters
     // serialised on them)
@@ -757,9 +762,8 @@ static cudaError_t launch_logits_t(const LogitsArgs& a, cudaStream_t st) {
     if (a.part && route_tc_usable(a.T, a.d, a.N, a.bf16, a.has_prefetch, sep_pre)) {
         cudaError_t e = launch_route_tc(a, a.part, st);
         if (e != cudaSuccess || !a.has_prefetch) return e;
-        route_score_kernel<W><<<(a.T + 7) / 8, 256, 0, st>>>((const W*)(a.x_pre ? a.x_pre : a.x), a.w_ord, a.T,
-                                                             a.d, a.score);
-        return cudaGetLastError();
+        return launch_pdl(route_score_kernel<W>, dim3((a.T + 7) / 8), dim3(256), 0, st,
+                          (const W*)(a.x_pre ? a.x_pre : a.x), a.w_ord, a.T, a.d, a.score);
     }
     // (a row quad must not straddle the router / prefetch-router boundary when
     // the two routers read different inputs)
@@ -771,9 +775,8 @@ static cudaError_t launch_logits_t(const LogitsArgs& a, cudaStream_t st) {
             (const W*)a.w_prefetch, a.w_ord, a.T, a.d, a.N, rows, a.logits_r, a.logits_p, a.score);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess || !a.has_prefetch) return e;
-        route_score_kernel<W><<<(a.T + 7) / 8, 256, 0, st>>>((const W*)(a.x_pre ? a.x_pre : a.x), a.w_ord, a.T,
-                                                             a.d, a.score);
-        return cudaGetLastError();
+        return launch_pdl(route_score_kernel<W>, dim3((a.T + 7) / 8), dim3(256), 0, st,
+                          (const W*)(a.x_pre ? a.x_pre : a.x), a.w_ord, a.T, a.d, a.score);
     }
     const int n_out = a.has_prefetch ? 2 * a.N + 1 : a.N;
     const int t_tiles = (a.T + TT - 1) / TT;
@@ -799,18 +802,17 @@ cudaError_t launch_logits(const LogitsArgs& a, cudaStream_t st) {
 cudaError_t launch_route_select(const RouteSelectArgs& a, cudaStream_t st) {
     const int warps = 8;
     dim3 grid((a.T + warps - 1) / warps);
-    route_select_kernel<<<grid, warps * 32, 0, st>>>(
-        a.logits_r, a.logits_p, a.score, a.theta, a.logit_tau, a.T, a.N, a.k, a.delta_max,
-        a.has_prefetch, a.topk_idx, a.topk_gate, a.router_prob, a.delta_hat, a.prefetch_mask,
-        a.delta_star, a.qp);
-    return cudaGetLastError();
+    return launch_pdl(route_select_kernel, grid, dim3(warps * 32), 0, st, a.logits_r, a.logits_p, a.score, a.theta,
+                      a.logit_tau, a.T, a.N, a.k, a.delta_max, a.has_prefetch, a.topk_idx, a.topk_gate,
+                      a.router_prob, a.delta_hat, a.prefetch_mask, a.delta_star, a.qp);
 }
 
 cudaError_t launch_batch_resident(const float* qp, int T, int N, int n_res, uint64_t* out, float* part,
                                   cudaStream_t st) {
     if (T >= 8 * kResParts && part) {
-        batch_resident_part_kernel<<<kResParts, 256, 0, st>>>(qp, T, N, part);
-        batch_resident_final_kernel<<<1, 64, 0, st>>>(part, N, n_res, out);
+        cudaError_t e = launch_pdl(batch_resident_part_kernel, dim3(kResParts), dim3(256), 0, st, qp, T, N, part);
+        if (e != cudaSuccess) return e;
+        return launch_pdl(batch_resident_final_kernel, dim3(1), dim3(64), 0, st, (const float*)part, N, n_res, out);
     } else {
         batch_resident_kernel<<<1, 1024, 0, st>>>(qp, T, N, n_res, out);
     }
@@ -820,11 +822,9 @@ cudaError_t launch_batch_resident(const float* qp, int T, int N, int n_res, uint
 cudaError_t launch_select_resident(const SelectArgs& a, cudaStream_t st) {
     const int warps = 8;
     dim3 grid((a.T + warps - 1) / warps);
-    select_resident_kernel<<<grid, warps * 32, 0, st>>>(
-        a.router_prob, a.topk_idx, a.prefetch_mask, a.resident, a.policy, a.gamma, a.delta_hat,
-        a.delta_star, a.T, a.N, a.k, a.renorm, a.final_idx, a.final_gate, a.final_kind,
-        a.fetch_mask, a.counters, a.err);
-    return cudaGetLastError();
+    return launch_pdl(select_resident_kernel, grid, dim3(warps * 32), 0, st, a.router_prob, a.topk_idx,
+                      a.prefetch_mask, a.resident, a.policy, a.gamma, a.delta_hat, a.delta_star, a.T, a.N, a.k,
+                      a.renorm, a.final_idx, a.final_gate, a.final_kind, a.fetch_mask, a.counters, a.err);
 }
 
 }  // namespace moe

@@ -45,6 +45,7 @@ __host__ __device__ inline uint32_t rt_stage_bytes(int n_out) {
 }
 
 __global__ void __launch_bounds__(kRtThreads, 1) route_tc_kernel(const __grid_constant__ RouteTcParams p) {
+    grid_dep_wait();  // x is written before this launch; no tensor memory taken before it
     extern __shared__ unsigned char rt_smem_raw[];
     __shared__ __align__(8) uint64_t full[kRtStages], empty[kRtStages], done;
     __shared__ uint32_t tmem_base_s;
@@ -150,6 +151,7 @@ __global__ void __launch_bounds__(256) route_tc_reduce_kernel(const float* __res
                                                               int N, int n_out, const float* __restrict__ bias,
                                                               float* __restrict__ logits_r,
                                                               float* __restrict__ logits_p) {
+    grid_dep_wait();  // the previous kernels' outputs (dependent launch)
     const int n4 = n_out / 4;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T * n4; i += gridDim.x * blockDim.x) {
         const int tok = i / n4, c = (i % n4) * 4;
@@ -193,14 +195,13 @@ cudaError_t launch_route_tc(const LogitsArgs& a, float* part, cudaStream_t st) {
     const size_t smem = (size_t)kRtStages * rt_stage_bytes(p.n_out) + 1024;
     cudaError_t e = allow_max_smem(route_tc_kernel);
     if (e != cudaSuccess) return e;
-    route_tc_kernel<<<dim3(m_tiles, splits), kRtThreads, smem, st>>>(p);
-    e = note_launch(reinterpret_cast<const void*>(route_tc_kernel), kRtThreads, smem, cudaGetLastError());
+    e = note_launch(reinterpret_cast<const void*>(route_tc_kernel), kRtThreads, smem,
+                    launch_pdl(route_tc_kernel, dim3(m_tiles, splits), dim3(kRtThreads), smem, st, p));
     if (e != cudaSuccess) return e;
     const int n4 = a.T * (p.n_out / 4);
     const int blocks = (n4 + 255) / 256 < 4 * 152 ? (n4 + 255) / 256 : 4 * 152;
-    route_tc_reduce_kernel<<<blocks, 256, 0, st>>>(part, splits, a.T, a.N, p.n_out, a.bias, a.logits_r,
-                                                   a.logits_p);
-    return cudaGetLastError();
+    return launch_pdl(route_tc_reduce_kernel, dim3(blocks), dim3(256), 0, st, (const float*)part, splits, a.T, a.N,
+                      p.n_out, a.bias, a.logits_r, a.logits_p);
 }
 
 }  // namespace moe

@@ -27,10 +27,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-}  // namespace
-
-moe_status encode_bf16_2d(void* out128, const void* base, uint64_t inner, uint64_t outer,
-                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+moe_status encode_2d(void* out128, CUtensorMapDataType type, const void* base, uint64_t inner, uint64_t outer,
+                     uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
     auto fn = encode_fn();
     if (!fn) return MOE_ERR_CUDA;
     if ((reinterpret_cast<uintptr_t>(base) & 15u) || (row_stride_bytes & 15u)) return MOE_ERR_INVALID_ARG;
@@ -40,12 +38,26 @@ moe_status encode_bf16_2d(void* out128, const void* base, uint64_t inner, uint64
     const cuuint64_t strides[1] = {row_stride_bytes};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+    CUresult r = fn(&m, type, 2, const_cast<void*>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return MOE_ERR_INVALID_ARG;
     std::memcpy(out128, &m, sizeof(m));
     return MOE_OK;
+}
+
+}  // namespace
+
+moe_status encode_bf16_2d(void* out128, const void* base, uint64_t inner, uint64_t outer,
+                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+    return encode_2d(out128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, inner, outer, row_stride_bytes, box_inner,
+                     box_outer);
+}
+
+moe_status encode_f32_2d(void* out128, const void* base, uint64_t inner, uint64_t outer,
+                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+    return encode_2d(out128, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, inner, outer, row_stride_bytes, box_inner,
+                     box_outer);
 }
 
 moe_status encode_expert_tmaps(ExpertEntry& E, int d) {

@@ -221,7 +221,9 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* final_idx,
  *   bf16 layers only; otherwise MOE_ERR_UNSUPPORTED.
  *   y_perm [T*k, d] float32: row pos = the expert output for slot perm[pos]
  *   (ungated); y_shared [T, d] float32 (NULL if n_shared == 0) = sum of the
- *   shared experts' outputs.
+ *   shared experts' outputs.  x must be 16-byte aligned, and so must y_perm
+ *   and y_shared for batches of more than 64 tokens (MOE_ERR_INVALID_ARG
+ *   otherwise).
  *   Kernels (moe_expert_ffn_path names the choice for a call): batches of
  *   more than 64 tokens of bf16 layers run as a tcgen05 tensor-core grouped
  *   GEMM; dense bf16 batches of 4..64 tokens (d a multiple of 128, expert

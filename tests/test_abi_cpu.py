@@ -97,6 +97,20 @@ def test_null_buffers_rejected_before_cuda():
     assert st == moe.MOE_ERR_INVALID_ARG
 
 
+def test_prefill_ffn_rejects_misaligned_outputs_before_cuda():
+    """The prefill tensor-core FFN writes y_perm and y_shared with TMA stores:
+    an output that is not 16-byte aligned is an argument error, found before
+    any CUDA call."""
+    L = moe.lib()
+    D = _raw_dims(T=100, d=256, N=8, k=2, I=128)
+    n = moe.moe_workspace_size(D)
+    fake_ws = C.c_void_p(1 << 20)
+    x, table, offs, perm = C.c_void_p(0x1000), C.c_void_p(0x2000), C.c_void_p(0x3000), C.c_void_p(0x4000)
+    fn = L.moe_expert_ffn
+    st = fn(C.byref(D), x, table, offs, perm, C.c_float(1.0), C.c_void_p(0x5004), None, fake_ws, n, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+
+
 def test_staging_failure_is_reported_on_the_host():
     """An injected copy failure makes moe_stage_experts return
     MOE_ERR_STAGING before anything is queued (no GPU fault involved)."""
