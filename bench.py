@@ -420,13 +420,24 @@ def main():
                 "avg_launch_ms": statistics.mean(k_ms),
                 "traffic": recorded_traffic(ksrc, wl_name)}
     else:
-        achieved = sum(k_flops) / (sum(k_ms) / 1e3) / 1e12
-        roof = {"kernel": "moe_expert_ffn (gather + ffn_tc_kernel<1> + ffn_tc_kernel<2>)",
-                "ffn_path": path, "bound": "tensor", "achieved": achieved, "peak": bf16_tflops, "unit": "TFLOP/s",
-                "frac": achieved / bf16_tflops, "peak_source": peak_src + " bf16 burst",
-                "algorithmic_flops_per_launch": float(statistics.mean(ff)),
-                "avg_launch_ms": statistics.mean(k_ms),
-                "traffic": recorded_traffic("ffn_tc.cu", wl_name)}
+        # prefill: the bound is whichever roofline time is longer, the FLOPs at the
+        # bf16 peak or the expert weight bytes at the HBM bandwidth (a short batch
+        # of many experts, e.g. Granite-shaped at 1024 tokens, is HBM-bound)
+        tflops = sum(k_flops) / (sum(k_ms) / 1e3) / 1e12
+        gbs = sum(k_bytes) / (sum(k_ms) / 1e3) / 1e9
+        t_flop = statistics.mean(ff) / (bf16_tflops * 1e12)
+        t_byte = statistics.mean(fb) / (hbm_gbs * 1e9)
+        common = {"kernel": "moe_expert_ffn (gather + ffn_tc_kernel<1> + ffn_tc_kernel<2>)", "ffn_path": path}
+        if t_byte > t_flop:
+            roof = dict(common, bound="hbm", achieved=gbs, peak=hbm_gbs, unit="GB/s", frac=gbs / hbm_gbs,
+                        peak_source=peak_src, tensor_frac=tflops / bf16_tflops)
+        else:
+            roof = dict(common, bound="tensor", achieved=tflops, peak=bf16_tflops, unit="TFLOP/s",
+                        frac=tflops / bf16_tflops, peak_source=peak_src + " bf16 burst", hbm_frac=gbs / hbm_gbs)
+        roof.update({"algorithmic_flops_per_launch": float(statistics.mean(ff)),
+                     "algorithmic_bytes_per_launch": float(statistics.mean(fb)),
+                     "avg_launch_ms": statistics.mean(k_ms),
+                     "traffic": recorded_traffic("ffn_tc.cu", wl_name)})
 
     # the cache counters of the timed steps
     cache_info = None
