@@ -97,6 +97,10 @@ def lib():
             L.orc_cache_update.argtypes = [C.c_int, C.c_int, _IP, C.c_double, C.c_int, _DP, C.c_uint64,
                                            C.POINTER(C.c_int), _DP]
             L.orc_cache_update.restype = C.c_uint64
+            L.orc_prefetch_depth.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, _FP,
+                                             C.POINTER(_FP), C.POINTER(_FP), C.c_double, C.c_int, _DP, _IP,
+                                             C.POINTER(C.c_uint64), C.POINTER(C.c_uint64), _DP]
+            L.orc_prefetch_depth.restype = None
             L.orc_layer_forward.argtypes = [C.POINTER(_Cfg), C.POINTER(_Inputs), C.POINTER(_Outputs)]
             _lib = L
     return _lib
@@ -218,6 +222,36 @@ def cache_update(routed, heat, decay, capacity, old_cache):
     m = lib().orc_cache_update(len(heat), len(routed), routed.ctypes.data_as(_IP), float(decay), int(capacity),
                                _d(heat), C.c_uint64(old_cache), C.byref(hits), C.byref(gap))
     return int(m), heat, hits.value, gap.value
+
+
+def prefetch_depth(x, Ws, biases, K, tau, d_min):
+    """Confidence-aware prefetch depth over J look-ahead routers (SPICE
+    write-up, confidence-aware adaptive prefetch).  Ws: J arrays [N, d];
+    biases: None or J arrays [N] (entries may be None).  Returns
+    (conf [T,J] float64, depth [T] int, tok_masks [T,J] uint64,
+    layer_masks [J] uint64, margin [T] float64)."""
+    xs = f32(x)
+    T, d = xs.shape
+    J = len(Ws)
+    Wf = [f32(W) for W in Ws]
+    N = Wf[0].shape[0]
+    Wp = (_FP * J)(*[_f(W) for W in Wf])
+    if biases is None:
+        bp = None
+        keep = []
+    else:
+        keep = [None if b is None else f32(b) for b in biases]
+        bp = (_FP * J)(*[C.cast(None, _FP) if b is None else _f(b) for b in keep])
+    conf = np.zeros((T, J), np.float64)
+    depth = np.zeros(T, np.int32)
+    tok = np.zeros((T, J), np.uint64)
+    lay = np.zeros(J, np.uint64)
+    margin = np.zeros(T, np.float64)
+    lib().orc_prefetch_depth(T, d, N, int(K), J, _f(xs), Wp, bp, float(tau), int(d_min), _d(conf),
+                             depth.ctypes.data_as(_IP), tok.ctypes.data_as(C.POINTER(C.c_uint64)),
+                             lay.ctypes.data_as(C.POINTER(C.c_uint64)), _d(margin))
+    del keep
+    return conf, depth.astype(np.int64), tok, lay, margin
 
 
 # ---- whole layer ---------------------------------------------------------

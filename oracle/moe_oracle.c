@@ -23,6 +23,9 @@
  *     surrogate" (y_e ~ y_shared + B_e A_e h).
  *   - shared experts, combine         : SPICE write-up, LoRE section (the
  *     always-active shared expert) and the gate-weighted MoE sum.
+ *   - look-ahead prefetch depth       : SPICE write-up, confidence-aware
+ *     adaptive prefetch (top-K mass confidence, stop below the threshold,
+ *     minimum depth).
  *   - persistent expert cache         : ELMoE-3D (CSDN post), expert-axis
  *     elasticity: heat statistics, top-K subset, dynamic update, and the
  *     practice note on heat decay (multiply every heat by a factor just
@@ -306,6 +309,69 @@ uint64_t orc_cache_update(int N, int n_slots, const int* routed, double decay, i
     if (hits) *hits = h;
     free(count); free(idx);
     return cache;
+}
+
+/* Confidence-aware prefetch depth (SPICE write-up, section on
+ * confidence-aware adaptive prefetch): a draft predicts, from the current
+ * hidden state, the expert distribution of each of the next J layers; its
+ * confidence C is the probability mass on the predicted top-K experts;
+ * prediction goes one layer deeper while C stays at or above tau and stops
+ * at the first layer below it; the depth is never below the minimum depth
+ * D_min that lets a transfer finish within the layers it runs ahead of.
+ * The draft's prediction head is the identity here: layer l+j's router
+ * applied to the current x (the trained head is not given).
+ *   x[T,d]; W[j] = router of look-ahead layer j [N,d]; bias[j] [N] or NULL.
+ *   conf[T,J] = sum of the K largest of softmax(x W[j]^T + bias[j]).
+ *   depth[T]  = min(J, max(d_min, c)), c = number of leading layers
+ *               j = 0, 1, ... whose conf >= tau (the scan stops at the first
+ *               below tau).
+ *   tok_masks[T,J] = the top-K set of layer j when j < depth[t], else 0.
+ *   layer_masks[J] = OR over tokens of tok_masks[., j].
+ *   margin[T] (optional): the smallest |conf - tau| over the layers the scan
+ *               reads, and the logit gap at position K over the layers kept. */
+void orc_prefetch_depth(int T, int d, int N, int K, int J, const float* x, const float* const* W,
+                        const float* const* bias, double tau, int d_min, double* conf, int* depth,
+                        uint64_t* tok_masks, uint64_t* layer_masks, double* margin) {
+    double* l = (double*)malloc(sizeof(double) * (size_t)N);
+    double* p = (double*)malloc(sizeof(double) * (size_t)N);
+    int* idx = (int*)malloc(sizeof(int) * (size_t)N);
+    for (int j = 0; j < J; ++j) layer_masks[j] = 0;
+    for (int t = 0; t < T; ++t) {
+        double m = INFINITY;
+        int c = 0, scanning = 1;
+        uint64_t set[64];
+        double gap[64];
+        for (int j = 0; j < J; ++j) {
+            orc_logits(1, d, N, x + (size_t)t * d, W[j], bias ? bias[j] : 0, l);
+            orc_softmax(N, l, p);
+            orc_topk(N, N, l, idx);
+            double mass = 0.0;
+            set[j] = 0;
+            for (int i = 0; i < K; ++i) {
+                mass += p[idx[i]];
+                set[j] |= (uint64_t)1 << idx[i];
+            }
+            gap[j] = K < N ? l[idx[K - 1]] - l[idx[K]] : INFINITY;
+            conf[(size_t)t * J + j] = mass;
+            if (scanning) {
+                const double dm = fabs(mass - tau);
+                if (dm < m) m = dm;
+                if (mass >= tau) c += 1;
+                else scanning = 0;
+            }
+        }
+        int dep = c > d_min ? c : d_min;
+        if (dep > J) dep = J;
+        depth[t] = dep;
+        for (int j = 0; j < J; ++j) {
+            const uint64_t s_j = j < dep ? set[j] : 0;
+            tok_masks[(size_t)t * J + j] = s_j;
+            layer_masks[j] |= s_j;
+            if (j < dep && gap[j] < m) m = gap[j];
+        }
+        if (margin) margin[t] = m;
+    }
+    free(l); free(p); free(idx);
 }
 
 typedef struct {

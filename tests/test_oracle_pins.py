@@ -486,3 +486,98 @@ def test_cache_hand_worked_step():
     assert cache == 0b00011
     np.testing.assert_array_equal(heat, [1, 2, 0, 1, 0])
     assert hits == 1 and gap == 0.0
+
+
+# ---- look-ahead prefetch depth (SPICE, confidence-aware adaptive prefetch) --
+
+def test_lookahead_confidence_is_largest_k_subset_mass():
+    """The confidence of a look-ahead layer is the probability mass on its
+    top-K experts: brute force over every K-subset, the largest subset mass
+    equals it; K = N gives the whole distribution (1)."""
+    rng = np.random.default_rng(21)
+    for trial in range(40):
+        N = int(rng.integers(2, 9))
+        K = int(rng.integers(1, N + 1))
+        d, T, J = 16, 3, 2
+        x = rng.standard_normal((T, d)).astype(np.float32)
+        Ws = [rng.standard_normal((N, d)).astype(np.float32) * 0.3 for _ in range(J)]
+        conf, _, tok, _, _ = oracle.prefetch_depth(x, Ws, None, K, 0.5, 0)
+        for t in range(T):
+            for j in range(J):
+                lg = Ws[j].astype(np.float64) @ x[t].astype(np.float64)
+                p = torch.softmax(torch.from_numpy(lg), 0).numpy()
+                best = max(sum(p[list(c)]) for c in itertools.combinations(range(N), K))
+                assert abs(conf[t, j] - best) < 1e-12
+                if K == N:
+                    assert abs(conf[t, j] - 1.0) < 1e-12
+
+
+def test_lookahead_uniform_prediction_and_ties():
+    """Zero router weights: every expert has probability 1/N, so the
+    confidence is exactly K/N and the predicted set is the K lowest indices.
+    A threshold at or below K/N keeps all J layers; above it only d_min."""
+    N, K, d, T, J = 8, 2, 32, 4, 3
+    x = np.random.default_rng(3).standard_normal((T, d)).astype(np.float32)
+    Ws = [np.zeros((N, d), np.float32) for _ in range(J)]
+    conf, depth, tok, lay, _ = oracle.prefetch_depth(x, Ws, None, K, 0.25, 0)
+    np.testing.assert_array_equal(conf, np.full((T, J), 0.25))
+    np.testing.assert_array_equal(depth, np.full(T, J))
+    np.testing.assert_array_equal(tok, np.full((T, J), 0b11, np.uint64))
+    for d_min, expect in ((0, 0), (2, 2), (5, J)):
+        conf, depth, tok, lay, _ = oracle.prefetch_depth(x, Ws, None, K, 0.2500001, d_min)
+        np.testing.assert_array_equal(depth, np.full(T, expect))
+        for j in range(J):
+            assert lay[j] == (0b11 if j < expect else 0)
+
+
+def test_lookahead_hand_worked_stop_at_first_low_layer():
+    """N = 4, K = 1, zero weights, the bias sets each look-ahead layer's top
+    probability: 0.95, 0.92, 0.50, 0.99.  At tau = 0.9 the scan keeps layers
+    0 and 1 and stops at layer 2, so layer 3 (0.99) is not reached: depth 2.
+    d_min raises the depth (3), J caps it (4)."""
+    N, d, J = 4, 8, 4
+    tops = [0.95, 0.92, 0.50, 0.99]
+    biases = []
+    for p in tops:
+        b = np.zeros(N, np.float32)
+        b[1] = math.log(3 * p / (1 - p))  # p = a / (a + 3) for expert 1
+        biases.append(b)
+    x = np.ones((1, d), np.float32)
+    Ws = [np.zeros((N, d), np.float32) for _ in range(J)]
+    for d_min, expect in ((0, 2), (2, 2), (3, 3), (9, 4)):
+        conf, depth, tok, lay, margin = oracle.prefetch_depth(x, Ws, biases, 1, 0.9, d_min)
+        np.testing.assert_allclose(conf[0], tops, rtol=1e-6)
+        assert depth[0] == expect
+        np.testing.assert_array_equal(tok[0], [0b10 if j < expect else 0 for j in range(J)])
+        np.testing.assert_array_equal(lay, tok[0])
+        # the scan read layers 0..2: the nearest to tau is 0.92
+        assert abs(margin[0] - 0.02) < 1e-6
+
+
+def test_lookahead_depth_monotone_in_tau_and_masks_are_top_k():
+    """A higher threshold never deepens the prefetch; a kept layer's token
+    mask is the top-K of its logits; the layer mask is the OR over tokens."""
+    rng = np.random.default_rng(5)
+    N, K, d, T, J = 16, 4, 64, 12, 4
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    Ws = [(rng.standard_normal((N, d)) * 0.25).astype(np.float32) for _ in range(J)]
+    prev = None
+    for tau in (0.0, 0.3, 0.5, 0.7, 0.9, 1.01):
+        conf, depth, tok, lay, _ = oracle.prefetch_depth(x, Ws, None, K, tau, 1)
+        if prev is not None:
+            assert (depth <= prev).all()
+        prev = depth
+        for t in range(T):
+            for j in range(J):
+                if j < depth[t]:
+                    lg = Ws[j].astype(np.float64) @ x[t].astype(np.float64)
+                    top = sorted(range(N), key=lambda e: (-lg[e], e))[:K]
+                    assert tok[t, j] == sum(1 << e for e in top)
+                else:
+                    assert tok[t, j] == 0
+        for j in range(J):
+            acc = 0
+            for t in range(T):
+                acc |= int(tok[t, j])
+            assert int(lay[j]) == acc
+    assert (prev == 1).all()  # tau above 1: nothing passes, d_min = 1 remains
