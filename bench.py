@@ -15,6 +15,11 @@ Other workloads (--workload): the Granite, Mixtral (dense and FloE 10 %) and
 Qwen2-57B shapes, and dsv2lite-cache-decode-T1: one-token decode steps over a
 persistent expert cache (capacity 24, heat decay 0.99) that moe_cache_update
 refreshes every step; its line adds the cache's hit rate and admitted experts.
+dsv2lite-lookahead-decode-T8: every 8-token step also runs SPICE's
+confidence-aware look-ahead over the next 4 layers of a synthetic stack
+(moe_prefetch_depth, tau 0.3, d_min 1); its line adds the depth histogram, the
+look-ahead call's time and how many of the next layer's routed slots the
+prediction covered.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
         [--workload NAME]
@@ -39,7 +44,7 @@ sys.path.insert(0, ROOT)
 
 import numpy as np  # noqa: E402
 
-from workloads import CONFIGS, make_tokens, make_weights  # noqa: E402
+from workloads import CONFIGS, make_lookahead_routers, make_tokens, make_weights  # noqa: E402
 
 # name -> (layer config, tokens per step, phase[, FloE keep fraction])
 WORKLOADS = {
@@ -54,12 +59,19 @@ WORKLOADS = {
     "mixtral-floe10-decode-T8": ("mixtral", 8, "decode", 0.1),
     "qwen2-prefill-T4096": ("qwen2", 4096, "prefill"),
     "dsv2lite-cache-decode-T1": ("dsv2lite", 1, "decode"),
+    "dsv2lite-lookahead-decode-T8": ("dsv2lite", 8, "decode"),
 }
 # Multi-step decode with a persistent expert cache (ELMoE-3D heat map with
 # decay): the layer runs every step with resident = the cache, which
 # moe_cache_update then refreshes from the step's routed experts.
 # name -> (cache capacity, heat decay, distinct one-token steps replayed)
 CACHE_WORKLOADS = {"dsv2lite-cache-decode-T1": (24, 0.99, 64)}
+# Decode with SPICE's confidence-aware look-ahead: every step also predicts
+# the expert sets of the next J layers from the step's hidden state
+# (moe_prefetch_depth over the synthetic stack's look-ahead routers).
+# name -> (look-ahead layers J, confidence threshold tau, minimum depth d_min)
+LOOKAHEAD_WORKLOADS = {"dsv2lite-lookahead-decode-T8": (4, 0.3, 1)}
+PCIE4_X16_BYTES_PER_S = 32e9  # the host link of the pages' offloading setups
 DEFAULT_WORKLOAD = "dsv2lite-decode-T8"
 METRIC = "MoE-layer tokens/sec (decode & prefill) and % of HBM/tensor roofline, 1xGB300"
 FALLBACK_HBM_GBS = 6800.0
@@ -313,9 +325,28 @@ def main():
         for L in layers:
             L.resident = cache_t
 
+    la_cfg = LOOKAHEAD_WORKLOADS.get(wl_name)
+    if la_cfg:
+        la_J, la_tau, la_dmin = la_cfg
+        la_W, la_b = make_lookahead_routers(cfg, la_J)
+        la_Wd = [torch.from_numpy(w).to(dev).to(base.dt).contiguous() for w in la_W]
+        la_bd = None if la_b is None else [torch.from_numpy(b).to(dev) for b in la_b]
+        la_logits = torch.zeros((la_J, T, cfg.N), dtype=torch.float32, device=dev)
+        la_conf = torch.zeros((T, la_J), dtype=torch.float32, device=dev)
+        la_depth = torch.zeros(T, dtype=torch.int32, device=dev)
+        la_tok = torch.zeros((T, la_J), dtype=torch.int64, device=dev)
+        la_lay = torch.zeros(la_J, dtype=torch.int64, device=dev)
+
+        def lookahead(c, x):
+            moe.moe_prefetch_depth(layers[c].dims.with_T(T), x, la_Wd, la_bd, la_tau, la_dmin, la_logits, la_conf,
+                                   la_depth, la_tok, la_lay, layers[c].ws, stream)
+
     def step(i):
         c = i % n_copies
-        if cache_cfg:
+        if la_cfg:
+            forward(layers[c], bufs[c], xs[c], stream=stream)
+            lookahead(c, xs[c])
+        elif cache_cfg:
             forward(layers[c], bufs[c], xs[i % n_x], stream=stream, n_resident=0)
             moe.moe_cache_update(layers[c].dims.with_T(T), bufs[c].topk_idx, decay, capacity, heat_t, cache_t,
                                  admit_t, cstats_t, stream)
@@ -452,6 +483,58 @@ def main():
                               "loop also stages every admitted expert from pinned host memory before the "
                               "next step"}
 
+    # ---- the look-ahead step alone, and what it predicted
+    la_info = None
+    if la_cfg:
+        g_la = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_la, stream=stream):
+            lookahead(0, xs[0])
+        n_la = 200
+        la_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        torch.cuda.synchronize()
+        la_ev[0].record(stream)
+        for _ in range(n_la):
+            g_la.replay()
+        la_ev[1].record(stream)
+        torch.cuda.synchronize()
+        la_us = la_ev[0].elapsed_time(la_ev[1]) * 1e3 / n_la
+        # prediction quality over the distinct batches: the next layer's actual
+        # routed sets (its router on x + this layer's output, through the same
+        # entry point with tau = 0, one look-ahead layer) against the experts
+        # predicted for it
+        depths, confs, covered, routed_slots, staged = [], [], 0, 0, np.zeros(la_J)
+        nxt_tok = torch.zeros((T, 1), dtype=torch.int64, device=dev)
+        nxt_lay = torch.zeros(1, dtype=torch.int64, device=dev)
+        nxt_logits = torch.zeros((1, T, cfg.N), dtype=torch.float32, device=dev)
+        nxt_conf = torch.zeros((T, 1), dtype=torch.float32, device=dev)
+        nxt_depth = torch.zeros(T, dtype=torch.int32, device=dev)
+        for c in range(n_copies):
+            forward(layers[c], bufs[c], xs[c], stream=stream)
+            lookahead(c, xs[c])
+            h1 = (xs[c].float() + bufs[c].out).to(base.dt).contiguous()
+            moe.moe_prefetch_depth(layers[c].dims.with_T(T), h1, la_Wd[:1],
+                                   None if la_bd is None else la_bd[:1], 0.0, 0, nxt_logits, nxt_conf, nxt_depth,
+                                   nxt_tok, nxt_lay, layers[c].ws, stream)
+            torch.cuda.synchronize()
+            depths += la_depth.cpu().tolist()
+            confs.append(la_conf.double().cpu().numpy())
+            pred = int(la_lay[0].item()) & ((1 << 64) - 1)
+            for t in range(T):
+                actual = int(nxt_tok[t, 0].item()) & ((1 << 64) - 1)
+                covered += bin(actual & pred).count("1")
+                routed_slots += cfg.k
+            staged += [bin(int(v) & ((1 << 64) - 1)).count("1") for v in la_lay.cpu().tolist()]
+        la_info = {"look_ahead_layers": la_J, "tau": la_tau, "d_min": la_dmin,
+                   "us_per_call": la_us, "launches_per_call": la_J + 1,
+                   "mean_depth": float(np.mean(depths)),
+                   "depth_histogram": np.bincount(np.asarray(depths), minlength=la_J + 1).tolist(),
+                   "mean_confidence_per_layer": np.concatenate(confs).mean(axis=0).round(4).tolist(),
+                   "experts_to_stage_per_layer": (staged / n_copies).round(2).tolist(),
+                   "next_layer_coverage": covered / routed_slots,
+                   "note": "draft head = the look-ahead routers on the current hidden state; coverage = "
+                           "routed slots of the next layer (its router on x + this layer's output) whose "
+                           "expert was predicted for it"}
+
     # ---- end to end through the public API: pinned host x -> device, layer
     # forward, result -> pinned host, every step
     x_host = [xs[c].cpu().pin_memory() for c in range(n_x)]
@@ -472,7 +555,10 @@ def main():
         c = i % n_copies
         xc = xs[i % n_x]
         xc.copy_(x_host[i % n_x], non_blocking=True)
-        if cache_cfg:
+        if la_cfg:
+            forward(layers[c], bufs[c], xc, stream=stream)
+            lookahead(c, xc)
+        elif cache_cfg:
             forward(layers[c], bufs[c], xc, stream=stream, n_resident=0)
             moe.moe_cache_update(layers[c].dims.with_T(T), bufs[c].topk_idx, decay, capacity, heat_t, cache_t,
                                  admit_t, None, stream)
@@ -556,6 +642,17 @@ def main():
         "routing": routing,
         "clocks": clocks,
     }
+    if la_info:
+        # SPICE's minimum depth for one expert of this layer, at the measured
+        # layer step time, over a PCIe 4.0 x16 link and over this box's
+        # measured host link
+        step_s = ms_per_step / 1e3
+        la_info["d_min_formula"] = {
+            "expert_bytes": expert_bytes, "layer_us": ms_per_step * 1e3,
+            "pcie4_x16": moe.moe_prefetch_min_depth(expert_bytes, PCIE4_X16_BYTES_PER_S, step_s),
+            "measured_host_link": moe.moe_prefetch_min_depth(expert_bytes, staging["gbps"] * 1e9, step_s)}
+        line["lookahead"] = la_info
+        line["config"]["lookahead"] = f"{la_J} layers, tau {la_tau}, d_min {la_dmin}"
     if cache_info:
         line["config"]["resident"] = f"expert cache of {capacity} (heat decay {decay})"
         line["e2e"]["h2d_bytes_per_step"] += cache_info["e2e_staged_bytes_per_step"]

@@ -95,6 +95,9 @@ _PROTOS = {
     "moe_expert_ffn_noalloc": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P], C.c_int),
     "moe_lore": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P], C.c_int),
     "moe_combine": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P], C.c_int),
+    "moe_prefetch_depth": ([_DIMS, C.c_int, _P, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_float, C.c_int,
+                            _P, _P, _P, _P, _P, _P, _SZ, _P], C.c_int),
+    "moe_prefetch_min_depth": ([C.c_double, C.c_double, C.c_double], C.c_int),
     "moe_cache_update": ([_DIMS, _P, C.c_float, C.c_int, _P, _P, _P, _P, _P], C.c_int),
     "moe_layer_forward": ([_DIMS, C.POINTER(moe_layer_args), C.POINTER(moe_layer_outputs), _P, _SZ,
                            _P], C.c_int),
@@ -245,6 +248,39 @@ def moe_select_resident(dims, router_prob, topk_idx, prefetch_mask, resident, po
         _ptr(fetch_mask, torch.int64, 1, "fetch_mask", True),
         _ptr(counters, torch.int32, MOE_NUM_COUNTERS, "counters", True),
         _ptr(ws, torch.uint8, name="ws"), ws.numel(), _stream(stream)), "moe_select_resident")
+
+
+def moe_prefetch_depth(dims, x, w_routers, biases, tau, d_min, logits, conf, depth, token_masks, layer_masks,
+                       ws, stream=None):
+    """Confidence-aware prefetch depth over len(w_routers) look-ahead layers
+    (SPICE, confidence-aware adaptive prefetch).  w_routers: device tensors
+    [N, d] in the layer's weight type; biases: None or a sequence of [N]
+    float32 tensors / None.  Outputs: logits [J, T, N] float32, conf [T, J]
+    float32, depth [T] int32, token_masks [T, J] and layer_masks [J] int64
+    (uint64 bit patterns)."""
+    T, d, N = dims.T, dims.d, dims.N
+    J = len(w_routers)
+    wt = wdtype(dims)
+    warr = (C.c_void_p * J)(*[_ptr(w, wt, N * d, f"w_routers[{j}]").value for j, w in enumerate(w_routers)])
+    barr = None
+    if biases is not None:
+        barr = (C.c_void_p * J)(*[(_ptr(b, torch.float32, N, f"biases[{j}]", True) or C.c_void_p()).value
+                                  for j, b in enumerate(biases)])
+    _check(lib().moe_prefetch_depth(
+        C.byref(dims), J, _ptr(x, wt, T * d, "x", T == 0), warr, barr, float(tau), int(d_min),
+        _ptr(logits, torch.float32, J * T * N, "logits", T == 0), _ptr(conf, torch.float32, T * J, "conf", T == 0),
+        _ptr(depth, torch.int32, T, "depth", T == 0), _ptr(token_masks, torch.int64, T * J, "token_masks", T == 0),
+        _ptr(layer_masks, torch.int64, J, "layer_masks"), _ptr(ws, torch.uint8, name="ws"), ws.numel(),
+        _stream(stream)), "moe_prefetch_depth")
+
+
+def moe_prefetch_min_depth(expert_bytes: float, link_bytes_per_s: float, layer_seconds: float) -> int:
+    """ceil(expert_bytes / (link bandwidth * layer time)) (SPICE's minimum
+    prefetch depth); host only."""
+    v = lib().moe_prefetch_min_depth(float(expert_bytes), float(link_bytes_per_s), float(layer_seconds))
+    if v < 0:
+        raise ValueError("moe_prefetch_min_depth: bad size, bandwidth or layer time")
+    return int(v)
 
 
 def moe_stage_experts(dims, host_fetch_mask: int, host_w_gate, host_w_up, host_w_down,

@@ -194,6 +194,13 @@ cudaError_t launch_layer_epilogue(const EpilogueArgs& a, cudaStream_t st);
 cudaError_t launch_wait_timeout_probe(DevError* err, cudaStream_t st);
 
 // persistent expert cache, one decode step (cache.cu)
+// confidence-aware look-ahead prefetch depth (lookahead.cu)
+constexpr int kMaxAhead = MOE_MAX_AHEAD;
+cudaError_t launch_lookahead_logits(const void* x, const void* const* w, const float* const* b, int J, int T, int d,
+                                    int N, bool bf16, float* logits, uint64_t* layer_masks, cudaStream_t st);
+cudaError_t launch_prefetch_depth(const float* logits, int T, int N, int K, int J, float tau, int d_min,
+                                  float* conf, int32_t* depth, uint64_t* tok_masks, uint64_t* layer_masks,
+                                  cudaStream_t st);
 cudaError_t launch_cache_update(const int32_t* topk_idx, int n_slots, int N, float decay, int capacity, float* heat,
                                 uint64_t* cache, uint64_t* admit, int32_t* stats, cudaStream_t st);
 

@@ -587,6 +587,59 @@ moe_status moe_cache_update(const moe_dims* dims, const int32_t* topk_idx, float
     return MOE_OK;
 }
 
+moe_status moe_prefetch_depth(const moe_dims* dims, int n_ahead, const void* x,
+                              const void* const* w_router_ahead, const float* const* bias_ahead, float tau,
+                              int d_min, float* logits_ahead, float* conf, int32_t* depth,
+                              uint64_t* token_masks, uint64_t* layer_masks, void* ws, size_t ws_bytes,
+                              void* stream) {
+    MOE_TRY(check_dims(dims));
+    MOE_TRY(check_ws(dims, ws, ws_bytes));
+    if (n_ahead < 1 || n_ahead > MOE_MAX_AHEAD || d_min < 0 || !std::isfinite(tau)) return MOE_ERR_INVALID_ARG;
+    if (!w_router_ahead || !layer_masks) return MOE_ERR_INVALID_ARG;
+    for (int j = 0; j < n_ahead; ++j)
+        if (!w_router_ahead[j] || !aligned16(w_router_ahead[j])) return MOE_ERR_INVALID_ARG;
+    if (dims->T > 0 && (!x || !aligned16(x) || !logits_ahead || !conf || !depth || !token_masks))
+        return MOE_ERR_INVALID_ARG;
+    if (dims->T == 0 || dims->T > kTcMinTokens)
+        MOE_CUDA(cudaMemsetAsync(layer_masks, 0, (size_t)n_ahead * sizeof(uint64_t), S(stream)));
+    if (dims->T == 0) return MOE_OK;
+    const WsLayout L = ws_layout(*dims);
+    const size_t plane = (size_t)dims->T * dims->N;
+    if (dims->T <= kTcMinTokens) {
+        // decode-size batch: every look-ahead router in one launch (which
+        // also zeroes the layer masks)
+        MOE_CUDA(launch_lookahead_logits(x, w_router_ahead, bias_ahead, n_ahead, dims->T, dims->d, dims->N,
+                                         bf16(dims), logits_ahead, layer_masks, S(stream)));
+        count();
+    }
+    for (int j = 0; j < n_ahead && dims->T > kTcMinTokens; ++j) {
+        // look-ahead layer j's router on the current hidden state, through the
+        // router GEMM paths (no prefetch router)
+        LogitsArgs la;
+        la.x = x; la.x_pre = nullptr; la.w_router = w_router_ahead[j]; la.w_prefetch = nullptr;
+        la.bias = bias_ahead ? bias_ahead[j] : nullptr; la.w_ord = nullptr;
+        la.T = dims->T; la.d = dims->d; la.N = dims->N; la.has_prefetch = 0; la.bf16 = bf16(dims);
+        la.logits_r = logits_ahead + (size_t)j * plane;
+        la.logits_p = ws_at<float>(ws, L.logits_p); la.score = ws_at<float>(ws, L.score);
+        la.part = ws_at<float>(ws, L.route_part); la.sms = sm_count(); la.err = ws_at<DevError>(ws, L.err);
+        MOE_CUDA(launch_logits(la, S(stream)));
+        count();
+    }
+    MOE_CUDA(launch_prefetch_depth(logits_ahead, dims->T, dims->N, dims->k, n_ahead, tau, d_min, conf, depth,
+                                   token_masks, layer_masks, S(stream)));
+    count();
+    return MOE_OK;
+}
+
+int moe_prefetch_min_depth(double expert_bytes, double link_bytes_per_s, double layer_seconds) {
+    if (!(expert_bytes >= 0.0) || !(link_bytes_per_s > 0.0) || !(layer_seconds > 0.0)) return -1;
+    const double q = expert_bytes / (link_bytes_per_s * layer_seconds);
+    if (!(q <= 2147483647.0)) return -1;
+    const double r = std::nearbyint(q);
+    if (std::fabs(q - r) <= 1e-9 * std::fmax(1.0, r)) return (int)r;
+    return (int)std::ceil(q);
+}
+
 moe_status moe_combine(const moe_dims* dims, const float* y_perm, const int32_t* inv_perm,
                        const float* final_gate, const int32_t* final_kind, const float* y_shared,
                        const float* y_lore, float* out, void* stream) {

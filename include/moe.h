@@ -286,6 +286,47 @@ moe_status moe_lore(const moe_dims* dims, const void* x, const int32_t* final_id
                     const int32_t* final_kind, const float* final_gate, const void* lore_a,
                     const void* lore_b, float* y_lore, void* ws, size_t ws_bytes, void* stream);
 
+/* Look-ahead layers handled by one moe_prefetch_depth call, at most. */
+#define MOE_MAX_AHEAD 16
+
+/* Confidence-aware prefetch depth (beyond the single layer forward; SPICE
+ * write-up, section on confidence-aware adaptive prefetch).  A draft predicts
+ * the expert distribution of each of the next n_ahead layers from the current
+ * hidden state x; the draft head is the identity here (look-ahead layer j's
+ * router applied to x).  For every token t and look-ahead layer j:
+ *   logits_ahead[j][t][e] = x_t . w_router_ahead[j][e] (+ bias_ahead[j][e])
+ *   conf[t][j]  = the probability mass (softmax over the N logits) on the
+ *                 top-k experts (k = dims->k; largest logits, lower index on
+ *                 ties)
+ *   depth[t]    = min(n_ahead, max(d_min, c)), c = the number of leading
+ *                 layers j = 0, 1, ... with conf >= tau (the scan stops at the
+ *                 first layer below tau)
+ *   token_masks[t][j] = the top-k set of layer j if j < depth[t], else 0
+ *   layer_masks[j]    = OR over tokens of token_masks[t][j]: the experts to
+ *                 stage for look-ahead layer j.
+ * x [T, d] and each w_router_ahead[j] [N, d] in the layer's weight type,
+ * 16-byte aligned; bias_ahead NULL or an array of n_ahead device pointers
+ * ([N] float32, entries may be NULL); w_router_ahead and bias_ahead are HOST
+ * arrays of device pointers.  logits_ahead [n_ahead, T, N] float32, conf
+ * [T, n_ahead] float32, depth [T] int32, token_masks [T, n_ahead] and
+ * layer_masks [n_ahead] uint64: device, written.  d_min comes from
+ * moe_prefetch_min_depth.  Errors: INVALID_ARG (n_ahead outside
+ * 1..MOE_MAX_AHEAD, d_min < 0, tau not finite, a NULL or misaligned buffer),
+ * UNSUPPORTED (N > 64).  Asynchronous. */
+moe_status moe_prefetch_depth(const moe_dims* dims, int n_ahead, const void* x,
+                              const void* const* w_router_ahead, const float* const* bias_ahead, float tau,
+                              int d_min, float* logits_ahead, float* conf, int32_t* depth,
+                              uint64_t* token_masks, uint64_t* layer_masks, void* ws, size_t ws_bytes,
+                              void* stream);
+
+/* The minimum prefetch depth (SPICE write-up, same section):
+ * ceil(expert_bytes / (link_bytes_per_s * layer_seconds)), the layers a
+ * transfer of one expert must start ahead so that it lands before its layer
+ * runs.  A quotient within 1e-9 (relative) of an integer counts as that
+ * integer.  Host only, no device work; -1 for a negative size, a
+ * non-positive bandwidth or layer time, or a depth above INT32_MAX. */
+int moe_prefetch_min_depth(double expert_bytes, double link_bytes_per_s, double layer_seconds);
+
 /* Persistent expert cache across decode steps (beyond the single layer
  * forward; ELMoE-3D, expert-axis elasticity: heat statistics of the experts
  * the routing function selects, the most frequently activated top-K kept

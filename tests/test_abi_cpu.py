@@ -169,3 +169,42 @@ def _dims(name, T):
 ])
 def test_expert_ffn_path_choice(name, T, keep, path):
     assert moe.moe_expert_ffn_path(_dims(name, T), keep) == path
+
+
+def test_prefetch_min_depth_closed_form():
+    """SPICE's minimum prefetch depth ceil(W_e / (B * T_layer)), on values
+    whose quotients are exact in binary floating point."""
+    f = moe.moe_prefetch_min_depth
+    assert f(2.0 ** 31, 2.0 ** 30, 0.5) == 4          # exactly 4
+    assert f(2.0 ** 31 + 2.0 ** 12, 2.0 ** 30, 0.5) == 5  # 4 + 2^-17: above 4
+    assert f(0.0, 1e9, 1e-3) == 0
+    assert f(3 * 17_301_504 * 2 / 2, 32e9, 1e-3) == 2  # 51.9 MB over 32 GB/s in 1 ms: 1.62 -> 2
+    # a quotient one rounding away from an integer counts as that integer
+    assert f(64e6, 32e9, 2e-3) == 1
+    for bad in ((-1.0, 1e9, 1e-3), (1.0, 0.0, 1e-3), (1.0, 1e9, 0.0), (1e30, 1.0, 1e-9)):
+        with pytest.raises(ValueError):
+            f(*bad)
+
+
+def test_prefetch_depth_rejects_bad_arguments_before_cuda():
+    """n_ahead outside 1..MOE_MAX_AHEAD, a negative d_min, a non-finite tau or
+    a missing router are argument errors found before any CUDA call."""
+    L = moe.lib()
+    D = _raw_dims(T=4, d=256, N=8, k=2, I=64)
+    n = moe.moe_workspace_size(D)
+    fake_ws = C.c_void_p(1 << 20)
+    x = C.c_void_p(0x1000)
+    w = (C.c_void_p * 17)(*([0x2000] * 17))
+    out = C.c_void_p(0x3000)
+    call = lambda J, tau, d_min, warr=w, xx=x: L.moe_prefetch_depth(
+        C.byref(D), J, xx, warr, None, C.c_float(tau), d_min, out, out, out, out, out, fake_ws, n, None)
+    assert call(0, 0.9, 0) == moe.MOE_ERR_INVALID_ARG
+    assert call(17, 0.9, 0) == moe.MOE_ERR_INVALID_ARG
+    assert call(2, 0.9, -1) == moe.MOE_ERR_INVALID_ARG
+    assert call(2, float("nan"), 0) == moe.MOE_ERR_INVALID_ARG
+    assert call(2, 0.9, 0, warr=(C.c_void_p * 2)(0x2000, None)) == moe.MOE_ERR_INVALID_ARG
+    assert call(2, 0.9, 0, warr=(C.c_void_p * 2)(0x2000, 0x2004)) == moe.MOE_ERR_INVALID_ARG
+    assert call(2, 0.9, 0, xx=None) == moe.MOE_ERR_INVALID_ARG
+    D64 = _raw_dims(T=4, d=256, N=65, k=2, I=64)
+    assert L.moe_prefetch_depth(C.byref(D64), 2, x, w, None, C.c_float(0.9), 0, out, out, out, out, out,
+                                fake_ws, n, None) == moe.MOE_ERR_UNSUPPORTED

@@ -35,6 +35,7 @@ ALL_RESIDENT = (1 << 64) - 1
 # Stream ids for the per-matrix generators.
 _S_ROUTER, _S_PREF_NOISE, _S_WORD, _S_THETA, _S_GATE, _S_UP, _S_DOWN = 1, 2, 3, 4, 5, 6, 7
 _S_SH_GATE, _S_SH_UP, _S_SH_DOWN, _S_LORE_A, _S_LORE_B, _S_BIAS, _S_X = 8, 9, 10, 11, 12, 13, 14
+_S_AHEAD = 15
 
 
 @dataclass(frozen=True)
@@ -238,6 +239,30 @@ def make_tokens(cfg: LayerConfig, T: int | None = None, seed: int | None = None,
     T = cfg.T if T is None else T
     x = _normal(seed, (_S_X, batch), (T, cfg.d), 1.0)
     return round_bf16(x) if cfg.wtype == "bf16" else x
+
+
+def make_lookahead_routers(cfg: LayerConfig, J: int, seed: int | None = None):
+    """Routers of the next J layers of a synthetic layer stack, for the
+    look-ahead prefetch depth: look-ahead layer j's router mixes this layer's
+    router with seeded N(0, 0.02^2) noise at constant norm, the noise share
+    a_j = min(0.9, 0.3 (j + 1)), and is scaled by 1.5 / (1 + j / 2), so the
+    predicted distributions drift and flatten with depth (bf16-exact for bf16
+    layers).  A Zipf router bias, when the layer has one, is shared by every
+    layer.  Returns (routers [J] of [N, d], biases [J] of [N] or None)."""
+    seed = cfg.seed if seed is None else seed
+    base = _normal(seed, (_S_ROUTER,), (cfg.N, cfg.d), 0.02)
+    Ws = []
+    for j in range(J):
+        a = min(0.9, 0.3 * (j + 1))
+        noise = _normal(seed, (_S_AHEAD, j), (cfg.N, cfg.d), 0.02)
+        w = (np.float32(math.sqrt(1.0 - a * a)) * base + np.float32(a) * noise) * np.float32(1.5 / (1.0 + 0.5 * j))
+        Ws.append(round_bf16(w) if cfg.wtype == "bf16" else np.ascontiguousarray(w, np.float32))
+    biases = None
+    if cfg.zipf > 0:
+        perm = _rng(seed, _S_BIAS).permutation(cfg.N)
+        b = (-cfg.zipf * np.log(perm.astype(np.float64) + 1.0)).astype(np.float32)
+        biases = [b] * J
+    return Ws, biases
 
 
 @lru_cache(maxsize=4)
