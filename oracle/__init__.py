@@ -101,6 +101,13 @@ def lib():
                                              C.POINTER(_FP), C.POINTER(_FP), C.c_double, C.c_int, _DP, _IP,
                                              C.POINTER(C.c_uint64), C.POINTER(C.c_uint64), _DP]
             L.orc_prefetch_depth.restype = None
+            _BP = C.POINTER(C.c_byte)
+            L.orc_bitslice_quantize.argtypes = [C.c_int, C.c_int, _FP, C.c_int, _BP, _FP]
+            L.orc_bitslice_quantize.restype = None
+            L.orc_bitslice_value.argtypes = [C.c_int, C.c_int]
+            L.orc_bitslice_value.restype = C.c_int
+            L.orc_bitslice_ffn.argtypes = [C.c_int, C.c_int, C.c_int, _FP, _BP, _FP, _BP, _FP, _BP, _FP, _DP]
+            L.orc_bitslice_ffn.restype = None
             L.orc_layer_forward.argtypes = [C.POINTER(_Cfg), C.POINTER(_Inputs), C.POINTER(_Outputs)]
             _lib = L
     return _lib
@@ -252,6 +259,38 @@ def prefetch_depth(x, Ws, biases, K, tau, d_min):
                              lay.ctypes.data_as(C.POINTER(C.c_uint64)), _d(margin))
     del keep
     return conf, depth.astype(np.int64), tok, lay, margin
+
+
+def bitslice_quantize(W, transpose=False):
+    """Symmetric per-row INT8 quantisation of W (or W^T) in float32
+    arithmetic, for the bit-sliced weights (ELMoE-3D).  Returns (q int8
+    [R, C], scale float32 [R])."""
+    Wf = f32(W)
+    rows, cols = Wf.shape
+    R, Cc = (cols, rows) if transpose else (rows, cols)
+    q = np.zeros((R, Cc), np.int8)
+    sc = np.zeros(R, np.float32)
+    lib().orc_bitslice_quantize(rows, cols, _f(Wf), int(bool(transpose)), q.ctypes.data_as(C.POINTER(C.c_byte)),
+                                sc.ctypes.data_as(_FP))
+    return q, sc
+
+
+def bitslice_value(q: int, b: int) -> int:
+    """The b-bit value of INT8 weight q: its top b bit planes recombined."""
+    return int(lib().orc_bitslice_value(int(q), int(b)))
+
+
+def bitslice_ffn(x, qg, sg, qu, su, qdT, sd, b):
+    """One expert on one token with b-bit weights: y [d] float64."""
+    x = f32(np.asarray(x).ravel())
+    I, d = qg.shape
+    y = np.zeros(d, np.float64)
+    bp = C.POINTER(C.c_byte)
+    cont = lambda a: np.ascontiguousarray(a, np.int8)
+    qg, qu, qdT = cont(qg), cont(qu), cont(qdT)
+    lib().orc_bitslice_ffn(d, I, int(b), _f(x), qg.ctypes.data_as(bp), _f(f32(sg)), qu.ctypes.data_as(bp),
+                           _f(f32(su)), qdT.ctypes.data_as(bp), _f(f32(sd)), _d(y))
+    return y
 
 
 # ---- whole layer ---------------------------------------------------------

@@ -26,6 +26,9 @@
  *   - look-ahead prefetch depth       : SPICE write-up, confidence-aware
  *     adaptive prefetch (top-K mass confidence, stop below the threshold,
  *     minimum depth).
+ *   - bit-sliced expert weights       : ELMoE-3D (CSDN post), bit-slicing
+ *     section (INT8 bit planes, top-b planes combined, shared scale) and the
+ *     layout note (an expert's planes stored contiguously).
  *   - persistent expert cache         : ELMoE-3D (CSDN post), expert-axis
  *     elasticity: heat statistics, top-K subset, dynamic update, and the
  *     practice note on heat decay (multiply every heat by a factor just
@@ -372,6 +375,84 @@ void orc_prefetch_depth(int T, int d, int N, int K, int J, const float* x, const
         if (margin) margin[t] = m;
     }
     free(l); free(p); free(idx);
+}
+
+/* Bit-sliced expert weights (ELMoE-3D, CSDN post, bit-slicing section and
+ * the data-layout note): each weight is an INT8 value with a scale shared
+ * across precisions; its 8 bits are stored as 8 binary planes, and a b-bit
+ * representation combines the top b planes (MSB-only: the lower planes are
+ * dropped; the learned LSB-enhancement scale is not used).
+ * Quantisation (the pages leave it open; symmetric per output row): for row
+ * r of the matrix the kernel reads (W itself, or W^T when transpose is set):
+ *   s_r = max_k |W[r,k]| / 127            (float32 arithmetic)
+ *   q[r,k] = clamp(rint(W[r,k] / s_r), -127, 127)   (float32 division,
+ *            round half to even; s_r = 0 gives q = 0)
+ * W is [rows_in, cols_in] row-major; the output is [R, C] with (R, C) =
+ * (rows_in, cols_in), or (cols_in, rows_in) when transpose != 0. */
+void orc_bitslice_quantize(int rows_in, int cols_in, const float* W, int transpose, signed char* q,
+                           float* scale) {
+    const int R = transpose ? cols_in : rows_in, Cc = transpose ? rows_in : cols_in;
+    for (int r = 0; r < R; ++r) {
+        float mx = 0.0f;
+        for (int c = 0; c < Cc; ++c) {
+            const float w = transpose ? W[(size_t)c * cols_in + r] : W[(size_t)r * cols_in + c];
+            const float a = fabsf(w);
+            if (a > mx) mx = a;
+        }
+        const float sr = mx / 127.0f;
+        scale[r] = sr;
+        for (int c = 0; c < Cc; ++c) {
+            const float w = transpose ? W[(size_t)c * cols_in + r] : W[(size_t)r * cols_in + c];
+            int v = 0;
+            if (sr > 0.0f) {
+                const float t = w / sr;
+                v = (int)rintf(t);
+                if (v > 127) v = 127;
+                if (v < -127) v = -127;
+            }
+            q[(size_t)r * Cc + c] = (signed char)v;
+        }
+    }
+}
+
+/* The b-bit value of an INT8 weight: decompose its two's-complement byte
+ * into the 8 bit planes, keep the top b (planes 7 .. 8-b) and recombine them
+ * with their place values (plane 7 carries -128, plane p < 7 carries 2^p). */
+int orc_bitslice_value(int q, int b) {
+    const unsigned byte = (unsigned)(unsigned char)(signed char)q;
+    int v = 0;
+    for (int p = 7; p >= 8 - b && p >= 0; --p) {
+        const int bit = (int)((byte >> p) & 1u);
+        v += bit * (p == 7 ? -128 : (1 << p));
+    }
+    return v;
+}
+
+/* One expert's SwiGLU FFN on one token with b-bit weights (FloE method §1
+ * form of the expert, ELMoE-3D bit-sliced weights):
+ *   g_c = sg[c] sum_k x_k v_b(qg[c,k]),  u_c = su[c] sum_k x_k v_b(qu[c,k])
+ *   h_c = SiLU(g_c) u_c,  y_j = sd[j] sum_c h_c v_b(qdT[j,c])
+ * qg, qu [I, d]; qdT [d, I] (the down projection quantised per output j). */
+void orc_bitslice_ffn(int d, int I, int b, const float* x, const signed char* qg, const float* sg,
+                      const signed char* qu, const float* su, const signed char* qdT, const float* sd,
+                      double* y) {
+    double* h = (double*)malloc(sizeof(double) * (size_t)I);
+    for (int c = 0; c < I; ++c) {
+        double g = 0.0, u = 0.0;
+        for (int k = 0; k < d; ++k) {
+            g += (double)x[k] * (double)orc_bitslice_value(qg[(size_t)c * d + k], b);
+            u += (double)x[k] * (double)orc_bitslice_value(qu[(size_t)c * d + k], b);
+        }
+        g *= (double)sg[c];
+        u *= (double)su[c];
+        h[c] = g / (1.0 + exp(-g)) * u;
+    }
+    for (int j = 0; j < d; ++j) {
+        double acc = 0.0;
+        for (int c = 0; c < I; ++c) acc += h[c] * (double)orc_bitslice_value(qdT[(size_t)j * I + c], b);
+        y[j] = acc * (double)sd[j];
+    }
+    free(h);
 }
 
 typedef struct {

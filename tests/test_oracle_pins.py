@@ -581,3 +581,62 @@ def test_lookahead_depth_monotone_in_tau_and_masks_are_top_k():
                 acc |= int(tok[t, j])
             assert int(lay[j]) == acc
     assert (prev == 1).all()  # tau above 1: nothing passes, d_min = 1 remains
+
+
+# ---- bit-sliced expert weights (ELMoE-3D, bit slicing) ----------------------
+
+def test_bitslice_top_planes_are_floor_truncation():
+    """Every INT8 value and every precision: recombining the top b bit planes
+    (plane 7 weighted -128) equals flooring the value to a multiple of
+    2^(8-b) (an arithmetic right shift then a left shift); b = 8 gives the
+    value itself."""
+    for q in range(-128, 128):
+        assert oracle.bitslice_value(q, 8) == q
+        for b in range(1, 9):
+            assert oracle.bitslice_value(q, b) == (q >> (8 - b)) << (8 - b), (q, b)
+
+
+def test_bitslice_quantisation_bound_and_layout():
+    """Per output row: the largest |q| is 127 on a nonzero row, every weight is
+    within half a step of s*q, a zero row gives s = 0 and q = 0, and the
+    transposed quantisation is the quantisation of W^T."""
+    rng = np.random.default_rng(8)
+    W = (rng.standard_normal((24, 96)) * 0.02).astype(np.float32)
+    W[5] = 0.0
+    q, s = oracle.bitslice_quantize(W)
+    assert q.shape == (24, 96) and s.shape == (24,)
+    for r in range(24):
+        if r == 5:
+            assert s[r] == 0.0 and (q[r] == 0).all()
+            continue
+        assert np.abs(q[r].astype(int)).max() == 127
+        err = np.abs(W[r].astype(np.float64) - float(s[r]) * q[r].astype(np.float64))
+        assert err.max() <= 0.5 * float(s[r]) * (1 + 1e-5)
+    qt, st = oracle.bitslice_quantize(W, transpose=True)
+    q2, s2 = oracle.bitslice_quantize(np.ascontiguousarray(W.T))
+    np.testing.assert_array_equal(qt, q2)
+    np.testing.assert_array_equal(st, s2)
+
+
+def test_bitslice_ffn_full_precision_is_the_dense_expert():
+    """With all 8 planes the bit-sliced expert is the dense SwiGLU expert on
+    the dequantised weights s*q (the dense expert oracle is pinned against
+    torch); fewer planes move the output further from it."""
+    rng = np.random.default_rng(12)
+    d, I = 64, 96
+    x = rng.standard_normal(d).astype(np.float32)
+    Wg, Wu, Wd = [(rng.standard_normal((I, d)) * 0.05).astype(np.float32) for _ in range(3)]
+    qg, sg = oracle.bitslice_quantize(Wg)
+    qu, su = oracle.bitslice_quantize(Wu)
+    qdT, sd = oracle.bitslice_quantize(Wd, transpose=True)   # [d, I]
+    y8 = oracle.bitslice_ffn(x, qg, sg, qu, su, qdT, sd, 8)
+    deq = lambda q, s: (q.astype(np.float64) * s.astype(np.float64)[:, None])
+    Wg8, Wu8 = deq(qg, sg), deq(qu, su)
+    Wd8 = deq(qdT, sd).T                                      # back to [I, d]
+    g, u = Wg8 @ x.astype(np.float64), Wu8 @ x.astype(np.float64)
+    h = g / (1 + np.exp(-g)) * u
+    np.testing.assert_allclose(y8, h @ Wd8, rtol=1e-12, atol=1e-14)
+    dense = oracle.expert_ffn(x, Wg8.astype(np.float32), Wu8.astype(np.float32), Wd8.astype(np.float32))
+    np.testing.assert_allclose(y8, dense, rtol=1e-5, atol=1e-7)
+    errs = [np.linalg.norm(oracle.bitslice_ffn(x, qg, sg, qu, su, qdT, sd, b) - y8) for b in (2, 4, 6)]
+    assert errs[0] > errs[1] > errs[2] > 0
