@@ -60,6 +60,7 @@ WORKLOADS = {
     "qwen2-prefill-T4096": ("qwen2", 4096, "prefill"),
     "dsv2lite-cache-decode-T1": ("dsv2lite", 1, "decode"),
     "dsv2lite-lookahead-decode-T8": ("dsv2lite", 8, "decode"),
+    "dsv2lite-bitslice4-draft-T1": ("dsv2lite", 1, "decode"),
 }
 # Multi-step decode with a persistent expert cache (ELMoE-3D heat map with
 # decay): the layer runs every step with resident = the cache, which
@@ -71,7 +72,11 @@ CACHE_WORKLOADS = {"dsv2lite-cache-decode-T1": (24, 0.99, 64)}
 # (moe_prefetch_depth over the synthetic stack's look-ahead routers).
 # name -> (look-ahead layers J, confidence threshold tau, minimum depth d_min)
 LOOKAHEAD_WORKLOADS = {"dsv2lite-lookahead-decode-T8": (4, 0.3, 1)}
-PCIE4_X16_BYTES_PER_S = 32e9  # the host link of the pages' offloading setups
+PCIE4_X16_BYTES_PER_S = 32e9
+# Draft layer with ELMoE-3D bit-sliced expert weights: per token, the router
+# (bf16) picks the top-k experts, whose FFN (and the shared experts') runs on
+# the top b bit planes of INT8 weights (moe_bitslice_ffn).  name -> b
+BITSLICE_WORKLOADS = {"dsv2lite-bitslice4-draft-T1": 4}  # the host link of the pages' offloading setups
 DEFAULT_WORKLOAD = "dsv2lite-decode-T8"
 METRIC = "MoE-layer tokens/sec (decode & prefill) and % of HBM/tensor roofline, 1xGB300"
 FALLBACK_HBM_GBS = 6800.0
@@ -241,12 +246,64 @@ def cpu_baseline(cfg, W, T, seconds, batch_offset=0):
                       f"CPU oracle, OpenMP over the tokens of a batch"}
 
 
+class BitsliceOracle:
+    """The draft layer of a bit-sliced workload through the float64 oracle:
+    router softmax and top-k, then the gate-weighted b-bit expert FFNs of the
+    routed experts plus the shared experts."""
+
+    def __init__(self, cfg, W, bits):
+        import oracle
+        self.o, self.cfg, self.W, self.bits, self.q = oracle, cfg, W, bits, {}
+
+    def _q(self, key, Wg, Wu, Wd):
+        if key not in self.q:
+            o = self.o
+            self.q[key] = (o.bitslice_quantize(Wg) + o.bitslice_quantize(Wu) + o.bitslice_quantize(Wd, transpose=True))
+        return self.q[key]
+
+    def token(self, x):
+        o, cfg, W = self.o, self.cfg, self.W
+        lg = o.logits(x[None], W.w_router, W.router_bias)[0]
+        p = o.softmax(lg[None])[0]
+        y = np.zeros(cfg.d)
+        for e in o.topk(lg, cfg.k):
+            e = int(e)
+            y += p[e] * o.bitslice_ffn(x, *self._q(("r", e), W.w_gate[e], W.w_up[e], W.w_down[e]), self.bits)
+        for sh in range(cfg.n_shared):
+            y += o.bitslice_ffn(x, *self._q(("s", sh), W.sh_gate[sh], W.sh_up[sh], W.sh_down[sh]), self.bits)
+        return y
+
+
 def run_reference(args, wl_name, cfg, T, world, rank):
     """Reference arm: the float64 oracle timed on the host cores, one batch of
     T tokens per step, for at most about two minutes."""
     if rank != 0:
         return
     import oracle
+    if wl_name in BITSLICE_WORKLOADS:
+        W = make_weights(cfg)
+        bo = BitsliceOracle(cfg, W, BITSLICE_WORKLOADS[wl_name])
+        warm = min(args.warmup, 3)
+        for i in range(warm):
+            bo.token(make_tokens(cfg, T=1, batch=20_000 + i)[0])
+        budget, t0, steps = 120.0, time.perf_counter(), 0
+        while steps < args.steps:
+            bo.token(make_tokens(cfg, T=1, batch=30_000 + steps)[0])
+            steps += 1
+            if time.perf_counter() - t0 > budget:
+                break
+        el = time.perf_counter() - t0
+        value = steps / el
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": steps,
+                "warmup": warm, "ms_per_step": 1e3 * el / steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "impl": "reference", "config": {"workload": wl_name, "tokens_per_step": 1},
+                "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                 "sample": f"{steps} one-token draft steps (of {args.steps} requested; capped "
+                                           f"at {budget:.0f} s), quantisation of the experts included"},
+                "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
     T = min(T, 32)  # a step is a bounded sample of the batch (tokens are independent)
     W = make_weights(cfg)
     warm = min(args.warmup, 3)  # the oracle has no caches to warm beyond a first call
@@ -275,6 +332,175 @@ def run_reference(args, wl_name, cfg, T, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_bitslice(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src):
+    """Timed draft layer with b-bit bit-sliced expert weights (see
+    BITSLICE_WORKLOADS): one step = the bf16 router (moe_route, top-k gates)
+    and one moe_bitslice_ffn call over the routed and the shared experts,
+    over several packed copies of the planes so that the planes one step
+    reads come from HBM."""
+    import torch
+    import expert_routing_ffn_gb300 as moe
+    bits = BITSLICE_WORKLOADS[wl_name]
+    d, I, N, k, ns, Is = cfg.d, cfg.I, cfg.N, cfg.k, cfg.n_shared, cfg.I_shared
+    assert Is == I or ns == 0
+    dt = torch.bfloat16
+    step_bytes = (k + ns) * 3 * I * d * bits / 8
+    n_copies = int(min(8, max(2, math.ceil(1 + 2 * L2_BYTES / step_bytes))))
+    w8 = 8 * I * d // 32
+
+    def pack_set(mats, n):
+        P = [torch.zeros(n * w8, dtype=torch.int32, device=dev) for _ in range(3)]
+        S = [torch.zeros(n * (I if m < 2 else d), dtype=torch.float32, device=dev) for m in range(3)]
+        for e in range(n):
+            for m in range(3):
+                w = torch.from_numpy(mats[m][e]).to(dev).to(dt)
+                R = I if m < 2 else d
+                moe.moe_bitslice_pack(w, m == 2, P[m][e * w8:(e + 1) * w8], S[m][e * R:(e + 1) * R])
+        return P, S
+
+    # the routed experts, then the shared experts, back to back
+    cat = lambda a, b: np.concatenate([a, b]) if ns else a
+    planes = pack_set((cat(W.w_gate, W.sh_gate), cat(W.w_up, W.sh_up), cat(W.w_down, W.sh_down)), N + ns)
+    torch.cuda.synchronize()
+    # further copies of every plane at distinct addresses (the same values)
+    copies = [planes] + [([t.clone() for t in planes[0]], planes[1]) for _ in range(n_copies - 1)]
+    dims = moe.make_dims(T, d, N, k, I, ns, Is, cfg.r, wtype=cfg.wtype)
+    ws = torch.zeros(moe.moe_workspace_size(dims), dtype=torch.uint8, device=dev)
+    w_router = torch.from_numpy(W.w_router).to(dev).to(dt)
+    bias = None if W.router_bias is None else torch.from_numpy(W.router_bias).to(dev)
+    n_x = 64
+    xs = [torch.from_numpy(make_tokens(cfg, T=T, batch=replica_batch(rank, i))).to(dev).to(dt).contiguous()
+          for i in range(n_x)]
+    topk_idx = torch.zeros((T, k), dtype=torch.int32, device=dev)
+    topk_gate = torch.zeros((T, k), dtype=torch.float32, device=dev)
+    prob = torch.zeros((T, N), dtype=torch.float32, device=dev)
+    dhat = torch.zeros(T, dtype=torch.int32, device=dev)
+    pmask = torch.zeros(T, dtype=torch.int64, device=dev)
+    y = torch.zeros((T, d), dtype=torch.float32, device=dev)
+    scratch = torch.zeros(moe.moe_bitslice_scratch_size(d, I, T, k + ns), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
+
+    def ffn(c):
+        P, S = copies[c % n_copies]
+        moe.moe_bitslice_ffn(d, I, N, bits, xs_cur[0], topk_idx, topk_gate, P[0], S[0], P[1], S[1], P[2], S[2], y,
+                             scratch, n_shared=ns, stream=stream)
+
+    xs_cur = [xs[0]]
+
+    def step(i):
+        xs_cur[0] = xs[i % n_x]
+        moe.moe_route(dims, xs_cur[0], w_router, bias, None, None, None, None, cfg.tau, 0, topk_idx, topk_gate,
+                      prob, dhat, pmask, None, None, ws, stream)
+        ffn(i)
+
+    for i in range(max(args.warmup, n_copies)):
+        step(i)
+    st, det = moe.moe_check(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device error {moe.status_string(st)} ({det})")
+    n_graphs = max(n_copies, n_x)
+    graphs = []
+    n0 = moe.moe_launch_total()
+    for c in range(n_graphs):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(c)
+        graphs.append(g)
+    launches_per_step = (moe.moe_launch_total() - n0) // n_graphs
+    for i in range(args.warmup):
+        graphs[i % n_graphs].replay()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index or 0) as clk:
+        ev0.record(stream)
+        for i in range(args.steps):
+            graphs[i % n_graphs].replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms_total = max_over_ranks(world, ev0.elapsed_time(ev1))
+    ms_per_step = ms_total / args.steps
+    value = whole_job_tokens_per_s(world, T, args.steps, ms_total)
+    clocks = clk.summary()
+
+    # the bit-sliced FFN call alone (routing of each token batch in place):
+    # algorithmic bytes = the top-b planes of the distinct routed experts and
+    # the shared experts, plus their scales
+    n_k = max(50, min(2000, args.steps // 2))
+    fb = []
+    for c in range(n_x):
+        step(c)
+        torch.cuda.synchronize()
+        u = len(set(topk_idx.cpu().numpy().ravel().tolist()))
+        fb.append((u + ns) * (3 * I * d * bits / 8 + 4 * (2 * I + d)))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_k)]
+    for i in range(n_k):
+        c = i % n_x
+        xs_cur[0] = xs[c]
+        moe.moe_route(dims, xs[c], w_router, bias, None, None, None, None, cfg.tau, 0, topk_idx, topk_gate,
+                      prob, dhat, pmask, None, None, ws, stream)
+        evs[i][0].record(stream)
+        ffn(i)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    k_ms = [a.elapsed_time(b) for a, b in evs]
+    k_bytes = [fb[i % n_x] for i in range(n_k)]
+    achieved = sum(k_bytes) / (sum(k_ms) / 1e3) / 1e9
+    roof = {"kernel": "moe_bitslice_ffn (bitslice_gateup_kernel + bitslice_down_kernel + bitslice_sum_kernel)",
+            "ffn_path": f"bitslice-b{bits}", "bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+            "frac": achieved / hbm_gbs, "peak_source": peak_src,
+            "algorithmic_bytes_per_launch": float(statistics.mean(fb)), "avg_launch_ms": statistics.mean(k_ms),
+            "traffic": None}
+
+    # end to end: pinned host x -> device, draft layer, y -> pinned host, every step
+    x_host = [xs[c].cpu().pin_memory() for c in range(n_x)]
+    y_host = torch.empty_like(y, device="cpu").pin_memory()
+    n_e2e = max(20, min(args.steps, 1000))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        xs[i % n_x].copy_(x_host[i % n_x], non_blocking=True)
+        step(i)
+        y_host.copy_(y, non_blocking=True)
+        stream.synchronize()
+    e2e_s = max_over_ranks(world, time.perf_counter() - t0)
+    e2e_value = world * T * n_e2e / e2e_s
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": f"b{bits} bit planes of int8 (f32 accumulate)",
+        "data": "synthetic (seeded N(0,0.02^2) weights, N(0,1) tokens; shapes of the named model)",
+        "config": {"workload": wl_name, "tokens_per_step": T, "d": d, "experts": N, "top_k": k,
+                   "intermediate": I, "shared_experts": ns, "bits": bits, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: {n_copies} rotating copies of every expert's planes",
+                   "cuda_graph": True},
+        "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": xs[0].numel() * xs[0].element_size(),
+                "d2h_bytes_per_step": y.numel() * 4, "steps": n_e2e,
+                "note": "moe_route + moe_bitslice_ffn per step with pinned-host copies and a stream sync, no graph"},
+        "gpu_launches": int(launches_per_step * args.steps),
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        bo = BitsliceOracle(cfg, W, bits)
+        bo.token(make_tokens(cfg, T=1, batch=10_000)[0])  # quantises the experts it reads
+        n_tok, t0 = 0, time.perf_counter()
+        while True:
+            bo.token(make_tokens(cfg, T=1, batch=10_001 + n_tok)[0])
+            n_tok += 1
+            el = time.perf_counter() - t0
+            if el >= args.cpu_seconds:
+                break
+        line["cpu_baseline"] = {"value": n_tok / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{n_tok} one-token draft steps ({el:.1f} s) through the float64 "
+                                          f"oracle, single thread, experts quantised beforehand when first read"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     wl_name = args.workload
@@ -298,6 +524,12 @@ def main():
     hbm_gbs, bf16_tflops, peak_src = peaks()
 
     W = make_weights(cfg)
+    if wl_name in BITSLICE_WORKLOADS:
+        run_bitslice(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     base = DeviceLayer(cfg, W, T, device=str(dev))
     esize = 2 if cfg.wtype == "bf16" else 4
     expert_bytes = 3 * cfg.I * cfg.d * esize

@@ -95,6 +95,11 @@ _PROTOS = {
     "moe_expert_ffn_noalloc": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P], C.c_int),
     "moe_lore": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P], C.c_int),
     "moe_combine": ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _P], C.c_int),
+    "moe_bitslice_pack": ([C.c_int, C.c_int, C.c_int, _P, C.c_int, _P, _P, _P], C.c_int),
+    "moe_bitslice_scratch_size": ([C.c_int, C.c_int, C.c_int, C.c_int], C.c_size_t),
+    "moe_bitslice_ffn": ([C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, _P, C.c_int, C.c_int, _P, _P, _P, _P,
+                          _P, _P,
+                          _P, _P, C.c_int, _P, _P, _SZ, _P], C.c_int),
     "moe_prefetch_depth": ([_DIMS, C.c_int, _P, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_float, C.c_int,
                             _P, _P, _P, _P, _P, _P, _SZ, _P], C.c_int),
     "moe_prefetch_min_depth": ([C.c_double, C.c_double, C.c_double], C.c_int),
@@ -272,6 +277,45 @@ def moe_prefetch_depth(dims, x, w_routers, biases, tau, d_min, logits, conf, dep
         _ptr(depth, torch.int32, T, "depth", T == 0), _ptr(token_masks, torch.int64, T * J, "token_masks", T == 0),
         _ptr(layer_masks, torch.int64, J, "layer_masks"), _ptr(ws, torch.uint8, name="ws"), ws.numel(),
         _stream(stream)), "moe_prefetch_depth")
+
+
+def moe_bitslice_pack(w, transpose, planes, scales, stream=None):
+    """Pack one weight matrix w [rows, cols] (bf16 or float32 CUDA tensor), or
+    its transpose, into 8 bit planes: planes int32 [8 * R * C / 32] (uint32
+    bit patterns), scales float32 [R]."""
+    rows, cols = w.shape
+    R, Cc = (cols, rows) if transpose else (rows, cols)
+    wt = MOE_DTYPE_BF16 if w.dtype == torch.bfloat16 else MOE_DTYPE_F32
+    _check(lib().moe_bitslice_pack(rows, cols, wt, _ptr(w, (torch.bfloat16, torch.float32), rows * cols, "w"),
+                                   int(bool(transpose)), _ptr(planes, torch.int32, 8 * R * Cc // 32, "planes"),
+                                   _ptr(scales, torch.float32, R, "scales"), _stream(stream)), "moe_bitslice_pack")
+
+
+def moe_bitslice_scratch_size(d, I, T, slots) -> int:
+    return int(lib().moe_bitslice_scratch_size(int(d), int(I), int(T), int(slots)))
+
+
+def moe_bitslice_ffn(d, I, N, bits, x, idx, gate, planes_gate, scales_gate, planes_up, scales_up, planes_down,
+                     scales_down, y, scratch, accumulate=False, n_shared=0, stream=None):
+    """Draft FFN with b-bit weights: y[t] (+)= sum_s gate[t,s] FFN_b(idx[t,s], x_t)
+    + sum_i FFN_b(N + i, x_t) over the n_shared shared experts.  x [T, d] bf16
+    or float32; idx [T, k] int32; gate [T, k] float32 or None; planes / scales
+    as written by moe_bitslice_pack for the N routed then the n_shared shared
+    experts back to back (down projection packed transposed); y [T, d]
+    float32; scratch uint8."""
+    T, k = idx.shape
+    xt = MOE_DTYPE_BF16 if x.dtype == torch.bfloat16 else MOE_DTYPE_F32
+    w8 = lambda R, Cc: 8 * (N + n_shared) * R * Cc // 32
+    NS = N + n_shared
+    _check(lib().moe_bitslice_ffn(
+        int(d), int(I), int(N), int(n_shared), int(bits), xt, _ptr(x, (torch.bfloat16, torch.float32), T * d, "x", T == 0), T, k,
+        _ptr(idx, torch.int32, T * k, "idx", T == 0), _ptr(gate, torch.float32, T * k, "gate", True),
+        _ptr(planes_gate, torch.int32, w8(I, d), "planes_gate"), _ptr(scales_gate, torch.float32, NS * I, "scales_gate"),
+        _ptr(planes_up, torch.int32, w8(I, d), "planes_up"), _ptr(scales_up, torch.float32, NS * I, "scales_up"),
+        _ptr(planes_down, torch.int32, w8(d, I), "planes_down"),
+        _ptr(scales_down, torch.float32, NS * d, "scales_down"), int(bool(accumulate)),
+        _ptr(y, torch.float32, T * d, "y", T == 0), _ptr(scratch, torch.uint8, name="scratch"), scratch.numel(),
+        _stream(stream)), "moe_bitslice_ffn")
 
 
 def moe_prefetch_min_depth(expert_bytes: float, link_bytes_per_s: float, layer_seconds: float) -> int:

@@ -1,0 +1,305 @@
+// Bit-sliced expert weights: a low-precision draft of the expert FFN.
+//
+// ELMoE-3D (CSDN post), bit-slicing section: each weight is an INT8 value
+// with a scale shared by every precision; its 8 bits are stored as 8 binary
+// planes, and a b-bit representation combines the top b planes (plane 7
+// carries -128, plane p < 7 carries 2^p; the learned LSB-enhancement scale is
+// not used).  Its data-layout note keeps an expert's planes contiguous so that
+// the top b planes are one read.  Layout here, per matrix [R, C] (R output
+// rows, C inputs, C a multiple of 32):
+//   planes [8][R][C/32] uint32: slot s holds plane 7 - s (MSB first), bit i
+//          of word w of row r = bit of q[r][32 w + i]; the top b planes are
+//          slots 0 .. b-1, the first b * R * C/32 words;
+//   scales [R] float32: s_r = max_c |W[r][c]| / 127, q = rint(W / s_r)
+//          clamped to +-127 (symmetric per output row; the pages leave the
+//          quantiser open).
+// Gate and up are [I, d]; the down projection is packed transposed, [d, I],
+// so that every matrix is read as row dot products.
+//
+// A row dot product over bit planes: sum_k v_k q_b[r][k] = sum over the top b
+// planes p of w_p * (sum of v_k over the set bits of plane p).  The masked
+// sums come from a table built once per block in shared memory: for every
+// group of 4 consecutive inputs, the 16 sums of its subsets, so that a 32-bit
+// plane word costs 8 table reads.  Table layout [v][j][w] (v the 4-bit
+// pattern, j the nibble of the word, w the word, padded to a multiple of 32
+// words): lanes reading consecutive words hit distinct banks.
+#include <cmath>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+constexpr int kBsThreads = 512;  // 16 warps per block
+
+__host__ __device__ inline int bs_words_pad(int cols) { return ((cols / 32) + 31) / 32 * 32; }
+__host__ __device__ inline size_t bs_table_bytes(int cols) { return (size_t)16 * 8 * bs_words_pad(cols) * 4; }
+
+__device__ __forceinline__ float bs_load(const __nv_bfloat16* p, size_t i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ float bs_load(const float* p, size_t i) { return p[i]; }
+
+// ---------------------------------------------------------------- pack
+// One block per output row: the row's largest magnitude, its scale, then a
+// warp per 32-input word: every lane quantises one input and 8 ballots form
+// the word of each plane.
+template <typename W>
+__global__ void __launch_bounds__(256) bitslice_pack_kernel(const W* __restrict__ w, int rows_in, int cols_in,
+                                                           int transpose, uint32_t* __restrict__ planes,
+                                                           float* __restrict__ scales) {
+    grid_dep_wait();
+    __shared__ float red[8];
+    const int R = transpose ? cols_in : rows_in, C = transpose ? rows_in : cols_in;
+    const int r = blockIdx.x, words = C / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    auto at = [&](int c) -> float {
+        return transpose ? bs_load(w, (size_t)c * cols_in + r) : bs_load(w, (size_t)r * cols_in + c);
+    };
+    float mx = 0.f;
+    for (int c = threadIdx.x; c < C; c += blockDim.x) mx = fmaxf(mx, fabsf(at(c)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    mx = red[0];
+    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) mx = fmaxf(mx, red[i]);
+    const float s = __fdiv_rn(mx, 127.0f);
+    if (threadIdx.x == 0) scales[r] = s;
+    for (int wd = warp; wd < words; wd += blockDim.x >> 5) {
+        int q = 0;
+        if (s > 0.f) {
+            q = (int)rintf(__fdiv_rn(at(wd * 32 + lane), s));
+            q = q > 127 ? 127 : q < -127 ? -127 : q;
+        }
+        const unsigned byte = (unsigned)(q & 0xff);
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            const uint32_t word = __ballot_sync(0xffffffffu, (byte >> p) & 1u);
+            if (lane == 0) planes[((size_t)(7 - p) * R + r) * words + wd] = word;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- table
+// Subset sums of every 4 consecutive values of v[0 .. cols): tbl[v][j][w].
+__device__ __forceinline__ void bs_build_table(const float* __restrict__ v, int cols, float* tbl) {
+    const int words = cols / 32, wp = bs_words_pad(cols);
+    for (int n = threadIdx.x; n < cols / 4; n += blockDim.x) {
+        const int wd = n % words, j = n / words;  // consecutive threads: consecutive words
+        const int k0 = wd * 32 + j * 4;
+        float e[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) e[i] = v[k0 + i];
+        float sum[16];
+        sum[0] = 0.f;
+#pragma unroll
+        for (int m = 1; m < 16; ++m) sum[m] = sum[m & (m - 1)] + e[__ffs(m) - 1];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) tbl[(m * 8 + j) * wp + wd] = sum[m];
+    }
+}
+
+// sum over the set bits of one plane word: 8 table reads
+__device__ __forceinline__ float bs_word_sum(const float* tbl, int wp, int wd, uint32_t bits) {
+    float a = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a += tbl[(((bits >> (4 * j)) & 15u) * 8 + j) * wp + wd];
+    return a;
+}
+
+template <int B>
+__device__ __forceinline__ float bs_plane_weight(int slot) {
+    return slot == 0 ? -128.f : (float)(1 << (7 - slot));
+}
+
+// Slot s of token t: a routed slot (s < k) names idx[t][s] with gate[t][s];
+// slot k + i is shared expert i, stored as expert N + i, gate 1.
+__device__ __forceinline__ int bs_expert(const BitsliceArgs& a, int t, int s) {
+    if (s >= a.k) return a.N + (s - a.k);
+    const int e = a.idx[(size_t)t * a.k + s];
+    return e >= 0 && e < a.N ? e : -1;  // no expert: a zero contribution
+}
+
+// ---------------------------------------------------------------- gate / up
+// Block (persistent over rows, token t): the table over x_t, then a warp per
+// (slot, channel) row of this token: g and u over the top B planes, h =
+// SiLU(g) u.  Routed slots naming no expert in 0..N-1 give h = 0.
+template <typename W, int B>
+__global__ void __launch_bounds__(kBsThreads) bitslice_gateup_kernel(BitsliceArgs a, const W* __restrict__ x) {
+    grid_dep_wait();  // x and the routed experts come from the previous launches
+    extern __shared__ __align__(16) float bs_tbl[];
+    const int t = blockIdx.y, d = a.d, I = a.I, words = d / 32, wp = bs_words_pad(d);
+    float* xv = bs_tbl + (size_t)16 * 8 * wp;  // x_t as float
+    for (int i = threadIdx.x; i < d; i += blockDim.x) xv[i] = bs_load(x, (size_t)t * d + i);
+    __syncthreads();
+    bs_build_table(xv, d, bs_tbl);
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const size_t mat = (size_t)8 * I * words;  // words of one expert's matrix
+    const int S = a.k + a.ns;
+    for (int row = blockIdx.x * nw + warp; row < S * I; row += gridDim.x * nw) {
+        const int slot = row / I, c = row % I;
+        const int e = bs_expert(a, t, slot);
+        float h = 0.f;
+        if (e >= 0 && e < a.N + a.ns) {
+            const uint32_t* pg = a.planes_gate + (size_t)e * mat + (size_t)c * words;
+            const uint32_t* pu = a.planes_up + (size_t)e * mat + (size_t)c * words;
+            float ag = 0.f, au = 0.f;
+            // every plane word of the row (d <= 4096: at most 4 per lane) is
+            // loaded before the table reads that consume them
+            uint32_t bg[4][B], bu[4][B];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int wd = lane + 32 * i;
+#pragma unroll
+                for (int sl = 0; sl < B; ++sl) {
+                    bg[i][sl] = wd < words ? pg[(size_t)sl * I * words + wd] : 0u;
+                    bu[i][sl] = wd < words ? pu[(size_t)sl * I * words + wd] : 0u;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int wd = lane + 32 * i;
+                if (wd < words) {
+#pragma unroll
+                    for (int sl = 0; sl < B; ++sl) {
+                        ag += bs_plane_weight<B>(sl) * bs_word_sum(bs_tbl, wp, wd, bg[i][sl]);
+                        au += bs_plane_weight<B>(sl) * bs_word_sum(bs_tbl, wp, wd, bu[i][sl]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                ag += __shfl_xor_sync(0xffffffffu, ag, o);
+                au += __shfl_xor_sync(0xffffffffu, au, o);
+            }
+            const float g = ag * a.scales_gate[(size_t)e * I + c], u = au * a.scales_up[(size_t)e * I + c];
+            h = g / (1.f + expf(-g)) * u;
+        }
+        if (lane == 0) a.h[((size_t)t * S + slot) * I + c] = h;
+    }
+}
+
+// ---------------------------------------------------------------- down
+// Block (persistent over output rows, (token, slot) pair): the table over
+// h of the pair, then a warp per output j: y_part = s_d[j] * the dot of h
+// with the top B planes of row j of W_down^T.
+template <int B>
+__global__ void __launch_bounds__(kBsThreads) bitslice_down_kernel(BitsliceArgs a) {
+    grid_dep_wait();  // h comes from the gate / up launch
+    extern __shared__ __align__(16) float bs_tbl[];
+    const int pair = blockIdx.y, d = a.d, I = a.I, words = I / 32, wp = bs_words_pad(I);
+    const int S = a.k + a.ns;
+    const int e = bs_expert(a, pair / S, pair % S);
+    if (e < 0 || e >= a.N + a.ns) {  // no expert: a zero contribution
+        for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < d; j += gridDim.x * blockDim.x)
+            a.y_part[(size_t)pair * d + j] = 0.f;
+        return;
+    }
+    bs_build_table(a.h + (size_t)pair * I, I, bs_tbl);
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const size_t mat = (size_t)8 * d * words;
+    for (int j = blockIdx.x * nw + warp; j < d; j += gridDim.x * nw) {
+        const uint32_t* pd = a.planes_down + (size_t)e * mat + (size_t)j * words;
+        float acc = 0.f;
+        // I <= 8192: at most 8 words per lane, loaded 4 at a time ahead of use
+        for (int w0 = 0; w0 < words; w0 += 128) {
+            uint32_t bd[4][B];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int wd = w0 + lane + 32 * i;
+#pragma unroll
+                for (int sl = 0; sl < B; ++sl) bd[i][sl] = wd < words ? pd[(size_t)sl * d * words + wd] : 0u;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int wd = w0 + lane + 32 * i;
+                if (wd < words) {
+#pragma unroll
+                    for (int sl = 0; sl < B; ++sl)
+                        acc += bs_plane_weight<B>(sl) * bs_word_sum(bs_tbl, wp, wd, bd[i][sl]);
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) a.y_part[(size_t)pair * d + j] = acc * a.scales_down[(size_t)e * d + j];
+    }
+}
+
+// ---------------------------------------------------------------- gated sum
+// y[t][j] (+)= sum over slots s, in order, of gate[t][s] * y_part[t S + s][j]
+// (S = k + ns slots per token; a shared slot's gate is 1).
+__global__ void __launch_bounds__(256) bitslice_sum_kernel(BitsliceArgs a) {
+    grid_dep_wait();
+    const size_t n = (size_t)a.T * a.d;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t t = i / a.d, j = i % a.d;
+        const int S = a.k + a.ns;
+        float acc = a.accumulate ? a.y[i] : 0.f;
+        for (int s = 0; s < S; ++s) {
+            const float g = (s < a.k && a.gate) ? a.gate[t * a.k + s] : 1.f;
+            acc += g * a.y_part[(t * S + s) * a.d + j];
+        }
+        a.y[i] = acc;
+    }
+}
+
+// ---------------------------------------------------------------- host
+cudaError_t launch_bitslice_pack(int rows_in, int cols_in, bool bf16, const void* w, int transpose, uint32_t* planes,
+                                 float* scales, cudaStream_t st) {
+    const int R = transpose ? cols_in : rows_in;
+    if (bf16)
+        return launch_pdl(bitslice_pack_kernel<__nv_bfloat16>, dim3(R), dim3(256), 0, st,
+                          static_cast<const __nv_bfloat16*>(w), rows_in, cols_in, transpose, planes, scales);
+    return launch_pdl(bitslice_pack_kernel<float>, dim3(R), dim3(256), 0, st, static_cast<const float*>(w), rows_in,
+                      cols_in, transpose, planes, scales);
+}
+
+template <typename W, int B>
+static cudaError_t bs_ffn(const BitsliceArgs& a, const void* x, int sms, cudaStream_t st) {
+    const size_t smem1 = bs_table_bytes(a.d) + (size_t)a.d * 4;
+    cudaError_t e = allow_max_smem(bitslice_gateup_kernel<W, B>);
+    if (e != cudaSuccess) return e;
+    // gate / up: about two blocks per SM over all tokens
+    const int rows1 = (a.k + a.ns) * a.I, per1 = (rows1 + 15) / 16;
+    int g1 = (2 * sms + a.T - 1) / a.T;
+    g1 = g1 < 1 ? 1 : g1 > per1 ? per1 : g1;
+    e = launch_pdl(bitslice_gateup_kernel<W, B>, dim3(g1, a.T), dim3(kBsThreads), smem1, st, a,
+                   static_cast<const W*>(x));
+    if (e != cudaSuccess) return e;
+    const size_t smem2 = bs_table_bytes(a.I);
+    e = allow_max_smem(bitslice_down_kernel<B>);
+    if (e != cudaSuccess) return e;
+    const int pairs = a.T * (a.k + a.ns), per2 = (a.d + 15) / 16;
+    int g2 = (2 * sms + pairs - 1) / pairs;
+    g2 = g2 < 1 ? 1 : g2 > per2 ? per2 : g2;
+    e = launch_pdl(bitslice_down_kernel<B>, dim3(g2, pairs), dim3(kBsThreads), smem2, st, a);
+    if (e != cudaSuccess) return e;
+    const size_t n = (size_t)a.T * a.d;
+    const int g3 = (int)((n + 255) / 256 < 4 * (size_t)sms ? (n + 255) / 256 : 4 * (size_t)sms);
+    return launch_pdl(bitslice_sum_kernel, dim3(g3), dim3(256), 0, st, a);
+}
+
+template <typename W>
+static cudaError_t bs_ffn_bits(const BitsliceArgs& a, const void* x, int sms, cudaStream_t st) {
+    switch (a.bits) {
+        case 1: return bs_ffn<W, 1>(a, x, sms, st);
+        case 2: return bs_ffn<W, 2>(a, x, sms, st);
+        case 3: return bs_ffn<W, 3>(a, x, sms, st);
+        case 4: return bs_ffn<W, 4>(a, x, sms, st);
+        case 5: return bs_ffn<W, 5>(a, x, sms, st);
+        case 6: return bs_ffn<W, 6>(a, x, sms, st);
+        case 7: return bs_ffn<W, 7>(a, x, sms, st);
+        case 8: return bs_ffn<W, 8>(a, x, sms, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_bitslice_ffn(const BitsliceArgs& a, const void* x, bool bf16, int sms, cudaStream_t st) {
+    return bf16 ? bs_ffn_bits<__nv_bfloat16>(a, x, sms, st) : bs_ffn_bits<float>(a, x, sms, st);
+}
+
+size_t bitslice_table_bytes(int cols) { return bs_table_bytes(cols); }
+
+}  // namespace moe

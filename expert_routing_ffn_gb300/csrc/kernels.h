@@ -194,6 +194,22 @@ cudaError_t launch_layer_epilogue(const EpilogueArgs& a, cudaStream_t st);
 cudaError_t launch_wait_timeout_probe(DevError* err, cudaStream_t st);
 
 // persistent expert cache, one decode step (cache.cu)
+// bit-sliced expert weights (bitslice.cu)
+struct BitsliceArgs {
+    int d, I, N, ns, T, k, bits, accumulate;  // ns shared experts: experts N .. N+ns-1, slots k .. k+ns-1
+    const int32_t* idx;     // [T, k] expert per routed slot
+    const float* gate;      // [T, k] or NULL (1)
+    const uint32_t *planes_gate, *planes_up, *planes_down;  // [N][8][R][C/32]
+    const float *scales_gate, *scales_up, *scales_down;     // [N][R]
+    float* h;               // [T*(k+ns), I] scratch
+    float* y_part;          // [T*(k+ns), d] scratch
+    float* y;               // [T, d]
+};
+cudaError_t launch_bitslice_pack(int rows_in, int cols_in, bool bf16, const void* w, int transpose, uint32_t* planes,
+                                 float* scales, cudaStream_t st);
+cudaError_t launch_bitslice_ffn(const BitsliceArgs& a, const void* x, bool bf16, int sms, cudaStream_t st);
+size_t bitslice_table_bytes(int cols);
+
 // confidence-aware look-ahead prefetch depth (lookahead.cu)
 constexpr int kMaxAhead = MOE_MAX_AHEAD;
 cudaError_t launch_lookahead_logits(const void* x, const void* const* w, const float* const* b, int J, int T, int d,

@@ -640,6 +640,50 @@ int moe_prefetch_min_depth(double expert_bytes, double link_bytes_per_s, double 
     return (int)std::ceil(q);
 }
 
+moe_status moe_bitslice_pack(int rows, int cols, moe_dtype wtype, const void* w, int transpose,
+                             uint32_t* planes, float* scales, void* stream) {
+    if (rows <= 0 || cols <= 0 || !w || !planes || !scales) return MOE_ERR_INVALID_ARG;
+    if (wtype != MOE_DTYPE_BF16 && wtype != MOE_DTYPE_F32) return MOE_ERR_UNSUPPORTED;
+    if ((transpose ? rows : cols) % 32 != 0) return MOE_ERR_INVALID_ARG;
+    MOE_CUDA(launch_bitslice_pack(rows, cols, wtype == MOE_DTYPE_BF16, w, transpose, planes, scales, S(stream)));
+    count();
+    return MOE_OK;
+}
+
+size_t moe_bitslice_scratch_size(int d, int I, int T, int slots) {
+    if (d <= 0 || I <= 0 || T < 0 || slots <= 0) return 0;
+    return (size_t)T * slots * ((size_t)I + d) * sizeof(float);
+}
+
+moe_status moe_bitslice_ffn(int d, int I, int N, int n_shared, int bits, moe_dtype xtype, const void* x, int T, int k,
+                            const int32_t* idx, const float* gate, const uint32_t* planes_gate,
+                            const float* scales_gate, const uint32_t* planes_up, const float* scales_up,
+                            const uint32_t* planes_down, const float* scales_down, int accumulate, float* y,
+                            void* scratch, size_t scratch_bytes, void* stream) {
+    if (d <= 0 || I <= 0 || N <= 0 || n_shared < 0 || T < 0 || k <= 0 || bits < 1 || bits > 8)
+        return MOE_ERR_INVALID_ARG;
+    if (d % 32 != 0 || I % 32 != 0) return MOE_ERR_INVALID_ARG;
+    if (d > 4096 || I > 8192) return MOE_ERR_UNSUPPORTED;
+    if (xtype != MOE_DTYPE_BF16 && xtype != MOE_DTYPE_F32) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    if (!x || !idx || !planes_gate || !scales_gate || !planes_up || !scales_up || !planes_down || !scales_down ||
+        !y || !scratch)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(planes_gate) || !aligned16(planes_up) || !aligned16(planes_down) ||
+        !aligned16(scratch))
+        return MOE_ERR_INVALID_ARG;
+    if (scratch_bytes < moe_bitslice_scratch_size(d, I, T, k + n_shared)) return MOE_ERR_CAPACITY;
+    BitsliceArgs a;
+    a.d = d; a.I = I; a.N = N; a.ns = n_shared; a.T = T; a.k = k; a.bits = bits; a.accumulate = accumulate ? 1 : 0;
+    a.idx = idx; a.gate = gate;
+    a.planes_gate = planes_gate; a.planes_up = planes_up; a.planes_down = planes_down;
+    a.scales_gate = scales_gate; a.scales_up = scales_up; a.scales_down = scales_down;
+    a.h = static_cast<float*>(scratch); a.y_part = a.h + (size_t)T * (k + n_shared) * I; a.y = y;
+    MOE_CUDA(launch_bitslice_ffn(a, x, xtype == MOE_DTYPE_BF16, sm_count(), S(stream)));
+    count(3);
+    return MOE_OK;
+}
+
 moe_status moe_combine(const moe_dims* dims, const float* y_perm, const int32_t* inv_perm,
                        const float* final_gate, const int32_t* final_kind, const float* y_shared,
                        const float* y_lore, float* out, void* stream) {

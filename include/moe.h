@@ -327,6 +327,51 @@ moe_status moe_prefetch_depth(const moe_dims* dims, int n_ahead, const void* x,
  * non-positive bandwidth or layer time, or a depth above INT32_MAX. */
 int moe_prefetch_min_depth(double expert_bytes, double link_bytes_per_s, double layer_seconds);
 
+/* Bit-sliced expert weights (beyond the single layer forward; ELMoE-3D,
+ * bit-slicing section and its data-layout note): a low-precision draft of the
+ * expert FFN.  Each weight is an INT8 value q with a scale per output row
+ * (s_r = max |W[r][.]| / 127, q = rint(W / s_r) clamped to +-127, float32
+ * arithmetic); its 8 bits are stored as binary planes and a b-bit weight is
+ * s_r times the top b planes recombined (plane 7 carries -128, plane p < 7
+ * carries 2^p: the value floored to a multiple of 2^(8-b)).
+ *
+ * moe_bitslice_pack: W [rows, cols] row-major in wtype (device); transpose
+ * != 0 packs W^T.  With (R, C) = (rows, cols), or (cols, rows) transposed,
+ * C a multiple of 32: planes [8][R][C/32] uint32, slot s = plane 7 - s (the
+ * top b planes are the first b*R*C/32 words), bit i of word w of row r =
+ * that plane's bit of q[r][32w + i]; scales [R] float32.  Device, written.
+ * Errors: INVALID_ARG (sizes, C not a multiple of 32, NULL), UNSUPPORTED
+ * (wtype).  Asynchronous. */
+moe_status moe_bitslice_pack(int rows, int cols, moe_dtype wtype, const void* w, int transpose,
+                             uint32_t* planes, float* scales, void* stream);
+
+/* Scratch bytes moe_bitslice_ffn needs for T tokens of `slots` slots each
+ * (k + n_shared): T*slots*(I + d)*4 (0 for bad sizes). */
+size_t moe_bitslice_scratch_size(int d, int I, int T, int slots);
+
+/* The draft FFN with b-bit weights for T tokens of k routed slots and the
+ * n_shared shared experts:
+ *   y[t] (+)= sum over routed slots s, in order, of gate[t][s] *
+ *             FFN_b(idx[t][s], x_t), then + FFN_b(N + i, x_t) for every
+ *             shared expert i, in order
+ *   FFN_b(e, x) = Wd_b^T-rows . (SiLU(Wg_b x) (.) Wu_b x)   (float32 math)
+ * planes_gate / planes_up: the N routed and then the n_shared shared
+ * experts' [I, d] gate / up matrices packed one after another
+ * ([N + n_shared][8][I][d/32], scales [N + n_shared][I]); planes_down: their
+ * W_down [I, d] packed transposed ([N + n_shared][8][d][I/32], scales
+ * [N + n_shared][d]); x [T, d] in xtype; idx [T, k] int32 (a routed slot
+ * naming no expert in 0..N-1 contributes 0); gate [T, k] float32 or NULL
+ * (every gate 1); accumulate != 0 adds to y [T, d] float32, else overwrites
+ * it; scratch of moe_bitslice_scratch_size(d, I, T, k + n_shared) bytes.
+ * All device pointers, planes and x 16-byte aligned.  d and I multiples of
+ * 32, d <= 4096, I <= 8192, bits in 1..8.  Errors: INVALID_ARG, UNSUPPORTED
+ * (xtype, sizes beyond those).  Asynchronous. */
+moe_status moe_bitslice_ffn(int d, int I, int N, int n_shared, int bits, moe_dtype xtype, const void* x, int T, int k,
+                            const int32_t* idx, const float* gate, const uint32_t* planes_gate,
+                            const float* scales_gate, const uint32_t* planes_up, const float* scales_up,
+                            const uint32_t* planes_down, const float* scales_down, int accumulate, float* y,
+                            void* scratch, size_t scratch_bytes, void* stream);
+
 /* Persistent expert cache across decode steps (beyond the single layer
  * forward; ELMoE-3D, expert-axis elasticity: heat statistics of the experts
  * the routing function selects, the most frequently activated top-K kept
