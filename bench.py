@@ -226,7 +226,19 @@ def whole_job_tokens_per_s(world: int, T: int, steps: int, ms_max: float) -> flo
     return world * T * steps / (ms_max / 1e3)
 
 
-def cpu_baseline(cfg, W, T, seconds, batch_offset=0):
+def oracle_step(cfg, W, x, wl_name):
+    """One step of the workload through the float64 oracle: the layer forward,
+    and for a look-ahead workload the prefetch depth over its look-ahead
+    routers."""
+    import oracle
+    oracle.layer_forward(cfg, W, x)
+    la = LOOKAHEAD_WORKLOADS.get(wl_name)
+    if la:
+        Ws, bs = make_lookahead_routers(cfg, la[0])
+        oracle.prefetch_depth(x, Ws, bs, cfg.k, la[1], la[2])
+
+
+def cpu_baseline(cfg, W, T, seconds, batch_offset=0, wl_name=None):
     """The float64 oracle, as it stands, on a bounded sample of the workload:
     batches of min(T, 32) tokens until `seconds` have passed (at least one)."""
     import oracle
@@ -234,7 +246,7 @@ def cpu_baseline(cfg, W, T, seconds, batch_offset=0):
     n_tok, t0, b = 0, time.perf_counter(), 0
     while True:
         x = make_tokens(cfg, T=T, batch=10_000 + batch_offset + b)
-        oracle.layer_forward(cfg, W, x)
+        oracle_step(cfg, W, x, wl_name)
         n_tok += T
         b += 1
         el = time.perf_counter() - t0
@@ -308,10 +320,10 @@ def run_reference(args, wl_name, cfg, T, world, rank):
     W = make_weights(cfg)
     warm = min(args.warmup, 3)  # the oracle has no caches to warm beyond a first call
     for i in range(warm):
-        oracle.layer_forward(cfg, W, make_tokens(cfg, T=T, batch=20_000 + i))
+        oracle_step(cfg, W, make_tokens(cfg, T=T, batch=20_000 + i), wl_name)
     budget, t0, n, steps = 120.0, time.perf_counter(), 0, 0
     while steps < args.steps:
-        oracle.layer_forward(cfg, W, make_tokens(cfg, T=T, batch=30_000 + steps))
+        oracle_step(cfg, W, make_tokens(cfg, T=T, batch=30_000 + steps), wl_name)
         n += T
         steps += 1
         if time.perf_counter() - t0 > budget:
@@ -893,7 +905,7 @@ def main():
                                "experts staged from pinned host memory"
         line["cache"] = cache_info
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg, W, T, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(cfg, W, T, args.cpu_seconds, wl_name=wl_name)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
