@@ -208,3 +208,34 @@ def test_prefetch_depth_rejects_bad_arguments_before_cuda():
     D64 = _raw_dims(T=4, d=256, N=65, k=2, I=64)
     assert L.moe_prefetch_depth(C.byref(D64), 2, x, w, None, C.c_float(0.9), 0, out, out, out, out, out,
                                 fake_ws, n, None) == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_bitslice_rejects_bad_arguments_before_cuda():
+    """Bit-sliced weights: bits outside 1..8, widths that are not multiples of
+    32, a too-small scratch, an unsupported width and a NULL buffer are
+    reported before any CUDA call; an empty batch is a no-op."""
+    L = moe.lib()
+    p = C.c_void_p(0x1000)
+    bf16 = moe.MOE_DTYPE_BF16
+    ok_scratch = moe.moe_bitslice_scratch_size(256, 512, 2, 3)
+    assert ok_scratch == 2 * 3 * (512 + 256) * 4
+    assert moe.moe_bitslice_scratch_size(256, 512, 2, 0) == 0
+
+    def ffn(d=256, I=512, N=4, ns=1, bits=4, T=2, k=2, scratch=ok_scratch, x=p):
+        return L.moe_bitslice_ffn(d, I, N, ns, bits, bf16, x, T, k, p, None, p, p, p, p, p, p, 0, p, p, scratch, None)
+
+    assert ffn(bits=0) == moe.MOE_ERR_INVALID_ARG
+    assert ffn(bits=9) == moe.MOE_ERR_INVALID_ARG
+    assert ffn(d=250) == moe.MOE_ERR_INVALID_ARG
+    assert ffn(I=500) == moe.MOE_ERR_INVALID_ARG
+    assert ffn(d=4128) == moe.MOE_ERR_UNSUPPORTED
+    assert ffn(I=8224) == moe.MOE_ERR_UNSUPPORTED
+    assert ffn(scratch=ok_scratch - 4) == moe.MOE_ERR_CAPACITY
+    assert ffn(x=None) == moe.MOE_ERR_INVALID_ARG
+    assert ffn(x=C.c_void_p(0x1004)) == moe.MOE_ERR_INVALID_ARG  # misaligned
+    assert ffn(T=0, x=None) == moe.MOE_OK
+    # packing: the packed width must be a multiple of 32
+    assert L.moe_bitslice_pack(64, 100, bf16, p, 0, p, p, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_bitslice_pack(100, 64, bf16, p, 1, p, p, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_bitslice_pack(64, 96, 7, p, 0, p, p, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_bitslice_pack(64, 96, bf16, None, 0, p, p, None) == moe.MOE_ERR_INVALID_ARG
