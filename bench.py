@@ -92,6 +92,9 @@ def parse():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--plane-copies", type=int, default=0,
+                   help="bit-sliced workloads: rotating copies of the planes (0: enough to defeat L2; "
+                        "small values make small cases for profiling)")
     return p.parse_args()
 
 
@@ -358,6 +361,8 @@ def run_bitslice(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src):
     dt = torch.bfloat16
     step_bytes = (k + ns) * 3 * I * d * bits / 8
     n_copies = int(min(8, max(2, math.ceil(1 + 2 * L2_BYTES / step_bytes))))
+    if args.plane_copies > 0:
+        n_copies = args.plane_copies
     w8 = 8 * I * d // 32
 
     def pack_set(mats, n):

@@ -20,9 +20,11 @@
 // planes p of w_p * (sum of v_k over the set bits of plane p).  The masked
 // sums come from a table built once per block in shared memory: for every
 // group of 4 consecutive inputs, the 16 sums of its subsets, so that a 32-bit
-// plane word costs 8 table reads.  Table layout [v][j][w] (v the 4-bit
-// pattern, j the nibble of the word, w the word, padded to a multiple of 32
-// words): lanes reading consecutive words hit distinct banks.
+// plane word costs 8 table reads.  Table layout [j][v][w] (j the nibble of
+// the word, v the 4-bit pattern, w the word), rows of a fixed 128 words
+// (inputs <= 4096): an index is the pattern shifted by a constant plus the
+// lane's word, the nibble's row a constant offset; lanes reading consecutive
+// words hit distinct banks.
 #include <cmath>
 
 #include "common.cuh"
@@ -32,8 +34,8 @@ namespace moe {
 
 constexpr int kBsThreads = 512;  // 16 warps per block
 
-__host__ __device__ inline int bs_words_pad(int cols) { return ((cols / 32) + 31) / 32 * 32; }
-__host__ __device__ inline size_t bs_table_bytes(int cols) { return (size_t)16 * 8 * bs_words_pad(cols) * 4; }
+constexpr int kBsRowShift = 7;                        // table row = 128 words
+constexpr size_t kBsTableBytes = (size_t)8 * 16 * (1 << kBsRowShift) * 4;  // 64 KB
 
 __device__ __forceinline__ float bs_load(const __nv_bfloat16* p, size_t i) { return __bfloat162float(p[i]); }
 __device__ __forceinline__ float bs_load(const float* p, size_t i) { return p[i]; }
@@ -80,9 +82,9 @@ __global__ void __launch_bounds__(256) bitslice_pack_kernel(const W* __restrict_
 }
 
 // ---------------------------------------------------------------- table
-// Subset sums of every 4 consecutive values of v[0 .. cols): tbl[v][j][w].
+// Subset sums of every 4 consecutive values of v[0 .. cols): tbl[j][v][w].
 __device__ __forceinline__ void bs_build_table(const float* __restrict__ v, int cols, float* tbl) {
-    const int words = cols / 32, wp = bs_words_pad(cols);
+    const int words = cols / 32;
     for (int n = threadIdx.x; n < cols / 4; n += blockDim.x) {
         const int wd = n % words, j = n / words;  // consecutive threads: consecutive words
         const int k0 = wd * 32 + j * 4;
@@ -94,16 +96,20 @@ __device__ __forceinline__ void bs_build_table(const float* __restrict__ v, int 
 #pragma unroll
         for (int m = 1; m < 16; ++m) sum[m] = sum[m & (m - 1)] + e[__ffs(m) - 1];
 #pragma unroll
-        for (int m = 0; m < 16; ++m) tbl[(m * 8 + j) * wp + wd] = sum[m];
+        for (int m = 0; m < 16; ++m) tbl[((j * 16 + m) << kBsRowShift) + wd] = sum[m];
     }
 }
 
-// sum over the set bits of one plane word: 8 table reads
-__device__ __forceinline__ float bs_word_sum(const float* tbl, int wp, int wd, uint32_t bits) {
-    float a = 0.f;
+// sum over the set bits of one plane word: 8 table reads (tw = the table at
+// this lane's word)
+__device__ __forceinline__ float bs_word_sum(const float* tw, uint32_t bits) {
+    float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) a += tbl[(((bits >> (4 * j)) & 15u) * 8 + j) * wp + wd];
-    return a;
+    for (int j = 0; j < 8; j += 2) {
+        a0 += tw[(j * 16 + ((bits >> (4 * j)) & 15u)) << kBsRowShift];
+        a1 += tw[((j + 1) * 16 + ((bits >> (4 * j + 4)) & 15u)) << kBsRowShift];
+    }
+    return a0 + a1;
 }
 
 template <int B>
@@ -127,8 +133,8 @@ template <typename W, int B>
 __global__ void __launch_bounds__(kBsThreads) bitslice_gateup_kernel(BitsliceArgs a, const W* __restrict__ x) {
     grid_dep_wait();  // x and the routed experts come from the previous launches
     extern __shared__ __align__(16) float bs_tbl[];
-    const int t = blockIdx.y, d = a.d, I = a.I, words = d / 32, wp = bs_words_pad(d);
-    float* xv = bs_tbl + (size_t)16 * 8 * wp;  // x_t as float
+    const int t = blockIdx.y, d = a.d, I = a.I, words = d / 32;
+    float* xv = bs_tbl + kBsTableBytes / 4;  // x_t as float
     for (int i = threadIdx.x; i < d; i += blockDim.x) xv[i] = bs_load(x, (size_t)t * d + i);
     __syncthreads();
     bs_build_table(xv, d, bs_tbl);
@@ -162,8 +168,8 @@ __global__ void __launch_bounds__(kBsThreads) bitslice_gateup_kernel(BitsliceArg
                 if (wd < words) {
 #pragma unroll
                     for (int sl = 0; sl < B; ++sl) {
-                        ag += bs_plane_weight<B>(sl) * bs_word_sum(bs_tbl, wp, wd, bg[i][sl]);
-                        au += bs_plane_weight<B>(sl) * bs_word_sum(bs_tbl, wp, wd, bu[i][sl]);
+                        ag += bs_plane_weight<B>(sl) * bs_word_sum(bs_tbl + wd, bg[i][sl]);
+                        au += bs_plane_weight<B>(sl) * bs_word_sum(bs_tbl + wd, bu[i][sl]);
                     }
                 }
             }
@@ -187,7 +193,7 @@ template <int B>
 __global__ void __launch_bounds__(kBsThreads) bitslice_down_kernel(BitsliceArgs a) {
     grid_dep_wait();  // h comes from the gate / up launch
     extern __shared__ __align__(16) float bs_tbl[];
-    const int pair = blockIdx.y, d = a.d, I = a.I, words = I / 32, wp = bs_words_pad(I);
+    const int pair = blockIdx.y, d = a.d, I = a.I, words = I / 32;
     const int S = a.k + a.ns;
     const int e = bs_expert(a, pair / S, pair % S);
     if (e < 0 || e >= a.N + a.ns) {  // no expert: a zero contribution
@@ -202,7 +208,7 @@ __global__ void __launch_bounds__(kBsThreads) bitslice_down_kernel(BitsliceArgs 
     for (int j = blockIdx.x * nw + warp; j < d; j += gridDim.x * nw) {
         const uint32_t* pd = a.planes_down + (size_t)e * mat + (size_t)j * words;
         float acc = 0.f;
-        // I <= 8192: at most 8 words per lane, loaded 4 at a time ahead of use
+        // I <= 4096: at most 4 words per lane, loaded ahead of use
         for (int w0 = 0; w0 < words; w0 += 128) {
             uint32_t bd[4][B];
 #pragma unroll
@@ -217,7 +223,7 @@ __global__ void __launch_bounds__(kBsThreads) bitslice_down_kernel(BitsliceArgs 
                 if (wd < words) {
 #pragma unroll
                     for (int sl = 0; sl < B; ++sl)
-                        acc += bs_plane_weight<B>(sl) * bs_word_sum(bs_tbl, wp, wd, bd[i][sl]);
+                        acc += bs_plane_weight<B>(sl) * bs_word_sum(bs_tbl + wd, bd[i][sl]);
                 }
             }
         }
@@ -258,7 +264,7 @@ cudaError_t launch_bitslice_pack(int rows_in, int cols_in, bool bf16, const void
 
 template <typename W, int B>
 static cudaError_t bs_ffn(const BitsliceArgs& a, const void* x, int sms, cudaStream_t st) {
-    const size_t smem1 = bs_table_bytes(a.d) + (size_t)a.d * 4;
+    const size_t smem1 = kBsTableBytes + (size_t)a.d * 4;
     cudaError_t e = allow_max_smem(bitslice_gateup_kernel<W, B>);
     if (e != cudaSuccess) return e;
     // gate / up: about two blocks per SM over all tokens
@@ -268,7 +274,7 @@ static cudaError_t bs_ffn(const BitsliceArgs& a, const void* x, int sms, cudaStr
     e = launch_pdl(bitslice_gateup_kernel<W, B>, dim3(g1, a.T), dim3(kBsThreads), smem1, st, a,
                    static_cast<const W*>(x));
     if (e != cudaSuccess) return e;
-    const size_t smem2 = bs_table_bytes(a.I);
+    const size_t smem2 = kBsTableBytes;
     e = allow_max_smem(bitslice_down_kernel<B>);
     if (e != cudaSuccess) return e;
     const int pairs = a.T * (a.k + a.ns), per2 = (a.d + 15) / 16;
@@ -300,6 +306,6 @@ cudaError_t launch_bitslice_ffn(const BitsliceArgs& a, const void* x, bool bf16,
     return bf16 ? bs_ffn_bits<__nv_bfloat16>(a, x, sms, st) : bs_ffn_bits<float>(a, x, sms, st);
 }
 
-size_t bitslice_table_bytes(int cols) { return bs_table_bytes(cols); }
+size_t bitslice_table_bytes(int) { return kBsTableBytes; }
 
 }  // namespace moe

@@ -663,7 +663,7 @@ moe_status moe_bitslice_ffn(int d, int I, int N, int n_shared, int bits, moe_dty
     if (d <= 0 || I <= 0 || N <= 0 || n_shared < 0 || T < 0 || k <= 0 || bits < 1 || bits > 8)
         return MOE_ERR_INVALID_ARG;
     if (d % 32 != 0 || I % 32 != 0) return MOE_ERR_INVALID_ARG;
-    if (d > 4096 || I > 8192) return MOE_ERR_UNSUPPORTED;
+    if (d > 4096 || I > 4096) return MOE_ERR_UNSUPPORTED;
     if (xtype != MOE_DTYPE_BF16 && xtype != MOE_DTYPE_F32) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
     if (!x || !idx || !planes_gate || !scales_gate || !planes_up || !scales_up || !planes_down || !scales_down ||

@@ -229,7 +229,7 @@ def test_bitslice_rejects_bad_arguments_before_cuda():
     assert ffn(d=250) == moe.MOE_ERR_INVALID_ARG
     assert ffn(I=500) == moe.MOE_ERR_INVALID_ARG
     assert ffn(d=4128) == moe.MOE_ERR_UNSUPPORTED
-    assert ffn(I=8224) == moe.MOE_ERR_UNSUPPORTED
+    assert ffn(I=4128) == moe.MOE_ERR_UNSUPPORTED
     assert ffn(scratch=ok_scratch - 4) == moe.MOE_ERR_CAPACITY
     assert ffn(x=None) == moe.MOE_ERR_INVALID_ARG
     assert ffn(x=C.c_void_p(0x1004)) == moe.MOE_ERR_INVALID_ARG  # misaligned
