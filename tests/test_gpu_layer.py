@@ -364,6 +364,31 @@ def test_expert_cache_over_decode_steps_matches_oracle():
         layer.set_resident((1 << 64) - 1)
 
 
+@pytest.mark.parametrize("tau", [0.6, 0.97])
+@pytest.mark.parametrize("T", [1, 1024])
+def test_granite_prefetch_thresholds_match_oracle(tau, T):
+    """The Granite-shaped layer (SUBSTITUTE, available set = the prefetch set)
+    at APEX's other two thresholds besides the default 0.9: delta_hat, the
+    prefetch sets, the substitutes and the output against the oracle at the
+    same tau; a lower threshold prefetches fewer experts on average."""
+    cfg0, W = _host("granite")
+    layer = _device("granite", T)
+    x = make_tokens(cfg0, T=T, batch=5)
+    bufs = LayerBuffers(layer, T)
+    forward(layer, bufs, x_device(x, layer.dt), tau=tau)
+    st, det = moe.moe_check(layer.ws)
+    assert st == moe.MOE_OK, (moe.status_string(st), det)
+    cfg = cfg0.with_(tau=tau)
+    R = oracle.layer_forward(cfg, W, x)
+    check_routing(cfg, R, bufs)
+    check_selection(cfg, R, bufs)
+    check_output(cfg, R, bufs.out)
+    if T > 1:
+        R9 = oracle.layer_forward(cfg0, W, x, route_only=True)
+        dh, dh9 = R.delta_hat.mean(), R9.delta_hat.mean()
+        assert (dh < dh9) if tau < cfg0.tau else (dh > dh9)
+
+
 def st_ok(layer):
     st, _ = moe.moe_check(layer.ws)
     return st == moe.MOE_OK
