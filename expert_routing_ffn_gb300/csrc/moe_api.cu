@@ -664,6 +664,7 @@ moe_status moe_bitslice_ffn(int d, int I, int N, int n_shared, int bits, moe_dty
         return MOE_ERR_INVALID_ARG;
     if (d % 32 != 0 || I % 32 != 0) return MOE_ERR_INVALID_ARG;
     if (d > 4096 || I > 4096) return MOE_ERR_UNSUPPORTED;
+    if ((long long)T * (k + n_shared) > 65535) return MOE_ERR_UNSUPPORTED;  // (token, slot) pairs on grid.y
     if (xtype != MOE_DTYPE_BF16 && xtype != MOE_DTYPE_F32) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
     if (!x || !idx || !planes_gate || !scales_gate || !planes_up || !scales_up || !planes_down || !scales_down ||

@@ -364,7 +364,7 @@ size_t moe_bitslice_scratch_size(int d, int I, int T, int slots);
  * (every gate 1); accumulate != 0 adds to y [T, d] float32, else overwrites
  * it; scratch of moe_bitslice_scratch_size(d, I, T, k + n_shared) bytes.
  * All device pointers, planes and x 16-byte aligned.  d and I multiples of
- * 32, d <= 4096, I <= 4096, bits in 1..8.  Errors: INVALID_ARG, UNSUPPORTED
+ * 32, d <= 4096, I <= 4096, T * (k + n_shared) <= 65535, bits in 1..8.  Errors: INVALID_ARG, UNSUPPORTED
  * (xtype, sizes beyond those).  Asynchronous. */
 moe_status moe_bitslice_ffn(int d, int I, int N, int n_shared, int bits, moe_dtype xtype, const void* x, int T, int k,
                             const int32_t* idx, const float* gate, const uint32_t* planes_gate,

@@ -230,6 +230,7 @@ def test_bitslice_rejects_bad_arguments_before_cuda():
     assert ffn(I=500) == moe.MOE_ERR_INVALID_ARG
     assert ffn(d=4128) == moe.MOE_ERR_UNSUPPORTED
     assert ffn(I=4128) == moe.MOE_ERR_UNSUPPORTED
+    assert ffn(T=30000, k=2, ns=1, scratch=1 << 40) == moe.MOE_ERR_UNSUPPORTED  # 90000 (token, slot) pairs
     assert ffn(scratch=ok_scratch - 4) == moe.MOE_ERR_CAPACITY
     assert ffn(x=None) == moe.MOE_ERR_INVALID_ARG
     assert ffn(x=C.c_void_p(0x1004)) == moe.MOE_ERR_INVALID_ARG  # misaligned
