@@ -12,10 +12,15 @@
  *   5. moe_combine          gate-weighted combine plus shared experts
  * plus moe_stage_experts (pinned host -> HBM expert copies on a side stream)
  * and moe_layer_forward (all stages chained on one stream).
+ * Beyond the single forward: moe_cache_update (a persistent expert cache
+ * across decode steps), moe_prefetch_depth / moe_prefetch_min_depth (a
+ * confidence-aware look-ahead over the next layers) and moe_bitslice_pack /
+ * moe_bitslice_ffn (a low-precision draft FFN on bit-sliced INT8 weights).
  *
  * Conventions (all entry points):
- *   - Every function returns moe_status; nothing aborts, traps, throws or
- *     prints.  Host-detectable argument errors are returned before any work
+ *   - Every function returns moe_status (the two size helpers and
+ *     moe_prefetch_min_depth return their value); nothing aborts, traps,
+ *     throws or prints.  Host-detectable argument errors are returned before any work
  *     is queued.  Errors found by a kernel (a bad expert index, an available
  *     set smaller than k, a timed-out wait) are recorded in the device error
  *     word inside the workspace and reported by moe_check().
@@ -39,7 +44,11 @@
  *     §4.3 execution modes and Algorithm 1 (stall_free_select).
  *   SPICE: Speculative Prefetching with Low-Rank Expert Surrogates and
  *     Heterogeneous Orchestration for MoE Inference (PaperDaily write-up),
- *     sections on the LoRE low-rank surrogate and CPU-GPU orchestration.
+ *     sections on the LoRE low-rank surrogate, CPU-GPU orchestration and
+ *     confidence-aware adaptive prefetch.
+ *   ELMoE-3D (CSDN post): expert-axis elasticity (heat statistics, top-K
+ *     subset, heat decay) and the bit-slicing section with its data-layout
+ *     note.
  *   FloE: On-the-Fly MoE Inference on Memory-constrained GPU (paper notes),
  *     method §1 (contextual sparsity forward), §3 (sparse GEMV, compact
  *     asynchronous transfer).
