@@ -640,3 +640,14 @@ def test_bitslice_ffn_full_precision_is_the_dense_expert():
     np.testing.assert_allclose(y8, dense, rtol=1e-5, atol=1e-7)
     errs = [np.linalg.norm(oracle.bitslice_ffn(x, qg, sg, qu, su, qdT, sd, b) - y8) for b in (2, 4, 6)]
     assert errs[0] > errs[1] > errs[2] > 0
+
+
+def test_bitslice_quantiser_rounds_half_steps_to_even():
+    """A row whose largest magnitude is 127 has scale exactly 1, so its other
+    entries land on exact half-steps: round half to even (0.5 -> 0, 1.5 -> 2,
+    2.5 -> 2, -0.5 -> 0, -1.5 -> -2), not half away from zero; -127 stays the
+    symmetric minimum."""
+    W = np.array([[127.0, 0.5, 1.5, 2.5, -0.5, -1.5, -127.0, 3.0] * 4], np.float32)
+    q, s = oracle.bitslice_quantize(W)
+    assert s[0] == 1.0
+    np.testing.assert_array_equal(q[0, :8], [127, 0, 2, 2, 0, -2, -127, 3])
