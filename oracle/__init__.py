@@ -242,6 +242,8 @@ def prefetch_depth(x, Ws, biases, K, tau, d_min):
     J = len(Ws)
     Wf = [f32(W) for W in Ws]
     N = Wf[0].shape[0]
+    if not (1 <= J <= 64 and 1 <= K <= N <= 64):
+        raise ValueError("prefetch_depth: 1 <= J <= 64 look-ahead layers and 1 <= K <= N <= 64 experts")
     Wp = (_FP * J)(*[_f(W) for W in Wf])
     if biases is None:
         bp = None
