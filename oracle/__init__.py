@@ -319,9 +319,12 @@ class LayerResult:
     resident: int
     resident_gap: float
 
-    def excluded(self, eps: float = 1e-5) -> np.ndarray:
-        """Tokens with any decisive margin below eps (near ties)."""
-        return (self.margin < eps).any(axis=1)
+    def excluded(self, eps: float = 1e-5, floe: bool = True) -> np.ndarray:
+        """Tokens with any decisive margin below eps (near ties).  floe=False
+        leaves the FloE channel-gap margin out (for comparisons that accept
+        either side of a near-tied channel instead of dropping the token)."""
+        m = self.margin if floe else np.delete(self.margin, M_FLOE, axis=1)
+        return (m < eps).any(axis=1)
 
 
 def resident_mask(cfg, W, x_batch) -> tuple[int, float]:

@@ -8,14 +8,14 @@
  * Every step is the plain definition from the source pages, in double
  * precision, with no blocking, fusion or reordering:
  *   - router softmax / top-k          : APEX (Adaptive Expert Prefetching for
- *     Edge MoE Inference) blog, §1 and Algorithm 1 (alpha = softmax(q_r));
+ *     Edge MoE Inference) blog, §1 and §4.3 (alpha = softmax(q_r));
  *     SPICE write-up, section on the MoE I/O bottleneck (top-6 of 64).
  *   - prefetch router                 : APEX §4.1 (linear + softmax).
  *   - oracle budget delta*            : APEX §4.2, definition of delta*.
  *   - ordinal-logistic CDF delta_hat  : APEX §4.2, p_delta(x) and the
  *     inference rule delta_hat = min{delta : p_delta >= tau}.
- *   - stall-free substitution         : APEX §4.3, Algorithm 1
- *     (stall_free_select); correctness-preserving mode, APEX §4.3.
+ *   - stall-free substitution         : APEX §4.3, the stall-free
+ *     selection of the correctness-preserving mode.
  *   - SwiGLU expert FFN, FloE sparsity: FloE (On-the-Fly MoE Inference on
  *     Memory-constrained GPU), method §1, the contextual-sparsity forward
  *     a^S(x) = (SiLU(x W_gate) (.) S_t(x W_up)) W_down.
@@ -166,34 +166,36 @@ int orc_delta_star(int N, int k, const int* routed, const double* lp) {
     return N - k;
 }
 
-/* Stall-free selection (APEX §4.3, Algorithm 1), step by step:
- *   if the routed set is inside the prefetched set, return it;
- *   keep    = routed ∩ prefetched;
- *   missing = routed − prefetched;
- *   subs    = the |missing| members of (prefetched − keep) with the largest
- *             original router probability alpha;
- *   return keep ∪ subs.
+/* Stall-free selection (APEX §4.3, the stall-free expert selection of its
+ * correctness-preserving mode).  Meaning of the rule: the layer runs only on
+ * experts that are already available, with as many experts as it routed.
+ * Every routed expert that is available stays; each routed expert that is
+ * not is replaced, and the replacements are the available non-routed experts
+ * that the ORIGINAL router rates highest.  Written as a definition: with
+ * m = |routed \ available| and pool = available \ routed, the result is
+ *   (routed ∩ available)  ∪  { e ∈ pool : fewer than m members of pool rank
+ *                                          above e by alpha }
+ * (larger alpha ranks above; equal alpha: the lower index ranks above).
  * Sets are bitmasks over N <= 64 experts.  Returns the selected set, or
- * all-ones when the pool is too small to replace every missing expert. */
+ * all-ones when the pool holds fewer than m experts. */
 uint64_t orc_stall_free_select(int N, uint64_t routed, const double* alpha,
-                               uint64_t prefetched) {
-    if ((routed & ~prefetched) == 0) return routed;
-    uint64_t keep = routed & prefetched;
-    uint64_t missing = routed & ~prefetched;
-    int n_missing = 0;
-    for (int e = 0; e < N; ++e) n_missing += (int)((missing >> e) & 1);
-    uint64_t pool = prefetched & ~keep;
-    uint64_t subs = 0;
-    for (int s = 0; s < n_missing; ++s) {
-        int best = -1;
-        for (int e = 0; e < N; ++e)
-            if (((pool >> e) & 1) && !((subs >> e) & 1) &&
-                (best < 0 || ranks_above(alpha[e], e, alpha[best], best)))
-                best = e;
-        if (best < 0) return ~(uint64_t)0;
-        subs |= (uint64_t)1 << best;
+                               uint64_t available) {
+    const uint64_t pool = available & ~routed;
+    int m = 0, pool_size = 0;
+    for (int e = 0; e < N; ++e) {
+        m += (int)(((routed & ~available) >> e) & 1);
+        pool_size += (int)((pool >> e) & 1);
     }
-    return keep | subs;
+    if (pool_size < m) return ~(uint64_t)0;
+    uint64_t chosen = routed & available;
+    for (int e = 0; e < N; ++e) {
+        if (!((pool >> e) & 1)) continue;
+        int above = 0;
+        for (int f = 0; f < N; ++f)
+            if (f != e && ((pool >> f) & 1) && ranks_above(alpha[f], f, alpha[e], e)) ++above;
+        if (above < m) chosen |= (uint64_t)1 << e;
+    }
+    return chosen;
 }
 
 static double silu(double z) { return z / (1.0 + exp(-z)); }
@@ -574,7 +576,7 @@ static void one_token(const orc_cfg* c, const orc_inputs* in, const orc_outputs*
             }
         }
     }
-    /* Substitution only for the misses chosen for it: Algorithm 1 applied to
+    /* Substitution only for the misses chosen for it: the stall-free selection applied to
      * the routed experts that are not sent to LoRE. */
     uint64_t final_set = rmask;
     o->status[t] = 0;

@@ -277,8 +277,12 @@ def test_exact_policy_with_staging_matches_plain_moe():
 @pytest.mark.parametrize("T", [1, 8, 32])
 def test_floe_sparse_matches_oracle(T):
     """FloE contextual sparsity (method §1): each token keeps the m channels
-    with the largest |x W_up| (m = ceil(0.1 I) = 1434 for I = 14336); the kept
-    sets are bit-exact and the outputs within the bf16 tolerance."""
+    with the largest |x W_up| (m = ceil(0.1 I) = 1434 for I = 14336).  Kept
+    sets are bit-exact on every slot whose |u| gap at the keep boundary is at
+    least 1e-5 of max |u|; on the other slots (14336 channels make such gaps
+    common) the GPU set must still be a valid top-m: m channels, none left
+    out whose |u| exceeds a kept one's by more than that band.  Outputs on
+    every token within the bf16 tolerance, those slots included."""
     cfg, W = _host("mixtral")
     layer = _device("mixtral", T)
     kf = np.float32(0.1)
@@ -290,8 +294,8 @@ def test_floe_sparse_matches_oracle(T):
     st, det = moe.moe_check(layer.ws)
     assert st == moe.MOE_OK, (moe.status_string(st), det)
     R = oracle.layer_forward(cfg, W, x, keep_m=m)
-    check_selection(cfg, R, bufs)
-    check_output(cfg, R, bufs.out)
+    check_selection(cfg, R, bufs, floe=False)
+    check_output(cfg, R, bufs.out, floe=False)
     ptr, words = moe.moe_floe_kept_mask(layer.dims.with_T(T), layer.ws)
     rows = int(bufs.expert_offsets[-1])
     off = ptr - layer.ws.data_ptr()
@@ -299,17 +303,27 @@ def test_floe_sparse_matches_oracle(T):
     kept = kept.reshape(rows, words)
     inv = to_np(bufs.inv_perm).reshape(T, cfg.k)
     fi = to_np(bufs.final_idx)
-    keep_tok = ~R.excluded()
-    n_checked = 0
-    for t in np.nonzero(keep_tok)[0]:
+    n_exact = n_band = 0
+    for t in range(T):
         for s in range(cfg.k):
             e = fi[t, s]
             pos = inv[t, s]
             so = list(R.final_idx[t]).index(e)
             bits = np.unpackbits(kept[pos].view(np.uint8), bitorder="little")[:cfg.I]
-            assert (np.nonzero(bits)[0] == R.kept[t, so]).all(), f"kept channels differ (token {t})"
-            n_checked += 1
-    assert n_checked > 0
+            got = np.nonzero(bits)[0]
+            au = np.abs(W.w_up[e].astype(np.float64) @ x[t].astype(np.float64))
+            band = 1e-5 * au.max()
+            srt = np.sort(au)[::-1]
+            if srt[m - 1] - srt[m] >= band:
+                assert (got == R.kept[t, so]).all(), f"kept channels differ (token {t}, slot {s})"
+                n_exact += 1
+            else:
+                assert got.size == m, f"token {t}, slot {s}: {got.size} channels kept"
+                out = np.ones(cfg.I, bool)
+                out[got] = False
+                assert au[got].min() >= au[out].max() - band, f"token {t}, slot {s}: not a top-m set"
+                n_band += 1
+    assert n_exact > 0 and n_exact >= 4 * n_band
 
 
 def test_expert_cache_over_decode_steps_matches_oracle():

@@ -186,11 +186,28 @@ def _closed_form(N, k, alpha, avail):
     return set(cand[:k])
 
 
+def _best_total_alpha(N, routed, alpha, avail):
+    """Brute force over every way of filling the missing slots: among the
+    supersets of (routed & available) inside the available set with as many
+    members as routed, the largest total alpha; equal totals: the
+    lexicographically smallest sorted index list."""
+    keep = [e for e in range(N) if (routed >> e) & 1 and (avail >> e) & 1]
+    pool = [e for e in range(N) if (avail >> e) & 1 and not (routed >> e) & 1]
+    m = bin(routed).count("1") - len(keep)
+    best = None
+    for sub in itertools.combinations(pool, m):
+        key = (-sum(alpha[e] for e in sub), sorted(keep + list(sub)))
+        if best is None or key < best:
+            best = key
+    return set(best[1])
+
+
 @pytest.mark.parametrize("N,k", [(6, 2), (6, 3)])
 def test_stall_free_exhaustive(N, k):
-    """Every ordering of alpha x every available set with |A| >= k: the literal
-    Algorithm 1 equals the top-k of alpha over A, has k members, lies inside A
-    and keeps every routed expert that was available."""
+    """Every ordering of alpha x every available set with |A| >= k: the
+    selection equals the filling of the missing slots with the largest total
+    alpha (brute force), equals the top-k of alpha over A, has k members, lies
+    inside A and keeps every routed expert that was available."""
     for perm in itertools.permutations(range(N)):
         alpha = np.array(perm, np.float64) + 1.0
         alpha /= alpha.sum()
@@ -202,8 +219,30 @@ def test_stall_free_exhaustive(N, k):
             got = oracle.stall_free_select(N, rmask, alpha, avail)
             gs = set(_ids(got, N))
             assert gs == _closed_form(N, k, alpha, avail)
+            if avail & ~rmask and perm[0] % 2 == 0:
+                assert gs == _best_total_alpha(N, rmask, alpha, avail)
             assert len(gs) == k and got & ~avail == 0
             assert (rmask & avail) & ~got == 0
+
+
+def test_stall_free_brute_force_with_ties_and_short_pool():
+    """Integer-valued alpha (many ties) on N = 7: brute force over every
+    filling; a pool smaller than the number of missing experts is refused."""
+    rng = np.random.default_rng(17)
+    N = 7
+    for _ in range(60):
+        alpha = rng.integers(1, 4, N).astype(np.float64)
+        alpha /= alpha.sum()
+        for k in (2, 3):
+            order = sorted(range(N), key=lambda e: (-alpha[e], e))
+            rmask = _mask(order[:k])
+            for avail in range(1 << N):
+                got = oracle.stall_free_select(N, rmask, alpha, avail)
+                missing = bin(rmask & ~avail).count("1")
+                if bin(avail & ~rmask).count("1") < missing:
+                    assert got == (1 << 64) - 1
+                    continue
+                assert set(_ids(got, N)) == _best_total_alpha(N, rmask, alpha, avail)
 
 
 def test_stall_free_sampled_n8_ignores_prefetch_scores():
