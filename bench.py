@@ -80,7 +80,14 @@ BITSLICE_WORKLOADS = {"dsv2lite-bitslice4-draft-T1": 4}  # the host link of the 
 DEFAULT_WORKLOAD = "dsv2lite-decode-T8"
 METRIC = "MoE-layer tokens/sec (decode & prefill) and % of HBM/tensor roofline, 1xGB300"
 FALLBACK_HBM_GBS = 6800.0
+# nominal figures of the part, reported beside the measured-peak fractions:
+# HBM3e at about 8 TB/s, dense (no 2:4 sparsity) bf16 tensor throughput
+NOMINAL_HBM_GBS = 8000.0
+NOMINAL_BF16_TFLOPS = 2250.0
 L2_BYTES = 129 * 1024 * 1024
+# The prefill half of the default line: the largest single-GPU layer shape
+PREFILL_WORKLOAD = "qwen2-prefill-T4096"
+CLOCK_WINDOW_S = 1.2
 
 
 def parse():
@@ -91,6 +98,8 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-prefill", action="store_true",
+                   help="default workload only: skip the prefill half of the line")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--plane-copies", type=int, default=0,
                    help="bit-sliced workloads: rotating copies of the planes (0: enough to defeat L2; "
@@ -184,6 +193,51 @@ class ClockSampler:
                 "sm_max_mhz": smax or None, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def timed_replays(replay, n_graphs, steps, stream, dev, world, window_s=CLOCK_WINDOW_S):
+    """Time exactly `steps` replays (replay(i) replays graph i % n_graphs) with
+    CUDA events on `stream`, between barriers, and sample the clocks over a
+    window of at least `window_s` seconds that contains the timed steps: the
+    same graphs are replayed, untimed, for about window_s before the timed
+    steps and a quarter of it after them (more warm-up under the same load).
+    Returns (slowest rank's ms for the timed steps, clock summary)."""
+    import torch
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n_graphs):
+        replay(i)
+    torch.cuda.synchronize()
+    est = max(1e-6, (time.perf_counter() - t0) / n_graphs)
+    pre = int(min(200_000, math.ceil(window_s / est)))
+    post = int(min(50_000, math.ceil(0.25 * window_s / est)))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index or 0) as clk:
+        for i in range(pre):
+            replay(i)
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(steps):
+            replay(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        for i in range(post):
+            replay(i)
+        torch.cuda.synchronize()
+    ms_total = max_over_ranks(world, ev0.elapsed_time(ev1))
+    summ = clk.summary()
+    summ["window"] = f"{pre} untimed + {steps} timed + {post} untimed replays of the same step"
+    return ms_total, summ
+
+
+def fractions(achieved: float, peak: float, nominal: float, peak_src: str) -> dict:
+    """Achieved against the measured peak (the roofline fraction) and against
+    the part's nominal figure, each labelled."""
+    return {"frac": achieved / peak, "peak": peak, "peak_source": peak_src,
+            "nominal_peak": nominal, "frac_of_nominal": achieved / nominal}
+
+
 def dist_setup(n_gpus):
     """Rank bookkeeping from the torchrun environment.  One process per GPU
     (NCCL); without CUDA (the multi-process tests on CPU) the gloo backend."""
@@ -241,24 +295,82 @@ def oracle_step(cfg, W, x, wl_name):
         oracle.prefetch_depth(x, Ws, bs, cfg.k, la[1], la[2])
 
 
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
 def cpu_baseline(cfg, W, T, seconds, batch_offset=0, wl_name=None):
-    """The float64 oracle, as it stands, on a bounded sample of the workload:
-    batches of min(T, 32) tokens until `seconds` have passed (at least one)."""
+    """The float64 oracle, as it stands, on a bounded sample of the workload,
+    on every core of the process's affinity mask, plus a single-thread figure.
+
+    Decode (T <= 64): whole T-token batches, as many running at once as the
+    cores allow (one OpenMP thread per token), until `seconds` have passed.
+    Prefill: tokens of one T-token batch (its batch resident set computed once,
+    beforehand), in chunks of one token per core, until `seconds` have passed."""
     import oracle
-    T = min(T, 32)
-    n_tok, t0, b = 0, time.perf_counter(), 0
-    while True:
-        x = make_tokens(cfg, T=T, batch=10_000 + batch_offset + b)
-        oracle_step(cfg, W, x, wl_name)
-        n_tok += T
-        b += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return {"value": n_tok / el, "unit": "tokens/s", "cores": min(oracle.num_threads(), T),
-            "kind": "oracle",
-            "sample": f"{b} batches of {T} tokens ({n_tok} tokens, {el:.1f} s) through the float64 "
-                      f"CPU oracle, OpenMP over the tokens of a batch"}
+    from concurrent.futures import ThreadPoolExecutor
+    cores = host_cores()
+    base_threads = oracle.num_threads()
+
+    def run_decode(threads, budget, offset):
+        par = max(1, threads // T)
+
+        def one(b):
+            oracle.set_num_threads(min(T, threads))
+            oracle_step(cfg, W, make_tokens(cfg, T=T, batch=10_000 + batch_offset + offset + b), wl_name)
+            return T
+
+        n_tok, b, t0 = 0, 0, time.perf_counter()
+        with ThreadPoolExecutor(par) as ex:
+            while True:
+                n_tok += sum(ex.map(one, range(b, b + par)))
+                b += par
+                el = time.perf_counter() - t0
+                if el >= budget:
+                    break
+        return n_tok, el, b, min(T, threads) * par
+
+    def run_prefill(threads, budget, x, resident, order):
+        oracle.set_num_threads(threads)
+        n_tok, t0 = 0, time.perf_counter()
+        while n_tok < len(order):
+            rows = np.sort(order[n_tok:n_tok + threads])
+            oracle.layer_forward(cfg, W, x[rows], resident=resident)
+            n_tok += len(rows)
+            el = time.perf_counter() - t0
+            if el >= budget:
+                break
+        return n_tok, el
+
+    try:
+        if T <= 64:
+            n, el, b, used = run_decode(cores, seconds, 0)
+            n1, el1, b1, _ = run_decode(1, max(1.0, seconds / 4), 50_000)
+            res = {"value": n / el, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                   "sample": f"{b} batches of {T} tokens ({n} tokens, {el:.1f} s) through the float64 CPU "
+                             f"oracle, {max(1, cores // T)} batches at a time, OpenMP over the tokens of a "
+                             f"batch; {cores} cores in the affinity mask",
+                   "single_thread": {"value": n1 / el1, "unit": "tokens/s", "cores": 1,
+                                     "sample": f"{b1} batches of {T} tokens ({n1} tokens, {el1:.1f} s), "
+                                               f"one thread"}}
+        else:
+            x = make_tokens(cfg, T=T, batch=10_000 + batch_offset)
+            resident, _ = oracle.resident_mask(cfg, W, x)
+            order = np.random.default_rng(batch_offset).permutation(T)
+            n, el = run_prefill(cores, seconds, x, resident, order)
+            n1, el1 = run_prefill(1, max(2.0, seconds / 4), x, resident, order[::-1].copy())
+            res = {"value": n / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                   "sample": f"{n} of the {T} tokens of one prefill batch (seeded sample, {el:.1f} s) through "
+                             f"the float64 CPU oracle, {cores} tokens at a time (OpenMP over tokens), the "
+                             f"batch resident set computed beforehand; {cores} cores in the affinity mask",
+                   "single_thread": {"value": n1 / el1, "unit": "tokens/s", "cores": 1,
+                                     "sample": f"{n1} tokens of the same batch ({el1:.1f} s), one thread"}}
+    finally:
+        oracle.set_num_threads(base_threads)
+    return res
 
 
 class BitsliceOracle:
@@ -289,65 +401,110 @@ class BitsliceOracle:
         return y
 
 
-def run_reference(args, wl_name, cfg, T, world, rank):
-    """Reference arm: the float64 oracle timed on the host cores, one batch of
-    T tokens per step, for at most about two minutes."""
-    if rank != 0:
-        return
+def workload_cfg(wl_name):
+    """(layer config, tokens per step, phase) of a named workload."""
+    cfg_name, T, phase = WORKLOADS[wl_name][:3]
+    cfg = CONFIGS[cfg_name]
+    if len(WORKLOADS[wl_name]) > 3:
+        cfg = cfg.with_(keep_frac=WORKLOADS[wl_name][3])
+    return cfg, T, phase
+
+
+def reference_line(args, wl_name, steps, warmup, budget=120.0):
+    """Reference arm: the float64 oracle timed on the host cores, one bounded
+    sample of the workload per step (at most 32 tokens of the batch, every
+    core of the affinity mask), for at most `budget` seconds."""
     import oracle
+    cfg, T, phase = workload_cfg(wl_name)
     if wl_name in BITSLICE_WORKLOADS:
         W = make_weights(cfg)
         bo = BitsliceOracle(cfg, W, BITSLICE_WORKLOADS[wl_name])
-        warm = min(args.warmup, 3)
+        warm = min(warmup, 3)
         for i in range(warm):
             bo.token(make_tokens(cfg, T=1, batch=20_000 + i)[0])
-        budget, t0, steps = 120.0, time.perf_counter(), 0
-        while steps < args.steps:
-            bo.token(make_tokens(cfg, T=1, batch=30_000 + steps)[0])
-            steps += 1
+        t0, n = time.perf_counter(), 0
+        while n < steps:
+            bo.token(make_tokens(cfg, T=1, batch=30_000 + n)[0])
+            n += 1
             if time.perf_counter() - t0 > budget:
                 break
         el = time.perf_counter() - t0
-        value = steps / el
-        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": steps,
-                "warmup": warm, "ms_per_step": 1e3 * el / steps, "higher_is_better": True,
+        value = n / el
+        return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": n,
+                "warmup": warm, "ms_per_step": 1e3 * el / n, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "impl": "reference", "config": {"workload": wl_name, "tokens_per_step": 1},
                 "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                 "sample": f"{steps} one-token draft steps (of {args.steps} requested; capped "
+                                 "sample": f"{n} one-token draft steps (of {steps} requested; capped "
                                            f"at {budget:.0f} s), quantisation of the experts included"},
                 "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line), flush=True)
-        return
-    T = min(T, 32)  # a step is a bounded sample of the batch (tokens are independent)
     W = make_weights(cfg)
-    warm = min(args.warmup, 3)  # the oracle has no caches to warm beyond a first call
+    cores = host_cores()
+    Ts = min(T, 32)  # a step is a bounded sample of the batch (tokens are independent)
+    resident = None
+    if T > 64:
+        # prefill: tokens of one full batch, with the batch resident set of that batch
+        x_full = make_tokens(cfg, T=T, batch=30_000)
+        resident, _ = oracle.resident_mask(cfg, W, x_full)
+        order = np.random.default_rng(0).permutation(T)
+        Ts = min(32, max(cores, 8))
+    warm = min(warmup, 3)  # the oracle has no caches to warm beyond a first call
+
+    def one(i):
+        if resident is None:
+            oracle_step(cfg, W, make_tokens(cfg, T=Ts, batch=30_000 + i), wl_name)
+        else:
+            rows = np.sort(order[(i * Ts) % T:(i * Ts) % T + Ts])
+            oracle.layer_forward(cfg, W, x_full[rows], resident=resident)
+        return Ts
+
     for i in range(warm):
-        oracle_step(cfg, W, make_tokens(cfg, T=T, batch=20_000 + i), wl_name)
-    budget, t0, n, steps = 120.0, time.perf_counter(), 0, 0
-    while steps < args.steps:
-        oracle_step(cfg, W, make_tokens(cfg, T=T, batch=30_000 + steps), wl_name)
-        n += T
-        steps += 1
+        one(10_000 + i if resident is None else i)
+    t0, n, k = time.perf_counter(), 0, 0
+    while k < steps:
+        n += one(k)
+        k += 1
         if time.perf_counter() - t0 > budget:
             break
     el = time.perf_counter() - t0
     value = n / el
-    cores = min(oracle.num_threads(), T)
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": steps,
-            "warmup": warm, "ms_per_step": 1e3 * el / steps, "higher_is_better": True,
+    used = min(oracle.num_threads(), Ts)
+    what = (f"{k} steps of {Ts} tokens (of {steps} requested; capped at {budget:.0f} s)" if resident is None else
+            f"{k} steps of {Ts} of the {T} tokens of one prefill batch (of {steps} requested; capped at "
+            f"{budget:.0f} s), the batch resident set computed beforehand")
+    return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": k,
+            "warmup": warm, "ms_per_step": 1e3 * el / k, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": wl_name, "tokens_per_step": T},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": f"{steps} steps of {T} tokens (of {args.steps} requested; "
-                                       f"capped at {budget:.0f} s)"},
+            "config": {"workload": wl_name, "tokens_per_step": Ts},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                             "sample": what},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
+
+
+def run_reference(args, wl_name, rank, with_prefill=False):
+    """The reference arm's line, printed by rank 0 only (the other ranks of a
+    torchrun launch exit without work); with_prefill adds the prefill
+    workload's oracle timing under "prefill"."""
+    if rank != 0:
+        return
+    line = reference_line(args, wl_name, args.steps, args.warmup)
+    if with_prefill:
+        line["prefill"] = nested(reference_line(args, PREFILL_WORKLOAD, max(3, min(args.steps, 100)),
+                                                args.warmup, budget=45.0))
     print(json.dumps(line), flush=True)
 
 
-def run_bitslice(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src):
+NESTED_DROP = ("metric", "n_gpus", "higher_is_better", "scaling", "vs_baseline", "data", "impl")
+
+
+def nested(line: dict) -> dict:
+    """A workload's line as the value of a key of another line."""
+    return {k: v for k, v in line.items() if k not in NESTED_DROP}
+
+
+def run_bitslice(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src, steps, warmup):
     """Timed draft layer with b-bit bit-sliced expert weights (see
     BITSLICE_WORKLOADS): one step = the bf16 router (moe_route, top-k gates)
     and one moe_bitslice_ffn call over the routed and the shared experts,
@@ -411,7 +568,7 @@ def run_bitslice(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src):
                       prob, dhat, pmask, None, None, ws, stream)
         ffn(i)
 
-    for i in range(max(args.warmup, n_copies)):
+    for i in range(max(warmup, n_copies)):
         step(i)
     st, det = moe.moe_check(ws)
     if st != moe.MOE_OK:
@@ -425,28 +582,17 @@ def run_bitslice(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src):
             step(c)
         graphs.append(g)
     launches_per_step = (moe.moe_launch_total() - n0) // n_graphs
-    for i in range(args.warmup):
+    for i in range(warmup):
         graphs[i % n_graphs].replay()
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(dev.index or 0) as clk:
-        ev0.record(stream)
-        for i in range(args.steps):
-            graphs[i % n_graphs].replay()
-        ev1.record(stream)
-        torch.cuda.synchronize()
-    barrier(world)
-    ms_total = max_over_ranks(world, ev0.elapsed_time(ev1))
-    ms_per_step = ms_total / args.steps
-    value = whole_job_tokens_per_s(world, T, args.steps, ms_total)
-    clocks = clk.summary()
+    ms_total, clocks = timed_replays(lambda i: graphs[i % n_graphs].replay(), n_graphs, steps, stream, dev, world)
+    ms_per_step = ms_total / steps
+    value = whole_job_tokens_per_s(world, T, steps, ms_total)
 
     # the bit-sliced FFN call alone (routing of each token batch in place):
     # algorithmic bytes = the top-b planes of the distinct routed experts and
     # the shared experts, plus their scales
-    n_k = max(50, min(2000, args.steps // 2))
+    n_k = max(50, min(2000, steps // 2))
     fb = []
     for c in range(n_x):
         step(c)
@@ -465,17 +611,18 @@ def run_bitslice(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src):
     torch.cuda.synchronize()
     k_ms = [a.elapsed_time(b) for a, b in evs]
     k_bytes = [fb[i % n_x] for i in range(n_k)]
-    achieved = sum(k_bytes) / (sum(k_ms) / 1e3) / 1e9
+    med_ms = statistics.median(k_ms)
+    achieved = statistics.mean(k_bytes) / (med_ms / 1e3) / 1e9
     roof = {"kernel": "moe_bitslice_ffn (bitslice_gateup_kernel + bitslice_down_kernel + bitslice_sum_kernel)",
-            "ffn_path": f"bitslice-b{bits}", "bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
-            "frac": achieved / hbm_gbs, "peak_source": peak_src,
-            "algorithmic_bytes_per_launch": float(statistics.mean(fb)), "avg_launch_ms": statistics.mean(k_ms),
-            "traffic": None}
+            "ffn_path": f"bitslice-b{bits}", "bound": "hbm", "achieved": achieved, "unit": "GB/s",
+            **fractions(achieved, hbm_gbs, NOMINAL_HBM_GBS, peak_src),
+            "algorithmic_bytes_per_launch": float(statistics.mean(fb)), "median_launch_ms": med_ms,
+            "avg_launch_ms": statistics.mean(k_ms), "launches_timed": n_k, "traffic": None}
 
     # end to end: pinned host x -> device, draft layer, y -> pinned host, every step
     x_host = [xs[c].cpu().pin_memory() for c in range(n_x)]
     y_host = torch.empty_like(y, device="cpu").pin_memory()
-    n_e2e = max(20, min(args.steps, 1000))
+    n_e2e = max(20, min(steps, 1000))
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(n_e2e):
@@ -486,8 +633,8 @@ def run_bitslice(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src):
     e2e_s = max_over_ranks(world, time.perf_counter() - t0)
     e2e_value = world * T * n_e2e / e2e_s
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": f"b{bits} bit planes of int8 (f32 accumulate)",
         "data": "synthetic (seeded N(0,0.02^2) weights, N(0,1) tokens; shapes of the named model)",
         "config": {"workload": wl_name, "tokens_per_step": T, "d": d, "experts": N, "top_k": k,
@@ -498,7 +645,7 @@ def run_bitslice(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src):
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": xs[0].numel() * xs[0].element_size(),
                 "d2h_bytes_per_step": y.numel() * 4, "steps": n_e2e,
                 "note": "moe_route + moe_bitslice_ffn per step with pinned-host copies and a stream sync, no graph"},
-        "gpu_launches": int(launches_per_step * args.steps),
+        "gpu_launches": int(launches_per_step * steps),
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -514,39 +661,20 @@ def run_bitslice(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src):
         line["cpu_baseline"] = {"value": n_tok / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                                 "sample": f"{n_tok} one-token draft steps ({el:.1f} s) through the float64 "
                                           f"oracle, single thread, experts quantised beforehand when first read"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    return line
 
 
-def main():
-    args = parse()
-    wl_name = args.workload
-    cfg_name, T, phase = WORKLOADS[wl_name][:3]
-    cfg = CONFIGS[cfg_name]
-    if len(WORKLOADS[wl_name]) > 3:
-        cfg = cfg.with_(keep_frac=WORKLOADS[wl_name][3])
-    if args.impl == "reference":
-        world = int(os.environ.get("WORLD_SIZE", "1"))
-        rank = int(os.environ.get("RANK", "0"))
-        run_reference(args, wl_name, cfg, T, world, rank)
-        return
-
+def run_workload(args, wl_name, world, rank, dev, steps, warmup, with_cpu=True):
+    """Measure one workload; returns its JSON line (a dict)."""
     import torch
     import expert_routing_ffn_gb300 as moe
-    from expert_routing_ffn_gb300.layer import DeviceLayer, LayerBuffers, forward, layer_args
+    from expert_routing_ffn_gb300.layer import DeviceLayer, LayerBuffers, forward
 
-    world, rank, local = dist_setup(args.gpus)
-    dev = torch.device("cuda", local if world > 1 else 0)
-    moe.lib()  # fails loudly if the CUDA library is missing
+    cfg, T, phase = workload_cfg(wl_name)
     hbm_gbs, bf16_tflops, peak_src = peaks()
-
     W = make_weights(cfg)
     if wl_name in BITSLICE_WORKLOADS:
-        run_bitslice(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src)
-        if world > 1:
-            import torch.distributed as dist
-            dist.destroy_process_group()
-        return
+        return run_bitslice(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src, steps, warmup)
     base = DeviceLayer(cfg, W, T, device=str(dev))
     esize = 2 if cfg.wtype == "bf16" else 4
     expert_bytes = 3 * cfg.I * cfg.d * esize
@@ -603,7 +731,7 @@ def main():
             forward(layers[c], bufs[c], xs[c], stream=stream)
 
     # eager warm-up, error check, then one CUDA graph per layer copy
-    for i in range(max(args.warmup, n_copies)):
+    for i in range(max(warmup, n_copies)):
         step(i)
     for L in layers:
         st, det = moe.moe_check(L.ws)
@@ -618,27 +746,23 @@ def main():
             step(c)
         graphs.append(g)
     launches_per_step = (moe.moe_launch_total() - n0) // n_graphs
-    for i in range(args.warmup):
+    for i in range(warmup):
         graphs[i % n_graphs].replay()
     torch.cuda.synchronize()
-    if cache_cfg:
-        cstats_t.zero_()
 
-    # ---- timed region: exactly K steps
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(dev.index or 0) as clk:
+    # ---- timed region: exactly K steps (clocks sampled over a window around them)
+    ms_total, clocks = timed_replays(lambda i: graphs[i % n_graphs].replay(), n_graphs, steps, stream, dev, world)
+    if cache_cfg:
+        # the cache counters of the timed steps only: restart them and replay again
+        cstats_t.zero_()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ev0.record(stream)
-        for i in range(args.steps):
+        for i in range(steps):
             graphs[i % n_graphs].replay()
         ev1.record(stream)
         torch.cuda.synchronize()
-    barrier(world)
-    ms_total = max_over_ranks(world, ev0.elapsed_time(ev1))
-    ms_per_step = ms_total / args.steps
-    value = whole_job_tokens_per_s(world, T, args.steps, ms_total)
-    clocks = clk.summary()
+    ms_per_step = ms_total / steps
+    value = whole_job_tokens_per_s(world, T, steps, ms_total)
 
     # ---- dominant kernel: the expert FFN stage, timed alone on the same stream
     # (route/select/permute outputs of each copy are already in place).
@@ -668,7 +792,7 @@ def main():
         else:
             fb.append(u * expert_bytes + shared_bytes)
         ff.append(6.0 * cfg.d * (int(off[-1]) * cfg.I + T * cfg.n_shared * cfg.I_shared))
-    n_k = max(10 if phase == "prefill" else 50, min(2000, args.steps // 2))
+    n_k = max(10 if phase == "prefill" else 50, min(2000, steps // 2))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_k)]
     for i in range(n_k + n_copies):
         c = i % n_copies
@@ -685,8 +809,9 @@ def main():
     k_bytes = [fb[(i + n_copies) % n_copies] for i in range(n_k)]
     k_flops = [ff[(i + n_copies) % n_copies] for i in range(n_k)]
     path = moe.moe_expert_ffn_path(layers[0].dims.with_T(T), cfg.keep_frac)
+    med_ms = statistics.median(k_ms)
     if phase == "decode":
-        achieved = sum(k_bytes) / (sum(k_ms) / 1e3) / 1e9
+        achieved = statistics.mean(k_bytes) / (med_ms / 1e3) / 1e9
         kname, ksrc = {
             "tc-decode": ("moe_expert_ffn (ffn_tcd_kernel + gemv_reduce_kernel)",
                           "ffn_tcd.cu"),
@@ -694,36 +819,37 @@ def main():
             "gemv-floe": ("moe_expert_ffn (floe up/select/union/plan + sparse ffn_gemv_kernel"
                           " + gemv_reduce_kernel)", "ffn_gemv.cu"),
         }.get(path, ("moe_expert_ffn (ffn_gemv_kernel + gemv_reduce_kernel)", "ffn_gemv.cu"))
-        roof = {"kernel": kname, "ffn_path": path, "bound": "hbm",
-                "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
-                "peak_source": peak_src, "algorithmic_bytes_per_launch": float(statistics.mean(fb)),
-                "avg_launch_ms": statistics.mean(k_ms),
+        roof = {"kernel": kname, "ffn_path": path, "bound": "hbm", "achieved": achieved, "unit": "GB/s",
+                **fractions(achieved, hbm_gbs, NOMINAL_HBM_GBS, peak_src),
+                "algorithmic_bytes_per_launch": float(statistics.mean(fb)), "median_launch_ms": med_ms,
+                "avg_launch_ms": statistics.mean(k_ms), "launches_timed": n_k,
                 "traffic": recorded_traffic(ksrc, wl_name)}
     else:
         # prefill: the bound is whichever roofline time is longer, the FLOPs at the
         # bf16 peak or the expert weight bytes at the HBM bandwidth (a short batch
         # of many experts, e.g. Granite-shaped at 1024 tokens, is HBM-bound)
-        tflops = sum(k_flops) / (sum(k_ms) / 1e3) / 1e12
-        gbs = sum(k_bytes) / (sum(k_ms) / 1e3) / 1e9
+        tflops = statistics.mean(k_flops) / (med_ms / 1e3) / 1e12
+        gbs = statistics.mean(k_bytes) / (med_ms / 1e3) / 1e9
         t_flop = statistics.mean(ff) / (bf16_tflops * 1e12)
         t_byte = statistics.mean(fb) / (hbm_gbs * 1e9)
         common = {"kernel": "moe_expert_ffn (gather + ffn_tc_kernel<1> + ffn_tc_kernel<2>)", "ffn_path": path}
         if t_byte > t_flop:
-            roof = dict(common, bound="hbm", achieved=gbs, peak=hbm_gbs, unit="GB/s", frac=gbs / hbm_gbs,
-                        peak_source=peak_src, tensor_frac=tflops / bf16_tflops)
+            roof = dict(common, bound="hbm", achieved=gbs, unit="GB/s",
+                        **fractions(gbs, hbm_gbs, NOMINAL_HBM_GBS, peak_src), tensor_frac=tflops / bf16_tflops)
         else:
-            roof = dict(common, bound="tensor", achieved=tflops, peak=bf16_tflops, unit="TFLOP/s",
-                        frac=tflops / bf16_tflops, peak_source=peak_src + " bf16 burst", hbm_frac=gbs / hbm_gbs)
+            roof = dict(common, bound="tensor", achieved=tflops, unit="TFLOP/s",
+                        **fractions(tflops, bf16_tflops, NOMINAL_BF16_TFLOPS, peak_src + " bf16 burst"),
+                        hbm_frac=gbs / hbm_gbs)
         roof.update({"algorithmic_flops_per_launch": float(statistics.mean(ff)),
                      "algorithmic_bytes_per_launch": float(statistics.mean(fb)),
-                     "avg_launch_ms": statistics.mean(k_ms),
+                     "median_launch_ms": med_ms, "avg_launch_ms": statistics.mean(k_ms), "launches_timed": n_k,
                      "traffic": recorded_traffic("ffn_tc.cu", wl_name)})
 
     # the cache counters of the timed steps
     cache_info = None
     if cache_cfg:
         cs = cstats_t.cpu().numpy().astype(np.int64)
-        steps_done = args.steps
+        steps_done = steps
         cache_info = {"capacity": capacity, "decay": decay, "start": f"experts 0..{capacity - 1}",
                       "hit_rate": float(cs[0]) / max(1, cs[1]), "miss_rate": 1.0 - float(cs[0]) / max(1, cs[1]),
                       "admitted_per_step": float(cs[2]) / steps_done, "evicted_per_step": float(cs[3]) / steps_done,
@@ -788,7 +914,7 @@ def main():
     # forward, result -> pinned host, every step
     x_host = [xs[c].cpu().pin_memory() for c in range(n_x)]
     out_host = [torch.empty_like(bufs[c].out, device="cpu").pin_memory() for c in range(n_copies)]
-    n_e2e = max(5 if phase == "prefill" else 20, min(args.steps, 1000))
+    n_e2e = max(5 if phase == "prefill" else 20, min(steps, 1000))
     if cache_cfg:
         host_w_c = [[layers[0].w_gate[e].cpu().pin_memory() for e in range(cfg.N)],
                     [layers[0].w_up[e].cpu().pin_memory() for e in range(cfg.N)],
@@ -871,7 +997,7 @@ def main():
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "steps": steps, "warmup": warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": cfg.wtype if cfg.wtype == "bf16" else "f32",
         "data": "synthetic (seeded N(0,0.02^2) weights, N(0,1) tokens; shapes of the named model)",
@@ -886,7 +1012,7 @@ def main():
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": xs[0].numel() * xs[0].element_size(),
                 "d2h_bytes_per_step": bufs[0].out.numel() * 4, "steps": n_e2e,
                 "note": "moe_layer_forward per step with pinned-host copies and a stream sync, no graph"},
-        "gpu_launches": int(launches_per_step * args.steps),
+        "gpu_launches": int(launches_per_step * steps),
         "staging": staging,
         "routing": routing,
         "clocks": clocks,
@@ -909,8 +1035,48 @@ def main():
         line["e2e"]["note"] += "; plus the cache update, the admitted-expert mask read back and the admitted " \
                                "experts staged from pinned host memory"
         line["cache"] = cache_info
-    if rank == 0 and not args.no_cpu_baseline:
+    # the whole step against the same bound: the FFN's algorithmic work plus
+    # the router and prefetch-router weights (decode) or FLOPs (prefill)
+    router_bytes = 2 * cfg.N * cfg.d * esize + 4 * cfg.d
+    if roof["bound"] == "hbm":
+        work = float(statistics.mean(fb)) + router_bytes
+        ach = work / (ms_per_step / 1e3) / 1e9
+        line["layer_roofline"] = {"bound": "hbm", "bytes_per_step": work, "achieved": ach, "unit": "GB/s",
+                                  **fractions(ach, hbm_gbs, NOMINAL_HBM_GBS, peak_src)}
+    else:
+        work = float(statistics.mean(ff)) + 2.0 * T * 2 * cfg.N * cfg.d
+        ach = work / (ms_per_step / 1e3) / 1e12
+        line["layer_roofline"] = {"bound": "tensor", "flops_per_step": work, "achieved": ach, "unit": "TFLOP/s",
+                                  **fractions(ach, bf16_tflops, NOMINAL_BF16_TFLOPS, peak_src + " bf16 burst")}
+    if rank == 0 and with_cpu and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, W, T, args.cpu_seconds, wl_name=wl_name)
+    del layers, bufs, base
+    return line
+
+
+def main():
+    args = parse()
+    wl_name = args.workload
+    both = wl_name == DEFAULT_WORKLOAD and not args.no_prefill
+    if args.impl == "reference":
+        run_reference(args, wl_name, int(os.environ.get("RANK", "0")), both)
+        return
+
+    import torch
+    import expert_routing_ffn_gb300 as moe
+
+    world, rank, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local if world > 1 else 0)
+    moe.lib()  # fails loudly if the CUDA library is missing
+    line = run_workload(args, wl_name, world, rank, dev, args.steps, args.warmup)
+    if both:
+        # the prefill half of the metric: the largest single-GPU layer shape,
+        # its own timed steps, roofline, end-to-end figure and CPU baseline
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        pf = run_workload(args, PREFILL_WORKLOAD, world, rank, dev, max(10, min(args.steps, 100)),
+                          max(3, min(args.warmup, 5)))
+        line["prefill"] = nested(pf)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

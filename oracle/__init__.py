@@ -77,6 +77,8 @@ def lib():
         if _lib is None:
             L = C.CDLL(build())
             L.orc_num_threads.restype = C.c_int
+            L.orc_set_num_threads.argtypes = [C.c_int]
+            L.orc_set_num_threads.restype = None
             L.orc_logits.argtypes = [C.c_int, C.c_int, C.c_int, _FP, _FP, _FP, _DP]
             L.orc_softmax.argtypes = [C.c_int, _DP, _DP]
             L.orc_topk.argtypes = [C.c_int, C.c_int, _DP, _IP]
@@ -136,6 +138,11 @@ def f32(a) -> np.ndarray:
 
 def num_threads() -> int:
     return lib().orc_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    """OpenMP threads of the calling Python thread's later oracle calls."""
+    lib().orc_set_num_threads(int(n))
 
 
 # ---- single steps (used by the pins) -------------------------------------

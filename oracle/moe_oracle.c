@@ -62,6 +62,15 @@ int orc_num_threads(void) {
 #endif
 }
 
+/* Threads of the calling thread's later parallel regions (n >= 1). */
+void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* Does value a (index ia) rank above value b (index ib)?  Larger first,
  * equal values ordered by the lower index. */
 static int ranks_above(double a, int ia, double b, int ib) {

@@ -68,9 +68,8 @@ def test_two_gloo_ranks_agree_on_time_and_whole_job_tokens():
 def test_reference_arm_prints_on_rank_zero_only():
     sys.path.insert(0, ROOT)
     import bench
-    from workloads import CONFIGS
     args = type("A", (), {"steps": 1, "warmup": 3})()
     buf = io.StringIO()
     with contextlib.redirect_stdout(buf):
-        bench.run_reference(args, "tiny-test", CONFIGS["tiny"], 2, 2, 1)
+        bench.run_reference(args, "dsv2lite-decode-T8", 1, with_prefill=True)
     assert buf.getvalue() == ""

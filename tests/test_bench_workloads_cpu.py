@@ -38,3 +38,27 @@ def test_oracle_steps_of_the_added_workloads_run():
     for y in ys.values():
         assert y.shape == (cfg.d,) and np.isfinite(y).all()
     assert np.linalg.norm(ys[2] - ys[8]) > np.linalg.norm(ys[4] - ys[8]) > 0
+
+
+def test_cpu_baseline_uses_every_core_and_reports_one_thread():
+    """Decode: several T-token batches at once so that every core of the
+    affinity mask has a token; prefill: tokens of one batch, one per core.
+    Both carry a single-thread figure."""
+    cfg = CONFIGS["tiny"]
+    W = make_weights(cfg)
+    r = bench.cpu_baseline(cfg, W, 2, 0.2)
+    cores = bench.host_cores()
+    assert r["kind"] == "oracle" and r["value"] > 0
+    assert r["cores"] == 2 * max(1, cores // 2) or cores < 2
+    assert r["single_thread"]["cores"] == 1 and r["single_thread"]["value"] > 0
+    p = bench.cpu_baseline(cfg, W, 96, 0.2)
+    assert p["cores"] == cores and p["value"] > 0 and p["single_thread"]["value"] > 0
+    assert "of the 96 tokens" in p["sample"]
+
+
+def test_fractions_and_nested_lines():
+    f = bench.fractions(5000.0, 6694.5, bench.NOMINAL_HBM_GBS, "measured")
+    assert f["frac"] == 5000.0 / 6694.5 and f["frac_of_nominal"] == 5000.0 / 8000.0
+    line = {"metric": "m", "value": 1.0, "impl": "reference", "roofline": {}, "n_gpus": 1}
+    assert bench.nested(line) == {"value": 1.0, "roofline": {}}
+    assert bench.WORKLOADS[bench.PREFILL_WORKLOAD][2] == "prefill"
