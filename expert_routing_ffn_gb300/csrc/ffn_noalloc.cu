@@ -18,9 +18,14 @@
 //     ordering between them, or different host threads) race on the array.
 //     Order them on one stream, or use moe_expert_ffn with separate
 //     workspaces.
-// The array's device address is looked up once per device, with that device
-// current, on the first call made while it is current; make that first call
+// The array's device address is looked up once per CUDA context (the first
+// call made while that context is current does it), and remembered under the
+// context's unique ID: a context created later, after cudaDeviceReset or by
+// the driver API, gets its own lookup.  Make the first call in a context
 // outside of any stream capture.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -36,29 +41,80 @@ constexpr size_t kScratchBytes = (size_t)16 << 20;
 static __device__ __align__(256) unsigned char g_ffn_scratch[kScratchBytes];
 
 std::mutex g_mu;
-void* g_scratch_dev[64] = {};
-int g_sms[64] = {};
 
-// Device address of g_ffn_scratch and the SM count of the current device,
-// found once per device (the first call on a device does this set-up).
-cudaError_t scratch_for_current_device(void** ptr, int* sms) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_dev[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_ffn_scratch);
-        if (e != cudaSuccess) return e;
-        int n = 0;
-        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        g_sms[dev] = n;
-        g_scratch_dev[dev] = p;
+// One remembered lookup: the context's ID, the array's address in it and the
+// SM count of its device.
+struct ScratchEntry {
+    unsigned long long ctx_id;
+    void* ptr;
+    int sms;
+};
+constexpr int kMaxContexts = 64;
+ScratchEntry g_entries[kMaxContexts] = {};
+int g_n_entries = 0, g_next_slot = 0;
+
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+
+// ID of the context current on this thread; 0 if there is none.
+cudaError_t current_context_id(unsigned long long* id) {
+    *id = 0;
+    if (!g_ctx_current || !g_ctx_id) {
+        void* a = nullptr;
+        void* b = nullptr;
+        cudaDriverEntryPointQueryResult qa, qb;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 4000, cudaEnableDefault, &qa) != cudaSuccess ||
+            qa != cudaDriverEntryPointSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) != cudaSuccess ||
+            qb != cudaDriverEntryPointSuccess)
+            return cudaErrorNotSupported;
+        g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(a);
+        g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(b);
     }
-    *ptr = g_scratch_dev[dev];
-    *sms = g_sms[dev];
+    CUcontext ctx = nullptr;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (!ctx) return cudaSuccess;
+    return g_ctx_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Device address of g_ffn_scratch in the current context and the SM count of
+// the current device (the first call in a context does this set-up).
+cudaError_t scratch_for_current_device(void** ptr, int* sms) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    unsigned long long id = 0;
+    cudaError_t e = current_context_id(&id);
+    if (e != cudaSuccess) return e;
+    if (id != 0)
+        for (int i = 0; i < g_n_entries; ++i)
+            if (g_entries[i].ctx_id == id) {
+                *ptr = g_entries[i].ptr;
+                *sms = g_entries[i].sms;
+                return cudaSuccess;
+            }
+    // set-up in this context: the runtime makes the device's primary context
+    // current if none is, and loads the module that holds the array
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_ffn_scratch);
+    if (e != cudaSuccess) return e;
+    int dev = 0, n = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (id == 0) {
+        e = current_context_id(&id);
+        if (e != cudaSuccess) return e;
+    }
+    if (id != 0) {
+        ScratchEntry& slot = g_entries[g_next_slot];
+        slot.ctx_id = id;
+        slot.ptr = p;
+        slot.sms = n;
+        g_next_slot = (g_next_slot + 1) % kMaxContexts;
+        if (g_n_entries < kMaxContexts) ++g_n_entries;
+    }
+    *ptr = p;
+    *sms = n;
     return cudaSuccess;
 }
 

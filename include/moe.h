@@ -276,8 +276,11 @@ moe_status moe_floe_kept_mask(const moe_dims* dims, void* ws, size_t ws_bytes, c
  *   before anything is queued (decode sizes fit: e.g. 32 tokens at d = 2048
  *   or d = 4096).  device_status (device int32[2], may be NULL) receives the
  *   call's device error code and detail when its kernels have run.
- *   The first call on a device looks the array up (cudaGetSymbolAddress);
- *   make it outside of any stream capture.  All calls share the array: calls
+ *   The first call in a CUDA context looks the array's address up
+ *   (cudaGetSymbolAddress) and remembers it under the context's unique ID,
+ *   so a context made after cudaDeviceReset, or a non-primary one, gets its
+ *   own lookup; make that first call outside of any stream capture.
+ *   All calls share the array: calls
  *   whose kernels overlap on the GPU race, so order them on one stream.
  *   Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call. */
 moe_status moe_expert_ffn_noalloc(const moe_dims* dims, const void* x, const void* table,
