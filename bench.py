@@ -61,6 +61,7 @@ WORKLOADS = {
     "dsv2lite-cache-decode-T1": ("dsv2lite", 1, "decode"),
     "dsv2lite-lookahead-decode-T8": ("dsv2lite", 8, "decode"),
     "dsv2lite-bitslice4-draft-T1": ("dsv2lite", 1, "decode"),
+    "dsv2lite-hetero-decode-T8": ("dsv2lite", 8, "decode"),
 }
 # Multi-step decode with a persistent expert cache (ELMoE-3D heat map with
 # decay): the layer runs every step with resident = the cache, which
@@ -73,10 +74,19 @@ CACHE_WORKLOADS = {"dsv2lite-cache-decode-T1": (24, 0.99, 64)}
 # name -> (look-ahead layers J, confidence threshold tau, minimum depth d_min)
 LOOKAHEAD_WORKLOADS = {"dsv2lite-lookahead-decode-T8": (4, 0.3, 1)}
 PCIE4_X16_BYTES_PER_S = 32e9
+# the cost model of the oracle's HETERO step (reference arm, CPU baseline):
+# a 17.3 MB expert over PCIe 4.0 x16, 5 us on the GPU, 200 us per host row
+PCIE4_HETERO_COST = dict(link_bps=PCIE4_X16_BYTES_PER_S, expert_bytes=17301504.0, gpu_expert_s=5e-6,
+                         cpu_row_s=200e-6, hidden_bytes=4096.0)
 # Draft layer with ELMoE-3D bit-sliced expert weights: per token, the router
 # (bf16) picks the top-k experts, whose FFN (and the shared experts') runs on
 # the top b bit planes of INT8 weights (moe_bitslice_ffn).  name -> b
 BITSLICE_WORKLOADS = {"dsv2lite-bitslice4-draft-T1": 4}  # the host link of the pages' offloading setups
+# SPICE's heterogeneous orchestration: high-confidence misses (router prob >=
+# gamma) computed exactly, each missing expert fetched or run on the host cores
+# by the per-miss cost model with parameters measured in the same run; also run
+# with the link of the pages' PCIe 4.0 x16 setups.  name -> None
+HETERO_WORKLOADS = {"dsv2lite-hetero-decode-T8": None}
 DEFAULT_WORKLOAD = "dsv2lite-decode-T8"
 METRIC = "MoE-layer tokens/sec (decode & prefill) and % of HBM/tensor roofline, 1xGB300"
 FALLBACK_HBM_GBS = 6800.0
@@ -288,6 +298,9 @@ def oracle_step(cfg, W, x, wl_name):
     and for a look-ahead workload the prefetch depth over its look-ahead
     routers."""
     import oracle
+    if wl_name in HETERO_WORKLOADS:
+        oracle.layer_forward(cfg, W, x, policy=oracle.POL_HETERO, cost=PCIE4_HETERO_COST)
+        return
     oracle.layer_forward(cfg, W, x)
     la = LOOKAHEAD_WORKLOADS.get(wl_name)
     if la:
@@ -664,6 +677,159 @@ def run_bitslice(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src, 
     return line
 
 
+def run_hetero(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src, steps, warmup):
+    """Timed layer steps on the heterogeneous CPU-GPU path
+    (moe_layer_forward_hetero): the cost model's parameters are measured
+    first (the host link by expert copies, the GPU time of one expert from
+    the decode FFN stage, the host time of one expert row from
+    moe_cpu_experts), then the layer runs with them and again with the link
+    of a PCIe 4.0 x16 setup.  A step is host-orchestrated (the host waits for
+    the decisions), so it is timed on the host clock around synchronised
+    steps; the LoRE/substitute-only policy (HYBRID) is timed the same way
+    for comparison."""
+    import torch
+    import expert_routing_ffn_gb300 as moe
+    from expert_routing_ffn_gb300.layer import DeviceLayer, HeteroHost, LayerBuffers, forward, forward_hetero
+    esize = 2
+    expert_bytes = 3 * cfg.I * cfg.d * esize
+    layer = DeviceLayer(cfg, W, T, device=str(dev))
+    host = HeteroHost(layer, T)
+    bufs = LayerBuffers(layer, T)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
+    side = torch.cuda.Stream(device=dev)
+    ev = torch.cuda.Event()
+    n_x = 64
+    xs = [torch.from_numpy(make_tokens(cfg, T=T, batch=replica_batch(rank, i))).to(dev).to(layer.dt).contiguous()
+          for i in range(n_x)]
+    D = layer.dims.with_T(T)
+
+    # link: 8 experts from pinned host memory
+    mask = (1 << 8) - 1
+    moe.moe_stage_experts(D, mask, host.w_gate, host.w_up, host.w_down, list(layer.w_gate), list(layer.w_up),
+                          list(layer.w_down), side, ev)
+    side.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(3):
+        nb = moe.moe_stage_experts(D, mask, host.w_gate, host.w_up, host.w_down, list(layer.w_gate),
+                                   list(layer.w_up), list(layer.w_down), side, ev)
+    side.synchronize()
+    link = 3 * nb / (time.perf_counter() - t0)
+    # GPU time of one expert: the decode FFN stage's bytes per second applied to one expert
+    forward(layer, bufs, xs[0], stream=stream)
+    torch.cuda.synchronize()
+    off = bufs.expert_offsets.cpu().numpy()
+    u = int((np.diff(off) > 0).sum())
+    ffn_bytes = u * expert_bytes + cfg.n_shared * 3 * cfg.I_shared * cfg.d * esize
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(30)]
+    for a, b in evs:
+        a.record(stream)
+        moe.moe_expert_ffn(D, xs[0], layer.table, bufs.expert_offsets, bufs.perm, 1.0, bufs.y_perm, bufs.y_shared,
+                           layer.ws, stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    ffn_ms = statistics.median([a.elapsed_time(b) for a, b in evs])
+    gpu_expert_s = expert_bytes / (ffn_bytes / (ffn_ms / 1e3))
+    # host time of one expert row: moe_cpu_experts on one host slot
+    hk = torch.zeros((T, cfg.k), dtype=torch.int32)
+    hi = torch.zeros((T, cfg.k), dtype=torch.int32)
+    for t in range(T):
+        hi[t] = torch.arange(cfg.k, dtype=torch.int32) + t
+    hk[0, 0] = moe.MOE_KIND_CPU
+    host.x.copy_(xs[0].cpu())
+    times = []
+    for _ in range(12):
+        t1 = time.perf_counter()
+        moe.moe_cpu_experts(D, host.x, hi, hk, host.w_gate, host.w_up, host.w_down, host.y_rows, host.scratch)
+        times.append(time.perf_counter() - t1)
+    cpu_row_s = statistics.median(times[2:])
+    measured = dict(link_bps=link, expert_bytes=float(expert_bytes), gpu_expert_s=gpu_expert_s,
+                    cpu_row_s=cpu_row_s, hidden_bytes=float(cfg.d * esize))
+    pcie = dict(measured, link_bps=PCIE4_X16_BYTES_PER_S)
+
+    def lib_cost(c):
+        return moe.hetero_cost(c["link_bps"], c["expert_bytes"], c["gpu_expert_s"], c["cpu_row_s"], c["hidden_bytes"])
+
+    def timed(cost, n):
+        cst = lib_cost(cost)
+        acc = {"cpu_slots": 0, "fetch_experts": 0, "lore_slots": 0, "fetch_bytes": 0.0, "cpu_link_bytes": 0.0,
+               "host_ms": 0.0, "wait_ms": 0.0}
+        for i in range(max(3, warmup)):
+            forward_hetero(layer, bufs, xs[i % n_x], host, cst, side, ev, stream=stream)
+        stream.synchronize()
+        t1 = time.perf_counter()
+        for i in range(n):
+            st = forward_hetero(layer, bufs, xs[i % n_x], host, cst, side, ev, stream=stream)
+            stream.synchronize()
+            for key in acc:
+                acc[key] += getattr(st, key)
+        el = time.perf_counter() - t1
+        res = {"tokens_per_s": T * n / el, "ms_per_step": 1e3 * el / n, "steps": n,
+               "fetch_min_rows": moe.moe_hetero_fetch_min_rows(cst)}
+        res.update({f"{key}_per_step": v / n for key, v in acc.items()})
+        return res, el
+
+    n_steps = max(20, min(steps, 400))
+    main_res, el = timed(measured, n_steps)
+    pcie_res, _ = timed(pcie, n_steps)
+    # the LoRE/substitute-only policy, eager and synchronised the same way
+    for i in range(3):
+        forward(layer, bufs, xs[i % n_x], stream=stream)
+    stream.synchronize()
+    t1 = time.perf_counter()
+    for i in range(n_steps):
+        forward(layer, bufs, xs[i % n_x], stream=stream)
+        stream.synchronize()
+    hybrid_tps = T * n_steps / (time.perf_counter() - t1)
+    st, det = moe.moe_check(layer.ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device error {moe.status_string(st)} ({det})")
+
+    # end to end: pinned host x -> device, the hetero step, out -> pinned host
+    x_host = [xs[c].cpu().pin_memory() for c in range(n_x)]
+    out_host = torch.empty_like(bufs.out, device="cpu").pin_memory()
+    cst = lib_cost(measured)
+    t1 = time.perf_counter()
+    for i in range(n_steps):
+        xs[i % n_x].copy_(x_host[i % n_x], non_blocking=True)
+        forward_hetero(layer, bufs, xs[i % n_x], host, cst, side, ev, stream=stream)
+        out_host.copy_(bufs.out, non_blocking=True)
+        stream.synchronize()
+    e2e_value = world * T * n_steps / max_over_ranks(world, time.perf_counter() - t1)
+    value = world * T * n_steps / max_over_ranks(world, el)
+    ach = ffn_bytes / (ffn_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": n_steps,
+        "warmup": max(3, warmup), "ms_per_step": main_res["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,0.02^2) weights, N(0,1) tokens; shapes of the named model)",
+        "config": {"workload": wl_name, "tokens_per_step": T, "d": cfg.d, "experts": cfg.N, "top_k": cfg.k,
+                   "intermediate": cfg.I, "shared_experts": cfg.n_shared, "miss_policy": "hetero",
+                   "gamma": cfg.gamma, "resident": cfg.n_resident, "parallelism": f"replicas x{world}",
+                   "timing": "host clock around synchronised steps (the host waits for each step's decisions)",
+                   "l2": "one layer copy; every fetched expert is copied in from pinned host memory each step"},
+        "roofline": {"kernel": "moe_expert_ffn (decode FFN stage of this layer, timed alone)", "bound": "hbm",
+                     "achieved": ach, "unit": "GB/s", **fractions(ach, hbm_gbs, NOMINAL_HBM_GBS, peak_src),
+                     "algorithmic_bytes_per_launch": float(ffn_bytes), "median_launch_ms": ffn_ms,
+                     "traffic": None},
+        "hetero": {"cost_measured": measured, "measured_link": main_res, "pcie4_x16_link": dict(pcie_res, cost=pcie),
+                   "hybrid_policy_tokens_per_s": hybrid_tps,
+                   "note": "cpu slots, fetched experts and link bytes per step; HYBRID = LoRE or substitute for "
+                           "every miss (no exact miss), the same host-synchronised loop"},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": xs[0].numel() * 2,
+                "d2h_bytes_per_step": bufs.out.numel() * 4, "steps": n_steps,
+                "note": "moe_layer_forward_hetero per step with pinned-host copies of x and out"},
+        "gpu_launches": None,
+    }
+    n0 = moe.moe_launch_total()
+    forward_hetero(layer, bufs, xs[0], host, cst, side, ev, stream=stream)
+    stream.synchronize()
+    line["gpu_launches"] = int((moe.moe_launch_total() - n0) * n_steps)
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, W, T, args.cpu_seconds, wl_name=wl_name)
+    return line
+
+
 def run_workload(args, wl_name, world, rank, dev, steps, warmup, with_cpu=True):
     """Measure one workload; returns its JSON line (a dict)."""
     import torch
@@ -675,6 +841,8 @@ def run_workload(args, wl_name, world, rank, dev, steps, warmup, with_cpu=True):
     W = make_weights(cfg)
     if wl_name in BITSLICE_WORKLOADS:
         return run_bitslice(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src, steps, warmup)
+    if wl_name in HETERO_WORKLOADS:
+        return run_hetero(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src, steps, warmup)
     base = DeviceLayer(cfg, W, T, device=str(dev))
     esize = 2 if cfg.wtype == "bf16" else 4
     expert_bytes = 3 * cfg.I * cfg.d * esize

@@ -24,11 +24,13 @@ LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CAPACITY = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_STAGING, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_INDEX = 4, 5, 6, 7
 MOE_DTYPE_F32, MOE_DTYPE_BF16 = 0, 1
-MOE_MISS_EXACT, MOE_MISS_SUBSTITUTE, MOE_MISS_LORE, MOE_MISS_HYBRID = 0, 1, 2, 3
-MOE_KIND_COMPUTE, MOE_KIND_FETCH, MOE_KIND_LORE = 0, 1, 2
-MOE_NUM_COUNTERS = 8
+MOE_MISS_EXACT, MOE_MISS_SUBSTITUTE, MOE_MISS_LORE, MOE_MISS_HYBRID, MOE_MISS_HETERO = 0, 1, 2, 3, 4
+MOE_KIND_COMPUTE, MOE_KIND_FETCH, MOE_KIND_LORE, MOE_KIND_CPU = 0, 1, 2, 3
+(MOE_CNT_HIT, MOE_CNT_SUBSTITUTE, MOE_CNT_LORE, MOE_CNT_FETCH, MOE_CNT_OVERLAP, MOE_CNT_DELTA_HAT,
+ MOE_CNT_DELTA_STAR, MOE_CNT_SHORTFALL, MOE_CNT_CPU) = range(9)
+MOE_NUM_COUNTERS = 9
 COUNTER_NAMES = ["hit", "substitute", "lore", "fetch", "overlap", "delta_hat_sum",
-                 "delta_star_sum", "shortfall"]
+                 "delta_star_sum", "shortfall", "cpu"]
 
 
 class MoeError(RuntimeError):
@@ -69,6 +71,27 @@ class moe_layer_outputs(C.Structure):
         "expert_offsets", "perm", "inv_perm", "y_perm", "y_shared", "y_lore", "out")]
 
 
+class moe_hetero_cost(C.Structure):
+    """SPICE's per-miss cost model: link bytes/s, expert bytes, GPU seconds of
+    one expert, host seconds per token row of one expert, hidden-state bytes."""
+    _fields_ = [(n, C.c_double) for n in ("link_bytes_per_s", "expert_bytes", "gpu_expert_s", "cpu_row_s",
+                                          "hidden_bytes")]
+
+
+class moe_hetero_host(C.Structure):
+    _fields_ = [("x", _VP), ("final_idx", _VP), ("final_kind", _VP), ("masks", _VP), ("y_rows", _VP),
+                ("scratch", _VP), ("scratch_bytes", C.c_size_t)]
+
+
+class moe_hetero_stats(C.Structure):
+    _fields_ = [("cpu_slots", C.c_int32), ("fetch_experts", C.c_int32), ("fetch_min_rows", C.c_int32),
+                ("lore_slots", C.c_int32), ("fetch_bytes", C.c_double), ("cpu_link_bytes", C.c_double),
+                ("host_ms", C.c_double), ("wait_ms", C.c_double)]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
 _lib = None
 _lock = threading.Lock()
 
@@ -107,6 +130,15 @@ _PROTOS = {
     "moe_layer_forward": ([_DIMS, C.POINTER(moe_layer_args), C.POINTER(moe_layer_outputs), _P, _SZ,
                            _P], C.c_int),
     "moe_check": ([_P, _P, C.POINTER(C.c_int), C.POINTER(C.c_int32)], C.c_int),
+    "moe_hetero_fetch_min_rows": ([C.POINTER(moe_hetero_cost)], C.c_int),
+    "moe_select_hetero": ([_DIMS, _P, _P, _P, _P, _F, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
+                          C.c_int),
+    "moe_cpu_experts_scratch_size": ([_DIMS], C.c_size_t),
+    "moe_cpu_experts": ([_DIMS, _P, _P, _P, _P, _P, _P, _I, _P, _P, _SZ, C.POINTER(C.c_int32),
+                         C.POINTER(C.c_int32)], C.c_int),
+    "moe_layer_forward_hetero": ([_DIMS, C.POINTER(moe_layer_args), C.POINTER(moe_layer_outputs),
+                                  C.POINTER(moe_hetero_cost), _P, _P, _P, _P, _P, _P, C.POINTER(moe_hetero_host),
+                                  _I, _P, _SZ, _P, _P, _P, C.POINTER(moe_hetero_stats)], C.c_int),
     "moe_testing_fail_copies_after": ([C.c_int], None),
     "moe_testing_wait_timeout": ([C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
 }
@@ -431,6 +463,105 @@ def moe_layer_forward(dims, args: moe_layer_args, outs: moe_layer_outputs, ws, s
     _check(lib().moe_layer_forward(C.byref(dims), C.byref(args), C.byref(outs),
                                    _ptr(ws, torch.uint8, name="ws"), ws.numel(), _stream(stream)),
            "moe_layer_forward")
+
+
+def hetero_cost(link_bytes_per_s, expert_bytes, gpu_expert_s, cpu_row_s, hidden_bytes) -> moe_hetero_cost:
+    c = moe_hetero_cost()
+    c.link_bytes_per_s, c.expert_bytes, c.gpu_expert_s = link_bytes_per_s, expert_bytes, gpu_expert_s
+    c.cpu_row_s, c.hidden_bytes = cpu_row_s, hidden_bytes
+    return c
+
+
+def moe_hetero_fetch_min_rows(cost: moe_hetero_cost) -> int:
+    """The smallest number of a missing expert's token rows for which
+    fetching it beats computing it on the host (SPICE's cost model)."""
+    v = lib().moe_hetero_fetch_min_rows(C.byref(cost))
+    if v < 0:
+        raise ValueError("moe_hetero_fetch_min_rows: bad cost model")
+    return int(v)
+
+
+def moe_select_hetero(dims, router_prob, topk_idx, prefetch_mask, resident, gamma, fetch_min_rows, delta_hat,
+                      delta_star, final_idx, final_gate, final_kind, perm, inv_perm, fetch_mask, cpu_mask,
+                      counters, ws, stream=None):
+    T, N, k = dims.T, dims.N, dims.k
+    _check(lib().moe_select_hetero(
+        C.byref(dims), _ptr(router_prob, torch.float32, T * N, "router_prob"),
+        _ptr(topk_idx, torch.int32, T * k, "topk_idx"),
+        _ptr(prefetch_mask, torch.int64, T, "prefetch_mask", True),
+        _ptr(resident, torch.int64, 1, "resident", True), float(gamma), int(fetch_min_rows),
+        _ptr(delta_hat, torch.int32, T, "delta_hat", True), _ptr(delta_star, torch.int32, T, "delta_star", True),
+        _ptr(final_idx, torch.int32, T * k, "final_idx"), _ptr(final_gate, torch.float32, T * k, "final_gate"),
+        _ptr(final_kind, torch.int32, T * k, "final_kind"), _ptr(perm, torch.int32, T * k, "perm"),
+        _ptr(inv_perm, torch.int32, T * k, "inv_perm"), _ptr(fetch_mask, torch.int64, 1, "fetch_mask", True),
+        _ptr(cpu_mask, torch.int64, 1, "cpu_mask", True),
+        _ptr(counters, torch.int32, MOE_NUM_COUNTERS, "counters", True),
+        _ptr(ws, torch.uint8, name="ws"), ws.numel(), _stream(stream)), "moe_select_hetero")
+
+
+def moe_cpu_experts_scratch_size(dims) -> int:
+    return int(lib().moe_cpu_experts_scratch_size(C.byref(dims)))
+
+
+def _host_ptr(t, dtype, numel, name):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if t.numel() < numel:
+        raise ValueError(f"{name} has {t.numel()} elements, needs {numel}")
+    return C.c_void_p(t.data_ptr())
+
+
+def _host_array(ts, name):
+    a = (C.c_void_p * len(ts))()
+    for i, t in enumerate(ts):
+        if t is None:
+            continue
+        if t.is_cuda:
+            raise TypeError(f"{name}[{i}] must be host memory")
+        a[i] = t.data_ptr()
+    return a
+
+
+def moe_cpu_experts(dims, host_x, host_final_idx, host_final_kind, host_w_gate, host_w_up, host_w_down, host_y_rows,
+                    scratch, n_threads=0):
+    """The host slots' expert FFN on the host cores (all host tensors):
+    returns (rows computed, y_perm row of the first)."""
+    T, d, k = dims.T, dims.d, dims.k
+    n_rows, first = C.c_int32(), C.c_int32()
+    arrs = [_host_array(w, n) for w, n in ((host_w_gate, "host_w_gate"), (host_w_up, "host_w_up"),
+                                            (host_w_down, "host_w_down"))]
+    _check(lib().moe_cpu_experts(
+        C.byref(dims), _host_ptr(host_x, wdtype(dims), T * d, "host_x"),
+        _host_ptr(host_final_idx, torch.int32, T * k, "host_final_idx"),
+        _host_ptr(host_final_kind, torch.int32, T * k, "host_final_kind"),
+        *[C.cast(a, C.c_void_p) for a in arrs], int(n_threads),
+        _host_ptr(host_y_rows, torch.float32, T * k * d, "host_y_rows"),
+        _host_ptr(scratch, torch.uint8, 0, "scratch"), scratch.numel(), C.byref(n_rows), C.byref(first)),
+        "moe_cpu_experts")
+    return n_rows.value, first.value
+
+
+def moe_layer_forward_hetero(dims, args: moe_layer_args, outs: moe_layer_outputs, cost: moe_hetero_cost,
+                             host_w_gate, host_w_up, host_w_down, dev_w_gate, dev_w_up, dev_w_down,
+                             host: moe_hetero_host, ws, stage_stream, stage_event, n_threads=0, stream=None):
+    """One layer forward on the heterogeneous CPU-GPU path; returns its stats."""
+    st = moe_hetero_stats()
+    hw = [_host_array(w, n) for w, n in ((host_w_gate, "host_w_gate"), (host_w_up, "host_w_up"),
+                                          (host_w_down, "host_w_down"))]
+    dw = [_ptr_array(w, n) for w, n in ((dev_w_gate, "dev_w_gate"), (dev_w_up, "dev_w_up"),
+                                         (dev_w_down, "dev_w_down"))]
+    if stage_event.cuda_event == 0:  # torch creates the CUDA event on its first record
+        stage_event.record(stage_stream)
+    _check(lib().moe_layer_forward_hetero(
+        C.byref(dims), C.byref(args), C.byref(outs), C.byref(cost), *[C.cast(a, C.c_void_p) for a in hw],
+        *[C.cast(a, C.c_void_p) for a in dw], C.byref(host), int(n_threads), _ptr(ws, torch.uint8, name="ws"),
+        ws.numel(), _stream(stream), _stream(stage_stream), C.c_void_p(stage_event.cuda_event), C.byref(st)),
+        "moe_layer_forward_hetero")
+    return st
 
 
 def moe_check(ws, stream=None):

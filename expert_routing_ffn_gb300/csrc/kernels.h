@@ -50,6 +50,11 @@ struct SelectArgs {
     int32_t* counters; DevError* err;
 };
 cudaError_t launch_select_resident(const SelectArgs& a, cudaStream_t st);
+// heterogeneous path: FETCH -> CPU per expert by the cost threshold, host slots
+// placed after the GPU segments of the permutation (one block)
+cudaError_t launch_hetero_decide(const int32_t* final_idx, int32_t* final_kind, int n_slots, int N,
+                                 int fetch_min_rows, uint64_t* fetch_mask, uint64_t* cpu_mask, int32_t* perm,
+                                 int32_t* inv_perm, int32_t* counters, cudaStream_t st);
 
 struct PermuteArgs {
     const int32_t *final_idx, *final_kind;

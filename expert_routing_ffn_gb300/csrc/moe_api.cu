@@ -1,6 +1,7 @@
 // C ABI of the MoE layer (include/moe.h): argument checks, workspace layout,
 // expert table, and the launch sequence of each stage.
 #include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -193,7 +194,8 @@ moe_status prep_select(const moe_dims* dims, const float* router_prob, const int
                        const int32_t* delta_hat, const int32_t* delta_star, int32_t* final_idx,
                        float* final_gate, int32_t* final_kind, uint64_t* fetch_mask, int32_t* counters,
                        void* ws, SelectArgs& a) {
-    if (policy < MOE_MISS_EXACT || policy > MOE_MISS_HYBRID) return MOE_ERR_INVALID_ARG;
+    // HETERO only through moe_select_hetero (its callers check the rest)
+    if (policy < MOE_MISS_EXACT || policy > MOE_MISS_HETERO) return MOE_ERR_INVALID_ARG;
     if ((policy == MOE_MISS_LORE || policy == MOE_MISS_HYBRID) && dims->r <= 0) return MOE_ERR_INVALID_ARG;
     if (!router_prob || !topk_idx || !final_idx || !final_gate || !final_kind) return MOE_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(*dims);
@@ -341,6 +343,31 @@ moe_status moe_select_resident(const moe_dims* dims, const float* router_prob,
     MOE_TRY(prep_select(dims, router_prob, topk_idx, prefetch_mask, resident, policy, gamma, delta_hat,
                         delta_star, final_idx, final_gate, final_kind, fetch_mask, counters, ws, a));
     MOE_CUDA(launch_select_resident(a, S(stream)));
+    count();
+    return MOE_OK;
+}
+
+moe_status moe_select_hetero(const moe_dims* dims, const float* router_prob, const int32_t* topk_idx,
+                             const uint64_t* prefetch_mask, const uint64_t* resident, float gamma,
+                             int fetch_min_rows, const int32_t* delta_hat, const int32_t* delta_star,
+                             int32_t* final_idx, float* final_gate, int32_t* final_kind, int32_t* perm,
+                             int32_t* inv_perm, uint64_t* fetch_mask, uint64_t* cpu_mask, int32_t* counters,
+                             void* ws, size_t ws_bytes, void* stream) {
+    MOE_TRY(check_dims(dims));
+    MOE_TRY(check_ws(dims, ws, ws_bytes));
+    if (fetch_min_rows < 1 || !(gamma >= 0.f) || (gamma > 0.f && dims->r <= 0) || !perm || !inv_perm)
+        return MOE_ERR_INVALID_ARG;
+    if (counters) MOE_CUDA(cudaMemsetAsync(counters, 0, MOE_NUM_COUNTERS * sizeof(int32_t), S(stream)));
+    if (fetch_mask) MOE_CUDA(cudaMemsetAsync(fetch_mask, 0, sizeof(uint64_t), S(stream)));
+    if (cpu_mask) MOE_CUDA(cudaMemsetAsync(cpu_mask, 0, sizeof(uint64_t), S(stream)));
+    if (dims->T == 0) return MOE_OK;
+    SelectArgs a;
+    MOE_TRY(prep_select(dims, router_prob, topk_idx, prefetch_mask, resident, MOE_MISS_HETERO, gamma, delta_hat,
+                        delta_star, final_idx, final_gate, final_kind, nullptr, counters, ws, a));
+    MOE_CUDA(launch_select_resident(a, S(stream)));
+    count();
+    MOE_CUDA(launch_hetero_decide(final_idx, final_kind, dims->T * dims->k, dims->N, fetch_min_rows, fetch_mask,
+                                  cpu_mask, perm, inv_perm, counters, S(stream)));
     count();
     return MOE_OK;
 }
@@ -703,6 +730,7 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_layer_args* A,
                              const moe_layer_outputs* O, void* ws, size_t ws_bytes, void* stream) {
     MOE_TRY(check_dims(dims));
     if (!A || !O) return MOE_ERR_INVALID_ARG;
+    if (A->policy == MOE_MISS_HETERO) return MOE_ERR_INVALID_ARG;  // moe_layer_forward_hetero
     const uint64_t* resident = A->n_resident > 0 ? O->batch_resident : A->resident;
     const uint64_t* pref_mask = A->use_prefetch_mask ? O->prefetch_mask : nullptr;
     if (dims->T > 0 && dims->T <= kFrontMaxTokens && dims->T * dims->k <= kFrontMaxSlots) {
@@ -785,6 +813,114 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_layer_args* A,
     MOE_TRY(moe_combine(dims, O->y_perm, O->inv_perm, O->final_gate, O->final_kind,
                         dims->n_shared > 0 ? O->y_shared : nullptr, lore ? O->y_lore : nullptr,
                         O->out, stream));
+    return MOE_OK;
+}
+
+moe_status moe_layer_forward_hetero(const moe_dims* dims, const moe_layer_args* A, const moe_layer_outputs* O,
+                                    const moe_hetero_cost* cost, const void* const* host_w_gate,
+                                    const void* const* host_w_up, const void* const* host_w_down,
+                                    void* const* dev_w_gate, void* const* dev_w_up, void* const* dev_w_down,
+                                    const moe_hetero_host* H, int n_threads, void* ws, size_t ws_bytes,
+                                    void* stream, void* stage_stream, void* stage_event, moe_hetero_stats* stats) {
+    using clk = std::chrono::steady_clock;
+    MOE_TRY(check_dims(dims));
+    MOE_TRY(check_ws(dims, ws, ws_bytes));
+    if (!A || !O || !cost || !H || !host_w_gate || !host_w_up || !host_w_down || !dev_w_gate || !dev_w_up ||
+        !dev_w_down || !stage_event)
+        return MOE_ERR_INVALID_ARG;
+    if (A->keep_frac != 1.f || (A->x_pre && A->x_pre != A->x)) return MOE_ERR_INVALID_ARG;
+    if (!H->x || !H->final_idx || !H->final_kind || !H->masks || !H->y_rows || !H->scratch ||
+        H->scratch_bytes < moe_cpu_experts_scratch_size(dims))
+        return MOE_ERR_INVALID_ARG;
+    if (!O->out || !O->y_perm || !O->perm || !O->inv_perm || !O->expert_offsets || !O->final_idx ||
+        !O->final_kind || !O->final_gate || (dims->n_shared > 0 && !O->y_shared))
+        return MOE_ERR_INVALID_ARG;
+    const int nmin = moe_hetero_fetch_min_rows(cost);
+    if (nmin < 1) return MOE_ERR_INVALID_ARG;
+    moe_hetero_stats st;
+    std::memset(&st, 0, sizeof(st));
+    st.fetch_min_rows = nmin;
+    if (stats) *stats = st;
+    const int T = dims->T, k = dims->k, d = dims->d;
+    if (T == 0) return MOE_OK;
+    cudaStream_t s = S(stream);
+    const size_t esz = bf16(dims) ? 2 : 4;
+    const auto t0 = clk::now();
+
+    // (1) routing and miss handling on the GPU; decisions (and, for small
+    //     batches, the hidden state) down to the host
+    MOE_TRY(moe_route(dims, A->x, A->w_router, A->router_bias, A->x_pre, A->w_prefetch, A->w_ord, A->theta,
+                      A->tau, A->n_resident, O->topk_idx, O->topk_gate, O->router_prob, O->delta_hat,
+                      O->prefetch_mask, O->delta_star, O->batch_resident, ws, ws_bytes, stream));
+    const uint64_t* resident = A->n_resident > 0 ? O->batch_resident : A->resident;
+    const uint64_t* pref_mask = A->use_prefetch_mask ? O->prefetch_mask : nullptr;
+    MOE_TRY(moe_select_hetero(dims, O->router_prob, O->topk_idx, pref_mask, resident, A->gamma, nmin, O->delta_hat,
+                              O->delta_star, O->final_idx, O->final_gate, O->final_kind, O->perm, O->inv_perm,
+                              O->fetch_mask, nullptr, O->counters, ws, ws_bytes, stream));
+    const size_t n_slots = (size_t)T * k;
+    MOE_CUDA(cudaMemcpyAsync(H->final_idx, O->final_idx, n_slots * 4, cudaMemcpyDeviceToHost, s));
+    MOE_CUDA(cudaMemcpyAsync(H->final_kind, O->final_kind, n_slots * 4, cudaMemcpyDeviceToHost, s));
+    const size_t x_bytes = (size_t)T * d * esz;
+    const bool x_whole = x_bytes <= ((size_t)4 << 20);
+    if (x_whole) MOE_CUDA(cudaMemcpyAsync(H->x, A->x, x_bytes, cudaMemcpyDeviceToHost, s));
+    MOE_CUDA(cudaStreamSynchronize(s));
+    uint64_t fetch = 0, cpu = 0;
+    int cpu_slots = 0, lore_slots = 0, cpu_tokens = 0;
+    for (int t = 0; t < T; ++t) {
+        bool any = false;
+        for (int j = 0; j < k; ++j) {
+            const int e = H->final_idx[(size_t)t * k + j], kd = H->final_kind[(size_t)t * k + j];
+            if (e < 0 || e >= dims->N) continue;
+            if (kd == MOE_KIND_FETCH) fetch |= 1ull << e;
+            if (kd == MOE_KIND_CPU) { cpu |= 1ull << e; ++cpu_slots; any = true; }
+            if (kd == MOE_KIND_LORE) ++lore_slots;
+        }
+        if (any && !x_whole) {  // large batch: only the rows of tokens with host slots
+            MOE_CUDA(cudaMemcpyAsync(static_cast<char*>(H->x) + (size_t)t * d * esz,
+                                     static_cast<const char*>(A->x) + (size_t)t * d * esz, d * esz,
+                                     cudaMemcpyDeviceToHost, s));
+        }
+        cpu_tokens += any ? 1 : 0;
+    }
+    if (!x_whole && cpu_slots) MOE_CUDA(cudaStreamSynchronize(s));
+    H->masks[0] = fetch;
+    H->masks[1] = cpu;
+    st.wait_ms = std::chrono::duration<double, std::milli>(clk::now() - t0).count();
+
+    // (2) fetches on the staging stream; GPU experts, LoRE and shared experts
+    //     on `stream`; the host slots on the host cores meanwhile
+    if (fetch) {
+        size_t nb = 0;
+        MOE_TRY(moe_stage_experts(dims, fetch, host_w_gate, host_w_up, host_w_down, dev_w_gate, dev_w_up,
+                                  dev_w_down, stage_stream, stage_event, &nb));
+        MOE_CUDA(cudaStreamWaitEvent(s, reinterpret_cast<cudaEvent_t>(stage_event), 0));
+        st.fetch_bytes = (double)nb;
+        st.fetch_experts = __builtin_popcountll(fetch);
+    }
+    MOE_TRY(moe_permute(dims, O->final_idx, O->final_kind, O->expert_offsets, O->perm, O->inv_perm, ws, ws_bytes,
+                        stream));
+    MOE_TRY(moe_expert_ffn(dims, A->x, A->table, O->expert_offsets, O->perm, 1.f, O->y_perm, O->y_shared, ws,
+                           ws_bytes, stream));
+    const bool lore = dims->r > 0 && A->lore_a && A->lore_b && O->y_lore;
+    if (lore)
+        MOE_TRY(moe_lore(dims, A->x, O->final_idx, O->final_kind, O->final_gate, A->lore_a, A->lore_b, O->y_lore,
+                         ws, ws_bytes, stream));
+    int32_t n_rows = 0, first = 0;
+    const auto th = clk::now();
+    MOE_TRY(moe_cpu_experts(dims, H->x, H->final_idx, H->final_kind, host_w_gate, host_w_up, host_w_down,
+                            n_threads, H->y_rows, H->scratch, H->scratch_bytes, &n_rows, &first));
+    st.host_ms = std::chrono::duration<double, std::milli>(clk::now() - th).count();
+
+    // (3) the host rows into y_perm after the GPU rows, then every slot merged
+    if (n_rows)
+        MOE_CUDA(cudaMemcpyAsync(O->y_perm + (size_t)first * d, H->y_rows, (size_t)n_rows * d * sizeof(float),
+                                 cudaMemcpyHostToDevice, s));
+    MOE_TRY(moe_combine(dims, O->y_perm, O->inv_perm, O->final_gate, O->final_kind,
+                        dims->n_shared > 0 ? O->y_shared : nullptr, lore ? O->y_lore : nullptr, O->out, stream));
+    st.cpu_slots = n_rows;
+    st.lore_slots = lore_slots;
+    st.cpu_link_bytes = (double)cpu_tokens * d * esz + (double)n_rows * d * sizeof(float);
+    if (stats) *stats = st;
     return MOE_OK;
 }
 

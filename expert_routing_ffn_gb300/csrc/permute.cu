@@ -25,9 +25,11 @@ __device__ __forceinline__ int permute_key(const int32_t* __restrict__ final_idx
                                            DevError* __restrict__ err) {
     if (i >= n_slots) return -1;
     const int x = final_idx[i];
-    const bool lore = final_kind[i] == MOE_KIND_LORE;
+    const int kd = final_kind[i];
+    const bool lore = kd == MOE_KIND_LORE;
     if (x >= N && (!LORE || lore)) { if (err) set_error(err, MOE_ERR_DEVICE_INDEX, i); return -1; }
-    return (x >= 0 && x < N && lore == LORE) ? x : -1;
+    const bool mine = LORE ? lore : (kd == MOE_KIND_COMPUTE || kd == MOE_KIND_FETCH);
+    return (x >= 0 && x < N && mine) ? x : -1;
 }
 
 // per warp and expert: the warp's slot count; returns this slot's rank among
@@ -110,8 +112,8 @@ __global__ void __launch_bounds__(kPermChunk) permute_scatter_kernel(const int32
             const int pos = base[key] + cnt[warp][key] + rank;
             perm[pos] = slot;
             inv_perm[slot] = pos;
-        } else {
-            inv_perm[slot] = -1;
+        } else if (LORE || final_kind[slot] != MOE_KIND_CPU) {
+            inv_perm[slot] = -1;  // host slots keep the position moe_select_hetero gave them
         }
     }
     if (c == 0) {

@@ -154,11 +154,14 @@ __device__ __forceinline__ void permute_block(const int32_t* __restrict__ final_
     __shared__ int s_off[kMaxExperts + 1];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
     for (int i = tid; i < 32 * kMaxExperts; i += blockDim.x) (&cnt[0][0])[i] = 0;
-    int key = -1;  // expert of this slot, -1: no computed expert (LoRE, empty, past the end)
+    int key = -1;  // expert of this slot, -1: no GPU-computed expert (LoRE, host, empty, past the end)
+    bool host = false;
     if (tid < n_slots) {
         const int x = final_idx[tid];
+        const int kd = final_kind[tid];
         if (x >= N) set_error(err, MOE_ERR_DEVICE_INDEX, tid);
-        if (x >= 0 && x < N && final_kind[tid] != MOE_KIND_LORE) key = x;
+        host = kd == MOE_KIND_CPU;
+        if (x >= 0 && x < N && (kd == MOE_KIND_COMPUTE || kd == MOE_KIND_FETCH)) key = x;
     }
     __syncthreads();
     const uint32_t peers = __match_any_sync(0xffffffffu, key);
@@ -184,7 +187,7 @@ __device__ __forceinline__ void permute_block(const int32_t* __restrict__ final_
             const int pos = s_off[key] + cnt[warp][key] + rank;
             perm[pos] = tid;
             inv_perm[tid] = pos;
-        } else {
+        } else if (!host) {  // host slots keep the position moe_select_hetero gave them
             inv_perm[tid] = -1;
         }
     }

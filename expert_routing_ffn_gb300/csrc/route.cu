@@ -528,6 +528,9 @@ __device__ __forceinline__ void select_token(
             case MOE_MISS_EXACT: fetch |= bit; break;
             case MOE_MISS_LORE: lore |= bit; break;
             case MOE_MISS_SUBSTITUTE: to_sub |= bit; break;
+            case MOE_MISS_HETERO:  // exact either way: fetch or host (decided per expert afterwards)
+                if (ae < gamma) lore |= bit; else fetch |= bit;
+                break;
             default:
                 if (ae < gamma) lore |= bit; else to_sub |= bit;
         }

@@ -177,3 +177,44 @@ def forward(layer: DeviceLayer, bufs: LayerBuffers, x, stream=None, **kw):
     _check(lib().moe_layer_forward(C.byref(dims), C.byref(args), C.byref(outs), ws_ptr, ws_bytes,
                                    _stream(stream)), "moe_layer_forward")
     return bufs
+
+
+class HeteroHost:
+    """Pinned host buffers and the host copy of the routed experts for the
+    heterogeneous CPU-GPU path (moe_layer_forward_hetero), sized for T tokens.
+    The host weights are the layer's own device values copied down once."""
+
+    def __init__(self, layer: DeviceLayer, T: int):
+        from . import moe_cpu_experts_scratch_size, moe_hetero_host
+        cfg = layer.cfg
+        k, d = cfg.k, cfg.d
+        pin = dict(pin_memory=True)
+        self.T = T
+        self.x = torch.empty((T, d), dtype=layer.dt, **pin)
+        self.final_idx = torch.empty((T, k), dtype=torch.int32, **pin)
+        self.final_kind = torch.empty((T, k), dtype=torch.int32, **pin)
+        self.masks = torch.zeros(2, dtype=torch.int64, **pin)
+        self.y_rows = torch.empty((T * k, d), dtype=torch.float32, **pin)
+        self.scratch = torch.empty(moe_cpu_experts_scratch_size(layer.dims.with_T(T)), dtype=torch.uint8)
+        self.w_gate = [layer.w_gate[e].cpu().pin_memory() for e in range(cfg.N)]
+        self.w_up = [layer.w_up[e].cpu().pin_memory() for e in range(cfg.N)]
+        self.w_down = [layer.w_down[e].cpu().pin_memory() for e in range(cfg.N)]
+        h = moe_hetero_host()
+        h.x, h.final_idx, h.final_kind = self.x.data_ptr(), self.final_idx.data_ptr(), self.final_kind.data_ptr()
+        h.masks, h.y_rows = self.masks.data_ptr(), self.y_rows.data_ptr()
+        h.scratch, h.scratch_bytes = self.scratch.data_ptr(), self.scratch.numel()
+        self.struct = h
+
+
+def forward_hetero(layer: DeviceLayer, bufs: LayerBuffers, x, host: HeteroHost, cost, stage_stream, stage_event,
+                   n_threads=0, stream=None, **kw):
+    """One layer forward on the heterogeneous path (moe_layer_forward_hetero):
+    high-confidence misses fetched or run on the host cores by the cost model.
+    Returns the call's moe_hetero_stats."""
+    from . import moe_layer_forward_hetero
+    T = x.shape[0]
+    assert T <= bufs.T and T <= host.T and x.is_contiguous() and x.dtype == layer.dt
+    args = layer_args(layer, x, **kw)
+    return moe_layer_forward_hetero(layer.dims.with_T(T), args, bufs.outputs_struct(), cost, host.w_gate, host.w_up,
+                                    host.w_down, list(layer.w_gate), list(layer.w_up), list(layer.w_down),
+                                    host.struct, layer.ws, stage_stream, stage_event, n_threads, stream)

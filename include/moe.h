@@ -14,8 +14,11 @@
  * and moe_layer_forward (all stages chained on one stream).
  * Beyond the single forward: moe_cache_update (a persistent expert cache
  * across decode steps), moe_prefetch_depth / moe_prefetch_min_depth (a
- * confidence-aware look-ahead over the next layers) and moe_bitslice_pack /
- * moe_bitslice_ffn (a low-precision draft FFN on bit-sliced INT8 weights).
+ * confidence-aware look-ahead over the next layers), moe_bitslice_pack /
+ * moe_bitslice_ffn (a low-precision draft FFN on bit-sliced INT8 weights) and
+ * the heterogeneous CPU-GPU path: moe_hetero_fetch_min_rows,
+ * moe_select_hetero, moe_cpu_experts and moe_layer_forward_hetero (exact
+ * host execution of high-confidence misses chosen by a cost model).
  *
  * Conventions (all entry points):
  *   - Every function returns moe_status (the two size helpers and
@@ -82,11 +85,17 @@ typedef enum {
                                  correctness-preserving mode) */
     MOE_MISS_SUBSTITUTE = 1,  /* stall-free substitution (APEX §4.3, Algorithm 1) */
     MOE_MISS_LORE = 2,        /* LoRE surrogate y_shared + B_e A_e x (SPICE, LoRE section) */
-    MOE_MISS_HYBRID = 3       /* router prob < gamma -> LoRE, else substitute */
+    MOE_MISS_HYBRID = 3,      /* router prob < gamma -> LoRE, else substitute */
+    MOE_MISS_HETERO = 4       /* router prob < gamma -> LoRE, else exact: fetched to the GPU
+                                 or computed on the host, per expert by the cost model
+                                 (SPICE, CPU-GPU collaboration); moe_select_hetero only */
 } moe_miss_policy;
 
-/* Kind of each final slot. */
-typedef enum { MOE_KIND_COMPUTE = 0, MOE_KIND_FETCH = 1, MOE_KIND_LORE = 2 } moe_slot_kind;
+/* Kind of each final slot.  CPU: an exact expert computed on the host cores
+ * (moe_cpu_experts) and merged in the combine like a computed slot. */
+typedef enum {
+    MOE_KIND_COMPUTE = 0, MOE_KIND_FETCH = 1, MOE_KIND_LORE = 2, MOE_KIND_CPU = 3
+} moe_slot_kind;
 
 /* Layer dimensions.  T: tokens in this call (<= the T the workspace was sized
  * for); d: hidden size (multiple of 256); N: routed experts (<= 64);
@@ -111,7 +120,8 @@ enum {
     MOE_CNT_DELTA_HAT = 5,  /* sum over tokens of delta_hat */
     MOE_CNT_DELTA_STAR = 6, /* sum over tokens of delta* */
     MOE_CNT_SHORTFALL = 7,  /* tokens whose available set had fewer than k experts */
-    MOE_NUM_COUNTERS = 8
+    MOE_CNT_CPU = 8,        /* slots computed on the host cores (HETERO) */
+    MOE_NUM_COUNTERS = 9
 };
 
 const char* moe_status_string(moe_status s);
@@ -206,6 +216,73 @@ moe_status moe_stage_experts(const moe_dims* dims, uint64_t host_fetch_mask,
                              void* const* dev_w_gate, void* const* dev_w_up,
                              void* const* dev_w_down, void* stage_stream, void* done_event,
                              size_t* bytes);
+
+/* Heterogeneous CPU-GPU orchestration (SPICE write-up, section on CPU-GPU
+ * collaboration for prefetch misses, Fig. 6 and its cost model).  A routed
+ * expert outside the available set whose router probability is at least
+ * gamma must be computed exactly; it is either fetched (its weights copied
+ * to the GPU, then computed there) or computed on the host cores from the
+ * host copy of its weights, with only the token rows crossing the link.  Per
+ * missing expert e with n_e such token rows in the batch:
+ *   fetch cost = W_e / B + T_gpu          CPU cost = n_e * (t_cpu + 2 H / B)
+ * and e is fetched iff the fetch cost is the smaller (ties go to the host).
+ * Times in seconds, sizes in bytes. */
+typedef struct {
+    double link_bytes_per_s;  /* B: host <-> device link bandwidth */
+    double expert_bytes;      /* W_e: one routed expert's gate, up and down matrices */
+    double gpu_expert_s;      /* T_gpu: one routed expert's FFN on the GPU */
+    double cpu_row_s;         /* t_cpu: one token row of one expert's FFN on the host */
+    double hidden_bytes;      /* H: one token's hidden state (d x element size) */
+} moe_hetero_cost;
+
+/* The smallest n_e for which fetching wins under *cost (1 if it always
+ * wins; INT32_MAX if it never does).  Host only; -1 for a negative, NaN or
+ * missing parameter or a non-positive bandwidth. */
+int moe_hetero_fetch_min_rows(const moe_hetero_cost* cost);
+
+/* Miss handling of the heterogeneous path: moe_select_resident with
+ * MOE_MISS_HETERO (router prob < gamma -> LoRE, needs dims->r > 0 when
+ * gamma > 0), then per missing expert: n_e >= fetch_min_rows -> its slots
+ * are FETCH, else CPU.  Also places the CPU slots after the GPU segments of
+ * the permutation: with n_gpu the number of COMPUTE and FETCH slots, the j-th
+ * CPU slot (t, s) in slot order gets inv_perm[t*k+s] = n_gpu + j and
+ * perm[n_gpu + j] = t*k+s; moe_permute, called next, fills the entries of
+ * the other slots and leaves these.  fetch_mask / cpu_mask (device uint64,
+ * may be NULL) = the experts with FETCH / CPU slots; counters as in
+ * moe_select_resident plus MOE_CNT_CPU (MOE_CNT_FETCH counts only the slots
+ * left to fetch).  Errors as moe_select_resident; INVALID_ARG also for
+ * fetch_min_rows < 1. */
+moe_status moe_select_hetero(const moe_dims* dims, const float* router_prob, const int32_t* topk_idx,
+                             const uint64_t* prefetch_mask, const uint64_t* resident, float gamma,
+                             int fetch_min_rows, const int32_t* delta_hat, const int32_t* delta_star,
+                             int32_t* final_idx, float* final_gate, int32_t* final_kind, int32_t* perm,
+                             int32_t* inv_perm, uint64_t* fetch_mask, uint64_t* cpu_mask, int32_t* counters,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/* Host scratch bytes moe_cpu_experts needs for dims (T*k*I*4 plus
+ * bookkeeping; 0 for bad dims). */
+size_t moe_cpu_experts_scratch_size(const moe_dims* dims);
+
+/* The host side of the heterogeneous path: every CPU slot's expert FFN,
+ * computed exactly on the host cores from the host copy of the weights
+ * (bf16 or float32 values, float32 arithmetic):
+ *   y_rows[j] = (SiLU(x_t Wg_e^T) (.) x_t Wu_e^T) Wd_e   (ungated)
+ * for the j-th CPU slot (t, s) in slot order, e = final_idx[t*k+s].
+ * HOST pointers, all of them: host_x [T, d] (layer type), host_final_idx /
+ * host_final_kind [T, k] (copies of moe_select_hetero's outputs),
+ * host_w_gate/up/down[e] ([I, d] each), host_y_rows [T*k, d] float32,
+ * scratch of moe_cpu_experts_scratch_size bytes.  n_threads <= 0: every core
+ * of the process's affinity mask.  *n_rows = the CPU slots computed;
+ * *first_row = n_gpu, the y_perm row of the first of them (copy the rows
+ * there before moe_combine).  The work of one call is spread over a pool of
+ * host threads that the library starts on first use and keeps.  The result
+ * does not depend on n_threads.  No CUDA call.  Errors: INVALID_ARG (NULL,
+ * an index out of range, scratch too small), UNSUPPORTED (dims). */
+moe_status moe_cpu_experts(const moe_dims* dims, const void* host_x, const int32_t* host_final_idx,
+                           const int32_t* host_final_kind, const void* const* host_w_gate,
+                           const void* const* host_w_up, const void* const* host_w_down, int n_threads,
+                           float* host_y_rows, void* scratch, size_t scratch_bytes, int32_t* n_rows,
+                           int32_t* first_row);
 
 /* Stage 3a — token permutation by expert.
  *   Slots (t, s) of kind COMPUTE or FETCH are grouped by expert, stable in
@@ -443,6 +520,51 @@ typedef struct {
 moe_status moe_layer_forward(const moe_dims* dims, const moe_layer_args* args,
                              const moe_layer_outputs* outs, void* ws, size_t ws_bytes,
                              void* stream);
+
+/* Host buffers of moe_layer_forward_hetero (pinned host memory, caller-owned;
+ * sized for dims->T). */
+typedef struct {
+    void* x;              /* [T, d] layer type: the hidden state staged to the host */
+    int32_t* final_idx;   /* [T, k] */
+    int32_t* final_kind;  /* [T, k] */
+    uint64_t* masks;      /* [2]: fetch mask, CPU mask */
+    float* y_rows;        /* [T*k, d] float32: CPU-slot outputs */
+    void* scratch;        /* moe_cpu_experts scratch */
+    size_t scratch_bytes;
+} moe_hetero_host;
+
+/* What one moe_layer_forward_hetero call did. */
+typedef struct {
+    int32_t cpu_slots;        /* slots computed on the host */
+    int32_t fetch_experts;    /* experts copied to the GPU */
+    int32_t fetch_min_rows;   /* the cost model's threshold */
+    int32_t lore_slots;       /* slots served by LoRE */
+    double fetch_bytes;       /* expert bytes queued host -> device */
+    double cpu_link_bytes;    /* token rows down and CPU results up */
+    double host_ms;           /* host FFN time */
+    double wait_ms;           /* time the host waited for the routing decisions */
+} moe_hetero_stats;
+
+/* One layer forward on the heterogeneous path, orchestrated in three steps
+ * (SPICE, Fig. 6): (1) routing and miss handling run on `stream`, then the
+ * hidden state and the decisions are copied to host->* and the host waits
+ * for them; (2) the fetched experts' copies are queued on stage_stream
+ * (moe_stage_experts into dev_w_*, stage_event recorded, `stream` waits on
+ * it), the GPU experts, LoRE and the shared experts are queued on `stream`,
+ * and meanwhile the host cores compute the CPU slots (moe_cpu_experts);
+ * (3) the CPU rows are copied into y_perm and moe_combine merges every slot.
+ * args->policy is ignored (HETERO with args->gamma); args->keep_frac must be
+ * 1 and args->x_pre NULL or x.  Returns when step 3 is queued; host->y_rows
+ * must stay untouched until `stream` has passed it.  *stats (may be NULL).
+ * Errors: those of the stages, CUDA, STAGING. */
+moe_status moe_layer_forward_hetero(const moe_dims* dims, const moe_layer_args* args,
+                                    const moe_layer_outputs* outs, const moe_hetero_cost* cost,
+                                    const void* const* host_w_gate, const void* const* host_w_up,
+                                    const void* const* host_w_down, void* const* dev_w_gate,
+                                    void* const* dev_w_up, void* const* dev_w_down,
+                                    const moe_hetero_host* host, int n_threads, void* ws, size_t ws_bytes,
+                                    void* stream, void* stage_stream, void* stage_event,
+                                    moe_hetero_stats* stats);
 
 /* Synchronise `stream`, read and clear the device error word of `ws`.
  * *device_status receives MOE_OK or the first error a kernel recorded;

@@ -26,9 +26,12 @@ _lock = threading.Lock()
 _lib = None
 
 # decisive-margin columns (match the M_* enum in moe_oracle.c)
-M_TOPK, M_PREFETCH, M_THETA, M_DSTAR, M_SUBST, M_GAMMA, M_FLOE = range(7)
+M_TOPK, M_PREFETCH, M_THETA, M_DSTAR, M_SUBST, M_GAMMA, M_FLOE, M_COST = range(8)
 M_COUNT = 8
-MARGIN_NAMES = ["topk", "prefetch", "theta", "delta_star", "substitute", "gamma", "floe"]
+MARGIN_NAMES = ["topk", "prefetch", "theta", "delta_star", "substitute", "gamma", "floe", "cost"]
+POL_HETERO = 4
+KIND_CPU = 3
+COST_FIELDS = ("link_bps", "expert_bytes", "gpu_expert_s", "cpu_row_s", "hidden_bytes")
 
 
 def build(force: bool = False) -> str:
@@ -48,7 +51,8 @@ class _Cfg(C.Structure):
     _fields_ = [(n, C.c_int) for n in ("T", "d", "N", "k", "I", "n_shared", "I_shared", "r",
                                        "delta_max", "renorm", "policy", "use_prefetch",
                                        "m_keep", "has_prefetch", "route_only")] + [
-        ("tau", C.c_double), ("gamma", C.c_double), ("resident", C.c_uint64)]
+        ("tau", C.c_double), ("gamma", C.c_double), ("resident", C.c_uint64)] + [
+        (n, C.c_double) for n in ("link_bps", "expert_bytes", "gpu_expert_s", "cpu_row_s", "hidden_bytes")]
 
 
 _FP = C.POINTER(C.c_float)
@@ -111,6 +115,8 @@ def lib():
             L.orc_bitslice_ffn.argtypes = [C.c_int, C.c_int, C.c_int, _FP, _BP, _FP, _BP, _FP, _BP, _FP, _DP]
             L.orc_bitslice_ffn.restype = None
             L.orc_layer_forward.argtypes = [C.POINTER(_Cfg), C.POINTER(_Inputs), C.POINTER(_Outputs)]
+            L.orc_hetero_fetch.argtypes = [C.c_int] + [C.c_double] * 5 + [_DP]
+            L.orc_hetero_fetch.restype = C.c_int
             _lib = L
     return _lib
 
@@ -217,6 +223,14 @@ def lore(x, A, B) -> np.ndarray:
     v = np.zeros(d, np.float64)
     lib().orc_lore(d, r, _f(x), _f(A), _f(B), _d(v))
     return v
+
+
+def hetero_fetch(n: int, cost: dict) -> tuple[bool, float]:
+    """SPICE's per-miss cost model for an expert needed by n token rows:
+    (fetch wins, relative cost gap).  cost: the COST_FIELDS."""
+    m = C.c_double()
+    f = lib().orc_hetero_fetch(int(n), *[float(cost[k]) for k in COST_FIELDS], C.byref(m))
+    return bool(f), m.value
 
 
 def batch_resident(lp, n_res):
@@ -347,12 +361,13 @@ def resident_mask(cfg, W, x_batch) -> tuple[int, float]:
 def layer_forward(cfg, W, x, resident: int | None = None, x_pre=None, keep_m: int | None = None,
                   policy: int | None = None, gamma: float | None = None, tau: float | None = None,
                   renorm: int = 0, use_prefetch: bool | None = None,
-                  route_only: bool = False) -> LayerResult:
+                  route_only: bool = False, cost: dict | None = None) -> LayerResult:
     """Run the whole layer for the tokens x [T, d].
 
     resident: batch-level resident mask (default: computed from x itself with
     the config's n_resident).  keep_m: FloE channels kept (default: dense).
     route_only: stop after the routing decisions (outputs stay zero).
+    cost: the HETERO policy's cost model (COST_FIELDS), required with it.
     """
     x = f32(x)
     T, d = x.shape
@@ -372,6 +387,11 @@ def layer_forward(cfg, W, x, resident: int | None = None, x_pre=None, keep_m: in
     c.tau = cfg.tau if tau is None else tau
     c.gamma = cfg.gamma if gamma is None else gamma
     c.resident = resident
+    if c.policy == POL_HETERO:
+        if cost is None:
+            raise ValueError("the HETERO policy needs its cost model")
+        for k_ in COST_FIELDS:
+            setattr(c, k_, float(cost[k_]))
     keep = [x]  # keep arrays alive
     inp = _Inputs()
     inp.x = _f(x)

@@ -29,6 +29,9 @@
  *   - bit-sliced expert weights       : ELMoE-3D (CSDN post), bit-slicing
  *     section (INT8 bit planes, top-b planes combined, shared scale) and the
  *     layout note (an expert's planes stored contiguously).
+ *   - CPU-GPU orchestration           : SPICE write-up, section on CPU-GPU
+ *     collaboration for prefetch misses (Fig. 6 and the per-miss cost
+ *     model: fetch cost W_e/B + T_gpu against CPU cost T_cpu + 2H/B).
  *   - persistent expert cache         : ELMoE-3D (CSDN post), expert-axis
  *     elasticity: heat statistics, top-K subset, dynamic update, and the
  *     practice note on heat decay (multiply every heat by a factor just
@@ -47,11 +50,11 @@
 #include <omp.h>
 #endif
 
-enum { POL_EXACT = 0, POL_SUBSTITUTE = 1, POL_LORE = 2, POL_HYBRID = 3 };
-enum { KIND_COMPUTE = 0, KIND_FETCH = 1, KIND_LORE = 2 };
+enum { POL_EXACT = 0, POL_SUBSTITUTE = 1, POL_LORE = 2, POL_HYBRID = 3, POL_HETERO = 4 };
+enum { KIND_COMPUTE = 0, KIND_FETCH = 1, KIND_LORE = 2, KIND_CPU = 3 };
 enum {
     M_TOPK = 0, M_PREFETCH = 1, M_THETA = 2, M_DSTAR = 3, M_SUBST = 4,
-    M_GAMMA = 5, M_FLOE = 6, M_COUNT = 8
+    M_GAMMA = 5, M_FLOE = 6, M_COST = 7, M_COUNT = 8
 };
 
 int orc_num_threads(void) {
@@ -466,6 +469,24 @@ void orc_bitslice_ffn(int d, int I, int b, const float* x, const signed char* qg
     free(h);
 }
 
+/* SPICE's per-miss cost model (CPU-GPU collaboration section): a missing
+ * expert that must be computed exactly is either fetched, at a cost of its
+ * weight bytes over the link plus its FFN time on the GPU, or run on the
+ * CPU, at a cost of the CPU FFN time plus one hidden state down and one
+ * result up the link.  Here the CPU time and the hidden state grow with the
+ * n token rows that need the expert in this batch:
+ *   fetch = W_e / B + T_gpu        cpu = n t_cpu + 2 (n H) / B
+ * Returns 1 (fetch) when fetch < cpu, else 0 (the CPU; equal costs go to the
+ * CPU).  *margin = |fetch - cpu| / max(fetch, cpu). */
+int orc_hetero_fetch(int n, double link_bps, double expert_bytes, double gpu_expert_s, double cpu_row_s,
+                     double hidden_bytes, double* margin) {
+    const double fetch = expert_bytes / link_bps + gpu_expert_s;
+    const double cpu = (double)n * cpu_row_s + 2.0 * ((double)n * hidden_bytes) / link_bps;
+    const double big = fetch > cpu ? fetch : cpu;
+    if (margin) *margin = big > 0.0 ? fabs(fetch - cpu) / big : 0.0;
+    return fetch < cpu;
+}
+
 typedef struct {
     int T, d, N, k, I, n_shared, I_shared, r, delta_max;
     int renorm;            /* 1: gates renormalised over the final set */
@@ -476,6 +497,9 @@ typedef struct {
     int route_only;        /* stop after the routing decisions (no expert math) */
     double tau, gamma;
     uint64_t resident;     /* batch-level resident mask */
+    /* HETERO cost model (link bytes/s, expert bytes, GPU expert seconds,
+     * CPU seconds per token row, hidden-state bytes per token) */
+    double link_bps, expert_bytes, gpu_expert_s, cpu_row_s, hidden_bytes;
 } orc_cfg;
 
 typedef struct {
@@ -576,6 +600,14 @@ static void one_token(const orc_cfg* c, const orc_inputs* in, const orc_outputs*
             case POL_EXACT: fetch_set |= bit; break;
             case POL_LORE: lore_set |= bit; break;
             case POL_SUBSTITUTE: subst_routed |= bit; break;
+            case POL_HETERO: {
+                /* a low-confidence miss goes to LoRE, the others are computed
+                 * exactly (fetched or on the CPU: decided over the batch) */
+                double dist = fabs(a[e] - c->gamma);
+                if (dist < mg[M_GAMMA]) mg[M_GAMMA] = dist;
+                if (a[e] < c->gamma) lore_set |= bit; else fetch_set |= bit;
+                break;
+            }
             default: {
                 /* HYBRID: a low-confidence miss (alpha < gamma) goes to LoRE,
                  * the others are substituted */
@@ -668,9 +700,31 @@ static void one_token(const orc_cfg* c, const orc_inputs* in, const orc_outputs*
     free(ye);
 }
 
-/* Whole layer, token by token (tokens are independent). */
+/* Whole layer, token by token (tokens are independent).  Under HETERO the
+ * exact misses are then split between fetch and CPU per expert, by the cost
+ * model over the n rows of the batch that need that expert; both are exact,
+ * so the outputs do not change, only the slot kinds. */
 void orc_layer_forward(const orc_cfg* c, const orc_inputs* in, const orc_outputs* o) {
     int T = c->T;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int t = 0; t < T; ++t) one_token(c, in, o, t);
+    if (c->policy != POL_HETERO) return;
+    int rows[64] = {0};
+    for (size_t s = 0; s < (size_t)T * c->k; ++s)
+        if (o->final_kind[s] == KIND_FETCH && o->final_idx[s] >= 0) rows[o->final_idx[s]] += 1;
+    int fetch[64];
+    double gap[64];
+    for (int e = 0; e < c->N; ++e)
+        fetch[e] = rows[e] > 0 ? orc_hetero_fetch(rows[e], c->link_bps, c->expert_bytes, c->gpu_expert_s,
+                                                  c->cpu_row_s, c->hidden_bytes, &gap[e])
+                               : 1;
+    for (int t = 0; t < T; ++t)
+        for (int i = 0; i < c->k; ++i) {
+            const size_t s = (size_t)t * c->k + i;
+            const int e = o->final_idx[s];
+            if (o->final_kind[s] != KIND_FETCH || e < 0) continue;
+            if (!fetch[e]) o->final_kind[s] = KIND_CPU;
+            double* mg = o->margin + (size_t)t * M_COUNT;
+            if (gap[e] < mg[M_COST]) mg[M_COST] = gap[e];
+        }
 }
