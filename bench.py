@@ -62,12 +62,17 @@ WORKLOADS = {
     "dsv2lite-lookahead-decode-T8": ("dsv2lite", 8, "decode"),
     "dsv2lite-bitslice4-draft-T1": ("dsv2lite", 1, "decode"),
     "dsv2lite-hetero-decode-T8": ("dsv2lite", 8, "decode"),
+    "dsv2lite-cache-exact-decode-T1": ("dsv2lite", 1, "decode"),
 }
 # Multi-step decode with a persistent expert cache (ELMoE-3D heat map with
 # decay): the layer runs every step with resident = the cache, which
 # moe_cache_update then refreshes from the step's routed experts.
 # name -> (cache capacity, heat decay, distinct one-token steps replayed)
 CACHE_WORKLOADS = {"dsv2lite-cache-decode-T1": (24, 0.99, 64)}
+# The same cache under the EXACT policy: every miss computed exactly, so a step
+# waits for its missing experts (a stall unless their admission copy was already
+# in flight).  name -> (capacity, decay, distinct one-token steps replayed)
+CACHE_EXACT_WORKLOADS = {"dsv2lite-cache-exact-decode-T1": (24, 0.99, 64)}
 # Decode with SPICE's confidence-aware look-ahead: every step also predicts
 # the expert sets of the next J layers from the step's hidden state
 # (moe_prefetch_depth over the synthetic stack's look-ahead routers).
@@ -300,6 +305,9 @@ def oracle_step(cfg, W, x, wl_name):
     import oracle
     if wl_name in HETERO_WORKLOADS:
         oracle.layer_forward(cfg, W, x, policy=oracle.POL_HETERO, cost=PCIE4_HETERO_COST)
+        return
+    if wl_name in CACHE_EXACT_WORKLOADS:
+        oracle.layer_forward(cfg, W, x, policy=0)
         return
     oracle.layer_forward(cfg, W, x)
     la = LOOKAHEAD_WORKLOADS.get(wl_name)
@@ -830,6 +838,108 @@ def run_hetero(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src, st
     return line
 
 
+def run_cache_exact(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src, steps, warmup):
+    """Decode steps over the overlapped expert cache under the EXACT policy
+    (moe_cache_step): misses are computed exactly, so a step whose missing
+    experts were not already admitted and in flight waits for their copies.
+    Host clock around the steps (the host reads each step's fetch mask)."""
+    import torch
+    import expert_routing_ffn_gb300 as moe
+    from expert_routing_ffn_gb300.layer import CachePipeline, DeviceLayer, LayerBuffers, forward
+    capacity, decay, n_x = CACHE_EXACT_WORKLOADS[wl_name]
+    expert_bytes = 3 * cfg.I * cfg.d * 2
+    layer = DeviceLayer(cfg, W, T, device=str(dev))
+    bufs = LayerBuffers(layer, T)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
+    xs = [torch.from_numpy(make_tokens(cfg, T=T, batch=replica_batch(rank, i))).to(dev).to(layer.dt).contiguous()
+          for i in range(n_x)]
+    pipe = CachePipeline(layer, capacity, decay, stream=stream)
+    pipe.start((1 << capacity) - 1)
+    for i in range(max(3, warmup)):
+        pipe.step(bufs, xs[i % n_x], policy=moe.MOE_MISS_EXACT, n_resident=0)
+    stream.synchronize()
+    n = max(50, min(steps, 1000))
+    p = pipe.pipe
+    base = (p.staged_experts, p.staged_bytes, p.in_time_experts, p.stall_experts, p.stall_steps)
+    hits = slots = 0
+    t0 = time.perf_counter()
+    for i in range(n):
+        pipe.step(bufs, xs[i % n_x], policy=moe.MOE_MISS_EXACT, n_resident=0)
+    stream.synchronize()
+    el = time.perf_counter() - t0
+    d = [a - b for a, b in zip((p.staged_experts, p.staged_bytes, p.in_time_experts, p.stall_experts,
+                                p.stall_steps), base)]
+    st = pipe.stats.cpu().numpy()  # hits / slots since start (includes warm-up)
+    hits, slots = int(st[0]), int(st[1])
+    # end to end with pinned-host copies of x and out every step
+    x_host = [xs[c].cpu().pin_memory() for c in range(n_x)]
+    out_host = torch.empty_like(bufs.out, device="cpu").pin_memory()
+    t1 = time.perf_counter()
+    for i in range(n):
+        xs[i % n_x].copy_(x_host[i % n_x], non_blocking=True)
+        pipe.step(bufs, xs[i % n_x], policy=moe.MOE_MISS_EXACT, n_resident=0)
+        out_host.copy_(bufs.out, non_blocking=True)
+        stream.synchronize()
+    e2e_s = time.perf_counter() - t1
+    pipe.drain()
+    stt, det = moe.moe_check(layer.ws)
+    if stt != moe.MOE_OK:
+        raise RuntimeError(f"device error {moe.status_string(stt)} ({det})")
+    # the FFN stage of this layer, timed alone (all experts on the device)
+    forward(layer, bufs, xs[0], stream=stream, policy=moe.MOE_MISS_EXACT)
+    torch.cuda.synchronize()
+    off = bufs.expert_offsets.cpu().numpy()
+    ffn_bytes = int((np.diff(off) > 0).sum()) * expert_bytes + cfg.n_shared * 3 * cfg.I_shared * cfg.d * 2
+    D = layer.dims.with_T(T)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+    for a, b in evs:
+        a.record(stream)
+        moe.moe_expert_ffn(D, xs[0], layer.table, bufs.expert_offsets, bufs.perm, 1.0, bufs.y_perm, bufs.y_shared,
+                           layer.ws, stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    ffn_ms = statistics.median([a.elapsed_time(b) for a, b in evs])
+    ach = ffn_bytes / (ffn_ms / 1e3) / 1e9
+    step_s = el / n
+    link = d[1] / max(1e-9, el) if d[1] else None
+    line = {
+        "metric": METRIC, "value": world * T * n / max_over_ranks(world, el), "unit": "tokens/s", "n_gpus": world,
+        "steps": n, "warmup": max(3, warmup), "ms_per_step": 1e3 * step_s, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,0.02^2) weights, N(0,1) tokens; shapes of the named model)",
+        "config": {"workload": wl_name, "tokens_per_step": T, "d": cfg.d, "experts": cfg.N, "top_k": cfg.k,
+                   "intermediate": cfg.I, "shared_experts": cfg.n_shared, "miss_policy": "exact",
+                   "resident": f"expert cache of {capacity} (heat decay {decay})",
+                   "parallelism": f"replicas x{world}",
+                   "timing": "host clock around the steps (each EXACT step reads its fetch mask on the host)"},
+        "roofline": {"kernel": "moe_expert_ffn (decode FFN stage of this layer, timed alone)", "bound": "hbm",
+                     "achieved": ach, "unit": "GB/s", **fractions(ach, hbm_gbs, NOMINAL_HBM_GBS, peak_src),
+                     "algorithmic_bytes_per_launch": float(ffn_bytes), "median_launch_ms": ffn_ms, "traffic": None},
+        "cache": {"capacity": capacity, "decay": decay, "hit_rate": hits / max(1, slots),
+                  "stall_rate": d[4] / n, "stalled_experts_per_step": d[3] / n,
+                  "in_time_experts_per_step": d[2] / n, "copied_experts_per_step": d[0] / n,
+                  "copied_bytes_per_step": d[1] / n,
+                  "d_min_measured_link": (moe.moe_prefetch_min_depth(expert_bytes, link, step_s) if link else None),
+                  "d_min_pcie4_x16": moe.moe_prefetch_min_depth(expert_bytes, PCIE4_X16_BYTES_PER_S, step_s),
+                  "note": "stall = a step that copied a missing expert on demand and waited for it; in time = a "
+                          "miss whose admission copy was already in flight or landed (the GPU waits only on its "
+                          "event); hit rate over all steps since the start"},
+        "e2e": {"value": world * T * n / max_over_ranks(world, e2e_s), "unit": "tokens/s",
+                "h2d_bytes_per_step": xs[0].numel() * 2 + d[1] / n, "d2h_bytes_per_step": bufs.out.numel() * 4 + 40,
+                "steps": n, "note": "moe_cache_step per step with pinned-host copies of x and out"},
+        "gpu_launches": None,
+    }
+    n0 = moe.moe_launch_total()
+    pipe.step(bufs, xs[0], policy=moe.MOE_MISS_EXACT, n_resident=0)
+    stream.synchronize()
+    line["gpu_launches"] = int((moe.moe_launch_total() - n0) * n)
+    pipe.drain()
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, W, T, args.cpu_seconds, wl_name=wl_name)
+    return line
+
+
 def run_workload(args, wl_name, world, rank, dev, steps, warmup, with_cpu=True):
     """Measure one workload; returns its JSON line (a dict)."""
     import torch
@@ -843,6 +953,8 @@ def run_workload(args, wl_name, world, rank, dev, steps, warmup, with_cpu=True):
         return run_bitslice(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src, steps, warmup)
     if wl_name in HETERO_WORKLOADS:
         return run_hetero(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src, steps, warmup)
+    if wl_name in CACHE_EXACT_WORKLOADS:
+        return run_cache_exact(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src, steps, warmup)
     base = DeviceLayer(cfg, W, T, device=str(dev))
     esize = 2 if cfg.wtype == "bf16" else 4
     expert_bytes = 3 * cfg.I * cfg.d * esize
@@ -1022,9 +1134,9 @@ def run_workload(args, wl_name, world, rank, dev, steps, warmup, with_cpu=True):
                       "hit_rate": float(cs[0]) / max(1, cs[1]), "miss_rate": 1.0 - float(cs[0]) / max(1, cs[1]),
                       "admitted_per_step": float(cs[2]) / steps_done, "evicted_per_step": float(cs[3]) / steps_done,
                       "stage_bytes_per_step": float(cs[2]) / steps_done * expert_bytes,
-                      "note": "timed steps: layer (resident = cache, HYBRID misses) + cache update; the e2e "
-                              "loop also stages every admitted expert from pinned host memory before the "
-                              "next step"}
+                      "note": "timed steps: layer (resident = cache, HYBRID misses) + cache update in CUDA "
+                              "graphs; the pipeline and e2e loops also copy every admitted expert from pinned "
+                              "host memory (moe_cache_step), overlapped with the following steps"}
 
     # ---- the look-ahead step alone, and what it predicted
     la_info = None
@@ -1084,45 +1196,50 @@ def run_workload(args, wl_name, world, rank, dev, steps, warmup, with_cpu=True):
     out_host = [torch.empty_like(bufs[c].out, device="cpu").pin_memory() for c in range(n_copies)]
     n_e2e = max(5 if phase == "prefill" else 20, min(steps, 1000))
     if cache_cfg:
-        host_w_c = [[layers[0].w_gate[e].cpu().pin_memory() for e in range(cfg.N)],
-                    [layers[0].w_up[e].cpu().pin_memory() for e in range(cfg.N)],
-                    [layers[0].w_down[e].cpu().pin_memory() for e in range(cfg.N)]]
-        side_c = torch.cuda.Stream(device=dev)
-        done_c = torch.cuda.Event()
-        admit_host = torch.zeros(1, dtype=torch.int64).pin_memory()
-        staged_bytes = 0
+        # the overlapped pipeline: admissions copied on a staging stream while
+        # later steps run on the experts already landed (one layer copy)
+        from expert_routing_ffn_gb300.layer import CachePipeline
+        pipe = CachePipeline(layers[0], capacity, decay, stream=stream)
+        pipe.start((1 << capacity) - 1)
+        for i in range(max(3, warmup)):
+            pipe.step(bufs[0], xs[i % n_x], n_resident=0)
+        stream.synchronize()
+        # steps back to back (the host never waits on the step path)
+        n_pipe = max(50, min(steps, 2000))
+        s0 = pipe.pipe.staged_bytes
+        t0 = time.perf_counter()
+        for i in range(n_pipe):
+            pipe.step(bufs[0], xs[i % n_x], n_resident=0)
+        stream.synchronize()
+        pipe_s = time.perf_counter() - t0
+        cache_info["pipeline"] = {"tokens_per_s": world * T * n_pipe / max_over_ranks(world, pipe_s),
+                                  "us_per_step": 1e6 * pipe_s / n_pipe, "steps": n_pipe,
+                                  "staged_bytes_per_step": (pipe.pipe.staged_bytes - s0) / n_pipe,
+                                  "note": "moe_cache_step back to back: layer on cache & landed, heat/cache "
+                                          "update, admissions copied on a staging stream; host clock"}
+        s0 = pipe.pipe.staged_bytes
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(n_e2e):
-        c = i % n_copies
+        c = 0 if cache_cfg else i % n_copies
         xc = xs[i % n_x]
         xc.copy_(x_host[i % n_x], non_blocking=True)
         if la_cfg:
             forward(layers[c], bufs[c], xc, stream=stream)
             lookahead(c, xc)
         elif cache_cfg:
-            forward(layers[c], bufs[c], xc, stream=stream, n_resident=0)
-            moe.moe_cache_update(layers[c].dims.with_T(T), bufs[c].topk_idx, decay, capacity, heat_t, cache_t,
-                                 admit_t, None, stream)
-            admit_host.copy_(admit_t, non_blocking=True)
+            pipe.step(bufs[0], xc, n_resident=0)
         else:
             forward(layers[c], bufs[c], xc, stream=stream)
         out_host[c].copy_(bufs[c].out, non_blocking=True)
         stream.synchronize()
-        if cache_cfg and int(admit_host[0]) != 0:
-            # the experts entering the cache, copied into the weights the next
-            # step reads before it may start
-            nxt = (i + 1) % n_copies
-            staged_bytes += moe.moe_stage_experts(
-                layers[nxt].dims.with_T(T), int(admit_host[0]) & ((1 << 64) - 1), *host_w_c,
-                list(layers[nxt].w_gate), list(layers[nxt].w_up), list(layers[nxt].w_down), side_c, done_c)
-            stream.wait_event(done_c)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(world, time.perf_counter() - t0)
     e2e_value = world * T * n_e2e / e2e_s
     if cache_cfg:
-        cache_info["e2e_staged_bytes_per_step"] = staged_bytes / n_e2e
+        cache_info["e2e_staged_bytes_per_step"] = (pipe.pipe.staged_bytes - s0) / n_e2e
+        pipe.drain()
 
     # ---- expert staging over the host link (EXACT-mode fetches): copy every
     # expert of one layer copy from pinned host memory with moe_stage_experts
@@ -1199,9 +1316,9 @@ def run_workload(args, wl_name, world, rank, dev, steps, warmup, with_cpu=True):
     if cache_info:
         line["config"]["resident"] = f"expert cache of {capacity} (heat decay {decay})"
         line["e2e"]["h2d_bytes_per_step"] += cache_info["e2e_staged_bytes_per_step"]
-        line["e2e"]["d2h_bytes_per_step"] += 8
-        line["e2e"]["note"] += "; plus the cache update, the admitted-expert mask read back and the admitted " \
-                               "experts staged from pinned host memory"
+        line["e2e"]["d2h_bytes_per_step"] += 32
+        line["e2e"]["note"] = "moe_cache_step per step (layer, cache update, admissions copied on a staging " \
+                              "stream) with pinned-host copies of x and out and a stream sync"
         line["cache"] = cache_info
     # the whole step against the same bound: the FFN's algorithmic work plus
     # the router and prefetch-router weights (decode) or FLOPs (prefill)

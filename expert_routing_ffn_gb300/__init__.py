@@ -92,6 +92,20 @@ class moe_hetero_stats(C.Structure):
         return {n: getattr(self, n) for n, _ in self._fields_}
 
 
+MOE_CACHE_RING, MOE_CACHE_FLIGHTS = 16, 8
+
+
+class moe_cache_pipe(C.Structure):
+    """State of the overlapped expert-cache pipeline (include/moe.h)."""
+    _fields_ = [("capacity", C.c_int), ("decay", C.c_float), ("max_flight_experts", C.c_int),
+                ("host_ring", _VP), ("step_events", _VP * MOE_CACHE_RING), ("copy_events", _VP * MOE_CACHE_FLIGHTS),
+                ("dev_masks", _VP), ("dev_heat", _VP), ("dev_stats", _VP),
+                ("step", C.c_longlong), ("consumed", C.c_longlong), ("landed", C.c_uint64), ("in_flight", C.c_uint64),
+                ("flight_mask", C.c_uint64 * MOE_CACHE_FLIGHTS),
+                ("staged_experts", C.c_longlong), ("staged_bytes", C.c_longlong), ("in_time_experts", C.c_longlong),
+                ("stall_experts", C.c_longlong), ("stall_steps", C.c_longlong), ("dev_ring", _VP)]
+
+
 _lib = None
 _lock = threading.Lock()
 
@@ -131,6 +145,10 @@ _PROTOS = {
                            _P], C.c_int),
     "moe_check": ([_P, _P, C.POINTER(C.c_int), C.POINTER(C.c_int32)], C.c_int),
     "moe_hetero_fetch_min_rows": ([C.POINTER(moe_hetero_cost)], C.c_int),
+    "moe_cache_start": ([_DIMS, C.POINTER(moe_cache_pipe), _U64, _P], C.c_int),
+    "moe_cache_step": ([_DIMS, C.POINTER(moe_layer_args), C.POINTER(moe_layer_outputs), C.POINTER(moe_cache_pipe),
+                        _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P], C.c_int),
+    "moe_cache_drain": ([_DIMS, C.POINTER(moe_cache_pipe), _P, _P, _P, _P, _P, _P, _P], C.c_int),
     "moe_select_hetero": ([_DIMS, _P, _P, _P, _P, _F, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
                           C.c_int),
     "moe_cpu_experts_scratch_size": ([_DIMS], C.c_size_t),
@@ -562,6 +580,32 @@ def moe_layer_forward_hetero(dims, args: moe_layer_args, outs: moe_layer_outputs
         ws.numel(), _stream(stream), _stream(stage_stream), C.c_void_p(stage_event.cuda_event), C.byref(st)),
         "moe_layer_forward_hetero")
     return st
+
+
+def moe_cache_start(dims, pipe: moe_cache_pipe, start_set: int, stream=None):
+    _check(lib().moe_cache_start(C.byref(dims), C.byref(pipe), C.c_uint64(start_set & (2**64 - 1)), _stream(stream)),
+           "moe_cache_start")
+
+
+def moe_cache_step(dims, args: moe_layer_args, outs: moe_layer_outputs, pipe: moe_cache_pipe, host_w, dev_w, ws,
+                   stage_stream, stream=None):
+    """host_w / dev_w: three C arrays of the N experts' host (pinned) and
+    device pointers each (gate, up, down), built once by the caller."""
+    _check(lib().moe_cache_step(C.byref(dims), C.byref(args), C.byref(outs), C.byref(pipe),
+                                *[C.cast(a, C.c_void_p) for a in host_w], *[C.cast(a, C.c_void_p) for a in dev_w],
+                                C.c_void_p(ws.data_ptr()), ws.numel(), _stream(stream), _stream(stage_stream)),
+           "moe_cache_step")
+
+
+def moe_cache_step_prepared(call_args):
+    """moe_cache_step with its ctypes arguments built once (a decode loop's
+    fast path): call_args = the tuple moe_cache_step would pass."""
+    _check(lib().moe_cache_step(*call_args), "moe_cache_step")
+
+
+def moe_cache_drain(dims, pipe: moe_cache_pipe, host_w, dev_w, stage_stream):
+    _check(lib().moe_cache_drain(C.byref(dims), C.byref(pipe), *[C.cast(a, C.c_void_p) for a in host_w],
+                                 *[C.cast(a, C.c_void_p) for a in dev_w], _stream(stage_stream)), "moe_cache_drain")
 
 
 def moe_check(ws, stream=None):

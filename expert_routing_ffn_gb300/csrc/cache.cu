@@ -10,6 +10,12 @@
 //   cache   <- the `capacity` experts of largest heat, lowest index on ties
 //   admit   <- new cache & ~old cache (the experts to stage in before the
 //              next step), plus hit / slot / admit / evict counters.
+// With a resident output (the overlapped cache pipeline, which passes the
+// landed mask, the experts whose weights have arrived, by value) it also
+// writes resident <- new cache & landed, the set the next step runs on,
+// counts hits against the old resident set (what the step actually ran on)
+// instead of the old cache, and may write the four masks into a read-back
+// entry that the host can read (mapped pinned memory).
 // One block of 64 threads (N <= 64): a shared-memory histogram of the routed
 // slots, the heat update, then every thread ranks its expert against all
 // others and a ballot forms the new cache.
@@ -21,7 +27,9 @@ namespace moe {
 __global__ void __launch_bounds__(64) cache_update_kernel(const int32_t* __restrict__ topk_idx, int n_slots, int N,
                                                           float decay, int capacity, float* __restrict__ heat,
                                                           uint64_t* __restrict__ cache, uint64_t* __restrict__ admit,
-                                                          int32_t* __restrict__ stats) {
+                                                          int32_t* __restrict__ stats, uint64_t landed,
+                                                          uint64_t* __restrict__ resident,
+                                                          uint64_t* __restrict__ readback) {
     __shared__ int cnt[kMaxExperts];
     __shared__ float h[kMaxExperts];
     __shared__ uint32_t bits[2];
@@ -30,6 +38,7 @@ __global__ void __launch_bounds__(64) cache_update_kernel(const int32_t* __restr
     cnt[e] = 0;
     __syncthreads();
     const uint64_t old = *cache;
+    const uint64_t ran_on = resident ? *resident : old;  // the set this step's layer used
     for (int i = e; i < n_slots; i += blockDim.x) {
         const int x = topk_idx[i];
         if (x >= 0 && x < N) atomicAdd(&cnt[x], 1);
@@ -45,7 +54,7 @@ __global__ void __launch_bounds__(64) cache_update_kernel(const int32_t* __restr
     const bool in = e < N && rank < capacity;
     const uint32_t b = __ballot_sync(0xffffffffu, in);
     // hits: routed slots whose expert was in the old cache
-    int hit = (e < N && ((old >> e) & 1)) ? cnt[e] : 0, slots = e < N ? cnt[e] : 0;
+    int hit = (e < N && ((ran_on >> e) & 1)) ? cnt[e] : 0, slots = e < N ? cnt[e] : 0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         hit += __shfl_xor_sync(0xffffffffu, hit, o);
@@ -58,6 +67,13 @@ __global__ void __launch_bounds__(64) cache_update_kernel(const int32_t* __restr
         const uint64_t nw = (uint64_t)bits[0] | ((uint64_t)bits[1] << 32);
         *cache = nw;
         if (admit) *admit = nw & ~old;
+        if (resident) *resident = nw & landed;
+        if (readback) {  // cache, landed, resident, admit: straight into the host's read-back entry
+            readback[0] = nw;
+            readback[1] = landed;
+            readback[2] = nw & landed;
+            readback[3] = nw & ~old;
+        }
         if (stats) {
             stats[0] += s_hits[0] + s_hits[1];
             stats[1] += s_slots[0] + s_slots[1];
@@ -68,8 +84,10 @@ __global__ void __launch_bounds__(64) cache_update_kernel(const int32_t* __restr
 }
 
 cudaError_t launch_cache_update(const int32_t* topk_idx, int n_slots, int N, float decay, int capacity, float* heat,
-                                uint64_t* cache, uint64_t* admit, int32_t* stats, cudaStream_t st) {
-    cache_update_kernel<<<1, 64, 0, st>>>(topk_idx, n_slots, N, decay, capacity, heat, cache, admit, stats);
+                                uint64_t* cache, uint64_t* admit, int32_t* stats, cudaStream_t st, uint64_t landed,
+                                uint64_t* resident, uint64_t* readback) {
+    cache_update_kernel<<<1, 64, 0, st>>>(topk_idx, n_slots, N, decay, capacity, heat, cache, admit, stats, landed,
+                                          resident, readback);
     return cudaGetLastError();
 }
 

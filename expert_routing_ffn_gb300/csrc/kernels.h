@@ -223,7 +223,10 @@ cudaError_t launch_prefetch_depth(const float* logits, int T, int N, int K, int 
                                   float* conf, int32_t* depth, uint64_t* tok_masks, uint64_t* layer_masks,
                                   cudaStream_t st);
 cudaError_t launch_cache_update(const int32_t* topk_idx, int n_slots, int N, float decay, int capacity, float* heat,
-                                uint64_t* cache, uint64_t* admit, int32_t* stats, cudaStream_t st);
+                                uint64_t* cache, uint64_t* admit, int32_t* stats, cudaStream_t st,
+                                uint64_t landed = ~0ull, uint64_t* resident = nullptr, uint64_t* readback = nullptr);
+// launch counter of moe_launch_total, for launches queued outside moe_api.cu
+void note_launches(int n);
 
 struct CombineArgs {
     const float* y_perm; const int32_t* inv_perm; const float* final_gate;

@@ -218,3 +218,76 @@ def forward_hetero(layer: DeviceLayer, bufs: LayerBuffers, x, host: HeteroHost, 
     return moe_layer_forward_hetero(layer.dims.with_T(T), args, bufs.outputs_struct(), cost, host.w_gate, host.w_up,
                                     host.w_down, list(layer.w_gate), list(layer.w_up), list(layer.w_down),
                                     host.struct, layer.ws, stage_stream, stage_event, n_threads, stream)
+
+
+class CachePipeline:
+    """The overlapped expert-cache pipeline of one layer (moe_cache_start /
+    moe_cache_step): heat-decayed cache of `capacity` experts, admissions
+    copied from pinned host memory on a staging stream while later steps run
+    on the experts already landed.  The host copies are the layer's own
+    device values copied down once."""
+
+    def __init__(self, layer: DeviceLayer, capacity: int, decay: float, max_flight_experts: int = 0,
+                 stream=None):
+        from . import MOE_CACHE_FLIGHTS, MOE_CACHE_RING, moe_cache_pipe
+        cfg, dev = layer.cfg, layer.device
+        self.layer = layer
+        self.stream = stream if stream is not None else torch.cuda.current_stream(dev)
+        self.stage_stream = torch.cuda.Stream(device=dev)
+        self.ring = torch.zeros(MOE_CACHE_RING * 4, dtype=torch.int64).pin_memory()
+        self.masks = torch.zeros(4, dtype=torch.int64, device=dev)
+        self.heat = torch.zeros(cfg.N, dtype=torch.float32, device=dev)
+        self.stats = torch.zeros(4, dtype=torch.int32, device=dev)
+        self.events = [torch.cuda.Event() for _ in range(MOE_CACHE_RING + MOE_CACHE_FLIGHTS)]
+        for ev in self.events:  # torch creates the CUDA event on its first record
+            ev.record(self.stream)
+        self.host_w = [[layer.w_gate[e].cpu().pin_memory() for e in range(cfg.N)],
+                       [layer.w_up[e].cpu().pin_memory() for e in range(cfg.N)],
+                       [layer.w_down[e].cpu().pin_memory() for e in range(cfg.N)]]
+        self._host_arr = [(C.c_void_p * cfg.N)(*[t.data_ptr() for t in m]) for m in self.host_w]
+        self._dev_arr = [(C.c_void_p * cfg.N)(*[t.data_ptr() for t in m])
+                         for m in (list(layer.w_gate), list(layer.w_up), list(layer.w_down))]
+        p = moe_cache_pipe()
+        p.capacity, p.decay, p.max_flight_experts = capacity, decay, max_flight_experts
+        p.host_ring = self.ring.data_ptr()
+        for i in range(MOE_CACHE_RING):
+            p.step_events[i] = self.events[i].cuda_event
+        for i in range(MOE_CACHE_FLIGHTS):
+            p.copy_events[i] = self.events[MOE_CACHE_RING + i].cuda_event
+        p.dev_masks, p.dev_heat, p.dev_stats = self.masks.data_ptr(), self.heat.data_ptr(), self.stats.data_ptr()
+        self.pipe = p
+        self._args = {}
+
+    def start(self, start_set: int):
+        from . import moe_cache_start
+        self.stream.synchronize()
+        moe_cache_start(self.layer.dims.with_T(1), self.pipe, start_set, self.stream)
+
+    def step(self, bufs: LayerBuffers, x, **kw):
+        """One pipeline step; the ctypes arguments of a (tokens, x, options,
+        buffers) combination are built once and reused."""
+        from . import moe_cache_step_prepared
+        T = x.shape[0]
+        key = (T, x.data_ptr(), tuple(sorted(kw.items())), id(bufs))
+        hit = self._args.get(key)
+        if hit is None:
+            if len(self._args) > 64:
+                self._args.clear()
+            dims, args, outs = self.layer.dims.with_T(T), layer_args(self.layer, x, **kw), bufs.outputs_struct()
+            hit = (C.byref(dims), C.byref(args), C.byref(outs), C.byref(self.pipe),
+                   *[C.cast(a, C.c_void_p) for a in self._host_arr], *[C.cast(a, C.c_void_p) for a in self._dev_arr],
+                   C.c_void_p(self.layer.ws.data_ptr()), self.layer.ws.numel(), _stream(self.stream),
+                   _stream(self.stage_stream), dims, args, outs)
+            self._args[key] = hit
+        moe_cache_step_prepared(hit[:14])
+
+    def drain(self):
+        from . import moe_cache_drain
+        moe_cache_drain(self.layer.dims.with_T(1), self.pipe, self._host_arr, self._dev_arr, self.stage_stream)
+
+    def resident_used(self, step: int) -> int:
+        """The resident set step `step` ran on (its read-back must have completed)."""
+        from . import MOE_CACHE_RING
+        if step == 0:
+            return as_u64(int(self.ring[2].item())) if self.pipe.step == 0 else None
+        return as_u64(int(self.ring[((step - 1) % MOE_CACHE_RING) * 4 + 2].item()))

@@ -566,6 +566,78 @@ moe_status moe_layer_forward_hetero(const moe_dims* dims, const moe_layer_args* 
                                     void* stream, void* stage_stream, void* stage_event,
                                     moe_hetero_stats* stats);
 
+/* Overlapped expert-cache pipeline for decode loops (beyond the single
+ * layer forward; ELMoE-3D expert-axis elasticity with its heat decay; SPICE
+ * write-up, confidence-aware prefetch: copies must start D_min =
+ * ceil(W_e / (B T_layer)) layers ahead to land in time).  The layer runs on
+ * resident = cache & landed, where `landed` holds the experts whose weights
+ * have arrived.  Each step queues, with no host synchronisation on the step
+ * path: the layer forward; the heat / cache update (moe_cache_update's
+ * rule), which also forms the next step's resident set from the host's
+ * landed mask (passed by value); and a read-back of the masks (written by
+ * that kernel straight into the pinned ring when the ring is mapped into
+ * the device's address space, else copied).  Read-backs of earlier
+ * steps that have completed are consumed at the start of a step: every
+ * expert of that step's cache that has neither landed nor is in flight is
+ * copied from pinned host memory on stage_stream (moe_stage_experts into
+ * dev_w_*), and lands in the resident set when its event has completed (a
+ * later step), so copies overlap the steps that keep running on the old
+ * set.  An evicted expert loses its landed status, so a later admission
+ * copies it again.  Under MOE_MISS_EXACT the layer instead waits for its
+ * misses: the host reads the fetch mask (synchronising), misses already in
+ * flight are waited for on the GPU (they landed in time for the layer), the
+ * others are copied at once and waited for (a stall).
+ * The caller creates the events (cudaEvent_t as void*, timing disabled is
+ * fine) and the buffers, zeroes the struct's state fields, sets the
+ * configuration and calls moe_cache_start once; the struct then carries the
+ * pipeline's state between steps.  One pipeline per layer; not thread-safe. */
+#define MOE_CACHE_RING 16
+#define MOE_CACHE_FLIGHTS 8
+typedef struct {
+    /* configuration */
+    int capacity;                          /* experts in the cache */
+    float decay;                           /* heat decay per step, in [0, 1] */
+    int max_flight_experts;                /* experts being copied at once, at most (<= 0: no bound) */
+    /* caller-owned resources */
+    uint64_t* host_ring;                   /* pinned host uint64[MOE_CACHE_RING * 4] */
+    void* step_events[MOE_CACHE_RING];     /* one per ring entry */
+    void* copy_events[MOE_CACHE_FLIGHTS];  /* one per copy batch in flight */
+    uint64_t* dev_masks;                   /* device uint64[4]: cache, (reserved), resident, admit */
+    float* dev_heat;                       /* device float32[N] */
+    int32_t* dev_stats;                    /* device int32[4] or NULL: moe_cache_update's counters */
+    /* state (kept by the library) */
+    long long step, consumed;
+    uint64_t landed, in_flight;
+    uint64_t flight_mask[MOE_CACHE_FLIGHTS];
+    /* totals since moe_cache_start */
+    long long staged_experts, staged_bytes;    /* admission and stall copies queued */
+    long long in_time_experts;                 /* EXACT misses that were already in flight or landed */
+    long long stall_experts, stall_steps;      /* EXACT misses copied on demand, and the steps with any */
+    uint64_t* dev_ring;                        /* the ring's device address if mapped, else NULL (set by start) */
+} moe_cache_pipe;
+
+/* Reset the pipeline's state: cache = landed = resident = start_set (experts
+ * preloaded on the device), heat = 0, admit = 0, counters zeroed; queued on
+ * `stream`.  Errors: INVALID_ARG (NULL resources, capacity < 0, decay
+ * outside [0, 1], start_set with experts >= N), CUDA. */
+moe_status moe_cache_start(const moe_dims* dims, moe_cache_pipe* pipe, uint64_t start_set, void* stream);
+
+/* One decode step of the pipeline (see above): args as for
+ * moe_layer_forward (its resident / n_resident are replaced by the
+ * pipeline's), outs its outputs; host_w_* pinned host copies and dev_w_*
+ * device homes of the N routed experts.  Errors: those of the stages, CUDA,
+ * STAGING. */
+moe_status moe_cache_step(const moe_dims* dims, const moe_layer_args* args, const moe_layer_outputs* outs,
+                          moe_cache_pipe* pipe, const void* const* host_w_gate, const void* const* host_w_up,
+                          const void* const* host_w_down, void* const* dev_w_gate, void* const* dev_w_up,
+                          void* const* dev_w_down, void* ws, size_t ws_bytes, void* stream, void* stage_stream);
+
+/* Wait for every copy in flight and every queued read-back, and fold them
+ * into the state (for the end of a run or a test). */
+moe_status moe_cache_drain(const moe_dims* dims, moe_cache_pipe* pipe, const void* const* host_w_gate,
+                           const void* const* host_w_up, const void* const* host_w_down, void* const* dev_w_gate,
+                           void* const* dev_w_up, void* const* dev_w_down, void* stage_stream);
+
 /* Synchronise `stream`, read and clear the device error word of `ws`.
  * *device_status receives MOE_OK or the first error a kernel recorded;
  * *detail (may be NULL) a code-specific detail (token, expert or stage). */
