@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kPermChunk) permute_scatter_kernel(const int32
         if (LORE) return;
         // only the plan of the path moe_expert_ffn will take
         if (plan.tc_plan) {
-            if (tid == 0) build_tc_plan(plan, s_off);
+            build_tc_plan(plan, s_off);
         } else {
             build_plan(plan, s_off);
         }

@@ -122,22 +122,39 @@ __device__ __forceinline__ void build_plan(const PlanArgs& a, const int* off) {
 }
 
 // Tensor-core plan (see TcPlan): shared-expert group first, then every
-// routed expert with rows.
+// routed expert with rows, in expert order.  Built by a whole block (every
+// thread calls it; N <= blockDim.x): thread e places expert e's segment from
+// one scan of (has rows, row tiles) packed as count + (tiles << 8).
 __device__ __forceinline__ void build_tc_plan(const PlanArgs& a, const int* off) {
     TcPlan& P = *a.tc_plan;
-    int n = 0, t1 = 0, t2 = 0;
-    const int n2 = a.d / 256;
-    auto add = [&](int shared, int expert, int row0, int rows, int n1) {
-        TcSeg& s = P.seg[n++];
-        s.shared = shared; s.expert = expert; s.row0 = row0; s.rows = rows;
-        s.m_tiles = (rows + 127) / 128; s.n1 = n1; s.tile1 = t1; s.tile2 = t2;
-        t1 += s.m_tiles * n1;
-        t2 += s.m_tiles * n2;
-    };
-    if (a.n_shared > 0) add(1, a.N, 0, a.T, a.n_shared * a.I_shared / 128);
-    for (int e = 0; e < a.N; ++e)
-        if (off[e + 1] > off[e]) add(0, e, off[e], off[e + 1] - off[e], a.I / 128);
-    P.n_seg = n; P.n_tiles1 = t1; P.n_tiles2 = t2;
+    const int tid = threadIdx.x;
+    const int n1 = a.I / 128, n2 = a.d / 256;
+    const bool sh = a.n_shared > 0;
+    const int sh_m = sh ? (a.T + 127) / 128 : 0, sh_n1 = sh ? a.n_shared * a.I_shared / 128 : 0;
+    int rows = 0, m = 0;
+    if (tid < a.N) {
+        rows = off[tid + 1] - off[tid];
+        m = (rows + 127) / 128;
+    }
+    int tot;
+    const int before = block_exclusive_scan((rows > 0 ? 1 : 0) | (m << 8), &tot);
+    if (rows > 0) {
+        TcSeg& s = P.seg[(sh ? 1 : 0) + (before & 0xff)];
+        const int m_prev = before >> 8;
+        s.shared = 0; s.expert = tid; s.row0 = off[tid]; s.rows = rows; s.m_tiles = m; s.n1 = n1;
+        s.tile1 = sh_m * sh_n1 + m_prev * n1;
+        s.tile2 = sh_m * n2 + m_prev * n2;
+    }
+    if (tid == 0) {
+        if (sh) {
+            TcSeg& s = P.seg[0];
+            s.shared = 1; s.expert = a.N; s.row0 = 0; s.rows = a.T; s.m_tiles = sh_m; s.n1 = sh_n1;
+            s.tile1 = 0; s.tile2 = 0;
+        }
+        P.n_seg = (sh ? 1 : 0) + (tot & 0xff);
+        P.n_tiles1 = sh_m * sh_n1 + (tot >> 8) * n1;
+        P.n_tiles2 = sh_m * n2 + (tot >> 8) * n2;
+    }
 }
 
 // Up to blockDim.x (<= 1024) slots: one block, one thread per slot.  Slots with the same
@@ -193,7 +210,7 @@ __device__ __forceinline__ void permute_block(const int32_t* __restrict__ final_
     }
     // only the plan of the path moe_expert_ffn will take
     if (plan.tc_plan) {
-        if (tid == 0) build_tc_plan(plan, s_off);
+        build_tc_plan(plan, s_off);
     } else {
         build_plan(plan, s_off);
     }

@@ -492,6 +492,11 @@ __global__ void __launch_bounds__(64) batch_resident_final_kernel(const float* _
 
 // ---------------------------------------------------------------------------
 // Miss handling, one warp per token (APEX §4.3 Algorithm 1; SPICE LoRE).
+// Lane l holds experts l and l + 32.  Every decision is lane-parallel: the
+// misses are classified by ballots, the substitutes are the pool members of
+// pool rank below the number of substitutions (one pass of independent rank
+// comparisons, as in route_select_token), and each final expert is written to
+// its slot (its rank by router probability) by the lane that holds it.
 __device__ __forceinline__ void select_token(
     int t, const float* __restrict__ router_prob, const int32_t* __restrict__ topk_idx,
     const uint64_t* __restrict__ prefetch_mask, const uint64_t* __restrict__ resident, int policy,
@@ -504,49 +509,59 @@ __device__ __forceinline__ void select_token(
     const int e0 = lane, e1 = lane + 32;
     const float a0 = e0 < N ? router_prob[(size_t)t * N + e0] : -INFINITY;
     const float a1 = e1 < N ? router_prob[(size_t)t * N + e1] : -INFINITY;
-    uint64_t routed = 0;
-    bool bad = false;
-    for (int j = 0; j < k; ++j) {
-        const int e = topk_idx[(size_t)t * k + j];
-        if (e < 0 || e >= N) bad = true;
-        else routed |= 1ull << e;
-    }
+    // the routed set: lane j < k reads slot j
+    const int re = lane < k ? topk_idx[(size_t)t * k + lane] : 0;
+    const bool bad = __any_sync(0xffffffffu, lane < k && (re < 0 || re >= N));
     if (bad) {
         if (lane == 0) set_error(err, MOE_ERR_DEVICE_INDEX, t);
         return;
     }
+    const uint32_t rlo = __reduce_or_sync(0xffffffffu, lane < k && re < 32 ? 1u << re : 0u);
+    const uint32_t rhi = __reduce_or_sync(0xffffffffu, lane < k && re >= 32 ? 1u << (re - 32) : 0u);
+    const uint64_t routed = (uint64_t)rlo | ((uint64_t)rhi << 32);
     const uint64_t pref = prefetch_mask ? prefetch_mask[t] : ~0ull;
     const uint64_t res = resident ? *resident : ~0ull;
     const uint64_t avail = pref & res & vm;
     const uint64_t missing = routed & ~avail;
+    // misses: LoRE below gamma (HYBRID, HETERO), the rest fetched or substituted
     uint64_t lore = 0, fetch = 0, to_sub = 0;
-    for (uint64_t mm = missing; mm; mm &= mm - 1) {
-        const int e = __ffsll((long long)mm) - 1;
-        const uint64_t bit = 1ull << e;
-        const float ae = __shfl_sync(0xffffffffu, e < 32 ? a0 : a1, e & 31);
-        switch (policy) {
-            case MOE_MISS_EXACT: fetch |= bit; break;
-            case MOE_MISS_LORE: lore |= bit; break;
-            case MOE_MISS_SUBSTITUTE: to_sub |= bit; break;
-            case MOE_MISS_HETERO:  // exact either way: fetch or host (decided per expert afterwards)
-                if (ae < gamma) lore |= bit; else fetch |= bit;
-                break;
-            default:
-                if (ae < gamma) lore |= bit; else to_sub |= bit;
+    if (missing) {
+        if (policy == MOE_MISS_EXACT) {
+            fetch = missing;
+        } else if (policy == MOE_MISS_LORE) {
+            lore = missing;
+        } else if (policy == MOE_MISS_SUBSTITUTE) {
+            to_sub = missing;
+        } else {
+            const bool l0 = ((missing >> e0) & 1) && a0 < gamma;
+            const bool l1 = ((missing >> e1) & 1) && a1 < gamma;
+            lore = (uint64_t)__ballot_sync(0xffffffffu, l0) | ((uint64_t)__ballot_sync(0xffffffffu, l1) << 32);
+            if (policy == MOE_MISS_HETERO) fetch = missing & ~lore;  // exact either way: fetch or host
+            else to_sub = missing & ~lore;
         }
     }
     // substitutes: the available, non-routed experts with the largest router
-    // probability, one per substituted miss
-    uint64_t pool = avail & ~routed, subs = 0;
+    // probability, one per substituted miss (the whole pool if it is smaller)
+    const uint64_t pool = avail & ~routed;
     const int n_sub = __popcll(to_sub);
+    uint64_t subs = 0;
     bool shortfall = false;
-    for (int j = 0; j < n_sub; ++j) {
-        if (!pool) { shortfall = true; break; }
-        float v; int i;
-        lane_best(a0, a1, pool, lane, v, i);
-        warp_argmax(v, i);
-        subs |= 1ull << i;
-        pool &= ~(1ull << i);
+    if (n_sub > 0) {
+        if (__popcll(pool) <= n_sub) {
+            subs = pool;
+            shortfall = __popcll(pool) < n_sub;
+        } else {
+            int p0 = 0, p1 = 0;  // pool members ahead of e0 / e1
+#pragma unroll 8
+            for (int j = 0; j < 64; ++j) {
+                const float aj = __shfl_sync(0xffffffffu, j < 32 ? a0 : a1, j & 31);
+                const bool in = (pool >> j) & 1;
+                p0 += (in && (aj > a0 || (aj == a0 && j < e0))) ? 1 : 0;
+                p1 += (in && (aj > a1 || (aj == a1 && j < e1))) ? 1 : 0;
+            }
+            const bool s0 = ((pool >> e0) & 1) && p0 < n_sub, s1 = ((pool >> e1) & 1) && p1 < n_sub;
+            subs = (uint64_t)__ballot_sync(0xffffffffu, s0) | ((uint64_t)__ballot_sync(0xffffffffu, s1) << 32);
+        }
     }
     const uint64_t fin = (routed & ~missing) | lore | fetch | subs;
     // canonical slot order: descending router probability, lowest index first
@@ -559,31 +574,34 @@ __device__ __forceinline__ void select_token(
         c1 += (aj > a1 || (aj == a1 && j < e1)) ? 1 : 0;
     }
     const bool f0 = (fin >> e0) & 1, f1 = (fin >> e1) & 1;
+    const int nf = __popcll(fin);
     float gsum = 0.f;
-    int idx[kMaxTopK];
-    float gate[kMaxTopK];
-    for (int j = 0; j < k; ++j) {
-        const bool own0 = f0 && c0 == j, own1 = f1 && c1 == j;
-        const uint32_t b = __ballot_sync(0xffffffffu, own0 || own1);
-        if (!b) { idx[j] = -1; gate[j] = 0.f; continue; }
-        const int owner = __ffs(b) - 1;
-        const float v = __shfl_sync(0xffffffffu, own0 ? a0 : a1, owner);
-        const int i = __shfl_sync(0xffffffffu, own0 ? e0 : e1, owner);
-        idx[j] = i;
-        gate[j] = v;
-        gsum += v;
+    if (renorm) {  // the final gates summed in slot order
+        float g = 0.f;
+        for (int j = 0; j < nf; ++j) {
+            const uint32_t b0 = __ballot_sync(0xffffffffu, f0 && c0 == j);
+            const uint32_t b1 = __ballot_sync(0xffffffffu, f1 && c1 == j);
+            const int src = b0 ? __ffs(b0) - 1 : __ffs(b1) - 1;
+            const float v = __shfl_sync(0xffffffffu, b0 ? a0 : a1, src);
+            g += v;
+        }
+        gsum = g;
+    }
+    auto put = [&](int slot, int e, float a) {
+        const size_t sl = (size_t)t * k + slot;
+        final_idx[sl] = e;
+        final_gate[sl] = (renorm && gsum > 0.f) ? a / gsum : a;
+        final_kind[sl] = ((lore >> e) & 1) ? MOE_KIND_LORE : ((fetch >> e) & 1) ? MOE_KIND_FETCH : MOE_KIND_COMPUTE;
+    };
+    if (f0 && c0 < k) put(c0, e0, a0);
+    if (f1 && c1 < k) put(c1, e1, a1);
+    if (lane >= nf && lane < k) {  // fewer final experts than slots (a capacity shortfall)
+        const size_t sl = (size_t)t * k + lane;
+        final_idx[sl] = -1;
+        final_gate[sl] = 0.f;
+        final_kind[sl] = MOE_KIND_COMPUTE;
     }
     if (lane == 0) {
-        for (int j = 0; j < k; ++j) {
-            const size_t sl = (size_t)t * k + j;
-            const int e = idx[j];
-            final_idx[sl] = e;
-            final_gate[sl] = (renorm && gsum > 0.f) ? gate[j] / gsum : gate[j];
-            int kind = MOE_KIND_COMPUTE;
-            if (e >= 0 && ((lore >> e) & 1)) kind = MOE_KIND_LORE;
-            else if (e >= 0 && ((fetch >> e) & 1)) kind = MOE_KIND_FETCH;
-            final_kind[sl] = kind;
-        }
         if (fetch_mask && fetch) atomicOr(reinterpret_cast<unsigned long long*>(fetch_mask),
                                           (unsigned long long)fetch);
         if (counters) {
@@ -714,17 +732,23 @@ __global__ void __launch_bounds__(256) route_front_kernel(const __grid_constant_
         batch_resident_block(qp, T, N, a.n_resident, bres);
         if (tid == 0) *a.batch_resident = *bres;
     }
-    if (tid == 0) {
-        if (sa.counters)
-            for (int i = 0; i < MOE_NUM_COUNTERS; ++i) sa.counters[i] = 0;
-        if (sa.fetch_mask) *sa.fetch_mask = 0ull;
-    }
+    // the slot counters and the fetch mask gather in shared memory and go out
+    // with plain stores (this block is their only writer): global atomics on
+    // lines this thread has just cleared cost microseconds on the critical path
+    __shared__ int32_t s_cnt[MOE_NUM_COUNTERS];
+    __shared__ unsigned long long s_fetch;
+    if (tid < MOE_NUM_COUNTERS) s_cnt[tid] = 0;
+    if (tid == 0) s_fetch = 0ull;
     __syncthreads();
     const uint64_t* resident = a.n_resident > 0 ? bres : sa.resident;
     for (int t = warp; t < T; t += nw)
         select_token(t, prob, tki, sa.prefetch_mask ? pm : nullptr, resident, sa.policy, sa.gamma, dh,
-                     sa.delta_star ? ds : nullptr, N, k, sa.renorm, fi, fg, fk, sa.fetch_mask, sa.counters, sa.err);
+                     sa.delta_star ? ds : nullptr, N, k, sa.renorm, fi, fg, fk,
+                     sa.fetch_mask ? reinterpret_cast<uint64_t*>(&s_fetch) : nullptr, sa.counters ? s_cnt : nullptr,
+                     sa.err);
     __syncthreads();
+    if (sa.counters && tid < MOE_NUM_COUNTERS) sa.counters[tid] = s_cnt[tid];
+    if (sa.fetch_mask && tid == 0) *sa.fetch_mask = s_fetch;
     for (int i = tid; i < T * k; i += blockDim.x) {
         sa.final_idx[i] = fi[i];
         sa.final_gate[i] = fg[i];
