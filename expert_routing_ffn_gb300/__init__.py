@@ -145,6 +145,7 @@ _PROTOS = {
                            _P], C.c_int),
     "moe_check": ([_P, _P, C.POINTER(C.c_int), C.POINTER(C.c_int32)], C.c_int),
     "moe_hetero_fetch_min_rows": ([C.POINTER(moe_hetero_cost)], C.c_int),
+    "moe_set_graph_replay": ([C.c_int], None),
     "moe_cache_start": ([_DIMS, C.POINTER(moe_cache_pipe), _U64, _P], C.c_int),
     "moe_cache_step": ([_DIMS, C.POINTER(moe_layer_args), C.POINTER(moe_layer_outputs), C.POINTER(moe_cache_pipe),
                         _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P], C.c_int),
@@ -606,6 +607,11 @@ def moe_cache_step_prepared(call_args):
 def moe_cache_drain(dims, pipe: moe_cache_pipe, host_w, dev_w, stage_stream):
     _check(lib().moe_cache_drain(C.byref(dims), C.byref(pipe), *[C.cast(a, C.c_void_p) for a in host_w],
                                  *[C.cast(a, C.c_void_p) for a in dev_w], _stream(stage_stream)), "moe_cache_drain")
+
+
+def moe_set_graph_replay(enabled: bool):
+    """moe_layer_forward's graph replay on (default) or off."""
+    lib().moe_set_graph_replay(int(bool(enabled)))
 
 
 def moe_check(ws, stream=None):

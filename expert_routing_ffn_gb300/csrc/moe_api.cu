@@ -734,8 +734,14 @@ moe_status moe_combine(const moe_dims* dims, const float* y_perm, const int32_t*
     return MOE_OK;
 }
 
-moe_status moe_layer_forward(const moe_dims* dims, const moe_layer_args* A,
-                             const moe_layer_outputs* O, void* ws, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The launch sequence of one layer forward (moe_layer_forward runs it
+// directly, or captures it once into a CUDA graph and replays that).
+moe_status layer_forward_launch(const moe_dims* dims, const moe_layer_args* A, const moe_layer_outputs* O,
+                                void* ws, size_t ws_bytes, void* stream) {
     MOE_TRY(check_dims(dims));
     if (!A || !O) return MOE_ERR_INVALID_ARG;
     if (A->policy == MOE_MISS_HETERO) return MOE_ERR_INVALID_ARG;  // moe_layer_forward_hetero
@@ -821,6 +827,97 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_layer_args* A,
     MOE_TRY(moe_combine(dims, O->y_perm, O->inv_perm, O->final_gate, O->final_kind,
                         dims->n_shared > 0 ? O->y_shared : nullptr, lore ? O->y_lore : nullptr,
                         O->out, stream));
+    return MOE_OK;
+}
+
+// Instantiated graphs of moe_layer_forward, keyed by the exact bytes of its
+// arguments (dims, the layer arguments, the output pointers, the workspace)
+// and the device.  A replay reads the same buffers at the same addresses, so
+// the values in them may change between calls.
+struct GraphEntry {
+    int device;
+    moe_dims dims;
+    moe_layer_args args;
+    moe_layer_outputs outs;
+    void* ws;
+    size_t ws_bytes;
+    cudaGraphExec_t exec;
+    int launches;
+    uint64_t last_use;
+};
+constexpr int kMaxGraphs = 48;
+std::mutex g_graph_mu;
+GraphEntry g_graphs[kMaxGraphs];
+int g_n_graphs = 0;
+uint64_t g_graph_clock = 0;
+std::atomic<int> g_graphs_enabled{1};
+
+bool same_call(const GraphEntry& g, int dev, const moe_dims* D, const moe_layer_args* A, const moe_layer_outputs* O,
+               void* ws, size_t ws_bytes) {
+    return g.device == dev && g.ws == ws && g.ws_bytes == ws_bytes && !std::memcmp(&g.dims, D, sizeof(moe_dims)) &&
+           !std::memcmp(&g.args, A, sizeof(moe_layer_args)) && !std::memcmp(&g.outs, O, sizeof(moe_layer_outputs));
+}
+
+}  // namespace
+
+extern "C" {
+
+void moe_set_graph_replay(int enabled) { g_graphs_enabled.store(enabled ? 1 : 0); }
+
+moe_status moe_layer_forward(const moe_dims* dims, const moe_layer_args* A, const moe_layer_outputs* O, void* ws,
+                             size_t ws_bytes, void* stream) {
+    MOE_TRY(check_dims(dims));
+    if (!A || !O) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = S(stream);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    // inside the caller's own capture, or with replay off: plain launches
+    if (dims->T == 0 || !g_graphs_enabled.load() || cudaStreamIsCapturing(s, &cap) != cudaSuccess ||
+        cap != cudaStreamCaptureStatusNone || s == nullptr)
+        return layer_forward_launch(dims, A, O, ws, ws_bytes, stream);
+    int dev = 0;
+    MOE_CUDA(cudaGetDevice(&dev));
+    {
+        std::lock_guard<std::mutex> lock(g_graph_mu);
+        for (int i = 0; i < g_n_graphs; ++i) {
+            GraphEntry& g = g_graphs[i];
+            if (!same_call(g, dev, dims, A, O, ws, ws_bytes)) continue;
+            g.last_use = ++g_graph_clock;
+            MOE_CUDA(cudaGraphLaunch(g.exec, s));
+            count(g.launches);
+            return MOE_OK;
+        }
+    }
+    // first call with these arguments: capture the launch sequence
+    if (!side_stream()) return MOE_ERR_CUDA;  // created outside the capture
+    MOE_CUDA(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
+    const uint64_t before = g_launches.load();
+    const moe_status st = layer_forward_launch(dims, A, O, ws, ws_bytes, stream);
+    const int launches = (int)(g_launches.load() - before);
+    cudaGraph_t graph = nullptr;
+    const cudaError_t e = cudaStreamEndCapture(s, &graph);
+    if (st != MOE_OK) {
+        if (graph) cudaGraphDestroy(graph);
+        return st;
+    }
+    if (e != cudaSuccess) return record_cuda(e, "cudaStreamEndCapture");
+    cudaGraphExec_t exec = nullptr;
+    const cudaError_t ei = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (ei != cudaSuccess) return record_cuda(ei, "cudaGraphInstantiate");
+    MOE_CUDA(cudaGraphLaunch(exec, s));  // the capture's launches are counted already
+    std::lock_guard<std::mutex> lock(g_graph_mu);
+    int slot = g_n_graphs;
+    if (g_n_graphs == kMaxGraphs) {  // replace the least recently used
+        slot = 0;
+        for (int i = 1; i < kMaxGraphs; ++i)
+            if (g_graphs[i].last_use < g_graphs[slot].last_use) slot = i;
+        cudaGraphExecDestroy(g_graphs[slot].exec);
+    } else {
+        ++g_n_graphs;
+    }
+    GraphEntry& g = g_graphs[slot];
+    g.device = dev; g.dims = *dims; g.args = *A; g.outs = *O; g.ws = ws; g.ws_bytes = ws_bytes;
+    g.exec = exec; g.launches = launches; g.last_use = ++g_graph_clock;
     return MOE_OK;
 }
 

@@ -521,6 +521,17 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_layer_args* args,
                              const moe_layer_outputs* outs, void* ws, size_t ws_bytes,
                              void* stream);
 
+/* moe_layer_forward replays CUDA graphs: the first call with a given set of
+ * arguments (the bytes of dims, args and outs, the workspace and the device)
+ * on a non-default stream that is not being captured captures the call's
+ * launch sequence into a graph; later calls with the same arguments launch
+ * that graph (one host call instead of one per kernel).  The buffers are
+ * read at replay time, so their contents may change between calls; a call
+ * made while the caller captures its own graph, or on the legacy default
+ * stream, launches the kernels directly.  Up to 48 graphs are kept (least
+ * recently used replaced).  enabled = 0 turns replay off for later calls. */
+void moe_set_graph_replay(int enabled);
+
 /* Host buffers of moe_layer_forward_hetero (pinned host memory, caller-owned;
  * sized for dims->T). */
 typedef struct {
