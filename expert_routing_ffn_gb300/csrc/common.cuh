@@ -212,10 +212,12 @@ __device__ __forceinline__ float4 unit_table_sum(const UnitTable& U, int u, cons
 // m_tiles x d/256; tile index = first tile + nt * m_tiles + mt.
 struct TcSeg {
     int shared, expert, row0, rows, m_tiles, n1, tile1, tile2;
+    int mbase;  // index of this segment's first (segment, row tile) dependency counter
 };
 struct TcPlan {
     int n_seg, n_tiles1, n_tiles2;
-    int pad[13];
+    int n_mt;  // (segment, row tile) pairs: the dependency counters in use
+    int pad[12];
     TcSeg seg[kMaxExperts + 1];
 };
 
@@ -254,7 +256,7 @@ constexpr int kTcdMaxCtas = 160;  // grid of that path: min(SMs, kTcdMaxCtas)
 // ---------------------------------------------------------------- workspace
 struct WsLayout {
     size_t err, ticket, logits_r, logits_p, score, route_part, qp, res_part, plan_hdr, segs, seg_first, perm_counts, lore_z,
-        lore_off, lore_list, lore_pos, lore_counts, lore_zp, lore_v, tc_plan,
+        lore_off, lore_list, lore_pos, lore_counts, lore_zp, lore_v, tc_plan, tc_dep,
         x_perm, h_routed, h_shared, floe_u, floe_kept, floe_list, floe_count, partial, total;
     int max_segs, max_partial_rows;
 };
@@ -321,6 +323,8 @@ __host__ __device__ inline WsLayout ws_layout(const moe_dims& D) {
     L.lore_zp = take(lore_grouped ? 8 * T * (size_t)D.k * (size_t)(D.r > 0 ? D.r : 1) * 4 : 0);  // 8 d-splits
     L.lore_v = take(lore_grouped ? T * (size_t)D.k * (size_t)D.d * 4 : 0);
     L.tc_plan = take(sizeof(TcPlan));
+    // per (segment, row tile) counters of the prefill FFN's phase dependency
+    L.tc_dep = take(tc ? ((T + T * D.k) / 128 + N + 4) * 4 : 0);
     L.x_perm = take(tc || tcd ? T * D.k * (size_t)D.d * 2 : 0);
     L.h_routed = take(tc ? T * D.k * (size_t)D.I * 2 : 0);
     L.h_shared = take(tc ? T * (size_t)D.n_shared * D.I_shared * 2 : 0);

@@ -1,12 +1,21 @@
 // Stage 3b, prefill-size batches: the grouped SwiGLU expert FFN on the
 // 5th-generation tensor cores (tcgen05, accumulators in tensor memory), fed
-// by TMA.  Two persistent launches:
+// by TMA.  One persistent launch runs two kinds of tiles:
 //   phase 1: for every (expert segment, 128-row tile, 128-channel tile):
 //            [gate | up] = X_tile . [Wg_tile ; Wu_tile]^T  (M=128, N=256)
 //            epilogue h = SiLU(gate) * up  -> h (bf16)
 //   phase 2: for every (segment, 128-row tile, 256-column tile of d):
 //            y = h_tile . Wd  (K = I; Wd is [I, d], an MN-major operand)
 //            epilogue -> y (fp32, ungated)
+// Tiles are numbered phase 1 first, then phase 2, and CTA c takes tiles c,
+// c + G, c + 2G, ...  A phase-2 tile needs the h rows of its (segment, row
+// tile) from every phase-1 channel tile: each epilogue warp counts its
+// finished phase-1 tile on that pair's counter (after its stores have
+// completed), and the producer of a phase-2 tile waits for the count before
+// loading h.  A phase-2 tile depends only on phase-1 tiles of the same or an
+// earlier round, which never wait, so every wait ends; so the end of phase 1
+// and the start of phase 2 overlap instead of the second launch waiting for
+// the slowest CTA of the first.
 // Shared experts form one segment whose channels are the concatenation of
 // all shared experts (so phase 2 sums them, as y_shared requires).
 //
@@ -56,18 +65,56 @@ struct TcTile {
     int seg, mt, nt;
 };
 
-template <int PHASE>
-__device__ __forceinline__ bool tc_tile(const TcPlan& P, int t, TcTile& out) {
-    const int total = PHASE == 1 ? P.n_tiles1 : P.n_tiles2;
-    if (t >= total) return false;
+// Tile t of phase `phase` (t counted within the phase).
+__device__ __forceinline__ void tc_tile(const TcPlan& P, int phase, int t, TcTile& out) {
     int s = 0;
-    while (s + 1 < P.n_seg && (PHASE == 1 ? P.seg[s + 1].tile1 : P.seg[s + 1].tile2) <= t) ++s;
+    while (s + 1 < P.n_seg && (phase == 1 ? P.seg[s + 1].tile1 : P.seg[s + 1].tile2) <= t) ++s;
     const TcSeg& S = P.seg[s];
-    const int local = t - (PHASE == 1 ? S.tile1 : S.tile2);
+    const int local = t - (phase == 1 ? S.tile1 : S.tile2);
     out.seg = s;
     out.mt = local % S.m_tiles;
     out.nt = local / S.m_tiles;
-    return true;
+}
+
+// Global tile g: phase 1 below n_tiles1, phase 2 after.
+__device__ __forceinline__ int tc_tile_global(const TcPlan& P, int g, TcTile& out) {
+    if (g < P.n_tiles1) {
+        tc_tile(P, 1, g, out);
+        return 1;
+    }
+    tc_tile(P, 2, g - P.n_tiles1, out);
+    return 2;
+}
+
+// ---------------------------------------------------------------- phase dependency
+// Phase-1 h rows written by other CTAs (TMA stores and plain stores), read by
+// this CTA's TMA loads: the writer orders its completed stores before a
+// release increment, the reader acquires the count and orders it before its
+// async-proxy loads.
+__device__ __forceinline__ void dep_signal(int* cnt) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(cnt), "r"(1) : "memory");
+}
+
+__device__ __forceinline__ bool dep_wait(const int* cnt, int target, volatile int* abort_flag, DevError* err) {
+    const long long t0 = clock64();
+    for (uint32_t i = 0;; ++i) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+        if (v >= target) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            return true;
+        }
+        if ((i & 15) == 15) {
+            if (*abort_flag) return false;
+            if (clock64() - t0 > kTcWaitCycles) {
+                set_error(err, MOE_ERR_TIMEOUT, 7);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+        __nanosleep(128);
+    }
 }
 
 // ---------------------------------------------------------------- epilogue stores
@@ -110,15 +157,20 @@ __device__ __forceinline__ void tma_store_wait_read() {
 __device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // ---------------------------------------------------------------- kernel
-template <int PHASE>
-__global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_constant__ TcParams p) {
-    grid_dep_wait();  // the plan, x_perm / h: no tensor memory taken before it
+struct TcFusedParams {
+    TcParams p1, p2;  // the two phases' tensor maps and outputs
+    int* dep;         // per (segment, row tile): phase-1 epilogue warps done (zeroed by the gather)
+};
+
+__global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_constant__ TcFusedParams fp) {
+    grid_dep_wait();  // the plan, x_perm, the zeroed counters: no tensor memory taken before it
     extern __shared__ unsigned char tc_smem_raw[];
     __shared__ __align__(8) uint64_t full[kTcStages], empty[kTcStages], tfull[2], tempty[2], drain;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
     __shared__ TcPlan plan_s;
 
+    const TcParams& p = fp.p1;  // fields common to both phases
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t smem_base = (smem_u32(tc_smem_raw) + 1023u) & ~1023u;
     volatile int* abort_flag = &abort_s;
@@ -149,17 +201,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
     const uint32_t tmem_base = tmem_base_s;
     const TcPlan& P = plan_s;
     const int d = p.d;
+    const int n_tiles = P.n_tiles1 + P.n_tiles2;
 
     if (warp == 0) {
         // ---------------- TMA producer
         if (lane == 0) {
             int it = 0;
             TcTile tl;
-            for (int t = blockIdx.x; tc_tile<PHASE>(P, t, tl) && !*abort_flag; t += gridDim.x) {
+            for (int g = blockIdx.x; g < n_tiles && !*abort_flag; g += gridDim.x) {
+                const int phase = tc_tile_global(P, g, tl);
                 const TcSeg& S = P.seg[tl.seg];
-                const CUtensorMap* amap = S.shared ? &p.map_a_shared : &p.map_a_routed;
+                const TcParams& q = phase == 1 ? fp.p1 : fp.p2;
+                if (phase == 2 &&
+                    !dep_wait(fp.dep + S.mbase + tl.mt, 4 * S.n1, abort_flag, p.err))
+                    break;
+                const CUtensorMap* amap = S.shared ? &q.map_a_shared : &q.map_a_routed;
                 const int arow = S.row0 + tl.mt * kTcBM;
-                const int nk = PHASE == 1 ? d / (int)kTcBK
+                const int nk = phase == 1 ? d / (int)kTcBK
                                           : (S.shared ? p.n_shared * p.I_shared : p.I) / (int)kTcBK;
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const int st = it % kTcStages;
@@ -169,7 +227,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                     const uint32_t b_dst = a_dst + kTcStageA;
                     mbar_arrive_expect_tx(&full[st], kTcStageBytes);
                     tma_load_2d(a_dst, amap, kb * kTcBK, arow, &full[st]);
-                    if (PHASE == 1) {
+                    if (phase == 1) {
                         int e, nrow;
                         if (S.shared) {
                             const int per = p.I_shared / 128;
@@ -207,16 +265,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
     } else if (warp == 1) {
         // ---------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = tc_idesc(kTcBM, kTcBN, PHASE == 1 ? 0 : 1);
+            constexpr uint32_t idesc1 = tc_idesc(kTcBM, kTcBN, 0);
+            constexpr uint32_t idesc2 = tc_idesc(kTcBM, kTcBN, 1);
             int it = 0, local = 0;
             TcTile tl;
-            for (int t = blockIdx.x; tc_tile<PHASE>(P, t, tl) && !*abort_flag; t += gridDim.x, ++local) {
+            for (int g = blockIdx.x; g < n_tiles && !*abort_flag; g += gridDim.x, ++local) {
+                const int phase = tc_tile_global(P, g, tl);
                 const TcSeg& S = P.seg[tl.seg];
                 const int ab = local & 1;
                 if (!tc_wait(&tempty[ab], ((local >> 1) & 1) ^ 1, abort_flag, p.err, 3)) break;
                 tc_fence_after();
                 const uint32_t tmem_d = tmem_base + ab * kTcBN;
-                const int nk = PHASE == 1 ? d / (int)kTcBK
+                const int nk = phase == 1 ? d / (int)kTcBK
                                           : (S.shared ? p.n_shared * p.I_shared : p.I) / (int)kTcBK;
                 bool ok = true;
                 for (int kb = 0; kb < nk; ++kb, ++it) {
@@ -225,12 +285,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                     tc_fence_after();
                     const uint32_t a_addr = smem_base + st * kTcStageBytes;
                     const uint32_t b_addr = a_addr + kTcStageA;
+                    if (phase == 1) {
 #pragma unroll
-                    for (int kk = 0; kk < (int)kTcBK / 16; ++kk) {
-                        const uint64_t ad = smem_desc(a_addr + kk * 32, 16, 1024);
-                        const uint64_t bd = PHASE == 1 ? smem_desc(b_addr + kk * 32, 16, 1024)
-                                                       : smem_desc(b_addr + kk * 16 * 128, 64 * kTcBK * 2, 1024);
-                        tc_mma(tmem_d, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+                        for (int kk = 0; kk < (int)kTcBK / 16; ++kk)
+                            tc_mma(tmem_d, smem_desc(a_addr + kk * 32, 16, 1024), smem_desc(b_addr + kk * 32, 16, 1024),
+                                   idesc1, (kb | kk) ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < (int)kTcBK / 16; ++kk)
+                            tc_mma(tmem_d, smem_desc(a_addr + kk * 32, 16, 1024),
+                                   smem_desc(b_addr + kk * 16 * 128, 64 * kTcBK * 2, 1024), idesc2,
+                                   (kb | kk) ? 1u : 0u);
                     }
                     tc_commit(&empty[st]);  // frees the stage when these MMAs are done
                 }
@@ -258,9 +323,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
         int local = 0;
         TcTile tl;
         // decisions stay warp-uniform: tcgen05.ld is a whole-warp instruction
-        for (int t = blockIdx.x; tc_tile<PHASE>(P, t, tl); t += gridDim.x, ++local) {
+        for (int g = blockIdx.x; g < n_tiles; g += gridDim.x, ++local) {
             if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+            const int phase = tc_tile_global(P, g, tl);
             const TcSeg& S = P.seg[tl.seg];
+            const TcParams& q = phase == 1 ? fp.p1 : fp.p2;
             const int ab = local & 1;
             bool ok = true;
             if (lane == 0) ok = tc_wait(&tfull[ab], (local >> 1) & 1, abort_flag, p.err, 5);
@@ -271,11 +338,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
             const bool valid = row_in_seg < S.rows;
             const bool boxed = tl.mt * kTcBM + quarter * 32 + 32 <= S.rows;
             const int box_row = S.row0 + tl.mt * kTcBM + quarter * 32;
-            const CUtensorMap* omap = S.shared ? &p.map_out_shared : &p.map_out_routed;
+            const CUtensorMap* omap = S.shared ? &q.map_out_shared : &q.map_out_routed;
             const long long grow = (long long)S.row0 + row_in_seg;
-            if (PHASE == 1) {
-                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(S.shared ? p.out_shared : p.out_routed);
-                const long long ld = S.shared ? p.ld_out_shared : p.ld_out_routed;
+            if (phase == 1) {
+                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(S.shared ? q.out_shared : q.out_routed);
+                const long long ld = S.shared ? q.ld_out_shared : q.ld_out_routed;
                 __nv_bfloat16* dst = out + grow * ld + (long long)tl.nt * 128;
 #pragma unroll 1
                 for (int c = 0; c < 128; c += 64) {  // 64 channels = one 128-byte box row
@@ -285,25 +352,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                     }
 #pragma unroll 1
                     for (int hh = 0; hh < 2; ++hh) {
-                        float g[32], u[32];
-                        tmem_ld32(taddr + c + hh * 32, g);
-                        tmem_ld32(taddr + 128 + c + hh * 32, u);
+                        float gv[32], uv[32];
+                        tmem_ld32(taddr + c + hh * 32, gv);
+                        tmem_ld32(taddr + 128 + c + hh * 32, uv);
                         uint32_t w[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float h0 = g[2 * i] / (1.f + expf(-g[2 * i])) * u[2 * i];
-                            const float h1 = g[2 * i + 1] / (1.f + expf(-g[2 * i + 1])) * u[2 * i + 1];
+                            const float h0 = gv[2 * i] / (1.f + expf(-gv[2 * i])) * uv[2 * i];
+                            const float h1 = gv[2 * i + 1] / (1.f + expf(-gv[2 * i + 1])) * uv[2 * i + 1];
                             w[i] = pack_bf16x2(h0, h1);
                         }
                         if (boxed) {
 #pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                st_shared_v4(orow + ((((uint32_t)(hh * 4 + q)) ^ sw) << 4), w[4 * q], w[4 * q + 1],
-                                             w[4 * q + 2], w[4 * q + 3]);
+                            for (int qq = 0; qq < 4; ++qq)
+                                st_shared_v4(orow + ((((uint32_t)(hh * 4 + qq)) ^ sw) << 4), w[4 * qq],
+                                             w[4 * qq + 1], w[4 * qq + 2], w[4 * qq + 3]);
                         } else if (valid) {
                             uint4* o = reinterpret_cast<uint4*>(dst + c + hh * 32);
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) o[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                            for (int qq = 0; qq < 4; ++qq)
+                                o[qq] = make_uint4(w[4 * qq], w[4 * qq + 1], w[4 * qq + 2], w[4 * qq + 3]);
                         }
                     }
                     if (boxed) {
@@ -313,8 +381,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                     }
                 }
             } else {
-                float* out = static_cast<float*>(S.shared ? p.out_shared : p.out_routed);
-                const long long ld = S.shared ? p.ld_out_shared : p.ld_out_routed;
+                float* out = static_cast<float*>(S.shared ? q.out_shared : q.out_routed);
+                const long long ld = S.shared ? q.ld_out_shared : q.ld_out_routed;
                 float* dst = out + grow * ld + (long long)tl.nt * kTcBN;
 #pragma unroll 1
                 for (int c = 0; c < kTcBN; c += 32) {  // 32 columns = one 128-byte box row
@@ -324,10 +392,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                         if (lane == 0) tma_store_wait_read();
                         __syncwarp();
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            st_shared_v4(orow + (((uint32_t)q ^ sw) << 4), __float_as_uint(v[4 * q]),
-                                         __float_as_uint(v[4 * q + 1]), __float_as_uint(v[4 * q + 2]),
-                                         __float_as_uint(v[4 * q + 3]));
+                        for (int qq = 0; qq < 8; ++qq)
+                            st_shared_v4(orow + (((uint32_t)qq ^ sw) << 4), __float_as_uint(v[4 * qq]),
+                                         __float_as_uint(v[4 * qq + 1]), __float_as_uint(v[4 * qq + 2]),
+                                         __float_as_uint(v[4 * qq + 3]));
                         fence_async_smem();
                         __syncwarp();
                         if (lane == 0) tma_store_2d(omap, tl.nt * kTcBN + c, box_row, obox);
@@ -341,6 +409,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[ab]);
+            if (phase == 1) {
+                // this warp's rows of h are complete in global memory: count
+                // them for the phase-2 tiles of this (segment, row tile)
+                if (lane == 0) tma_store_wait_all();
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) dep_signal(fp.dep + S.mbase + tl.mt);
+            }
         }
         // the block's shared memory stays allocated until these stores have
         // read it, and the output is complete when the grid ends
@@ -357,13 +433,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
 }
 
 // ---------------------------------------------------------------- gather
-// x_perm[pos] = x[perm[pos] / k] for the routed rows (bf16, 16-byte copies).
+// x_perm[pos] = x[perm[pos] / k] for the routed rows (bf16, 16-byte copies);
+// block 0 also clears the FFN kernel's phase-dependency counters.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x,
                                                           const int32_t* __restrict__ perm,
                                                           const int32_t* __restrict__ expert_offsets,
                                                           int N, int k, int chunks_per_row,
-                                                          int rows_cap, uint4* __restrict__ x_perm) {
+                                                          int rows_cap, uint4* __restrict__ x_perm,
+                                                          int* __restrict__ dep, int n_dep) {
     grid_dep_wait();  // the previous kernels' outputs (dependent launch)
+    if (blockIdx.x == 0 && dep)
+        for (int i = threadIdx.x; i < n_dep; i += blockDim.x) dep[i] = 0;
     const int n_rows = expert_offsets[N];
     for (int pos = blockIdx.x; pos < n_rows && pos < rows_cap; pos += gridDim.x) {
         const int tok = perm[pos] / k;
@@ -374,15 +454,16 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 
 // ---------------------------------------------------------------- host
 cudaError_t launch_gather_rows(const void* x, const int32_t* perm, const int32_t* expert_offsets, int N,
-                               int k, int d, int rows_cap, void* x_perm, cudaStream_t st) {
+                               int k, int d, int rows_cap, void* x_perm, cudaStream_t st, int* dep, int n_dep) {
     const int chunks = d / 8;
     const int g_rows = rows_cap < 4096 ? (rows_cap > 0 ? rows_cap : 1) : 4096;
     return launch_pdl(gather_rows_kernel, dim3(g_rows), dim3(256), 0, st, static_cast<const uint4*>(x), perm,
-                      expert_offsets, N, k, chunks, rows_cap, static_cast<uint4*>(x_perm));
+                      expert_offsets, N, k, chunks, rows_cap, static_cast<uint4*>(x_perm), dep, n_dep);
 }
 
 cudaError_t launch_tc_ffn(const TcLaunch& a, cudaStream_t st) {
-    cudaError_t e = launch_gather_rows(a.x, a.perm, a.expert_offsets, a.N, a.k, a.d, a.rows_cap, a.x_perm, st);
+    cudaError_t e = launch_gather_rows(a.x, a.perm, a.expert_offsets, a.N, a.k, a.d, a.rows_cap, a.x_perm, st,
+                                       a.dep, a.n_dep);
     if (e != cudaSuccess) return e;
 
     TcParams p1;
@@ -416,15 +497,14 @@ cudaError_t launch_tc_ffn(const TcLaunch& a, cudaStream_t st) {
         return cudaErrorInvalidValue;
     p2.ld_out_shared = a.d; p2.ld_out_routed = a.d;
 
-    e = allow_max_smem(ffn_tc_kernel<1>);
+    TcFusedParams fp;
+    fp.p1 = p1;
+    fp.p2 = p2;
+    fp.dep = a.dep;
+    e = allow_max_smem(ffn_tc_kernel);
     if (e != cudaSuccess) return e;
-    e = allow_max_smem(ffn_tc_kernel<2>);
-    if (e != cudaSuccess) return e;
-    e = note_launch(reinterpret_cast<const void*>(ffn_tc_kernel<1>), kTcThreads, kTcSmemBytes,
-                    launch_pdl(ffn_tc_kernel<1>, dim3(a.grid), dim3(kTcThreads), kTcSmemBytes, st, p1));
-    if (e != cudaSuccess) return e;
-    return note_launch(reinterpret_cast<const void*>(ffn_tc_kernel<2>), kTcThreads, kTcSmemBytes,
-                       launch_pdl(ffn_tc_kernel<2>, dim3(a.grid), dim3(kTcThreads), kTcSmemBytes, st, p2));
+    return note_launch(reinterpret_cast<const void*>(ffn_tc_kernel), kTcThreads, kTcSmemBytes,
+                       launch_pdl(ffn_tc_kernel, dim3(a.grid), dim3(kTcThreads), kTcSmemBytes, st, fp));
 }
 
 }  // namespace moe

@@ -149,12 +149,15 @@ struct TcLaunch {
     const void* x; const int32_t* perm; const int32_t* expert_offsets; const ExpertEntry* table;
     const TcPlan* plan; void* x_perm; void* h_routed; void* h_shared; float* y_perm; float* y_shared;
     int T, d, N, k, I, I_shared, n_shared, rows_cap, grid; DevError* err;
+    int* dep; int n_dep;  // per (segment, row tile) phase-dependency counters (workspace)
 };
-// tensor-core expert FFN: gather, phase 1 (gate/up + SwiGLU), phase 2 (down)
+// tensor-core expert FFN: gather, then one launch of phase 1 (gate/up + SwiGLU)
+// and phase 2 (down) tiles
 cudaError_t launch_tc_ffn(const TcLaunch& a, cudaStream_t st);
 // x_perm[pos] = x[perm[pos] / k] for the routed rows (bf16 rows of d values)
 cudaError_t launch_gather_rows(const void* x, const int32_t* perm, const int32_t* expert_offsets, int N,
-                               int k, int d, int rows_cap, void* x_perm, cudaStream_t st);
+                               int k, int d, int rows_cap, void* x_perm, cudaStream_t st, int* dep = nullptr,
+                               int n_dep = 0);
 
 struct TcdLaunch {
     const void* x; const int32_t* perm; const int32_t* expert_offsets; const ExpertEntry* table;

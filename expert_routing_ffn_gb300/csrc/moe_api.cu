@@ -476,11 +476,13 @@ moe_status expert_ffn_impl(const moe_dims* dims, const void* x, const void* tabl
         t.table = static_cast<const ExpertEntry*>(table); t.plan = ws_at<TcPlan>(ws, L.tc_plan);
         t.x_perm = ws_at<void>(ws, L.x_perm); t.h_routed = ws_at<void>(ws, L.h_routed);
         t.h_shared = ws_at<void>(ws, L.h_shared); t.y_perm = y_perm; t.y_shared = y_shared;
+        t.dep = ws_at<int>(ws, L.tc_dep);
+        t.n_dep = (int)((dims->T + dims->T * dims->k) / 128 + dims->N + 4);
         t.T = dims->T; t.d = dims->d; t.N = dims->N; t.k = dims->k; t.I = dims->I;
         t.I_shared = dims->I_shared; t.n_shared = dims->n_shared; t.rows_cap = dims->T * dims->k;
         t.grid = sm_count(); t.err = ws_at<DevError>(ws, L.err);
         MOE_CUDA(launch_tc_ffn(t, S(stream)));
-        count(3);
+        count(2);
         return MOE_OK;
     }
     if (!floe && tcd_usable(*dims)) {

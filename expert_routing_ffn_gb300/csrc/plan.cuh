@@ -144,13 +144,15 @@ __device__ __forceinline__ void build_tc_plan(const PlanArgs& a, const int* off)
         s.shared = 0; s.expert = tid; s.row0 = off[tid]; s.rows = rows; s.m_tiles = m; s.n1 = n1;
         s.tile1 = sh_m * sh_n1 + m_prev * n1;
         s.tile2 = sh_m * n2 + m_prev * n2;
+        s.mbase = sh_m + m_prev;
     }
     if (tid == 0) {
         if (sh) {
             TcSeg& s = P.seg[0];
             s.shared = 1; s.expert = a.N; s.row0 = 0; s.rows = a.T; s.m_tiles = sh_m; s.n1 = sh_n1;
-            s.tile1 = 0; s.tile2 = 0;
+            s.tile1 = 0; s.tile2 = 0; s.mbase = 0;
         }
+        P.n_mt = sh_m + (tot >> 8);
         P.n_seg = (sh ? 1 : 0) + (tot & 0xff);
         P.n_tiles1 = sh_m * sh_n1 + (tot >> 8) * n1;
         P.n_tiles2 = sh_m * n2 + (tot >> 8) * n2;
