@@ -944,7 +944,7 @@ def run_workload(args, wl_name, world, rank, dev, steps, warmup, with_cpu=True):
     """Measure one workload; returns its JSON line (a dict)."""
     import torch
     import expert_routing_ffn_gb300 as moe
-    from expert_routing_ffn_gb300.layer import DeviceLayer, LayerBuffers, forward
+    from expert_routing_ffn_gb300.layer import DeviceLayer, LayerBuffers, forward, forward_host
 
     cfg, T, phase = workload_cfg(wl_name)
     hbm_gbs, bf16_tflops, peak_src = peaks()
@@ -1218,20 +1218,30 @@ def run_workload(args, wl_name, world, rank, dev, steps, warmup, with_cpu=True):
                                   "note": "moe_cache_step back to back: layer on cache & landed, heat/cache "
                                           "update, admissions copied on a staging stream; host clock"}
         s0 = pipe.pipe.staged_bytes
+    plain = not la_cfg and not cache_cfg
+    if plain:
+        # moe_layer_forward_host: copy in, layer, copy out as one replayed
+        # graph per (layer copy, input buffer); captured here, before timing
+        for i in range(max(n_copies, n_x)):
+            forward_host(layers[i % n_copies], bufs[i % n_copies], xs[i % n_x], x_host[i % n_x],
+                         out_host[i % n_copies], stream=stream)
+        stream.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(n_e2e):
         c = 0 if cache_cfg else i % n_copies
         xc = xs[i % n_x]
+        if plain:
+            forward_host(layers[c], bufs[c], xc, x_host[i % n_x], out_host[c], stream=stream)
+            stream.synchronize()
+            continue
         xc.copy_(x_host[i % n_x], non_blocking=True)
         if la_cfg:
             forward(layers[c], bufs[c], xc, stream=stream)
             lookahead(c, xc)
-        elif cache_cfg:
-            pipe.step(bufs[0], xc, n_resident=0)
         else:
-            forward(layers[c], bufs[c], xc, stream=stream)
+            pipe.step(bufs[0], xc, n_resident=0)
         out_host[c].copy_(bufs[c].out, non_blocking=True)
         stream.synchronize()
     torch.cuda.synchronize()
@@ -1296,7 +1306,8 @@ def run_workload(args, wl_name, world, rank, dev, steps, warmup, with_cpu=True):
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": xs[0].numel() * xs[0].element_size(),
                 "d2h_bytes_per_step": bufs[0].out.numel() * 4, "steps": n_e2e,
-                "note": "moe_layer_forward per step with pinned-host copies and a stream sync, no graph"},
+                "note": "moe_layer_forward_host per step (pinned x in, layer, out to pinned memory, replayed "
+                        "as one CUDA graph by the library) and a stream sync"},
         "gpu_launches": int(launches_per_step * steps),
         "staging": staging,
         "routing": routing,

@@ -146,6 +146,8 @@ _PROTOS = {
     "moe_check": ([_P, _P, C.POINTER(C.c_int), C.POINTER(C.c_int32)], C.c_int),
     "moe_hetero_fetch_min_rows": ([C.POINTER(moe_hetero_cost)], C.c_int),
     "moe_set_graph_replay": ([C.c_int], None),
+    "moe_layer_forward_host": ([_DIMS, C.POINTER(moe_layer_args), C.POINTER(moe_layer_outputs), _P, _P, _P, _SZ, _P],
+                               C.c_int),
     "moe_cache_start": ([_DIMS, C.POINTER(moe_cache_pipe), _U64, _P], C.c_int),
     "moe_cache_step": ([_DIMS, C.POINTER(moe_layer_args), C.POINTER(moe_layer_outputs), C.POINTER(moe_cache_pipe),
                         _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P], C.c_int),

@@ -843,6 +843,8 @@ struct GraphEntry {
     moe_layer_outputs outs;
     void* ws;
     size_t ws_bytes;
+    const void* host_x;  // moe_layer_forward_host: the copies in and out are part of the graph
+    float* host_out;
     cudaGraphExec_t exec;
     int launches;
     uint64_t last_use;
@@ -855,10 +857,29 @@ uint64_t g_graph_clock = 0;
 std::atomic<int> g_graphs_enabled{1};
 
 bool same_call(const GraphEntry& g, int dev, const moe_dims* D, const moe_layer_args* A, const moe_layer_outputs* O,
-               void* ws, size_t ws_bytes) {
-    return g.device == dev && g.ws == ws && g.ws_bytes == ws_bytes && !std::memcmp(&g.dims, D, sizeof(moe_dims)) &&
+               void* ws, size_t ws_bytes, const void* host_x, const float* host_out) {
+    return g.device == dev && g.ws == ws && g.ws_bytes == ws_bytes && g.host_x == host_x &&
+           g.host_out == host_out && !std::memcmp(&g.dims, D, sizeof(moe_dims)) &&
            !std::memcmp(&g.args, A, sizeof(moe_layer_args)) && !std::memcmp(&g.outs, O, sizeof(moe_layer_outputs));
 }
+
+// The launch sequence, with the input copied in from host_x first and the
+// output copied out to host_out last when those are given.
+moe_status layer_forward_with_copies(const moe_dims* D, const moe_layer_args* A, const moe_layer_outputs* O,
+                                     void* ws, size_t ws_bytes, void* stream, const void* host_x, float* host_out) {
+    cudaStream_t s = S(stream);
+    const size_t x_bytes = (size_t)D->T * D->d * (D->wtype == MOE_DTYPE_BF16 ? 2 : 4);
+    if (host_x) MOE_CUDA(cudaMemcpyAsync(const_cast<void*>(A->x), host_x, x_bytes, cudaMemcpyHostToDevice, s));
+    MOE_TRY(layer_forward_launch(D, A, O, ws, ws_bytes, stream));
+    if (host_out)
+        MOE_CUDA(cudaMemcpyAsync(host_out, O->out, (size_t)D->T * D->d * sizeof(float), cudaMemcpyDeviceToHost, s));
+    return MOE_OK;
+}
+
+// Graph replay of one call (see moe_set_graph_replay); plain launches when
+// the stream is being captured, is the legacy default stream, or replay is off.
+moe_status forward_replayed(const moe_dims* dims, const moe_layer_args* A, const moe_layer_outputs* O, void* ws,
+                            size_t ws_bytes, void* stream, const void* host_x, float* host_out);
 
 }  // namespace
 
@@ -870,19 +891,36 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_layer_args* A, cons
                              size_t ws_bytes, void* stream) {
     MOE_TRY(check_dims(dims));
     if (!A || !O) return MOE_ERR_INVALID_ARG;
+    return forward_replayed(dims, A, O, ws, ws_bytes, stream, nullptr, nullptr);
+}
+
+moe_status moe_layer_forward_host(const moe_dims* dims, const moe_layer_args* A, const moe_layer_outputs* O,
+                                  const void* host_x, float* host_out, void* ws, size_t ws_bytes, void* stream) {
+    MOE_TRY(check_dims(dims));
+    if (!A || !O || !A->x || !O->out || (dims->T > 0 && (!host_x || !host_out))) return MOE_ERR_INVALID_ARG;
+    if (A->x_pre && A->x_pre != A->x) return MOE_ERR_INVALID_ARG;
+    return forward_replayed(dims, A, O, ws, ws_bytes, stream, host_x, host_out);
+}
+
+}  // extern "C"
+
+namespace {
+
+moe_status forward_replayed(const moe_dims* dims, const moe_layer_args* A, const moe_layer_outputs* O, void* ws,
+                            size_t ws_bytes, void* stream, const void* host_x, float* host_out) {
     cudaStream_t s = S(stream);
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     // inside the caller's own capture, or with replay off: plain launches
     if (dims->T == 0 || !g_graphs_enabled.load() || cudaStreamIsCapturing(s, &cap) != cudaSuccess ||
         cap != cudaStreamCaptureStatusNone || s == nullptr)
-        return layer_forward_launch(dims, A, O, ws, ws_bytes, stream);
+        return layer_forward_with_copies(dims, A, O, ws, ws_bytes, stream, host_x, host_out);
     int dev = 0;
     MOE_CUDA(cudaGetDevice(&dev));
     {
         std::lock_guard<std::mutex> lock(g_graph_mu);
         for (int i = 0; i < g_n_graphs; ++i) {
             GraphEntry& g = g_graphs[i];
-            if (!same_call(g, dev, dims, A, O, ws, ws_bytes)) continue;
+            if (!same_call(g, dev, dims, A, O, ws, ws_bytes, host_x, host_out)) continue;
             g.last_use = ++g_graph_clock;
             MOE_CUDA(cudaGraphLaunch(g.exec, s));
             count(g.launches);
@@ -893,7 +931,7 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_layer_args* A, cons
     if (!side_stream()) return MOE_ERR_CUDA;  // created outside the capture
     MOE_CUDA(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
     const uint64_t before = g_launches.load();
-    const moe_status st = layer_forward_launch(dims, A, O, ws, ws_bytes, stream);
+    const moe_status st = layer_forward_with_copies(dims, A, O, ws, ws_bytes, stream, host_x, host_out);
     const int launches = (int)(g_launches.load() - before);
     cudaGraph_t graph = nullptr;
     const cudaError_t e = cudaStreamEndCapture(s, &graph);
@@ -919,9 +957,14 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_layer_args* A, cons
     }
     GraphEntry& g = g_graphs[slot];
     g.device = dev; g.dims = *dims; g.args = *A; g.outs = *O; g.ws = ws; g.ws_bytes = ws_bytes;
+    g.host_x = host_x; g.host_out = host_out;
     g.exec = exec; g.launches = launches; g.last_use = ++g_graph_clock;
     return MOE_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 moe_status moe_layer_forward_hetero(const moe_dims* dims, const moe_layer_args* A, const moe_layer_outputs* O,
                                     const moe_hetero_cost* cost, const void* const* host_w_gate,

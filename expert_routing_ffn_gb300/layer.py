@@ -179,6 +179,33 @@ def forward(layer: DeviceLayer, bufs: LayerBuffers, x, stream=None, **kw):
     return bufs
 
 
+def forward_host(layer: DeviceLayer, bufs: LayerBuffers, x, host_x, host_out, stream=None, **kw):
+    """One layer forward with the input and the output in (pinned) host
+    memory, through moe_layer_forward_host: host_x [T, d] is copied into the
+    device buffer x, the layer runs, bufs.out is copied to host_out [T, d]
+    float32; all on `stream`, replayed as one CUDA graph per argument set.
+    Synchronise the stream before reading host_out."""
+    T = x.shape[0]
+    assert T <= bufs.T and x.is_contiguous() and x.dtype == layer.dt and x.is_cuda
+    assert not host_x.is_cuda and host_x.dtype == layer.dt and host_x.is_contiguous() and host_x.numel() >= x.numel()
+    assert not host_out.is_cuda and host_out.dtype == torch.float32 and host_out.numel() >= T * layer.cfg.d
+    cache = layer.__dict__.setdefault("_call_cache", {})
+    key = (T, x.data_ptr(), tuple(sorted(kw.items())), layer.ws.data_ptr())
+    hit = cache.get(key)
+    if hit is None:
+        if len(cache) > 64:
+            cache.clear()
+        hit = (layer.dims.with_T(T), layer_args(layer, x, **kw), C.c_void_p(layer.ws.data_ptr()),
+               layer.ws.numel())
+        cache[key] = hit
+    dims, args, ws_ptr, ws_bytes = hit
+    outs = bufs.outputs_struct()
+    _check(lib().moe_layer_forward_host(C.byref(dims), C.byref(args), C.byref(outs), C.c_void_p(host_x.data_ptr()),
+                                        C.c_void_p(host_out.data_ptr()), ws_ptr, ws_bytes, _stream(stream)),
+           "moe_layer_forward_host")
+    return bufs
+
+
 class HeteroHost:
     """Pinned host buffers and the host copy of the routed experts for the
     heterogeneous CPU-GPU path (moe_layer_forward_hetero), sized for T tokens.

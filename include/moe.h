@@ -521,6 +521,17 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_layer_args* args,
                              const moe_layer_outputs* outs, void* ws, size_t ws_bytes,
                              void* stream);
 
+/* moe_layer_forward with the input and the output in host memory: copies
+ * host_x ([T, d], the layer's type) into args->x, runs the layer, copies
+ * outs->out ([T, d] float32) to host_out, all queued on `stream` (pinned host
+ * buffers make the copies asynchronous; synchronise before reading
+ * host_out).  Replayed as one CUDA graph per argument set, like
+ * moe_layer_forward, the copies included.  args->x_pre must be NULL or x.
+ * Errors: those of moe_layer_forward, INVALID_ARG for missing buffers. */
+moe_status moe_layer_forward_host(const moe_dims* dims, const moe_layer_args* args,
+                                  const moe_layer_outputs* outs, const void* host_x, float* host_out,
+                                  void* ws, size_t ws_bytes, void* stream);
+
 /* moe_layer_forward replays CUDA graphs: the first call with a given set of
  * arguments (the bytes of dims, args and outs, the workspace and the device)
  * on a non-default stream that is not being captured captures the call's

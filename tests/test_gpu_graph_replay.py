@@ -84,3 +84,31 @@ def test_replay_on_another_stream_and_inside_a_caller_capture():
     torch.cuda.synchronize()
     assert torch.equal(ref, b.out)
     assert moe.moe_check(layer.ws)[0] == moe.MOE_OK
+
+
+@pytest.mark.parametrize("name,T", [("dsv2lite", 8), ("granite", 200)])
+def test_forward_with_host_buffers(name, T):
+    """moe_layer_forward_host copies the pinned input in and the output out
+    around the layer, replayed as one graph: new host inputs in the same
+    buffer give the new outputs, bitwise those of the device-buffer call."""
+    from expert_routing_ffn_gb300.layer import forward_host
+    cfg = CONFIGS[name]
+    W = make_weights(cfg)
+    layer = DeviceLayer(cfg, W, T)
+    stream = torch.cuda.Stream()
+    xd = torch.empty((T, cfg.d), dtype=layer.dt, device="cuda")
+    host_x = torch.empty((T, cfg.d), dtype=layer.dt).pin_memory()
+    host_out = torch.empty((T, cfg.d), dtype=torch.float32).pin_memory()
+    b = LayerBuffers(layer, T)
+    ref_b = LayerBuffers(layer, T)
+    for batch in (60, 61, 63):  # seeds without near-tie tokens (checked on the oracle)
+        x = make_tokens(cfg, T=T, batch=batch)
+        host_x.copy_(torch.from_numpy(x).to(layer.dt))
+        forward_host(layer, b, xd, host_x, host_out, stream=stream)
+        stream.synchronize()
+        forward(layer, ref_b, x_device(x, layer.dt), stream=stream)
+        stream.synchronize()
+        assert torch.equal(host_out, ref_b.out.cpu())
+    assert moe.moe_check(layer.ws)[0] == moe.MOE_OK
+    R = oracle.layer_forward(cfg, W, x)
+    check_output(cfg, R, host_out.cuda())
