@@ -115,6 +115,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prefill", action="store_true",
                    help="default workload only: skip the prefill half of the line")
+    p.add_argument("--clock-window", type=float, default=CLOCK_WINDOW_S,
+                   help="seconds of replays around the timed steps while clocks are sampled "
+                        "(0 for profiler runs: the timed steps alone)")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--plane-copies", type=int, default=0,
                    help="bit-sliced workloads: rotating copies of the planes (0: enough to defeat L2; "
@@ -606,7 +609,8 @@ def run_bitslice(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src, 
     for i in range(warmup):
         graphs[i % n_graphs].replay()
     torch.cuda.synchronize()
-    ms_total, clocks = timed_replays(lambda i: graphs[i % n_graphs].replay(), n_graphs, steps, stream, dev, world)
+    ms_total, clocks = timed_replays(lambda i: graphs[i % n_graphs].replay(), n_graphs, steps, stream, dev, world,
+                                     args.clock_window)
     ms_per_step = ms_total / steps
     value = whole_job_tokens_per_s(world, T, steps, ms_total)
 
@@ -1031,7 +1035,8 @@ def run_workload(args, wl_name, world, rank, dev, steps, warmup, with_cpu=True):
     torch.cuda.synchronize()
 
     # ---- timed region: exactly K steps (clocks sampled over a window around them)
-    ms_total, clocks = timed_replays(lambda i: graphs[i % n_graphs].replay(), n_graphs, steps, stream, dev, world)
+    ms_total, clocks = timed_replays(lambda i: graphs[i % n_graphs].replay(), n_graphs, steps, stream, dev, world,
+                                     args.clock_window)
     if cache_cfg:
         # the cache counters of the timed steps only: restart them and replay again
         cstats_t.zero_()
