@@ -782,7 +782,11 @@ def run_hetero(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src, st
         return res, el
 
     n_steps = max(20, min(steps, 400))
-    main_res, el = timed(measured, n_steps)
+    barrier(world)
+    with ClockSampler(dev.index or 0) as clk:
+        main_res, el = timed(measured, n_steps)
+    clocks = clk.summary()
+    barrier(world)
     pcie_res, _ = timed(pcie, n_steps)
     # the LoRE/substitute-only policy, eager and synchronised the same way
     for i in range(3):
@@ -831,6 +835,7 @@ def run_hetero(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src, st
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": xs[0].numel() * 2,
                 "d2h_bytes_per_step": bufs.out.numel() * 4, "steps": n_steps,
                 "note": "moe_layer_forward_hetero per step with pinned-host copies of x and out"},
+        "clocks": clocks,
         "gpu_launches": None,
     }
     n0 = moe.moe_launch_total()
@@ -867,11 +872,15 @@ def run_cache_exact(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_sr
     p = pipe.pipe
     base = (p.staged_experts, p.staged_bytes, p.in_time_experts, p.stall_experts, p.stall_steps)
     hits = slots = 0
-    t0 = time.perf_counter()
-    for i in range(n):
-        pipe.step(bufs, xs[i % n_x], policy=moe.MOE_MISS_EXACT, n_resident=0)
-    stream.synchronize()
-    el = time.perf_counter() - t0
+    barrier(world)
+    with ClockSampler(dev.index or 0) as clk:
+        t0 = time.perf_counter()
+        for i in range(n):
+            pipe.step(bufs, xs[i % n_x], policy=moe.MOE_MISS_EXACT, n_resident=0)
+        stream.synchronize()
+        el = time.perf_counter() - t0
+    clocks = clk.summary()
+    barrier(world)
     d = [a - b for a, b in zip((p.staged_experts, p.staged_bytes, p.in_time_experts, p.stall_experts,
                                 p.stall_steps), base)]
     st = pipe.stats.cpu().numpy()  # hits / slots since start (includes warm-up)
@@ -932,6 +941,7 @@ def run_cache_exact(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_sr
         "e2e": {"value": world * T * n / max_over_ranks(world, e2e_s), "unit": "tokens/s",
                 "h2d_bytes_per_step": xs[0].numel() * 2 + d[1] / n, "d2h_bytes_per_step": bufs.out.numel() * 4 + 40,
                 "steps": n, "note": "moe_cache_step per step with pinned-host copies of x and out"},
+        "clocks": clocks,
         "gpu_launches": None,
     }
     n0 = moe.moe_launch_total()
