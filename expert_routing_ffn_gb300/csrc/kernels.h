@@ -178,6 +178,7 @@ struct LoreArgs {
     // batches of more than kTcMinTokens tokens: the LoRE slots grouped by
     // expert (workspace), and the per-slot B_e z rows
     int32_t *g_off, *g_list, *g_pos, *g_counts; float *zp, *v;
+    bool skip_sum;  // grouped path: leave y_lore unwritten (launch_prefill_epilogue sums the v rows)
 };
 cudaError_t launch_lore(const LoreArgs& a, cudaStream_t st);
 // whether launch_lore takes the grouped path (given the workspace buffers)
@@ -196,6 +197,19 @@ struct EpilogueArgs {
 };
 // partial-row reduction + LoRE B + combine in one launch (moe_layer_forward)
 cudaError_t launch_layer_epilogue(const EpilogueArgs& a, cudaStream_t st);
+
+struct PrefillEpilogueArgs {
+    const float *y_perm, *y_shared;  // y_shared NULL: no shared experts
+    const int32_t *inv_perm, *final_idx, *final_kind; const float* final_gate;
+    // LoRE (lore_v NULL: none): the B_e z rows of the grouped slots (lore_v
+    // [pos, d], slot -> pos in g_pos, -1 for the other slots)
+    const float* lore_v; const int32_t* g_pos;
+    int T, d, k;
+    float* out;
+};
+// the tensor-core prefill path's tail of moe_layer_forward: the per-token
+// LoRE sum and the combine in one launch
+cudaError_t launch_prefill_epilogue(const PrefillEpilogueArgs& a, cudaStream_t st);
 
 // test probe: a bounded wait on an mbarrier nothing arrives on (records
 // MOE_ERR_TIMEOUT in err)

@@ -421,6 +421,58 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     }
 }
 
+// moe_layer_forward's tail on the tensor-core prefill path: combine_kernel
+// with the LoRE term summed here from the slots' B_e z rows (v, grouped
+// positions) instead of a y_lore row written by a separate launch.  The
+// operations are those of lore_sum_kernel then combine_kernel, element by
+// element, so the result is bitwise that of the stage-wise calls.
+__global__ void __launch_bounds__(256) prefill_epilogue_kernel(const PrefillEpilogueArgs a) {
+    grid_dep_wait();  // the FFN's y rows and the LoRE rows (dependent launch)
+    const int t = blockIdx.x;
+    const int q = blockIdx.y * blockDim.x + threadIdx.x;  // float4 column group
+    const int k = a.k, d = a.d;
+    __shared__ int s_pos[kMaxTopK], s_lp[kMaxTopK], s_kind[kMaxTopK];
+    __shared__ float s_g[kMaxTopK];
+    __shared__ float s_lg;
+    if (threadIdx.x < k) {  // one thread per slot
+        const size_t sl = (size_t)t * k + threadIdx.x;
+        s_pos[threadIdx.x] = a.inv_perm[sl];
+        s_g[threadIdx.x] = a.final_gate[sl];
+        s_kind[threadIdx.x] = a.final_kind[sl];
+        s_lp[threadIdx.x] = a.lore_v ? a.g_pos[sl] : -1;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {  // the LoRE gates summed in slot order
+        float lg = 0.f;
+        for (int s = 0; s < k; ++s)
+            if (s_kind[s] == MOE_KIND_LORE) lg += s_g[s];
+        s_lg = lg;
+    }
+    __syncthreads();
+    if (q >= d / 4) return;
+    const float sh_scale = 1.f + s_lg;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (a.y_shared) {
+        const float4 v = reinterpret_cast<const float4*>(a.y_shared + (size_t)t * d)[q];
+        acc.x = v.x * sh_scale; acc.y = v.y * sh_scale; acc.z = v.z * sh_scale; acc.w = v.w * sh_scale;
+    }
+    for (int s = 0; s < k; ++s) {
+        const int pos = s_pos[s];
+        if (pos < 0) continue;
+        const float g = s_g[s];
+        const float4 v = reinterpret_cast<const float4*>(a.y_perm + (size_t)pos * d)[q];
+        acc.x = fmaf(g, v.x, acc.x); acc.y = fmaf(g, v.y, acc.y);
+        acc.z = fmaf(g, v.z, acc.z); acc.w = fmaf(g, v.w, acc.w);
+    }
+    if (a.lore_v) {
+        float4 yl = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s = 0; s < k; ++s)
+            if (s_lp[s] >= 0) add4(yl, reinterpret_cast<const float4*>(a.lore_v + (size_t)s_lp[s] * d)[q]);
+        acc.x += yl.x; acc.y += yl.y; acc.z += yl.z; acc.w += yl.w;
+    }
+    reinterpret_cast<float4*>(a.out + (size_t)t * d)[q] = acc;
+}
+
 // moe_layer_forward's tail when the expert FFN left per-CTA partial rows
 // (GEMV and decode tensor-core paths).  Block = token t x 128 columns of d
 // (lane = 4 columns).  A "unit" is one segment row feeding the token: the
@@ -687,7 +739,7 @@ static cudaError_t launch_lore_grouped(const LoreArgs& a, cudaStream_t st) {
     const int gx = tiles < 304 ? tiles : 304;
     e = launch_pdl(lore_b_grouped_kernel<W>, dim3(gx, kLoreBY), dim3(256), 0, st, (const W*)a.B,
                    (const int32_t*)a.g_off, a.d, a.r, a.N, (const float*)a.z, a.v);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess || a.skip_sum) return e;
     return launch_pdl(lore_sum_kernel, dim3(a.T, (a.d / 4 + 255) / 256), dim3(256), 0, st, (const int32_t*)a.g_pos,
                       (const float*)a.v, a.d, a.k, a.y_lore);
 }
@@ -719,6 +771,11 @@ cudaError_t launch_lore(const LoreArgs& a, cudaStream_t st) {
                                                  a.k, a.r, a.N, a.z, a.y_lore);
     }
     return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_epilogue(const PrefillEpilogueArgs& a, cudaStream_t st) {
+    if (a.T == 0) return cudaSuccess;
+    return launch_pdl(prefill_epilogue_kernel, dim3(a.T, (a.d / 4 + 255) / 256), dim3(256), 0, st, a);
 }
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {

@@ -585,9 +585,13 @@ moe_status moe_floe_kept_mask(const moe_dims* dims, void* ws, size_t ws_bytes, c
     return MOE_OK;
 }
 
-moe_status moe_lore(const moe_dims* dims, const void* x, const int32_t* final_idx,
-                    const int32_t* final_kind, const float* final_gate, const void* lore_a,
-                    const void* lore_b, float* y_lore, void* ws, size_t ws_bytes, void* stream) {
+namespace {
+
+// moe_lore; skip_sum: on the grouped path leave y_lore unwritten (the
+// prefill epilogue sums the slots' v rows itself).
+moe_status lore_impl(const moe_dims* dims, const void* x, const int32_t* final_idx, const int32_t* final_kind,
+                     const float* final_gate, const void* lore_a, const void* lore_b, float* y_lore, void* ws,
+                     size_t ws_bytes, void* stream, bool skip_sum) {
     MOE_TRY(check_dims(dims));
     if (dims->r <= 0) return MOE_ERR_INVALID_ARG;
     MOE_TRY(check_ws(dims, ws, ws_bytes));
@@ -607,9 +611,20 @@ moe_status moe_lore(const moe_dims* dims, const void* x, const int32_t* final_id
     a.g_pos = ws_at<int32_t>(ws, L.lore_pos); a.g_counts = ws_at<int32_t>(ws, L.lore_counts);
     a.zp = ws_at<float>(ws, L.lore_zp);
     a.v = grouped ? ws_at<float>(ws, L.lore_v) : nullptr;
+    a.skip_sum = grouped && skip_sum;
     MOE_CUDA(launch_lore(a, S(stream)));
-    count(grouped ? 5 : 2);
+    // grouped: slot grouping (2 launches), z, z sum, B z and (unless skipped) the per-token sum
+    count(grouped ? (a.skip_sum ? 5 : 6) : 2);
     return MOE_OK;
+}
+
+}  // namespace
+
+moe_status moe_lore(const moe_dims* dims, const void* x, const int32_t* final_idx,
+                    const int32_t* final_kind, const float* final_gate, const void* lore_a,
+                    const void* lore_b, float* y_lore, void* ws, size_t ws_bytes, void* stream) {
+    return lore_impl(dims, x, final_idx, final_kind, final_gate, lore_a, lore_b, y_lore, ws, ws_bytes, stream,
+                     false);
 }
 
 moe_status moe_cache_update(const moe_dims* dims, const int32_t* topk_idx, float decay, int capacity,
@@ -790,6 +805,7 @@ moe_status layer_forward_launch(const moe_dims* dims, const moe_layer_args* A, c
             la.final_gate = O->final_gate; la.A = A->lore_a; la.B = A->lore_b; la.T = dims->T; la.d = dims->d;
             la.k = dims->k; la.r = dims->r; la.N = dims->N; la.bf16 = bf16(dims);
             la.z = ws_at<float>(ws, L.lore_z); la.y_lore = O->y_lore; la.err = ws_at<DevError>(ws, L.err);
+            la.skip_sum = false;
             SideStream* sd = side_stream();
             if (!sd) return MOE_ERR_CUDA;
             std::lock_guard<std::mutex> lock(sd->mu);
@@ -818,6 +834,28 @@ moe_status layer_forward_launch(const moe_dims* dims, const moe_layer_args* A, c
         if (!ea.out || !ea.y_perm || !O->inv_perm || (dims->n_shared > 0 && !ea.y_shared))
             return MOE_ERR_INVALID_ARG;
         MOE_CUDA(launch_layer_epilogue(ea, S(stream)));
+        count();
+        return MOE_OK;
+    }
+    if (dims->T > 0 && (!lore || lore_grouped_usable(dims->T, dims->d, dims->r, bf16(dims)))) {
+        // tensor-core prefill: the expert FFN, LoRE grouped by expert (its
+        // B_e z rows), then one launch for their per-token sum and the combine
+        if (!O->out || !O->inv_perm || !O->final_gate || !O->final_kind || !O->y_perm ||
+            (dims->n_shared > 0 && !O->y_shared))
+            return MOE_ERR_INVALID_ARG;
+        MOE_TRY(moe_expert_ffn(dims, A->x, A->table, O->expert_offsets, O->perm, A->keep_frac, O->y_perm,
+                               O->y_shared, ws, ws_bytes, stream));
+        if (lore)
+            MOE_TRY(lore_impl(dims, A->x, O->final_idx, O->final_kind, O->final_gate, A->lore_a, A->lore_b,
+                              O->y_lore, ws, ws_bytes, stream, true));
+        const WsLayout L = ws_layout(*dims);
+        PrefillEpilogueArgs pe;
+        pe.y_perm = O->y_perm; pe.y_shared = dims->n_shared > 0 ? O->y_shared : nullptr;
+        pe.inv_perm = O->inv_perm; pe.final_idx = O->final_idx; pe.final_kind = O->final_kind;
+        pe.final_gate = O->final_gate;
+        pe.lore_v = lore ? ws_at<float>(ws, L.lore_v) : nullptr; pe.g_pos = ws_at<int32_t>(ws, L.lore_pos);
+        pe.T = dims->T; pe.d = dims->d; pe.k = dims->k; pe.out = O->out;
+        MOE_CUDA(launch_prefill_epilogue(pe, S(stream)));
         count();
         return MOE_OK;
     }
