@@ -58,6 +58,7 @@ WORKLOADS = {
     "mixtral-floe10-decode-T1": ("mixtral", 1, "decode", 0.1),
     "mixtral-floe10-decode-T8": ("mixtral", 8, "decode", 0.1),
     "qwen2-prefill-T4096": ("qwen2", 4096, "prefill"),
+    "dsv2lite-prefill-T4096": ("dsv2lite", 4096, "prefill"),
     "dsv2lite-cache-decode-T1": ("dsv2lite", 1, "decode"),
     "dsv2lite-lookahead-decode-T8": ("dsv2lite", 8, "decode"),
     "dsv2lite-bitslice4-draft-T1": ("dsv2lite", 1, "decode"),
