@@ -162,6 +162,7 @@ _PROTOS = {
                                   _I, _P, _SZ, _P, _P, _P, C.POINTER(moe_hetero_stats)], C.c_int),
     "moe_testing_fail_copies_after": ([C.c_int], None),
     "moe_testing_wait_timeout": ([C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
+    "moe_testing_set_tc_pairs": ([C.c_int], None),
 }
 
 
@@ -627,6 +628,11 @@ def moe_check(ws, stream=None):
 
 def moe_testing_fail_copies_after(n: int):
     lib().moe_testing_fail_copies_after(int(n))
+
+
+def moe_testing_set_tc_pairs(mode: int):
+    """-1: the prefill FFN chooses single CTAs or CTA pairs; 0 / 1: force."""
+    lib().moe_testing_set_tc_pairs(int(mode))
 
 
 def moe_testing_wait_timeout(ws, stream=None):

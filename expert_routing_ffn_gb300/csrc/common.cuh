@@ -213,11 +213,15 @@ __device__ __forceinline__ float4 unit_table_sum(const UnitTable& U, int u, cons
 struct TcSeg {
     int shared, expert, row0, rows, m_tiles, n1, tile1, tile2;
     int mbase;  // index of this segment's first (segment, row tile) dependency counter
+    // the same tiles at CTA-pair granularity (256-row tiles of a 2-CTA MMA):
+    // m_pairs = ceil(rows / 256), first phase-1 / phase-2 pair tile
+    int m_pairs, tile1p, tile2p;
 };
 struct TcPlan {
     int n_seg, n_tiles1, n_tiles2;
     int n_mt;  // (segment, row tile) pairs: the dependency counters in use
-    int pad[12];
+    int n_tiles1p, n_tiles2p;  // pair tiles of the two phases
+    int pad[10];
     TcSeg seg[kMaxExperts + 1];
 };
 

@@ -30,7 +30,9 @@
 // leave their loops.
 #include <cuda.h>
 
+#include <atomic>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -39,12 +41,20 @@
 
 namespace moe {
 
-constexpr int kTcBM = 128, kTcBN = 256, kTcStages = 4, kTcThreads = 192;
+constexpr int kTcBM = 128, kTcBN = 256, kTcThreads = 192;
 constexpr uint32_t kTcStageA = kTcBM * kTcBK * 2;  // 16 KB
-constexpr uint32_t kTcStageB = kTcBN * kTcBK * 2;  // 32 KB
-constexpr uint32_t kTcStageBytes = kTcStageA + kTcStageB;
 constexpr uint32_t kTcOutBox = 32 * 128;  // one epilogue warp's staging box: 32 rows x 128 bytes
-constexpr uint32_t kTcSmemBytes = kTcStages * kTcStageBytes + 4 * kTcOutBox + 1024;  // + alignment slack
+// One CTA per tile: a stage holds A (128 rows) and all of B (256 rows), 4 stages.
+// A CTA pair per tile (2-CTA MMA, M = 256): each CTA's stage holds its 128 A
+// rows and its half of B, so 6 stages fit in the same shared memory and
+// cover 1.5x the load latency at the same MMA rate.
+template <bool PAIR>
+struct TcCfg {
+    static constexpr int kStages = PAIR ? 6 : 4;
+    static constexpr uint32_t kStageB = (PAIR ? kTcBN / 2 : kTcBN) * kTcBK * 2;  // 16 / 32 KB
+    static constexpr uint32_t kStageBytes = kTcStageA + kStageB;
+    static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 4 * kTcOutBox + 1024;  // + alignment slack
+};
 
 struct TcParams {
     CUtensorMap map_a_shared;  // phase 1: x [T, d];         phase 2: h_shared [T, ns*Is]
@@ -65,25 +75,113 @@ struct TcTile {
     int seg, mt, nt;
 };
 
-// Tile t of phase `phase` (t counted within the phase).
+// Tile t of phase `phase` (t counted within the phase); PAIR: 256-row tiles
+// (mt counts row pairs).
+template <bool PAIR>
 __device__ __forceinline__ void tc_tile(const TcPlan& P, int phase, int t, TcTile& out) {
+    auto first = [&](const TcSeg& S) {
+        return PAIR ? (phase == 1 ? S.tile1p : S.tile2p) : (phase == 1 ? S.tile1 : S.tile2);
+    };
     int s = 0;
-    while (s + 1 < P.n_seg && (phase == 1 ? P.seg[s + 1].tile1 : P.seg[s + 1].tile2) <= t) ++s;
+    while (s + 1 < P.n_seg && first(P.seg[s + 1]) <= t) ++s;
     const TcSeg& S = P.seg[s];
-    const int local = t - (phase == 1 ? S.tile1 : S.tile2);
+    const int local = t - first(S);
+    const int m = PAIR ? S.m_pairs : S.m_tiles;
     out.seg = s;
-    out.mt = local % S.m_tiles;
-    out.nt = local / S.m_tiles;
+    out.mt = local % m;
+    out.nt = local / m;
 }
 
-// Global tile g: phase 1 below n_tiles1, phase 2 after.
+// Global tile g: phase 1 below the phase-1 tile count, phase 2 after.
+template <bool PAIR>
 __device__ __forceinline__ int tc_tile_global(const TcPlan& P, int g, TcTile& out) {
-    if (g < P.n_tiles1) {
-        tc_tile(P, 1, g, out);
+    const int n1 = PAIR ? P.n_tiles1p : P.n_tiles1;
+    if (g < n1) {
+        tc_tile<PAIR>(P, 1, g, out);
         return 1;
     }
-    tc_tile(P, 2, g - P.n_tiles1, out);
+    tc_tile<PAIR>(P, 2, g - n1, out);
     return 2;
+}
+
+// ---------------------------------------------------------------- CTA pairs
+// The 2-CTA forms.  The even CTA of a cluster pair (the leader) issues the
+// MMAs, which read both CTAs' shared memory at the same offsets and write
+// each CTA's 128 accumulator rows into its own tensor memory; both CTAs'
+// stage loads complete on the leader's full barrier; the leader's commits
+// arrive on the barrier at the same offset in both CTAs.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// the shared::cluster address of `bar` in CTA `rank` of this cluster
+__device__ __forceinline__ uint32_t mapa_rank(const void* bar, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(bar)), "r"(rank));
+    return a;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// tile load into this CTA's shared memory, completing on the leader's barrier
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, int c0, int c1, uint32_t bar_cl) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(tmap), "r"(c0), "r"(c1), "r"(bar_cl) : "memory");
+}
+__device__ __forceinline__ void tc_mma_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// arrive on `bar` in both CTAs of the pair when the MMAs issued so far are done
+__device__ __forceinline__ void tc_commit_pair(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        ::"r"(smem_u32(bar)), "h"((uint16_t)3) : "memory");
+}
+// the same, on the leader's barrier only
+__device__ __forceinline__ void tc_commit_pair_local(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cl) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cl) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+// tc_wait with cluster-scope acquire (barriers that the peer CTA signals)
+__device__ __forceinline__ bool tc_wait_cl(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                           DevError* err, int where, bool honor_abort = true) {
+    const long long t0 = clock64();
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((i & 63) == 63) {
+            if (honor_abort && *abort_flag) return false;
+            if (clock64() - t0 > kTcWaitCycles) {
+                set_error(err, MOE_ERR_TIMEOUT, where);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+template <bool PAIR>
+__device__ __forceinline__ bool tcw(uint64_t* bar, uint32_t parity, volatile int* abort_flag, DevError* err,
+                                    int where, bool honor_abort = true) {
+    return PAIR ? tc_wait_cl(bar, parity, abort_flag, err, where, honor_abort)
+                : tc_wait(bar, parity, abort_flag, err, where, honor_abort);
 }
 
 // ---------------------------------------------------------------- phase dependency
@@ -162,10 +260,13 @@ struct TcFusedParams {
     int* dep;         // per (segment, row tile): phase-1 epilogue warps done (zeroed by the gather)
 };
 
+template <bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_constant__ TcFusedParams fp) {
+    using C = TcCfg<PAIR>;
+    constexpr int kS = C::kStages;
     grid_dep_wait();  // the plan, x_perm, the zeroed counters: no tensor memory taken before it
     extern __shared__ unsigned char tc_smem_raw[];
-    __shared__ __align__(8) uint64_t full[kTcStages], empty[kTcStages], tfull[2], tempty[2], drain;
+    __shared__ __align__(8) uint64_t full[kS], empty[kS], tfull[2], tempty[2], drain;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
     __shared__ TcPlan plan_s;
@@ -174,59 +275,82 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t smem_base = (smem_u32(tc_smem_raw) + 1023u) & ~1023u;
     volatile int* abort_flag = &abort_s;
+    // PAIR: the cluster is a CTA pair; rank 0 (the leader) issues the MMAs
+    const uint32_t rank = PAIR ? cluster_rank() : 0;
+    const bool leader = rank == 0;
+    const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;  // tile stream of this CTA / pair
+    const int n_units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    const int pair_rows = PAIR ? 2 * kTcBM : kTcBM;  // rows of a tile
+    const int row_off = (int)rank * kTcBM;           // this CTA's rows within the tile
+    constexpr int kEpiWarps = PAIR ? 8 : 4;          // epilogue warps per tile (both CTAs)
 
     for (int i = tid; i < (int)(sizeof(TcPlan) / 4); i += blockDim.x)
         reinterpret_cast<int*>(&plan_s)[i] = reinterpret_cast<const int*>(p.plan)[i];
     if (tid == 0) {
-        for (int s = 0; s < kTcStages; ++s) {
+        for (int s = 0; s < kS; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 4);  // one arrival per epilogue warp
+            mbar_init(&tempty[b], kEpiWarps);  // one arrival per epilogue warp (of both CTAs)
         }
         mbar_init(&drain, 1);
         fence_mbar_init();
         abort_s = 0;
     }
     if (warp == 1) {  // tensor memory: 512 columns = two 128x256 fp32 accumulators
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;"
-                     ::"r"(smem_u32(&tmem_base_s)));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        if constexpr (PAIR) {
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], 512;"
+                         ::"r"(smem_u32(&tmem_base_s)));
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;"
+                         ::"r"(smem_u32(&tmem_base_s)));
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // the peer's barriers are initialised before any remote arrival
     tc_fence_after();
     const uint32_t tmem_base = tmem_base_s;
     const TcPlan& P = plan_s;
     const int d = p.d;
-    const int n_tiles = P.n_tiles1 + P.n_tiles2;
+    const int n_tiles = PAIR ? P.n_tiles1p + P.n_tiles2p : P.n_tiles1 + P.n_tiles2;
 
     if (warp == 0) {
-        // ---------------- TMA producer
+        // ---------------- TMA producer (each CTA loads its own stages)
         if (lane == 0) {
             int it = 0;
             TcTile tl;
-            for (int g = blockIdx.x; g < n_tiles && !*abort_flag; g += gridDim.x) {
-                const int phase = tc_tile_global(P, g, tl);
+            for (int g = unit; g < n_tiles && !*abort_flag; g += n_units) {
+                const int phase = tc_tile_global<PAIR>(P, g, tl);
                 const TcSeg& S = P.seg[tl.seg];
                 const TcParams& q = phase == 1 ? fp.p1 : fp.p2;
                 if (phase == 2 &&
-                    !dep_wait(fp.dep + S.mbase + tl.mt, 4 * S.n1, abort_flag, p.err))
+                    !dep_wait(fp.dep + S.mbase + tl.mt, kEpiWarps * S.n1, abort_flag, p.err))
                     break;
                 const CUtensorMap* amap = S.shared ? &q.map_a_shared : &q.map_a_routed;
-                const int arow = S.row0 + tl.mt * kTcBM;
+                const int arow = S.row0 + tl.mt * pair_rows + row_off;
                 const int nk = phase == 1 ? d / (int)kTcBK
                                           : (S.shared ? p.n_shared * p.I_shared : p.I) / (int)kTcBK;
                 for (int kb = 0; kb < nk; ++kb, ++it) {
-                    const int st = it % kTcStages;
-                    const uint32_t par = ((it / kTcStages) & 1) ^ 1;
-                    if (!tc_wait(&empty[st], par, abort_flag, p.err, 1)) break;
-                    const uint32_t a_dst = smem_base + st * kTcStageBytes;
+                    const int st = it % kS;
+                    const uint32_t par = ((it / kS) & 1) ^ 1;
+                    if (!tcw<PAIR>(&empty[st], par, abort_flag, p.err, 1)) break;
+                    const uint32_t a_dst = smem_base + st * C::kStageBytes;
                     const uint32_t b_dst = a_dst + kTcStageA;
-                    mbar_arrive_expect_tx(&full[st], kTcStageBytes);
-                    tma_load_2d(a_dst, amap, kb * kTcBK, arow, &full[st]);
+                    // the stage's loads complete on the leader's full barrier, which
+                    // expects the bytes of both CTAs
+                    uint32_t bar = smem_u32(&full[st]);
+                    if constexpr (PAIR) bar = mapa_rank(&full[st], 0);
+                    if (leader) mbar_arrive_expect_tx(&full[st], (PAIR ? 2 : 1) * C::kStageBytes);
+                    auto load = [&](uint32_t dst, const void* tmap, int c0, int c1) {
+                        if constexpr (PAIR) tma_load_2d_pair(dst, tmap, c0, c1, bar);
+                        else tma_load_2d(dst, tmap, c0, c1, &full[st]);
+                    };
+                    load(a_dst, amap, kb * kTcBK, arow);
                     if (phase == 1) {
                         int e, nrow;
                         if (S.shared) {
@@ -238,8 +362,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                             nrow = tl.nt * 128;
                         }
                         const ExpertEntry* E = p.table + e;
-                        tma_load_2d(b_dst, E->tmap[0], kb * kTcBK, nrow, &full[st]);
-                        tma_load_2d(b_dst + kTcStageB / 2, E->tmap[1], kb * kTcBK, nrow, &full[st]);
+                        // B = [gate rows; up rows] (N = 256); a pair splits it by N:
+                        // the leader holds the gate rows, the peer the up rows
+                        if (!PAIR || leader) load(b_dst, E->tmap[0], kb * kTcBK, nrow);
+                        if (!PAIR) load(b_dst + C::kStageB / 2, E->tmap[1], kb * kTcBK, nrow);
+                        else if (!leader) load(b_dst, E->tmap[1], kb * kTcBK, nrow);
                     } else {
                         int e, krow;
                         if (S.shared) {
@@ -251,60 +378,78 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                             krow = kb * kTcBK;
                         }
                         const ExpertEntry* E = p.table + e;
+                        // B = 256 columns of Wd in 64-column boxes; a pair splits it by N
+                        constexpr int kBoxes = (PAIR ? kTcBN / 2 : kTcBN) / 64;
+                        const int col0 = tl.nt * kTcBN + (int)rank * (kTcBN / 2) * (PAIR ? 1 : 0);
 #pragma unroll
-                        for (int j = 0; j < kTcBN / 64; ++j)
-                            tma_load_2d(b_dst + j * (64 * kTcBK * 2), E->tmap[2], tl.nt * kTcBN + j * 64,
-                                        krow, &full[st]);
+                        for (int j = 0; j < kBoxes; ++j)
+                            load(b_dst + j * (64 * kTcBK * 2), E->tmap[2], col0 + j * 64, krow);
                     }
                 }
             }
-            // wait for the last loads in flight before the block may exit
-            for (int k = (it > kTcStages ? it - kTcStages : 0); k < it; ++k)
-                (void)tc_wait(&full[k % kTcStages], (k / kTcStages) & 1, abort_flag, p.err, 2, false);
+            if constexpr (PAIR) {
+                // this CTA's last stages have been consumed by the leader's MMAs
+                // (so their loads have landed) before the block may exit
+                for (int k = (it > kS ? it - kS : 0); k < it; ++k)
+                    (void)tc_wait_cl(&empty[k % kS], (k / kS) & 1, abort_flag, p.err, 2, false);
+            } else {
+                // wait for the last loads in flight before the block may exit
+                for (int k = (it > kS ? it - kS : 0); k < it; ++k)
+                    (void)tc_wait(&full[k % kS], (k / kS) & 1, abort_flag, p.err, 2, false);
+            }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc1 = tc_idesc(kTcBM, kTcBN, 0);
-            constexpr uint32_t idesc2 = tc_idesc(kTcBM, kTcBN, 1);
+        // ---------------- MMA issuer (the leader of a pair)
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc1 = tc_idesc(PAIR ? 2 * kTcBM : kTcBM, kTcBN, 0);
+            constexpr uint32_t idesc2 = tc_idesc(PAIR ? 2 * kTcBM : kTcBM, kTcBN, 1);
             int it = 0, local = 0;
             TcTile tl;
-            for (int g = blockIdx.x; g < n_tiles && !*abort_flag; g += gridDim.x, ++local) {
-                const int phase = tc_tile_global(P, g, tl);
+            auto mma = [&](uint32_t dt, uint64_t ad, uint64_t bd, uint32_t id, uint32_t acc) {
+                if constexpr (PAIR) tc_mma_pair(dt, ad, bd, id, acc);
+                else tc_mma(dt, ad, bd, id, acc);
+            };
+            auto commit = [&](uint64_t* bar) {
+                if constexpr (PAIR) tc_commit_pair(bar);
+                else tc_commit(bar);
+            };
+            for (int g = unit; g < n_tiles && !*abort_flag; g += n_units, ++local) {
+                const int phase = tc_tile_global<PAIR>(P, g, tl);
                 const TcSeg& S = P.seg[tl.seg];
                 const int ab = local & 1;
-                if (!tc_wait(&tempty[ab], ((local >> 1) & 1) ^ 1, abort_flag, p.err, 3)) break;
+                if (!tcw<PAIR>(&tempty[ab], ((local >> 1) & 1) ^ 1, abort_flag, p.err, 3)) break;
                 tc_fence_after();
                 const uint32_t tmem_d = tmem_base + ab * kTcBN;
                 const int nk = phase == 1 ? d / (int)kTcBK
                                           : (S.shared ? p.n_shared * p.I_shared : p.I) / (int)kTcBK;
                 bool ok = true;
                 for (int kb = 0; kb < nk; ++kb, ++it) {
-                    const int st = it % kTcStages;
-                    if (!tc_wait(&full[st], (it / kTcStages) & 1, abort_flag, p.err, 4)) { ok = false; break; }
+                    const int st = it % kS;
+                    if (!tcw<PAIR>(&full[st], (it / kS) & 1, abort_flag, p.err, 4)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_base + st * kTcStageBytes;
+                    const uint32_t a_addr = smem_base + st * C::kStageBytes;
                     const uint32_t b_addr = a_addr + kTcStageA;
                     if (phase == 1) {
 #pragma unroll
                         for (int kk = 0; kk < (int)kTcBK / 16; ++kk)
-                            tc_mma(tmem_d, smem_desc(a_addr + kk * 32, 16, 1024), smem_desc(b_addr + kk * 32, 16, 1024),
-                                   idesc1, (kb | kk) ? 1u : 0u);
+                            mma(tmem_d, smem_desc(a_addr + kk * 32, 16, 1024), smem_desc(b_addr + kk * 32, 16, 1024),
+                                idesc1, (kb | kk) ? 1u : 0u);
                     } else {
 #pragma unroll
                         for (int kk = 0; kk < (int)kTcBK / 16; ++kk)
-                            tc_mma(tmem_d, smem_desc(a_addr + kk * 32, 16, 1024),
-                                   smem_desc(b_addr + kk * 16 * 128, 64 * kTcBK * 2, 1024), idesc2,
-                                   (kb | kk) ? 1u : 0u);
+                            mma(tmem_d, smem_desc(a_addr + kk * 32, 16, 1024),
+                                smem_desc(b_addr + kk * 16 * 128, 64 * kTcBK * 2, 1024), idesc2,
+                                (kb | kk) ? 1u : 0u);
                     }
-                    tc_commit(&empty[st]);  // frees the stage when these MMAs are done
+                    commit(&empty[st]);  // frees the stage (in both CTAs) when these MMAs are done
                 }
                 if (!ok) break;
-                tc_commit(&tfull[ab]);      // accumulator ready for the epilogue
+                commit(&tfull[ab]);      // accumulator ready for the epilogue (of both CTAs)
             }
             // every MMA this thread issued has finished before tensor memory
             // is released
-            tc_commit(&drain);
+            if constexpr (PAIR) tc_commit_pair_local(&drain);
+            else tc_commit(&drain);
             (void)tc_wait(&drain, 0, abort_flag, p.err, 6, false);
         }
     } else {
@@ -317,27 +462,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
         // (the rows after them belong to the next segment).
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
-        const uint32_t obox = smem_base + kTcStages * kTcStageBytes + quarter * kTcOutBox;
+        const uint32_t obox = smem_base + kS * C::kStageBytes + quarter * kTcOutBox;
         const uint32_t orow = obox + lane * 128;
         const uint32_t sw = lane & 7;
+        // the accumulator's free barrier is the leader's
+        uint32_t tempty_cl0 = 0, tempty_cl1 = 0;
+        if constexpr (PAIR) {
+            tempty_cl0 = mapa_rank(&tempty[0], 0);
+            tempty_cl1 = mapa_rank(&tempty[1], 0);
+        }
         int local = 0;
         TcTile tl;
         // decisions stay warp-uniform: tcgen05.ld is a whole-warp instruction
-        for (int g = blockIdx.x; g < n_tiles; g += gridDim.x, ++local) {
+        for (int g = unit; g < n_tiles; g += n_units, ++local) {
             if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-            const int phase = tc_tile_global(P, g, tl);
+            const int phase = tc_tile_global<PAIR>(P, g, tl);
             const TcSeg& S = P.seg[tl.seg];
             const TcParams& q = phase == 1 ? fp.p1 : fp.p2;
             const int ab = local & 1;
             bool ok = true;
-            if (lane == 0) ok = tc_wait(&tfull[ab], (local >> 1) & 1, abort_flag, p.err, 5);
+            if (lane == 0) ok = tcw<PAIR>(&tfull[ab], (local >> 1) & 1, abort_flag, p.err, 5);
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + ab * kTcBN;
-            const int row_in_seg = tl.mt * kTcBM + r;
+            const int tile_row = tl.mt * pair_rows + row_off;  // first row of this CTA's part
+            const int row_in_seg = tile_row + r;
             const bool valid = row_in_seg < S.rows;
-            const bool boxed = tl.mt * kTcBM + quarter * 32 + 32 <= S.rows;
-            const int box_row = S.row0 + tl.mt * kTcBM + quarter * 32;
+            const bool boxed = tile_row + quarter * 32 + 32 <= S.rows;
+            const int box_row = S.row0 + tile_row + quarter * 32;
             const CUtensorMap* omap = S.shared ? &q.map_out_shared : &q.map_out_routed;
             const long long grow = (long long)S.row0 + row_in_seg;
             if (phase == 1) {
@@ -408,7 +560,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[ab]);
+            if (lane == 0) {
+                if (PAIR && !leader) mbar_arrive_remote(ab ? tempty_cl1 : tempty_cl0);
+                else mbar_arrive(&tempty[ab]);
+            }
             if (phase == 1) {
                 // this warp's rows of h are complete in global memory: count
                 // them for the phase-2 tiles of this (segment, row tile)
@@ -426,9 +581,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
 
     tc_fence_before();
     __syncthreads();
+    // a pair: the leader's MMAs (reading the peer's shared memory, writing its
+    // tensor memory) are done before either CTA frees or leaves
+    if constexpr (PAIR) cluster_sync();
     tc_fence_after();
     if (warp == 1) {
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base));
+        if constexpr (PAIR)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, 512;" ::"r"(tmem_base));
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base));
     }
 }
 
@@ -459,6 +620,82 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* perm, const int32_t
     const int g_rows = rows_cap < 4096 ? (rows_cap > 0 ? rows_cap : 1) : 4096;
     return launch_pdl(gather_rows_kernel, dim3(g_rows), dim3(256), 0, st, static_cast<const uint4*>(x), perm,
                       expert_offsets, N, k, chunks, rows_cap, static_cast<uint4*>(x_perm), dep, n_dep);
+}
+
+// ---------------------------------------------------------------- host
+// One CTA per tile, or CTA pairs (clusters of 2) running the 2-CTA MMA:
+// -1 chooses (one CTA per tile: on the measured shapes the pairs were no
+// faster), 0 and 1 force one or the other (tests).
+static std::atomic<int> g_tc_pairs{-1};
+
+void set_tc_pairs(int mode) { g_tc_pairs.store(mode < 0 ? -1 : (mode > 0 ? 1 : 0)); }
+
+static bool use_tc_pairs(int, int, int) { return g_tc_pairs.load() == 1; }
+
+template <bool PAIR>
+static cudaError_t launch_tc_kernel(const TcFusedParams& fp, int grid, cudaStream_t st) {
+    auto kern = ffn_tc_kernel<PAIR>;
+    cudaError_t e = allow_max_smem(kern);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = TcCfg<PAIR>::kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    int n_attr = 1;
+    if (PAIR) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        n_attr = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n_attr;
+    return note_launch(reinterpret_cast<const void*>(kern), kTcThreads, TcCfg<PAIR>::kSmemBytes,
+                       cudaLaunchKernelEx(&cfg, kern, fp));
+}
+
+// CTA pairs that can be resident at once (every CTA of the persistent grid
+// must be: phase-2 tiles wait on phase-1 tiles of other CTAs), at most
+// max_ctas / 2; 0 if pairs cannot run.  Cached per device.
+static cudaError_t tc_pair_clusters(int max_ctas, int* clusters) {
+    static std::mutex mu;
+    static int cache[64];
+    static bool have[64] = {false};
+    *clusters = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!have[dev]) {
+        e = allow_max_smem(ffn_tc_kernel<true>);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(max_ctas & ~1);
+        cfg.blockDim = dim3(kTcThreads);
+        cfg.dynamicSmemBytes = TcCfg<true>::kSmemBytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, ffn_tc_kernel<true>, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();  // pairs unavailable: one CTA per tile
+            n = 0;
+        }
+        cache[dev] = n;
+        have[dev] = true;
+    }
+    *clusters = cache[dev] < max_ctas / 2 ? cache[dev] : max_ctas / 2;
+    return cudaSuccess;
 }
 
 cudaError_t launch_tc_ffn(const TcLaunch& a, cudaStream_t st) {
@@ -501,10 +738,13 @@ cudaError_t launch_tc_ffn(const TcLaunch& a, cudaStream_t st) {
     fp.p1 = p1;
     fp.p2 = p2;
     fp.dep = a.dep;
-    e = allow_max_smem(ffn_tc_kernel);
-    if (e != cudaSuccess) return e;
-    return note_launch(reinterpret_cast<const void*>(ffn_tc_kernel), kTcThreads, kTcSmemBytes,
-                       launch_pdl(ffn_tc_kernel, dim3(a.grid), dim3(kTcThreads), kTcSmemBytes, st, fp));
+    int clusters = 0;
+    if (use_tc_pairs(a.T, a.k, a.N)) {
+        e = tc_pair_clusters(a.grid, &clusters);
+        if (e != cudaSuccess) return e;
+    }
+    if (clusters > 0) return launch_tc_kernel<true>(fp, 2 * clusters, st);
+    return launch_tc_kernel<false>(fp, a.grid, st);
 }
 
 }  // namespace moe

@@ -154,6 +154,8 @@ struct TcLaunch {
 // tensor-core expert FFN: gather, then one launch of phase 1 (gate/up + SwiGLU)
 // and phase 2 (down) tiles
 cudaError_t launch_tc_ffn(const TcLaunch& a, cudaStream_t st);
+// -1: choose one CTA per tile or CTA pairs by the batch; 0 / 1: force (tests)
+void set_tc_pairs(int mode);
 // x_perm[pos] = x[perm[pos] / k] for the routed rows (bf16 rows of d values)
 cudaError_t launch_gather_rows(const void* x, const int32_t* perm, const int32_t* expert_offsets, int N,
                                int k, int d, int rows_cap, void* x_perm, cudaStream_t st, int* dep = nullptr,

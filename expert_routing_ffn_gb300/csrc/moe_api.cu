@@ -420,6 +420,8 @@ moe_status moe_stage_experts(const moe_dims* dims, uint64_t host_fetch_mask,
 // test hook: make the n-th and later copies of moe_stage_experts fail (-1: off)
 void moe_testing_fail_copies_after(int n) { g_fail_copies_after.store(n); }
 
+void moe_testing_set_tc_pairs(int mode) { set_tc_pairs(mode); }
+
 moe_status moe_testing_wait_timeout(void* ws, size_t ws_bytes, void* stream) {
     if (!ws || ws_bytes < kAlign || reinterpret_cast<uintptr_t>(ws) % kAlign) return MOE_ERR_INVALID_ARG;
     MOE_CUDA(launch_wait_timeout_probe(static_cast<DevError*>(ws), S(stream)));

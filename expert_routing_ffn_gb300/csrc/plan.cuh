@@ -131,13 +131,16 @@ __device__ __forceinline__ void build_tc_plan(const PlanArgs& a, const int* off)
     const int n1 = a.I / 128, n2 = a.d / 256;
     const bool sh = a.n_shared > 0;
     const int sh_m = sh ? (a.T + 127) / 128 : 0, sh_n1 = sh ? a.n_shared * a.I_shared / 128 : 0;
-    int rows = 0, m = 0;
+    const int sh_p = sh ? (a.T + 255) / 256 : 0;
+    int rows = 0, m = 0, mp = 0;
     if (tid < a.N) {
         rows = off[tid + 1] - off[tid];
         m = (rows + 127) / 128;
+        mp = (rows + 255) / 256;
     }
-    int tot;
+    int tot, tot_p;
     const int before = block_exclusive_scan((rows > 0 ? 1 : 0) | (m << 8), &tot);
+    const int before_p = block_exclusive_scan(mp, &tot_p);
     if (rows > 0) {
         TcSeg& s = P.seg[(sh ? 1 : 0) + (before & 0xff)];
         const int m_prev = before >> 8;
@@ -145,17 +148,23 @@ __device__ __forceinline__ void build_tc_plan(const PlanArgs& a, const int* off)
         s.tile1 = sh_m * sh_n1 + m_prev * n1;
         s.tile2 = sh_m * n2 + m_prev * n2;
         s.mbase = sh_m + m_prev;
+        s.m_pairs = mp;
+        s.tile1p = sh_p * sh_n1 + before_p * n1;
+        s.tile2p = sh_p * n2 + before_p * n2;
     }
     if (tid == 0) {
         if (sh) {
             TcSeg& s = P.seg[0];
             s.shared = 1; s.expert = a.N; s.row0 = 0; s.rows = a.T; s.m_tiles = sh_m; s.n1 = sh_n1;
             s.tile1 = 0; s.tile2 = 0; s.mbase = 0;
+            s.m_pairs = sh_p; s.tile1p = 0; s.tile2p = 0;
         }
         P.n_mt = sh_m + (tot >> 8);
         P.n_seg = (sh ? 1 : 0) + (tot & 0xff);
         P.n_tiles1 = sh_m * sh_n1 + (tot >> 8) * n1;
         P.n_tiles2 = sh_m * n2 + (tot >> 8) * n2;
+        P.n_tiles1p = sh_p * sh_n1 + tot_p * n1;
+        P.n_tiles2p = sh_p * n2 + tot_p * n2;
     }
 }
 

@@ -25,6 +25,13 @@ void moe_testing_fail_copies_after(int n);
  * ws, MOE_ERR_CUDA if the launch fails. */
 moe_status moe_testing_wait_timeout(void* ws, size_t ws_bytes, void* stream);
 
+/* The tensor-core prefill FFN runs either one CTA per 128-row tile or CTA
+ * pairs (clusters of two SMs) on 256-row tiles with the 2-CTA MMA.  mode -1
+ * (the default) chooses by the batch; 0 forces single CTAs, 1 pairs (when
+ * the device can hold them).  Process-wide; lets a test run both kernels on
+ * the same inputs. */
+void moe_testing_set_tc_pairs(int mode);
+
 #ifdef __cplusplus
 }
 #endif
