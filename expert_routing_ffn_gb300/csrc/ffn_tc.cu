@@ -624,13 +624,20 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* perm, const int32_t
 
 // ---------------------------------------------------------------- host
 // One CTA per tile, or CTA pairs (clusters of 2) running the 2-CTA MMA:
-// -1 chooses (one CTA per tile: on the measured shapes the pairs were no
-// faster), 0 and 1 force one or the other (tests).
+// -1 chooses by the batch, 0 and 1 force one or the other (tests).  Pairs
+// once the routed rows average at least 256 per expert: measured on the same
+// GPU, alternating, the FFN stage took 342 against 366 us (DeepSeek-V2-Lite
+// shape, 4096 tokens) and 2.52 against 2.57 ms (Qwen2-57B shape); smaller
+// segments waste more of a 256-row tile on their ragged end.
 static std::atomic<int> g_tc_pairs{-1};
 
 void set_tc_pairs(int mode) { g_tc_pairs.store(mode < 0 ? -1 : (mode > 0 ? 1 : 0)); }
 
-static bool use_tc_pairs(int, int, int) { return g_tc_pairs.load() == 1; }
+static bool use_tc_pairs(int T, int k, int N) {
+    const int m = g_tc_pairs.load();
+    if (m >= 0) return m == 1;
+    return (long long)T * k >= 256LL * N;
+}
 
 template <bool PAIR>
 static cudaError_t launch_tc_kernel(const TcFusedParams& fp, int grid, cudaStream_t st) {
