@@ -1139,7 +1139,9 @@ def run_workload(args, wl_name, world, rank, dev, steps, warmup, with_cpu=True):
         gbs = statistics.mean(k_bytes) / (med_ms / 1e3) / 1e9
         t_flop = statistics.mean(ff) / (bf16_tflops * 1e12)
         t_byte = statistics.mean(fb) / (hbm_gbs * 1e9)
-        common = {"kernel": "moe_expert_ffn (gather + ffn_tc_kernel: gate/up and down tiles in one launch)", "ffn_path": path}
+        pairs = T * cfg.k >= 256 * cfg.N  # the library's rule for the 2-CTA tiles
+        common = {"kernel": "moe_expert_ffn (gather + ffn_tc_kernel%s: gate/up and down tiles in one launch)"
+                            % ("<pairs> on CTA pairs, 2-CTA MMA" if pairs else "<single>"), "ffn_path": path}
         if t_byte > t_flop:
             roof = dict(common, bound="hbm", achieved=gbs, unit="GB/s",
                         **fractions(gbs, hbm_gbs, NOMINAL_HBM_GBS, peak_src), tensor_frac=tflops / bf16_tflops)
