@@ -67,7 +67,17 @@ __global__ void __launch_bounds__(1024) floe_select_kernel(const float* __restri
     const int pos = blockIdx.x;
     if (pos >= expert_offsets[N]) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < I; i += blockDim.x) keys[i] = __float_as_uint(fabsf(u[(size_t)pos * I + i]));
+    // |u| as ordered keys: 16-byte loads, all in flight at once (the row was
+    // just written by the up pass and sits in L2)
+    const float* ur = u + (size_t)pos * I;
+    const int I4 = reinterpret_cast<uintptr_t>(ur) % 16 == 0 ? I / 4 : 0;
+#pragma unroll 4
+    for (int i = tid; i < I4; i += blockDim.x) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(ur) + i);
+        reinterpret_cast<uint4*>(keys)[i] = make_uint4(__float_as_uint(fabsf(v.x)), __float_as_uint(fabsf(v.y)),
+                                                       __float_as_uint(fabsf(v.z)), __float_as_uint(fabsf(v.w)));
+    }
+    for (int i = 4 * I4 + tid; i < I; i += blockDim.x) keys[i] = __float_as_uint(fabsf(__ldcg(ur + i)));
     for (int w = tid; w < words; w += blockDim.x) bits[w] = 0u;
     if (tid == 0) { s_prefix = 0u; s_remaining = m; }
     uint32_t mask = 0u;
