@@ -650,7 +650,7 @@ def run_bitslice(args, wl_name, cfg, T, W, dev, world, rank, hbm_gbs, peak_src, 
     k_bytes = [fb[i % n_x] for i in range(n_k)]
     med_ms = statistics.median(k_ms)
     achieved = statistics.mean(k_bytes) / (med_ms / 1e3) / 1e9
-    roof = {"kernel": "moe_bitslice_ffn (bitslice_gateup_kernel + bitslice_down_kernel + bitslice_sum_kernel)",
+    roof = {"kernel": "moe_bitslice_ffn (bitslice_gateup_kernel + bitslice_down_kernel with the gated slot sum)",
             "ffn_path": f"bitslice-b{bits}", "bound": "hbm", "achieved": achieved, "unit": "GB/s",
             **fractions(achieved, hbm_gbs, NOMINAL_HBM_GBS, peak_src),
             "algorithmic_bytes_per_launch": float(statistics.mean(fb)), "median_launch_ms": med_ms,

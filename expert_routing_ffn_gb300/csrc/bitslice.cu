@@ -134,6 +134,9 @@ __global__ void __launch_bounds__(kBsThreads) bitslice_gateup_kernel(BitsliceArg
     grid_dep_wait();  // x and the routed experts come from the previous launches
     extern __shared__ __align__(16) float bs_tbl[];
     const int t = blockIdx.y, d = a.d, I = a.I, words = d / 32;
+    // the down launch's completion counters start from zero every call
+    if (blockIdx.x == 0 && blockIdx.y == 0)
+        for (int i = threadIdx.x; i < a.T * (d / 16); i += blockDim.x) a.cnt[i] = 0;
     float* xv = bs_tbl + kBsTableBytes / 4;  // x_t as float
     for (int i = threadIdx.x; i < d; i += blockDim.x) xv[i] = bs_load(x, (size_t)t * d + i);
     __syncthreads();
@@ -185,25 +188,14 @@ __global__ void __launch_bounds__(kBsThreads) bitslice_gateup_kernel(BitsliceArg
     }
 }
 
-// ---------------------------------------------------------------- down
-// Block (persistent over output rows, (token, slot) pair): the table over
-// h of the pair, then a warp per output j: y_part = s_d[j] * the dot of h
-// with the top B planes of row j of W_down^T.
+// the y_part rows of one (token, slot) pair: a warp per output j of this
+// block's share
 template <int B>
-__global__ void __launch_bounds__(kBsThreads) bitslice_down_kernel(BitsliceArgs a) {
-    grid_dep_wait();  // h comes from the gate / up launch
-    extern __shared__ __align__(16) float bs_tbl[];
-    const int pair = blockIdx.y, d = a.d, I = a.I, words = I / 32;
-    const int S = a.k + a.ns;
-    const int e = bs_expert(a, pair / S, pair % S);
-    if (e < 0 || e >= a.N + a.ns) {  // no expert: a zero contribution
-        for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < d; j += gridDim.x * blockDim.x)
-            a.y_part[(size_t)pair * d + j] = 0.f;
-        return;
-    }
+__device__ __forceinline__ void bs_down_rows(const BitsliceArgs& a, int pair, int e, int lane, int warp, int nw,
+                                             float* bs_tbl) {
+    const int d = a.d, I = a.I, words = I / 32;
     bs_build_table(a.h + (size_t)pair * I, I, bs_tbl);
     __syncthreads();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const size_t mat = (size_t)8 * d * words;
     for (int j = blockIdx.x * nw + warp; j < d; j += gridDim.x * nw) {
         const uint32_t* pd = a.planes_down + (size_t)e * mat + (size_t)j * words;
@@ -233,23 +225,51 @@ __global__ void __launch_bounds__(kBsThreads) bitslice_down_kernel(BitsliceArgs 
     }
 }
 
-// ---------------------------------------------------------------- gated sum
-// y[t][j] (+)= sum over slots s, in order, of gate[t][s] * y_part[t S + s][j]
-// (S = k + ns slots per token; a shared slot's gate is 1).
-__global__ void __launch_bounds__(256) bitslice_sum_kernel(BitsliceArgs a) {
-    grid_dep_wait();
-    const size_t n = (size_t)a.T * a.d;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-        const size_t t = i / a.d, j = i % a.d;
-        const int S = a.k + a.ns;
-        float acc = a.accumulate ? a.y[i] : 0.f;
+// ---------------------------------------------------------------- down
+// Block (persistent over output rows, (token, slot) pair): the table over
+// h of the pair, then a warp per output j: y_part = s_d[j] * the dot of h
+// with the top B planes of row j of W_down^T.  Block x of every pair of a
+// token covers the same outputs j; the last of them to finish (a counter per
+// token and block x) forms y for those outputs: the gated sum over the
+// slots in order.
+template <int B>
+__global__ void __launch_bounds__(kBsThreads) bitslice_down_kernel(BitsliceArgs a) {
+    grid_dep_wait();  // h and the zeroed counters come from the gate / up launch
+    extern __shared__ __align__(16) float bs_tbl[];
+    __shared__ int s_last;
+    const int pair = blockIdx.y, d = a.d;
+    const int S = a.k + a.ns;
+    const int t = pair / S;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int e = bs_expert(a, t, pair % S);
+    if (e < 0 || e >= a.N + a.ns) {  // no expert: a zero contribution
+        for (int j = blockIdx.x * nw + warp; j < d; j += gridDim.x * nw)
+            if (lane == 0) a.y_part[(size_t)pair * d + j] = 0.f;
+    } else {
+        bs_down_rows<B>(a, pair, e, lane, warp, nw, bs_tbl);
+    }
+    // the gated sum over the token's slots, by the last block of this x
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = atomicAdd(a.cnt + (size_t)t * (d / 16) + blockIdx.x, 1) == S - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int i = threadIdx.x;; i += blockDim.x) {
+        const int j = blockIdx.x * nw + (i % nw) + (i / nw) * gridDim.x * nw;
+        if (j >= d) break;
+        const size_t at = (size_t)t * d + j;
+        float acc = a.accumulate ? a.y[at] : 0.f;
         for (int s = 0; s < S; ++s) {
-            const float g = (s < a.k && a.gate) ? a.gate[t * a.k + s] : 1.f;
-            acc += g * a.y_part[(t * S + s) * a.d + j];
+            const float g = (s < a.k && a.gate) ? a.gate[(size_t)t * a.k + s] : 1.f;
+            acc += g * __ldcg(a.y_part + ((size_t)t * S + s) * d + j);
         }
-        a.y[i] = acc;
+        a.y[at] = acc;
     }
 }
+
 
 // ---------------------------------------------------------------- host
 cudaError_t launch_bitslice_pack(int rows_in, int cols_in, bool bf16, const void* w, int transpose, uint32_t* planes,
@@ -280,11 +300,7 @@ static cudaError_t bs_ffn(const BitsliceArgs& a, const void* x, int sms, cudaStr
     const int pairs = a.T * (a.k + a.ns), per2 = (a.d + 15) / 16;
     int g2 = (2 * sms + pairs - 1) / pairs;
     g2 = g2 < 1 ? 1 : g2 > per2 ? per2 : g2;
-    e = launch_pdl(bitslice_down_kernel<B>, dim3(g2, pairs), dim3(kBsThreads), smem2, st, a);
-    if (e != cudaSuccess) return e;
-    const size_t n = (size_t)a.T * a.d;
-    const int g3 = (int)((n + 255) / 256 < 4 * (size_t)sms ? (n + 255) / 256 : 4 * (size_t)sms);
-    return launch_pdl(bitslice_sum_kernel, dim3(g3), dim3(256), 0, st, a);
+    return launch_pdl(bitslice_down_kernel<B>, dim3(g2, pairs), dim3(kBsThreads), smem2, st, a);
 }
 
 template <typename W>

@@ -228,6 +228,7 @@ struct BitsliceArgs {
     float* h;               // [T*(k+ns), I] scratch
     float* y_part;          // [T*(k+ns), d] scratch
     float* y;               // [T, d]
+    int* cnt;               // [T, d/16] scratch: finished (token, slot) blocks per (token, output block)
 };
 cudaError_t launch_bitslice_pack(int rows_in, int cols_in, bool bf16, const void* w, int transpose, uint32_t* planes,
                                  float* scales, cudaStream_t st);

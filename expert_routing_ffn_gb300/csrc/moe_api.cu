@@ -706,7 +706,8 @@ moe_status moe_bitslice_pack(int rows, int cols, moe_dtype wtype, const void* w,
 
 size_t moe_bitslice_scratch_size(int d, int I, int T, int slots) {
     if (d <= 0 || I <= 0 || T < 0 || slots <= 0) return 0;
-    return (size_t)T * slots * ((size_t)I + d) * sizeof(float);
+    // h and y_part rows, then the down launch's counters (T x d/16 int32)
+    return (size_t)T * slots * ((size_t)I + d) * sizeof(float) + (size_t)T * (d / 16) * sizeof(int32_t);
 }
 
 moe_status moe_bitslice_ffn(int d, int I, int N, int n_shared, int bits, moe_dtype xtype, const void* x, int T, int k,
@@ -734,8 +735,9 @@ moe_status moe_bitslice_ffn(int d, int I, int N, int n_shared, int bits, moe_dty
     a.planes_gate = planes_gate; a.planes_up = planes_up; a.planes_down = planes_down;
     a.scales_gate = scales_gate; a.scales_up = scales_up; a.scales_down = scales_down;
     a.h = static_cast<float*>(scratch); a.y_part = a.h + (size_t)T * (k + n_shared) * I; a.y = y;
+    a.cnt = reinterpret_cast<int*>(a.y_part + (size_t)T * (k + n_shared) * d);
     MOE_CUDA(launch_bitslice_ffn(a, x, xtype == MOE_DTYPE_BF16, sm_count(), S(stream)));
-    count(3);
+    count(2);
     return MOE_OK;
 }
 

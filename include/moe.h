@@ -435,7 +435,7 @@ moe_status moe_bitslice_pack(int rows, int cols, moe_dtype wtype, const void* w,
                              uint32_t* planes, float* scales, void* stream);
 
 /* Scratch bytes moe_bitslice_ffn needs for T tokens of `slots` slots each
- * (k + n_shared): T*slots*(I + d)*4 (0 for bad sizes). */
+ * (k + n_shared): T*slots*(I + d)*4 + T*(d/16)*4 (0 for bad sizes). */
 size_t moe_bitslice_scratch_size(int d, int I, int T, int slots);
 
 /* The draft FFN with b-bit weights for T tokens of k routed slots and the

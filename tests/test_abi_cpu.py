@@ -218,7 +218,7 @@ def test_bitslice_rejects_bad_arguments_before_cuda():
     p = C.c_void_p(0x1000)
     bf16 = moe.MOE_DTYPE_BF16
     ok_scratch = moe.moe_bitslice_scratch_size(256, 512, 2, 3)
-    assert ok_scratch == 2 * 3 * (512 + 256) * 4
+    assert ok_scratch == 2 * 3 * (512 + 256) * 4 + 2 * (256 // 16) * 4
     assert moe.moe_bitslice_scratch_size(256, 512, 2, 0) == 0
 
     def ffn(d=256, I=512, N=4, ns=1, bits=4, T=2, k=2, scratch=ok_scratch, x=p):
