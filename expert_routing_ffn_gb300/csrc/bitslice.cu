@@ -128,8 +128,11 @@ __device__ __forceinline__ int bs_expert(const BitsliceArgs& a, int t, int s) {
 // ---------------------------------------------------------------- gate / up
 // Block (persistent over rows, token t): the table over x_t, then a warp per
 // (slot, channel) row of this token: g and u over the top B planes, h =
-// SiLU(g) u.  Routed slots naming no expert in 0..N-1 give h = 0.
-template <typename W, int B>
+// SiLU(g) u.  Routed slots naming no expert in 0..N-1 give h = 0.  A warp
+// takes two rows per iteration and loads all their plane words (WPL words a
+// lane per plane and matrix, d <= 1024 * WPL) before the table reads that
+// consume them, so one row's loads are in flight during the other's sums.
+template <typename W, int B, int WPL>
 __global__ void __launch_bounds__(kBsThreads) bitslice_gateup_kernel(BitsliceArgs a, const W* __restrict__ x) {
     grid_dep_wait();  // x and the routed experts come from the previous launches
     extern __shared__ __align__(16) float bs_tbl[];
@@ -144,84 +147,104 @@ __global__ void __launch_bounds__(kBsThreads) bitslice_gateup_kernel(BitsliceArg
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const size_t mat = (size_t)8 * I * words;  // words of one expert's matrix
-    const int S = a.k + a.ns;
-    for (int row = blockIdx.x * nw + warp; row < S * I; row += gridDim.x * nw) {
-        const int slot = row / I, c = row % I;
-        const int e = bs_expert(a, t, slot);
-        float h = 0.f;
-        if (e >= 0 && e < a.N + a.ns) {
-            const uint32_t* pg = a.planes_gate + (size_t)e * mat + (size_t)c * words;
-            const uint32_t* pu = a.planes_up + (size_t)e * mat + (size_t)c * words;
-            float ag = 0.f, au = 0.f;
-            // every plane word of the row (d <= 4096: at most 4 per lane) is
-            // loaded before the table reads that consume them
-            uint32_t bg[4][B], bu[4][B];
+    const int S = a.k + a.ns, rows = S * I, stride = gridDim.x * nw;
+    for (int row0 = blockIdx.x * nw + warp; row0 < rows; row0 += 2 * stride) {
+        uint32_t bg[2][WPL][B], bu[2][WPL][B];
+        int e[2], c[2], slot[2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+        for (int r = 0; r < 2; ++r) {
+            const int row = row0 + r * stride;
+            slot[r] = row / I;
+            c[r] = row % I;
+            e[r] = row < rows ? bs_expert(a, t, slot[r]) : -1;
+            const bool ok = e[r] >= 0 && e[r] < a.N + a.ns;
+            const uint32_t* pg = a.planes_gate + (size_t)(ok ? e[r] : 0) * mat + (size_t)c[r] * words;
+            const uint32_t* pu = a.planes_up + (size_t)(ok ? e[r] : 0) * mat + (size_t)c[r] * words;
+#pragma unroll
+            for (int i = 0; i < WPL; ++i) {
                 const int wd = lane + 32 * i;
 #pragma unroll
                 for (int sl = 0; sl < B; ++sl) {
-                    bg[i][sl] = wd < words ? pg[(size_t)sl * I * words + wd] : 0u;
-                    bu[i][sl] = wd < words ? pu[(size_t)sl * I * words + wd] : 0u;
+                    bg[r][i][sl] = ok && wd < words ? pg[(size_t)sl * I * words + wd] : 0u;
+                    bu[r][i][sl] = ok && wd < words ? pu[(size_t)sl * I * words + wd] : 0u;
                 }
             }
+        }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int wd = lane + 32 * i;
-                if (wd < words) {
+        for (int r = 0; r < 2; ++r) {
+            const int row = row0 + r * stride;
+            if (row >= rows) break;
+            float h = 0.f;
+            if (e[r] >= 0 && e[r] < a.N + a.ns) {
+                float ag = 0.f, au = 0.f;
 #pragma unroll
-                    for (int sl = 0; sl < B; ++sl) {
-                        ag += bs_plane_weight<B>(sl) * bs_word_sum(bs_tbl + wd, bg[i][sl]);
-                        au += bs_plane_weight<B>(sl) * bs_word_sum(bs_tbl + wd, bu[i][sl]);
+                for (int i = 0; i < WPL; ++i) {
+                    const int wd = lane + 32 * i;
+                    if (wd < words) {
+#pragma unroll
+                        for (int sl = 0; sl < B; ++sl) {
+                            ag += bs_plane_weight<B>(sl) * bs_word_sum(bs_tbl + wd, bg[r][i][sl]);
+                            au += bs_plane_weight<B>(sl) * bs_word_sum(bs_tbl + wd, bu[r][i][sl]);
+                        }
                     }
                 }
-            }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                ag += __shfl_xor_sync(0xffffffffu, ag, o);
-                au += __shfl_xor_sync(0xffffffffu, au, o);
+                for (int o = 16; o > 0; o >>= 1) {
+                    ag += __shfl_xor_sync(0xffffffffu, ag, o);
+                    au += __shfl_xor_sync(0xffffffffu, au, o);
+                }
+                const float g = ag * a.scales_gate[(size_t)e[r] * I + c[r]];
+                const float u = au * a.scales_up[(size_t)e[r] * I + c[r]];
+                h = g / (1.f + expf(-g)) * u;
             }
-            const float g = ag * a.scales_gate[(size_t)e * I + c], u = au * a.scales_up[(size_t)e * I + c];
-            h = g / (1.f + expf(-g)) * u;
+            if (lane == 0) a.h[((size_t)t * S + slot[r]) * I + c[r]] = h;
         }
-        if (lane == 0) a.h[((size_t)t * S + slot) * I + c] = h;
     }
 }
 
 // the y_part rows of one (token, slot) pair: a warp per output j of this
-// block's share
-template <int B>
+// block's share, two outputs per iteration with all their plane words loaded
+// first (WPL words a lane per plane, I <= 1024 * WPL)
+template <int B, int WPL>
 __device__ __forceinline__ void bs_down_rows(const BitsliceArgs& a, int pair, int e, int lane, int warp, int nw,
                                              float* bs_tbl) {
     const int d = a.d, I = a.I, words = I / 32;
     bs_build_table(a.h + (size_t)pair * I, I, bs_tbl);
     __syncthreads();
     const size_t mat = (size_t)8 * d * words;
-    for (int j = blockIdx.x * nw + warp; j < d; j += gridDim.x * nw) {
-        const uint32_t* pd = a.planes_down + (size_t)e * mat + (size_t)j * words;
-        float acc = 0.f;
-        // I <= 4096: at most 4 words per lane, loaded ahead of use
-        for (int w0 = 0; w0 < words; w0 += 128) {
-            uint32_t bd[4][B];
+    const int stride = gridDim.x * nw;
+    for (int j0 = blockIdx.x * nw + warp; j0 < d; j0 += 2 * stride) {
+        uint32_t bd[2][WPL][B];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int wd = w0 + lane + 32 * i;
+        for (int r = 0; r < 2; ++r) {
+            const int j = j0 + r * stride;
+            const uint32_t* pd = a.planes_down + (size_t)e * mat + (size_t)(j < d ? j : 0) * words;
 #pragma unroll
-                for (int sl = 0; sl < B; ++sl) bd[i][sl] = wd < words ? pd[(size_t)sl * d * words + wd] : 0u;
-            }
+            for (int i = 0; i < WPL; ++i) {
+                const int wd = lane + 32 * i;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int wd = w0 + lane + 32 * i;
-                if (wd < words) {
-#pragma unroll
-                    for (int sl = 0; sl < B; ++sl)
-                        acc += bs_plane_weight<B>(sl) * bs_word_sum(bs_tbl + wd, bd[i][sl]);
-                }
+                for (int sl = 0; sl < B; ++sl)
+                    bd[r][i][sl] = j < d && wd < words ? pd[(size_t)sl * d * words + wd] : 0u;
             }
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) a.y_part[(size_t)pair * d + j] = acc * a.scales_down[(size_t)e * d + j];
+        for (int r = 0; r < 2; ++r) {
+            const int j = j0 + r * stride;
+            if (j >= d) break;
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < WPL; ++i) {
+                const int wd = lane + 32 * i;
+                if (wd < words) {
+#pragma unroll
+                    for (int sl = 0; sl < B; ++sl)
+                        acc += bs_plane_weight<B>(sl) * bs_word_sum(bs_tbl + wd, bd[r][i][sl]);
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (lane == 0) a.y_part[(size_t)pair * d + j] = acc * a.scales_down[(size_t)e * d + j];
+        }
     }
 }
 
@@ -232,7 +255,7 @@ __device__ __forceinline__ void bs_down_rows(const BitsliceArgs& a, int pair, in
 // token covers the same outputs j; the last of them to finish (a counter per
 // token and block x) forms y for those outputs: the gated sum over the
 // slots in order.
-template <int B>
+template <int B, int WPL>
 __global__ void __launch_bounds__(kBsThreads) bitslice_down_kernel(BitsliceArgs a) {
     grid_dep_wait();  // h and the zeroed counters come from the gate / up launch
     extern __shared__ __align__(16) float bs_tbl[];
@@ -246,7 +269,7 @@ __global__ void __launch_bounds__(kBsThreads) bitslice_down_kernel(BitsliceArgs 
         for (int j = blockIdx.x * nw + warp; j < d; j += gridDim.x * nw)
             if (lane == 0) a.y_part[(size_t)pair * d + j] = 0.f;
     } else {
-        bs_down_rows<B>(a, pair, e, lane, warp, nw, bs_tbl);
+        bs_down_rows<B, WPL>(a, pair, e, lane, warp, nw, bs_tbl);
     }
     // the gated sum over the token's slots, by the last block of this x
     __syncthreads();
@@ -282,38 +305,48 @@ cudaError_t launch_bitslice_pack(int rows_in, int cols_in, bool bf16, const void
                       cols_in, transpose, planes, scales);
 }
 
-template <typename W, int B>
+template <typename W, int B, int WPL1, int WPL2>
 static cudaError_t bs_ffn(const BitsliceArgs& a, const void* x, int sms, cudaStream_t st) {
     const size_t smem1 = kBsTableBytes + (size_t)a.d * 4;
-    cudaError_t e = allow_max_smem(bitslice_gateup_kernel<W, B>);
+    cudaError_t e = allow_max_smem(bitslice_gateup_kernel<W, B, WPL1>);
     if (e != cudaSuccess) return e;
     // gate / up: about two blocks per SM over all tokens
     const int rows1 = (a.k + a.ns) * a.I, per1 = (rows1 + 15) / 16;
     int g1 = (2 * sms + a.T - 1) / a.T;
     g1 = g1 < 1 ? 1 : g1 > per1 ? per1 : g1;
-    e = launch_pdl(bitslice_gateup_kernel<W, B>, dim3(g1, a.T), dim3(kBsThreads), smem1, st, a,
+    e = launch_pdl(bitslice_gateup_kernel<W, B, WPL1>, dim3(g1, a.T), dim3(kBsThreads), smem1, st, a,
                    static_cast<const W*>(x));
     if (e != cudaSuccess) return e;
     const size_t smem2 = kBsTableBytes;
-    e = allow_max_smem(bitslice_down_kernel<B>);
+    e = allow_max_smem(bitslice_down_kernel<B, WPL2>);
     if (e != cudaSuccess) return e;
     const int pairs = a.T * (a.k + a.ns), per2 = (a.d + 15) / 16;
     int g2 = (2 * sms + pairs - 1) / pairs;
     g2 = g2 < 1 ? 1 : g2 > per2 ? per2 : g2;
-    return launch_pdl(bitslice_down_kernel<B>, dim3(g2, pairs), dim3(kBsThreads), smem2, st, a);
+    return launch_pdl(bitslice_down_kernel<B, WPL2>, dim3(g2, pairs), dim3(kBsThreads), smem2, st, a);
+}
+
+// words a lane per plane: d (gate / up) and I (down) up to 2048 take 2, up to 4096 take 4
+template <typename W, int B>
+static cudaError_t bs_ffn_w(const BitsliceArgs& a, const void* x, int sms, cudaStream_t st) {
+    const bool small1 = a.d <= 2048, small2 = a.I <= 2048;
+    if (small1 && small2) return bs_ffn<W, B, 2, 2>(a, x, sms, st);
+    if (small1) return bs_ffn<W, B, 2, 4>(a, x, sms, st);
+    if (small2) return bs_ffn<W, B, 4, 2>(a, x, sms, st);
+    return bs_ffn<W, B, 4, 4>(a, x, sms, st);
 }
 
 template <typename W>
 static cudaError_t bs_ffn_bits(const BitsliceArgs& a, const void* x, int sms, cudaStream_t st) {
     switch (a.bits) {
-        case 1: return bs_ffn<W, 1>(a, x, sms, st);
-        case 2: return bs_ffn<W, 2>(a, x, sms, st);
-        case 3: return bs_ffn<W, 3>(a, x, sms, st);
-        case 4: return bs_ffn<W, 4>(a, x, sms, st);
-        case 5: return bs_ffn<W, 5>(a, x, sms, st);
-        case 6: return bs_ffn<W, 6>(a, x, sms, st);
-        case 7: return bs_ffn<W, 7>(a, x, sms, st);
-        case 8: return bs_ffn<W, 8>(a, x, sms, st);
+        case 1: return bs_ffn_w<W, 1>(a, x, sms, st);
+        case 2: return bs_ffn_w<W, 2>(a, x, sms, st);
+        case 3: return bs_ffn_w<W, 3>(a, x, sms, st);
+        case 4: return bs_ffn_w<W, 4>(a, x, sms, st);
+        case 5: return bs_ffn_w<W, 5>(a, x, sms, st);
+        case 6: return bs_ffn_w<W, 6>(a, x, sms, st);
+        case 7: return bs_ffn_w<W, 7>(a, x, sms, st);
+        case 8: return bs_ffn_w<W, 8>(a, x, sms, st);
         default: return cudaErrorInvalidValue;
     }
 }
