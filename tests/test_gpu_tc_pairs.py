@@ -76,3 +76,28 @@ def test_pairs_qwen2_prefill():
         del b
     rel = float((outs[0] - outs[1]).norm() / outs[0].norm())
     assert rel < 1e-5, rel
+
+
+def test_pairs_dsv2lite_prefill_4096_against_oracle():
+    """The DeepSeek-V2-Lite-shaped 4096-token prefill (the default takes
+    CTA pairs at this batch): routing on every token, outputs on a seeded
+    512-token subset against the oracle on the batch's resident set."""
+    import numpy as np
+    from expert_routing_ffn_gb300.layer import as_u64
+    from parity import to_np
+    cfg = CONFIGS["dsv2lite"]
+    W = make_weights(cfg)
+    T = 4096
+    layer = DeviceLayer(cfg, W, T)
+    x = make_tokens(cfg, T=T, batch=0)
+    b = LayerBuffers(layer, T)
+    forward(layer, b, x_device(x, layer.dt))
+    st, det = moe.moe_check(layer.ws)
+    assert st == moe.MOE_OK, (moe.status_string(st), det)
+    Rr = oracle.layer_forward(cfg, W, x, route_only=True)
+    assert as_u64(to_np(b.batch_resident)[0]) == Rr.resident
+    check_routing(cfg, Rr, b)
+    check_selection(cfg, Rr, b)
+    rows = np.sort(np.random.default_rng(1).choice(T, 512, replace=False))
+    R = oracle.layer_forward(cfg, W, x[rows], resident=Rr.resident)
+    check_output(cfg, R, b.out, tokens=rows)
