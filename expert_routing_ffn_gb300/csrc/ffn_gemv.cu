@@ -74,11 +74,14 @@ struct Producer {
         } else if (c_list_off >= 0) {
             // FloE: gate and down rows of the listed channels only
             mbar_arrive_expect_tx(&full[b], 2 * bytes);
-            // the list entries of the stage are loaded together (nch <= 2)
-            const int r0 = list[c_list_off + local];
-            const int r1 = nch > 1 ? list[c_list_off + local + 1] : 0;
-            for (int c = 0; c < nch; ++c) {
-                const size_t row = (size_t)(c == 0 ? r0 : r1);
+            // the list entries of the stage are loaded together (nch <= 4)
+            int rows[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) rows[c] = c < nch ? list[c_list_off + local + c] : 0;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (c >= nch) break;
+                const size_t row = (size_t)rows[c];
                 bulk_g2s(buf + c * row_bytes, w[0] + row * row_bytes, (uint32_t)row_bytes, &full[b], policy);
                 bulk_g2s(buf + 2 * mat_bytes + c * row_bytes, w[2] + row * row_bytes, (uint32_t)row_bytes,
                          &full[b], policy);
@@ -349,9 +352,16 @@ __device__ __forceinline__ void ffn_gemv_body(const GemvParams& p) {
         const int llo = ch - S.ch_start;
         const int lhi = min(hi, S.ch_start + S.I) - S.ch_start;
         if (FLOE && S.list_off == kUpOnly) {
-            if (S.rows == 1) gemv_piece_up<W, 3 * CH, 1>(p, S, llo, lhi, cta, sh, n_cons, stage_k);
-            else if (S.rows == 2) gemv_piece_up<W, 3 * CH, 2>(p, S, llo, lhi, cta, sh, n_cons, stage_k);
-            else { if (tid == 0) set_error(p.err, MOE_ERR_DEVICE_INDEX, seg); s_abort = 1; }
+            // (the up-only pass runs on the CH = 2 instantiation; the sparse
+            // pass's wider stages carry no up-only segments)
+            if constexpr (3 * CH * 2 <= 16) {
+                if (S.rows == 1) gemv_piece_up<W, 3 * CH, 1>(p, S, llo, lhi, cta, sh, n_cons, stage_k);
+                else if (S.rows == 2) gemv_piece_up<W, 3 * CH, 2>(p, S, llo, lhi, cta, sh, n_cons, stage_k);
+                else { if (tid == 0) set_error(p.err, MOE_ERR_DEVICE_INDEX, seg); s_abort = 1; }
+            } else {
+                if (tid == 0) set_error(p.err, MOE_ERR_DEVICE_INDEX, seg);
+                s_abort = 1;
+            }
         } else switch (S.rows) {
 #define MOE_PIECE(R)                                                                        \
     case R:                                                                                 \
@@ -508,8 +518,8 @@ int gemv_grid_for(int d, bool bf16, int sms) {
     return g > kGemvMaxCtas ? kGemvMaxCtas : g;
 }
 
-int gemv_stages(int d, bool bf16) {
-    const size_t stage = (size_t)3 * 2 * d * (bf16 ? 2 : 4);
+int gemv_stages(int d, bool bf16, int ch) {
+    const size_t stage = (size_t)3 * ch * d * (bf16 ? 2 : 4);
     const size_t budget = gemv_ctas_per_sm(d, bf16) == 2 ? 100 * 1024 : 200 * 1024;
     int ns = (int)(budget / stage);
     return ns < 2 ? 2 : (ns > kNSMax ? kNSMax : ns);
@@ -517,7 +527,14 @@ int gemv_stages(int d, bool bf16) {
 
 // floe = true selects the instantiation with the FloE modes (up-only and
 // sparse segments); the dense instantiation carries none of their code.
-cudaError_t launch_gemv(const GemvParams& p, int G, bool bf16, cudaStream_t st, bool floe) {
+// sparse = true: FloE's second pass (gate / down of the listed channels), 4
+// channels per stage, so a block barrier serves twice the bytes (p.NS from
+// gemv_stages(d, bf16, 4)).
+cudaError_t launch_gemv(const GemvParams& p, int G, bool bf16, cudaStream_t st, bool floe, bool sparse) {
+    if (bf16 && floe && sparse) {
+        if (p.d <= 2048) return launch_gemv_k(ffn_gemv_kernel_x2<__nv_bfloat16, 4, 4, true>, 256, 8, 4, 2, p, G, st);
+        return launch_gemv_k(ffn_gemv_kernel_x1<__nv_bfloat16, 4, 4, true>, 512, 8, 4, 2, p, G, st);
+    }
     if (bf16) {
 #ifdef MOE_XP_GEMV_ONE_CTA
         if (false)

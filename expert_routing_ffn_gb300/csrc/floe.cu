@@ -273,6 +273,7 @@ cudaError_t launch_floe_prepare(const FloeArgs& f, const PlanArgs& plan, const G
         GemvParams up = gp;
         up.up_pass = 1;
         up.prefetch_shared = 0;
+        up.NS = gemv_stages(f.d, true);  // the up pass's stages hold 2 x 3 rows
         e = launch_gemv(up, G, true, st, true);
     }
     if (e != cudaSuccess) return e;

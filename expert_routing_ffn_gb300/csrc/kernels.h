@@ -116,9 +116,10 @@ struct GemvParams {
     DevError* err;
     int prefetch_shared;          // > 0: that many shared experts pulled into L2 before the wait on routing
 };
-int gemv_stages(int d, bool bf16);
+int gemv_stages(int d, bool bf16, int ch = 2);
 int gemv_grid_for(int d, bool bf16, int sms);
-cudaError_t launch_gemv(const GemvParams& p, int G, bool bf16, cudaStream_t st, bool floe = false);
+cudaError_t launch_gemv(const GemvParams& p, int G, bool bf16, cudaStream_t st, bool floe = false,
+                        bool sparse = false);
 // one-token batches (every segment one row) of dense bf16 layers with d = 1536
 // or 2048: one channel per warp, the same plan and partial rows as launch_gemv
 bool gemv1_usable(int T, int d, bool bf16, bool floe);

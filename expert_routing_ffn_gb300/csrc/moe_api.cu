@@ -518,6 +518,7 @@ moe_status expert_ffn_impl(const moe_dims* dims, const void* x, const void* tabl
     p.floe_list = ws_at<int32_t>(ws, L.floe_list); p.I = dims->I; p.words = (dims->I + 31) / 32;
     p.up_pass = 0; p.prefetch_shared = prefetch_shared && !floe ? dims->n_shared : 0;
     if (floe) {
+        p.NS = gemv_stages(dims->d, bf16(dims), 4);  // the sparse pass: 4 channels per stage
         FloeArgs f;
         f.x = x; f.perm = perm; f.expert_offsets = expert_offsets; f.table = p.table;
         f.d = dims->d; f.I = dims->I; f.N = dims->N; f.topk = dims->k;
@@ -542,7 +543,7 @@ moe_status expert_ffn_impl(const moe_dims* dims, const void* x, const void* tabl
     if (gemv1_usable(dims->T, dims->d, bf16(dims), floe))
         MOE_CUDA(launch_gemv1(p, gemv_grid(dims), S(stream)));
     else
-        MOE_CUDA(launch_gemv(p, gemv_grid(dims), bf16(dims), S(stream), floe));
+        MOE_CUDA(launch_gemv(p, gemv_grid(dims), bf16(dims), S(stream), floe, floe));
     count();
     if (!reduce) return MOE_OK;
     GemvReduceArgs r;
