@@ -85,13 +85,12 @@ __global__ void __launch_bounds__(1024) floe_select_kernel(const float* __restri
         for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
         __syncthreads();
         const uint32_t prefix = s_prefix;
-        // lanes with the same bin add once (|u| values share few high bins)
+        // one shared-memory atomic per key in the current prefix (grouping
+        // equal bins of a warp with a match first measured slower: 20.4
+        // against 14.8 us for a 14336-channel row)
         for (int base = 0; base < I; base += blockDim.x) {
             const int i = base + tid;
-            const bool act = i < I && (keys[i] & mask) == prefix;
-            const int bin = act ? (int)((keys[i] >> shift) & 255u) : 256;
-            const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-            if (act && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+            if (i < I && (keys[i] & mask) == prefix) atomicAdd(&hist[(keys[i] >> shift) & 255u], 1);
         }
         __syncthreads();
         if (warp == 0) {
