@@ -216,6 +216,11 @@ __device__ __forceinline__ bool dep_wait(const int* cnt, int target, volatile in
 }
 
 // ---------------------------------------------------------------- epilogue stores
+// h = SiLU(g) * u = g / (1 + e^-g) * u with the fast exponential and
+// division (a few ulp in fp32; h is rounded to bf16).  Very negative g gives
+// e^-g = inf and h = -0, the limit.
+__device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.f + __expf(-g)) * u; }
+
 // 32 consecutive accumulator columns of this thread's TMEM lane, one wait.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     uint32_t r[32];
@@ -492,7 +497,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
             const int box_row = S.row0 + tile_row + quarter * 32;
             const CUtensorMap* omap = S.shared ? &q.map_out_shared : &q.map_out_routed;
             const long long grow = (long long)S.row0 + row_in_seg;
-            if (phase == 1) {
+            // rows past the segment's end (the next segment's rows, or the
+            // zero fill past the last one) are never stored: a warp holding
+            // none of the segment's rows reads nothing, and no thread runs the
+            // SiLU on a row it will not store
+            const bool any_valid = __any_sync(0xffffffffu, valid);
+            if (!any_valid) {
+            } else if (phase == 1) {
                 __nv_bfloat16* out = static_cast<__nv_bfloat16*>(S.shared ? q.out_shared : q.out_routed);
                 const long long ld = S.shared ? q.ld_out_shared : q.ld_out_routed;
                 __nv_bfloat16* dst = out + grow * ld + (long long)tl.nt * 128;
@@ -508,11 +519,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                         tmem_ld32(taddr + c + hh * 32, gv);
                         tmem_ld32(taddr + 128 + c + hh * 32, uv);
                         uint32_t w[16];
+                        if (valid) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float h0 = gv[2 * i] / (1.f + expf(-gv[2 * i])) * uv[2 * i];
-                            const float h1 = gv[2 * i + 1] / (1.f + expf(-gv[2 * i + 1])) * uv[2 * i + 1];
-                            w[i] = pack_bf16x2(h0, h1);
+                            for (int i = 0; i < 16; ++i)
+                                w[i] = pack_bf16x2(silu_mul(gv[2 * i], uv[2 * i]), silu_mul(gv[2 * i + 1], uv[2 * i + 1]));
                         }
                         if (boxed) {
 #pragma unroll
