@@ -263,7 +263,16 @@ __device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bu
 struct TcFusedParams {
     TcParams p1, p2;  // the two phases' tensor maps and outputs
     int* dep;         // per (segment, row tile): phase-1 epilogue warps done (zeroed by the gather)
+    int n_dep;        // counters in dep; the last is the tile counter of one-CTA tiles
 };
+
+// One CTA per tile: tiles are claimed in order from a global counter, so a
+// CTA that drew long tiles takes fewer of the rest.  The producer claims a
+// tile and passes its number to the MMA and epilogue warps through a small
+// ring in shared memory (kTq slots; a slot is free once all five consumers
+// have read it).  A CTA pair keeps the static order (tile stream c takes
+// tiles c, c + G, ...), so both CTAs of a pair see the same tiles.
+constexpr int kTq = 4;
 
 template <bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_constant__ TcFusedParams fp) {
@@ -275,6 +284,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
     __shared__ TcPlan plan_s;
+    __shared__ int tq[kTq];
+    __shared__ __align__(8) uint64_t tq_full[kTq], tq_empty[kTq];
 
     const TcParams& p = fp.p1;  // fields common to both phases
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -301,8 +312,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
             mbar_init(&tempty[b], kEpiWarps);  // one arrival per epilogue warp (of both CTAs)
         }
         mbar_init(&drain, 1);
+        for (int i = 0; i < kTq; ++i) {
+            mbar_init(&tq_full[i], 1);
+            mbar_init(&tq_empty[i], 1 + kEpiWarps);  // the MMA thread and each epilogue warp
+        }
         fence_mbar_init();
         abort_s = 0;
+        // the tile counter sits after every (segment, row tile) counter in use
+        if (!PAIR && p.plan->n_mt > fp.n_dep - 1) {
+            set_error(p.err, MOE_ERR_CAPACITY, p.plan->n_mt);
+            abort_s = 1;
+        }
     }
     if (warp == 1) {  // tensor memory: 512 columns = two 128x256 fp32 accumulators
         if constexpr (PAIR) {
@@ -323,13 +343,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
     const TcPlan& P = plan_s;
     const int d = p.d;
     const int n_tiles = PAIR ? P.n_tiles1p + P.n_tiles2p : P.n_tiles1 + P.n_tiles2;
+    // the j-th tile of this CTA, -1 after the last: claimed by the producer
+    // (one thread), read by the MMA thread and one lane of each epilogue warp
+    auto claim_tile = [&](int j) -> int {
+        if constexpr (PAIR) {
+            const int g = unit + j * n_units;
+            return g < n_tiles ? g : -1;
+        } else {
+            const int slot = j % kTq;
+            if (!tc_wait(&tq_empty[slot], ((j / kTq) & 1) ^ 1, abort_flag, p.err, 7)) return -1;
+            int g = atomicAdd(fp.dep + fp.n_dep - 1, 1);
+            if (g >= n_tiles) g = -1;
+            tq[slot] = g;
+            mbar_arrive(&tq_full[slot]);
+            return g;
+        }
+    };
+    auto next_tile = [&](int j) -> int {
+        if constexpr (PAIR) {
+            const int g = unit + j * n_units;
+            return g < n_tiles ? g : -1;
+        } else {
+            const int slot = j % kTq;
+            if (!tc_wait(&tq_full[slot], (j / kTq) & 1, abort_flag, p.err, 8)) return -1;
+            const int g = tq[slot];
+            mbar_arrive(&tq_empty[slot]);
+            return g;
+        }
+    };
 
     if (warp == 0) {
         // ---------------- TMA producer (each CTA loads its own stages)
         if (lane == 0) {
             int it = 0;
             TcTile tl;
-            for (int g = unit; g < n_tiles && !*abort_flag; g += n_units) {
+            for (int j = 0; !*abort_flag; ++j) {
+                const int g = claim_tile(j);
+                if (g < 0) break;
                 const int phase = tc_tile_global<PAIR>(P, g, tl);
                 const TcSeg& S = P.seg[tl.seg];
                 const TcParams& q = phase == 1 ? fp.p1 : fp.p2;
@@ -418,7 +468,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                 if constexpr (PAIR) tc_commit_pair(bar);
                 else tc_commit(bar);
             };
-            for (int g = unit; g < n_tiles && !*abort_flag; g += n_units, ++local) {
+            for (;; ++local) {
+                if (*abort_flag) break;
+                const int g = next_tile(local);
+                if (g < 0) break;
                 const int phase = tc_tile_global<PAIR>(P, g, tl);
                 const TcSeg& S = P.seg[tl.seg];
                 const int ab = local & 1;
@@ -479,8 +532,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
         int local = 0;
         TcTile tl;
         // decisions stay warp-uniform: tcgen05.ld is a whole-warp instruction
-        for (int g = unit; g < n_tiles; g += n_units, ++local) {
+        for (;; ++local) {
             if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+            int g = 0;
+            if (lane == 0) g = next_tile(local);
+            g = __shfl_sync(0xffffffffu, g, 0);
+            if (g < 0) break;
             const int phase = tc_tile_global<PAIR>(P, g, tl);
             const TcSeg& S = P.seg[tl.seg];
             const TcParams& q = phase == 1 ? fp.p1 : fp.p2;
@@ -755,6 +812,7 @@ cudaError_t launch_tc_ffn(const TcLaunch& a, cudaStream_t st) {
     fp.p1 = p1;
     fp.p2 = p2;
     fp.dep = a.dep;
+    fp.n_dep = a.n_dep;
     int clusters = 0;
     if (use_tc_pairs(a.T, a.k, a.N)) {
         e = tc_pair_clusters(a.grid, &clusters);
