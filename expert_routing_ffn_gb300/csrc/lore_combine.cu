@@ -3,6 +3,9 @@
 // SPICE write-up, LoRE section: a missing expert e is approximated by
 // y_shared + B_e A_e h with A_e [r, d], B_e [d, r], r << d; the shared part
 // is added once per token by the combine, scaled by the LoRE slots' gates.
+#include <algorithm>
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -350,6 +353,191 @@ __global__ void __launch_bounds__(256) lore_b_grouped_kernel(const W* __restrict
             }
         }
         __syncthreads();  // zs is rewritten by the next tile
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The same two products for bf16 layers on the tensor cores, as warp-level
+// MMAs with register operands (mma.sync): the rank r (16 to 64) is too short
+// a side for a shared-memory-staged tcgen05 tile, and with fragments loaded
+// straight from global memory no staging or block barrier is needed.  A warp
+// works on 16 grouped positions of one expert (kLoreMT), rows g = lane / 4
+// and g + 8 of each fragment, tq = lane % 4 the thread within its group.
+// Within a K step the products may be summed in any order, so each thread
+// loads contiguous 16-byte pieces and assigns their elements to the
+// fragment's K slots by a fixed bijection (the same on both operands).
+constexpr int kLoreMT = 16;     // grouped positions per warp tile
+constexpr int kLoreCB = 256;    // columns of d per warp item (B pass)
+
+// the expert and first grouped position of 16-position tile `tile` (tile
+// prefix counts in s_toff); false past the last tile
+__device__ __forceinline__ bool lore_mtile_of(const int* s_off, const int* s_toff, int N, int tile, int& e,
+                                              int& first) {
+    if (tile >= s_toff[N]) return false;
+    int lo = 0, hi = N - 1;  // the last expert with s_toff[e] <= tile
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_toff[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+    first = s_off[e] + (tile - s_toff[e]) * kLoreMT;
+    return true;
+}
+
+// s_off = g_off, s_toff[e] = 16-position tiles of the experts before e
+// (warp 0 scans: lane l holds experts l and l + 32)
+__device__ __forceinline__ void lore_mtile_table(const int32_t* __restrict__ g_off, int N, int* s_off,
+                                                 int* s_toff) {
+    for (int i = threadIdx.x; i <= N; i += blockDim.x) s_off[i] = g_off[i];
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        // exclusive prefix in expert order: experts 0..31 (lane l: c0), then
+        // 32..63 (lane l: c1), each half an inclusive warp scan
+        const int l = threadIdx.x;
+        const int c0 = l < N ? (s_off[l + 1] - s_off[l] + kLoreMT - 1) / kLoreMT : 0;
+        const int c1 = l + 32 < N ? (s_off[l + 33] - s_off[l + 32] + kLoreMT - 1) / kLoreMT : 0;
+        int a = c0, b = c1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int ta = __shfl_up_sync(0xffffffffu, a, o), tb = __shfl_up_sync(0xffffffffu, b, o);
+            if (l >= o) { a += ta; b += tb; }
+        }
+        const int half = __shfl_sync(0xffffffffu, a, 31), rest = __shfl_sync(0xffffffffu, b, 31);
+        if (l < N) s_toff[l] = a - c0;
+        if (l + 32 < N) s_toff[l + 32] = half + b - c1;
+        if (l == 0) s_toff[N] = half + rest;
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_tf32_1688(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t to_tf32(float f) {
+    uint32_t u;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(u) : "f"(f));
+    return u;
+}
+
+// zp[ks, pos, :] = A_e x_t over the d-range ks (of kLoreKS) for a 16-position
+// tile: M = positions, N = the R rank rows (R / 8 MMA columns), K = d in steps
+// of 32 values.  Thread tq's 16-byte piece [8 tq, 8 tq + 8) of a 32-value
+// step holds K slots {2tq, 2tq+1 | 2tq+8, 2tq+9} of two 16-deep MMA steps:
+// elements (0,1 | 2,3) for the first, (4,5 | 6,7) for the second.
+template <int R>
+__global__ void __launch_bounds__(256) lore_z_mma_kernel(const __nv_bfloat16* __restrict__ x,
+                                                         const __nv_bfloat16* __restrict__ A,
+                                                         const int32_t* __restrict__ g_off,
+                                                         const int32_t* __restrict__ g_list, int d, int k, int N,
+                                                         int n_pos, float* __restrict__ zp) {
+    grid_dep_wait();  // the grouping comes from the previous kernels
+    __shared__ int s_off[kMaxExperts + 1], s_toff[kMaxExperts + 1];
+    lore_mtile_table(g_off, N, s_off, s_toff);
+    const int lane = threadIdx.x & 31, g = lane >> 2, tq = lane & 3;
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    const int kc = d / kLoreKS;  // values of d per split (a multiple of 32)
+    const int items = s_toff[N] * kLoreKS;
+    for (int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); item < items; item += warps) {
+        const int tile = item / kLoreKS, ks = item % kLoreKS;
+        int e, first;
+        if (!lore_mtile_of(s_off, s_toff, N, tile, e, first)) break;
+        const int nt = min(kLoreMT, s_off[e + 1] - first);
+        const int t0 = g < nt ? g_list[first + g] / k : -1;
+        const int t1 = g + 8 < nt ? g_list[first + g + 8] / k : -1;
+        const uint4* x0 = t0 >= 0 ? reinterpret_cast<const uint4*>(x + (size_t)t0 * d) : nullptr;
+        const uint4* x1 = t1 >= 0 ? reinterpret_cast<const uint4*>(x + (size_t)t1 * d) : nullptr;
+        const uint4* a_rows = reinterpret_cast<const uint4*>(A + ((size_t)e * R + g) * d);  // row 8j + g: + 8j*d
+        float acc[R / 8][4];
+#pragma unroll
+        for (int j = 0; j < R / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+        const int v_lo = (ks * kc) / 8 + tq, v_hi = ((ks + 1) * kc) / 8;  // 16-byte vector indices
+#pragma unroll 2
+        for (int v = v_lo; v < v_hi; v += 4) {
+            const uint4 p0 = x0 ? __ldg(x0 + v) : make_uint4(0, 0, 0, 0);
+            const uint4 p1 = x1 ? __ldg(x1 + v) : make_uint4(0, 0, 0, 0);
+            uint4 bw[R / 8];
+#pragma unroll
+            for (int j = 0; j < R / 8; ++j) bw[j] = __ldg(a_rows + (size_t)j * d + v);
+#pragma unroll
+            for (int j = 0; j < R / 8; ++j) {
+                mma_bf16_16816(acc[j], p0.x, p1.x, p0.y, p1.y, bw[j].x, bw[j].y);
+                mma_bf16_16816(acc[j], p0.z, p1.z, p0.w, p1.w, bw[j].z, bw[j].w);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < R / 8; ++j) {
+            const int q = 8 * j + 2 * tq;
+            if (g < nt)
+                *reinterpret_cast<float2*>(zp + ((size_t)ks * n_pos + first + g) * R + q) =
+                    make_float2(acc[j][0], acc[j][1]);
+            if (g + 8 < nt)
+                *reinterpret_cast<float2*>(zp + ((size_t)ks * n_pos + first + g + 8) * R + q) =
+                    make_float2(acc[j][2], acc[j][3]);
+        }
+    }
+}
+
+// v[pos, c] = B_e[c, :] . zg[pos] for a 16-position tile and kLoreCB columns:
+// M = positions, N = columns (8 per MMA), K = R in tf32 steps of 8 (zg is
+// fp32; B_e's bf16 values are exact in tf32).  Thread tq's pair [2tq, 2tq+2)
+// of an 8-value step holds K slots tq and tq + 4.  The zg fragments are
+// loaded once per item and held across the columns.
+template <int R>
+__global__ void __launch_bounds__(256) lore_b_mma_kernel(const __nv_bfloat16* __restrict__ B,
+                                                         const int32_t* __restrict__ g_off, int d, int N,
+                                                         const float* __restrict__ zg, float* __restrict__ v) {
+    grid_dep_wait();  // zg comes from the previous kernel
+    __shared__ int s_off[kMaxExperts + 1], s_toff[kMaxExperts + 1];
+    lore_mtile_table(g_off, N, s_off, s_toff);
+    const int lane = threadIdx.x & 31, g = lane >> 2, tq = lane & 3;
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    const int n_cb = d / kLoreCB;
+    const int items = s_toff[N] * n_cb;
+    for (int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); item < items; item += warps) {
+        const int tile = item / n_cb, cb = item % n_cb;
+        int e, first;
+        if (!lore_mtile_of(s_off, s_toff, N, tile, e, first)) break;
+        const int nt = min(kLoreMT, s_off[e + 1] - first);
+        uint32_t af[R / 8][4];
+#pragma unroll
+        for (int s = 0; s < R / 8; ++s) {
+            float2 z0 = make_float2(0.f, 0.f), z1 = make_float2(0.f, 0.f);
+            if (g < nt) z0 = *reinterpret_cast<const float2*>(zg + (size_t)(first + g) * R + 8 * s + 2 * tq);
+            if (g + 8 < nt) z1 = *reinterpret_cast<const float2*>(zg + (size_t)(first + g + 8) * R + 8 * s + 2 * tq);
+            af[s][0] = to_tf32(z0.x); af[s][1] = to_tf32(z1.x);
+            af[s][2] = to_tf32(z0.y); af[s][3] = to_tf32(z1.y);
+        }
+        const __nv_bfloat16* Be = B + (size_t)e * d * R;
+        const int c_begin = cb * kLoreCB;
+#pragma unroll 4
+        for (int c0 = c_begin; c0 < c_begin + kLoreCB; c0 += 8) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint32_t* brow = reinterpret_cast<const uint32_t*>(Be + (size_t)(c0 + g) * R) + tq;
+#pragma unroll
+            for (int s = 0; s < R / 8; ++s) {
+                const uint32_t w = __ldg(brow + 4 * s);  // B_e[c0 + g][8s + 2tq, + 1]
+                mma_tf32_1688(acc, af[s][0], af[s][1], af[s][2], af[s][3], w << 16, w & 0xffff0000u);
+            }
+            const int c = c0 + 2 * tq;
+            if (g < nt) *reinterpret_cast<float2*>(v + (size_t)(first + g) * d + c) = make_float2(acc[0], acc[1]);
+            if (g + 8 < nt)
+                *reinterpret_cast<float2*>(v + (size_t)(first + g + 8) * d + c) = make_float2(acc[2], acc[3]);
+        }
     }
 }
 
@@ -730,15 +918,39 @@ static cudaError_t launch_lore_grouped(const LoreArgs& a, cudaStream_t st) {
     const int n_pos = a.T * a.k;
     const int tiles = n_pos / kLoreTile + a.N;
     const int gz = tiles < 160 ? tiles : 160;
-    e = launch_pdl(lore_z_grouped_kernel<W>, dim3(gz, kLoreKS), dim3(256), 0, st, (const W*)a.x, (const W*)a.A,
-                   (const int32_t*)a.g_off, (const int32_t*)a.g_list, a.d, a.k, a.r, a.N, n_pos, a.zp);
+    // bf16, r in {16, 32, 48, 64}, d a multiple of 256: the MMA forms
+    const bool mma = std::is_same<W, __nv_bfloat16>::value && a.r % 16 == 0 && a.r >= 16 && a.r <= 64 &&
+                     a.d % (kLoreKS * 32) == 0 && a.d % kLoreCB == 0;
+    const int mtiles = n_pos / kLoreMT + a.N;  // 16-position tiles, at most
+    const int g_cap = 4 * 152;
+    if (mma) {
+        const int gzm = std::min(g_cap, (mtiles * kLoreKS + 7) / 8);
+        const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(a.x);
+        const __nv_bfloat16* Ab = static_cast<const __nv_bfloat16*>(a.A);
+        auto zk = a.r == 16 ? lore_z_mma_kernel<16> : a.r == 32 ? lore_z_mma_kernel<32>
+                : a.r == 48 ? lore_z_mma_kernel<48> : lore_z_mma_kernel<64>;
+        e = launch_pdl(zk, dim3(gzm), dim3(256), 0, st, xb, Ab, (const int32_t*)a.g_off,
+                       (const int32_t*)a.g_list, a.d, a.k, a.N, n_pos, a.zp);
+    } else {
+        e = launch_pdl(lore_z_grouped_kernel<W>, dim3(gz, kLoreKS), dim3(256), 0, st, (const W*)a.x, (const W*)a.A,
+                       (const int32_t*)a.g_off, (const int32_t*)a.g_list, a.d, a.k, a.r, a.N, n_pos, a.zp);
+    }
     if (e != cudaSuccess) return e;
     e = launch_pdl(lore_z_sum_kernel, dim3(4 * 152), dim3(256), 0, st, a.final_gate, (const int32_t*)a.g_off,
                    (const int32_t*)a.g_list, a.r, a.N, n_pos, (const float*)a.zp, a.z);
     if (e != cudaSuccess) return e;
-    const int gx = tiles < 304 ? tiles : 304;
-    e = launch_pdl(lore_b_grouped_kernel<W>, dim3(gx, kLoreBY), dim3(256), 0, st, (const W*)a.B,
-                   (const int32_t*)a.g_off, a.d, a.r, a.N, (const float*)a.z, a.v);
+    if (mma) {
+        const int gbm = std::min(g_cap, (mtiles * (a.d / kLoreCB) + 7) / 8);
+        const __nv_bfloat16* Bb = static_cast<const __nv_bfloat16*>(a.B);
+        auto bk = a.r == 16 ? lore_b_mma_kernel<16> : a.r == 32 ? lore_b_mma_kernel<32>
+                : a.r == 48 ? lore_b_mma_kernel<48> : lore_b_mma_kernel<64>;
+        e = launch_pdl(bk, dim3(gbm), dim3(256), 0, st, Bb, (const int32_t*)a.g_off, a.d, a.N,
+                       (const float*)a.z, a.v);
+    } else {
+        const int gx = tiles < 304 ? tiles : 304;
+        e = launch_pdl(lore_b_grouped_kernel<W>, dim3(gx, kLoreBY), dim3(256), 0, st, (const W*)a.B,
+                       (const int32_t*)a.g_off, a.d, a.r, a.N, (const float*)a.z, a.v);
+    }
     if (e != cudaSuccess || a.skip_sum) return e;
     return launch_pdl(lore_sum_kernel, dim3(a.T, (a.d / 4 + 255) / 256), dim3(256), 0, st, (const int32_t*)a.g_pos,
                       (const float*)a.v, a.d, a.k, a.y_lore);

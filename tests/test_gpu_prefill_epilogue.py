@@ -102,3 +102,31 @@ def test_prefill_epilogue_repeats_bitwise():
         outs.append(bufs.out.clone())
     assert moe.moe_check(layer.ws)[0] == moe.MOE_OK
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+@pytest.mark.parametrize("r", [16, 32, 48, 64])
+def test_grouped_lore_on_tensor_cores_matches_oracle(r):
+    """Grouped LoRE products of a bf16 layer with r a multiple of 16 (up to
+    64) and d a multiple of 256 run as warp-level MMAs (z from bf16 x and
+    A_e, B_e z in tf32): the DeepSeek-V2-Lite shape at rank r, every miss a
+    LoRE slot (experts with more than 16 LoRE slots, so several 16-position
+    tiles), outputs against the oracle, and the stage-wise calls give the
+    same bits."""
+    cfg = CONFIGS["dsv2lite"].with_(r=r, name=f"dsv2lite-r{r}")
+    T = 256
+    W = make_weights(cfg)
+    layer = DeviceLayer(cfg, W, T)
+    x = make_tokens(cfg, T=T, batch=2)
+    xd = x_device(x, layer.dt)
+    b = LayerBuffers(layer, T)
+    forward(layer, b, xd, policy=MISS_LORE)
+    st, det = moe.moe_check(layer.ws)
+    assert st == moe.MOE_OK, (moe.status_string(st), det)
+    fi, fk = to_np(b.final_idx), to_np(b.final_kind)
+    per_expert = np.bincount(fi[fk == moe.MOE_KIND_LORE], minlength=cfg.N)
+    assert per_expert.max() > 16, per_expert
+    R = oracle.layer_forward(cfg, W, x, policy=MISS_LORE)
+    check_selection(cfg, R, b)
+    check_output(cfg, R, b.out)
+    s = _stagewise(cfg, layer, xd, T, MISS_LORE)
+    assert torch.equal(s.out, b.out)
