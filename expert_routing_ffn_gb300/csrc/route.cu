@@ -266,7 +266,31 @@ __global__ void __launch_bounds__(256) route_score_kernel(const W* __restrict__ 
     if (t >= T) return;
     const uint4* xr = reinterpret_cast<const uint4*>(x_pre + (size_t)t * d);
     float acc = 0.f;
-    for (int q = lane; q < d / V; q += 32) {
+    int q = lane;
+    if ((reinterpret_cast<uintptr_t>(w_ord) & 15) == 0) {
+        // four chunks per lane in flight (x and w loaded before the products,
+        // which keep the order of the loop below)
+        const float4* w4 = reinterpret_cast<const float4*>(w_ord);
+        for (; q + 96 < d / V; q += 128) {
+            uint4 xa[4];
+            float4 wa[4][V / 4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                xa[u] = xr[q + 32 * u];
+#pragma unroll
+                for (int i = 0; i < V / 4; ++i) wa[u][i] = w4[(q + 32 * u) * (V / 4) + i];
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                float xv[V];
+                unpack16(xa[u], xv, (W*)nullptr);
+                const float* wv = reinterpret_cast<const float*>(wa[u]);
+#pragma unroll
+                for (int j = 0; j < V; ++j) acc = fmaf(xv[j], wv[j], acc);
+            }
+        }
+    }
+    for (; q < d / V; q += 32) {
         float xv[V];
         unpack16(xr[q], xv, (W*)nullptr);
 #pragma unroll
