@@ -654,9 +654,13 @@ __global__ void __launch_bounds__(256) prefill_epilogue_kernel(const PrefillEpil
 // Warp 0 then combines in slot order.  Every sum runs in the order of the
 // separate kernels (gemv_reduce_kernel, lore_b_kernel, combine_kernel), so
 // the result is bitwise the one of the stage-wise calls.
+//
+// The slots, the permutation and the plan were written before the expert FFN
+// started (the FFN's own wait on them returned before it let this launch
+// begin), so they are read, and the LoRE B rows prefetched into L2, before
+// the wait on the FFN; its partial rows and the LoRE z rows after it.
 template <typename W, bool DIRECT>
 __global__ void __launch_bounds__(DIRECT ? 256 : 1024) layer_epilogue_kernel(const EpilogueArgs a) {
-    grid_dep_wait();  // the FFN's partial rows
     const int t = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int q = blockIdx.y * 32 + lane;  // float4 column group
@@ -729,6 +733,17 @@ __global__ void __launch_bounds__(DIRECT ? 256 : 1024) layer_epilogue_kernel(con
     }
     __syncthreads();
     const bool col_ok = q < d / 4;
+    if (warp == lore_warp && a.lore_b && col_ok) {
+        // this lane's four B rows of each LoRE slot: 4 r contiguous values
+        const char* B = static_cast<const char*>(a.lore_b);
+        for (int i = 0; i < s_nl; ++i) {
+            const int e = s_e[s_lore[i]];
+            const char* p = B + ((size_t)e * d + (size_t)q * 4) * r * sizeof(W);
+            for (int off = 0; off < 4 * r * (int)sizeof(W); off += 128)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(p + off));
+        }
+    }
+    grid_dep_wait();  // the FFN's partial rows (and, through the join, LoRE z)
     // LoRE term y_lore[t, j] = sum over LoRE slots, then over q, of B_e[j, q] z[q]
     // (the order of lore_b_kernel)
     if (warp == lore_warp && a.lore_b) {
