@@ -7,15 +7,15 @@
 //   phase 2: for every (segment, 128-row tile, 256-column tile of d):
 //            y = h_tile . Wd  (K = I; Wd is [I, d], an MN-major operand)
 //            epilogue -> y (fp32, ungated)
-// Tiles are numbered phase 1 first, then phase 2, and CTA c takes tiles c,
-// c + G, c + 2G, ...  A phase-2 tile needs the h rows of its (segment, row
-// tile) from every phase-1 channel tile: each epilogue warp counts its
-// finished phase-1 tile on that pair's counter (after its stores have
-// completed), and the producer of a phase-2 tile waits for the count before
-// loading h.  A phase-2 tile depends only on phase-1 tiles of the same or an
-// earlier round, which never wait, so every wait ends; so the end of phase 1
-// and the start of phase 2 overlap instead of the second launch waiting for
-// the slowest CTA of the first.
+// Tiles are numbered phase 1 first, then phase 2; one CTA per tile claims
+// numbers in order from a counter, pair c takes c, c + G, ...  A phase-2 tile
+// needs the h rows of its (segment, row tile) from every phase-1 channel
+// tile: each epilogue warp counts its finished phase-1 tile on that counter
+// (after its stores completed), and the producer of a phase-2 tile waits for
+// the count before loading h.  Every phase-1 tile is taken before any phase-2
+// tile and never waits on another CTA, so every wait ends; the end of phase 1
+// and the start of phase 2 overlap instead of a second launch waiting for the
+// slowest CTA of the first.
 // Shared experts form one segment whose channels are the concatenation of
 // all shared experts (so phase 2 sums them, as y_shared requires).
 //
