@@ -107,10 +107,10 @@ __global__ void __launch_bounds__(256) lore_b_kernel(const int32_t* __restrict__
 // A_e and B_e are read once per tile of up to kLoreTile slots of e instead of
 // once per slot.  Tile index -> (expert, first grouped position) from the
 // per-expert tile counts; every block walks tiles blockIdx.x, + gridDim.x, ...
-// Both products are register-tiled on the CUDA cores (rank r <= 64 is too
-// narrow a GEMM side to pay for a tensor-core pipeline): operands staged in
-// shared memory K-major as fp32, thread = 4 x 4 outputs from two 16-byte
-// shared loads per step.
+// These two kernels are the CUDA-core forms (fp32 layers, other ranks):
+// register-tiled, operands staged in shared memory K-major as fp32, thread =
+// 4 x 4 outputs from two 16-byte shared loads per step.  bf16 layers with r a
+// multiple of 16 up to 64 take the warp-level MMA forms below.
 constexpr int kLoreTile = 64;
 constexpr int kLoreKC = 32;  // values of d per shared-memory chunk (z pass)
 constexpr int kLoreKS = 8;   // d split over this many blocks per tile (z pass)
